@@ -1,0 +1,236 @@
+// pi_api.cu -- the extern "C" boundary: argument validation, work planning,
+// workspace layout and launch sequencing.  No arithmetic of the path lives
+// here; every step runs in the kernels.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "pi_internal.h"
+
+namespace pi {
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+int device_sms() {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lk(mu);
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+bool make_plan(const pi_layer_desc& desc, Plan* p) {
+    if (desc.d <= 0 || desc.d % 8 != 0 || desc.ffn <= 0 || desc.rank <= 0 || desc.rank % 8 != 0 ||
+        desc.batch < 1 || desc.batch > 32 || desc.d > (1 << 16) || desc.rank > 8192 ||
+        desc.ffn > (1 << 22))
+        return false;
+    if (desc.wdtype != PI_W_F16 && desc.wdtype != PI_W_INT4_G32) return false;
+    if (desc.wdtype == PI_W_INT4_G32 && desc.d % 32 != 0) return false;
+    if (desc.gated != 0 && desc.gated != 1) return false;
+    Plan q{};
+    q.d = desc.d;
+    q.F = desc.ffn;
+    q.r = desc.rank;
+    q.B = desc.batch;
+    q.int4 = desc.wdtype == PI_W_INT4_G32;
+    q.gated = desc.gated == 1;
+    q.W = (q.F + 31) / 32;
+    q.nsm = device_sms();
+    if (q.nsm <= 0) q.nsm = 1;
+    // predictor P1 x: enough (row, split) warps to cover the GPU twice, splits >= 256 elements
+    const int row_blocks = (q.r + 7) / 8;
+    int us = (2 * q.nsm + row_blocks - 1) / row_blocks;
+    const int max_us = (q.d + 255) / 256;
+    if (us > max_us) us = max_us;
+    if (us < 1) us = 1;
+    q.u_seg = ((q.d / 8 + us - 1) / us) * 8;
+    q.u_splits = (q.d + q.u_seg - 1) / q.u_seg;
+    // FC2: a block covers 256 threads x (8 fp16 | 16 INT4) columns
+    q.fc2_cols = 256 * (q.int4 ? 16 : 8);
+    q.fc2_tiles = (q.d + q.fc2_cols - 1) / q.fc2_cols;
+    int s2 = (2 * q.nsm + q.fc2_tiles - 1) / q.fc2_tiles;
+    const int max_s2 = (q.F + 7) / 8;
+    if (s2 > max_s2) s2 = max_s2;
+    q.fc2_splits = s2 < 1 ? 1 : s2;
+    size_t off = 0;
+    q.off_mask = off;  off = up(off + sizeof(uint32_t) * (size_t)q.B * q.W);
+    q.off_idx = off;   off = up(off + sizeof(int32_t) * (size_t)q.F);
+    q.off_count = off; off = up(off + sizeof(int32_t) * 4);
+    q.off_h = off;     off = up(off + sizeof(float) * (size_t)q.F * q.B);
+    q.off_upart = off; off = up(off + sizeof(float) * (size_t)q.u_splits * q.B * q.r);
+    q.off_part = off;  off = up(off + sizeof(float) * (size_t)q.fc2_splits * q.B * q.d);
+    q.total = off;
+    *p = q;
+    return true;
+}
+
+namespace {
+
+pi_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PI_OK : PI_ERR_CUDA; }
+
+bool weights_ok(const Plan& p, const pi_layer_weights* w, bool need_w1, bool need_w2, bool need_pred) {
+    if (!w) return false;
+    if (need_w1) {
+        if (!w->w1 || !w->b1 || !aligned16(w->w1)) return false;
+        if (p.int4 && (!w->w1_scales)) return false;
+        if (p.gated && (!w->wu || !aligned16(w->wu))) return false;
+    }
+    if (need_w2) {
+        if (!w->w2t || !w->b2 || !aligned16(w->w2t)) return false;
+        if (p.int4 && !w->w2t_scales) return false;
+    }
+    if (need_pred) {
+        if (!w->p1 || !w->p2 || !w->b1 || !aligned16(w->p1) || !aligned16(w->p2)) return false;
+    }
+    return true;
+}
+
+LayerPtrs ptrs(const pi_layer_weights* w) {
+    LayerPtrs l;
+    l.w1 = w->w1;
+    l.w1s = reinterpret_cast<const __half*>(w->w1_scales);
+    l.b1 = reinterpret_cast<const __half*>(w->b1);
+    l.wu = reinterpret_cast<const __half*>(w->wu);
+    l.w2t = w->w2t;
+    l.w2ts = reinterpret_cast<const __half*>(w->w2t_scales);
+    l.b2 = reinterpret_cast<const __half*>(w->b2);
+    l.p1 = reinterpret_cast<const __half*>(w->p1);
+    l.p2 = reinterpret_cast<const __half*>(w->p2);
+    l.table = w->table;
+    return l;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+    return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+}  // namespace
+}  // namespace pi
+
+using namespace pi;
+
+extern "C" {
+
+size_t pi_workspace_bytes(const pi_layer_desc* desc) {
+    Plan p;
+    if (!desc || !make_plan(*desc, &p)) return 0;
+    return p.total;
+}
+
+pi_status pi_workspace_layout(const pi_layer_desc* desc, pi_workspace_layout_t* out) {
+    Plan p;
+    if (!desc || !out || !make_plan(*desc, &p)) return PI_ERR_INVALID_ARG;
+    out->mask = p.off_mask;
+    out->idx = p.off_idx;
+    out->count = p.off_count;
+    out->h = p.off_h;
+    out->total = p.total;
+    return PI_OK;
+}
+
+pi_status pi_predict(const pi_layer_desc* desc, const pi_half* x, const pi_half* p1, const pi_half* p2,
+                     const pi_half* bpred, float tau, uint32_t* mask, void* workspace, size_t ws_bytes,
+                     void* stream) {
+    Plan p;
+    if (!desc || !make_plan(*desc, &p)) return PI_ERR_INVALID_ARG;
+    if (!x || !p1 || !p2 || !bpred || !mask || !aligned16(x) || !aligned16(p1) || !aligned16(p2))
+        return PI_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace) || ws_bytes < p.total) return PI_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return from_cuda(launch_predict(p, reinterpret_cast<const __half*>(x), reinterpret_cast<const __half*>(p1),
+                                    reinterpret_cast<const __half*>(p2), reinterpret_cast<const __half*>(bpred),
+                                    tau, mask, at<float>(workspace, p.off_upart), s));
+}
+
+pi_status pi_compact(const pi_layer_desc* desc, const uint32_t* mask, const int32_t* table, int32_t* idx,
+                     int32_t* orig_idx, int32_t* d_count, void* stream) {
+    Plan p;
+    if (!desc || !make_plan(*desc, &p)) return PI_ERR_INVALID_ARG;
+    if (!mask || !idx || !d_count || (orig_idx && !table)) return PI_ERR_INVALID_ARG;
+    return from_cuda(launch_compact(p, mask, table, idx, orig_idx, d_count, static_cast<cudaStream_t>(stream)));
+}
+
+pi_status pi_sparse_fc1(const pi_layer_desc* desc, const pi_half* x, const pi_layer_weights* w,
+                        const int32_t* idx, const int32_t* d_count, const uint32_t* mask, float* h,
+                        void* stream) {
+    Plan p;
+    if (!desc || !make_plan(*desc, &p)) return PI_ERR_INVALID_ARG;
+    if (!x || !aligned16(x) || !idx || !d_count || !h || !weights_ok(p, w, true, false, false))
+        return PI_ERR_INVALID_ARG;
+    if ((size_t)8 * p.d * sizeof(uint16_t) > 200 * 1024) return PI_ERR_UNSUPPORTED;
+    return from_cuda(launch_fc1(p, reinterpret_cast<const __half*>(x), ptrs(w), idx, d_count, mask, h,
+                                static_cast<cudaStream_t>(stream)));
+}
+
+pi_status pi_sparse_fc2(const pi_layer_desc* desc, const float* h, const int32_t* idx, const int32_t* d_count,
+                        const pi_layer_weights* w, float* y, void* workspace, size_t ws_bytes, void* stream) {
+    Plan p;
+    if (!desc || !make_plan(*desc, &p)) return PI_ERR_INVALID_ARG;
+    if (!h || !idx || !d_count || !y || !aligned16(y) || !weights_ok(p, w, false, true, false))
+        return PI_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace) || ws_bytes < p.total) return PI_ERR_WORKSPACE;
+    return from_cuda(launch_fc2(p, h, idx, d_count, ptrs(w), at<float>(workspace, p.off_part), y,
+                                static_cast<cudaStream_t>(stream)));
+}
+
+pi_status pi_ffn_layer(const pi_layer_desc* desc, const pi_half* x, const pi_layer_weights* w, float tau,
+                       void* workspace, size_t ws_bytes, float* y, void* stream) {
+    Plan p;
+    if (!desc || !make_plan(*desc, &p)) return PI_ERR_INVALID_ARG;
+    if (!x || !aligned16(x) || !y || !aligned16(y) || !weights_ok(p, w, true, true, true))
+        return PI_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace) || ws_bytes < p.total) return PI_ERR_WORKSPACE;
+    if ((size_t)8 * p.d * sizeof(uint16_t) > 200 * 1024) return PI_ERR_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const LayerPtrs l = ptrs(w);
+    const __half* xh = reinterpret_cast<const __half*>(x);
+    uint32_t* mask = at<uint32_t>(workspace, p.off_mask);
+    int32_t* idx = at<int32_t>(workspace, p.off_idx);
+    int32_t* cnt = at<int32_t>(workspace, p.off_count);
+    float* h = at<float>(workspace, p.off_h);
+    cudaError_t e = launch_predict(p, xh, l.p1, l.p2, l.b1, tau, mask, at<float>(workspace, p.off_upart), s);
+    if (e == cudaSuccess) e = launch_compact(p, mask, nullptr, idx, nullptr, cnt, s);
+    if (e == cudaSuccess) e = launch_fc1(p, xh, l, idx, cnt, p.B > 1 ? mask : nullptr, h, s);
+    if (e == cudaSuccess) e = launch_fc2(p, h, idx, cnt, l, at<float>(workspace, p.off_part), y, s);
+    return from_cuda(e);
+}
+
+pi_status pi_rmsnorm_half(int d, int batch, const float* y, float eps, pi_half* x_out, void* stream) {
+    if (d <= 0 || batch <= 0 || !y || !x_out || !(eps >= 0.f)) return PI_ERR_INVALID_ARG;
+    return from_cuda(launch_rmsnorm(d, batch, y, eps, reinterpret_cast<__half*>(x_out),
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+const char* pi_status_string(pi_status s) {
+    switch (s) {
+        case PI_OK: return "ok";
+        case PI_ERR_INVALID_ARG: return "invalid argument";
+        case PI_ERR_UNSUPPORTED: return "unsupported request";
+        case PI_ERR_CUDA: return "CUDA error";
+        case PI_ERR_TIMEOUT: return "device-side wait timed out";
+        case PI_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    }
+    return "unknown status";
+}
+
+pi_status pi_last_device_status(void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PI_ERR_CUDA;
+    return PI_OK;
+}
+
+}  // extern "C"

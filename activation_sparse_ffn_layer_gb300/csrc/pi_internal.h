@@ -1,0 +1,55 @@
+// pi_internal.h -- launchers shared between the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/pi.h"
+
+namespace pi {
+
+// Work split chosen for one layer descriptor on the current device.  Both the
+// workspace size and every launch are derived from it, so they always agree.
+struct Plan {
+    int d, F, r, B;
+    bool int4, gated;
+    int W;          // mask words per token, ceil(F/32)
+    int nsm;        // SMs of the device
+    int u_splits;   // predictor P1 x: splits of d (partial sums reduced in fixed order)
+    int u_seg;      // elements of d per split (multiple of 8)
+    int fc2_cols;   // columns per FC2 block
+    int fc2_tiles;  // ceil(d / fc2_cols)
+    int fc2_splits; // neuron splits of FC2 (partials reduced in fixed order)
+    // workspace offsets (bytes, 256-aligned)
+    size_t off_mask, off_idx, off_count, off_h, off_upart, off_part, total;
+};
+
+bool make_plan(const pi_layer_desc& desc, Plan* p);
+
+struct LayerPtrs {
+    const void* w1;
+    const __half* w1s;
+    const __half* b1;
+    const __half* wu;
+    const void* w2t;
+    const __half* w2ts;
+    const __half* b2;
+    const __half* p1;
+    const __half* p2;
+    const int32_t* table;
+};
+
+cudaError_t launch_predict(const Plan& p, const __half* x, const __half* p1, const __half* p2,
+                           const __half* bpred, float tau, uint32_t* mask, float* upart,
+                           cudaStream_t s);
+cudaError_t launch_compact(const Plan& p, const uint32_t* mask, const int32_t* table, int32_t* idx,
+                           int32_t* orig, int32_t* count, cudaStream_t s);
+cudaError_t launch_fc1(const Plan& p, const __half* x, const LayerPtrs& w, const int32_t* idx,
+                       const int32_t* count, const uint32_t* mask, float* h, cudaStream_t s);
+cudaError_t launch_fc2(const Plan& p, const float* h, const int32_t* idx, const int32_t* count,
+                       const LayerPtrs& w, float* partial, float* y, cudaStream_t s);
+cudaError_t launch_rmsnorm(int d, int B, const float* y, float eps, __half* x, cudaStream_t s);
+
+}  // namespace pi

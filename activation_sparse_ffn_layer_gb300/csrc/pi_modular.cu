@@ -1,0 +1,508 @@
+// pi_modular.cu -- the decode path as separate kernels (one per step).
+//
+//   predictor       k_predict_u (P1 x, split over d) + k_predict_s (P2 u + b > tau, ballot)
+//   compaction      k_compact   (popcount + block scan, ascending rows)
+//   FC1             k_fc1       (row gather, 16-byte loads, warp-shuffle dot products,
+//                                bias + ReLU (+ gate) fused)
+//   FC2             k_fc2_part  (gather-accumulate over W2t rows, neuron splits)
+//                   k_fc2_reduce(fixed-order sum of the splits + b2: no atomics)
+//   normalisation   k_rmsnorm
+//
+// The math follows the PowerInfer summary (CSDN), sections "Background"
+// (FC1 -> ReLU -> FC2, neurons are rows/columns), "Neuron-aware operator"
+// (test each neuron, touch only active rows/columns), "Adaptive sparse
+// predictor" and "Neuron placement and management" (neuron table).
+#include <cuda_runtime.h>
+
+#include "pi_common.cuh"
+#include "pi_internal.h"
+
+namespace pi {
+
+// ------------------------------------------------------------------ predictor
+
+// upart[s][b][i] = sum over split s of d of P1[i, c] x_b[c]; one warp per row.
+template <int TB>
+__global__ void __launch_bounds__(256) k_predict_u(const __half* __restrict__ x, int B, int b0,
+                                                   const __half* __restrict__ p1, int d, int r,
+                                                   int seg, float* __restrict__ upart) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int i = blockIdx.x * 8 + warp;
+    const int s = blockIdx.y;
+    if (i >= r) return;
+    const int c0 = s * seg;
+    const int c1 = min(d, c0 + seg);
+    float acc[TB];
+#pragma unroll
+    for (int t = 0; t < TB; ++t) acc[t] = 0.f;
+    const __half* row = p1 + (size_t)i * d;
+#pragma unroll 2
+    for (int c = c0 + lane * 8; c < c1; c += 256) {
+        float wf[8];
+        h8_to_f8(ld_stream16(row + c), wf);
+#pragma unroll
+        for (int t = 0; t < TB; ++t) {
+            float xf[8];
+            h8_to_f8(__ldg(reinterpret_cast<const uint4*>(x + (size_t)(b0 + t) * d + c)), xf);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[t] = fmaf(wf[e], xf[e], acc[t]);
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < TB; ++t) acc[t] = warp_sum(acc[t]);
+    if (lane == 0) {
+#pragma unroll
+        for (int t = 0; t < TB; ++t) upart[((size_t)s * B + b0 + t) * r + i] = acc[t];
+    }
+}
+
+// mask[b][w] bit e = (P2[32w+e] . u_b + bias[32w+e] > tau).  One warp per mask
+// word; G lanes share a row of P2 (16-byte loads), 32/G rows per step.
+template <int TB>
+__global__ void __launch_bounds__(128) k_predict_s(const __half* __restrict__ p2,
+                                                   const __half* __restrict__ bias,
+                                                   const float* __restrict__ upart, int usplits,
+                                                   int B, int b0, int r, int F, int W, float tau,
+                                                   uint32_t* __restrict__ mask) {
+    extern __shared__ __align__(16) float us[];  // [TB][r]
+    for (int e = threadIdx.x; e < TB * r; e += blockDim.x) {
+        const int t = e / r, i = e - t * r;
+        float v = 0.f;
+        for (int s = 0; s < usplits; ++s) v += upart[((size_t)s * B + b0 + t) * r + i];
+        us[e] = v;
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int w = blockIdx.x * 4 + warp;
+    if (w >= W) return;
+    const int nvec = r / 8;
+    int G = 1;
+    while (G * 2 <= nvec && G * 2 <= 32) G *= 2;
+    const int rpp = 32 / G;
+    const int g = lane / G, t = lane % G;
+    uint32_t bits[TB];
+#pragma unroll
+    for (int tt = 0; tt < TB; ++tt) bits[tt] = 0u;
+    for (int step = 0; step < G; ++step) {
+        const int k = w * 32 + step * rpp + g;
+        float acc[TB];
+#pragma unroll
+        for (int tt = 0; tt < TB; ++tt) acc[tt] = 0.f;
+        if (k < F) {
+            const __half* row = p2 + (size_t)k * r;
+            for (int v = t; v < nvec; v += G) {
+                float pf[8];
+                h8_to_f8(ld_stream16(row + v * 8), pf);
+#pragma unroll
+                for (int tt = 0; tt < TB; ++tt) {
+                    const float4* u4 = reinterpret_cast<const float4*>(us + tt * r + v * 8);
+                    const float4 a = u4[0], b = u4[1];
+                    acc[tt] = fmaf(pf[0], a.x, acc[tt]);
+                    acc[tt] = fmaf(pf[1], a.y, acc[tt]);
+                    acc[tt] = fmaf(pf[2], a.z, acc[tt]);
+                    acc[tt] = fmaf(pf[3], a.w, acc[tt]);
+                    acc[tt] = fmaf(pf[4], b.x, acc[tt]);
+                    acc[tt] = fmaf(pf[5], b.y, acc[tt]);
+                    acc[tt] = fmaf(pf[6], b.z, acc[tt]);
+                    acc[tt] = fmaf(pf[7], b.w, acc[tt]);
+                }
+            }
+        }
+        for (int o = G / 2; o > 0; o >>= 1) {
+#pragma unroll
+            for (int tt = 0; tt < TB; ++tt) acc[tt] += __shfl_xor_sync(FULL, acc[tt], o);
+        }
+        const float bk = (k < F) ? __half2float(bias[k]) : 0.f;
+#pragma unroll
+        for (int tt = 0; tt < TB; ++tt) {
+            const bool pred = (t == 0) && (k < F) && (acc[tt] + bk > tau);
+            const uint32_t bal = __ballot_sync(FULL, pred);
+            for (int gg = 0; gg < rpp; ++gg)
+                if ((bal >> (gg * G)) & 1u) bits[tt] |= 1u << (step * rpp + gg);
+        }
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int tt = 0; tt < TB; ++tt) mask[(size_t)(b0 + tt) * W + w] = bits[tt];
+    }
+}
+
+// ----------------------------------------------------------------- compaction
+
+// One block of 1024 threads: each thread takes one mask word (OR over the
+// batch), counts its bits, an exclusive block scan gives its output offset.
+__global__ void __launch_bounds__(1024) k_compact(const uint32_t* __restrict__ mask, int B, int W,
+                                                  int F, const int32_t* __restrict__ table,
+                                                  int32_t* __restrict__ idx,
+                                                  int32_t* __restrict__ orig,
+                                                  int32_t* __restrict__ count) {
+    __shared__ int wsum[32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int base = 0;
+    for (int w0 = 0; w0 < W; w0 += 1024) {
+        const int w = w0 + threadIdx.x;
+        uint32_t bits = 0u;
+        if (w < W) {
+            for (int b = 0; b < B; ++b) bits |= mask[(size_t)b * W + w];
+            if (w == W - 1 && (F & 31)) bits &= (1u << (F & 31)) - 1u;
+        }
+        const int c = __popc(bits);
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(FULL, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) wsum[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            int v = wsum[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(FULL, v, o);
+                if (lane >= o) v += u;
+            }
+            wsum[lane] = v;  // inclusive prefix over warps
+        }
+        __syncthreads();
+        int off = base + incl - c + (warp > 0 ? wsum[warp - 1] : 0);
+        while (bits) {
+            const int p = __ffs(bits) - 1;
+            bits &= bits - 1u;
+            const int k = w * 32 + p;
+            idx[off] = k;
+            if (orig) orig[off] = table[k];
+            ++off;
+        }
+        base += wsum[31];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) *count = base;
+}
+
+// ------------------------------------------------------------------------ FC1
+
+// KIND 0: fp16 rows; 1: fp16 gate + up rows (gated); 2: INT4 group-32 rows.
+// One warp per listed neuron (grid-stride), x for TB tokens staged in smem.
+template <int TB, int KIND>
+__global__ void __launch_bounds__(256) k_fc1(const __half* __restrict__ x, int B, int b0, int d,
+                                             LayerPtrs w, const int32_t* __restrict__ idx,
+                                             const int32_t* __restrict__ count,
+                                             const uint32_t* __restrict__ mask, int W,
+                                             float* __restrict__ h) {
+    const int n = *count;
+    if (n == 0) return;  // nothing predicted active: skip the layer's FC1 entirely
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    __half* xs = reinterpret_cast<__half*>(smem_raw);
+    const int nv = d / 8;
+    const uint4* xg = reinterpret_cast<const uint4*>(x + (size_t)b0 * d);
+    for (int e = threadIdx.x; e < TB * nv; e += blockDim.x) reinterpret_cast<uint4*>(xs)[e] = xg[e];
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int nw = (gridDim.x * blockDim.x) >> 5;
+    for (int j = gw; j < n; j += nw) {
+        const int k = idx[j];
+        float acc[TB], accu[TB];
+#pragma unroll
+        for (int t = 0; t < TB; ++t) acc[t] = accu[t] = 0.f;
+        if (KIND != 2) {
+            const uint4* row = reinterpret_cast<const uint4*>(static_cast<const __half*>(w.w1) + (size_t)k * d);
+            const uint4* rowu = KIND == 1 ? reinterpret_cast<const uint4*>(w.wu + (size_t)k * d) : nullptr;
+#pragma unroll 4
+            for (int c = lane; c < nv; c += 32) {
+                float wf[8], uf[8];
+                h8_to_f8(ld_stream16(row + c), wf);
+                if (KIND == 1) h8_to_f8(ld_stream16(rowu + c), uf);
+#pragma unroll
+                for (int t = 0; t < TB; ++t) {
+                    float xf[8];
+                    h8_to_f8(reinterpret_cast<const uint4*>(xs + (size_t)t * d)[c], xf);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        acc[t] = fmaf(wf[e], xf[e], acc[t]);
+                        if (KIND == 1) accu[t] = fmaf(uf[e], xf[e], accu[t]);
+                    }
+                }
+            }
+        } else {
+            const int ng = d / 32;
+            const uint4* row = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(w.w1) + (size_t)k * (d / 2));
+            const __half* sc = w.w1s + (size_t)k * ng;
+#pragma unroll 2
+            for (int g = lane; g < ng; g += 32) {
+                const uint4 q = ld_stream16(row + g);
+                const float s = __half2float(sc[g]);
+                const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+                float part[TB];
+#pragma unroll
+                for (int t = 0; t < TB; ++t) part[t] = 0.f;
+#pragma unroll
+                for (int wi = 0; wi < 4; ++wi) {
+                    float qf[8];
+                    q8_to_f8(qw[wi], qf);
+#pragma unroll
+                    for (int t = 0; t < TB; ++t) {
+                        float xf[8];
+                        h8_to_f8(*reinterpret_cast<const uint4*>(xs + (size_t)t * d + g * 32 + wi * 8), xf);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) part[t] = fmaf(qf[e], xf[e], part[t]);
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < TB; ++t) acc[t] = fmaf(s, part[t], acc[t]);
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < TB; ++t) {
+            acc[t] = warp_sum(acc[t]);
+            if (KIND == 1) accu[t] = warp_sum(accu[t]);
+        }
+        const float bk = __half2float(w.b1[k]);
+#pragma unroll
+        for (int t = 0; t < TB; ++t) {
+            if (lane == t) {
+                const float z = acc[t] + bk;
+                float hv = z > 0.f ? z : 0.f;
+                if (KIND == 1) hv *= accu[t];
+                if (mask != nullptr && B > 1 && !((mask[(size_t)(b0 + t) * W + (k >> 5)] >> (k & 31)) & 1u))
+                    hv = 0.f;
+                h[(size_t)j * B + b0 + t] = hv;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------------ FC2
+
+// part[s][b][c] = sum over listed neurons j of split s of h[j][b] * W2t[idx_j][c].
+// Block (column tile, split); each thread owns CPT consecutive columns.  Rows
+// whose h is zero for every token of the block are not read: ReLU already
+// removed those neurons from FC2.
+template <int TB, bool INT4>
+__global__ void __launch_bounds__(256) k_fc2_part(const float* __restrict__ h, int B, int b0,
+                                                  const int32_t* __restrict__ idx,
+                                                  const int32_t* __restrict__ count, int d,
+                                                  const void* __restrict__ w2t,
+                                                  const __half* __restrict__ w2ts,
+                                                  float* __restrict__ part) {
+    constexpr int CPT = INT4 ? 16 : 8;
+    constexpr int CH = 256;
+    const int n = *count;
+    const int S = gridDim.y, s = blockIdx.y;
+    const int chunk = (n + S - 1) / S;
+    const int j0 = min(n, s * chunk), j1 = min(n, j0 + chunk);
+    const int c = (blockIdx.x * blockDim.x + threadIdx.x) * CPT;
+    const bool active = c < d;
+    __shared__ int sidx[CH];
+    __shared__ float sh[CH * TB];
+    float acc[TB][CPT];
+#pragma unroll
+    for (int t = 0; t < TB; ++t)
+#pragma unroll
+        for (int e = 0; e < CPT; ++e) acc[t][e] = 0.f;
+    for (int base = j0; base < j1; base += CH) {
+        const int cnt = min(CH, j1 - base);
+        __syncthreads();
+        for (int e = threadIdx.x; e < cnt; e += blockDim.x) {
+            float any = 0.f;
+            for (int t = 0; t < TB; ++t) {
+                const float v = h[(size_t)(base + e) * B + b0 + t];
+                sh[e * TB + t] = v;
+                any = fmaxf(any, fabsf(v));
+            }
+            sidx[e] = any > 0.f ? idx[base + e] : -1;
+        }
+        __syncthreads();
+        if (!active) continue;
+#pragma unroll 4
+        for (int t = 0; t < cnt; ++t) {
+            const int k = sidx[t];
+            if (k < 0) continue;
+            if (!INT4) {
+                float wf[8];
+                h8_to_f8(ld_stream16(static_cast<const __half*>(w2t) + (size_t)k * d + c), wf);
+#pragma unroll
+                for (int tb = 0; tb < TB; ++tb) {
+                    const float hv = sh[t * TB + tb];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[tb][e] = fmaf(hv, wf[e], acc[tb][e]);
+                }
+            } else {
+                const uint2 q = ld_stream8(static_cast<const uint8_t*>(w2t) + (size_t)k * (d / 2) + c / 2);
+                const float sc = __half2float(w2ts[(size_t)k * (d / 32) + c / 32]);
+                float qa[8], qb[8];
+                q8_to_f8(q.x, qa);
+                q8_to_f8(q.y, qb);
+#pragma unroll
+                for (int tb = 0; tb < TB; ++tb) {
+                    const float hv = sh[t * TB + tb] * sc;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        acc[tb][e] = fmaf(hv, qa[e], acc[tb][e]);
+                        acc[tb][8 + e] = fmaf(hv, qb[e], acc[tb][8 + e]);
+                    }
+                }
+            }
+        }
+    }
+    if (!active) return;
+#pragma unroll
+    for (int tb = 0; tb < TB; ++tb) {
+        float4* dst = reinterpret_cast<float4*>(part + ((size_t)s * B + b0 + tb) * d + c);
+#pragma unroll
+        for (int e = 0; e < CPT / 4; ++e)
+            dst[e] = make_float4(acc[tb][4 * e], acc[tb][4 * e + 1], acc[tb][4 * e + 2], acc[tb][4 * e + 3]);
+    }
+}
+
+// y[b][c] = b2[c] + sum_{s = 0..S-1} part[s][b][c]   (fixed order: reproducible)
+__global__ void __launch_bounds__(256) k_fc2_reduce(const float* __restrict__ part, int S, int B,
+                                                    int d, const __half* __restrict__ b2,
+                                                    float* __restrict__ y) {
+    const int e4 = blockIdx.x * blockDim.x + threadIdx.x;
+    const int total4 = B * d / 4;
+    if (e4 >= total4) return;
+    const int c = (e4 * 4) % d;
+    float4 acc = make_float4(__half2float(b2[c]), __half2float(b2[c + 1]), __half2float(b2[c + 2]),
+                             __half2float(b2[c + 3]));
+    const float4* p = reinterpret_cast<const float4*>(part) + e4;
+    const size_t stride = (size_t)B * d / 4;
+    for (int s = 0; s < S; ++s) {
+        const float4 v = p[(size_t)s * stride];
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+    }
+    reinterpret_cast<float4*>(y)[e4] = acc;
+}
+
+// -------------------------------------------------------------- normalisation
+
+__global__ void __launch_bounds__(256) k_rmsnorm(const float* __restrict__ y, int d, float eps,
+                                                 __half* __restrict__ x) {
+    __shared__ float red[8];
+    const float* yb = y + (size_t)blockIdx.x * d;
+    float ss = 0.f;
+    for (int c = threadIdx.x; c < d; c += blockDim.x) ss = fmaf(yb[c], yb[c], ss);
+    ss = warp_sum(ss);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    if (warp == 0) {
+        float v = lane < 8 ? red[lane] : 0.f;
+        v = warp_sum(v);
+        if (lane == 0) red[0] = v;
+    }
+    __syncthreads();
+    const float scale = rsqrtf(red[0] / (float)d + eps);
+    __half* xb = x + (size_t)blockIdx.x * d;
+    for (int c = threadIdx.x; c < d; c += blockDim.x) xb[c] = __float2half_rn(yb[c] * scale);
+}
+
+// ------------------------------------------------------------------ launchers
+
+namespace {
+
+template <typename F>
+cudaError_t for_token_chunks(int B, F&& f) {
+    for (int b0 = 0; b0 < B;) {
+        const int left = B - b0;
+        const int tb = left >= 8 ? 8 : left >= 4 ? 4 : left >= 2 ? 2 : 1;
+        cudaError_t e = f(b0, tb);
+        if (e != cudaSuccess) return e;
+        b0 += tb;
+    }
+    return cudaSuccess;
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, size_t bytes) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+}  // namespace
+
+cudaError_t launch_predict(const Plan& p, const __half* x, const __half* p1, const __half* p2,
+                           const __half* bpred, float tau, uint32_t* mask, float* upart,
+                           cudaStream_t s) {
+    return for_token_chunks(p.B, [&](int b0, int tb) -> cudaError_t {
+        dim3 gu((p.r + 7) / 8, p.u_splits);
+        const int ws = (p.W + 3) / 4;
+        const size_t sm = (size_t)tb * p.r * sizeof(float);
+#define PI_PRED(TBV)                                                                               \
+    case TBV: {                                                                                    \
+        k_predict_u<TBV><<<gu, 256, 0, s>>>(x, p.B, b0, p1, p.d, p.r, p.u_seg, upart);             \
+        cudaError_t e = set_smem(k_predict_s<TBV>, sm);                                            \
+        if (e != cudaSuccess) return e;                                                            \
+        k_predict_s<TBV><<<ws, 128, sm, s>>>(p2, bpred, upart, p.u_splits, p.B, b0, p.r, p.F, p.W, \
+                                             tau, mask);                                           \
+        break;                                                                                     \
+    }
+        switch (tb) {
+            PI_PRED(1)
+            PI_PRED(2)
+            PI_PRED(4)
+            PI_PRED(8)
+        }
+#undef PI_PRED
+        return cudaGetLastError();
+    });
+}
+
+cudaError_t launch_compact(const Plan& p, const uint32_t* mask, const int32_t* table, int32_t* idx,
+                           int32_t* orig, int32_t* count, cudaStream_t s) {
+    k_compact<<<1, 1024, 0, s>>>(mask, p.B, p.W, p.F, table, idx, orig, count);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fc1(const Plan& p, const __half* x, const LayerPtrs& w, const int32_t* idx,
+                       const int32_t* count, const uint32_t* mask, float* h, cudaStream_t s) {
+    const int kind = p.int4 ? 2 : (p.gated ? 1 : 0);
+    return for_token_chunks(p.B, [&](int b0, int tb) -> cudaError_t {
+        const size_t sm = (size_t)tb * p.d * sizeof(__half);
+        const int blocks_max = (p.F + 7) / 8;
+        int grid = p.nsm * 4;
+        if (grid > blocks_max) grid = blocks_max;
+        cudaError_t e = cudaSuccess;
+#define PI_FC1(TBV, KV)                                                                       \
+    if (tb == TBV && kind == KV) {                                                            \
+        e = set_smem(k_fc1<TBV, KV>, sm);                                                     \
+        if (e != cudaSuccess) return e;                                                       \
+        k_fc1<TBV, KV><<<grid, 256, sm, s>>>(x, p.B, b0, p.d, w, idx, count, mask, p.W, h); \
+    }
+        PI_FC1(1, 0) PI_FC1(2, 0) PI_FC1(4, 0) PI_FC1(8, 0)
+        PI_FC1(1, 1) PI_FC1(2, 1) PI_FC1(4, 1) PI_FC1(8, 1)
+        PI_FC1(1, 2) PI_FC1(2, 2) PI_FC1(4, 2) PI_FC1(8, 2)
+#undef PI_FC1
+        return cudaGetLastError();
+    });
+}
+
+cudaError_t launch_fc2(const Plan& p, const float* h, const int32_t* idx, const int32_t* count,
+                       const LayerPtrs& w, float* partial, float* y, cudaStream_t s) {
+    cudaError_t e = for_token_chunks(p.B, [&](int b0, int tb) -> cudaError_t {
+        dim3 grid(p.fc2_tiles, p.fc2_splits);
+#define PI_FC2(TBV, IV)                                                                       \
+    if (tb == TBV && p.int4 == IV)                                                            \
+        k_fc2_part<TBV, IV><<<grid, 256, 0, s>>>(h, p.B, b0, idx, count, p.d, w.w2t, w.w2ts, \
+                                                 partial);
+        PI_FC2(1, false) PI_FC2(2, false) PI_FC2(4, false) PI_FC2(8, false)
+        PI_FC2(1, true) PI_FC2(2, true) PI_FC2(4, true) PI_FC2(8, true)
+#undef PI_FC2
+        return cudaGetLastError();
+    });
+    if (e != cudaSuccess) return e;
+    const int total4 = p.B * p.d / 4;
+    k_fc2_reduce<<<(total4 + 255) / 256, 256, 0, s>>>(partial, p.fc2_splits, p.B, p.d, w.b2, y);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm(int d, int B, const float* y, float eps, __half* x, cudaStream_t s) {
+    k_rmsnorm<<<B, 256, 0, s>>>(y, d, eps, x);
+    return cudaGetLastError();
+}
+
+}  // namespace pi

@@ -1,0 +1,176 @@
+/*
+ * pi.h -- C ABI of the neuron-aware sparse FFN decode path (one GPU, sm_103a).
+ *
+ * Per decode layer the path computes, for each token x (length d):
+ *   1. predictor:  u = P1 x,  s = P2 u + b,  neuron k predicted active iff s_k > tau
+ *   2. compaction: the ascending list of predicted-active storage rows
+ *   3. FC1:        h_j = ReLU(W1[idx_j] . x + b1[idx_j])     (gated: * (Wu[idx_j] . x))
+ *   4. FC2:        y = b2 + sum_j h_j * W2t[idx_j, :]
+ * following the pages describing PowerInfer (PowerInfer summary (CSDN)):
+ * section "Background" (FC1, ReLU, FC2 as products of the input with neurons,
+ * i.e. rows/columns of the weight matrices), section "Adaptive sparse
+ * predictor" (an input/hidden/output predictor of which neurons fire),
+ * section "Neuron-aware operator" (decide whether a neuron is active, then
+ * process only its row or column, with no dense-format conversion) and section
+ * "Neuron placement and management" (a table maps each stored neuron to its
+ * original position).
+ *
+ * Conventions for every entry point:
+ *  - Every pointer argument except the descriptors is DEVICE memory owned by
+ *    the caller; the library allocates nothing and keeps no pointer after the
+ *    call returns.  Descriptors (pi_layer_desc, pi_layer_weights) are HOST
+ *    structs read during the call only.
+ *  - All calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL = the legacy default stream).  Device-side counts stay on the device:
+ *    no call synchronises the host except pi_last_device_status.
+ *  - Arguments are validated on the host before anything is launched; a bad
+ *    argument returns PI_ERR_INVALID_ARG and launches nothing.  A failed launch
+ *    returns PI_ERR_CUDA.
+ *  - Binary16 data is passed as pi_half (IEEE 754 binary16 bit patterns).
+ *  - Per-neuron arrays (W1, Wu, W2t, their scales, b1, P2 rows, table) are in
+ *    STORAGE order: storage row k holds original neuron table[k].
+ *  - Masks: bit k of a mask is bit (k % 32) of 32-bit word k / 32; a batch of
+ *    B masks is B consecutive runs of ceil(F/32) words.
+ *  - Alignment: every weight, x and workspace pointer 16-byte aligned;
+ *    d % 8 == 0 (fp16) and d % 32 == 0 (INT4); rank % 8 == 0.
+ *  - Calls on distinct streams with distinct outputs and workspaces may run
+ *    concurrently; calls sharing a workspace must be stream-ordered.
+ */
+#ifndef PI_H
+#define PI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(PI_BUILD) && defined(__GNUC__)
+#define PI_API __attribute__((visibility("default")))
+#else
+#define PI_API
+#endif
+
+typedef uint16_t pi_half; /* IEEE 754 binary16 bit pattern */
+
+typedef enum {
+    PI_OK = 0,
+    PI_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment or descriptor      */
+    PI_ERR_UNSUPPORTED = 2, /* valid request this build does not implement       */
+    PI_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed              */
+    PI_ERR_TIMEOUT = 4,     /* a bounded device-side wait expired                */
+    PI_ERR_WORKSPACE = 5    /* workspace NULL, misaligned or smaller than needed */
+} pi_status;
+
+typedef enum {
+    PI_W_F16 = 0,     /* rows of d binary16 values                                    */
+    PI_W_INT4_G32 = 1 /* rows of d/2 bytes of INT4 codes (even element in the low      */
+                      /* nibble, two's complement, value q*scale) + d/32 binary16 scales */
+} pi_wdtype;
+
+typedef struct {
+    int d;            /* model width                                  */
+    int ffn;          /* FFN width F (number of neurons)              */
+    int rank;         /* predictor rank r                             */
+    int batch;        /* tokens B processed together (1..32)          */
+    pi_wdtype wdtype; /* FC1/FC2 weight format (Wu is always fp16)    */
+    int gated;        /* 1: h = ReLU(Wg x + bg) * (Wu x)              */
+} pi_layer_desc;
+
+typedef struct {
+    const void *w1;          /* [F, d] fp16, or [F, d/2] INT4 codes (gate rows when gated) */
+    const pi_half *w1_scales; /* [F, d/32] (INT4 only, else NULL)                           */
+    const pi_half *b1;       /* [F]  FC1 (gate) bias, also the predictor bias              */
+    const pi_half *wu;       /* [F, d] fp16 up-projection rows (gated only, else NULL)     */
+    const void *w2t;         /* [F, d] fp16 or INT4 codes: row k = neuron k's FC2 column   */
+    const pi_half *w2t_scales; /* [F, d/32] (INT4 only, else NULL)                         */
+    const pi_half *b2;       /* [d]                                                        */
+    const pi_half *p1;       /* [r, d] predictor input layer                               */
+    const pi_half *p2;       /* [F, r] predictor output layer (storage order)              */
+    const int32_t *table;    /* [F] storage row -> original neuron id                      */
+} pi_layer_weights;
+
+/* Bytes of workspace pi_predict, pi_sparse_fc2 and pi_ffn_layer need for
+ * `desc` (0 if the descriptor is invalid). */
+PI_API size_t pi_workspace_bytes(const pi_layer_desc *desc);
+
+/*
+ * Predictor (PowerInfer summary (CSDN), section "Adaptive sparse predictor").
+ *   u_b = P1 x_b (fp32), s_b = P2 u_b + bpred (fp32), mask_b bit k = s_bk > tau.
+ * x: [B, d] fp16.  mask: [B, ceil(F/32)] uint32 (bits past F are 0).
+ * workspace: >= pi_workspace_bytes(desc) bytes, 16-byte aligned.
+ */
+PI_API pi_status pi_predict(const pi_layer_desc *desc, const pi_half *x, const pi_half *p1,
+                     const pi_half *p2, const pi_half *bpred, float tau, uint32_t *mask,
+                     void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Active-neuron compaction (section "Neuron-aware operator": first decide
+ * which neurons are active; section "Neuron placement and management": the
+ * table gives each stored neuron's original position).
+ * For B == 1 compacts mask; for B > 1 compacts the union (bitwise OR) of the
+ * B masks.  idx: [F] int32, ascending storage rows, first *d_count valid.
+ * orig_idx (nullable, requires table): table[idx].  d_count: [1] int32.
+ */
+PI_API pi_status pi_compact(const pi_layer_desc *desc, const uint32_t *mask, const int32_t *table,
+                     int32_t *idx, int32_t *orig_idx, int32_t *d_count, void *stream);
+
+/*
+ * Row-gathered FC1 with fused bias and ReLU (section "Background"; section
+ * "Neuron-aware operator": only the rows of active neurons are read).
+ *   h[j*B + b] = ReLU(W1[idx_j] . x_b + b1[idx_j])  (gated: times Wu[idx_j] . x_b)
+ * for j < *d_count; when B > 1 and mask != NULL, h[j*B+b] = 0 wherever token
+ * b's own mask bit idx_j is 0.  h: [F*B] fp32 (neuron-major).
+ */
+PI_API pi_status pi_sparse_fc1(const pi_layer_desc *desc, const pi_half *x, const pi_layer_weights *w,
+                        const int32_t *idx, const int32_t *d_count, const uint32_t *mask,
+                        float *h, void *stream);
+
+/*
+ * FC2 as a gather-accumulate over W2t rows (section "Background"; section
+ * "Neuron-aware operator": only the columns of active neurons, stored as rows).
+ *   y[b*d + c] = b2[c] + sum_{j < *d_count} h[j*B + b] * W2t[idx_j, c]   (fp32)
+ * Reduced without atomics in a fixed order (bitwise reproducible).
+ */
+PI_API pi_status pi_sparse_fc2(const pi_layer_desc *desc, const float *h, const int32_t *idx,
+                        const int32_t *d_count, const pi_layer_weights *w, float *y,
+                        void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * One whole decode layer: predictor -> compaction -> FC1 -> FC2 on `stream`.
+ * x: [B, d] fp16; y: [B, d] fp32.  The per-token masks, the union index list
+ * and its count are left in the workspace (see pi_workspace_layout).
+ */
+PI_API pi_status pi_ffn_layer(const pi_layer_desc *desc, const pi_half *x, const pi_layer_weights *w,
+                       float tau, void *workspace, size_t ws_bytes, float *y, void *stream);
+
+/* Offsets (bytes) of the intermediates pi_ffn_layer leaves in the workspace. */
+typedef struct {
+    size_t mask;  /* uint32 [B, ceil(F/32)] per-token masks         */
+    size_t idx;   /* int32 [F] ascending active rows (union if B>1) */
+    size_t count; /* int32 [1]                                      */
+    size_t h;     /* float [F*B] FC1 outputs                        */
+    size_t total; /* == pi_workspace_bytes                          */
+} pi_workspace_layout_t;
+PI_API pi_status pi_workspace_layout(const pi_layer_desc *desc, pi_workspace_layout_t *out);
+
+/*
+ * Inter-layer normalisation of a decode stack: x_out[b, c] =
+ * fp16(y[b, c] / sqrt(mean_c(y[b, :]^2) + eps)) with round-to-nearest-even.
+ * y: [B, d] fp32; x_out: [B, d] fp16.
+ */
+PI_API pi_status pi_rmsnorm_half(int d, int batch, const float *y, float eps, pi_half *x_out,
+                          void *stream);
+
+PI_API const char *pi_status_string(pi_status s);
+
+/* Synchronises `stream`, then returns and clears the device status word set
+ * by bounded device-side waits (PI_OK or PI_ERR_TIMEOUT). */
+PI_API pi_status pi_last_device_status(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PI_H */
