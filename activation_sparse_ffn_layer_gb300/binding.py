@@ -43,7 +43,7 @@ _lib = None
 
 EXPORTS = ("pi_workspace_bytes", "pi_workspace_layout", "pi_predict", "pi_compact", "pi_sparse_fc1",
            "pi_sparse_fc2", "pi_ffn_layer", "pi_rmsnorm_half", "pi_status_string",
-           "pi_last_device_status")
+           "pi_last_device_status", "pi_launches_per_layer", "pi_ffn_stack", "pi_debug_wait_timeout")
 
 
 def library_path() -> str:
@@ -74,6 +74,9 @@ def lib(path: Optional[str] = None):
         "pi_rmsnorm_half": (I, [I, I, P, Fl, P, P]),
         "pi_status_string": (C.c_char_p, [I]),
         "pi_last_device_status": (I, [P]),
+        "pi_launches_per_layer": (I, [D]),
+        "pi_ffn_stack": (I, [D, I, C.POINTER(pi_layer_weights), P, P, Fl, Fl, P, S, P, P, P]),
+        "pi_debug_wait_timeout": (I, [C.c_longlong, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -167,6 +170,31 @@ def pi_ffn_layer(desc, x, wstruct, tau: float, workspace, y):
                                               _ptr(y), _stream()))
 
 
+def pi_ffn_stack(desc, wstructs, ranks, x, tau: float, eps: float, workspace, y, x_trace=None):
+    """`wstructs`: a ctypes array of pi_layer_weights (see weights_array);
+    `ranks`: a ctypes int array or None."""
+    n = len(wstructs)
+    _check("pi_ffn_stack", lib().pi_ffn_stack(C.byref(desc), n, wstructs, ranks, _ptr(x), float(tau), float(eps),
+                                              _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                              _ptr(y), _ptr(x_trace), _stream()))
+
+
+def weights_array(layers):
+    """A ctypes array of pi_layer_weights over a list of layers (keep them alive)."""
+    arr = (pi_layer_weights * len(layers))()
+    for i, w in enumerate(layers):
+        arr[i] = weights_struct(w)
+    return arr
+
+
+def ranks_array(layers):
+    return (C.c_int * len(layers))(*[int(w.r) for w in layers])
+
+
+def pi_debug_wait_timeout(timeout_ns: int):
+    _check("pi_debug_wait_timeout", lib().pi_debug_wait_timeout(int(timeout_ns), _stream()))
+
+
 def pi_rmsnorm_half(d: int, batch: int, y, eps: float, x_out):
     _check("pi_rmsnorm_half", lib().pi_rmsnorm_half(int(d), int(batch), _ptr(y), float(eps), _ptr(x_out),
                                                     _stream()))
@@ -174,6 +202,10 @@ def pi_rmsnorm_half(d: int, batch: int, y, eps: float, x_out):
 
 def pi_status_string(status: int) -> str:
     return lib().pi_status_string(int(status)).decode()
+
+
+def pi_launches_per_layer(desc) -> int:
+    return int(lib().pi_launches_per_layer(C.byref(desc)))
 
 
 def pi_last_device_status() -> int:

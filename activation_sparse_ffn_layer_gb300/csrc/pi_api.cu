@@ -65,13 +65,19 @@ bool make_plan(const pi_layer_desc& desc, Plan* p) {
     const int max_s2 = (q.F + 7) / 8;
     if (s2 > max_s2) s2 = max_s2;
     q.fc2_splits = s2 < 1 ? 1 : s2;
-    size_t off = 0;
+    // fused exchange region first (its epoch word stays at offset 0 for every
+    // descriptor that shares the workspace), then the per-step buffers
+    q.rmax_su = (size_t)16 * q.nsm + 2 * (size_t)q.r;
+    q.xchg_bytes = up(fused_workspace_bytes(q.d, q.F, q.rmax_su, q.nsm));
+    q.fused = q.B == 1 && fused_supported(q.d, q.F, q.r, q.int4, q.nsm);
+    size_t off = q.xchg_bytes;
     q.off_mask = off;  off = up(off + sizeof(uint32_t) * (size_t)q.B * q.W);
     q.off_idx = off;   off = up(off + sizeof(int32_t) * (size_t)q.F);
     q.off_count = off; off = up(off + sizeof(int32_t) * 4);
     q.off_h = off;     off = up(off + sizeof(float) * (size_t)q.F * q.B);
     q.off_upart = off; off = up(off + sizeof(float) * (size_t)q.u_splits * q.B * q.r);
     q.off_part = off;  off = up(off + sizeof(float) * (size_t)q.fc2_splits * q.B * q.d);
+    q.off_xbuf = off;  off = up(off + sizeof(uint16_t) * 2 * (size_t)q.B * q.d);
     q.total = off;
     *p = q;
     return true;
@@ -119,6 +125,65 @@ T* at(void* ws, size_t off) {
 }
 
 }  // namespace
+
+constexpr int kMaxStackLayers = 96;
+constexpr long long kWaitTimeoutNs = 2000000000ll;  // 2 s per wait
+
+// One decode step through n layers: the fused persistent kernel when the plan
+// allows it, else the per-step kernels with the normalisation between layers.
+cudaError_t run_stack(const Plan& p, int n, const LayerPtrs* lp, const int* ranks, const __half* x, float tau,
+                      float eps, void* ws, float* y, __half* x_trace, cudaStream_t s) {
+    uint32_t* mask = at<uint32_t>(ws, p.off_mask);
+    int32_t* idx = at<int32_t>(ws, p.off_idx);
+    int32_t* cnt = at<int32_t>(ws, p.off_count);
+    float* h = at<float>(ws, p.off_h);
+    if (p.fused) {
+        int rk[kMaxStackLayers];
+        for (int l = 0; l < n; ++l) rk[l] = ranks ? ranks[l] : p.r;
+        FusedStackArgs a{};
+        a.L = n;
+        a.d = p.d;
+        a.F = p.F;
+        a.G = p.nsm;
+        a.int4 = p.int4;
+        a.gated = p.gated;
+        a.tau = tau;
+        a.eps = eps;
+        a.timeout_ns = kWaitTimeoutNs;
+        a.layers = lp;
+        a.ranks = rk;
+        a.x_in = x;
+        a.y_out = y;
+        a.x_trace = x_trace;
+        a.xchg = ws;
+        a.rmax_su = p.rmax_su;
+        a.mask_out = mask;
+        a.idx_out = idx;
+        a.count_out = cnt;
+        a.h_out = h;
+        return launch_fused(a, s);
+    }
+    const __half* cur = x;
+    __half* xbuf = at<__half>(ws, p.off_xbuf);
+    for (int l = 0; l < n; ++l) {
+        Plan q = p;
+        q.r = ranks ? ranks[l] : p.r;
+        const LayerPtrs& w = lp[l];
+        cudaError_t e = launch_predict(q, cur, w.p1, w.p2, w.b1, tau, mask, at<float>(ws, p.off_upart), s);
+        if (e == cudaSuccess) e = launch_compact(q, mask, nullptr, idx, nullptr, cnt, s);
+        if (e == cudaSuccess) e = launch_fc1(q, cur, w, idx, cnt, q.B > 1 ? mask : nullptr, h, s);
+        if (e == cudaSuccess) e = launch_fc2(q, h, idx, cnt, w, at<float>(ws, p.off_part), y, s);
+        if (e != cudaSuccess) return e;
+        if (l + 1 < n) {
+            __half* nxt = x_trace ? x_trace + (size_t)l * p.B * p.d : xbuf + (size_t)(l % 2) * p.B * p.d;
+            e = launch_rmsnorm(p.d, p.B, y, eps, nxt, s);
+            if (e != cudaSuccess) return e;
+            cur = nxt;
+        }
+    }
+    return cudaSuccess;
+}
+
 }  // namespace pi
 
 using namespace pi;
@@ -195,24 +260,49 @@ pi_status pi_ffn_layer(const pi_layer_desc* desc, const pi_half* x, const pi_lay
         return PI_ERR_INVALID_ARG;
     if (!workspace || !aligned16(workspace) || ws_bytes < p.total) return PI_ERR_WORKSPACE;
     if ((size_t)8 * p.d * sizeof(uint16_t) > 200 * 1024) return PI_ERR_UNSUPPORTED;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     const LayerPtrs l = ptrs(w);
-    const __half* xh = reinterpret_cast<const __half*>(x);
-    uint32_t* mask = at<uint32_t>(workspace, p.off_mask);
-    int32_t* idx = at<int32_t>(workspace, p.off_idx);
-    int32_t* cnt = at<int32_t>(workspace, p.off_count);
-    float* h = at<float>(workspace, p.off_h);
-    cudaError_t e = launch_predict(p, xh, l.p1, l.p2, l.b1, tau, mask, at<float>(workspace, p.off_upart), s);
-    if (e == cudaSuccess) e = launch_compact(p, mask, nullptr, idx, nullptr, cnt, s);
-    if (e == cudaSuccess) e = launch_fc1(p, xh, l, idx, cnt, p.B > 1 ? mask : nullptr, h, s);
-    if (e == cudaSuccess) e = launch_fc2(p, h, idx, cnt, l, at<float>(workspace, p.off_part), y, s);
-    return from_cuda(e);
+    return from_cuda(run_stack(p, 1, &l, nullptr, reinterpret_cast<const __half*>(x), tau, 0.f, workspace, y,
+                               nullptr, static_cast<cudaStream_t>(stream)));
+}
+
+pi_status pi_ffn_stack(const pi_layer_desc* desc, int n_layers, const pi_layer_weights* layers, const int* ranks,
+                       const pi_half* x, float tau, float eps, void* workspace, size_t ws_bytes, float* y,
+                       pi_half* x_trace, void* stream) {
+    Plan p;
+    if (!desc || !make_plan(*desc, &p)) return PI_ERR_INVALID_ARG;
+    if (n_layers < 1 || n_layers > kMaxStackLayers || !layers || !x || !aligned16(x) || !y || !aligned16(y) ||
+        !(eps >= 0.f))
+        return PI_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace) || ws_bytes < p.total) return PI_ERR_WORKSPACE;
+    if ((size_t)8 * p.d * sizeof(uint16_t) > 200 * 1024) return PI_ERR_UNSUPPORTED;
+    LayerPtrs lp[kMaxStackLayers];
+    for (int l = 0; l < n_layers; ++l) {
+        if (!weights_ok(p, &layers[l], true, true, true)) return PI_ERR_INVALID_ARG;
+        if (ranks && (ranks[l] <= 0 || ranks[l] % 8 != 0 || ranks[l] > p.r)) return PI_ERR_INVALID_ARG;
+        lp[l] = ptrs(&layers[l]);
+    }
+    return from_cuda(run_stack(p, n_layers, lp, ranks, reinterpret_cast<const __half*>(x), tau, eps, workspace, y,
+                               reinterpret_cast<__half*>(x_trace), static_cast<cudaStream_t>(stream)));
 }
 
 pi_status pi_rmsnorm_half(int d, int batch, const float* y, float eps, pi_half* x_out, void* stream) {
     if (d <= 0 || batch <= 0 || !y || !x_out || !(eps >= 0.f)) return PI_ERR_INVALID_ARG;
     return from_cuda(launch_rmsnorm(d, batch, y, eps, reinterpret_cast<__half*>(x_out),
                                     static_cast<cudaStream_t>(stream)));
+}
+
+int pi_launches_per_layer(const pi_layer_desc* desc) {
+    Plan p;
+    if (!desc || !make_plan(*desc, &p)) return -1;
+    int chunks = 0;
+    for (int b0 = 0; b0 < p.B;) {
+        const int left = p.B - b0;
+        b0 += left >= 8 ? 8 : left >= 4 ? 4 : left >= 2 ? 2 : 1;
+        ++chunks;
+    }
+    if (p.fused) return 1;  // one persistent kernel
+    // predictor: 2 per token chunk; compaction: 1; FC1: 1 per chunk; FC2: 1 per chunk + 1 reduction
+    return 2 * chunks + 1 + chunks + chunks + 1;
 }
 
 const char* pi_status_string(pi_status s) {
@@ -228,9 +318,14 @@ const char* pi_status_string(pi_status s) {
 }
 
 pi_status pi_last_device_status(void* stream) {
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaStreamSynchronize(s) != cudaSuccess) return PI_ERR_CUDA;
-    return PI_OK;
+    int v = 0;
+    if (read_and_clear_status(&v, static_cast<cudaStream_t>(stream)) != cudaSuccess) return PI_ERR_CUDA;
+    return v == 0 ? PI_OK : static_cast<pi_status>(v);
+}
+
+pi_status pi_debug_wait_timeout(long long timeout_ns, void* stream) {
+    if (timeout_ns <= 0 || timeout_ns > 10000000000ll) return PI_ERR_INVALID_ARG;
+    return from_cuda(launch_wait_nothing(timeout_ns, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -1,0 +1,863 @@
+// pi_fused.cu -- the whole decode step of a layer stack in ONE persistent,
+// cooperative launch (one CTA per SM), batch 1.
+//
+// Per layer (PowerInfer summary (CSDN): "Adaptive sparse predictor",
+// "Neuron-aware operator", "Background"):
+//   A  u-partials  = P1[i, segment] . x              (items spread over all warps)
+//   B  mask units  = 16 rows of (P2 u + b > tau)      (units spread over CTAs)
+//   C  compaction of the mask (every CTA, redundantly), then this CTA's equal
+//      share of the active list: FC1 rows (bias + ReLU [+ gate]) and the FC2
+//      gather-accumulate of its neurons into a private partial y
+//   D  y columns   = b2 + sum of all partials (fixed order), sum of squares
+//   (next layer)   x = fp16(y / sqrt(mean(y^2) + eps))
+// with one grid barrier after each phase.
+//
+// The barrier is a single counter: each CTA adds 1 with release semantics and
+// spins (one thread, acquire loads) until the count reaches the barrier's
+// target.  Targets are relative to an epoch kept in the workspace and advanced
+// by every launch, so the counter is never reset.  Every wait is bounded by a
+// wall-clock limit: on expiry the status word becomes PI_ERR_TIMEOUT and the
+// kernel returns (the other CTAs then time out at their next barrier).
+// Exchanged data is written with plain stores and read with L2-only loads.
+//
+// While a layer's FC rows stream from HBM, the next layer's predictor rows of
+// this CTA are bulk-prefetched into L2.
+#include <cuda_runtime.h>
+
+#include "pi_common.cuh"
+#include "pi_internal.h"
+
+namespace pi {
+
+__device__ int g_pi_status = 0;
+
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kBarriersPerLayer = 4;
+
+PI_DEV unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+PI_DEV void prefetch_l2(const void* p, unsigned bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+PI_DEV unsigned ld_acquire(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+PI_DEV float4 ld_cg4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
+
+// Grid barrier number `k` of this launch.  Returns false (and sets the status
+// word) if the wait exceeded timeout_ns or another CTA already failed.
+PI_DEV bool grid_sync(unsigned* counter, unsigned target, long long timeout_ns, int* bad) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(counter) : "memory");
+        unsigned v = ld_acquire(counter);
+        if ((int)(v - target) < 0) {
+            const unsigned long long t0 = globaltimer();
+            int polls = 0;
+            while ((int)((v = ld_acquire(counter)) - target) < 0) {
+                if (++polls == 32) {
+                    polls = 0;
+                    if ((long long)(globaltimer() - t0) > timeout_ns || *(volatile int*)&g_pi_status != 0) {
+                        atomicExch(&g_pi_status, (int)PI_ERR_TIMEOUT);
+                        *bad = 1;
+                        break;
+                    }
+                }
+            }
+        }
+    }
+    __syncthreads();
+    return *(volatile int*)bad == 0;
+}
+
+}  // namespace
+
+struct FusedLayer {
+    const void* w1;
+    const __half* w1s;
+    const __half* b1;
+    const __half* wu;
+    const void* w2t;
+    const __half* w2ts;
+    const __half* b2;
+    const __half* p1;
+    const __half* p2;
+    int r;    // predictor rank
+    int su;   // splits of d in the P1 x items
+    int seg;  // elements per split (multiple of 8)
+};
+
+constexpr int kMaxFusedLayers = 96;
+
+struct FusedParams {
+    int L, d, F, M, W;   // M = ceil(F / 16) mask units, W = ceil(F / 32) mask words
+    float tau, eps;
+    long long timeout_ns;
+    const __half* x_in;     // [d]
+    float* y_out;           // [d]
+    __half* x_trace;        // nullable [L-1][d]: normalised inputs of layers 1..L-1
+    unsigned long long* epoch;  // [1] barriers completed by earlier launches
+    unsigned* counter;          // [1] barrier arrivals (mod 2^32)
+    float* xu;                  // [max su*r]
+    uint32_t* xmask;            // [W]
+    float* xyp;                 // [G][d]
+    float* xy;                  // [d]
+    float* xss;                 // [G]
+    uint32_t* mask_out;         // [W] plain mask of the last layer
+    int32_t* idx_out;           // [F]
+    int32_t* count_out;         // [1]
+    float* h_out;               // [F]
+    FusedLayer layers[kMaxFusedLayers];
+};
+
+// Dynamic smem layout (bytes): xf float[d] | u float[rmax] | ustage float[usmax]
+//   | m16 int[M] | upre int[M+1] | lidx int[cap] | lh float[cap] | scratch
+struct SmemPlan {
+    int d, rmax, usmax, M, cap;
+    __host__ __device__ int off_u() const { return d * 4; }
+    __host__ __device__ int off_ust() const { return off_u() + rmax * 4; }
+    __host__ __device__ int off_m16() const { return off_ust() + ((usmax + 3) / 4) * 16; }
+    __host__ __device__ int off_upre() const { return off_m16() + ((M + 1) / 2) * 8; }
+    __host__ __device__ int off_lidx() const { return off_upre() + (M + 1) * 4; }
+    __host__ __device__ int off_lh() const { return off_lidx() + cap * 4; }
+    __host__ __device__ int off_scr() const { return ((off_lh() + cap * 4 + 15) / 16) * 16; }
+    __host__ __device__ int bytes() const { return off_scr() + 4096 * 4; }
+};
+
+// dot of 8 fp16 weights with 8 fp32 values in smem
+PI_DEV float dot8(const uint4& w, const float* xs) {
+    float wf[8];
+    h8_to_f8(w, wf);
+    const float4 a = reinterpret_cast<const float4*>(xs)[0];
+    const float4 b = reinterpret_cast<const float4*>(xs)[1];
+    float acc = wf[0] * a.x;
+    acc = fmaf(wf[1], a.y, acc);
+    acc = fmaf(wf[2], a.z, acc);
+    acc = fmaf(wf[3], a.w, acc);
+    acc = fmaf(wf[4], b.x, acc);
+    acc = fmaf(wf[5], b.y, acc);
+    acc = fmaf(wf[6], b.z, acc);
+    acc = fmaf(wf[7], b.w, acc);
+    return acc;
+}
+
+// Block-wide exclusive scan of one int per thread (kThreads threads).
+PI_DEV int block_exscan(int v, int* scr, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(FULL, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) scr[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < kWarps ? scr[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(FULL, w, o);
+            if (lane >= o) w += t;
+        }
+        if (lane < kWarps) scr[lane] = w;
+    }
+    __syncthreads();
+    const int base = warp > 0 ? scr[warp - 1] : 0;
+    *total = scr[kWarps - 1];
+    __syncthreads();
+    return base + incl - v;
+}
+
+#ifdef PI_PHASE_TRACE
+// Phase timestamps of every CTA: [layer][slot][cta] globaltimer ns and clock64.
+constexpr int kTraceSlots = 8;
+constexpr int kTraceCtas = 256;
+__device__ unsigned long long g_pi_trace[96 * kTraceSlots * kTraceCtas];
+__device__ unsigned long long g_pi_trace_clk[96 * kTraceSlots * kTraceCtas];
+#define PI_STAMP(l, k)                                                              \
+    do {                                                                            \
+        if (tid == 0) {                                                             \
+            g_pi_trace[((l) * kTraceSlots + (k)) * kTraceCtas + c] = globaltimer(); \
+            g_pi_trace_clk[((l) * kTraceSlots + (k)) * kTraceCtas + c] = clock64(); \
+        }                                                                           \
+    } while (0)
+#else
+#define PI_STAMP(l, k) \
+    do {               \
+    } while (0)
+#endif
+
+// KIND 0: fp16 rows; 1: fp16 gate + up rows; 2: INT4 group-32 rows.
+// NCH: 4096-column chunks of d that each thread covers in FC2 (fp16 rows).
+template <int KIND, int NCH>
+__global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_constant__ FusedParams p) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int G = gridDim.x, c = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int d = p.d, F = p.F, M = p.M;
+    const long long tmo = p.timeout_ns;
+    int rmax = 8, usmax = 8;
+    for (int l = 0; l < p.L; ++l) {
+        rmax = max(rmax, p.layers[l].r);
+        usmax = max(usmax, p.layers[l].r * p.layers[l].su);
+    }
+    const int cap = F / G + 2;
+    const SmemPlan sp{d, rmax, usmax, M, cap};
+    float* xf = reinterpret_cast<float*>(smem);
+    float* us = reinterpret_cast<float*>(smem + sp.off_u());
+    float* ust = reinterpret_cast<float*>(smem + sp.off_ust());
+    uint16_t* m16 = reinterpret_cast<uint16_t*>(smem + sp.off_m16());
+    int* upre = reinterpret_cast<int*>(smem + sp.off_upre());
+    int* lidx = reinterpret_cast<int*>(smem + sp.off_lidx());
+    float* lh = reinterpret_cast<float*>(smem + sp.off_lh());
+    float* red = reinterpret_cast<float*>(smem + sp.off_scr());
+    int* scr = reinterpret_cast<int*>(smem + sp.off_scr());
+    __shared__ int bad;
+    __shared__ float rs_s;
+    __shared__ unsigned preds[8][kWarps];
+    if (tid == 0) bad = 0;
+
+    // barrier targets: the counter holds G arrivals per barrier ever completed
+    const unsigned long long ebase = __ldcg(p.epoch);
+    unsigned nbar = 0;
+    auto sync = [&]() -> bool {
+        ++nbar;
+        return grid_sync(p.counter, (unsigned)((ebase + nbar) * (unsigned long long)G), tmo, &bad);
+    };
+    // CTA 0 advances the epoch when it leaves, by every barrier this launch
+    // schedules (also after a failure: the counts then no longer matter, the
+    // status word reports the failure)
+    auto leave = [&]() {
+        if (c == 0 && tid == 0) {
+            const unsigned long long next = ebase + (unsigned long long)kBarriersPerLayer * p.L;
+            __stcg(p.epoch, next);
+        }
+    };
+
+    // prefetch this CTA's predictor rows of layer l into L2
+    auto prefetch_predictor = [&](int l) {
+        if (tid != 0 || l >= p.L) return;
+        const FusedLayer& ly = p.layers[l];
+        const int items = ly.r * ly.su;
+        for (int q = c * kWarps; q < items; q += G * kWarps) {
+            const int last = min(items, q + kWarps);
+            for (int t = q; t < last; ++t) {
+                const int i = t / ly.su, s = t % ly.su;
+                const int c0 = s * ly.seg, c1 = min(d, c0 + ly.seg);
+                prefetch_l2(ly.p1 + (size_t)i * d + c0, (unsigned)(c1 - c0) * 2u);
+            }
+        }
+        for (int m = c; m < M; m += G) {
+            const int rows = min(16, F - m * 16);
+            prefetch_l2(ly.p2 + (size_t)m * 16 * ly.r, (unsigned)(rows * ly.r * 2));
+        }
+    };
+    prefetch_predictor(0);
+    __syncthreads();
+
+    // phase-D columns of this CTA: a contiguous range of 4-column groups
+    const int ng4 = d / 4;
+    const int g0 = (int)(((long long)ng4 * c) / G), g1 = (int)(((long long)ng4 * (c + 1)) / G);
+    const int ngm = g1 - g0;
+    int PS = 1;
+    while (ngm > 0 && PS * 2 * ngm <= kThreads) PS *= 2;
+
+    for (int l = 0; l < p.L; ++l) {
+        const FusedLayer& ly = p.layers[l];
+        const int r = ly.r;
+        PI_STAMP(l, 0);
+
+        // ---------------------------------------------------------- phase A
+        if (l == 0) {
+            for (int i = tid; i < d; i += kThreads) xf[i] = __half2float(p.x_in[i]);
+        } else {
+            constexpr int NY = 2 * NCH;   // d <= NCH * 4096: at most 2*NCH float4 of y per thread
+            float4 yv[NY];
+#pragma unroll
+            for (int b = 0; b < NY; ++b) {
+                const int i4 = tid + b * kThreads;
+                if (i4 < d / 4) yv[b] = ld_cg4(p.xy + i4 * 4);
+            }
+            if (warp == 0) {
+                float s = 0.f;
+                for (int q = lane; q < G; q += 32) s += __ldcg(p.xss + q);
+                s = warp_sum(s);
+                if (lane == 0) rs_s = rsqrtf(s / (float)d + p.eps);
+            }
+            __syncthreads();
+            const float rs = rs_s;
+#pragma unroll
+            for (int b = 0; b < NY; ++b) {
+                const int i4 = tid + b * kThreads;
+                if (i4 < d / 4) {
+                    const __half h0 = __float2half_rn(yv[b].x * rs), h1 = __float2half_rn(yv[b].y * rs);
+                    const __half h2 = __float2half_rn(yv[b].z * rs), h3 = __float2half_rn(yv[b].w * rs);
+                    reinterpret_cast<float4*>(xf)[i4] =
+                        make_float4(__half2float(h0), __half2float(h1), __half2float(h2), __half2float(h3));
+                    if (p.x_trace && c == 0) {
+                        __half* xt = p.x_trace + (size_t)(l - 1) * d + i4 * 4;
+                        xt[0] = h0;
+                        xt[1] = h1;
+                        xt[2] = h2;
+                        xt[3] = h3;
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        PI_STAMP(l, 1);
+        {
+            const int items = r * ly.su;
+            for (int q = c * kWarps + warp; q < items; q += G * kWarps) {
+                const int i = q / ly.su, s = q % ly.su;
+                const int c0 = s * ly.seg, c1 = min(d, c0 + ly.seg);
+                const __half* row = ly.p1 + (size_t)i * d;
+                float acc = 0.f;
+#pragma unroll 8
+                for (int e = c0 + lane * 8; e < c1; e += 256) acc += dot8(ld_stream16(row + e), xf + e);
+                acc = warp_sum(acc);
+                if (lane == 0) p.xu[(size_t)s * r + i] = acc;
+            }
+        }
+        if (!sync()) { leave(); return; }
+        PI_STAMP(l, 2);
+
+        // ---------------------------------------------------------- phase B
+        {
+            const int nw = r * ly.su;  // multiple of 8: float4 loads
+            for (int w4 = tid; w4 < nw / 4; w4 += kThreads)
+                reinterpret_cast<float4*>(ust)[w4] = ld_cg4(p.xu + w4 * 4);
+            __syncthreads();
+            for (int i = tid; i < r; i += kThreads) {
+                float acc = 0.f;
+                for (int s = 0; s < ly.su; ++s) acc += ust[s * r + i];
+                us[i] = acc;
+            }
+        }
+        __syncthreads();
+        {
+            const int nvec = r / 8;
+            const int vpl = (nvec + 31) / 32;
+            // units of 16 rows: this CTA's units are m = c, c+G, ...; UB at a
+            // time, warp w taking row w of each, lanes across the row
+            constexpr int UB = 4;
+            for (int m0 = c; m0 < M; m0 += UB * G) {
+                float acc[UB], bk[UB];
+                int kk[UB];
+#pragma unroll
+                for (int b = 0; b < UB; ++b) {
+                    const int m = m0 + b * G;
+                    kk[b] = m < M ? m * 16 + warp : F;
+                    if (kk[b] > F) kk[b] = F;
+                    acc[b] = 0.f;
+                    bk[b] = (kk[b] < F && lane == 0) ? __half2float(ly.b1[kk[b]]) : 0.f;
+                }
+                for (int e = 0; e < vpl; ++e) {
+                    const int v = lane + 32 * e;
+                    uint4 pv[UB];
+#pragma unroll
+                    for (int b = 0; b < UB; ++b)
+                        if (kk[b] < F && v < nvec) pv[b] = ld_stream16(ly.p2 + (size_t)kk[b] * r + v * 8);
+#pragma unroll
+                    for (int b = 0; b < UB; ++b)
+                        if (kk[b] < F && v < nvec) acc[b] += dot8(pv[b], us + v * 8);
+                }
+#pragma unroll
+                for (int b = 0; b < UB; ++b) {
+                    const float a = warp_sum(acc[b]);
+                    if (lane == 0) preds[b][warp] = (kk[b] < F && a + bk[b] > p.tau) ? 1u : 0u;
+                }
+                __syncthreads();
+                if (tid < UB) {
+                    const int m = m0 + tid * G;
+                    if (m < M) {
+                        unsigned bits = 0;
+#pragma unroll
+                        for (int w = 0; w < 16; ++w) bits |= preds[tid][w] << w;
+                        reinterpret_cast<uint16_t*>(p.xmask)[m] = (uint16_t)bits;
+                        if (l == p.L - 1) reinterpret_cast<uint16_t*>(p.mask_out)[m] = (uint16_t)bits;
+                    }
+                }
+                __syncthreads();
+            }
+            if ((M & 1) && c == 0 && tid == 0) {
+                reinterpret_cast<uint16_t*>(p.xmask)[M] = 0;   // bits past F
+                if (l == p.L - 1) reinterpret_cast<uint16_t*>(p.mask_out)[M] = 0;
+            }
+        }
+        if (!sync()) { leave(); return; }
+        PI_STAMP(l, 3);
+
+        // ---------------------------------------------------------- phase C
+        int n_total;
+        {
+            // every CTA reads the whole mask (coalesced) and scans it
+            for (int w = tid; w < p.W; w += kThreads) reinterpret_cast<uint32_t*>(m16)[w] = __ldcg(p.xmask + w);
+            __syncthreads();
+            const int per = (M + kThreads - 1) / kThreads;
+            int cnt = 0;
+            for (int e = 0; e < per; ++e) {
+                const int m = tid * per + e;
+                if (m < M) cnt += __popc((unsigned)m16[m]);
+            }
+            int total;
+            int run = block_exscan(cnt, scr, &total);
+            for (int e = 0; e < per; ++e) {
+                const int m = tid * per + e;
+                if (m < M) {
+                    upre[m] = run;
+                    run += __popc((unsigned)m16[m]);
+                }
+            }
+            if (tid == 0) upre[M] = total;
+            n_total = total;
+        }
+        __syncthreads();
+        const int j0 = (int)(((long long)n_total * c) / G);
+        const int j1 = (int)(((long long)n_total * (c + 1)) / G);
+        const int nmine = j1 - j0;
+        // collect this CTA's neuron ids (storage rows) of list positions [j0, j1)
+        for (int m = tid; m < M; m += kThreads) {
+            const int lo = upre[m], hi = upre[m + 1];
+            if (hi <= j0 || lo >= j1) continue;
+            unsigned bits = (unsigned)m16[m];
+            int pos = lo;
+            while (bits) {
+                const int b = __ffs(bits) - 1;
+                bits &= bits - 1u;
+                if (pos >= j0 && pos < j1) {
+                    lidx[pos - j0] = m * 16 + b;
+                    if (l == p.L - 1) p.idx_out[pos] = m * 16 + b;
+                }
+                ++pos;
+            }
+        }
+        if (l == p.L - 1 && c == 0 && tid == 0) *p.count_out = n_total;
+        __syncthreads();
+        prefetch_predictor(l + 1);
+
+        // FC1: (neuron, segment) items spread over all warps so that every warp
+        // has loads in flight; segment dot products are combined in a fixed order
+        {
+            for (int q = tid; q < nmine; q += kThreads) lh[q] = __half2float(ly.b1[lidx[q]]);  // bias
+            const int ng = d / 32;
+            const int maxseg = KIND == 2 ? max(1, ng / 32) : max(1, d / 256);
+            int nseg = nmine > 0 ? kWarps / nmine : 1;
+            nseg = max(1, min(nseg, maxseg));
+            const int segE = KIND == 2 ? ((ng + nseg - 1) / nseg + 31) / 32 * 32   // groups
+                                       : ((d + nseg - 1) / nseg + 255) / 256 * 256;  // elements
+            nseg = KIND == 2 ? (ng + segE - 1) / segE : (d + segE - 1) / segE;
+            float* part = red;           // [nmine * nseg]
+            float* partu = red + 2048;   // gated: up-projection partials
+            for (int it = warp; it < nmine * nseg; it += kWarps) {
+                const int q = it / nseg, sg = it % nseg;
+                const int k = lidx[q];
+                float acc = 0.f, accu = 0.f;
+                if (KIND != 2) {
+                    const int e0 = sg * segE, e1 = min(d, e0 + segE);
+                    const __half* row = static_cast<const __half*>(ly.w1) + (size_t)k * d;
+                    const __half* rowu = KIND == 1 ? ly.wu + (size_t)k * d : nullptr;
+#pragma unroll 8
+                    for (int e = e0 + lane * 8; e < e1; e += 256) {
+                        acc += dot8(ld_stream16(row + e), xf + e);
+                        if (KIND == 1) accu += dot8(ld_stream16(rowu + e), xf + e);
+                    }
+                } else {
+                    const int gs0 = sg * segE, gs1 = min(ng, gs0 + segE);
+                    const uint8_t* row = static_cast<const uint8_t*>(ly.w1) + (size_t)k * (d / 2);
+                    const __half* sc = ly.w1s + (size_t)k * ng;
+#pragma unroll 4
+                    for (int g = gs0 + lane; g < gs1; g += 32) {
+                        const uint4 qv = ld_stream16(row + (size_t)g * 16);
+                        const float s = __half2float(sc[g]);
+                        const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+                        float pt = 0.f;
+#pragma unroll
+                        for (int wi = 0; wi < 4; ++wi) {
+                            float qf[8];
+                            q8_to_f8(qw[wi], qf);
+                            const float4 xa = reinterpret_cast<const float4*>(xf + g * 32 + wi * 8)[0];
+                            const float4 xb = reinterpret_cast<const float4*>(xf + g * 32 + wi * 8)[1];
+                            pt = fmaf(qf[0], xa.x, pt);
+                            pt = fmaf(qf[1], xa.y, pt);
+                            pt = fmaf(qf[2], xa.z, pt);
+                            pt = fmaf(qf[3], xa.w, pt);
+                            pt = fmaf(qf[4], xb.x, pt);
+                            pt = fmaf(qf[5], xb.y, pt);
+                            pt = fmaf(qf[6], xb.z, pt);
+                            pt = fmaf(qf[7], xb.w, pt);
+                        }
+                        acc = fmaf(s, pt, acc);
+                    }
+                }
+                acc = warp_sum(acc);
+                if (KIND == 1) accu = warp_sum(accu);
+                if (lane == 0) {
+                    part[it] = acc;
+                    if (KIND == 1) partu[it] = accu;
+                }
+            }
+            __syncthreads();
+            for (int q = tid; q < nmine; q += kThreads) {
+                float z = 0.f, zu = 0.f;
+                for (int sg = 0; sg < nseg; ++sg) {
+                    z += part[q * nseg + sg];
+                    if (KIND == 1) zu += partu[q * nseg + sg];
+                }
+                z += lh[q];
+                float hv = z > 0.f ? z : 0.f;
+                if (KIND == 1) hv *= zu;
+                lh[q] = hv;
+                if (l == p.L - 1) p.h_out[j0 + q] = hv;
+            }
+        }
+        __syncthreads();
+        PI_STAMP(l, 4);
+
+        // FC2: the whole CTA accumulates its neurons' W2t rows; rows whose
+        // FC1 output is zero are skipped (ReLU removed them from FC2)
+        if (KIND != 2) {
+            constexpr int RB = NCH == 1 ? 4 : (NCH == 2 ? 2 : 1);
+            float acc[NCH][8];
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[ch][e] = 0.f;
+            for (int q0 = 0; q0 < nmine; q0 += RB) {
+                uint4 wv[RB][NCH];
+                float hv[RB];
+#pragma unroll
+                for (int b = 0; b < RB; ++b) {
+                    const int q = q0 + b;
+                    hv[b] = q < nmine ? lh[q] : 0.f;
+                    if (hv[b] != 0.f) {
+                        const __half* row = static_cast<const __half*>(ly.w2t) + (size_t)lidx[q] * d;
+#pragma unroll
+                        for (int ch = 0; ch < NCH; ++ch) {
+                            const int col = ch * 4096 + tid * 8;
+                            if (col < d) wv[b][ch] = ld_stream16(row + col);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int b = 0; b < RB; ++b) {
+                    if (hv[b] == 0.f) continue;
+#pragma unroll
+                    for (int ch = 0; ch < NCH; ++ch) {
+                        const int col = ch * 4096 + tid * 8;
+                        if (col < d) {
+                            float wf[8];
+                            h8_to_f8(wv[b][ch], wf);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) acc[ch][e] = fmaf(hv[b], wf[e], acc[ch][e]);
+                        }
+                    }
+                }
+            }
+            float* dst = p.xyp + (size_t)c * d;
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch) {
+                const int col = ch * 4096 + tid * 8;
+                if (col < d) {
+                    float4* o = reinterpret_cast<float4*>(dst + col);
+                    __stcg(o, make_float4(acc[ch][0], acc[ch][1], acc[ch][2], acc[ch][3]));
+                    __stcg(o + 1, make_float4(acc[ch][4], acc[ch][5], acc[ch][6], acc[ch][7]));
+                }
+            }
+        } else {
+            // INT4: each thread owns 32 consecutive columns (one scale group)
+            float acc[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+            const int col = tid * 32;
+            const bool mine = col < d;
+            for (int q0 = 0; q0 < nmine; q0 += 4) {
+                uint4 wv[4];
+                float hs[4];
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    const int q = q0 + b;
+                    const float hv = q < nmine ? lh[q] : 0.f;
+                    hs[b] = 0.f;
+                    if (hv != 0.f && mine) {
+                        const size_t k = (size_t)lidx[q];
+                        wv[b] = ld_stream16(static_cast<const uint8_t*>(ly.w2t) + k * (d / 2) + col / 2);
+                        hs[b] = hv * __half2float(ly.w2ts[k * (d / 32) + col / 32]);
+                    }
+                }
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    if (hs[b] == 0.f) continue;
+                    const uint32_t qw[4] = {wv[b].x, wv[b].y, wv[b].z, wv[b].w};
+#pragma unroll
+                    for (int wi = 0; wi < 4; ++wi) {
+                        float qf[8];
+                        q8_to_f8(qw[wi], qf);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[wi * 8 + e] = fmaf(hs[b], qf[e], acc[wi * 8 + e]);
+                    }
+                }
+            }
+            if (mine) {
+                float4* o = reinterpret_cast<float4*>(p.xyp + (size_t)c * d + col);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    __stcg(o + e, make_float4(acc[4 * e], acc[4 * e + 1], acc[4 * e + 2], acc[4 * e + 3]));
+            }
+        }
+        PI_STAMP(l, 5);
+        if (!sync()) { leave(); return; }
+        PI_STAMP(l, 6);
+
+        // ---------------------------------------------------------- phase D
+        {
+            // this CTA's ngm 4-column groups x PS partial subsets; thread t ->
+            // group t % ngm, partials ps, ps + PS, ...; then a fixed tree over ps
+            const int gi = ngm > 0 ? tid % ngm : 0;
+            const int ps = ngm > 0 ? tid / ngm : PS;
+            const int col = (g0 + gi) * 4;
+            float4* red4 = reinterpret_cast<float4*>(red);
+            float4 bias = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (ps == 0 && ngm > 0)
+                bias = make_float4(__half2float(ly.b2[col]), __half2float(ly.b2[col + 1]),
+                                   __half2float(ly.b2[col + 2]), __half2float(ly.b2[col + 3]));
+            if (ps < PS) {
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                constexpr int NB = 4;
+                for (int q0 = ps; q0 < G; q0 += NB * PS) {
+                    float4 v[NB];
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) {
+                        const int q = q0 + b * PS;
+                        if (q < G) v[b] = ld_cg4(p.xyp + (size_t)q * d + col);
+                    }
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) {
+                        const int q = q0 + b * PS;
+                        if (q < G) {
+                            acc.x += v[b].x;
+                            acc.y += v[b].y;
+                            acc.z += v[b].z;
+                            acc.w += v[b].w;
+                        }
+                    }
+                }
+                red4[tid] = acc;
+            }
+            __syncthreads();
+            for (int s = PS / 2; s >= 1; s >>= 1) {
+                if (ps < s) {
+                    const float4 o = red4[tid + s * ngm];
+                    float4 a = red4[tid];
+                    a.x += o.x;
+                    a.y += o.y;
+                    a.z += o.z;
+                    a.w += o.w;
+                    red4[tid] = a;
+                }
+                __syncthreads();
+            }
+            float ss_local = 0.f;
+            if (ps == 0 && ngm > 0) {
+                const float4 a = red4[tid];
+                const float4 yv = make_float4(a.x + bias.x, a.y + bias.y, a.z + bias.z, a.w + bias.w);
+                __stcg(reinterpret_cast<float4*>(p.xy + col), yv);
+                if (l == p.L - 1) *reinterpret_cast<float4*>(p.y_out + col) = yv;
+                ss_local = yv.x * yv.x + yv.y * yv.y + yv.z * yv.z + yv.w * yv.w;
+            }
+            if (l + 1 < p.L) {
+                // fixed-order sum of squares of this CTA's columns
+                const float s = warp_sum(ss_local);
+                __syncthreads();
+                if (lane == 0) red[warp] = s;
+                __syncthreads();
+                if (tid == 0) {
+                    float t = 0.f;
+                    for (int w = 0; w < kWarps; ++w) t += red[w];
+                    __stcg(p.xss + c, t);
+                }
+            }
+        }
+        PI_STAMP(l, 7);
+        if (!sync()) { leave(); return; }
+    }
+    leave();
+}
+
+// A wait on a counter nothing increments: exercises the bounded-wait path.
+__device__ unsigned g_never_incremented = 0u;
+
+__global__ void k_wait_nothing(long long timeout_ns) {
+    __shared__ int bad;
+    if (threadIdx.x == 0) bad = 0;
+    // target 2 with one arrival: the count never gets there
+    (void)grid_sync(&g_never_incremented, g_never_incremented + 2u, timeout_ns, &bad);
+    if (threadIdx.x == 0) atomicSub(&g_never_incremented, 1u);
+}
+
+// ------------------------------------------------------------------ host side
+
+namespace {
+
+template <int KIND, int NCH>
+cudaError_t launch_kind(const FusedParams& prm, int G, size_t smem, cudaStream_t s) {
+    auto kern = k_fused_stack<KIND, NCH>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(G);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, prm);
+}
+
+size_t up256(size_t v) { return (v + 255) / 256 * 256; }
+
+// exchange region: epoch | counter | xu | xmask | xyp | xy | xss
+struct XchgLayout {
+    size_t counter, xu, xmask, xyp, xy, xss, total;
+    XchgLayout(int d, int F, size_t rmax_su, int G) {
+        const int W = (F + 31) / 32;
+        size_t off = 256;
+        counter = off;
+        off += 256;
+        xu = off;
+        off += up256(4ull * rmax_su);
+        xmask = off;
+        off += up256(4ull * W + 4);
+        xyp = off;
+        off += up256(4ull * (size_t)G * d);
+        xy = off;
+        off += up256(4ull * d);
+        xss = off;
+        off += up256(4ull * G);
+        total = off;
+    }
+};
+
+SmemPlan smem_plan(int d, int F, int rmax, size_t rmax_su, int G) {
+    return SmemPlan{d, rmax < 8 ? 8 : rmax, (int)rmax_su, (F + 15) / 16, F / G + 2};
+}
+
+}  // namespace
+
+size_t fused_workspace_bytes(int d, int F, size_t rmax_su, int G) { return XchgLayout(d, F, rmax_su, G).total; }
+
+bool fused_supported(int d, int F, int rmax, bool int4, int G) {
+    if (d > 16384 || d % 8 != 0 || G < 1) return false;
+    if (int4 && d % 32 != 0) return false;
+    const size_t rmax_su = (size_t)16 * G + 2 * (size_t)rmax;
+    return smem_plan(d, F, rmax, rmax_su, G).bytes() <= 220 * 1024;
+}
+
+cudaError_t launch_fused(const FusedStackArgs& a, cudaStream_t s) {
+    if (a.L < 1 || a.L > kMaxFusedLayers) return cudaErrorInvalidValue;
+    FusedParams prm = {};
+    const int G = a.G;
+    prm.L = a.L;
+    prm.d = a.d;
+    prm.F = a.F;
+    prm.M = (a.F + 15) / 16;
+    prm.W = (a.F + 31) / 32;
+    prm.tau = a.tau;
+    prm.eps = a.eps;
+    prm.timeout_ns = a.timeout_ns;
+    prm.x_in = a.x_in;
+    prm.y_out = a.y_out;
+    prm.x_trace = a.x_trace;
+    const XchgLayout xl(a.d, a.F, a.rmax_su, G);
+    char* ws = static_cast<char*>(a.xchg);
+    prm.epoch = reinterpret_cast<unsigned long long*>(ws);
+    prm.counter = reinterpret_cast<unsigned*>(ws + xl.counter);
+    prm.xu = reinterpret_cast<float*>(ws + xl.xu);
+    prm.xmask = reinterpret_cast<uint32_t*>(ws + xl.xmask);
+    prm.xyp = reinterpret_cast<float*>(ws + xl.xyp);
+    prm.xy = reinterpret_cast<float*>(ws + xl.xy);
+    prm.xss = reinterpret_cast<float*>(ws + xl.xss);
+    prm.mask_out = a.mask_out;
+    prm.idx_out = a.idx_out;
+    prm.count_out = a.count_out;
+    prm.h_out = a.h_out;
+    int rmax = 8;
+    for (int l = 0; l < a.L; ++l) {
+        const LayerPtrs& w = a.layers[l];
+        FusedLayer& f = prm.layers[l];
+        f.w1 = w.w1;
+        f.w1s = w.w1s;
+        f.b1 = w.b1;
+        f.wu = w.wu;
+        f.w2t = w.w2t;
+        f.w2ts = w.w2ts;
+        f.b2 = w.b2;
+        f.p1 = w.p1;
+        f.p2 = w.p2;
+        f.r = a.ranks[l];
+        // at most one (row, split) item per warp of the grid; splits >= 256 elements
+        int su = (16 * G) / f.r;
+        const int max_su = (a.d + 255) / 256;
+        if (su > max_su) su = max_su;
+        if (su < 1) su = 1;
+        f.seg = ((a.d / 8 + su - 1) / su) * 8;
+        f.su = (a.d + f.seg - 1) / f.seg;
+        if ((size_t)f.su * f.r > a.rmax_su) return cudaErrorInvalidValue;
+        rmax = f.r > rmax ? f.r : rmax;
+    }
+    const SmemPlan sp = smem_plan(a.d, a.F, rmax, a.rmax_su, G);
+    const size_t smem = sp.bytes();
+    if (smem > 227 * 1024) return cudaErrorInvalidValue;
+    if (a.int4) return launch_kind<2, 1>(prm, G, smem, s);
+    const int nch = (a.d + 4095) / 4096;
+    if (a.gated) {
+        if (nch == 1) return launch_kind<1, 1>(prm, G, smem, s);
+        if (nch == 2) return launch_kind<1, 2>(prm, G, smem, s);
+        return launch_kind<1, 4>(prm, G, smem, s);
+    }
+    if (nch == 1) return launch_kind<0, 1>(prm, G, smem, s);
+    if (nch == 2) return launch_kind<0, 2>(prm, G, smem, s);
+    return launch_kind<0, 4>(prm, G, smem, s);
+}
+
+cudaError_t launch_wait_nothing(long long timeout_ns, cudaStream_t s) {
+    k_wait_nothing<<<1, 32, 0, s>>>(timeout_ns);
+    return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_status(int* out, cudaStream_t s) {
+    int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_pi_status, sizeof(int), 0, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+    *out = v;
+    if (v != 0) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbolAsync(g_pi_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    }
+    return e;
+}
+
+}  // namespace pi
+
+#ifdef PI_PHASE_TRACE
+extern "C" __attribute__((visibility("default"))) int pi_debug_read_trace(unsigned long long* host,
+                                                                          unsigned long long* clk, int n) {
+    if (n > 96 * pi::kTraceSlots * pi::kTraceCtas) n = 96 * pi::kTraceSlots * pi::kTraceCtas;
+    if (cudaMemcpyFromSymbol(host, pi::g_pi_trace, sizeof(unsigned long long) * n) != cudaSuccess) return -1;
+    if (cudaMemcpyFromSymbol(clk, pi::g_pi_trace_clk, sizeof(unsigned long long) * n) != cudaSuccess) return -1;
+    return n;
+}
+#endif

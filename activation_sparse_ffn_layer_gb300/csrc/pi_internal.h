@@ -22,8 +22,10 @@ struct Plan {
     int fc2_cols;   // columns per FC2 block
     int fc2_tiles;  // ceil(d / fc2_cols)
     int fc2_splits; // neuron splits of FC2 (partials reduced in fixed order)
-    // workspace offsets (bytes, 256-aligned)
-    size_t off_mask, off_idx, off_count, off_h, off_upart, off_part, total;
+    // workspace offsets (bytes, 256-aligned); the fused exchange region comes first
+    size_t xchg_bytes, rmax_su;
+    bool fused;     // pi_ffn_layer / pi_ffn_stack take the fused persistent kernel
+    size_t off_mask, off_idx, off_count, off_h, off_upart, off_part, off_xbuf, total;
 };
 
 bool make_plan(const pi_layer_desc& desc, Plan* p);
@@ -51,5 +53,29 @@ cudaError_t launch_fc1(const Plan& p, const __half* x, const LayerPtrs& w, const
 cudaError_t launch_fc2(const Plan& p, const float* h, const int32_t* idx, const int32_t* count,
                        const LayerPtrs& w, float* partial, float* y, cudaStream_t s);
 cudaError_t launch_rmsnorm(int d, int B, const float* y, float eps, __half* x, cudaStream_t s);
+
+// ---- fused persistent stack (batch 1) ----
+struct FusedStackArgs {
+    int L, d, F, G;
+    bool int4, gated;
+    float tau, eps;
+    long long timeout_ns;
+    const LayerPtrs* layers;  // [L]
+    const int* ranks;         // [L]
+    const __half* x_in;       // [d]
+    float* y_out;             // [d]
+    __half* x_trace;          // nullable [L-1][d]
+    void* xchg;               // exchange region (zero-filled before first use)
+    size_t rmax_su;           // capacity of the u-partial exchange, entries
+    uint32_t* mask_out;
+    int32_t* idx_out;
+    int32_t* count_out;
+    float* h_out;
+};
+size_t fused_workspace_bytes(int d, int F, size_t rmax_su, int G);
+bool fused_supported(int d, int F, int rmax, bool int4, int G);
+cudaError_t launch_fused(const FusedStackArgs& a, cudaStream_t s);
+cudaError_t launch_wait_nothing(long long timeout_ns, cudaStream_t s);
+cudaError_t read_and_clear_status(int* out, cudaStream_t s);
 
 }  // namespace pi

@@ -1,10 +1,9 @@
-"""Decode-step runner over the C ABI: layers resident in HBM, one workspace,
-one stream, optionally replayed as a CUDA graph.
+"""Decode-step runner over the C ABI: layers resident in HBM, one zero-filled
+workspace, one stream, optionally replayed as a CUDA graph.
 
-A decode step for a stack of L layers is, per layer l:
-``y_l = pi_ffn_layer(x_l)`` and ``x_{l+1} = pi_rmsnorm_half(y_l)`` (the
-normalisation between layers of the stacked workloads).  Only launches go
-through here; all arithmetic is in ``libpi.so``.
+A decode step through a stack of L layers is one ``pi_ffn_stack`` call (layer
+l: predictor -> compaction -> FC1 -> FC2, then the normalisation that feeds
+layer l+1).  Only launches go through here; all arithmetic is in ``libpi.so``.
 """
 from __future__ import annotations
 
@@ -24,64 +23,48 @@ class DeviceLayer:
         self.desc = B.layer_desc(w, batch)
         self.ws = B.weights_struct(w)
 
-    def with_batch(self, batch: int) -> "DeviceLayer":
-        return DeviceLayer(self.w, batch)
-
 
 class DecodeStack:
     """Runs decode steps of `batch` tokens through a list of layers."""
 
-    def __init__(self, layers: List, batch: int = 1, tau: float = -0.05, eps: float = 1e-6,
-                 device: Optional[torch.device] = None):
+    def __init__(self, layers: List, batch: int = 1, tau: float = -0.05, eps: float = 1e-6):
         if not layers:
             raise ValueError("no layers")
-        self.layers = [l if isinstance(l, DeviceLayer) and l.batch == batch else
-                       DeviceLayer(l.w if isinstance(l, DeviceLayer) else l, batch) for l in layers]
+        ws = [l.w if isinstance(l, DeviceLayer) else l for l in layers]
+        self.layers = [DeviceLayer(w, batch) for w in ws]
+        self.weights = ws
         self.batch, self.tau, self.eps = batch, float(tau), float(eps)
-        w0 = self.layers[0].w
+        w0 = ws[0]
         self.d = w0.d
-        dev = device or w0.b1.device
-        ws = max(B.pi_workspace_bytes(l.desc) for l in self.layers)
-        if ws == 0:
+        dev = w0.b1.device
+        rmax = max(w.r for w in ws)
+        self.desc = B.desc_of(w0.d, w0.F, rmax, batch, w0.int4, w0.gated)
+        self.warr = B.weights_array(ws)
+        self.ranks = B.ranks_array(ws)
+        nbytes = B.pi_workspace_bytes(self.desc)
+        if nbytes == 0:
             raise ValueError("layer descriptor rejected by the library")
-        self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
-        self.x_in = torch.empty(batch, self.d, dtype=torch.float16, device=dev)
-        self.x_bufs = [torch.empty(batch, self.d, dtype=torch.float16, device=dev) for _ in range(2)]
-        self.y = torch.empty(batch, self.d, dtype=torch.float32, device=dev)
+        self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+        self.x_in = torch.zeros(batch, self.d, dtype=torch.float16, device=dev)
+        self.y = torch.zeros(batch, self.d, dtype=torch.float32, device=dev)
         self.graph: Optional[torch.cuda.CUDAGraph] = None
-        self.launches_per_step = None
 
-    def _run(self, x: torch.Tensor, y: torch.Tensor, xs_out: Optional[list] = None):
-        cur = x
-        for l, layer in enumerate(self.layers):
-            B.pi_ffn_layer(layer.desc, cur, layer.ws, self.tau, self.workspace, y)
-            if l + 1 < len(self.layers):
-                nxt = self.x_bufs[l % 2]
-                B.pi_rmsnorm_half(self.d, self.batch, y, self.eps, nxt)
-                if xs_out is not None:
-                    xs_out.append(nxt.clone())
-                cur = nxt
+    def _run(self, x: torch.Tensor, y: torch.Tensor, x_trace: Optional[torch.Tensor] = None):
+        B.pi_ffn_stack(self.desc, self.warr, self.ranks, x, self.tau, self.eps, self.workspace, y, x_trace)
 
     def step(self, x: torch.Tensor) -> torch.Tensor:
-        """One decode step, eager launches; returns the last layer's y."""
+        """One decode step (eager launch); returns the last layer's y."""
         self._run(x, self.y)
         return self.y
 
     def step_trace(self, x: torch.Tensor):
-        """Eager step that also returns every layer's input (for parity checks)."""
-        xs = [x.clone()]
-        ys = []
-        cur = x
-        for l, layer in enumerate(self.layers):
-            y = torch.empty_like(self.y)
-            B.pi_ffn_layer(layer.desc, cur, layer.ws, self.tau, self.workspace, y)
-            ys.append(y)
-            if l + 1 < len(self.layers):
-                nxt = torch.empty_like(self.x_in)
-                B.pi_rmsnorm_half(self.d, self.batch, y, self.eps, nxt)
-                xs.append(nxt)
-                cur = nxt
-        return xs, ys
+        """One step that also returns every layer's input (for parity checks):
+        (list of [B, d] fp16 inputs, last layer's y)."""
+        L = len(self.layers)
+        tr = torch.zeros(max(L - 1, 1), self.batch, self.d, dtype=torch.float16, device=x.device)
+        y = torch.zeros_like(self.y)
+        self._run(x, y, tr if L > 1 else None)
+        return [x.clone()] + [tr[l] for l in range(L - 1)], y
 
     def capture(self) -> None:
         """Record one step (reading self.x_in, writing self.y) as a CUDA graph."""
@@ -97,3 +80,10 @@ class DecodeStack:
 
     def replay(self) -> None:
         self.graph.replay()
+
+    def launches_per_step(self) -> int:
+        """Kernel launches of one step, as the library reports them."""
+        per = [B.pi_launches_per_layer(l.desc) for l in self.layers]
+        if all(n == 1 for n in per):
+            return 1                                  # one persistent kernel for the whole stack
+        return sum(per) + (len(self.layers) - 1)      # per-step kernels + normalisations

@@ -1,0 +1,440 @@
+"""Benchmark: sparse-FFN decode tokens/s at batch 1 on one GB300, with the
+achieved HBM bandwidth on the bytes the method must move.
+
+Default workload: the OPT-6.7B-shaped FFN stack (32 layers, d=4096, F=16384,
+predictor rank 256, Zipf(1.1) firing at 10%), one token per step through all
+32 layers (predictor -> compaction -> FC1 -> FC2, RMS normalisation between
+layers), inputs cycling over the run's 128 seeded tokens.  The 8.6 GB of
+layer weights read per step are far larger than L2, so no flush is needed.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c2] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
+instead (bounded sample of the same workload, scaled to tokens/s).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-FFN decode tokens/s at batch 1 and achieved HBM GB/s vs ~8 TB/s"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+        except Exception:
+            pass
+        finally:
+            if self.path and os.path.exists(self.path):
+                os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------- algorithmic bytes
+
+def layer_bytes(cfg, r, n_pred, n_relu, batch=1):
+    """Bytes the method must move for one layer and one decode step:
+    the predictor (P1, P2, bias) in full, the FC1 rows of the predicted-active
+    neurons (gate + up rows when gated), the FC2 rows of the neurons whose FC1
+    output is non-zero, and the small vectors (x, y, b2, mask, index list, h)."""
+    d, F = cfg.d, cfg.F
+    row = d // 2 + 2 * (d // 32) if cfg.int4 else 2 * d
+    pred = 2 * (r * d + F * r) + 2 * F
+    fc1 = n_pred * row * (2 if cfg.gated else 1)
+    fc2 = n_relu * row + 2 * d
+    small = batch * (2 * d + 4 * d) + batch * ((F + 31) // 32) * 4 + 4 * n_pred * (1 + batch)
+    return dict(predict=pred, fc1=fc1, fc2=fc2, small=small, total=pred + fc1 + fc2 + small)
+
+
+def measure_counts(P, st, tokens, cfg):
+    """Untimed eager pass: per token and layer, the predicted-active count and
+    the number of listed neurons with a non-zero FC1 output."""
+    import torch
+    counts = []
+    for t in range(tokens.shape[0]):
+        x = tokens[t:t + 1]
+        per = []
+        for l, layer in enumerate(st.layers):
+            y = st.y
+            P.pi_ffn_layer(layer.desc, x, layer.ws, st.tau, st.workspace, y)
+            lay = P.pi_workspace_layout(layer.desc)
+            n = int(st.workspace[lay.count:lay.count + 4].view(torch.int32).item())
+            h = st.workspace[lay.h:lay.h + 4 * max(n, 1)].view(torch.float32)[:n]
+            per.append((n, int((h != 0).sum().item())))
+            if l + 1 < len(st.layers):
+                xn = torch.empty_like(x)
+                P.pi_rmsnorm_half(cfg.d, 1, y, cfg.rms_eps, xn)
+                x = xn
+        counts.append(per)
+    return counts
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import activation_sparse_ffn_layer_gb300 as P
+    from activation_sparse_ffn_layer_gb300.runtime import DecodeStack
+    from synth import CONFIGS, make_layer, make_tokens
+
+    cfg = CONFIGS[args.config]
+    B = 1
+    layers = [make_layer(cfg, l, device="cuda") for l in range(cfg.layers)]
+    T = cfg.tokens
+    tokens = make_tokens(cfg, 0, T, device="cuda")
+    st = DecodeStack(layers, batch=B, tau=cfg.tau, eps=cfg.rms_eps)
+    weight_bytes = sum(w.nbytes() for w in layers)
+
+    # per-token algorithmic bytes (untimed)
+    counts = measure_counts(P, st, tokens, cfg)
+    per_tok = []
+    per_kernel = {"predict": 0, "fc1": 0, "fc2": 0}
+    for per in counts:
+        tot = 0
+        for l, (n, nz) in enumerate(per):
+            lb = layer_bytes(cfg, layers[l].r, n, nz, B)
+            tot += lb["total"]
+            for k in per_kernel:
+                per_kernel[k] += lb[k]
+        tot += (cfg.layers - 1) * B * (4 * cfg.d + 2 * cfg.d)   # inter-layer norm: read y, write x
+        per_tok.append(tot)
+    n_pred_mean = sum(n for per in counts for n, _ in per) / (T * cfg.layers)
+    n_relu_mean = sum(z for per in counts for _, z in per) / (T * cfg.layers)
+
+    st.capture()
+    stream = torch.cuda.current_stream()
+    K, W = args.steps, args.warmup
+    for i in range(W):
+        st.x_in.copy_(tokens[i % T:i % T + 1])
+        st.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(K):
+            t = (W + i) % T
+            st.x_in.copy_(tokens[t:t + 1])
+            st.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    clocks = clk.summary()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+        dist.barrier()
+    step_bytes = sum(per_tok[(W + i) % T] for i in range(K)) / K
+    tok_s = world * K * B / (ms / 1e3)
+    peak, peak_kind = _peaks()
+
+    # dominant step, timed live with CUDA events on the launching stream
+    kern = time_kernels(P, st, tokens, cfg, K=min(K, 256), W=W)
+    names = {"predict": "pi_predict", "fc1": "pi_sparse_fc1", "fc2": "pi_sparse_fc2"}
+    dom = max(kern["ms"], key=lambda k: kern["ms"][k])
+    dom_bytes = per_kernel.get(dom, 0) / (T * cfg.layers)        # mean bytes per launch
+    dom_ms = kern["ms"][dom] / kern["launches"][dom]
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9 if dom in per_kernel else None
+    roofline = {"kernel": names.get(dom, dom), "bound": "hbm",
+                "achieved": round(achieved, 1) if achieved else None, "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4) if achieved else None, "traffic": None,
+                "peak_kind": peak_kind,
+                "bytes_per_launch": int(dom_bytes), "us_per_launch": round(dom_ms * 1e3, 2),
+                "share_of_step": round(kern["ms"][dom] / sum(kern["ms"].values()), 3)}
+
+    e2e = time_e2e(st, tokens, K=min(K, 512), W=W)
+    out = {
+        "metric": METRIC, "value": round(tok_s, 2), "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": round(ms / K, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{cfg.key}: {cfg.name}, batch 1, {cfg.layers} layers per step",
+                   "batch": B, "layers": cfg.layers, "d": cfg.d, "ffn": cfg.F, "tokens_cycled": T,
+                   "weights": "int4-g32" if cfg.int4 else "fp16",
+                   "l2": f"inputs larger than L2 ({weight_bytes / 1e9:.1f} GB of layer weights per step)",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "achieved_gbs_step": round(step_bytes / (ms / K / 1e3) / 1e9, 1),
+        "frac_step": round(step_bytes / (ms / K / 1e3) / 1e9 / peak, 4),
+        "bytes_per_step": int(step_bytes),
+        "active": {"predicted_per_layer": round(n_pred_mean, 1), "relu_nonzero_per_layer": round(n_relu_mean, 1),
+                   "F": cfg.F},
+        "roofline": roofline,
+        "kernel_ms_per_step": {names.get(k, k): round(v / kern["steps"], 4) for k, v in kern["ms"].items()},
+        "e2e": e2e,
+        "gpu_launches": K * st.launches_per_step(),
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(cfg, layers, st, tokens, budget_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def time_kernels(P, st, tokens, cfg, K, W):
+    """Eager steps through the per-step entry points with CUDA events around
+    each call on the launching stream: total ms per entry point."""
+    import torch
+    stream = torch.cuda.current_stream()
+    ms = {"predict": 0.0, "compact": 0.0, "fc1": 0.0, "fc2": 0.0, "norm": 0.0}
+    launches = {k: 0 for k in ms}
+    T = tokens.shape[0]
+    bufs = {}
+    for step in range(W + K):
+        x = tokens[step % T:step % T + 1]
+        evs = []
+        for l, layer in enumerate(st.layers):
+            desc = layer.desc
+            lay = P.pi_workspace_layout(desc)
+            ws = st.workspace
+            mask = ws[lay.mask:lay.mask + 4 * ((layer.w.F + 31) // 32)].view(torch.int32)
+            idx = ws[lay.idx:lay.idx + 4 * layer.w.F].view(torch.int32)
+            cnt = ws[lay.count:lay.count + 4].view(torch.int32)
+            h = ws[lay.h:lay.h + 4 * layer.w.F].view(torch.float32)
+            marks = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+            marks[0].record(stream)
+            P.pi_predict(desc, x, layer.w.p1, layer.w.p2, layer.w.b1, st.tau, mask, ws)
+            marks[1].record(stream)
+            P.pi_compact(desc, mask, None, idx, None, cnt)
+            marks[2].record(stream)
+            P.pi_sparse_fc1(desc, x, layer.ws, idx, cnt, None, h)
+            marks[3].record(stream)
+            P.pi_sparse_fc2(desc, h, idx, cnt, layer.ws, st.y, ws)
+            marks[4].record(stream)
+            if l + 1 < len(st.layers):
+                xn = bufs.setdefault(l % 2, torch.empty_like(st.x_in))
+                P.pi_rmsnorm_half(cfg.d, 1, st.y, cfg.rms_eps, xn)
+                x = xn
+            marks[5].record(stream)
+            evs.append((l, marks))
+        torch.cuda.synchronize()
+        if step >= W:
+            for l, m in evs:
+                for i, k in enumerate(("predict", "compact", "fc1", "fc2", "norm")):
+                    if k == "norm" and l + 1 == len(st.layers):
+                        continue
+                    ms[k] += m[i].elapsed_time(m[i + 1])
+                    launches[k] += 1
+    return {"ms": ms, "launches": launches, "steps": K}
+
+
+def time_e2e(st, tokens, K, W):
+    """Through the public API with host buffers: per step, copy the token from
+    pinned host memory, run the step, copy y back and read it on the host."""
+    import torch
+    T = tokens.shape[0]
+    host_x = tokens.cpu().pin_memory()
+    host_y = torch.empty(st.y.shape, dtype=st.y.dtype).pin_memory()
+    stream = torch.cuda.current_stream()
+    for i in range(W):
+        st.x_in.copy_(host_x[i % T:i % T + 1], non_blocking=True)
+        st.replay()
+        host_y.copy_(st.y, non_blocking=True)
+        stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    acc = 0.0
+    e0.record(stream)
+    for i in range(K):
+        st.x_in.copy_(host_x[i % T:i % T + 1], non_blocking=True)
+        st.replay()
+        host_y.copy_(st.y, non_blocking=True)
+        stream.synchronize()
+        acc += float(host_y[0, 0])                 # the host reads the step's result
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    return {"value": round(K / (ms / 1e3), 2), "unit": "tokens/s",
+            "h2d_bytes_per_step": int(host_x[0:1].numel() * 2), "d2h_bytes_per_step": int(host_y.numel() * 4)}
+
+
+def cpu_baseline(cfg, layers, st, tokens, budget_s=15.0):
+    """The CPU oracle, as it stands, on a bounded sample: sampled layers of the
+    first tokens, each fed with the GPU's input to that layer; scaled to
+    tokens/s over the full depth."""
+    import oracle
+    cores = _cores()
+    oracle.set_threads(cores)
+    L = cfg.layers
+    sample_layers = sorted({0, 1, L // 2, L - 1}) if L > 1 else [0]
+    hosts = {l: oracle.host_layer(layers[l].to("cpu")) for l in sample_layers}
+    times = []
+    t_start = time.perf_counter()
+    t = 0
+    while True:
+        xs, _ = st.step_trace(tokens[t % tokens.shape[0]:t % tokens.shape[0] + 1])
+        for l in sample_layers:
+            x = xs[l][0].cpu()
+            t0 = time.perf_counter()
+            oracle.layer_step(x, hosts[l], cfg.tau)
+            times.append(time.perf_counter() - t0)
+        t += 1
+        if time.perf_counter() - t_start > budget_s and len(times) >= len(sample_layers):
+            break
+    per_layer = sum(times) / len(times)
+    return {"value": round(1.0 / (per_layer * L), 4), "unit": "tokens/s", "cores": oracle.threads(),
+            "kind": "oracle",
+            "sample": f"{len(times)} layer-token evaluations (layers {sample_layers}, {t} tokens), "
+                      f"mean {per_layer * 1e3:.1f} ms per layer, scaled to {L} layers"}
+
+
+# ------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import torch
+    import oracle
+    from synth import CONFIGS, make_layer, make_tokens
+
+    cfg = CONFIGS[args.config]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    L = cfg.layers
+    sample_layers = sorted({0, 1, L // 2, L - 1}) if L > 1 else [0]
+    hosts = {l: oracle.host_layer(make_layer(cfg, l, device=dev).to("cpu")) for l in sample_layers}
+    toks = make_tokens(cfg, 0, cfg.tokens, device="cpu")
+    cores = _cores()
+    oracle.set_threads(cores)
+
+    def one_step(i):
+        # a bounded sample of one decode step: one sampled layer of one token
+        l = sample_layers[i % len(sample_layers)]
+        x = toks[i % cfg.tokens]
+        oracle.layer_step(x, hosts[l], cfg.tau)
+
+    for i in range(args.warmup):
+        one_step(i)
+    t0 = time.perf_counter()
+    done = 0
+    for i in range(args.steps):
+        one_step(args.warmup + i)
+        done += 1
+        if time.perf_counter() - t0 > args.ref_seconds:
+            break
+    el = time.perf_counter() - t0
+    per_layer = el / done
+    value = 1.0 / (per_layer * L)
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": world,
+           "steps": done, "warmup": args.warmup, "ms_per_step": round(per_layer * L * 1e3, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": f"{cfg.key}: {cfg.name}, batch 1, {L} layers per step", "batch": 1,
+                      "layers": L},
+           "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": oracle.threads(),
+                            "kind": "oracle",
+                            "sample": f"{done} layer evaluations over layers {sample_layers} "
+                                      f"(token inputs of layer 0 used for every sampled layer), "
+                                      f"scaled to {L} layers per token"},
+           "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4096)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--config", default="c2")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-seconds", type=float, default=120.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -35,6 +35,11 @@
  *    d % 8 == 0 (fp16) and d % 32 == 0 (INT4); rank % 8 == 0.
  *  - Calls on distinct streams with distinct outputs and workspaces may run
  *    concurrently; calls sharing a workspace must be stream-ordered.
+ *  - A workspace must be zero-filled (e.g. cudaMemset) before its first use;
+ *    the library keeps it consistent from then on.  pi_ffn_layer and
+ *    pi_ffn_stack exchange data between thread blocks through it with bounded
+ *    waits: a wait that exceeds 2 s makes the kernel return early and sets the
+ *    device status read by pi_last_device_status (PI_ERR_TIMEOUT).
  */
 #ifndef PI_H
 #define PI_H
@@ -145,6 +150,21 @@ PI_API pi_status pi_sparse_fc2(const pi_layer_desc *desc, const float *h, const 
 PI_API pi_status pi_ffn_layer(const pi_layer_desc *desc, const pi_half *x, const pi_layer_weights *w,
                        float tau, void *workspace, size_t ws_bytes, float *y, void *stream);
 
+/*
+ * One decode step through a stack of n_layers (1..96) layers that share d,
+ * ffn, wdtype and gated; desc->rank is the largest rank and ranks[l] (NULL:
+ * all desc->rank) the rank of layer l.  Layer l computes y_l from x_l exactly
+ * as pi_ffn_layer does, and the next layer's input is the normalisation of
+ * its output, x_{l+1} = fp16(y_l / sqrt(mean(y_l^2) + eps)) (as
+ * pi_rmsnorm_half).  layers: HOST array of n_layers weight sets (device
+ * pointers inside).  x: [B, d] fp16 input of layer 0; y: [B, d] fp32 output
+ * of the last layer; x_trace (nullable): [n_layers-1, B, d] fp16, the inputs
+ * of layers 1..n_layers-1.  The workspace intermediates are the last layer's.
+ */
+PI_API pi_status pi_ffn_stack(const pi_layer_desc *desc, int n_layers, const pi_layer_weights *layers,
+                              const int *ranks, const pi_half *x, float tau, float eps, void *workspace,
+                              size_t ws_bytes, float *y, pi_half *x_trace, void *stream);
+
 /* Offsets (bytes) of the intermediates pi_ffn_layer leaves in the workspace. */
 typedef struct {
     size_t mask;  /* uint32 [B, ceil(F/32)] per-token masks         */
@@ -163,11 +183,21 @@ PI_API pi_status pi_workspace_layout(const pi_layer_desc *desc, pi_workspace_lay
 PI_API pi_status pi_rmsnorm_half(int d, int batch, const float *y, float eps, pi_half *x_out,
                           void *stream);
 
+/* Number of kernel launches one pi_ffn_layer call issues for `desc` (-1 if
+ * the descriptor is invalid). */
+PI_API int pi_launches_per_layer(const pi_layer_desc *desc);
+
 PI_API const char *pi_status_string(pi_status s);
 
 /* Synchronises `stream`, then returns and clears the device status word set
  * by bounded device-side waits (PI_OK or PI_ERR_TIMEOUT). */
 PI_API pi_status pi_last_device_status(void *stream);
+
+/* Diagnostics: launches one wait on a word that nothing writes, bounded by
+ * timeout_ns (1 ns .. 10 s).  The wait gives up, and the device status becomes
+ * PI_ERR_TIMEOUT (read it with pi_last_device_status); the GPU context stays
+ * usable.  For testing the bounded-wait path. */
+PI_API pi_status pi_debug_wait_timeout(long long timeout_ns, void *stream);
 
 #ifdef __cplusplus
 }

@@ -114,27 +114,43 @@ def zipf_probabilities(F: int, s: float, mean: float, cap: float = 0.999) -> tor
     return torch.clamp(hi * raw, max=cap)
 
 
+def _orth(Y: torch.Tensor) -> torch.Tensor:
+    """Orthonormal basis of the columns of Y (Cholesky-QR through an fp64
+    eigendecomposition of the small Gram matrix, done on the CPU)."""
+    G = (Y.T @ Y).double().cpu()
+    evals, evecs = torch.linalg.eigh(G)
+    evals = torch.clamp(evals, min=float(evals.max()) * 1e-13)
+    return Y @ (evecs / torch.sqrt(evals)).to(Y.device, Y.dtype)
+
+
 def _low_rank(W: torch.Tensor, r: int, g: torch.Generator, oversample: int = 16, power_iters: int = 2):
     """Rank-r truncated SVD factors (P1 = V_r^T, P2 = U_r S_r) of an fp32 matrix.
 
-    Exact SVD for small matrices; otherwise the randomized range finder with
-    power iterations of Halko, Martinsson and Tropp (SIAM Review 2011).
+    Exact SVD (fp64, CPU) for small matrices; otherwise the randomized range
+    finder with power iterations of Halko, Martinsson and Tropp (SIAM Review
+    2011): large products on W's device, small factorisations in fp64 on the CPU.
     """
     F, d = W.shape
     r = min(r, F, d)
     if F * d <= 4_000_000:
-        U, S, Vh = torch.linalg.svd(W.double(), full_matrices=False)
-        return Vh[:r].float(), (U[:, :r] * S[:r]).float()
+        U, S, Vh = torch.linalg.svd(W.double().cpu(), full_matrices=False)
+        return Vh[:r].float().to(W.device), (U[:, :r] * S[:r]).float().to(W.device)
     k = min(r + oversample, d)
     omega = torch.randn(d, k, generator=g, device=W.device, dtype=torch.float32)
-    Q, _ = torch.linalg.qr(W @ omega)
+    Q = _orth(W @ omega)
     for _ in range(power_iters):
-        Z, _ = torch.linalg.qr(W.T @ Q)
-        Q, _ = torch.linalg.qr(W @ Z)
+        Z = _orth(W.T @ Q)
+        Q = _orth(W @ Z)
     Bm = Q.T @ W                                   # [k, d]
-    Ub, S, Vh = torch.linalg.svd(Bm, full_matrices=False)
-    U = Q @ Ub
-    return Vh[:r].contiguous(), (U[:, :r] * S[:r]).contiguous()
+    evals, evecs = torch.linalg.eigh((Bm @ Bm.T).double().cpu())   # Bm Bm^T = Ub S^2 Ub^T
+    order = torch.argsort(evals, descending=True)[:r]
+    S = torch.sqrt(torch.clamp(evals[order], min=0.0))
+    Ub = evecs[:, order]
+    Ub_d = Ub.to(W.device, torch.float32)
+    S_d = S.to(W.device, torch.float32)
+    Vh = (Ub_d.T @ Bm) / torch.clamp(S_d, min=1e-30)[:, None]      # S^-1 Ub^T Bm
+    U = Q @ Ub_d
+    return Vh.contiguous(), (U * S_d).contiguous()
 
 
 def _quantize_g32(w: torch.Tensor):

@@ -27,13 +27,13 @@ def _check_layer(P, cfg, layer, batch, tokens, t0=0):
     w = make_layer(cfg, layer, device=DEV)
     wh = oracle.host_layer(w.to("cpu"))
     st = DecodeStack([w], batch=batch, tau=cfg.tau)
+    P.pi_ffn_layer  # the single-layer stack runs the same code path as pi_ffn_layer
     stats = []
     for s in range(tokens):
         x = make_tokens(cfg, t0 + s * batch, batch, device=DEV)
         y = st.step(x).clone()
         torch.cuda.synchronize()
-        desc = st.layers[0].desc
-        lay = P.pi_workspace_layout(desc)
+        lay = P.pi_workspace_layout(st.desc)
         W = (w.F + 31) // 32
         mask = st.workspace[lay.mask:lay.mask + 4 * batch * W].view(torch.int32).cpu().numpy() \
             .view(np.uint32).reshape(batch, W)

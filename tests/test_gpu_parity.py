@@ -31,7 +31,7 @@ def _layer(cfg, l=0):
 
 
 def _ws(P, desc):
-    return torch.empty(P.pi_workspace_bytes(desc), dtype=torch.uint8, device=DEV)
+    return torch.zeros(P.pi_workspace_bytes(desc), dtype=torch.uint8, device=DEV)
 
 
 def _run_layer(P, w, x, tau, batch=1):
