@@ -43,7 +43,8 @@ _lib = None
 
 EXPORTS = ("pi_workspace_bytes", "pi_workspace_layout", "pi_predict", "pi_compact", "pi_sparse_fc1",
            "pi_sparse_fc2", "pi_ffn_layer", "pi_rmsnorm_half", "pi_status_string",
-           "pi_last_device_status", "pi_launches_per_layer", "pi_ffn_stack", "pi_debug_wait_timeout")
+           "pi_last_device_status", "pi_launches_per_layer", "pi_ffn_stack", "pi_debug_wait_timeout",
+           "pi_sparse_fc2_noalloc")
 
 
 def library_path() -> str:
@@ -77,6 +78,7 @@ def lib(path: Optional[str] = None):
         "pi_launches_per_layer": (I, [D]),
         "pi_ffn_stack": (I, [D, I, C.POINTER(pi_layer_weights), P, P, Fl, Fl, P, S, P, P, P]),
         "pi_debug_wait_timeout": (I, [C.c_longlong, P]),
+        "pi_sparse_fc2_noalloc": (I, [D, P, P, P, Wt, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -162,6 +164,14 @@ def pi_sparse_fc2(desc, h, idx, d_count, wstruct, y, workspace):
     _check("pi_sparse_fc2", lib().pi_sparse_fc2(C.byref(desc), _ptr(h), _ptr(idx), _ptr(d_count),
                                                 C.byref(wstruct), _ptr(y), _ptr(workspace),
                                                 workspace.numel() * workspace.element_size(), _stream()))
+
+
+def pi_sparse_fc2_noalloc(desc, h, idx, d_count, wstruct, y):
+    """pi_sparse_fc2 without a workspace: for callers that cannot allocate
+    device memory (the partial sums live in a fixed array inside the library;
+    calls must not overlap on the GPU)."""
+    _check("pi_sparse_fc2_noalloc", lib().pi_sparse_fc2_noalloc(C.byref(desc), _ptr(h), _ptr(idx), _ptr(d_count),
+                                                                C.byref(wstruct), _ptr(y), _stream()))
 
 
 def pi_ffn_layer(desc, x, wstruct, tau: float, workspace, y):

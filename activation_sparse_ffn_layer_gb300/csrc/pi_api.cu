@@ -126,6 +126,13 @@ T* at(void* ws, size_t off) {
 
 }  // namespace
 
+bool fc2_args_ok(const Plan& p, const float* h, const int32_t* idx, const int32_t* d_count,
+                 const pi_layer_weights* w, const float* y) {
+    return h && idx && d_count && y && aligned16(y) && weights_ok(p, w, false, true, false);
+}
+
+LayerPtrs layer_ptrs(const pi_layer_weights* w) { return ptrs(w); }
+
 constexpr int kMaxStackLayers = 96;
 constexpr long long kWaitTimeoutNs = 2000000000ll;  // 2 s per wait
 

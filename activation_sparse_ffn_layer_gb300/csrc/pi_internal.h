@@ -78,4 +78,10 @@ cudaError_t launch_fused(const FusedStackArgs& a, cudaStream_t s);
 cudaError_t launch_wait_nothing(long long timeout_ns, cudaStream_t s);
 cudaError_t read_and_clear_status(int* out, cudaStream_t s);
 
+// Argument checks of pi_sparse_fc2 (without its workspace) and the weight
+// pointer bundle, shared with the allocation-free FC2 entry point.
+bool fc2_args_ok(const Plan& p, const float* h, const int32_t* idx, const int32_t* d_count,
+                 const pi_layer_weights* w, const float* y);
+LayerPtrs layer_ptrs(const pi_layer_weights* w);
+
 }  // namespace pi

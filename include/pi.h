@@ -143,6 +143,28 @@ PI_API pi_status pi_sparse_fc2(const pi_layer_desc *desc, const float *h, const 
                         void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * pi_sparse_fc2 for callers that cannot allocate device memory.  The pages
+ * have no counterpart to this entry point: it exists for callers such as a
+ * plug-in inside a host framework that owns the whole device memory pool and
+ * offers no allocation hook, or a service with a fixed device-memory budget
+ * that forbids allocation after start-up, which therefore cannot pass the
+ * workspace pi_sparse_fc2 needs.  Same arguments and result as pi_sparse_fc2
+ * without the workspace; the FC2 partial sums live in an 8 MiB array inside
+ * the library that every GPU loading the library holds until process exit.
+ *  - Returns PI_ERR_WORKSPACE when the partial sums of `desc` (splits x batch x
+ *    d floats) exceed that array; allocates nothing in any case.
+ *  - The first call on a device looks up the array's device address (once per
+ *    device, with that device current); make that first call before any
+ *    stream capture.
+ *  - All calls share the one array: calls whose executions overlap on the GPU
+ *    (different streams, or concurrent host threads) race and give wrong
+ *    results; keep them ordered on one stream.
+ */
+PI_API pi_status pi_sparse_fc2_noalloc(const pi_layer_desc *desc, const float *h, const int32_t *idx,
+                                       const int32_t *d_count, const pi_layer_weights *w, float *y,
+                                       void *stream);
+
+/*
  * One whole decode layer: predictor -> compaction -> FC1 -> FC2 on `stream`.
  * x: [B, d] fp16; y: [B, d] fp32.  The per-token masks, the union index list
  * and its count are left in the workspace (see pi_workspace_layout).
