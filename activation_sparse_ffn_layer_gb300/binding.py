@@ -76,7 +76,7 @@ def lib(path: Optional[str] = None):
         "pi_status_string": (C.c_char_p, [I]),
         "pi_last_device_status": (I, [P]),
         "pi_launches_per_layer": (I, [D]),
-        "pi_ffn_stack": (I, [D, I, C.POINTER(pi_layer_weights), P, P, Fl, Fl, P, S, P, P, P]),
+        "pi_ffn_stack": (I, [D, I, C.POINTER(pi_layer_weights), P, P, Fl, Fl, P, S, P, P, P, P]),
         "pi_debug_wait_timeout": (I, [C.c_longlong, P]),
         "pi_sparse_fc2_noalloc": (I, [D, P, P, P, Wt, P, P]),
     }
@@ -180,13 +180,14 @@ def pi_ffn_layer(desc, x, wstruct, tau: float, workspace, y):
                                               _ptr(y), _stream()))
 
 
-def pi_ffn_stack(desc, wstructs, ranks, x, tau: float, eps: float, workspace, y, x_trace=None):
+def pi_ffn_stack(desc, wstructs, ranks, x, tau: float, eps: float, workspace, y, x_trace=None,
+                 layer_counts=None):
     """`wstructs`: a ctypes array of pi_layer_weights (see weights_array);
-    `ranks`: a ctypes int array or None."""
+    `ranks`: a ctypes int array or None; `layer_counts`: int32 [L, 2] or None."""
     n = len(wstructs)
     _check("pi_ffn_stack", lib().pi_ffn_stack(C.byref(desc), n, wstructs, ranks, _ptr(x), float(tau), float(eps),
                                               _ptr(workspace), workspace.numel() * workspace.element_size(),
-                                              _ptr(y), _ptr(x_trace), _stream()))
+                                              _ptr(y), _ptr(x_trace), _ptr(layer_counts), _stream()))
 
 
 def weights_array(layers):

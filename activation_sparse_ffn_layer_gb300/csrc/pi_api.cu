@@ -139,7 +139,11 @@ constexpr long long kWaitTimeoutNs = 2000000000ll;  // 2 s per wait
 // One decode step through n layers: the fused persistent kernel when the plan
 // allows it, else the per-step kernels with the normalisation between layers.
 cudaError_t run_stack(const Plan& p, int n, const LayerPtrs* lp, const int* ranks, const __half* x, float tau,
-                      float eps, void* ws, float* y, __half* x_trace, cudaStream_t s) {
+                      float eps, void* ws, float* y, __half* x_trace, int32_t* layer_counts, cudaStream_t s) {
+    if (layer_counts) {
+        cudaError_t e = cudaMemsetAsync(layer_counts, 0, sizeof(int32_t) * 2 * (size_t)n, s);
+        if (e != cudaSuccess) return e;
+    }
     uint32_t* mask = at<uint32_t>(ws, p.off_mask);
     int32_t* idx = at<int32_t>(ws, p.off_idx);
     int32_t* cnt = at<int32_t>(ws, p.off_count);
@@ -168,6 +172,7 @@ cudaError_t run_stack(const Plan& p, int n, const LayerPtrs* lp, const int* rank
         a.idx_out = idx;
         a.count_out = cnt;
         a.h_out = h;
+        a.layer_counts = layer_counts;
         return launch_fused(a, s);
     }
     const __half* cur = x;
@@ -179,6 +184,7 @@ cudaError_t run_stack(const Plan& p, int n, const LayerPtrs* lp, const int* rank
         cudaError_t e = launch_predict(q, cur, w.p1, w.p2, w.b1, tau, mask, at<float>(ws, p.off_upart), s);
         if (e == cudaSuccess) e = launch_compact(q, mask, nullptr, idx, nullptr, cnt, s);
         if (e == cudaSuccess) e = launch_fc1(q, cur, w, idx, cnt, q.B > 1 ? mask : nullptr, h, s);
+        if (e == cudaSuccess && layer_counts) e = launch_count_active(q, cnt, h, layer_counts + 2 * l, s);
         if (e == cudaSuccess) e = launch_fc2(q, h, idx, cnt, w, at<float>(ws, p.off_part), y, s);
         if (e != cudaSuccess) return e;
         if (l + 1 < n) {
@@ -269,12 +275,12 @@ pi_status pi_ffn_layer(const pi_layer_desc* desc, const pi_half* x, const pi_lay
     if ((size_t)8 * p.d * sizeof(uint16_t) > 200 * 1024) return PI_ERR_UNSUPPORTED;
     const LayerPtrs l = ptrs(w);
     return from_cuda(run_stack(p, 1, &l, nullptr, reinterpret_cast<const __half*>(x), tau, 0.f, workspace, y,
-                               nullptr, static_cast<cudaStream_t>(stream)));
+                               nullptr, nullptr, static_cast<cudaStream_t>(stream)));
 }
 
 pi_status pi_ffn_stack(const pi_layer_desc* desc, int n_layers, const pi_layer_weights* layers, const int* ranks,
                        const pi_half* x, float tau, float eps, void* workspace, size_t ws_bytes, float* y,
-                       pi_half* x_trace, void* stream) {
+                       pi_half* x_trace, int32_t* layer_counts, void* stream) {
     Plan p;
     if (!desc || !make_plan(*desc, &p)) return PI_ERR_INVALID_ARG;
     if (n_layers < 1 || n_layers > kMaxStackLayers || !layers || !x || !aligned16(x) || !y || !aligned16(y) ||
@@ -289,7 +295,7 @@ pi_status pi_ffn_stack(const pi_layer_desc* desc, int n_layers, const pi_layer_w
         lp[l] = ptrs(&layers[l]);
     }
     return from_cuda(run_stack(p, n_layers, lp, ranks, reinterpret_cast<const __half*>(x), tau, eps, workspace, y,
-                               reinterpret_cast<__half*>(x_trace), static_cast<cudaStream_t>(stream)));
+                               reinterpret_cast<__half*>(x_trace), layer_counts, static_cast<cudaStream_t>(stream)));
 }
 
 pi_status pi_rmsnorm_half(int d, int batch, const float* y, float eps, pi_half* x_out, void* stream) {

@@ -115,6 +115,7 @@ struct FusedParams {
     int32_t* idx_out;           // [F]
     int32_t* count_out;         // [1]
     float* h_out;               // [F]
+    int32_t* layer_counts;      // nullable [L][2]: predicted-active, non-zero FC1 output
     FusedLayer layers[kMaxFusedLayers];
 };
 
@@ -518,6 +519,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                 lh[q] = hv;
                 if (l == p.L - 1) p.h_out[j0 + q] = hv;
             }
+            if (p.layer_counts) {
+                int nz = 0;
+                for (int q = tid; q < nmine; q += kThreads) nz += lh[q] != 0.f ? 1 : 0;
+                nz = __reduce_add_sync(FULL, nz);
+                if (lane == 0 && nz) atomicAdd(p.layer_counts + 2 * l + 1, nz);
+                if (c == 0 && tid == 0) p.layer_counts[2 * l] = n_total;
+            }
         }
         __syncthreads();
         PI_STAMP(l, 4);
@@ -792,6 +800,7 @@ cudaError_t launch_fused(const FusedStackArgs& a, cudaStream_t s) {
     prm.idx_out = a.idx_out;
     prm.count_out = a.count_out;
     prm.h_out = a.h_out;
+    prm.layer_counts = a.layer_counts;
     int rmax = 8;
     for (int l = 0; l < a.L; ++l) {
         const LayerPtrs& w = a.layers[l];

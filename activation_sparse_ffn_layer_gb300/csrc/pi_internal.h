@@ -53,6 +53,8 @@ cudaError_t launch_fc1(const Plan& p, const __half* x, const LayerPtrs& w, const
 cudaError_t launch_fc2(const Plan& p, const float* h, const int32_t* idx, const int32_t* count,
                        const LayerPtrs& w, float* partial, float* y, cudaStream_t s);
 cudaError_t launch_rmsnorm(int d, int B, const float* y, float eps, __half* x, cudaStream_t s);
+// out[0] = *count, out[1] = listed neurons whose h is non-zero for some token
+cudaError_t launch_count_active(const Plan& p, const int32_t* count, const float* h, int32_t* out, cudaStream_t s);
 
 // ---- fused persistent stack (batch 1) ----
 struct FusedStackArgs {
@@ -71,6 +73,7 @@ struct FusedStackArgs {
     int32_t* idx_out;
     int32_t* count_out;
     float* h_out;
+    int32_t* layer_counts;    // nullable [L][2] (zeroed by the caller of launch_fused)
 };
 size_t fused_workspace_bytes(int d, int F, size_t rmax_su, int G);
 bool fused_supported(int d, int F, int rmax, bool int4, int G);

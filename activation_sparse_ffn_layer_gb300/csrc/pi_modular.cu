@@ -401,6 +401,28 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const float* __restrict__ y, in
     for (int c = threadIdx.x; c < d; c += blockDim.x) xb[c] = __float2half_rn(yb[c] * scale);
 }
 
+// out[0] = n, out[1] = number of listed neurons with a non-zero h for some token
+__global__ void __launch_bounds__(256) k_count_active(const int32_t* __restrict__ count, const float* __restrict__ h,
+                                                      int B, int32_t* __restrict__ out) {
+    const int n = *count;
+    int nz = 0;
+    for (int j = threadIdx.x; j < n; j += blockDim.x) {
+        bool any = false;
+        for (int b = 0; b < B; ++b) any |= h[(size_t)j * B + b] != 0.f;
+        nz += any ? 1 : 0;
+    }
+    for (int o = 16; o > 0; o >>= 1) nz += __shfl_xor_sync(FULL, nz, o);
+    __shared__ int red[8];
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = nz;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int t = 0;
+        for (int w = 0; w < 8; ++w) t += red[w];
+        out[0] = n;
+        out[1] = t;
+    }
+}
+
 // ------------------------------------------------------------------ launchers
 
 namespace {
@@ -497,6 +519,11 @@ cudaError_t launch_fc2(const Plan& p, const float* h, const int32_t* idx, const 
     if (e != cudaSuccess) return e;
     const int total4 = p.B * p.d / 4;
     k_fc2_reduce<<<(total4 + 255) / 256, 256, 0, s>>>(partial, p.fc2_splits, p.B, p.d, w.b2, y);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_count_active(const Plan& p, const int32_t* count, const float* h, int32_t* out, cudaStream_t s) {
+    k_count_active<<<1, 256, 0, s>>>(count, h, p.B, out);
     return cudaGetLastError();
 }
 

@@ -49,8 +49,17 @@ class DecodeStack:
         self.y = torch.zeros(batch, self.d, dtype=torch.float32, device=dev)
         self.graph: Optional[torch.cuda.CUDAGraph] = None
 
-    def _run(self, x: torch.Tensor, y: torch.Tensor, x_trace: Optional[torch.Tensor] = None):
-        B.pi_ffn_stack(self.desc, self.warr, self.ranks, x, self.tau, self.eps, self.workspace, y, x_trace)
+    def _run(self, x: torch.Tensor, y: torch.Tensor, x_trace: Optional[torch.Tensor] = None,
+             layer_counts: Optional[torch.Tensor] = None):
+        B.pi_ffn_stack(self.desc, self.warr, self.ranks, x, self.tau, self.eps, self.workspace, y, x_trace,
+                       layer_counts)
+
+    def step_counts(self, x: torch.Tensor) -> torch.Tensor:
+        """One step that also returns, per layer, [predicted-active neurons,
+        neurons with a non-zero FC1 output] (int32 [L, 2], on the device)."""
+        cnt = torch.zeros(len(self.layers), 2, dtype=torch.int32, device=x.device)
+        self._run(x, self.y, None, cnt)
+        return cnt
 
     def step(self, x: torch.Tensor) -> torch.Tensor:
         """One decode step (eager launch); returns the last layer's y."""

@@ -120,27 +120,41 @@ def layer_bytes(cfg, r, n_pred, n_relu, batch=1):
     return dict(predict=pred, fc1=fc1, fc2=fc2, small=small, total=pred + fc1 + fc2 + small)
 
 
-def measure_counts(P, st, tokens, cfg):
-    """Untimed eager pass: per token and layer, the predicted-active count and
-    the number of listed neurons with a non-zero FC1 output."""
-    import torch
-    counts = []
+def measure_counts(st, tokens):
+    """Untimed pass: per token and layer, the predicted-active count and the
+    number of listed neurons with a non-zero FC1 output (one stack launch per
+    token, through pi_ffn_stack's layer_counts output)."""
+    out = []
     for t in range(tokens.shape[0]):
-        x = tokens[t:t + 1]
-        per = []
-        for l, layer in enumerate(st.layers):
-            y = st.y
-            P.pi_ffn_layer(layer.desc, x, layer.ws, st.tau, st.workspace, y)
-            lay = P.pi_workspace_layout(layer.desc)
-            n = int(st.workspace[lay.count:lay.count + 4].view(torch.int32).item())
-            h = st.workspace[lay.h:lay.h + 4 * max(n, 1)].view(torch.float32)[:n]
-            per.append((n, int((h != 0).sum().item())))
-            if l + 1 < len(st.layers):
-                xn = torch.empty_like(x)
-                P.pi_rmsnorm_half(cfg.d, 1, y, cfg.rms_eps, xn)
-                x = xn
-        counts.append(per)
-    return counts
+        cnt = st.step_counts(tokens[t:t + 1])
+        out.append([tuple(int(v) for v in row) for row in cnt.cpu().tolist()])
+    return out
+
+
+def kernel_source_hash():
+    """Hash of the fused kernel's sources: an ncu traffic figure is only
+    reported while it was taken on the current kernel."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "activation_sparse_ffn_layer_gb300", "csrc")
+    for name in ("pi_fused.cu", "pi_common.cuh", "pi_internal.h"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config_key):
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary
+    of this workload, or None if absent or taken on a different kernel."""
+    path = os.path.join(ROOT, "profiles", f"fused_stack_{config_key}_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
 
 
 # ------------------------------------------------------------------ our arm
@@ -171,16 +185,12 @@ def run_ours(args):
     weight_bytes = sum(w.nbytes() for w in layers)
 
     # per-token algorithmic bytes (untimed)
-    counts = measure_counts(P, st, tokens, cfg)
+    counts = measure_counts(st, tokens)
     per_tok = []
-    per_kernel = {"predict": 0, "fc1": 0, "fc2": 0}
     for per in counts:
         tot = 0
         for l, (n, nz) in enumerate(per):
-            lb = layer_bytes(cfg, layers[l].r, n, nz, B)
-            tot += lb["total"]
-            for k in per_kernel:
-                per_kernel[k] += lb[k]
+            tot += layer_bytes(cfg, layers[l].r, n, nz, B)["total"]
         tot += (cfg.layers - 1) * B * (4 * cfg.d + 2 * cfg.d)   # inter-layer norm: read y, write x
         per_tok.append(tot)
     n_pred_mean = sum(n for per in counts for n, _ in per) / (T * cfg.layers)
@@ -196,17 +206,22 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ka = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    kb = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     with ClockSampler(torch.cuda.current_device()) as clk:
         torch.cuda.synchronize()
         e0.record(stream)
         for i in range(K):
             t = (W + i) % T
             st.x_in.copy_(tokens[t:t + 1])
+            ka[i].record(stream)
             st.replay()
+            kb[i].record(stream)
         e1.record(stream)
         torch.cuda.synchronize()
     clocks = clk.summary()
     ms = e0.elapsed_time(e1)
+    kernel_ms = sum(a.elapsed_time(b) for a, b in zip(ka, kb))
     if world > 1:
         tt = torch.tensor([ms], device="cuda")
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -216,19 +231,14 @@ def run_ours(args):
     tok_s = world * K * B / (ms / 1e3)
     peak, peak_kind = _peaks()
 
-    # dominant step, timed live with CUDA events on the launching stream
-    kern = time_kernels(P, st, tokens, cfg, K=min(K, 256), W=W)
-    names = {"predict": "pi_predict", "fc1": "pi_sparse_fc1", "fc2": "pi_sparse_fc2"}
-    dom = max(kern["ms"], key=lambda k: kern["ms"][k])
-    dom_bytes = per_kernel.get(dom, 0) / (T * cfg.layers)        # mean bytes per launch
-    dom_ms = kern["ms"][dom] / kern["launches"][dom]
-    achieved = dom_bytes / (dom_ms / 1e3) / 1e9 if dom in per_kernel else None
-    roofline = {"kernel": names.get(dom, dom), "bound": "hbm",
-                "achieved": round(achieved, 1) if achieved else None, "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4) if achieved else None, "traffic": None,
-                "peak_kind": peak_kind,
-                "bytes_per_launch": int(dom_bytes), "us_per_launch": round(dom_ms * 1e3, 2),
-                "share_of_step": round(kern["ms"][dom] / sum(kern["ms"].values()), 3)}
+    # the dominant (and only) kernel of a step: one launch of the fused stack kernel
+    per_launch = kernel_ms / K
+    achieved = step_bytes / (per_launch / 1e3) / 1e9
+    traffic = recorded_traffic(cfg.key)
+    roofline = {"kernel": "k_fused_stack (pi_ffn_stack)", "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": traffic, "peak_kind": peak_kind, "bytes_per_launch": int(step_bytes),
+                "us_per_launch": round(per_launch * 1e3, 2), "share_of_step": round(kernel_ms / ms, 3)}
 
     e2e = time_e2e(st, tokens, K=min(K, 512), W=W)
     out = {
@@ -246,7 +256,6 @@ def run_ours(args):
         "active": {"predicted_per_layer": round(n_pred_mean, 1), "relu_nonzero_per_layer": round(n_relu_mean, 1),
                    "F": cfg.F},
         "roofline": roofline,
-        "kernel_ms_per_step": {names.get(k, k): round(v / kern["steps"], 4) for k, v in kern["ms"].items()},
         "e2e": e2e,
         "gpu_launches": K * st.launches_per_step(),
         "clocks": clocks,
@@ -257,53 +266,6 @@ def run_ours(args):
         print(json.dumps(out), flush=True)
     if world > 1:
         dist.destroy_process_group()
-
-
-def time_kernels(P, st, tokens, cfg, K, W):
-    """Eager steps through the per-step entry points with CUDA events around
-    each call on the launching stream: total ms per entry point."""
-    import torch
-    stream = torch.cuda.current_stream()
-    ms = {"predict": 0.0, "compact": 0.0, "fc1": 0.0, "fc2": 0.0, "norm": 0.0}
-    launches = {k: 0 for k in ms}
-    T = tokens.shape[0]
-    bufs = {}
-    for step in range(W + K):
-        x = tokens[step % T:step % T + 1]
-        evs = []
-        for l, layer in enumerate(st.layers):
-            desc = layer.desc
-            lay = P.pi_workspace_layout(desc)
-            ws = st.workspace
-            mask = ws[lay.mask:lay.mask + 4 * ((layer.w.F + 31) // 32)].view(torch.int32)
-            idx = ws[lay.idx:lay.idx + 4 * layer.w.F].view(torch.int32)
-            cnt = ws[lay.count:lay.count + 4].view(torch.int32)
-            h = ws[lay.h:lay.h + 4 * layer.w.F].view(torch.float32)
-            marks = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-            marks[0].record(stream)
-            P.pi_predict(desc, x, layer.w.p1, layer.w.p2, layer.w.b1, st.tau, mask, ws)
-            marks[1].record(stream)
-            P.pi_compact(desc, mask, None, idx, None, cnt)
-            marks[2].record(stream)
-            P.pi_sparse_fc1(desc, x, layer.ws, idx, cnt, None, h)
-            marks[3].record(stream)
-            P.pi_sparse_fc2(desc, h, idx, cnt, layer.ws, st.y, ws)
-            marks[4].record(stream)
-            if l + 1 < len(st.layers):
-                xn = bufs.setdefault(l % 2, torch.empty_like(st.x_in))
-                P.pi_rmsnorm_half(cfg.d, 1, st.y, cfg.rms_eps, xn)
-                x = xn
-            marks[5].record(stream)
-            evs.append((l, marks))
-        torch.cuda.synchronize()
-        if step >= W:
-            for l, m in evs:
-                for i, k in enumerate(("predict", "compact", "fc1", "fc2", "norm")):
-                    if k == "norm" and l + 1 == len(st.layers):
-                        continue
-                    ms[k] += m[i].elapsed_time(m[i + 1])
-                    launches[k] += 1
-    return {"ms": ms, "launches": launches, "steps": K}
 
 
 def time_e2e(st, tokens, K, W):

@@ -181,11 +181,15 @@ PI_API pi_status pi_ffn_layer(const pi_layer_desc *desc, const pi_half *x, const
  * pi_rmsnorm_half).  layers: HOST array of n_layers weight sets (device
  * pointers inside).  x: [B, d] fp16 input of layer 0; y: [B, d] fp32 output
  * of the last layer; x_trace (nullable): [n_layers-1, B, d] fp16, the inputs
- * of layers 1..n_layers-1.  The workspace intermediates are the last layer's.
+ * of layers 1..n_layers-1; layer_counts (nullable): [n_layers, 2] int32, per
+ * layer the number of predicted-active neurons and the number of those whose
+ * FC1 output is non-zero (for any token of the batch).  The workspace
+ * intermediates are the last layer's.
  */
 PI_API pi_status pi_ffn_stack(const pi_layer_desc *desc, int n_layers, const pi_layer_weights *layers,
                               const int *ranks, const pi_half *x, float tau, float eps, void *workspace,
-                              size_t ws_bytes, float *y, pi_half *x_trace, void *stream);
+                              size_t ws_bytes, float *y, pi_half *x_trace, int32_t *layer_counts,
+                              void *stream);
 
 /* Offsets (bytes) of the intermediates pi_ffn_layer leaves in the workspace. */
 typedef struct {

@@ -120,3 +120,19 @@ def test_bounded_wait_times_out_and_context_survives():
     close(y[0].cpu().numpy(), oracle.ffn_masked(x[0].cpu(), oracle.host_layer(w.to("cpu")), _mask_of(P, st)),
           "layer after timeout")
     assert P.pi_last_device_status() == 0
+
+
+def test_layer_counts_match_last_layer_workspace():
+    P = _pi()
+    from activation_sparse_ffn_layer_gb300.runtime import DecodeStack
+    cfg = small(CONFIGS["c2"], d=1024, F=4096, rank=64)
+    ws = [make_layer(cfg, l, device=DEV) for l in range(3)]
+    st = DecodeStack(ws, batch=1, tau=cfg.tau, eps=cfg.rms_eps)
+    x = make_tokens(cfg, 0, 1, device=DEV)
+    cnt = st.step_counts(x).cpu().numpy()
+    lay = P.pi_workspace_layout(st.desc)
+    n = int(st.workspace[lay.count:lay.count + 4].view(torch.int32).item())
+    h = st.workspace[lay.h:lay.h + 4 * n].view(torch.float32).cpu().numpy()
+    assert cnt.shape == (3, 2)
+    assert cnt[2, 0] == n and cnt[2, 1] == int((h != 0).sum())
+    assert np.all(cnt[:, 1] <= cnt[:, 0]) and np.all(cnt[:, 0] > 0)
