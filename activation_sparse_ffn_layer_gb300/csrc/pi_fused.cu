@@ -24,6 +24,8 @@
 // this CTA are bulk-prefetched into L2.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "pi_common.cuh"
 #include "pi_internal.h"
 
@@ -51,6 +53,53 @@ PI_DEV unsigned ld_acquire(const unsigned* p) {
     return v;
 }
 PI_DEV float4 ld_cg4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
+
+// ---- shared-memory mbarrier + 1D bulk copy (TMA) helpers
+PI_DEV unsigned smem_u32(const void* p) { return static_cast<unsigned>(__cvta_generic_to_shared(p)); }
+PI_DEV void mbar_init(unsigned long long* mbar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(mbar)), "r"(count) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+PI_DEV void mbar_arrive_expect_tx(unsigned long long* mbar, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(mbar)), "r"(bytes) : "memory");
+}
+PI_DEV bool mbar_test(unsigned long long* mbar, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n .reg .pred q;\n mbarrier.test_wait.parity.shared::cta.b64 q, [%1], %2;\n selp.u32 %0, 1, 0, q;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(mbar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// global -> shared bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned)
+PI_DEV void bulk_g2s(void* dst, const void* src, unsigned bytes, unsigned long long* mbar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(mbar))
+                 : "memory");
+}
+// Before leaving after a failure: wait (bounded) for this CTA's own bulk copy
+// still in flight, so none lands in shared memory after the CTA has exited.
+PI_DEV void mbar_drain(unsigned long long* mbar, unsigned parity, long long timeout_ns) {
+    const unsigned long long t0 = globaltimer();
+    while (!mbar_test(mbar, parity) && (long long)(globaltimer() - t0) <= timeout_ns) {
+    }
+}
+
+// Wait (bounded) until the mbarrier phase with this parity has completed.
+PI_DEV bool mbar_wait(unsigned long long* mbar, unsigned parity, long long timeout_ns, int* bad) {
+    if (mbar_test(mbar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (!mbar_test(mbar, parity)) {
+        if ((long long)(globaltimer() - t0) > timeout_ns || *(volatile int*)bad) {
+            atomicExch(&g_pi_status, (int)PI_ERR_TIMEOUT);
+            *(volatile int*)bad = 1;
+            return false;
+        }
+    }
+    return true;
+}
 
 // Grid barrier number `k` of this launch.  Returns false (and sets the status
 // word) if the wait exceeded timeout_ns or another CTA already failed.
@@ -116,13 +165,19 @@ struct FusedParams {
     int32_t* count_out;         // [1]
     float* h_out;               // [F]
     int32_t* layer_counts;      // nullable [L][2]: predicted-active, non-zero FC1 output
+    int pred_smem;              // 1: each CTA's predictor slice is bulk-copied to shared memory
+    int p1s_bytes, p2s_bytes, b1s_bytes;  // capacities of the shared predictor buffers
+    int w2s_bytes;              // staging buffer for this CTA's W2t rows (0: FC2 reads HBM directly)
     FusedLayer layers[kMaxFusedLayers];
 };
 
 // Dynamic smem layout (bytes): xf float[d] | u float[rmax] | ustage float[usmax]
 //   | m16 int[M] | upre int[M+1] | lidx int[cap] | lh float[cap] | scratch
+//   | P1 slice | P2 slice | bias slice   (the last three only with pred_smem)
 struct SmemPlan {
     int d, rmax, usmax, M, cap;
+    int p1s = 0, p2s = 0, b1s = 0;  // shared predictor buffers (bytes, 16-aligned), 0 if unused
+    int w2s = 0;                    // W2t row staging buffer (bytes, 16-aligned), 0 if unused
     __host__ __device__ int off_u() const { return d * 4; }
     __host__ __device__ int off_ust() const { return off_u() + rmax * 4; }
     __host__ __device__ int off_m16() const { return off_ust() + ((usmax + 3) / 4) * 16; }
@@ -130,7 +185,11 @@ struct SmemPlan {
     __host__ __device__ int off_lidx() const { return off_upre() + (M + 1) * 4; }
     __host__ __device__ int off_lh() const { return off_lidx() + cap * 4; }
     __host__ __device__ int off_scr() const { return ((off_lh() + cap * 4 + 15) / 16) * 16; }
-    __host__ __device__ int bytes() const { return off_scr() + 4096 * 4; }
+    __host__ __device__ int off_p1s() const { return off_scr() + 4096 * 4; }
+    __host__ __device__ int off_p2s() const { return off_p1s() + p1s; }
+    __host__ __device__ int off_b1s() const { return off_p2s() + p2s; }
+    __host__ __device__ int off_w2s() const { return off_b1s() + b1s; }
+    __host__ __device__ int bytes() const { return off_w2s() + w2s; }
 };
 
 // dot of 8 fp16 weights with 8 fp32 values in smem
@@ -211,7 +270,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
         usmax = max(usmax, p.layers[l].r * p.layers[l].su);
     }
     const int cap = F / G + 2;
-    const SmemPlan sp{d, rmax, usmax, M, cap};
+    SmemPlan sp{d, rmax, usmax, M, cap};
+    sp.p1s = p.pred_smem ? p.p1s_bytes : 0;
+    sp.p2s = p.pred_smem ? p.p2s_bytes : 0;
+    sp.b1s = p.pred_smem ? p.b1s_bytes : 0;
+    sp.w2s = p.w2s_bytes;
     float* xf = reinterpret_cast<float*>(smem);
     float* us = reinterpret_cast<float*>(smem + sp.off_u());
     float* ust = reinterpret_cast<float*>(smem + sp.off_ust());
@@ -221,10 +284,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
     float* lh = reinterpret_cast<float*>(smem + sp.off_lh());
     float* red = reinterpret_cast<float*>(smem + sp.off_scr());
     int* scr = reinterpret_cast<int*>(smem + sp.off_scr());
+    __half* p1s = reinterpret_cast<__half*>(smem + sp.off_p1s());
+    __half* p2s = reinterpret_cast<__half*>(smem + sp.off_p2s());
+    __half* b1s = reinterpret_cast<__half*>(smem + sp.off_b1s());
+    unsigned char* w2s = smem + sp.off_w2s();
+    // bytes of one staged W2t row: fp16 row, or INT4 codes followed by the scales
+    const int w2row = KIND == 2 ? d / 2 + d / 16 : 2 * d;
     __shared__ int bad;
     __shared__ float rs_s;
-    __shared__ unsigned preds[8][kWarps];
-    if (tid == 0) bad = 0;
+    __shared__ __align__(8) unsigned long long pred_mbar;
+    __shared__ __align__(8) unsigned long long w2_mbar;
+    if (tid == 0) {
+        bad = 0;
+        mbar_init(&pred_mbar, 1);
+        mbar_init(&w2_mbar, 1);
+    }
+    unsigned w2_uses = 0;   // completed-or-pending phases of w2_mbar
+    bool w2_pending = false;
 
     // barrier targets: the counter holds G arrivals per barrier ever completed
     const unsigned long long ebase = __ldcg(p.epoch);
@@ -236,44 +312,70 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
     // CTA 0 advances the epoch when it leaves, by every barrier this launch
     // schedules (also after a failure: the counts then no longer matter, the
     // status word reports the failure)
+    int inflight = -1;   // layer whose predictor copy is issued but not yet waited for
     auto leave = [&]() {
+        if (inflight >= 0) mbar_drain(&pred_mbar, (unsigned)(inflight & 1), tmo);
+        if (w2_pending) mbar_drain(&w2_mbar, (w2_uses - 1) & 1u, tmo);
         if (c == 0 && tid == 0) {
             const unsigned long long next = ebase + (unsigned long long)kBarriersPerLayer * p.L;
             __stcg(p.epoch, next);
         }
     };
 
-    // prefetch this CTA's predictor rows of layer l into L2
-    auto prefetch_predictor = [&](int l) {
-        if (tid != 0 || l >= p.L) return;
-        const FusedLayer& ly = p.layers[l];
-        const int items = ly.r * ly.su;
-        for (int q = c * kWarps; q < items; q += G * kWarps) {
-            const int last = min(items, q + kWarps);
-            for (int t = q; t < last; ++t) {
-                const int i = t / ly.su, s = t % ly.su;
-                const int c0 = s * ly.seg, c1 = min(d, c0 + ly.seg);
-                prefetch_l2(ly.p1 + (size_t)i * d + c0, (unsigned)(c1 - c0) * 2u);
-            }
-        }
-        for (int m = c; m < M; m += G) {
-            const int rows = min(16, F - m * 16);
-            prefetch_l2(ly.p2 + (size_t)m * 16 * ly.r, (unsigned)(rows * ly.r * 2));
-        }
+    // This CTA's share of layer l's predictor: P1 items [q0, q1) (item q =
+    // row q/su, segment q%su; consecutive items are contiguous in memory) and
+    // mask units [m0, m1) (16 rows of P2 each, contiguous).
+    // (sizes here are far below 2^32 / G, so 32-bit unsigned arithmetic is exact)
+    auto item_range = [&](const FusedLayer& ly, int* q0, int* q1) {
+        const unsigned items = (unsigned)(ly.r * ly.su);
+        *q0 = (int)(items * (unsigned)c / (unsigned)G);
+        *q1 = (int)(items * (unsigned)(c + 1) / (unsigned)G);
     };
-    prefetch_predictor(0);
+    const int um0 = (int)((unsigned)M * (unsigned)c / (unsigned)G);
+    const int um1 = (int)((unsigned)M * (unsigned)(c + 1) / (unsigned)G);
+    const int row0 = um0 * 16, row1 = min(F, um1 * 16);
+    // element offset of item q in P1
+    auto item_off = [&](const FusedLayer& ly, int q) -> size_t {
+        const int i = q / ly.su, sg = q % ly.su;
+        return (size_t)i * d + (size_t)sg * ly.seg;
+    };
+    // thread 0: bulk-copy layer l's predictor slice into shared memory
+    auto issue_predictor = [&](int l) {
+        const FusedLayer& ly = p.layers[l];
+        int q0, q1;
+        item_range(ly, &q0, &q1);
+        const size_t e0 = item_off(ly, q0), e1 = q1 < ly.r * ly.su ? item_off(ly, q1) : (size_t)ly.r * d;
+        const unsigned b_p1 = (unsigned)(2 * (e1 - e0));
+        const unsigned b_p2 = (unsigned)(2 * (size_t)ly.r * (row1 - row0));
+        const unsigned b_b1 = (unsigned)(2 * ((row1 - row0) & ~7));     // whole 16-byte pieces
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive_expect_tx(&pred_mbar, b_p1 + b_p2 + b_b1);
+        if (b_p1) bulk_g2s(p1s, ly.p1 + e0, b_p1, &pred_mbar);
+        if (b_p2) bulk_g2s(p2s, ly.p2 + (size_t)row0 * ly.r, b_p2, &pred_mbar);
+        if (b_b1) bulk_g2s(b1s, ly.b1 + row0, b_b1, &pred_mbar);
+    };
     __syncthreads();
+    if (p.pred_smem) {
+        if (tid == 0) issue_predictor(0);
+        inflight = 0;
+    }
 
     // phase-D columns of this CTA: a contiguous range of 4-column groups
     const int ng4 = d / 4;
     const int g0 = (int)(((long long)ng4 * c) / G), g1 = (int)(((long long)ng4 * (c + 1)) / G);
     const int ngm = g1 - g0;
-    int PS = 1;
-    while (ngm > 0 && PS * 2 * ngm <= kThreads) PS *= 2;
 
     for (int l = 0; l < p.L; ++l) {
         const FusedLayer& ly = p.layers[l];
         const int r = ly.r;
+        // layer l's predictor slices are consumed by then (phase B ended with a
+        // barrier): bring in layer l+1's once this CTA's FC rows are loaded
+        auto issue_next = [&]() {
+            if (p.pred_smem && l + 1 < p.L) {
+                if (tid == 0) issue_predictor(l + 1);
+                inflight = l + 1;
+            }
+        };
         PI_STAMP(l, 0);
 
         // ---------------------------------------------------------- phase A
@@ -316,16 +418,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
         __syncthreads();
         PI_STAMP(l, 1);
         {
-            const int items = r * ly.su;
-            for (int q = c * kWarps + warp; q < items; q += G * kWarps) {
-                const int i = q / ly.su, s = q % ly.su;
-                const int c0 = s * ly.seg, c1 = min(d, c0 + ly.seg);
-                const __half* row = ly.p1 + (size_t)i * d;
+            // this CTA's items [q0, q1), at most one per warp
+            int q0, q1;
+            item_range(ly, &q0, &q1);
+            if (p.pred_smem && mbar_wait(&pred_mbar, (unsigned)(l & 1), tmo, &bad)) inflight = -1;
+            for (int q = q0 + warp; q < q1; q += kWarps) {
+                const int i = q / ly.su, sg = q % ly.su;
+                const int c0 = sg * ly.seg, c1 = min(d, c0 + ly.seg);
+                const __half* row = p.pred_smem ? p1s + (item_off(ly, q) - item_off(ly, q0)) - c0
+                                                : ly.p1 + (size_t)i * d;
                 float acc = 0.f;
+                if (p.pred_smem) {
+#pragma unroll 4
+                    for (int e = c0 + lane * 8; e < c1; e += 256)
+                        acc += dot8(*reinterpret_cast<const uint4*>(row + e), xf + e);
+                } else {
 #pragma unroll 8
-                for (int e = c0 + lane * 8; e < c1; e += 256) acc += dot8(ld_stream16(row + e), xf + e);
+                    for (int e = c0 + lane * 8; e < c1; e += 256) acc += dot8(ld_stream16(row + e), xf + e);
+                }
                 acc = warp_sum(acc);
-                if (lane == 0) p.xu[(size_t)s * r + i] = acc;
+                if (lane == 0) p.xu[(size_t)sg * r + i] = acc;
             }
         }
         if (!sync()) { leave(); return; }
@@ -347,47 +459,93 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
         {
             const int nvec = r / 8;
             const int vpl = (nvec + 31) / 32;
-            // units of 16 rows: this CTA's units are m = c, c+G, ...; UB at a
-            // time, warp w taking row w of each, lanes across the row
-            constexpr int UB = 4;
-            for (int m0 = c; m0 < M; m0 += UB * G) {
-                float acc[UB], bk[UB];
-                int kk[UB];
+            // this CTA's units [um0, um1): one warp per unit of 16 rows.  Lane L
+            // accumulates, for each of the 16 rows, the products of the row's
+            // vectors L, L+32, ... with u; a halving butterfly then leaves the
+            // full dot product of row (L >> 1) in lanes L (16 shuffles for 16
+            // rows), and one ballot forms the unit's 16 mask bits.
+            for (int m = um0 + warp; m < um1; m += kWarps) {
+                const int rbase = m * 16;
+                float v[16];
 #pragma unroll
-                for (int b = 0; b < UB; ++b) {
-                    const int m = m0 + b * G;
-                    kk[b] = m < M ? m * 16 + warp : F;
-                    if (kk[b] > F) kk[b] = F;
-                    acc[b] = 0.f;
-                    bk[b] = (kk[b] < F && lane == 0) ? __half2float(ly.b1[kk[b]]) : 0.f;
-                }
+                for (int k = 0; k < 16; ++k) v[k] = 0.f;
                 for (int e = 0; e < vpl; ++e) {
-                    const int v = lane + 32 * e;
-                    uint4 pv[UB];
+                    const int vi = lane + 32 * e;
+                    if (vi < nvec) {
+                        float uf[8];
+                        {
+                            const float4 a = reinterpret_cast<const float4*>(us + vi * 8)[0];
+                            const float4 b = reinterpret_cast<const float4*>(us + vi * 8)[1];
+                            uf[0] = a.x; uf[1] = a.y; uf[2] = a.z; uf[3] = a.w;
+                            uf[4] = b.x; uf[5] = b.y; uf[6] = b.z; uf[7] = b.w;
+                        }
 #pragma unroll
-                    for (int b = 0; b < UB; ++b)
-                        if (kk[b] < F && v < nvec) pv[b] = ld_stream16(ly.p2 + (size_t)kk[b] * r + v * 8);
+                        for (int k = 0; k < 16; ++k) {
+                            const int row = rbase + k;
+                            if (row < F) {
+                                const uint4 w = p.pred_smem
+                                    ? *reinterpret_cast<const uint4*>(p2s + (size_t)(row - row0) * r + vi * 8)
+                                    : ld_stream16(ly.p2 + (size_t)row * r + vi * 8);
+                                float wf[8];
+                                h8_to_f8(w, wf);
 #pragma unroll
-                    for (int b = 0; b < UB; ++b)
-                        if (kk[b] < F && v < nvec) acc[b] += dot8(pv[b], us + v * 8);
-                }
-#pragma unroll
-                for (int b = 0; b < UB; ++b) {
-                    const float a = warp_sum(acc[b]);
-                    if (lane == 0) preds[b][warp] = (kk[b] < F && a + bk[b] > p.tau) ? 1u : 0u;
-                }
-                __syncthreads();
-                if (tid < UB) {
-                    const int m = m0 + tid * G;
-                    if (m < M) {
-                        unsigned bits = 0;
-#pragma unroll
-                        for (int w = 0; w < 16; ++w) bits |= preds[tid][w] << w;
-                        reinterpret_cast<uint16_t*>(p.xmask)[m] = (uint16_t)bits;
-                        if (l == p.L - 1) reinterpret_cast<uint16_t*>(p.mask_out)[m] = (uint16_t)bits;
+                                for (int t = 0; t < 8; ++t) v[k] = fmaf(wf[t], uf[t], v[k]);
+                            }
+                        }
                     }
                 }
-                __syncthreads();
+                // butterfly: after the step with offset o, a lane keeps the half of
+                // its values selected by its bit o and adds the partner's copy
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const bool hi = lane & 16;
+                    const float send = hi ? v[k] : v[k + 8];
+                    const float keep = hi ? v[k + 8] : v[k];
+                    v[k] = keep + __shfl_xor_sync(FULL, send, 16);
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const bool hi = lane & 8;
+                    const float send = hi ? v[k] : v[k + 4];
+                    const float keep = hi ? v[k + 4] : v[k];
+                    v[k] = keep + __shfl_xor_sync(FULL, send, 8);
+                }
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const bool hi = lane & 4;
+                    const float send = hi ? v[k] : v[k + 2];
+                    const float keep = hi ? v[k + 2] : v[k];
+                    v[k] = keep + __shfl_xor_sync(FULL, send, 4);
+                }
+                {
+                    const bool hi = lane & 2;
+                    const float send = hi ? v[0] : v[1];
+                    const float keep = hi ? v[1] : v[0];
+                    v[0] = keep + __shfl_xor_sync(FULL, send, 2);
+                }
+                v[0] += __shfl_xor_sync(FULL, v[0], 1);
+                // lane L now holds row k = 8*b16 + 4*b8 + 2*b4 + b2 of the unit
+                const int k = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+                const int row = rbase + k;
+                bool pred = false;
+                if (row < F && (lane & 1) == 0) {
+                    const int rl = row - row0;
+                    const float bk = (p.pred_smem && rl < ((row1 - row0) & ~7)) ? __half2float(b1s[rl])
+                                                                               : __half2float(ly.b1[row]);
+                    pred = v[0] + bk > p.tau;
+                }
+                const unsigned bal = __ballot_sync(FULL, pred);
+                if (lane == 0) {
+                    unsigned bits = 0;
+                    // the bit of row kk(L) sits at ballot position L (even lanes)
+#pragma unroll
+                    for (int L2 = 0; L2 < 32; L2 += 2) {
+                        const int kk = ((L2 >> 4) & 1) * 8 + ((L2 >> 3) & 1) * 4 + ((L2 >> 2) & 1) * 2 + ((L2 >> 1) & 1);
+                        bits |= ((bal >> L2) & 1u) << kk;
+                    }
+                    reinterpret_cast<uint16_t*>(p.xmask)[m] = (uint16_t)bits;
+                    if (l == p.L - 1) reinterpret_cast<uint16_t*>(p.mask_out)[m] = (uint16_t)bits;
+                }
             }
             if ((M & 1) && c == 0 && tid == 0) {
                 reinterpret_cast<uint16_t*>(p.xmask)[M] = 0;   // bits past F
@@ -422,8 +580,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
             n_total = total;
         }
         __syncthreads();
-        const int j0 = (int)(((long long)n_total * c) / G);
-        const int j1 = (int)(((long long)n_total * (c + 1)) / G);
+        const int j0 = (int)((unsigned)n_total * (unsigned)c / (unsigned)G);
+        const int j1 = (int)((unsigned)n_total * (unsigned)(c + 1) / (unsigned)G);
         const int nmine = j1 - j0;
         // collect this CTA's neuron ids (storage rows) of list positions [j0, j1)
         for (int m = tid; m < M; m += kThreads) {
@@ -443,7 +601,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
         }
         if (l == p.L - 1 && c == 0 && tid == 0) *p.count_out = n_total;
         __syncthreads();
-        prefetch_predictor(l + 1);
+        // few rows per CTA: stage all of this CTA's W2t rows in shared memory now,
+        // so their HBM latency overlaps FC1 (rows whose FC1 output turns out to
+        // be zero are loaded but not used)
+        const bool w2_staged = nmine > 0 && nmine * w2row <= p.w2s_bytes;
+        if (w2_staged) {
+            if (tid == 0) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive_expect_tx(&w2_mbar, (unsigned)(nmine * w2row));
+                for (int q = 0; q < nmine; ++q) {
+                    const size_t k = (size_t)lidx[q];
+                    if (KIND != 2) {
+                        bulk_g2s(w2s + (size_t)q * w2row, static_cast<const __half*>(ly.w2t) + k * d, 2u * d, &w2_mbar);
+                    } else {
+                        bulk_g2s(w2s + (size_t)q * w2row, static_cast<const uint8_t*>(ly.w2t) + k * (d / 2),
+                                 (unsigned)(d / 2), &w2_mbar);
+                        bulk_g2s(w2s + (size_t)q * w2row + d / 2, ly.w2ts + k * (d / 32), (unsigned)(d / 16),
+                                 &w2_mbar);
+                    }
+                }
+            }
+            ++w2_uses;
+            w2_pending = true;
+        }
 
         // FC1: (neuron, segment) items spread over all warps so that every warp
         // has loads in flight; segment dot products are combined in a fixed order
@@ -532,7 +712,42 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
 
         // FC2: the whole CTA accumulates its neurons' W2t rows; rows whose
         // FC1 output is zero are skipped (ReLU removed them from FC2)
-        if (KIND != 2) {
+        if (w2_staged) {
+            if (mbar_wait(&w2_mbar, (w2_uses - 1) & 1u, tmo, &bad)) w2_pending = false;
+        }
+        if (KIND != 2 && w2_staged) {
+            float acc[NCH][8];
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[ch][e] = 0.f;
+            for (int q = 0; q < nmine; ++q) {
+                const float hq = lh[q];
+                if (hq == 0.f) continue;
+                const __half* row = reinterpret_cast<const __half*>(w2s + (size_t)q * w2row);
+#pragma unroll
+                for (int ch = 0; ch < NCH; ++ch) {
+                    const int col = ch * 4096 + tid * 8;
+                    if (col < d) {
+                        float wf[8];
+                        h8_to_f8(*reinterpret_cast<const uint4*>(row + col), wf);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[ch][e] = fmaf(hq, wf[e], acc[ch][e]);
+                    }
+                }
+            }
+            issue_next();
+            float* dst = p.xyp + (size_t)c * d;
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch) {
+                const int col = ch * 4096 + tid * 8;
+                if (col < d) {
+                    float4* o = reinterpret_cast<float4*>(dst + col);
+                    __stcg(o, make_float4(acc[ch][0], acc[ch][1], acc[ch][2], acc[ch][3]));
+                    __stcg(o + 1, make_float4(acc[ch][4], acc[ch][5], acc[ch][6], acc[ch][7]));
+                }
+            }
+        } else if (KIND != 2) {
             constexpr int RB = NCH == 1 ? 4 : (NCH == 2 ? 2 : 1);
             float acc[NCH][8];
 #pragma unroll
@@ -570,6 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                     }
                 }
             }
+            issue_next();
             float* dst = p.xyp + (size_t)c * d;
 #pragma unroll
             for (int ch = 0; ch < NCH; ++ch) {
@@ -596,9 +812,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                     const float hv = q < nmine ? lh[q] : 0.f;
                     hs[b] = 0.f;
                     if (hv != 0.f && mine) {
-                        const size_t k = (size_t)lidx[q];
-                        wv[b] = ld_stream16(static_cast<const uint8_t*>(ly.w2t) + k * (d / 2) + col / 2);
-                        hs[b] = hv * __half2float(ly.w2ts[k * (d / 32) + col / 32]);
+                        if (w2_staged) {
+                            const unsigned char* row = w2s + (size_t)q * w2row;
+                            wv[b] = *reinterpret_cast<const uint4*>(row + col / 2);
+                            hs[b] = hv * __half2float(reinterpret_cast<const __half*>(row + d / 2)[col / 32]);
+                        } else {
+                            const size_t k = (size_t)lidx[q];
+                            wv[b] = ld_stream16(static_cast<const uint8_t*>(ly.w2t) + k * (d / 2) + col / 2);
+                            hs[b] = hv * __half2float(ly.w2ts[k * (d / 32) + col / 32]);
+                        }
                     }
                 }
 #pragma unroll
@@ -614,6 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                     }
                 }
             }
+            issue_next();
             if (mine) {
                 float4* o = reinterpret_cast<float4*>(p.xyp + (size_t)c * d + col);
 #pragma unroll
@@ -627,29 +850,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
 
         // ---------------------------------------------------------- phase D
         {
-            // this CTA's ngm 4-column groups x PS partial subsets; thread t ->
-            // group t % ngm, partials ps, ps + PS, ...; then a fixed tree over ps
-            const int gi = ngm > 0 ? tid % ngm : 0;
-            const int ps = ngm > 0 ? tid / ngm : PS;
-            const int col = (g0 + gi) * 4;
-            float4* red4 = reinterpret_cast<float4*>(red);
-            float4 bias = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (ps == 0 && ngm > 0)
-                bias = make_float4(__half2float(ly.b2[col]), __half2float(ly.b2[col + 1]),
-                                   __half2float(ly.b2[col + 2]), __half2float(ly.b2[col + 3]));
-            if (ps < PS) {
+            // this CTA's ngm 4-column groups: one warp per group, lanes over the
+            // G partials (q = lane, lane+32, ...), then a fixed xor-tree
+            float ss_local = 0.f;
+            for (int gi = warp; gi < ngm; gi += kWarps) {
+                const int col = (g0 + gi) * 4;
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                constexpr int NB = 4;
-                for (int q0 = ps; q0 < G; q0 += NB * PS) {
+                constexpr int NB = 8;
+                for (int q0 = lane; q0 < G; q0 += NB * 32) {
                     float4 v[NB];
 #pragma unroll
                     for (int b = 0; b < NB; ++b) {
-                        const int q = q0 + b * PS;
+                        const int q = q0 + b * 32;
                         if (q < G) v[b] = ld_cg4(p.xyp + (size_t)q * d + col);
                     }
 #pragma unroll
                     for (int b = 0; b < NB; ++b) {
-                        const int q = q0 + b * PS;
+                        const int q = q0 + b * 32;
                         if (q < G) {
                             acc.x += v[b].x;
                             acc.y += v[b].y;
@@ -658,34 +875,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                         }
                     }
                 }
-                red4[tid] = acc;
-            }
-            __syncthreads();
-            for (int s = PS / 2; s >= 1; s >>= 1) {
-                if (ps < s) {
-                    const float4 o = red4[tid + s * ngm];
-                    float4 a = red4[tid];
-                    a.x += o.x;
-                    a.y += o.y;
-                    a.z += o.z;
-                    a.w += o.w;
-                    red4[tid] = a;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    acc.x += __shfl_xor_sync(FULL, acc.x, o);
+                    acc.y += __shfl_xor_sync(FULL, acc.y, o);
+                    acc.z += __shfl_xor_sync(FULL, acc.z, o);
+                    acc.w += __shfl_xor_sync(FULL, acc.w, o);
                 }
-                __syncthreads();
-            }
-            float ss_local = 0.f;
-            if (ps == 0 && ngm > 0) {
-                const float4 a = red4[tid];
-                const float4 yv = make_float4(a.x + bias.x, a.y + bias.y, a.z + bias.z, a.w + bias.w);
-                __stcg(reinterpret_cast<float4*>(p.xy + col), yv);
-                if (l == p.L - 1) *reinterpret_cast<float4*>(p.y_out + col) = yv;
-                ss_local = yv.x * yv.x + yv.y * yv.y + yv.z * yv.z + yv.w * yv.w;
+                if (lane == 0) {
+                    const float4 yv = make_float4(acc.x + __half2float(ly.b2[col]), acc.y + __half2float(ly.b2[col + 1]),
+                                                  acc.z + __half2float(ly.b2[col + 2]), acc.w + __half2float(ly.b2[col + 3]));
+                    __stcg(reinterpret_cast<float4*>(p.xy + col), yv);
+                    if (l == p.L - 1) *reinterpret_cast<float4*>(p.y_out + col) = yv;
+                    ss_local += yv.x * yv.x + yv.y * yv.y + yv.z * yv.z + yv.w * yv.w;
+                }
             }
             if (l + 1 < p.L) {
                 // fixed-order sum of squares of this CTA's columns
-                const float s = warp_sum(ss_local);
-                __syncthreads();
-                if (lane == 0) red[warp] = s;
+                if (lane == 0) red[warp] = ss_local;
                 __syncthreads();
                 if (tid == 0) {
                     float t = 0.f;
@@ -825,7 +1032,41 @@ cudaError_t launch_fused(const FusedStackArgs& a, cudaStream_t s) {
         if ((size_t)f.su * f.r > a.rmax_su) return cudaErrorInvalidValue;
         rmax = f.r > rmax ? f.r : rmax;
     }
-    const SmemPlan sp = smem_plan(a.d, a.F, rmax, a.rmax_su, G);
+    SmemPlan sp = smem_plan(a.d, a.F, rmax, a.rmax_su, G);
+    // shared predictor slices when they fit: P1 items, P2 units and bias of one CTA
+    {
+        size_t p1b = 16;
+        for (int l = 0; l < a.L; ++l) {
+            const FusedLayer& f = prm.layers[l];
+            const size_t items = (size_t)f.r * f.su;
+            p1b = std::max(p1b, ((items + G - 1) / G) * (size_t)f.seg * 2);
+        }
+        const size_t units = ((size_t)prm.M + G - 1) / G;
+        const size_t p2b = units * 16 * (size_t)rmax * 2, b1b = units * 16 * 2;
+        auto r16 = [](size_t v) { return (int)((v + 15) / 16 * 16); };
+        SmemPlan with = sp;
+        with.p1s = r16(p1b);
+        with.p2s = r16(p2b);
+        with.b1s = r16(b1b);
+        if ((size_t)with.bytes() <= 227 * 1024) {
+            sp = with;
+            prm.pred_smem = 1;
+            prm.p1s_bytes = with.p1s;
+            prm.p2s_bytes = with.p2s;
+            prm.b1s_bytes = with.b1s;
+        }
+    }
+    // the rest of shared memory stages W2t rows when a CTA has few of them
+    {
+        const size_t w2row = a.int4 ? (size_t)a.d / 2 + a.d / 16 : (size_t)2 * a.d;
+        const bool tma_ok = !a.int4 || (a.d % 256 == 0);     // 16-byte multiples for the scales
+        // leave room for the kernel's static shared variables
+        const long long room = 227ll * 1024 - 1024 - sp.bytes();
+        if (tma_ok && room >= (long long)(2 * w2row)) {
+            sp.w2s = (int)(room / 16 * 16);
+            prm.w2s_bytes = sp.w2s;
+        }
+    }
     const size_t smem = sp.bytes();
     if (smem > 227 * 1024) return cudaErrorInvalidValue;
     if (a.int4) return launch_kind<2, 1>(prm, G, smem, s);
