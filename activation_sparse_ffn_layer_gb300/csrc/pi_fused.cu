@@ -167,7 +167,7 @@ struct FusedParams {
     int32_t* layer_counts;      // nullable [L][2]: predicted-active, non-zero FC1 output
     int pred_smem;              // 1: each CTA's predictor slice is bulk-copied to shared memory
     int p1s_bytes, p2s_bytes, b1s_bytes;  // capacities of the shared predictor buffers
-    int w2s_bytes;              // staging buffer for this CTA's W2t rows (0: FC2 reads HBM directly)
+    int stage_bytes;            // shared staging region (predictor slices, then this CTA's FC rows)
     FusedLayer layers[kMaxFusedLayers];
 };
 
@@ -177,7 +177,8 @@ struct FusedParams {
 struct SmemPlan {
     int d, rmax, usmax, M, cap;
     int p1s = 0, p2s = 0, b1s = 0;  // shared predictor buffers (bytes, 16-aligned), 0 if unused
-    int w2s = 0;                    // W2t row staging buffer (bytes, 16-aligned), 0 if unused
+    int stage = 0;                  // staging region (bytes, 16-aligned): the predictor buffers
+                                    // in phases A-B, this CTA's FC rows in phase C
     __host__ __device__ int off_u() const { return d * 4; }
     __host__ __device__ int off_ust() const { return off_u() + rmax * 4; }
     __host__ __device__ int off_m16() const { return off_ust() + ((usmax + 3) / 4) * 16; }
@@ -185,11 +186,11 @@ struct SmemPlan {
     __host__ __device__ int off_lidx() const { return off_upre() + (M + 1) * 4; }
     __host__ __device__ int off_lh() const { return off_lidx() + cap * 4; }
     __host__ __device__ int off_scr() const { return ((off_lh() + cap * 4 + 15) / 16) * 16; }
-    __host__ __device__ int off_p1s() const { return off_scr() + 4096 * 4; }
+    __host__ __device__ int off_stage() const { return off_scr() + 4096 * 4; }
+    __host__ __device__ int off_p1s() const { return off_stage(); }
     __host__ __device__ int off_p2s() const { return off_p1s() + p1s; }
     __host__ __device__ int off_b1s() const { return off_p2s() + p2s; }
-    __host__ __device__ int off_w2s() const { return off_b1s() + b1s; }
-    __host__ __device__ int bytes() const { return off_w2s() + w2s; }
+    __host__ __device__ int bytes() const { return off_stage() + stage; }
 };
 
 // dot of 8 fp16 weights with 8 fp32 values in smem
@@ -274,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
     sp.p1s = p.pred_smem ? p.p1s_bytes : 0;
     sp.p2s = p.pred_smem ? p.p2s_bytes : 0;
     sp.b1s = p.pred_smem ? p.b1s_bytes : 0;
-    sp.w2s = p.w2s_bytes;
+    sp.stage = p.stage_bytes;
     float* xf = reinterpret_cast<float*>(smem);
     float* us = reinterpret_cast<float*>(smem + sp.off_u());
     float* ust = reinterpret_cast<float*>(smem + sp.off_ust());
@@ -287,20 +288,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
     __half* p1s = reinterpret_cast<__half*>(smem + sp.off_p1s());
     __half* p2s = reinterpret_cast<__half*>(smem + sp.off_p2s());
     __half* b1s = reinterpret_cast<__half*>(smem + sp.off_b1s());
-    unsigned char* w2s = smem + sp.off_w2s();
-    // bytes of one staged W2t row: fp16 row, or INT4 codes followed by the scales
-    const int w2row = KIND == 2 ? d / 2 + d / 16 : 2 * d;
+    unsigned char* stage = smem + sp.off_stage();
+    // bytes of one staged weight row: fp16 row, or INT4 codes followed by the scales
+    const int wrow = KIND == 2 ? d / 2 + d / 16 : 2 * d;
+    const int fc1_rows = KIND == 1 ? 2 : 1;   // gate and up rows when gated
     __shared__ int bad;
     __shared__ float rs_s;
     __shared__ __align__(8) unsigned long long pred_mbar;
-    __shared__ __align__(8) unsigned long long w2_mbar;
+    __shared__ __align__(8) unsigned long long w1_mbar;   // staged FC1 rows
+    __shared__ __align__(8) unsigned long long w2_mbar;   // staged W2t rows
     if (tid == 0) {
         bad = 0;
         mbar_init(&pred_mbar, 1);
+        mbar_init(&w1_mbar, 1);
         mbar_init(&w2_mbar, 1);
     }
-    unsigned w2_uses = 0;   // completed-or-pending phases of w2_mbar
-    bool w2_pending = false;
+    unsigned w2_uses = 0;   // completed-or-pending phases of w1_mbar and w2_mbar (used in pairs)
+    bool w1_pending = false, w2_pending = false;
 
     // barrier targets: the counter holds G arrivals per barrier ever completed
     const unsigned long long ebase = __ldcg(p.epoch);
@@ -315,6 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
     int inflight = -1;   // layer whose predictor copy is issued but not yet waited for
     auto leave = [&]() {
         if (inflight >= 0) mbar_drain(&pred_mbar, (unsigned)(inflight & 1), tmo);
+        if (w1_pending) mbar_drain(&w1_mbar, (w2_uses - 1) & 1u, tmo);
         if (w2_pending) mbar_drain(&w2_mbar, (w2_uses - 1) & 1u, tmo);
         if (c == 0 && tid == 0) {
             const unsigned long long next = ebase + (unsigned long long)kBarriersPerLayer * p.L;
@@ -372,6 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
         // barrier): bring in layer l+1's once this CTA's FC rows are loaded
         auto issue_next = [&]() {
             if (p.pred_smem && l + 1 < p.L) {
+                __syncthreads();   // the region may still hold this CTA's staged FC rows
                 if (tid == 0) issue_predictor(l + 1);
                 inflight = l + 1;
             }
@@ -471,26 +477,33 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                 for (int k = 0; k < 16; ++k) v[k] = 0.f;
                 for (int e = 0; e < vpl; ++e) {
                     const int vi = lane + 32 * e;
-                    if (vi < nvec) {
-                        float uf[8];
-                        {
-                            const float4 a = reinterpret_cast<const float4*>(us + vi * 8)[0];
-                            const float4 b = reinterpret_cast<const float4*>(us + vi * 8)[1];
-                            uf[0] = a.x; uf[1] = a.y; uf[2] = a.z; uf[3] = a.w;
-                            uf[4] = b.x; uf[5] = b.y; uf[6] = b.z; uf[7] = b.w;
+                    const bool vok = vi < nvec;
+                    const int vc = vok ? vi : nvec - 1;   // clamped: loads stay in bounds, result masked
+                    float uf[8];
+                    {
+                        const float4 a = reinterpret_cast<const float4*>(us + vc * 8)[0];
+                        const float4 b = reinterpret_cast<const float4*>(us + vc * 8)[1];
+                        const float z = vok ? 1.f : 0.f;
+                        uf[0] = a.x * z; uf[1] = a.y * z; uf[2] = a.z * z; uf[3] = a.w * z;
+                        uf[4] = b.x * z; uf[5] = b.y * z; uf[6] = b.z * z; uf[7] = b.w * z;
+                    }
+                    // 8 rows' vectors are requested before any arithmetic on them
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint4 w[8];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const int row = min(rbase + 8 * h + k, F - 1);
+                            w[k] = p.pred_smem
+                                       ? *reinterpret_cast<const uint4*>(p2s + (size_t)(row - row0) * r + vc * 8)
+                                       : ld_stream16(ly.p2 + (size_t)row * r + vc * 8);
                         }
 #pragma unroll
-                        for (int k = 0; k < 16; ++k) {
-                            const int row = rbase + k;
-                            if (row < F) {
-                                const uint4 w = p.pred_smem
-                                    ? *reinterpret_cast<const uint4*>(p2s + (size_t)(row - row0) * r + vi * 8)
-                                    : ld_stream16(ly.p2 + (size_t)row * r + vi * 8);
-                                float wf[8];
-                                h8_to_f8(w, wf);
+                        for (int k = 0; k < 8; ++k) {
+                            float wf[8];
+                            h8_to_f8(w[k], wf);
 #pragma unroll
-                                for (int t = 0; t < 8; ++t) v[k] = fmaf(wf[t], uf[t], v[k]);
-                            }
+                            for (int t = 0; t < 8; ++t) v[8 * h + k] = fmaf(wf[t], uf[t], v[8 * h + k]);
                         }
                     }
                 }
@@ -601,28 +614,39 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
         }
         if (l == p.L - 1 && c == 0 && tid == 0) *p.count_out = n_total;
         __syncthreads();
-        // few rows per CTA: stage all of this CTA's W2t rows in shared memory now,
-        // so their HBM latency overlaps FC1 (rows whose FC1 output turns out to
-        // be zero are loaded but not used)
-        const bool w2_staged = nmine > 0 && nmine * w2row <= p.w2s_bytes;
-        if (w2_staged) {
+        // few rows per CTA: stage all of this CTA's FC1 rows, then its W2t rows, in
+        // shared memory now with bulk copies (FC1 rows first, so they arrive
+        // first); W2t rows of neurons whose FC1 output turns out to be zero are
+        // loaded but not used.  The region held this layer's predictor slices,
+        // consumed before the last grid barrier.
+        const bool rows_staged = nmine > 0 && nmine * (fc1_rows + 1) * wrow <= p.stage_bytes;
+        unsigned char* s_w1 = stage;                                  // [nmine] W1 (gate) rows
+        unsigned char* s_wu = stage + (size_t)nmine * wrow;           // [nmine] up rows (gated)
+        unsigned char* s_w2 = stage + (size_t)nmine * fc1_rows * wrow;  // [nmine] W2t rows
+        if (rows_staged) {
             if (tid == 0) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                mbar_arrive_expect_tx(&w2_mbar, (unsigned)(nmine * w2row));
-                for (int q = 0; q < nmine; ++q) {
-                    const size_t k = (size_t)lidx[q];
+                mbar_arrive_expect_tx(&w1_mbar, (unsigned)(nmine * fc1_rows * wrow));
+                mbar_arrive_expect_tx(&w2_mbar, (unsigned)(nmine * wrow));
+                auto stage_row = [&](unsigned char* dst, const void* codes, const __half* scales, size_t k,
+                                     unsigned long long* mb) {
                     if (KIND != 2) {
-                        bulk_g2s(w2s + (size_t)q * w2row, static_cast<const __half*>(ly.w2t) + k * d, 2u * d, &w2_mbar);
+                        bulk_g2s(dst, static_cast<const __half*>(codes) + k * d, 2u * d, mb);
                     } else {
-                        bulk_g2s(w2s + (size_t)q * w2row, static_cast<const uint8_t*>(ly.w2t) + k * (d / 2),
-                                 (unsigned)(d / 2), &w2_mbar);
-                        bulk_g2s(w2s + (size_t)q * w2row + d / 2, ly.w2ts + k * (d / 32), (unsigned)(d / 16),
-                                 &w2_mbar);
+                        bulk_g2s(dst, static_cast<const uint8_t*>(codes) + k * (d / 2), (unsigned)(d / 2), mb);
+                        bulk_g2s(dst + d / 2, scales + k * (d / 32), (unsigned)(d / 16), mb);
                     }
-                }
+                };
+                for (int q = 0; q < nmine; ++q)
+                    stage_row(s_w1 + (size_t)q * wrow, ly.w1, ly.w1s, (size_t)lidx[q], &w1_mbar);
+                if (KIND == 1)
+                    for (int q = 0; q < nmine; ++q)
+                        stage_row(s_wu + (size_t)q * wrow, ly.wu, nullptr, (size_t)lidx[q], &w1_mbar);
+                for (int q = 0; q < nmine; ++q)
+                    stage_row(s_w2 + (size_t)q * wrow, ly.w2t, ly.w2ts, (size_t)lidx[q], &w2_mbar);
             }
             ++w2_uses;
-            w2_pending = true;
+            w1_pending = w2_pending = true;
         }
 
         // FC1: (neuron, segment) items spread over all warps so that every warp
@@ -638,26 +662,40 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
             nseg = KIND == 2 ? (ng + segE - 1) / segE : (d + segE - 1) / segE;
             float* part = red;           // [nmine * nseg]
             float* partu = red + 2048;   // gated: up-projection partials
+            if (rows_staged && mbar_wait(&w1_mbar, (w2_uses - 1) & 1u, tmo, &bad)) w1_pending = false;
             for (int it = warp; it < nmine * nseg; it += kWarps) {
                 const int q = it / nseg, sg = it % nseg;
                 const int k = lidx[q];
                 float acc = 0.f, accu = 0.f;
                 if (KIND != 2) {
                     const int e0 = sg * segE, e1 = min(d, e0 + segE);
-                    const __half* row = static_cast<const __half*>(ly.w1) + (size_t)k * d;
-                    const __half* rowu = KIND == 1 ? ly.wu + (size_t)k * d : nullptr;
+                    if (rows_staged) {
+                        const __half* row = reinterpret_cast<const __half*>(s_w1 + (size_t)q * wrow);
+                        const __half* rowu = reinterpret_cast<const __half*>(s_wu + (size_t)q * wrow);
+#pragma unroll 4
+                        for (int e = e0 + lane * 8; e < e1; e += 256) {
+                            acc += dot8(*reinterpret_cast<const uint4*>(row + e), xf + e);
+                            if (KIND == 1) accu += dot8(*reinterpret_cast<const uint4*>(rowu + e), xf + e);
+                        }
+                    } else {
+                        const __half* row = static_cast<const __half*>(ly.w1) + (size_t)k * d;
+                        const __half* rowu = KIND == 1 ? ly.wu + (size_t)k * d : nullptr;
 #pragma unroll 8
-                    for (int e = e0 + lane * 8; e < e1; e += 256) {
-                        acc += dot8(ld_stream16(row + e), xf + e);
-                        if (KIND == 1) accu += dot8(ld_stream16(rowu + e), xf + e);
+                        for (int e = e0 + lane * 8; e < e1; e += 256) {
+                            acc += dot8(ld_stream16(row + e), xf + e);
+                            if (KIND == 1) accu += dot8(ld_stream16(rowu + e), xf + e);
+                        }
                     }
                 } else {
                     const int gs0 = sg * segE, gs1 = min(ng, gs0 + segE);
-                    const uint8_t* row = static_cast<const uint8_t*>(ly.w1) + (size_t)k * (d / 2);
-                    const __half* sc = ly.w1s + (size_t)k * ng;
+                    const uint8_t* row = rows_staged ? s_w1 + (size_t)q * wrow
+                                                     : static_cast<const uint8_t*>(ly.w1) + (size_t)k * (d / 2);
+                    const __half* sc = rows_staged ? reinterpret_cast<const __half*>(s_w1 + (size_t)q * wrow + d / 2)
+                                                   : ly.w1s + (size_t)k * ng;
 #pragma unroll 4
                     for (int g = gs0 + lane; g < gs1; g += 32) {
-                        const uint4 qv = ld_stream16(row + (size_t)g * 16);
+                        const uint4 qv = rows_staged ? *reinterpret_cast<const uint4*>(row + (size_t)g * 16)
+                                                     : ld_stream16(row + (size_t)g * 16);
                         const float s = __half2float(sc[g]);
                         const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
                         float pt = 0.f;
@@ -712,10 +750,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
 
         // FC2: the whole CTA accumulates its neurons' W2t rows; rows whose
         // FC1 output is zero are skipped (ReLU removed them from FC2)
-        if (w2_staged) {
-            if (mbar_wait(&w2_mbar, (w2_uses - 1) & 1u, tmo, &bad)) w2_pending = false;
-        }
-        if (KIND != 2 && w2_staged) {
+        if (rows_staged && mbar_wait(&w2_mbar, (w2_uses - 1) & 1u, tmo, &bad)) w2_pending = false;
+        if (KIND != 2 && rows_staged) {
             float acc[NCH][8];
 #pragma unroll
             for (int ch = 0; ch < NCH; ++ch)
@@ -724,7 +760,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
             for (int q = 0; q < nmine; ++q) {
                 const float hq = lh[q];
                 if (hq == 0.f) continue;
-                const __half* row = reinterpret_cast<const __half*>(w2s + (size_t)q * w2row);
+                const __half* row = reinterpret_cast<const __half*>(s_w2 + (size_t)q * wrow);
 #pragma unroll
                 for (int ch = 0; ch < NCH; ++ch) {
                     const int col = ch * 4096 + tid * 8;
@@ -812,8 +848,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                     const float hv = q < nmine ? lh[q] : 0.f;
                     hs[b] = 0.f;
                     if (hv != 0.f && mine) {
-                        if (w2_staged) {
-                            const unsigned char* row = w2s + (size_t)q * w2row;
+                        if (rows_staged) {
+                            const unsigned char* row = s_w2 + (size_t)q * wrow;
                             wv[b] = *reinterpret_cast<const uint4*>(row + col / 2);
                             hs[b] = hv * __half2float(reinterpret_cast<const __half*>(row + d / 2)[col / 32]);
                         } else {
@@ -1048,7 +1084,7 @@ cudaError_t launch_fused(const FusedStackArgs& a, cudaStream_t s) {
         with.p1s = r16(p1b);
         with.p2s = r16(p2b);
         with.b1s = r16(b1b);
-        if ((size_t)with.bytes() <= 227 * 1024) {
+        if ((size_t)with.off_stage() + with.p1s + with.p2s + with.b1s <= 227 * 1024 - 1024) {
             sp = with;
             prm.pred_smem = 1;
             prm.p1s_bytes = with.p1s;
@@ -1056,16 +1092,15 @@ cudaError_t launch_fused(const FusedStackArgs& a, cudaStream_t s) {
             prm.b1s_bytes = with.b1s;
         }
     }
-    // the rest of shared memory stages W2t rows when a CTA has few of them
+    // the staging region takes the rest of shared memory (leaving room for the
+    // kernel's static shared variables); it must at least hold the predictor slices
     {
-        const size_t w2row = a.int4 ? (size_t)a.d / 2 + a.d / 16 : (size_t)2 * a.d;
-        const bool tma_ok = !a.int4 || (a.d % 256 == 0);     // 16-byte multiples for the scales
-        // leave room for the kernel's static shared variables
-        const long long room = 227ll * 1024 - 1024 - sp.bytes();
-        if (tma_ok && room >= (long long)(2 * w2row)) {
-            sp.w2s = (int)(room / 16 * 16);
-            prm.w2s_bytes = sp.w2s;
-        }
+        const bool tma_ok = !a.int4 || (a.d % 256 == 0);     // 16-byte multiples for INT4 scales
+        const int pred = sp.p1s + sp.p2s + sp.b1s;
+        const long long room = 227ll * 1024 - 1024 - sp.off_stage();
+        const int st = tma_ok ? (int)(room / 16 * 16) : pred;
+        sp.stage = st > pred ? st : pred;
+        prm.stage_bytes = tma_ok ? sp.stage : 0;
     }
     const size_t smem = sp.bytes();
     if (smem > 227 * 1024) return cudaErrorInvalidValue;
