@@ -70,14 +70,17 @@ bool make_plan(const pi_layer_desc& desc, Plan* p) {
     q.rmax_su = (size_t)16 * q.nsm + 2 * (size_t)q.r;
     q.xchg_bytes = up(fused_workspace_bytes(q.d, q.F, q.rmax_su, q.nsm));
     q.fused = q.B == 1 && fused_supported(q.d, q.F, q.r, q.int4, q.nsm);
+    q.tc = tc_supported(q);
+    q.part_floats = q.tc ? tc_part_floats(q) : (size_t)q.fc2_splits * q.B * q.d;
     size_t off = q.xchg_bytes;
     q.off_mask = off;  off = up(off + sizeof(uint32_t) * (size_t)q.B * q.W);
     q.off_idx = off;   off = up(off + sizeof(int32_t) * (size_t)q.F);
     q.off_count = off; off = up(off + sizeof(int32_t) * 4);
     q.off_h = off;     off = up(off + sizeof(float) * (size_t)q.F * q.B);
     q.off_upart = off; off = up(off + sizeof(float) * (size_t)q.u_splits * q.B * q.r);
-    q.off_part = off;  off = up(off + sizeof(float) * (size_t)q.fc2_splits * q.B * q.d);
+    q.off_part = off;  off = up(off + sizeof(float) * q.part_floats);
     q.off_xbuf = off;  off = up(off + sizeof(uint16_t) * 2 * (size_t)q.B * q.d);
+    q.off_live = off;  off = up(off + (size_t)q.F);
     q.total = off;
     *p = q;
     return true;
@@ -183,9 +186,10 @@ cudaError_t run_stack(const Plan& p, int n, const LayerPtrs* lp, const int* rank
         const LayerPtrs& w = lp[l];
         cudaError_t e = launch_predict(q, cur, w.p1, w.p2, w.b1, tau, mask, at<float>(ws, p.off_upart), s);
         if (e == cudaSuccess) e = launch_compact(q, mask, nullptr, idx, nullptr, cnt, s);
-        if (e == cudaSuccess) e = launch_fc1(q, cur, w, idx, cnt, q.B > 1 ? mask : nullptr, h, s);
+        uint8_t* live = at<uint8_t>(ws, p.off_live);
+        if (e == cudaSuccess) e = launch_fc1(q, cur, w, idx, cnt, q.B > 1 ? mask : nullptr, h, live, s);
         if (e == cudaSuccess && layer_counts) e = launch_count_active(q, cnt, h, layer_counts + 2 * l, s);
-        if (e == cudaSuccess) e = launch_fc2(q, h, idx, cnt, w, at<float>(ws, p.off_part), y, s);
+        if (e == cudaSuccess) e = launch_fc2(q, h, idx, cnt, w, q.tc ? live : nullptr, at<float>(ws, p.off_part), y, s);
         if (e != cudaSuccess) return e;
         if (l + 1 < n) {
             __half* nxt = x_trace ? x_trace + (size_t)l * p.B * p.d : xbuf + (size_t)(l % 2) * p.B * p.d;
@@ -250,7 +254,7 @@ pi_status pi_sparse_fc1(const pi_layer_desc* desc, const pi_half* x, const pi_la
     if (!x || !aligned16(x) || !idx || !d_count || !h || !weights_ok(p, w, true, false, false))
         return PI_ERR_INVALID_ARG;
     if ((size_t)8 * p.d * sizeof(uint16_t) > 200 * 1024) return PI_ERR_UNSUPPORTED;
-    return from_cuda(launch_fc1(p, reinterpret_cast<const __half*>(x), ptrs(w), idx, d_count, mask, h,
+    return from_cuda(launch_fc1(p, reinterpret_cast<const __half*>(x), ptrs(w), idx, d_count, mask, h, nullptr,
                                 static_cast<cudaStream_t>(stream)));
 }
 
@@ -261,7 +265,7 @@ pi_status pi_sparse_fc2(const pi_layer_desc* desc, const float* h, const int32_t
     if (!h || !idx || !d_count || !y || !aligned16(y) || !weights_ok(p, w, false, true, false))
         return PI_ERR_INVALID_ARG;
     if (!workspace || !aligned16(workspace) || ws_bytes < p.total) return PI_ERR_WORKSPACE;
-    return from_cuda(launch_fc2(p, h, idx, d_count, ptrs(w), at<float>(workspace, p.off_part), y,
+    return from_cuda(launch_fc2(p, h, idx, d_count, ptrs(w), nullptr, at<float>(workspace, p.off_part), y,
                                 static_cast<cudaStream_t>(stream)));
 }
 
@@ -314,7 +318,9 @@ int pi_launches_per_layer(const pi_layer_desc* desc) {
         ++chunks;
     }
     if (p.fused) return 1;  // one persistent kernel
-    // predictor: 2 per token chunk; compaction: 1; FC1: 1 per chunk; FC2: 1 per chunk + 1 reduction
+    // predictor: 2 per token chunk; compaction: 1; then FC1 + FC2 + the FC2
+    // reduction (tcgen05 path: all tokens at once) or FC1 and FC2 per chunk + 1
+    if (p.tc) return 2 * chunks + 1 + 1 + 2;
     return 2 * chunks + 1 + chunks + chunks + 1;
 }
 

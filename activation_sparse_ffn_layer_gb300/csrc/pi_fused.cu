@@ -1121,6 +1121,18 @@ cudaError_t launch_wait_nothing(long long timeout_ns, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+int* status_word() {
+    static int* cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (cache[dev] == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_pi_status) != cudaSuccess) return nullptr;
+        cache[dev] = static_cast<int*>(ptr);
+    }
+    return cache[dev];
+}
+
 cudaError_t read_and_clear_status(int* out, cudaStream_t s) {
     int v = 0;
     cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_pi_status, sizeof(int), 0, cudaMemcpyDeviceToHost, s);

@@ -25,7 +25,9 @@ struct Plan {
     // workspace offsets (bytes, 256-aligned); the fused exchange region comes first
     size_t xchg_bytes, rmax_su;
     bool fused;     // pi_ffn_layer / pi_ffn_stack take the fused persistent kernel
-    size_t off_mask, off_idx, off_count, off_h, off_upart, off_part, off_xbuf, total;
+    bool tc;        // FC1 / FC2 take the tcgen05 batched path (batch 16..32, fp16 weights)
+    size_t part_floats;  // FC2 partial sums of whichever FC2 path the plan takes
+    size_t off_mask, off_idx, off_count, off_h, off_upart, off_part, off_xbuf, off_live, total;
 };
 
 bool make_plan(const pi_layer_desc& desc, Plan* p);
@@ -48,13 +50,25 @@ cudaError_t launch_predict(const Plan& p, const __half* x, const __half* p1, con
                            cudaStream_t s);
 cudaError_t launch_compact(const Plan& p, const uint32_t* mask, const int32_t* table, int32_t* idx,
                            int32_t* orig, int32_t* count, cudaStream_t s);
+// live (nullable): FC1 marks listed rows whose h is non-zero for some token
+// (tcgen05 path only); FC2 may then skip the other rows' W2t reads.
 cudaError_t launch_fc1(const Plan& p, const __half* x, const LayerPtrs& w, const int32_t* idx,
-                       const int32_t* count, const uint32_t* mask, float* h, cudaStream_t s);
+                       const int32_t* count, const uint32_t* mask, float* h, uint8_t* live, cudaStream_t s);
 cudaError_t launch_fc2(const Plan& p, const float* h, const int32_t* idx, const int32_t* count,
-                       const LayerPtrs& w, float* partial, float* y, cudaStream_t s);
+                       const LayerPtrs& w, const uint8_t* live, float* partial, float* y, cudaStream_t s);
 cudaError_t launch_rmsnorm(int d, int B, const float* y, float eps, __half* x, cudaStream_t s);
 // out[0] = *count, out[1] = listed neurons whose h is non-zero for some token
 cudaError_t launch_count_active(const Plan& p, const int32_t* count, const float* h, int32_t* out, cudaStream_t s);
+
+// ---- tcgen05 batched path (pi_tc.cu) ----
+bool tc_supported(const Plan& p);
+int tc_tokens(const Plan& p);       // N of the MMAs: batch rounded up to 16 or 32
+int tc_slots(const Plan& p);        // partial tiles per CTA of the FC2 split
+size_t tc_part_floats(const Plan& p);
+cudaError_t launch_fc1_tc(const Plan& p, const __half* x, const LayerPtrs& w, const int32_t* idx,
+                          const int32_t* count, const uint32_t* mask, float* h, uint8_t* live, cudaStream_t s);
+cudaError_t launch_fc2_tc(const Plan& p, const float* h, const int32_t* idx, const int32_t* count,
+                          const LayerPtrs& w, const uint8_t* live, float* partial, float* y, cudaStream_t s);
 
 // ---- fused persistent stack (batch 1) ----
 struct FusedStackArgs {
@@ -80,6 +94,8 @@ bool fused_supported(int d, int F, int rmax, bool int4, int G);
 cudaError_t launch_fused(const FusedStackArgs& a, cudaStream_t s);
 cudaError_t launch_wait_nothing(long long timeout_ns, cudaStream_t s);
 cudaError_t read_and_clear_status(int* out, cudaStream_t s);
+// Device address of the status word that bounded waits set on expiry (current device).
+int* status_word();
 
 // Argument checks of pi_sparse_fc2 (without its workspace) and the weight
 // pointer bundle, shared with the allocation-free FC2 entry point.

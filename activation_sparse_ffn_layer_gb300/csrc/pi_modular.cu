@@ -481,7 +481,8 @@ cudaError_t launch_compact(const Plan& p, const uint32_t* mask, const int32_t* t
 }
 
 cudaError_t launch_fc1(const Plan& p, const __half* x, const LayerPtrs& w, const int32_t* idx,
-                       const int32_t* count, const uint32_t* mask, float* h, cudaStream_t s) {
+                       const int32_t* count, const uint32_t* mask, float* h, uint8_t* live, cudaStream_t s) {
+    if (p.tc) return launch_fc1_tc(p, x, w, idx, count, mask, h, live, s);
     const int kind = p.int4 ? 2 : (p.gated ? 1 : 0);
     return for_token_chunks(p.B, [&](int b0, int tb) -> cudaError_t {
         const size_t sm = (size_t)tb * p.d * sizeof(__half);
@@ -504,7 +505,8 @@ cudaError_t launch_fc1(const Plan& p, const __half* x, const LayerPtrs& w, const
 }
 
 cudaError_t launch_fc2(const Plan& p, const float* h, const int32_t* idx, const int32_t* count,
-                       const LayerPtrs& w, float* partial, float* y, cudaStream_t s) {
+                       const LayerPtrs& w, const uint8_t* live, float* partial, float* y, cudaStream_t s) {
+    if (p.tc) return launch_fc2_tc(p, h, idx, count, w, live, partial, y, s);
     cudaError_t e = for_token_chunks(p.B, [&](int b0, int tb) -> cudaError_t {
         dim3 grid(p.fc2_tiles, p.fc2_splits);
 #define PI_FC2(TBV, IV)                                                                       \

@@ -22,7 +22,7 @@
 namespace pi {
 namespace {
 
-// 8 MiB of fp32 partial sums: splits x batch x d must fit.
+// 8 MiB of fp32 partial sums: the plan's FC2 partials must fit.
 constexpr size_t kNoallocScratchFloats = (size_t(8) << 20) / sizeof(float);
 
 static __device__ __align__(256) float g_fc2_scratch[kNoallocScratchFloats];
@@ -61,10 +61,10 @@ extern "C" pi_status pi_sparse_fc2_noalloc(const pi_layer_desc* desc, const floa
     if (!fc2_args_ok(p, h, idx, d_count, w, y)) return PI_ERR_INVALID_ARG;
     // every partial-sum slot the reduction reads is written by the same call
     // first, so nothing in the array has to start at zero
-    const size_t need = (size_t)p.fc2_splits * p.B * p.d;
-    if (need > kNoallocScratchFloats) return PI_ERR_WORKSPACE;
+    if (p.part_floats > kNoallocScratchFloats) return PI_ERR_WORKSPACE;
     float* scratch = nullptr;
     if (scratch_address(&scratch) != cudaSuccess) return PI_ERR_CUDA;
-    const cudaError_t e = launch_fc2(p, h, idx, d_count, layer_ptrs(w), scratch, y, static_cast<cudaStream_t>(stream));
+    const cudaError_t e =
+        launch_fc2(p, h, idx, d_count, layer_ptrs(w), nullptr, scratch, y, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PI_OK : PI_ERR_CUDA;
 }

@@ -127,6 +127,9 @@ PI_API pi_status pi_compact(const pi_layer_desc *desc, const uint32_t *mask, con
  *   h[j*B + b] = ReLU(W1[idx_j] . x_b + b1[idx_j])  (gated: times Wu[idx_j] . x_b)
  * for j < *d_count; when B > 1 and mask != NULL, h[j*B+b] = 0 wherever token
  * b's own mask bit idx_j is 0.  h: [F*B] fp32 (neuron-major).
+ * For 16 <= B <= 32, fp16 weights and d % 128 == 0 the rows are gathered once
+ * for all B tokens and multiplied on the tcgen05 tensor cores (fp16 x fp16
+ * products, fp32 accumulation); otherwise CUDA cores in chunks of <= 8 tokens.
  */
 PI_API pi_status pi_sparse_fc1(const pi_layer_desc *desc, const pi_half *x, const pi_layer_weights *w,
                         const int32_t *idx, const int32_t *d_count, const uint32_t *mask,
@@ -137,6 +140,9 @@ PI_API pi_status pi_sparse_fc1(const pi_layer_desc *desc, const pi_half *x, cons
  * "Neuron-aware operator": only the columns of active neurons, stored as rows).
  *   y[b*d + c] = b2[c] + sum_{j < *d_count} h[j*B + b] * W2t[idx_j, c]   (fp32)
  * Reduced without atomics in a fixed order (bitwise reproducible).
+ * Under the same conditions as pi_sparse_fc1 the tensor cores take it, with h
+ * split into fp16 hi = fp16(h) and lo = fp16(h - hi) so that fp32 accuracy is
+ * kept.
  */
 PI_API pi_status pi_sparse_fc2(const pi_layer_desc *desc, const float *h, const int32_t *idx,
                         const int32_t *d_count, const pi_layer_weights *w, float *y,
@@ -151,8 +157,10 @@ PI_API pi_status pi_sparse_fc2(const pi_layer_desc *desc, const float *h, const 
  * workspace pi_sparse_fc2 needs.  Same arguments and result as pi_sparse_fc2
  * without the workspace; the FC2 partial sums live in an 8 MiB array inside
  * the library that every GPU loading the library holds until process exit.
- *  - Returns PI_ERR_WORKSPACE when the partial sums of `desc` (splits x batch x
- *    d floats) exceed that array; allocates nothing in any case.
+ *  - Returns PI_ERR_WORKSPACE when the partial sums of `desc` exceed that
+ *    array (splits x batch x d floats on the CUDA-core path; SMs x tiles per
+ *    SM x 16 or 32 x 128 floats on the batch 16..32 tensor-core path);
+ *    allocates nothing in any case.
  *  - The first call on a device looks up the array's device address (once per
  *    device, with that device current); make that first call before any
  *    stream capture.

@@ -1,0 +1,201 @@
+"""Parity of the batched tcgen05 path (batch 16..32, fp16 weights) against the
+fp64 CPU oracle, through the C ABI.
+
+FC1 and FC2 are checked in isolation (same index list, same FC1 output fed to
+both sides) and as a whole layer, on shapes that exercise the work split:
+ragged per-CTA row shares, several 128-row tiles per CTA (both accumulator
+buffers reused), several FC2 pieces per CTA, padded token counts (17, 20, 24)
+and a batch that is not a multiple of 4 (h copied in 4-byte pieces).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synth import CONFIGS, make_layer, make_tokens, small
+from tests.parity import close, mask_matches, unpack_mask
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _pi():
+    import activation_sparse_ffn_layer_gb300 as P
+    P.lib()
+    return P
+
+
+def _ws(P, desc):
+    return torch.zeros(P.pi_workspace_bytes(desc), dtype=torch.uint8, device=DEV)
+
+
+CASES = [
+    ("fp16", small(CONFIGS["c1"], d=256, F=1000, rank=32)),
+    ("fp16-d1024", small(CONFIGS["c3"], d=1024, F=4099, rank=64)),
+    ("gated", small(CONFIGS["c4"], d=512, F=1500, rank=64)),
+]
+
+
+def _masks(P, w, cfg, x, desc, ws, batch):
+    W = (w.F + 31) // 32
+    mask = torch.zeros(batch, W, dtype=torch.int32, device=DEV)
+    P.pi_predict(desc, x, w.p1, w.p2, w.b1, cfg.tau, mask, ws)
+    idx = torch.zeros(w.F, dtype=torch.int32, device=DEV)
+    cnt = torch.zeros(1, dtype=torch.int32, device=DEV)
+    P.pi_compact(desc, mask, None, idx, None, cnt)
+    torch.cuda.synchronize()
+    return mask, idx, cnt
+
+
+def _check_fc(P, w, wh, x, desc, ws, mask, idx, cnt, batch, what, sample=None):
+    n = int(cnt.item())
+    assert n > 0
+    h = torch.full((w.F * batch,), float("nan"), dtype=torch.float32, device=DEV)
+    wsx = P.weights_struct(w)
+    P.pi_sparse_fc1(desc, x, wsx, idx, cnt, mask, h)
+    y = torch.empty(batch, w.d, dtype=torch.float32, device=DEV)
+    P.pi_sparse_fc2(desc, h, idx, cnt, wsx, y, ws)
+    torch.cuda.synchronize()
+    idx_h = idx.cpu().numpy()[:n]
+    hg = h.cpu().numpy()[: n * batch].reshape(n, batch)
+    mk = mask.cpu().numpy().view(np.uint32)
+    toks = range(batch) if sample is None else sample
+    for b in toks:
+        own = unpack_mask(mk[b], w.F)[idx_h]
+        ho = np.where(own, oracle.fc1(x[b].cpu(), wh, idx_h), 0.0)
+        close(hg[:, b], ho, f"{what} fc1 token {b}")
+        yo = oracle.fc2(hg[:, b].astype(np.float64), wh, idx_h)
+        close(y[b].cpu().numpy(), yo, f"{what} fc2 token {b}")
+    return n
+
+
+@pytest.mark.parametrize("kind,cfg", CASES, ids=[c[0] for c in CASES])
+@pytest.mark.parametrize("batch", [16, 17, 24, 32])
+def test_tc_fc1_fc2_parity(kind, cfg, batch):
+    P = _pi()
+    w = make_layer(cfg, 0, device=DEV)
+    wh = w.to("cpu")
+    x = make_tokens(cfg, 0, batch, device=DEV)
+    desc = P.layer_desc(w, batch)
+    ws = _ws(P, desc)
+    mask, idx, cnt = _masks(P, w, cfg, x, desc, ws, batch)
+    _check_fc(P, w, wh, x, desc, ws, mask, idx, cnt, batch, f"{kind} B={batch}")
+
+
+def test_tc_many_tiles_per_cta():
+    """A union list long enough that every CTA runs three or more 128-row FC1
+    tiles (both TMEM accumulator buffers reused) and that FC2 ranges cross
+    column-tile boundaries."""
+    P = _pi()
+    cfg = small(CONFIGS["c1"], d=256, F=72000, rank=32, mean_rate=0.35)
+    w = make_layer(cfg, 0, device=DEV)
+    wh = w.to("cpu")
+    batch = 32
+    x = make_tokens(cfg, 0, batch, device=DEV)
+    desc = P.layer_desc(w, batch)
+    ws = _ws(P, desc)
+    mask, idx, cnt = _masks(P, w, cfg, x, desc, ws, batch)
+    n = int(cnt.item())
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert n > 2 * 128 * sms, n
+    _check_fc(P, w, wh, x, desc, ws, mask, idx, cnt, batch, "many tiles", sample=[0, 13, 31])
+
+
+def test_tc_tiny_union():
+    """Fewer listed rows than SMs: most CTAs get no rows (they must leave
+    cleanly) and FC2 pieces are single rows."""
+    P = _pi()
+    cfg = small(CONFIGS["c1"], d=256, F=1000, rank=32)
+    w = make_layer(cfg, 0, device=DEV)
+    wh = w.to("cpu")
+    batch = 16
+    x = make_tokens(cfg, 0, batch, device=DEV)
+    desc = P.layer_desc(w, batch)
+    ws = _ws(P, desc)
+    W = (w.F + 31) // 32
+    words = np.zeros((batch, W), np.uint32)
+    rng = np.random.default_rng(5)
+    rows = rng.choice(w.F, size=7, replace=False)
+    for r in rows:
+        words[rng.integers(batch), r // 32] |= np.uint32(1 << (r % 32))
+    mask = torch.from_numpy(words.view(np.int32)).to(DEV)
+    idx = torch.zeros(w.F, dtype=torch.int32, device=DEV)
+    cnt = torch.zeros(1, dtype=torch.int32, device=DEV)
+    P.pi_compact(desc, mask, None, idx, None, cnt)
+    torch.cuda.synchronize()
+    assert int(cnt.item()) == 7
+    _check_fc(P, w, wh, x, desc, ws, mask, idx, cnt, batch, "tiny union")
+
+
+def test_tc_empty_union():
+    P = _pi()
+    cfg = small(CONFIGS["c1"], d=256, F=1000, rank=32)
+    w = make_layer(cfg, 0, device=DEV)
+    batch = 16
+    desc = P.layer_desc(w, batch)
+    ws = _ws(P, desc)
+    idx = torch.zeros(w.F, dtype=torch.int32, device=DEV)
+    cnt = torch.zeros(1, dtype=torch.int32, device=DEV)
+    h = torch.zeros(w.F * batch, dtype=torch.float32, device=DEV)
+    y = torch.full((batch, w.d), float("nan"), dtype=torch.float32, device=DEV)
+    wsx = P.weights_struct(w)
+    x = make_tokens(cfg, 0, batch, device=DEV)
+    P.pi_sparse_fc1(desc, x, wsx, idx, cnt, None, h)
+    P.pi_sparse_fc2(desc, h, idx, cnt, wsx, y, ws)
+    torch.cuda.synchronize()
+    b2 = w.b2.float().cpu().numpy()
+    assert np.array_equal(y.cpu().numpy(), np.broadcast_to(b2, (batch, w.d)))
+
+
+@pytest.mark.parametrize("kind,cfg", CASES, ids=[c[0] for c in CASES])
+def test_tc_layer_matches_oracle_and_batch1(kind, cfg):
+    """Whole layer at batch 16 (FC2 skips rows that FC1 found dead): every
+    row equals the oracle's masked FFN and the batch-1 result of its token."""
+    P = _pi()
+    w = make_layer(cfg, 0, device=DEV)
+    wh = oracle.host_layer(w.to("cpu"))
+    batch = 16
+    x = make_tokens(cfg, 0, batch, device=DEV)
+    desc = P.layer_desc(w, batch)
+    ws = _ws(P, desc)
+    y = torch.empty(batch, w.d, dtype=torch.float32, device=DEV)
+    P.pi_ffn_layer(desc, x, P.weights_struct(w), cfg.tau, ws, y)
+    torch.cuda.synchronize()
+    lay = P.pi_workspace_layout(desc)
+    W = (w.F + 31) // 32
+    mask = ws[lay.mask:lay.mask + 4 * batch * W].view(torch.int32).cpu().numpy().view(np.uint32).reshape(batch, W)
+    yb = y.cpu().numpy()
+    d1 = P.layer_desc(w, 1)
+    ws1 = _ws(P, d1)
+    off1 = P.pi_workspace_layout(d1).mask
+    y1 = torch.empty(1, w.d, dtype=torch.float32, device=DEV)
+    same = 0
+    for b in range(batch):
+        o = oracle.predict(x[b].cpu(), wh, cfg.tau)
+        mask_matches(mask[b], o, w.F, cfg.tau, f"{kind} token {b}")
+        close(yb[b], oracle.ffn_masked(x[b].cpu(), wh, mask[b]), f"{kind} layer token {b}")
+        P.pi_ffn_layer(d1, x[b:b + 1].contiguous(), P.weights_struct(w), cfg.tau, ws1, y1)
+        torch.cuda.synchronize()
+        m1 = ws1[off1:off1 + 4 * W].view(torch.int32).cpu().numpy().view(np.uint32)
+        if np.array_equal(mask[b], m1):  # an in-band score may land on either side
+            same += 1
+            close(yb[b], y1.cpu().numpy()[0], f"{kind} batched row {b} vs batch 1")
+    assert same >= batch - 2
+
+
+def test_tc_layer_repeatable_bitwise():
+    P = _pi()
+    cfg = CASES[1][1]
+    w = make_layer(cfg, 0, device=DEV)
+    batch = 32
+    x = make_tokens(cfg, 0, batch, device=DEV)
+    desc = P.layer_desc(w, batch)
+    ws = _ws(P, desc)
+    outs = []
+    for _ in range(3):
+        y = torch.empty(batch, w.d, dtype=torch.float32, device=DEV)
+        P.pi_ffn_layer(desc, x, P.weights_struct(w), cfg.tau, ws, y)
+        torch.cuda.synchronize()
+        outs.append(y.cpu().numpy())
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+    assert P.pi_last_device_status() == 0
