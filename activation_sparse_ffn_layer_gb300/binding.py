@@ -69,7 +69,7 @@ def lib(path: Optional[str] = None):
         "pi_workspace_layout": (I, [D, C.POINTER(pi_workspace_layout_t)]),
         "pi_predict": (I, [D, P, P, P, P, Fl, P, P, S, P]),
         "pi_compact": (I, [D, P, P, P, P, P, P]),
-        "pi_sparse_fc1": (I, [D, P, Wt, P, P, P, P, P]),
+        "pi_sparse_fc1": (I, [D, P, Wt, P, P, P, P, P, S, P]),
         "pi_sparse_fc2": (I, [D, P, P, P, Wt, P, P, S, P]),
         "pi_ffn_layer": (I, [D, P, Wt, Fl, P, S, P, P]),
         "pi_rmsnorm_half": (I, [I, I, P, Fl, P, P]),
@@ -155,9 +155,10 @@ def pi_compact(desc, mask, table, idx, orig_idx, d_count):
                                           _ptr(d_count), _stream()))
 
 
-def pi_sparse_fc1(desc, x, wstruct, idx, d_count, mask, h):
+def pi_sparse_fc1(desc, x, wstruct, idx, d_count, mask, h, workspace):
     _check("pi_sparse_fc1", lib().pi_sparse_fc1(C.byref(desc), _ptr(x), C.byref(wstruct), _ptr(idx),
-                                                _ptr(d_count), _ptr(mask), _ptr(h), _stream()))
+                                                _ptr(d_count), _ptr(mask), _ptr(h), _ptr(workspace),
+                                                workspace.numel() * workspace.element_size(), _stream()))
 
 
 def pi_sparse_fc2(desc, h, idx, d_count, wstruct, y, workspace):

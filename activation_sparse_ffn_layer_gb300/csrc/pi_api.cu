@@ -80,7 +80,8 @@ bool make_plan(const pi_layer_desc& desc, Plan* p) {
     q.off_upart = off; off = up(off + sizeof(float) * (size_t)q.u_splits * q.B * q.r);
     q.off_part = off;  off = up(off + sizeof(float) * q.part_floats);
     q.off_xbuf = off;  off = up(off + sizeof(uint16_t) * 2 * (size_t)q.B * q.d);
-    q.off_live = off;  off = up(off + (size_t)q.F);
+    q.off_live = off;  off = up(off + sizeof(int32_t) * (size_t)q.F);
+    q.off_uhl = off;   off = up(off + (q.tc ? tc_uhl_bytes(q) : 0));
     q.total = off;
     *p = q;
     return true;
@@ -184,10 +185,11 @@ cudaError_t run_stack(const Plan& p, int n, const LayerPtrs* lp, const int* rank
         Plan q = p;
         q.r = ranks ? ranks[l] : p.r;
         const LayerPtrs& w = lp[l];
-        cudaError_t e = launch_predict(q, cur, w.p1, w.p2, w.b1, tau, mask, at<float>(ws, p.off_upart), s);
+        cudaError_t e = launch_predict(q, cur, w.p1, w.p2, w.b1, tau, mask, ws, s);
         if (e == cudaSuccess) e = launch_compact(q, mask, nullptr, idx, nullptr, cnt, s);
-        uint8_t* live = at<uint8_t>(ws, p.off_live);
-        if (e == cudaSuccess) e = launch_fc1(q, cur, w, idx, cnt, q.B > 1 ? mask : nullptr, h, live, s);
+        int32_t* live = at<int32_t>(ws, p.off_live);
+        if (e == cudaSuccess)
+            e = launch_fc1(q, cur, w, idx, cnt, q.B > 1 ? mask : nullptr, at<float>(ws, p.off_part), h, live, s);
         if (e == cudaSuccess && layer_counts) e = launch_count_active(q, cnt, h, layer_counts + 2 * l, s);
         if (e == cudaSuccess) e = launch_fc2(q, h, idx, cnt, w, q.tc ? live : nullptr, at<float>(ws, p.off_part), y, s);
         if (e != cudaSuccess) return e;
@@ -235,7 +237,7 @@ pi_status pi_predict(const pi_layer_desc* desc, const pi_half* x, const pi_half*
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return from_cuda(launch_predict(p, reinterpret_cast<const __half*>(x), reinterpret_cast<const __half*>(p1),
                                     reinterpret_cast<const __half*>(p2), reinterpret_cast<const __half*>(bpred),
-                                    tau, mask, at<float>(workspace, p.off_upart), s));
+                                    tau, mask, workspace, s));
 }
 
 pi_status pi_compact(const pi_layer_desc* desc, const uint32_t* mask, const int32_t* table, int32_t* idx,
@@ -248,14 +250,15 @@ pi_status pi_compact(const pi_layer_desc* desc, const uint32_t* mask, const int3
 
 pi_status pi_sparse_fc1(const pi_layer_desc* desc, const pi_half* x, const pi_layer_weights* w,
                         const int32_t* idx, const int32_t* d_count, const uint32_t* mask, float* h,
-                        void* stream) {
+                        void* workspace, size_t ws_bytes, void* stream) {
     Plan p;
     if (!desc || !make_plan(*desc, &p)) return PI_ERR_INVALID_ARG;
     if (!x || !aligned16(x) || !idx || !d_count || !h || !weights_ok(p, w, true, false, false))
         return PI_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace) || ws_bytes < p.total) return PI_ERR_WORKSPACE;
     if ((size_t)8 * p.d * sizeof(uint16_t) > 200 * 1024) return PI_ERR_UNSUPPORTED;
-    return from_cuda(launch_fc1(p, reinterpret_cast<const __half*>(x), ptrs(w), idx, d_count, mask, h, nullptr,
-                                static_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_fc1(p, reinterpret_cast<const __half*>(x), ptrs(w), idx, d_count, mask,
+                                at<float>(workspace, p.off_part), h, nullptr, static_cast<cudaStream_t>(stream)));
 }
 
 pi_status pi_sparse_fc2(const pi_layer_desc* desc, const float* h, const int32_t* idx, const int32_t* d_count,
@@ -320,7 +323,9 @@ int pi_launches_per_layer(const pi_layer_desc* desc) {
     if (p.fused) return 1;  // one persistent kernel
     // predictor: 2 per token chunk; compaction: 1; then FC1 + FC2 + the FC2
     // reduction (tcgen05 path: all tokens at once) or FC1 and FC2 per chunk + 1
-    if (p.tc) return 2 * chunks + 1 + 1 + 2;
+    // tcgen05 path: predictor u + finish + s, compaction, FC1 + finish, FC2 + reduction
+    if (p.tc && p.r % 16 == 0) return 3 + 1 + 2 + 2;
+    if (p.tc) return 2 * chunks + 1 + 2 + 2;
     return 2 * chunks + 1 + chunks + chunks + 1;
 }
 

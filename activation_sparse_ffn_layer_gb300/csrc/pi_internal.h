@@ -27,7 +27,7 @@ struct Plan {
     bool fused;     // pi_ffn_layer / pi_ffn_stack take the fused persistent kernel
     bool tc;        // FC1 / FC2 take the tcgen05 batched path (batch 16..32, fp16 weights)
     size_t part_floats;  // FC2 partial sums of whichever FC2 path the plan takes
-    size_t off_mask, off_idx, off_count, off_h, off_upart, off_part, off_xbuf, off_live, total;
+    size_t off_mask, off_idx, off_count, off_h, off_upart, off_part, off_xbuf, off_live, off_uhl, total;
 };
 
 bool make_plan(const pi_layer_desc& desc, Plan* p);
@@ -45,17 +45,18 @@ struct LayerPtrs {
     const int32_t* table;
 };
 
+// ws: the layer workspace (u partial sums and, on the tcgen05 path, u hi | lo rows)
 cudaError_t launch_predict(const Plan& p, const __half* x, const __half* p1, const __half* p2,
-                           const __half* bpred, float tau, uint32_t* mask, float* upart,
-                           cudaStream_t s);
+                           const __half* bpred, float tau, uint32_t* mask, void* ws, cudaStream_t s);
 cudaError_t launch_compact(const Plan& p, const uint32_t* mask, const int32_t* table, int32_t* idx,
                            int32_t* orig, int32_t* count, cudaStream_t s);
 // live (nullable): FC1 marks listed rows whose h is non-zero for some token
 // (tcgen05 path only); FC2 may then skip the other rows' W2t reads.
 cudaError_t launch_fc1(const Plan& p, const __half* x, const LayerPtrs& w, const int32_t* idx,
-                       const int32_t* count, const uint32_t* mask, float* h, uint8_t* live, cudaStream_t s);
+                       const int32_t* count, const uint32_t* mask, float* partial, float* h, int32_t* live,
+                       cudaStream_t s);
 cudaError_t launch_fc2(const Plan& p, const float* h, const int32_t* idx, const int32_t* count,
-                       const LayerPtrs& w, const uint8_t* live, float* partial, float* y, cudaStream_t s);
+                       const LayerPtrs& w, const int32_t* live, float* partial, float* y, cudaStream_t s);
 cudaError_t launch_rmsnorm(int d, int B, const float* y, float eps, __half* x, cudaStream_t s);
 // out[0] = *count, out[1] = listed neurons whose h is non-zero for some token
 cudaError_t launch_count_active(const Plan& p, const int32_t* count, const float* h, int32_t* out, cudaStream_t s);
@@ -63,12 +64,16 @@ cudaError_t launch_count_active(const Plan& p, const int32_t* count, const float
 // ---- tcgen05 batched path (pi_tc.cu) ----
 bool tc_supported(const Plan& p);
 int tc_tokens(const Plan& p);       // N of the MMAs: batch rounded up to 16 or 32
-int tc_slots(const Plan& p);        // partial tiles per CTA of the FC2 split
-size_t tc_part_floats(const Plan& p);
+size_t tc_part_floats(const Plan& p);  // partial tiles of the stream-K splits
+size_t tc_uhl_bytes(const Plan& p);    // u as fp16 hi | lo rows
+cudaError_t launch_predict_tc(const Plan& p, const __half* x, const __half* p1, const __half* p2,
+                              const __half* bpred, float tau, uint32_t* mask, float* part, __half* uhl,
+                              cudaStream_t s);
 cudaError_t launch_fc1_tc(const Plan& p, const __half* x, const LayerPtrs& w, const int32_t* idx,
-                          const int32_t* count, const uint32_t* mask, float* h, uint8_t* live, cudaStream_t s);
+                          const int32_t* count, const uint32_t* mask, float* part, float* h, int32_t* live,
+                          cudaStream_t s);
 cudaError_t launch_fc2_tc(const Plan& p, const float* h, const int32_t* idx, const int32_t* count,
-                          const LayerPtrs& w, const uint8_t* live, float* partial, float* y, cudaStream_t s);
+                          const LayerPtrs& w, const int32_t* live, float* partial, float* y, cudaStream_t s);
 
 // ---- fused persistent stack (batch 1) ----
 struct FusedStackArgs {

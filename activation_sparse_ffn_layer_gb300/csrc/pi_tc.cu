@@ -45,7 +45,7 @@ namespace {
 
 constexpr int kTcThreads = 288;      // warps 0-3 load, 4-7 epilogue, 8 MMA
 constexpr int kLoaders = 128;
-constexpr int kRingBudget = 200 * 1024;
+constexpr int kRingBudget = 220 * 1024;
 constexpr int kTileA = 16384;        // 128 x 64 fp16 operand tile
 
 PI_DEV unsigned long long tc_timer() {
@@ -99,11 +99,14 @@ PI_DEV void bar_drain(unsigned long long* b, unsigned parity, long long timeout_
     }
 }
 
+// cp.async copies carry no compiler memory clobber: their shared-memory
+// results are only read after cp_wait / cp_wait_all (which have one), and
+// leaving it off lets the compiler keep row ids in registers across copies.
 PI_DEV void cp16(void* dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(su32(dst)), "l"(src) : "memory");
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(su32(dst)), "l"(src));
 }
 PI_DEV void cp4(void* dst, const void* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(su32(dst)), "l"(src) : "memory");
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(su32(dst)), "l"(src));
 }
 PI_DEV void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -135,6 +138,13 @@ PI_DEV void tc_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "m
 PI_DEV uint64_t sdesc(unsigned addr, unsigned lbo, unsigned sbo) {
     return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
+}
+// Same for the 128-byte-swizzled K-major layout: rows of 128 bytes (64 fp16
+// of K), 8-row atoms of 1024 bytes (1024-byte aligned), 16-byte chunk c of row
+// r stored at chunk position c ^ (r % 8); K-steps advance the start by 32 bytes.
+PI_DEV uint64_t sdesc_sw128(unsigned addr) {
+    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 // Instruction descriptor of kind::f16: fp32 D, fp16 A and B, A major-ness,
 // B K-major, N >> 3 at bit 17, M >> 4 at bit 24.
@@ -180,191 +190,326 @@ PI_DEV unsigned char* align1024(unsigned char* p) {
 
 constexpr int tmem_cols_for(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : 256; }
 
-// ------------------------------------------------------------------------ FC1
+// ------------------------------------------------- row-tile GEMMs (FC1, predictor)
+//
+// D[m, t] = sum_k A[row(m), k] Bop[t, k] over 128-row tiles of A (rows
+// gathered through idx, or contiguous), K in chunks of 64, N = tokens.
+//   MODE 0  FC1            A = W1 rows (gathered),          Bop = x
+//   MODE 1  FC1 gated      A = Wg and Wu rows (gathered),   Bop = x
+//   MODE 2  predictor u    A = P1 rows,                     Bop = x
+//   MODE 3  predictor s    A = P2 rows,                     Bop = u (hi | lo fp16)
+// Modes 0-2 split the (tile x K-chunk) space evenly over the CTAs and write
+// one partial tile per tile touched; a finish kernel adds the partials of each
+// tile in ascending CTA order and applies the epilogue.  Mode 3 has short K
+// (the rank) and many tiles: each CTA takes whole tiles and thresholds s in
+// its own epilogue (mask bits by warp ballot: a warp's 32 TMEM lanes are the
+// 32 rows of one mask word).
 
-template <bool GATED, int NT>
-struct Fc1Cfg {
-    static constexpr int NA = GATED ? 2 : 1;            // operand tiles per stage (gate, up)
-    static constexpr int X = NT * 128;                   // NT tokens x 64 fp16
+struct Span {
+    int tile, kc0, kc1;
+};
+
+template <int MODE, int NT>
+struct RowsCfg {
+    static constexpr bool GATHER = MODE <= 1;
+    static constexpr bool DIRECT = MODE == 3;
+    static constexpr int NA = MODE == 1 ? 2 : 1;            // A operand tiles per stage
+    static constexpr int NB = DIRECT ? 2 * NT : NT;          // B operand rows
+    static constexpr int X = NB * 128;                       // NB rows x 64 fp16
     static constexpr int STAGE = NA * kTileA + X;
-    static constexpr int S = kRingBudget / STAGE > 8 ? 8 : kRingBudget / STAGE;
-    static constexpr int LAG = S - 2;                    // stages whose copies stay in flight
-    static constexpr int ACC = NA * NT;                  // TMEM columns per accumulator buffer
+    // even ring of stages, filled two K-chunks at a time (256 contiguous bytes
+    // of every row per visit); LAGP pairs of copies stay in flight
+    static constexpr int S0 = kRingBudget / STAGE > 12 ? 12 : kRingBudget / STAGE;
+    static constexpr int S = S0 & ~1;
+    static constexpr int LAGP = S / 2 >= 4 ? S / 2 - 2 : S / 2 - 1;
+    static constexpr int ACC = NA * NB;                      // TMEM columns per accumulator buffer
+    static constexpr int COLS = NA * NT;                     // partial columns (modes 0-2)
     static constexpr int TMEM = tmem_cols_for(2 * ACC);
     static constexpr size_t SMEM = (size_t)S * STAGE + 1024;
 };
 
-struct TcFc1Args {
-    const __half* x;
-    const __half* w1;
-    const __half* wu;
-    const __half* b1;
-    const int32_t* idx;
-    const int32_t* count;
-    const uint32_t* mask;  // per-token masks [B][W] (nullable)
-    float* h;              // [count][B]
-    uint8_t* live;         // nullable [F]: 1 where some token's h is non-zero
+struct TcRowsArgs {
+    const __half* a0;      // A rows (row length K)
+    const __half* a1;      // up-projection rows (gated FC1)
+    const int32_t* idx;    // gathered row ids (FC1)
+    const int32_t* count;  // device row count (FC1), else R rows
+    int R;
+    const __half* bop;     // B operand rows [bop_rows][K] fp16
+    int bop_rows;
+    int K, B;
+    float* part;           // modes 0-2: [G][slots][COLS][128]
+    int slots;
+    const __half* bias;    // mode 3: s threshold
+    float tau;
+    uint32_t* mask;        // mode 3: [B][W]
+    int W;
     int* status;
     long long timeout_ns;
-    int B, d, W;
 };
 
-// h[j, t] = act(W1[idx_j] . x_t + b1[idx_j]) for the union list, zero where
-// token t's own mask does not list idx_j.
-template <bool GATED, int NT>
-__global__ void __launch_bounds__(kTcThreads, 1) k_fc1_tc(TcFc1Args a) {
-    using C = Fc1Cfg<GATED, NT>;
+template <int MODE, int NT>
+__global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
+    using C = RowsCfg<MODE, NT>;
     extern __shared__ unsigned char dsm[];
     __shared__ __align__(8) unsigned long long full[C::S], empty[C::S], accf[2], acce[2], drain;
     __shared__ unsigned tmem_slot;
     __shared__ int abort_flag;
+    __shared__ int srow[128];  // A row ids of the current tile (-1 past the end)
 
-    const int n = *a.count;
+    const int R = a.count != nullptr ? *a.count : a.R;
     const int G = gridDim.x, g = blockIdx.x;
-    const int r0 = (int)((long long)n * g / G), r1 = (int)((long long)n * (g + 1) / G);
-    const int len = r1 - r0;
-    if (len <= 0) return;
-    const int ntile = (len + 127) / 128;
-    const int nk = a.d / 64;
-    const int total = ntile * nk;
+    const int ntile = (R + 127) / 128;
+    const int nk = (a.K + 63) / 64;
+    const long long U = (long long)ntile * nk;
+    const long long u0 = U * g / G, u1 = U * (g + 1) / G;
+    int npiece;
+    if (C::DIRECT)
+        npiece = ntile > g ? (ntile - 1 - g) / G + 1 : 0;
+    else
+        npiece = u0 < u1 ? (int)((u1 - 1) / nk - u0 / nk) + 1 : 0;
+    if (npiece == 0) return;
+    auto span = [&](int p) {
+        Span s;
+        if (C::DIRECT) {
+            s.tile = g + p * G;
+            s.kc0 = 0;
+            s.kc1 = nk;
+        } else {
+            s.tile = (int)(u0 / nk) + p;
+            const long long lo = (long long)s.tile * nk;
+            s.kc0 = (int)((u0 > lo ? u0 : lo) - lo);
+            s.kc1 = (int)((u1 < lo + nk ? u1 : lo + nk) - lo);
+        }
+        return s;
+    };
     unsigned char* ring = align1024(dsm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    if (tid == 0) {
-        for (int s = 0; s < C::S; ++s) {
-            bar_init(&full[s], kLoaders);
-            bar_init(&empty[s], 1);
+    // warp 8 sets up barriers and tensor memory while the loaders fetch the
+    // first tile's row ids
+    if (warp == 8) {
+        if (lane == 0) {
+            for (int s = 0; s < C::S; ++s) {
+                bar_init(&full[s], kLoaders);
+                bar_init(&empty[s], 1);
+            }
+            for (int b = 0; b < 2; ++b) {
+                bar_init(&accf[b], 1);
+                bar_init(&acce[b], 128);
+            }
+            bar_init(&drain, 1);
+            abort_flag = 0;
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         }
-        for (int b = 0; b < 2; ++b) {
-            bar_init(&accf[b], 1);
-            bar_init(&acce[b], 128);
-        }
-        bar_init(&drain, 1);
-        abort_flag = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        __syncwarp();
+        tmem_alloc(&tmem_slot, C::TMEM);
+    } else if (warp < 4) {
+        const Span s0 = span(0);
+        const int rows = R - 128 * s0.tile < 128 ? R - 128 * s0.tile : 128;
+        srow[tid] = tid < rows ? (C::GATHER ? a.idx[128 * s0.tile + tid] : 128 * s0.tile + tid) : -1;
     }
-    if (warp == 8) tmem_alloc(&tmem_slot, C::TMEM);
     tc_before();
     __syncthreads();
     tc_after();
     const unsigned tmem = tmem_slot;
     const Ctl ctl{a.status, a.timeout_ns, &abort_flag};
-    auto tile_lo = [&](int i) { return r0 + (int)((long long)len * i / ntile); };
 
     if (warp < 4) {
-        // ---- loaders: thread t copies chunk kc of 8 rows per stage (each warp
-        // instruction covers 8 rows x 64 contiguous bytes; the 8 lanes of a
-        // shared-memory phase hit 8 different banks groups)
+        // ---- loaders.  A tiles use the 128-byte-swizzled layout, so the 8
+        // lanes of one shared-memory phase copy the 8 chunks of one row's 128
+        // bytes without bank conflicts.  Stages go out in pairs: a warp
+        // instruction copies 2 rows x 256 contiguous bytes (both K-chunks).
         const int t = tid, w = t >> 5, l = t & 31;
-        const int kc = 4 * (w & 1) + (l >> 3);
-        const int rb = w >> 1;
-        int it = 0;
-        bool ok = true;
-        for (int i = 0; i < ntile && ok; ++i) {
-            const int tr0 = tile_lo(i), rows = tile_lo(i + 1) - tr0;
-            const __half* src[8];
-            const __half* srcu[8];
+        int total = 0;
+        for (int p = 0; p < npiece; ++p) {
+            const Span sp = span(p);
+            total += sp.kc1 - sp.kc0;
+        }
+        int pc = 0;
+        Span sp = span(0);
+        int ks = sp.kc0;
+        // this thread's rows: pair issue (16 rows) and single-stage issue (8 rows)
+        long long pr[16], sr[8];
+        auto take_rows = [&]() {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int row = 8 * (2 * q + rb) + (l & 7);
-                src[q] = nullptr;
-                srcu[q] = nullptr;
-                if (row < rows) {
-                    const size_t k = (size_t)a.idx[tr0 + row];
-                    src[q] = a.w1 + k * a.d + kc * 8;
-                    if (GATED) srcu[q] = a.wu + k * a.d + kc * 8;
+            for (int i = 0; i < 16; ++i) {
+                const int rid = srow[2 * (4 * i + w) + (l >> 4)];
+                pr[i] = rid >= 0 ? (long long)rid * a.K : -1;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int rid = srow[4 * (4 * i + w) + (l >> 3)];
+                sr[i] = rid >= 0 ? (long long)rid * a.K : -1;
+            }
+        };
+        auto load_rows = [&]() {
+            loaders_sync_any(false);  // nobody still reads the previous tile's ids
+            const int rows = R - 128 * sp.tile < 128 ? R - 128 * sp.tile : 128;
+            srow[t] = t < rows ? (C::GATHER ? a.idx[128 * sp.tile + t] : 128 * sp.tile + t) : -1;
+            loaders_sync_any(false);
+            take_rows();
+        };
+        auto next_piece = [&]() {
+            if (ks == sp.kc1 && pc + 1 < npiece) {
+                ++pc;
+                sp = span(pc);
+                ks = sp.kc0;
+                load_rows();
+            }
+        };
+        // chunk c of K-chunk kchunk of `row` (element offset base, -1: none)
+        // into the A tile(s) of slot st
+        auto copy_a = [&](unsigned char* st, int row, long long base, int kchunk, int c) {
+            if (base < 0) return;
+            const unsigned off = (row >> 3) * 1024 + (row & 7) * 128 + ((c ^ (row & 7)) << 4);
+            const long long gofs = base + kchunk * 64 + c * 8;
+            cp16(st + off, a.a0 + gofs);
+            if (MODE == 1) cp16(st + kTileA + off, a.a1 + gofs);
+        };
+        // B operand chunk of K-chunk kchunk into slot st (no swizzle)
+        auto copy_b = [&](unsigned char* st, int kchunk) {
+            const int k0 = kchunk * 64;
+            const int kvalid = a.K - k0 < 64 ? a.K - k0 : 64;
+#pragma unroll
+            for (int pp = t; pp < C::NB * 8; pp += kLoaders) {
+                const int gg = pp >> 5, ll = pp & 31;
+                const int tok = 8 * (gg >> 1) + (ll & 7), kx = 4 * (gg & 1) + (ll >> 3);
+                if (tok < a.bop_rows && kx * 8 < kvalid)
+                    cp16(st + C::NA * kTileA + kx * (C::NB * 16) + (tok >> 3) * 128 + (tok & 7) * 16,
+                         a.bop + (size_t)tok * a.K + k0 + kx * 8);
+            }
+        };
+        take_rows();
+        const int npairs = (total + 1) / 2;
+        bool ok = true;
+        for (int it = 0; it < total; it += 2) {
+            const int ng = total - it < 2 ? total - it : 2;
+            bool good = true;
+            for (int u = 0; u < ng; ++u) {
+                const int st = it + u;
+                if (good && st >= C::S && !bar_wait(&empty[st % C::S], ((st / C::S) - 1) & 1, ctl)) good = false;
+            }
+            if (loaders_sync_any(!good)) {  // stop together
+                ok = false;
+                break;
+            }
+            unsigned char* s0 = ring + (size_t)(it % C::S) * C::STAGE;
+            unsigned char* s1 = ring + (size_t)((it + 1) % C::S) * C::STAGE;
+            if (ng == 2 && ks + 1 < sp.kc1) {
+                const int u = (l >> 3) & 1, c = l & 7;
+                if (c * 8 < a.K - (ks + u) * 64) {
+                    unsigned char* sd = u ? s1 : s0;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) copy_a(sd, 2 * (4 * i + w) + (l >> 4), pr[i], ks + u, c);
+                }
+                copy_b(s0, ks);
+                copy_b(s1, ks + 1);
+                ks += 2;
+                next_piece();
+            } else {
+                for (int u = 0; u < ng; ++u) {
+                    unsigned char* st = u == 0 ? s0 : s1;
+                    if ((l & 7) * 8 < a.K - ks * 64) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) copy_a(st, 4 * (4 * i + w) + (l >> 3), sr[i], ks, l & 7);
+                    }
+                    copy_b(st, ks);
+                    ++ks;
+                    next_piece();
                 }
             }
-            for (int ks = 0; ks < nk; ++ks, ++it) {
-                const int s = it % C::S;
-                if (it >= C::S && !bar_wait(&empty[s], ((it / C::S) - 1) & 1, ctl)) {
-                    ok = false;
-                    break;
-                }
-                unsigned char* st = ring + (size_t)s * C::STAGE;
-                const int k0 = ks * 64;
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    if (src[q] != nullptr) {
-                        const int row = 8 * (2 * q + rb) + (l & 7);
-                        const unsigned off = kc * 2048 + (row >> 3) * 128 + (row & 7) * 16;
-                        cp16(st + off, src[q] + k0);
-                        if (GATED) cp16(st + kTileA + off, srcu[q] + k0);
-                    }
-                }
-#pragma unroll
-                for (int p = t; p < NT * 8; p += kLoaders) {
-                    const int gg = p >> 5, ll = p & 31;
-                    const int tok = 8 * (gg >> 1) + (ll & 7), kx = 4 * (gg & 1) + (ll >> 3);
-                    if (tok < a.B)
-                        cp16(st + C::NA * kTileA + kx * (NT * 16) + (tok >> 3) * 128 + (tok & 7) * 16,
-                             a.x + (size_t)tok * a.d + k0 + kx * 8);
-                }
-                cp_commit();
-                if (it >= C::LAG) {
-                    cp_wait<C::LAG>();
-                    fence_async_smem();
-                    bar_arrive(&full[(it - C::LAG) % C::S]);
-                }
+            cp_commit();
+            const int pd = it / 2 - C::LAGP;
+            if (pd >= 0) {
+                cp_wait<C::LAGP>();
+                fence_async_smem();
+                bar_arrive(&full[(2 * pd) % C::S]);
+                if (2 * pd + 1 < total) bar_arrive(&full[(2 * pd + 1) % C::S]);
+            }
+        }
+        if (ok) {
+            // release the pairs still in flight one by one, oldest first
+            const int first = npairs - C::LAGP < 0 ? 0 : npairs - C::LAGP;
+            for (int pd = first; pd < npairs; ++pd) {
+                const int newer = npairs - 1 - pd;  // groups committed after pair pd
+                if (newer >= 3)
+                    cp_wait<3>();
+                else if (newer == 2)
+                    cp_wait<2>();
+                else if (newer == 1)
+                    cp_wait<1>();
+                else
+                    cp_wait<0>();
+                fence_async_smem();
+                bar_arrive(&full[(2 * pd) % C::S]);
+                if (2 * pd + 1 < total) bar_arrive(&full[(2 * pd + 1) % C::S]);
             }
         }
         cp_wait_all();
-        if (ok) {
-            fence_async_smem();
-            for (int q = total - C::LAG < 0 ? 0 : total - C::LAG; q < total; ++q) bar_arrive(&full[q % C::S]);
-        }
     } else if (warp < 8) {
         // ---- epilogue: TMEM lane m = row m of the tile
         const int e = warp - 4, m = 32 * e + lane;
-        for (int i = 0; i < ntile; ++i) {
-            const int b = i & 1;
-            if (!bar_wait(&accf[b], (i >> 1) & 1, ctl)) break;
+        for (int p = 0; p < npiece; ++p) {
+            const int b = p & 1;
+            if (!bar_wait(&accf[b], (p >> 1) & 1, ctl)) break;
             tc_after();
-            float z[NT], zu[GATED ? NT : 1];
             const unsigned ta = tmem + ((unsigned)(32 * e) << 16) + (unsigned)(b * C::ACC);
+            const Span sp = span(p);
+            if (C::DIRECT) {
+                float vh[NT], vl[NT];
 #pragma unroll
-            for (int c = 0; c < NT; c += 16) {
-                tmem_ld16(ta + c, z + c);
-                if (GATED) tmem_ld16(ta + NT + c, zu + c);
-            }
-            tmem_wait_ld();
-            tc_before();
-            bar_arrive(&acce[b]);
-            const int tr0 = tile_lo(i), rows = tile_lo(i + 1) - tr0;
-            if (m < rows) {
-                const int j = tr0 + m;
-                const int k = a.idx[j];
-                const float bk = __half2float(a.b1[k]);
-                float* hrow = a.h + (size_t)j * a.B;
-                bool any = false;
+                for (int c = 0; c < NT; c += 16) {
+                    tmem_ld16(ta + c, vh + c);
+                    tmem_ld16(ta + NT + c, vl + c);
+                }
+                tmem_wait_ld();
+                tc_before();
+                bar_arrive(&acce[b]);
+                const int k = 128 * sp.tile + m;
+                const float bk = k < R ? __half2float(a.bias[k]) : 0.f;
+                const int word = (128 * sp.tile + 32 * e) >> 5;
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
-                    if (t < a.B) {
-                        float v = z[t] + bk;
-                        v = v > 0.f ? v : 0.f;
-                        if (GATED) v *= zu[t];
-                        if (a.mask != nullptr && !((a.mask[(size_t)t * a.W + (k >> 5)] >> (k & 31)) & 1u)) v = 0.f;
-                        hrow[t] = v;
-                        any |= v != 0.f;
-                    }
+                    const bool on = k < R && (vh[t] + vl[t]) + bk > a.tau;
+                    const unsigned bits = __ballot_sync(FULL, on);
+                    if (lane == 0 && t < a.B && word < a.W) a.mask[(size_t)t * a.W + word] = bits;
                 }
-                if (a.live != nullptr) a.live[j] = any ? 1 : 0;
+            } else {
+                float v[C::NA][NT];
+#pragma unroll
+                for (int q = 0; q < C::NA; ++q)
+#pragma unroll
+                    for (int c = 0; c < NT; c += 16) tmem_ld16(ta + q * C::NB + c, v[q] + c);
+                tmem_wait_ld();
+                tc_before();
+                bar_arrive(&acce[b]);
+                if (p < a.slots) {
+                    float* dst = a.part + ((size_t)g * a.slots + p) * C::COLS * 128 + m;
+#pragma unroll
+                    for (int q = 0; q < C::NA; ++q)
+#pragma unroll
+                        for (int t = 0; t < NT; ++t)
+                            if (t < a.B) dst[(size_t)(q * NT + t) * 128] = v[q][t];
+                } else if (lane == 0) {
+                    atomicExch(a.status, (int)PI_ERR_WORKSPACE);
+                }
             }
         }
     } else if (lane == 0) {
         // ---- MMA issuer
-        const unsigned idesc = idesc_f16(128, NT, false);
+        const unsigned idesc = idesc_f16(128, C::NB, false);
         int it = 0;
         bool ok = true;
-        for (int i = 0; i < ntile && ok; ++i) {
-            const int b = i & 1;
-            if (i >= 2 && !bar_wait(&acce[b], ((i >> 1) - 1) & 1, ctl)) {
+        for (int p = 0; p < npiece && ok; ++p) {
+            const Span sp = span(p);
+            const int b = p & 1;
+            if (p >= 2 && !bar_wait(&acce[b], ((p >> 1) - 1) & 1, ctl)) {
                 ok = false;
                 break;
             }
             tc_after();
             const unsigned dcol = tmem + (unsigned)(b * C::ACC);
-            for (int ks = 0; ks < nk; ++ks, ++it) {
+            for (int ks = sp.kc0; ks < sp.kc1; ++ks, ++it) {
                 const int s = it % C::S;
                 if (!bar_wait(&full[s], (it / C::S) & 1, ctl)) {
                     ok = false;
@@ -373,12 +518,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fc1_tc(TcFc1Args a) {
                 tc_after();
                 const unsigned sa = su32(ring + (size_t)s * C::STAGE);
                 const unsigned sx = sa + C::NA * kTileA;
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t bd = sdesc(sx + kk * 2 * NT * 16, NT * 16, 128);
-                    const unsigned acc = (ks | kk) ? 1u : 0u;
-                    mma_f16(dcol, sdesc(sa + kk * 4096, 2048, 128), bd, idesc, acc);
-                    if (GATED) mma_f16(dcol + NT, sdesc(sa + kTileA + kk * 4096, 2048, 128), bd, idesc, acc);
+                const int ksteps = (a.K - 64 * ks < 64 ? a.K - 64 * ks : 64) / 16;
+                for (int kk = 0; kk < ksteps; ++kk) {
+                    const uint64_t bd = sdesc(sx + kk * 2 * C::NB * 16, C::NB * 16, 128);
+                    const unsigned acc = (ks > sp.kc0 || kk > 0) ? 1u : 0u;
+                    mma_f16(dcol, sdesc_sw128(sa + kk * 32), bd, idesc, acc);
+                    if (MODE == 1) mma_f16(dcol + C::NB, sdesc_sw128(sa + kTileA + kk * 32), bd, idesc, acc);
                 }
                 mma_commit(&empty[s]);
             }
@@ -386,8 +531,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fc1_tc(TcFc1Args a) {
         }
         if (ok) {
             // every slot's last release has arrived before the CTA may exit
-            for (int s = 0; s < C::S && s < total; ++s) {
-                const int last = s + ((total - 1 - s) / C::S) * C::S;
+            for (int s = 0; s < C::S && s < it; ++s) {
+                const int last = s + ((it - 1 - s) / C::S) * C::S;
                 bar_drain(&empty[s], (last / C::S) & 1, a.timeout_ns);
             }
         } else {
@@ -403,6 +548,101 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fc1_tc(TcFc1Args a) {
     }
 }
 
+// The CTAs of a stream-K split (CTA g owns units [U*g/G, U*(g+1)/G)) that
+// touch tile `tile` (units [tile*nk, (tile+1)*nk)) form one contiguous range
+// [rng[0], rng[1]]; slot[g] is the partial slot CTA g wrote for the tile (-1:
+// empty share).  All threads of the block take part; the caller syncs after.
+constexpr int kMaxCtas = 1024;
+PI_DEV void cover_setup(long long U, int G, int nk, int tile, int* slot, int* rng) {
+    const long long lo = (long long)tile * nk, hi = lo + nk;
+    if (threadIdx.x == 0) {
+        rng[0] = G;
+        rng[1] = -1;
+    }
+    __syncthreads();
+    for (int g = threadIdx.x; g < G && g < kMaxCtas; g += blockDim.x) {
+        const long long u0 = U * g / G, u1 = U * (g + 1) / G;
+        const bool hit = u0 < u1 && u0 < hi && u1 > lo;
+        slot[g] = hit ? tile - (int)(u0 / nk) : -1;
+        if (hit) {
+            atomicMin(&rng[0], g);
+            atomicMax(&rng[1], g);
+        }
+    }
+}
+
+// Ascending-CTA sum; loads go out eight at a time so their latencies overlap.
+PI_DEV float sum_cover(const float* __restrict__ part, const int* slot, const int* rng, int slots, int cols,
+                       int col, int m) {
+    float acc = 0.f;
+    for (int g0 = rng[0]; g0 <= rng[1]; g0 += 8) {
+        float v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int g = g0 + k;
+            const int sl = g <= rng[1] ? slot[g] : -1;
+            v[k] = (sl >= 0 && sl < slots) ? __ldcg(part + (((size_t)g * slots + sl) * cols + col) * 128 + m) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc += v[k];
+    }
+    return acc;
+}
+
+// h[j, t] = act(Z[j, t] + b1[idx_j]) (gated: times Zu[j, t]), zero where token
+// t's own mask does not list idx_j; live[j] = some h[j, :] != 0.
+// Block: 32 consecutive rows (lane) x B tokens (warp).
+template <bool GATED>
+__global__ void __launch_bounds__(1024) k_fc1_finish(const float* __restrict__ part, int slots, int G, int nk,
+                                                     const int32_t* __restrict__ count, int B, int NT,
+                                                     const int32_t* __restrict__ idx, const __half* __restrict__ b1,
+                                                     const uint32_t* __restrict__ mask, int W,
+                                                     float* __restrict__ h, int32_t* __restrict__ live) {
+    __shared__ int slot[kMaxCtas];
+    __shared__ int rng[2];
+    __shared__ int any[32];
+    const int n = *count;
+    const int j0 = blockIdx.x * 32;
+    if (j0 >= n) return;
+    const int lane = threadIdx.x & 31, t = threadIdx.x >> 5;
+    cover_setup((long long)((n + 127) / 128) * nk, G, nk, j0 >> 7, slot, rng);
+    if (threadIdx.x < 32) any[threadIdx.x] = 0;
+    __syncthreads();
+    const int j = j0 + lane;
+    const int cols = (GATED ? 2 : 1) * NT;
+    if (j < n) {
+        const int m = j & 127;
+        const int k = idx[j];
+        float v = sum_cover(part, slot, rng, slots, cols, t, m) + __half2float(b1[k]);
+        v = v > 0.f ? v : 0.f;
+        if (GATED) v *= sum_cover(part, slot, rng, slots, cols, NT + t, m);
+        if (mask != nullptr && !((mask[(size_t)t * W + (k >> 5)] >> (k & 31)) & 1u)) v = 0.f;
+        h[(size_t)j * B + t] = v;
+        if (v != 0.f) any[lane] = 1;
+    }
+    __syncthreads();
+    if (t == 0 && j < n && live != nullptr) live[j] = any[lane] ? 1 : 0;
+}
+
+// u[t, i] = sum of the P1 x partials, stored as fp16 hi = fp16(u) and
+// lo = fp16(u - hi) rows: uhl[t][i] = hi, uhl[NT + t][i] = lo (zero rows for
+// padded tokens t >= B).  Block: 32 consecutive i (lane) x NT tokens (warp).
+__global__ void __launch_bounds__(1024) k_u_finish(const float* __restrict__ part, int slots, int G, int nk, int r,
+                                                   int B, int NT, __half* __restrict__ uhl) {
+    __shared__ int slot[kMaxCtas];
+    __shared__ int rng[2];
+    const int i0 = blockIdx.x * 32;
+    const int lane = threadIdx.x & 31, t = threadIdx.x >> 5;
+    cover_setup((long long)((r + 127) / 128) * nk, G, nk, i0 >> 7, slot, rng);
+    __syncthreads();
+    const int i = i0 + lane;
+    if (i >= r) return;
+    const float u = t < B ? sum_cover(part, slot, rng, slots, NT, t, i & 127) : 0.f;
+    const __half hi = __float2half_rn(u);
+    uhl[(size_t)t * r + i] = hi;
+    uhl[(size_t)(NT + t) * r + i] = __float2half_rn(u - __half2float(hi));
+}
+
 // ------------------------------------------------------------------------ FC2
 
 template <int NT>
@@ -410,11 +650,12 @@ struct Fc2Cfg {
     static constexpr int BOP = 2 * NT * 64 * 2;          // (hi | lo) tokens x 64 rows fp16
     static constexpr int RAW = 64 * NT * 4;              // 64 rows x B fp32 of h, as copied
     static constexpr int STAGE = kTileA + BOP + RAW;
-    static constexpr int S = kRingBudget / STAGE > 8 ? 8 : kRingBudget / STAGE;
+    static constexpr int IDX = 64 * 2 * 4;               // 64 row ids + 64 live flags (int32)
+    static constexpr int S = kRingBudget / (STAGE + IDX) > 8 ? 8 : kRingBudget / (STAGE + IDX);
     static constexpr int LAG = S - 2;
     static constexpr int ACC = 2 * NT;
     static constexpr int TMEM = tmem_cols_for(2 * ACC);
-    static constexpr size_t SMEM = (size_t)S * STAGE + 1024;
+    static constexpr size_t SMEM = (size_t)S * (STAGE + IDX) + 1024;
 };
 
 struct TcFc2Args {
@@ -422,7 +663,7 @@ struct TcFc2Args {
     const int32_t* idx;
     const int32_t* count;
     const __half* w2t;
-    const uint8_t* live;   // nullable: rows with live == 0 have h == 0 for every token
+    const int32_t* live;   // nullable: rows with live == 0 have h == 0 for every token
     float* part;           // [G][slots][NT][128]
     int* status;
     long long timeout_ns;
@@ -534,6 +775,39 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fc2_tc(TcFc2Args a) {
                 cv_st = 0;
             }
         };
+        // Row ids and live flags of stage q sit in a small ring (slot q % S),
+        // copied LAG + 1 stages ahead of use, so no loader waits on them.
+        int32_t* sidx = reinterpret_cast<int32_t*>(ring + (size_t)C::S * C::STAGE);
+        int32_t* slive = sidx + C::S * 64;
+        int total = 0;
+        for (int p = 0; p < npiece; ++p) {
+            Piece pc;
+            fc2_piece(u0, u1, n, p, &pc);
+            total += (pc.j1 - pc.j0 + 63) / 64;
+        }
+        int fq = 0, fpiece = 0, fst = 0;  // next stage whose row ids to copy
+        auto copy_ids = [&]() {
+            Piece pc;
+            fc2_piece(u0, u1, n, fpiece, &pc);
+            const int jb = pc.j0 + 64 * fst;
+            const int kk = t & 63;
+            const int j = jb + kk;
+            if (j < pc.j1) {
+                if (t < 64)
+                    cp4(sidx + (fq % C::S) * 64 + kk, a.idx + j);
+                else if (a.live != nullptr)
+                    cp4(slive + (fq % C::S) * 64 + kk, a.live + j);
+            }
+            ++fq;
+            if (64 * (++fst) >= pc.j1 - pc.j0) {
+                ++fpiece;
+                fst = 0;
+            }
+        };
+        while (fq < total && fq <= C::LAG) copy_ids();
+        cp_commit();
+        cp_wait_all();
+        loaders_sync_any(false);
         for (int pi_ = 0; pi_ < npiece && ok; ++pi_) {
             Piece pc;
             fc2_piece(u0, u1, n, pi_, &pc);
@@ -546,15 +820,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fc2_tc(TcFc2Args a) {
                 unsigned char* sb = ring + (size_t)s * C::STAGE;
                 const int jb = pc.j0 + 64 * st;
                 if (good) {
+                    int kv[8];
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         const int kk = 8 * q + (l & 7);
-                        const int j = jb + kk;
+                        const bool in = jb + kk < pc.j1;
+                        const bool alive = a.live == nullptr || slive[s * 64 + kk] != 0;
+                        kv[q] = (in && alive) ? sidx[s * 64 + kk] : -1;
+                    }
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const int kk = 8 * q + (l & 7);
                         unsigned char* dst = sb + mc * 128 + (kk >> 3) * 2048 + (kk & 7) * 16;
-                        bool take = j < pc.j1;
-                        if (take && a.live != nullptr) take = a.live[j] != 0;
-                        if (take)
-                            cp16(dst, a.w2t + (size_t)a.idx[j] * a.d + col0 + mc * 8);
+                        if (kv[q] >= 0)
+                            cp16(dst, a.w2t + (size_t)kv[q] * a.d + col0 + mc * 8);
                         else
                             *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
                     }
@@ -566,10 +845,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fc2_tc(TcFc2Args a) {
                     } else {
                         for (int c = t; c < nrow * a.B; c += kLoaders) cp4(raw + 4 * c, hsrc + c);
                     }
+                    if (fq < total) copy_ids();  // ids of stage it + LAG + 1
                 }
                 cp_commit();
                 if (it >= C::LAG) cp_wait<C::LAG>();
-                // every loader's copies of stage it - LAG have landed; stop together
+                // every loader's copies of stage it - LAG (and the ids of stage
+                // it + 1) have landed; stop together
                 if (loaders_sync_any(!good || *(volatile int*)&abort_flag)) {
                     ok = false;
                     break;
@@ -661,32 +942,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fc2_tc(TcFc2Args a) {
 }
 
 // y[t, c] = b2[c] + sum over the CTAs whose range touches column tile c / 128
-// of their partial (ascending CTA order: reproducible).
-__global__ void __launch_bounds__(256) k_fc2_tc_reduce(const float* __restrict__ part, int slots, int G,
-                                                       const int32_t* __restrict__ count, int B, int NT, int d,
-                                                       const __half* __restrict__ b2, float* __restrict__ y) {
-    const int e = blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= B * d) return;
-    const int t = e / d, c = e - t * d;
-    float acc = __half2float(b2[c]);
+// of their partial (ascending CTA order: reproducible).  Block: the 128
+// columns of one tile x 8 tokens.
+__global__ void __launch_bounds__(1024) k_fc2_tc_reduce(const float* __restrict__ part, int slots, int G,
+                                                        const int32_t* __restrict__ count, int B, int NT, int d,
+                                                        const __half* __restrict__ b2, float* __restrict__ y) {
+    __shared__ int slot[kMaxCtas];
+    __shared__ int rng[2];
+    const int ct = blockIdx.x;
+    const int m = threadIdx.x & 127, t = blockIdx.y * 8 + (threadIdx.x >> 7);
     const int n = *count;
-    if (n > 0) {
-        const int nct = d / 128, ct = c / 128, m = c % 128;
-        const long long U = (long long)nct * n;
-        const long long lo = (long long)ct * n, hi = lo + n;
-        long long gs = lo * G / U;
-        int gg = (int)gs;
-        while (gg > 0 && U * gg / G > lo) --gg;          // u0(gg) <= lo
-        while (gg < G && U * (gg + 1) / G <= lo) ++gg;   // first range reaching past lo
-        for (; gg < G; ++gg) {
-            const long long u0 = U * gg / G, u1 = U * (gg + 1) / G;
-            if (u0 >= hi) break;
-            if (u0 >= u1) continue;
-            const int slot = ct - (int)(u0 / n);
-            if (slot < slots) acc += part[(((size_t)gg * slots + slot) * NT + t) * 128 + m];
-        }
+    const int c = ct * 128 + m;
+    if (n == 0) {  // uniform over the block
+        if (t < B) y[(size_t)t * d + c] = __half2float(b2[c]);
+        return;
     }
-    y[e] = acc;
+    cover_setup((long long)(d / 128) * n, G, n, ct, slot, rng);
+    __syncthreads();
+    if (t >= B) return;
+    y[(size_t)t * d + c] = __half2float(b2[c]) + sum_cover(part, slot, rng, slots, NT, t, m);
 }
 
 template <typename K>
@@ -698,60 +972,147 @@ constexpr long long kTcTimeoutNs = 2000000000ll;
 
 }  // namespace
 
-bool tc_supported(const Plan& p) { return !p.int4 && p.B >= 16 && p.B <= 32 && p.d % 128 == 0; }
+namespace {
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+int slots_for(int tiles, int G) { return ceil_div(tiles, G) + 2; }
+// CTAs of the u = P1 x split.  P1 is small: at least 8 K-chunks per CTA keeps
+// the number of partials per u element (the finish kernel's fan-in) low.
+int u_grid(const Plan& p) {
+    const int units = ceil_div(p.r, 128) * ceil_div(p.d, 64);
+    const int G = p.nsm > 0 ? p.nsm : 1;
+    return units / 8 < 1 ? 1 : (units / 8 < G ? units / 8 : G);
+}
+}  // namespace
+
+bool tc_supported(const Plan& p) {
+    return !p.int4 && p.B >= 16 && p.B <= 32 && p.d % 128 == 0 && p.nsm <= kMaxCtas;
+}
 
 int tc_tokens(const Plan& p) { return p.B <= 16 ? 16 : 32; }
 
-int tc_slots(const Plan& p) { return (p.d / 128) / (p.nsm > 0 ? p.nsm : 1) + 2; }
+size_t tc_part_floats(const Plan& p) {
+    const size_t G = p.nsm > 0 ? p.nsm : 1, nt = tc_tokens(p);
+    const size_t fc1 = G * slots_for(ceil_div(p.F, 128), (int)G) * (p.gated ? 2 : 1) * nt * 128;
+    const size_t fc2 = G * slots_for(p.d / 128, (int)G) * nt * 128;
+    const size_t pu = (size_t)u_grid(p) * slots_for(ceil_div(p.r, 128), u_grid(p)) * nt * 128;
+    size_t m = fc1 > fc2 ? fc1 : fc2;
+    return m > pu ? m : pu;
+}
 
-size_t tc_part_floats(const Plan& p) { return (size_t)p.nsm * tc_slots(p) * tc_tokens(p) * 128; }
+size_t tc_uhl_bytes(const Plan& p) { return (size_t)2 * tc_tokens(p) * p.r * sizeof(__half); }
 
-cudaError_t launch_fc1_tc(const Plan& p, const __half* x, const LayerPtrs& w, const int32_t* idx,
-                          const int32_t* count, const uint32_t* mask, float* h, uint8_t* live, cudaStream_t s) {
+namespace {
+
+template <int MODE, int NT>
+cudaError_t launch_rows(const TcRowsArgs& a, int grid, cudaStream_t s) {
+    using C = RowsCfg<MODE, NT>;
+    cudaError_t e = prep(k_rows_tc<MODE, NT>, C::SMEM);
+    if (e != cudaSuccess) return e;
+    k_rows_tc<MODE, NT><<<grid, kTcThreads, C::SMEM, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_rows_nt(const TcRowsArgs& a, int nt, int grid, cudaStream_t s) {
+    return nt == 16 ? launch_rows<MODE, 16>(a, grid, s) : launch_rows<MODE, 32>(a, grid, s);
+}
+
+}  // namespace
+
+cudaError_t launch_predict_tc(const Plan& p, const __half* x, const __half* p1, const __half* p2,
+                              const __half* bpred, float tau, uint32_t* mask, float* part, __half* uhl,
+                              cudaStream_t s) {
     int* status = status_word();
     if (status == nullptr) return cudaErrorInvalidDevice;
-    TcFc1Args a{x, static_cast<const __half*>(w.w1), w.wu, w.b1, idx, count, mask, h, live, status, kTcTimeoutNs,
-                p.B, p.d, p.W};
-    const int grid = p.nsm;
-#define PI_FC1TC(GV, NV)                                                          \
-    {                                                                             \
-        cudaError_t e = prep(k_fc1_tc<GV, NV>, Fc1Cfg<GV, NV>::SMEM);            \
-        if (e != cudaSuccess) return e;                                           \
-        k_fc1_tc<GV, NV><<<grid, kTcThreads, Fc1Cfg<GV, NV>::SMEM, s>>>(a);        \
-        return cudaGetLastError();                                                \
-    }
-    const int nt = tc_tokens(p);
-    if (p.gated) {
-        if (nt == 16) PI_FC1TC(true, 16)
-        PI_FC1TC(true, 32)
-    }
-    if (nt == 16) PI_FC1TC(false, 16)
-    PI_FC1TC(false, 32)
-#undef PI_FC1TC
+    const int G = p.nsm, nt = tc_tokens(p);
+    // u = P1 x (stream-K over (r tiles x d chunks)), finished into fp16 hi | lo rows
+    const int Gu = u_grid(p);
+    TcRowsArgs a{};
+    a.a0 = p1;
+    a.R = p.r;
+    a.bop = x;
+    a.bop_rows = p.B;
+    a.K = p.d;
+    a.B = p.B;
+    a.part = part;
+    a.slots = slots_for(ceil_div(p.r, 128), Gu);
+    a.status = status;
+    a.timeout_ns = kTcTimeoutNs;
+    cudaError_t e = launch_rows_nt<2>(a, nt, Gu, s);
+    if (e != cudaSuccess) return e;
+    k_u_finish<<<ceil_div(p.r, 32), 32 * nt, 0, s>>>(part, a.slots, Gu, ceil_div(p.d, 64), p.r, p.B, nt, uhl);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // s = P2 u + b > tau over whole 128-row tiles, mask words by ballot
+    TcRowsArgs b{};
+    b.a0 = p2;
+    b.R = p.F;
+    b.bop = uhl;
+    b.bop_rows = 2 * nt;
+    b.K = p.r;
+    b.B = p.B;
+    b.bias = bpred;
+    b.tau = tau;
+    b.mask = mask;
+    b.W = p.W;
+    b.status = status;
+    b.timeout_ns = kTcTimeoutNs;
+    return launch_rows_nt<3>(b, nt, G, s);
+}
+
+cudaError_t launch_fc1_tc(const Plan& p, const __half* x, const LayerPtrs& w, const int32_t* idx,
+                          const int32_t* count, const uint32_t* mask, float* part, float* h, int32_t* live,
+                          cudaStream_t s) {
+    int* status = status_word();
+    if (status == nullptr) return cudaErrorInvalidDevice;
+    const int G = p.nsm, nt = tc_tokens(p);
+    TcRowsArgs a{};
+    a.a0 = static_cast<const __half*>(w.w1);
+    a.a1 = w.wu;
+    a.idx = idx;
+    a.count = count;
+    a.bop = x;
+    a.bop_rows = p.B;
+    a.K = p.d;
+    a.B = p.B;
+    a.part = part;
+    a.slots = slots_for(ceil_div(p.F, 128), G);
+    a.status = status;
+    a.timeout_ns = kTcTimeoutNs;
+    cudaError_t e = p.gated ? launch_rows_nt<1>(a, nt, G, s) : launch_rows_nt<0>(a, nt, G, s);
+    if (e != cudaSuccess) return e;
+    const int blocks = ceil_div(p.F, 32);
+    if (p.gated)
+        k_fc1_finish<true><<<blocks, 32 * p.B, 0, s>>>(part, a.slots, G, ceil_div(p.d, 64), count, p.B, nt, idx, w.b1,
+                                                   mask, p.W, h, live);
+    else
+        k_fc1_finish<false><<<blocks, 32 * p.B, 0, s>>>(part, a.slots, G, ceil_div(p.d, 64), count, p.B, nt, idx, w.b1,
+                                                    mask, p.W, h, live);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_fc2_tc(const Plan& p, const float* h, const int32_t* idx, const int32_t* count,
-                          const LayerPtrs& w, const uint8_t* live, float* partial, float* y, cudaStream_t s) {
+                          const LayerPtrs& w, const int32_t* live, float* partial, float* y, cudaStream_t s) {
     int* status = status_word();
     if (status == nullptr) return cudaErrorInvalidDevice;
-    const int slots = tc_slots(p), nt = tc_tokens(p);
+    const int G = p.nsm, nt = tc_tokens(p);
+    const int slots = slots_for(p.d / 128, G);
     TcFc2Args a{h, idx, count, static_cast<const __half*>(w.w2t), live, partial, status, kTcTimeoutNs,
                 p.B, p.d, slots};
-    const int grid = p.nsm;
     cudaError_t e;
     if (nt == 16) {
         e = prep(k_fc2_tc<16>, Fc2Cfg<16>::SMEM);
         if (e != cudaSuccess) return e;
-        k_fc2_tc<16><<<grid, kTcThreads, Fc2Cfg<16>::SMEM, s>>>(a);
+        k_fc2_tc<16><<<G, kTcThreads, Fc2Cfg<16>::SMEM, s>>>(a);
     } else {
         e = prep(k_fc2_tc<32>, Fc2Cfg<32>::SMEM);
         if (e != cudaSuccess) return e;
-        k_fc2_tc<32><<<grid, kTcThreads, Fc2Cfg<32>::SMEM, s>>>(a);
+        k_fc2_tc<32><<<G, kTcThreads, Fc2Cfg<32>::SMEM, s>>>(a);
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const int total = p.B * p.d;
-    k_fc2_tc_reduce<<<(total + 255) / 256, 256, 0, s>>>(partial, slots, grid, count, p.B, nt, p.d, w.b2, y);
+    k_fc2_tc_reduce<<<dim3(p.d / 128, ceil_div(p.B, 8)), 1024, 0, s>>>(partial, slots, G, count, p.B, nt, p.d,
+                                                                        w.b2, y);
     return cudaGetLastError();
 }
 

@@ -96,7 +96,7 @@ typedef struct {
     const int32_t *table;    /* [F] storage row -> original neuron id                      */
 } pi_layer_weights;
 
-/* Bytes of workspace pi_predict, pi_sparse_fc2 and pi_ffn_layer need for
+/* Bytes of workspace pi_predict, pi_sparse_fc1, pi_sparse_fc2 and pi_ffn_layer need for
  * `desc` (0 if the descriptor is invalid). */
 PI_API size_t pi_workspace_bytes(const pi_layer_desc *desc);
 
@@ -105,6 +105,9 @@ PI_API size_t pi_workspace_bytes(const pi_layer_desc *desc);
  *   u_b = P1 x_b (fp32), s_b = P2 u_b + bpred (fp32), mask_b bit k = s_bk > tau.
  * x: [B, d] fp16.  mask: [B, ceil(F/32)] uint32 (bits past F are 0).
  * workspace: >= pi_workspace_bytes(desc) bytes, 16-byte aligned.
+ * For 16 <= B <= 32, fp16 weights, d % 128 == 0 and rank % 16 == 0 both
+ * products run on the tcgen05 tensor cores; u enters P2 u as two fp16 halves
+ * hi = fp16(u), lo = fp16(u - hi), which keeps fp32 accuracy.
  */
 PI_API pi_status pi_predict(const pi_layer_desc *desc, const pi_half *x, const pi_half *p1,
                      const pi_half *p2, const pi_half *bpred, float tau, uint32_t *mask,
@@ -130,10 +133,12 @@ PI_API pi_status pi_compact(const pi_layer_desc *desc, const uint32_t *mask, con
  * For 16 <= B <= 32, fp16 weights and d % 128 == 0 the rows are gathered once
  * for all B tokens and multiplied on the tcgen05 tensor cores (fp16 x fp16
  * products, fp32 accumulation); otherwise CUDA cores in chunks of <= 8 tokens.
+ * workspace: >= pi_workspace_bytes(desc) bytes, 16-byte aligned (partial
+ * sums of the tensor-core split).
  */
 PI_API pi_status pi_sparse_fc1(const pi_layer_desc *desc, const pi_half *x, const pi_layer_weights *w,
                         const int32_t *idx, const int32_t *d_count, const uint32_t *mask,
-                        float *h, void *stream);
+                        float *h, void *workspace, size_t ws_bytes, void *stream);
 
 /*
  * FC2 as a gather-accumulate over W2t rows (section "Background"; section

@@ -162,7 +162,7 @@ def test_fc1_fc2_parity(kind, cfg, batch):
     assert n > 0
     h = torch.full((w.F * batch,), float("nan"), dtype=torch.float32, device=DEV)
     wsx = P.weights_struct(w)
-    P.pi_sparse_fc1(desc, x, wsx, idx, cnt, mask if batch > 1 else None, h)
+    P.pi_sparse_fc1(desc, x, wsx, idx, cnt, mask if batch > 1 else None, h, ws)
     y = torch.empty(batch, w.d, dtype=torch.float32, device=DEV)
     P.pi_sparse_fc2(desc, h, idx, cnt, wsx, y, ws)
     torch.cuda.synchronize()

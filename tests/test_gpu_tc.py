@@ -52,7 +52,7 @@ def _check_fc(P, w, wh, x, desc, ws, mask, idx, cnt, batch, what, sample=None):
     assert n > 0
     h = torch.full((w.F * batch,), float("nan"), dtype=torch.float32, device=DEV)
     wsx = P.weights_struct(w)
-    P.pi_sparse_fc1(desc, x, wsx, idx, cnt, mask, h)
+    P.pi_sparse_fc1(desc, x, wsx, idx, cnt, mask, h, ws)
     y = torch.empty(batch, w.d, dtype=torch.float32, device=DEV)
     P.pi_sparse_fc2(desc, h, idx, cnt, wsx, y, ws)
     torch.cuda.synchronize()
@@ -80,6 +80,35 @@ def test_tc_fc1_fc2_parity(kind, cfg, batch):
     ws = _ws(P, desc)
     mask, idx, cnt = _masks(P, w, cfg, x, desc, ws, batch)
     _check_fc(P, w, wh, x, desc, ws, mask, idx, cnt, batch, f"{kind} B={batch}")
+
+
+PRED_CASES = [
+    ("r32", small(CONFIGS["c1"], d=256, F=1000, rank=32)),          # K shorter than one 64-chunk
+    ("r96-F4099", small(CONFIGS["c3"], d=1024, F=4099, rank=96)),   # ragged K chunk, ragged last tile/word
+    ("r512", small(CONFIGS["c3"], d=2048, F=20000, rank=512)),      # several u tiles, many s tiles per CTA
+]
+
+
+@pytest.mark.parametrize("name,cfg", PRED_CASES, ids=[c[0] for c in PRED_CASES])
+@pytest.mark.parametrize("batch", [16, 29, 32])
+def test_tc_predict_parity(name, cfg, batch):
+    """Masks of the tensor-core predictor equal the oracle's outside the guard
+    band, for every token; bits past F stay 0."""
+    P = _pi()
+    w = make_layer(cfg, 0, device=DEV)
+    wh = oracle.host_layer(w.to("cpu"))
+    x = make_tokens(cfg, 0, batch, device=DEV)
+    desc = P.layer_desc(w, batch)
+    ws = _ws(P, desc)
+    W = (w.F + 31) // 32
+    mask = torch.full((batch, W), -1, dtype=torch.int32, device=DEV)
+    P.pi_predict(desc, x, w.p1, w.p2, w.b1, cfg.tau, mask, ws)
+    torch.cuda.synchronize()
+    mk = mask.cpu().numpy().view(np.uint32)
+    amb = 0
+    for b in range(batch):
+        amb += mask_matches(mk[b], oracle.predict(x[b].cpu(), wh, cfg.tau), w.F, cfg.tau, f"{name} token {b}")
+    assert amb <= batch
 
 
 def test_tc_many_tiles_per_cta():
@@ -140,7 +169,7 @@ def test_tc_empty_union():
     y = torch.full((batch, w.d), float("nan"), dtype=torch.float32, device=DEV)
     wsx = P.weights_struct(w)
     x = make_tokens(cfg, 0, batch, device=DEV)
-    P.pi_sparse_fc1(desc, x, wsx, idx, cnt, None, h)
+    P.pi_sparse_fc1(desc, x, wsx, idx, cnt, None, h, ws)
     P.pi_sparse_fc2(desc, h, idx, cnt, wsx, y, ws)
     torch.cuda.synchronize()
     b2 = w.b2.float().cpu().numpy()

@@ -27,7 +27,7 @@ def _case(P, cfg, batch, token0):
     P.pi_compact(desc, mask, None, idx, None, cnt)
     h = torch.zeros(w.F * batch, dtype=torch.float32, device=DEV)
     wsx = P.weights_struct(w)
-    P.pi_sparse_fc1(desc, x, wsx, idx, cnt, mask if batch > 1 else None, h)
+    P.pi_sparse_fc1(desc, x, wsx, idx, cnt, mask if batch > 1 else None, h, ws)
     y_ref = torch.empty(batch, w.d, dtype=torch.float32, device=DEV)
     P.pi_sparse_fc2(desc, h, idx, cnt, wsx, y_ref, ws)
     return w, desc, wsx, h, idx, cnt, y_ref
