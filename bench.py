@@ -45,6 +45,27 @@ def _cores():
         return os.cpu_count() or 1
 
 
+# ------------------------------------------------------------------ ranks
+
+def max_over_ranks(value: float, device: str = "cuda") -> float:
+    """The largest `value` over all ranks (the slowest rank bounds the job);
+    the value itself with one process."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(ms_max: float, steps: int, batch: int, world: int) -> float:
+    """Whole-job tokens/s: every rank runs `steps` steps of `batch` tokens on
+    its own GPU (independent replicas, weak scaling); the job takes as long as
+    its slowest rank."""
+    return world * steps * batch / (ms_max / 1e3)
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -120,13 +141,14 @@ def layer_bytes(cfg, r, n_pred, n_relu, batch=1):
     return dict(predict=pred, fc1=fc1, fc2=fc2, small=small, total=pred + fc1 + fc2 + small)
 
 
-def measure_counts(st, tokens):
-    """Untimed pass: per token and layer, the predicted-active count and the
-    number of listed neurons with a non-zero FC1 output (one stack launch per
-    token, through pi_ffn_stack's layer_counts output)."""
+def measure_counts(st, tokens, B=1):
+    """Untimed pass: per step (B tokens) and layer, the predicted-active count
+    (the union of the B tokens' masks) and the number of listed neurons with a
+    non-zero FC1 output for some token (one stack launch per step, through
+    pi_ffn_stack's layer_counts output)."""
     out = []
-    for t in range(tokens.shape[0]):
-        cnt = st.step_counts(tokens[t:t + 1])
+    for t in range(0, tokens.shape[0], B):
+        cnt = st.step_counts(tokens[t:t + B])
         out.append([tuple(int(v) for v in row) for row in cnt.cpu().tolist()])
     return out
 
@@ -177,30 +199,32 @@ def run_ours(args):
     from synth import CONFIGS, make_layer, make_tokens
 
     cfg = CONFIGS[args.config]
-    B = 1
-    layers = [make_layer(cfg, l, device="cuda") for l in range(cfg.layers)]
-    T = cfg.tokens
+    B = args.batch
+    L = args.layers if args.layers else cfg.layers
+    layers = [make_layer(cfg, l, device="cuda") for l in range(L)]
+    NS = max(cfg.tokens // B, 4)          # distinct steps of B tokens, cycled
+    T = NS * B
     tokens = make_tokens(cfg, 0, T, device="cuda")
     st = DecodeStack(layers, batch=B, tau=cfg.tau, eps=cfg.rms_eps)
     weight_bytes = sum(w.nbytes() for w in layers)
 
-    # per-token algorithmic bytes (untimed)
-    counts = measure_counts(st, tokens)
-    per_tok = []
+    # per-step algorithmic bytes (untimed)
+    counts = measure_counts(st, tokens, B)
+    per_step = []
     for per in counts:
         tot = 0
         for l, (n, nz) in enumerate(per):
             tot += layer_bytes(cfg, layers[l].r, n, nz, B)["total"]
-        tot += (cfg.layers - 1) * B * (4 * cfg.d + 2 * cfg.d)   # inter-layer norm: read y, write x
-        per_tok.append(tot)
-    n_pred_mean = sum(n for per in counts for n, _ in per) / (T * cfg.layers)
-    n_relu_mean = sum(z for per in counts for _, z in per) / (T * cfg.layers)
+        tot += (L - 1) * B * (4 * cfg.d + 2 * cfg.d)   # inter-layer norm: read y, write x
+        per_step.append(tot)
+    n_pred_mean = sum(n for per in counts for n, _ in per) / (NS * L)
+    n_relu_mean = sum(z for per in counts for _, z in per) / (NS * L)
 
     st.capture()
     stream = torch.cuda.current_stream()
     K, W = args.steps, args.warmup
     for i in range(W):
-        st.x_in.copy_(tokens[i % T:i % T + 1])
+        st.x_in.copy_(tokens[(i % NS) * B:(i % NS + 1) * B])
         st.replay()
     torch.cuda.synchronize()
     if world > 1:
@@ -212,8 +236,8 @@ def run_ours(args):
         torch.cuda.synchronize()
         e0.record(stream)
         for i in range(K):
-            t = (W + i) % T
-            st.x_in.copy_(tokens[t:t + 1])
+            t = (W + i) % NS
+            st.x_in.copy_(tokens[t * B:(t + 1) * B])
             ka[i].record(stream)
             st.replay()
             kb[i].record(stream)
@@ -223,30 +247,31 @@ def run_ours(args):
     ms = e0.elapsed_time(e1)
     kernel_ms = sum(a.elapsed_time(b) for a, b in zip(ka, kb))
     if world > 1:
-        tt = torch.tensor([ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+        ms = max_over_ranks(ms, "cuda")
         dist.barrier()
-    step_bytes = sum(per_tok[(W + i) % T] for i in range(K)) / K
-    tok_s = world * K * B / (ms / 1e3)
+    step_bytes = sum(per_step[(W + i) % NS] for i in range(K)) / K
+    tok_s = job_throughput(ms, K, B, world)
     peak, peak_kind = _peaks()
 
-    # the dominant (and only) kernel of a step: one launch of the fused stack kernel
+    # batch 1: a step is one launch of the fused stack kernel (the dominant and
+    # only kernel); batch > 1: the per-step kernels of the graph, timed together
     per_launch = kernel_ms / K
     achieved = step_bytes / (per_launch / 1e3) / 1e9
-    traffic = recorded_traffic(cfg.key)
-    roofline = {"kernel": "k_fused_stack (pi_ffn_stack)", "bound": "hbm", "achieved": round(achieved, 1),
+    fused = st.launches_per_step() == 1
+    traffic = recorded_traffic(cfg.key) if fused and B == 1 and L == cfg.layers else None
+    roofline = {"kernel": "k_fused_stack (pi_ffn_stack)" if fused else "batched step (pi_ffn_stack graph)",
+                "bound": "hbm", "achieved": round(achieved, 1),
                 "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "traffic": traffic, "peak_kind": peak_kind, "bytes_per_launch": int(step_bytes),
                 "us_per_launch": round(per_launch * 1e3, 2), "share_of_step": round(kernel_ms / ms, 3)}
 
-    e2e = time_e2e(st, tokens, K=min(K, 512), W=W)
+    e2e = time_e2e(st, tokens, K=min(K, 512), W=W, B=B)
     out = {
         "metric": METRIC, "value": round(tok_s, 2), "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": round(ms / K, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"{cfg.key}: {cfg.name}, batch 1, {cfg.layers} layers per step",
-                   "batch": B, "layers": cfg.layers, "d": cfg.d, "ffn": cfg.F, "tokens_cycled": T,
+        "config": {"workload": f"{cfg.key}: {cfg.name}, batch {B}, {L} layers per step",
+                   "batch": B, "layers": L, "d": cfg.d, "ffn": cfg.F, "tokens_cycled": T,
                    "weights": "int4-g32" if cfg.int4 else "fp16",
                    "l2": f"inputs larger than L2 ({weight_bytes / 1e9:.1f} GB of layer weights per step)",
                    "parallelism": "replicas" if world > 1 else "single"},
@@ -268,16 +293,18 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def time_e2e(st, tokens, K, W):
-    """Through the public API with host buffers: per step, copy the token from
-    pinned host memory, run the step, copy y back and read it on the host."""
+def time_e2e(st, tokens, K, W, B=1):
+    """Through the public API with host buffers: per step, copy the step's B
+    tokens from pinned host memory, run the step, copy y back and read it on
+    the host."""
     import torch
-    T = tokens.shape[0]
+    NS = tokens.shape[0] // B
     host_x = tokens.cpu().pin_memory()
     host_y = torch.empty(st.y.shape, dtype=st.y.dtype).pin_memory()
     stream = torch.cuda.current_stream()
     for i in range(W):
-        st.x_in.copy_(host_x[i % T:i % T + 1], non_blocking=True)
+        t = i % NS
+        st.x_in.copy_(host_x[t * B:(t + 1) * B], non_blocking=True)
         st.replay()
         host_y.copy_(st.y, non_blocking=True)
         stream.synchronize()
@@ -285,7 +312,8 @@ def time_e2e(st, tokens, K, W):
     acc = 0.0
     e0.record(stream)
     for i in range(K):
-        st.x_in.copy_(host_x[i % T:i % T + 1], non_blocking=True)
+        t = i % NS
+        st.x_in.copy_(host_x[t * B:(t + 1) * B], non_blocking=True)
         st.replay()
         host_y.copy_(st.y, non_blocking=True)
         stream.synchronize()
@@ -293,8 +321,8 @@ def time_e2e(st, tokens, K, W):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
-    return {"value": round(K / (ms / 1e3), 2), "unit": "tokens/s",
-            "h2d_bytes_per_step": int(host_x[0:1].numel() * 2), "d2h_bytes_per_step": int(host_y.numel() * 4)}
+    return {"value": round(K * B / (ms / 1e3), 2), "unit": "tokens/s",
+            "h2d_bytes_per_step": int(host_x[0:B].numel() * 2), "d2h_bytes_per_step": int(host_y.numel() * 4)}
 
 
 def cpu_baseline(cfg, layers, st, tokens, budget_s=15.0):
@@ -304,14 +332,17 @@ def cpu_baseline(cfg, layers, st, tokens, budget_s=15.0):
     import oracle
     cores = _cores()
     oracle.set_threads(cores)
-    L = cfg.layers
+    L = len(layers)
+    B = st.batch
+    NS = tokens.shape[0] // B
     sample_layers = sorted({0, 1, L // 2, L - 1}) if L > 1 else [0]
     hosts = {l: oracle.host_layer(layers[l].to("cpu")) for l in sample_layers}
     times = []
     t_start = time.perf_counter()
     t = 0
     while True:
-        xs, _ = st.step_trace(tokens[t % tokens.shape[0]:t % tokens.shape[0] + 1])
+        k = t % NS  # the first token of each step is evaluated
+        xs, _ = st.step_trace(tokens[k * B:(k + 1) * B])
         for l in sample_layers:
             x = xs[l][0].cpu()
             t0 = time.perf_counter()
@@ -385,6 +416,8 @@ def main():
     ap.add_argument("--steps", type=int, default=4096)
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--config", default="c2")
+    ap.add_argument("--batch", type=int, default=1, help="tokens per step (the headline workload is 1)")
+    ap.add_argument("--layers", type=int, default=0, help="layers of the stack (0: the workload's own)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0)
