@@ -38,6 +38,7 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBarriersPerLayer = 4;
+constexpr int kRingMax = 8;   // P2 ring slots at most
 
 PI_DEV unsigned long long globaltimer() {
     unsigned long long t;
@@ -168,6 +169,8 @@ struct FusedParams {
     int pred_smem;              // 1: each CTA's predictor slice is bulk-copied to shared memory
     int p1s_bytes, p2s_bytes, b1s_bytes;  // capacities of the shared predictor buffers
     int stage_bytes;            // shared staging region (predictor slices, then this CTA's FC rows)
+    int ring_slots;             // without pred_smem: P2 units stream through this many slots of
+    int ring_unit;              // ring_unit bytes (16 rows of the largest rank) in the staging region
     FusedLayer layers[kMaxFusedLayers];
 };
 
@@ -297,11 +300,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
     __shared__ __align__(8) unsigned long long pred_mbar;
     __shared__ __align__(8) unsigned long long w1_mbar;   // staged FC1 rows
     __shared__ __align__(8) unsigned long long w2_mbar;   // staged W2t rows
+    __shared__ __align__(8) unsigned long long ring_full[kRingMax];   // P2 unit ring
+    __shared__ int ring_uses[kRingMax];                                // copies issued per slot
+    const int ns = p.ring_slots;
     if (tid == 0) {
         bad = 0;
         mbar_init(&pred_mbar, 1);
         mbar_init(&w1_mbar, 1);
         mbar_init(&w2_mbar, 1);
+        for (int q = 0; q < kRingMax; ++q) {
+            mbar_init(&ring_full[q], 1);
+            ring_uses[q] = 0;
+        }
     }
     unsigned w2_uses = 0;   // completed-or-pending phases of w1_mbar and w2_mbar (used in pairs)
     bool w1_pending = false, w2_pending = false;
@@ -319,6 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
     int inflight = -1;   // layer whose predictor copy is issued but not yet waited for
     auto leave = [&]() {
         if (inflight >= 0) mbar_drain(&pred_mbar, (unsigned)(inflight & 1), tmo);
+        for (int q = 0; q < ns; ++q)
+            if (ring_uses[q] > 0) mbar_drain(&ring_full[q], (unsigned)((ring_uses[q] - 1) & 1), tmo);
         if (w1_pending) mbar_drain(&w1_mbar, (w2_uses - 1) & 1u, tmo);
         if (w2_pending) mbar_drain(&w2_mbar, (w2_uses - 1) & 1u, tmo);
         if (c == 0 && tid == 0) {
@@ -359,10 +371,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
         if (b_p2) bulk_g2s(p2s, ly.p2 + (size_t)row0 * ly.r, b_p2, &pred_mbar);
         if (b_b1) bulk_g2s(b1s, ly.b1 + row0, b_b1, &pred_mbar);
     };
+    // P2 ring (no shared predictor slices): unit k of this CTA's range goes to
+    // slot k % ns; issued by one thread (the first ns units of a layer by thread
+    // 0, later ones by the warp that owns the slot), which counts the slot's uses.
+    const int nunits = um1 - um0;
+    auto issue_unit = [&](const FusedLayer& ly, int k) {
+        const int q = k % ns;
+        const int rb = row0 + 16 * k;
+        const int rows = min(16, row1 - rb);
+        const unsigned bytes = (unsigned)(2 * rows * ly.r);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive_expect_tx(&ring_full[q], bytes);
+        bulk_g2s(stage + (size_t)q * p.ring_unit, ly.p2 + (size_t)rb * ly.r, bytes, &ring_full[q]);
+        ring_uses[q] += 1;
+    };
+    // uses of slot q in one layer (every layer has the same units)
+    auto ring_per_layer = [&](int q) { return nunits > q ? (nunits - 1 - q) / ns + 1 : 0; };
     __syncthreads();
     if (p.pred_smem) {
         if (tid == 0) issue_predictor(0);
         inflight = 0;
+    } else if (ns > 0 && tid == 0) {
+        for (int k = 0; k < ns && k < nunits; ++k) issue_unit(p.layers[0], k);
     }
 
     // phase-D columns of this CTA: a contiguous range of 4-column groups
@@ -376,10 +406,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
         // layer l's predictor slices are consumed by then (phase B ended with a
         // barrier): bring in layer l+1's once this CTA's FC rows are loaded
         auto issue_next = [&]() {
-            if (p.pred_smem && l + 1 < p.L) {
+            if (l + 1 < p.L && (p.pred_smem || ns > 0)) {
                 __syncthreads();   // the region may still hold this CTA's staged FC rows
-                if (tid == 0) issue_predictor(l + 1);
-                inflight = l + 1;
+                if (p.pred_smem) {
+                    if (tid == 0) issue_predictor(l + 1);
+                    inflight = l + 1;
+                } else if (tid == 0) {
+                    for (int k = 0; k < ns && k < nunits; ++k) issue_unit(p.layers[l + 1], k);
+                }
             }
         };
         PI_STAMP(l, 0);
@@ -470,8 +504,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
             // vectors L, L+32, ... with u; a halving butterfly then leaves the
             // full dot product of row (L >> 1) in lanes L (16 shuffles for 16
             // rows), and one ballot forms the unit's 16 mask bits.
-            for (int m = um0 + warp; m < um1; m += kWarps) {
+            // With the P2 ring, warp q < ns owns slot q and takes units q, q+ns,
+            // ...: each slot's copies are waited for, read and refilled in
+            // order by one warp, so a wait never sees an older phase of its slot.
+            const int mstep = ns > 0 ? ns : kWarps;
+            const bool unit_warp = ns == 0 || warp < ns;
+            for (int m = um0 + warp; unit_warp && m < um1; m += mstep) {
                 const int rbase = m * 16;
+                const __half* p2r = nullptr;   // this unit's rows in the ring
+                if (ns > 0) {
+                    const int k = m - um0;     // k % ns == warp
+                    if (!mbar_wait(&ring_full[warp], (unsigned)((l * ring_per_layer(warp) + k / ns) & 1), tmo, &bad))
+                        break;
+                    p2r = reinterpret_cast<const __half*>(stage + (size_t)warp * p.ring_unit);
+                }
                 float v[16];
 #pragma unroll
                 for (int k = 0; k < 16; ++k) v[k] = 0.f;
@@ -496,6 +542,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                             const int row = min(rbase + 8 * h + k, F - 1);
                             w[k] = p.pred_smem
                                        ? *reinterpret_cast<const uint4*>(p2s + (size_t)(row - row0) * r + vc * 8)
+                                   : p2r != nullptr
+                                       ? *reinterpret_cast<const uint4*>(p2r + (size_t)(row - rbase) * r + vc * 8)
                                        : ld_stream16(ly.p2 + (size_t)row * r + vc * 8);
                         }
 #pragma unroll
@@ -548,6 +596,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                     pred = v[0] + bk > p.tau;
                 }
                 const unsigned bal = __ballot_sync(FULL, pred);
+                // the unit's slot is read: refill it with unit k + ns of this layer
+                if (ns > 0 && lane == 0 && m - um0 + ns < nunits) issue_unit(ly, m - um0 + ns);
                 if (lane == 0) {
                     unsigned bits = 0;
                     // the bit of row kk(L) sits at ballot position L (even lanes)
@@ -1101,6 +1151,13 @@ cudaError_t launch_fused(const FusedStackArgs& a, cudaStream_t s) {
         const int st = tma_ok ? (int)(room / 16 * 16) : pred;
         sp.stage = st > pred ? st : pred;
         prm.stage_bytes = tma_ok ? sp.stage : 0;
+        // predictor slices too large for shared memory: stream P2 in 16-row units
+        const int unit = 16 * rmax * 2;
+        const int slots = prm.stage_bytes / unit;
+        if (!prm.pred_smem && slots >= 2) {
+            prm.ring_slots = slots < kRingMax ? slots : kRingMax;
+            prm.ring_unit = unit;
+        }
     }
     const size_t smem = sp.bytes();
     if (smem > 227 * 1024) return cudaErrorInvalidValue;
