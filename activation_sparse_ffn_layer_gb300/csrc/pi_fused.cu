@@ -175,8 +175,10 @@ struct FusedParams {
 };
 
 // Dynamic smem layout (bytes): xf float[d] | u float[rmax] | ustage float[usmax]
-//   | m16 int[M] | upre int[M+1] | lidx int[cap] | lh float[cap] | scratch
+//   | scratch | m16 int[M] | upre int[M+1] | lidx int[cap] | lh float[cap]
 //   | P1 slice | P2 slice | bias slice   (the last three only with pred_smem)
+// The mask and active-list buffers (m16 .. lh) are live only in phase C before
+// FC2 ends, so the P2 ring may span them together with the staging region.
 struct SmemPlan {
     int d, rmax, usmax, M, cap;
     int p1s = 0, p2s = 0, b1s = 0;  // shared predictor buffers (bytes, 16-aligned), 0 if unused
@@ -184,12 +186,12 @@ struct SmemPlan {
                                     // in phases A-B, this CTA's FC rows in phase C
     __host__ __device__ int off_u() const { return d * 4; }
     __host__ __device__ int off_ust() const { return off_u() + rmax * 4; }
-    __host__ __device__ int off_m16() const { return off_ust() + ((usmax + 3) / 4) * 16; }
+    __host__ __device__ int off_scr() const { return ((off_ust() + ((usmax + 3) / 4) * 16 + 15) / 16) * 16; }
+    __host__ __device__ int off_m16() const { return off_scr() + 4096 * 4; }
     __host__ __device__ int off_upre() const { return off_m16() + ((M + 1) / 2) * 8; }
     __host__ __device__ int off_lidx() const { return off_upre() + (M + 1) * 4; }
     __host__ __device__ int off_lh() const { return off_lidx() + cap * 4; }
-    __host__ __device__ int off_scr() const { return ((off_lh() + cap * 4 + 15) / 16) * 16; }
-    __host__ __device__ int off_stage() const { return off_scr() + 4096 * 4; }
+    __host__ __device__ int off_stage() const { return ((off_lh() + cap * 4 + 15) / 16) * 16; }
     __host__ __device__ int off_p1s() const { return off_stage(); }
     __host__ __device__ int off_p2s() const { return off_p1s() + p1s; }
     __host__ __device__ int off_b1s() const { return off_p2s() + p2s; }
@@ -292,6 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
     __half* p2s = reinterpret_cast<__half*>(smem + sp.off_p2s());
     __half* b1s = reinterpret_cast<__half*>(smem + sp.off_b1s());
     unsigned char* stage = smem + sp.off_stage();
+    unsigned char* ring = smem + sp.off_m16();   // P2 ring (phase B; spans m16 .. stage)
     // bytes of one staged weight row: fp16 row, or INT4 codes followed by the scales
     const int wrow = KIND == 2 ? d / 2 + d / 16 : 2 * d;
     const int fc1_rows = KIND == 1 ? 2 : 1;   // gate and up rows when gated
@@ -382,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
         const unsigned bytes = (unsigned)(2 * rows * ly.r);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         mbar_arrive_expect_tx(&ring_full[q], bytes);
-        bulk_g2s(stage + (size_t)q * p.ring_unit, ly.p2 + (size_t)rb * ly.r, bytes, &ring_full[q]);
+        bulk_g2s(ring + (size_t)q * p.ring_unit, ly.p2 + (size_t)rb * ly.r, bytes, &ring_full[q]);
         ring_uses[q] += 1;
     };
     // uses of slot q in one layer (every layer has the same units)
@@ -516,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                     const int k = m - um0;     // k % ns == warp
                     if (!mbar_wait(&ring_full[warp], (unsigned)((l * ring_per_layer(warp) + k / ns) & 1), tmo, &bad))
                         break;
-                    p2r = reinterpret_cast<const __half*>(stage + (size_t)warp * p.ring_unit);
+                    p2r = reinterpret_cast<const __half*>(ring + (size_t)warp * p.ring_unit);
                 }
                 float v[16];
 #pragma unroll
@@ -1152,8 +1155,9 @@ cudaError_t launch_fused(const FusedStackArgs& a, cudaStream_t s) {
         sp.stage = st > pred ? st : pred;
         prm.stage_bytes = tma_ok ? sp.stage : 0;
         // predictor slices too large for shared memory: stream P2 in 16-row units
+        // through the mask/list buffers and the staging region
         const int unit = 16 * rmax * 2;
-        const int slots = prm.stage_bytes / unit;
+        const int slots = prm.stage_bytes > 0 ? (prm.stage_bytes + sp.off_stage() - sp.off_m16()) / unit : 0;
         if (!prm.pred_smem && slots >= 2) {
             prm.ring_slots = slots < kRingMax ? slots : kRingMax;
             prm.ring_unit = unit;
