@@ -71,7 +71,8 @@ bool make_plan(const pi_layer_desc& desc, Plan* p) {
     q.xchg_bytes = up(fused_workspace_bytes(q.d, q.F, q.rmax_su, q.nsm));
     q.fused = q.B == 1 && fused_supported(q.d, q.F, q.r, q.int4, q.nsm);
     q.tc = tc_supported(q);
-    q.part_floats = q.tc ? tc_part_floats(q) : (size_t)q.fc2_splits * q.B * q.d;
+    q.st = !q.tc && st_supported(q);
+    q.part_floats = q.tc ? tc_part_floats(q) : q.st ? st_part_floats(q) : (size_t)q.fc2_splits * q.B * q.d;
     size_t off = q.xchg_bytes;
     q.off_mask = off;  off = up(off + sizeof(uint32_t) * (size_t)q.B * q.W);
     q.off_idx = off;   off = up(off + sizeof(int32_t) * (size_t)q.F);
@@ -81,7 +82,7 @@ bool make_plan(const pi_layer_desc& desc, Plan* p) {
     q.off_part = off;  off = up(off + sizeof(float) * q.part_floats);
     q.off_xbuf = off;  off = up(off + sizeof(uint16_t) * 2 * (size_t)q.B * q.d);
     q.off_live = off;  off = up(off + sizeof(int32_t) * (size_t)q.F);
-    q.off_uhl = off;   off = up(off + (q.tc ? tc_uhl_bytes(q) : 0));
+    q.off_uhl = off;   off = up(off + (q.tc ? tc_uhl_bytes(q) : q.st ? st_u_bytes(q) : 0));
     q.total = off;
     *p = q;
     return true;
@@ -191,7 +192,8 @@ cudaError_t run_stack(const Plan& p, int n, const LayerPtrs* lp, const int* rank
         if (e == cudaSuccess)
             e = launch_fc1(q, cur, w, idx, cnt, q.B > 1 ? mask : nullptr, at<float>(ws, p.off_part), h, live, s);
         if (e == cudaSuccess && layer_counts) e = launch_count_active(q, cnt, h, layer_counts + 2 * l, s);
-        if (e == cudaSuccess) e = launch_fc2(q, h, idx, cnt, w, q.tc ? live : nullptr, at<float>(ws, p.off_part), y, s);
+        if (e == cudaSuccess)
+            e = launch_fc2(q, h, idx, cnt, w, (q.tc || q.st) ? live : nullptr, at<float>(ws, p.off_part), y, s);
         if (e != cudaSuccess) return e;
         if (l + 1 < n) {
             __half* nxt = x_trace ? x_trace + (size_t)l * p.B * p.d : xbuf + (size_t)(l % 2) * p.B * p.d;
@@ -325,6 +327,7 @@ int pi_launches_per_layer(const pi_layer_desc* desc) {
     // reduction (tcgen05 path: all tokens at once) or FC1 and FC2 per chunk + 1
     // tcgen05 path: predictor u + finish + s, compaction, FC1 + finish, FC2 + reduction
     if (p.tc && p.r % 16 == 0) return 3 + 1 + 2 + 2;
+    if (p.st) return 3 + 1 + 2 + 2;   // same structure on CUDA cores (plus a mask memset)
     if (p.tc) return 2 * chunks + 1 + 2 + 2;
     return 2 * chunks + 1 + chunks + chunks + 1;
 }

@@ -26,6 +26,7 @@ struct Plan {
     size_t xchg_bytes, rmax_su;
     bool fused;     // pi_ffn_layer / pi_ffn_stack take the fused persistent kernel
     bool tc;        // FC1 / FC2 take the tcgen05 batched path (batch 16..32, fp16 weights)
+    bool st;        // ... or the CUDA-core streamed batched path (batch 2..8, fp16 weights)
     size_t part_floats;  // FC2 partial sums of whichever FC2 path the plan takes
     size_t off_mask, off_idx, off_count, off_h, off_upart, off_part, off_xbuf, off_live, off_uhl, total;
 };
@@ -73,6 +74,28 @@ cudaError_t launch_fc1_tc(const Plan& p, const __half* x, const LayerPtrs& w, co
                           const int32_t* count, const uint32_t* mask, float* part, float* h, int32_t* live,
                           cudaStream_t s);
 cudaError_t launch_fc2_tc(const Plan& p, const float* h, const int32_t* idx, const int32_t* count,
+                          const LayerPtrs& w, const int32_t* live, float* partial, float* y, cudaStream_t s);
+
+// fixed-order finishing of the stream-K partials (shared by both batched paths):
+// nt = partial columns per token group, G = CTAs of the split, slots = tiles per CTA
+cudaError_t launch_fc1_finish(const Plan& p, int nt, int G, int slots, const float* part, const int32_t* count,
+                              const int32_t* idx, const __half* b1, const uint32_t* mask, float* h, int32_t* live,
+                              cudaStream_t s);
+cudaError_t launch_fc2_reduce(const Plan& p, int nt, int G, int slots, const float* part, const int32_t* count,
+                              const __half* b2, float* y, cudaStream_t s);
+
+// ---- CUDA-core streamed batched path (pi_stream.cu, batch 2..8, fp16 weights) ----
+bool st_supported(const Plan& p);
+int st_tokens(const Plan& p);          // token slots of the kernels: 2, 4 or 8
+size_t st_part_floats(const Plan& p);
+size_t st_u_bytes(const Plan& p);      // u as fp32 rows [B][r]
+cudaError_t launch_predict_st(const Plan& p, const __half* x, const __half* p1, const __half* p2,
+                              const __half* bpred, float tau, uint32_t* mask, float* part, float* u32,
+                              cudaStream_t s);
+cudaError_t launch_fc1_st(const Plan& p, const __half* x, const LayerPtrs& w, const int32_t* idx,
+                          const int32_t* count, const uint32_t* mask, float* part, float* h, int32_t* live,
+                          cudaStream_t s);
+cudaError_t launch_fc2_st(const Plan& p, const float* h, const int32_t* idx, const int32_t* count,
                           const LayerPtrs& w, const int32_t* live, float* partial, float* y, cudaStream_t s);
 
 // ---- fused persistent stack (batch 1) ----

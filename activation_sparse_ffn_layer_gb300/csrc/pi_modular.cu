@@ -453,6 +453,10 @@ cudaError_t launch_predict(const Plan& p, const __half* x, const __half* p1, con
         return launch_predict_tc(p, x, p1, p2, bpred, tau, mask,
                                  reinterpret_cast<float*>(static_cast<char*>(ws) + p.off_part),
                                  reinterpret_cast<__half*>(static_cast<char*>(ws) + p.off_uhl), s);
+    if (p.st)
+        return launch_predict_st(p, x, p1, p2, bpred, tau, mask,
+                                 reinterpret_cast<float*>(static_cast<char*>(ws) + p.off_part),
+                                 reinterpret_cast<float*>(static_cast<char*>(ws) + p.off_uhl), s);
     float* upart = reinterpret_cast<float*>(static_cast<char*>(ws) + p.off_upart);
     return for_token_chunks(p.B, [&](int b0, int tb) -> cudaError_t {
         dim3 gu((p.r + 7) / 8, p.u_splits);
@@ -488,6 +492,7 @@ cudaError_t launch_fc1(const Plan& p, const __half* x, const LayerPtrs& w, const
                        const int32_t* count, const uint32_t* mask, float* partial, float* h, int32_t* live,
                        cudaStream_t s) {
     if (p.tc) return launch_fc1_tc(p, x, w, idx, count, mask, partial, h, live, s);
+    if (p.st) return launch_fc1_st(p, x, w, idx, count, mask, partial, h, live, s);
     const int kind = p.int4 ? 2 : (p.gated ? 1 : 0);
     return for_token_chunks(p.B, [&](int b0, int tb) -> cudaError_t {
         const size_t sm = (size_t)tb * p.d * sizeof(__half);
@@ -512,6 +517,7 @@ cudaError_t launch_fc1(const Plan& p, const __half* x, const LayerPtrs& w, const
 cudaError_t launch_fc2(const Plan& p, const float* h, const int32_t* idx, const int32_t* count,
                        const LayerPtrs& w, const int32_t* live, float* partial, float* y, cudaStream_t s) {
     if (p.tc) return launch_fc2_tc(p, h, idx, count, w, live, partial, y, s);
+    if (p.st) return launch_fc2_st(p, h, idx, count, w, live, partial, y, s);
     cudaError_t e = for_token_chunks(p.B, [&](int b0, int tb) -> cudaError_t {
         dim3 grid(p.fc2_tiles, p.fc2_splits);
 #define PI_FC2(TBV, IV)                                                                       \

@@ -1,5 +1,6 @@
-"""Parity of the batched tcgen05 path (batch 16..32, fp16 weights) against the
-fp64 CPU oracle, through the C ABI.
+"""Parity of the streamed batched paths (fp16 weights: CUDA cores at batch
+2..8, tcgen05 tensor cores at batch 16..32) against the fp64 CPU oracle,
+through the C ABI.
 
 FC1 and FC2 are checked in isolation (same index list, same FC1 output fed to
 both sides) and as a whole layer, on shapes that exercise the work split:
@@ -70,7 +71,7 @@ def _check_fc(P, w, wh, x, desc, ws, mask, idx, cnt, batch, what, sample=None):
 
 
 @pytest.mark.parametrize("kind,cfg", CASES, ids=[c[0] for c in CASES])
-@pytest.mark.parametrize("batch", [16, 17, 24, 32])
+@pytest.mark.parametrize("batch", [2, 3, 5, 8, 16, 17, 24, 32])
 def test_tc_fc1_fc2_parity(kind, cfg, batch):
     P = _pi()
     w = make_layer(cfg, 0, device=DEV)
@@ -90,7 +91,7 @@ PRED_CASES = [
 
 
 @pytest.mark.parametrize("name,cfg", PRED_CASES, ids=[c[0] for c in PRED_CASES])
-@pytest.mark.parametrize("batch", [16, 29, 32])
+@pytest.mark.parametrize("batch", [2, 7, 16, 29, 32])
 def test_tc_predict_parity(name, cfg, batch):
     """Masks of the tensor-core predictor equal the oracle's outside the guard
     band, for every token; bits past F stay 0."""
@@ -111,7 +112,8 @@ def test_tc_predict_parity(name, cfg, batch):
     assert amb <= batch
 
 
-def test_tc_many_tiles_per_cta():
+@pytest.mark.parametrize("batch", [8, 32])
+def test_tc_many_tiles_per_cta(batch):
     """A union list long enough that every CTA runs three or more 128-row FC1
     tiles (both TMEM accumulator buffers reused) and that FC2 ranges cross
     column-tile boundaries."""
@@ -119,25 +121,24 @@ def test_tc_many_tiles_per_cta():
     cfg = small(CONFIGS["c1"], d=256, F=72000, rank=32, mean_rate=0.35)
     w = make_layer(cfg, 0, device=DEV)
     wh = w.to("cpu")
-    batch = 32
     x = make_tokens(cfg, 0, batch, device=DEV)
     desc = P.layer_desc(w, batch)
     ws = _ws(P, desc)
     mask, idx, cnt = _masks(P, w, cfg, x, desc, ws, batch)
     n = int(cnt.item())
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert n > 2 * 128 * sms, n
-    _check_fc(P, w, wh, x, desc, ws, mask, idx, cnt, batch, "many tiles", sample=[0, 13, 31])
+    assert n > (2 if batch >= 16 else 1) * 128 * sms, n   # more 128-row tiles than CTAs
+    _check_fc(P, w, wh, x, desc, ws, mask, idx, cnt, batch, "many tiles", sample=sorted({0, batch // 2, batch - 1}))
 
 
-def test_tc_tiny_union():
+@pytest.mark.parametrize("batch", [4, 16])
+def test_tc_tiny_union(batch):
     """Fewer listed rows than SMs: most CTAs get no rows (they must leave
     cleanly) and FC2 pieces are single rows."""
     P = _pi()
     cfg = small(CONFIGS["c1"], d=256, F=1000, rank=32)
     w = make_layer(cfg, 0, device=DEV)
     wh = w.to("cpu")
-    batch = 16
     x = make_tokens(cfg, 0, batch, device=DEV)
     desc = P.layer_desc(w, batch)
     ws = _ws(P, desc)
@@ -156,11 +157,11 @@ def test_tc_tiny_union():
     _check_fc(P, w, wh, x, desc, ws, mask, idx, cnt, batch, "tiny union")
 
 
-def test_tc_empty_union():
+@pytest.mark.parametrize("batch", [4, 16])
+def test_tc_empty_union(batch):
     P = _pi()
     cfg = small(CONFIGS["c1"], d=256, F=1000, rank=32)
     w = make_layer(cfg, 0, device=DEV)
-    batch = 16
     desc = P.layer_desc(w, batch)
     ws = _ws(P, desc)
     idx = torch.zeros(w.F, dtype=torch.int32, device=DEV)
@@ -177,13 +178,13 @@ def test_tc_empty_union():
 
 
 @pytest.mark.parametrize("kind,cfg", CASES, ids=[c[0] for c in CASES])
-def test_tc_layer_matches_oracle_and_batch1(kind, cfg):
-    """Whole layer at batch 16 (FC2 skips rows that FC1 found dead): every
-    row equals the oracle's masked FFN and the batch-1 result of its token."""
+@pytest.mark.parametrize("batch", [6, 16])
+def test_tc_layer_matches_oracle_and_batch1(kind, cfg, batch):
+    """Whole layer (FC2 skips rows that FC1 found dead): every row equals the
+    oracle's masked FFN and the batch-1 result of its token."""
     P = _pi()
     w = make_layer(cfg, 0, device=DEV)
     wh = oracle.host_layer(w.to("cpu"))
-    batch = 16
     x = make_tokens(cfg, 0, batch, device=DEV)
     desc = P.layer_desc(w, batch)
     ws = _ws(P, desc)
@@ -209,14 +210,14 @@ def test_tc_layer_matches_oracle_and_batch1(kind, cfg):
         if np.array_equal(mask[b], m1):  # an in-band score may land on either side
             same += 1
             close(yb[b], y1.cpu().numpy()[0], f"{kind} batched row {b} vs batch 1")
-    assert same >= batch - 2
+    assert same >= batch - 2 if batch > 4 else same >= batch - 1
 
 
-def test_tc_layer_repeatable_bitwise():
+@pytest.mark.parametrize("batch", [8, 32])
+def test_tc_layer_repeatable_bitwise(batch):
     P = _pi()
     cfg = CASES[1][1]
     w = make_layer(cfg, 0, device=DEV)
-    batch = 32
     x = make_tokens(cfg, 0, batch, device=DEV)
     desc = P.layer_desc(w, batch)
     ws = _ws(P, desc)
