@@ -3,6 +3,7 @@
 // here; every step runs in the kernels.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "pi_internal.h"
@@ -72,7 +73,15 @@ bool make_plan(const pi_layer_desc& desc, Plan* p) {
     q.fused = q.B == 1 && fused_supported(q.d, q.F, q.r, q.int4, q.nsm);
     q.tc = tc_supported(q);
     q.st = !q.tc && st_supported(q);
-    q.part_floats = q.tc ? tc_part_floats(q) : q.st ? st_part_floats(q) : (size_t)q.fc2_splits * q.B * q.d;
+    q.pred = tc_pred_supported(q) ? 2 : (st_pred_supported(q) ? 1 : 0);
+    {
+        // partial sums of whichever paths the plan takes (the stream-K sizes
+        // cover the predictor and both FFN products)
+        size_t part = (size_t)q.fc2_splits * q.B * q.d;
+        if (q.pred == 2 || q.tc) part = std::max(part, tc_part_floats(q));
+        if (q.pred == 1 || q.st) part = std::max(part, st_part_floats(q));
+        q.part_floats = part;
+    }
     size_t off = q.xchg_bytes;
     q.off_mask = off;  off = up(off + sizeof(uint32_t) * (size_t)q.B * q.W);
     q.off_idx = off;   off = up(off + sizeof(int32_t) * (size_t)q.F);
@@ -82,7 +91,7 @@ bool make_plan(const pi_layer_desc& desc, Plan* p) {
     q.off_part = off;  off = up(off + sizeof(float) * q.part_floats);
     q.off_xbuf = off;  off = up(off + sizeof(uint16_t) * 2 * (size_t)q.B * q.d);
     q.off_live = off;  off = up(off + sizeof(int32_t) * (size_t)q.F);
-    q.off_uhl = off;   off = up(off + (q.tc ? tc_uhl_bytes(q) : q.st ? st_u_bytes(q) : 0));
+    q.off_uhl = off;   off = up(off + (q.pred == 2 ? tc_uhl_bytes(q) : q.pred == 1 ? st_u_bytes(q) : 0));
     q.total = off;
     *p = q;
     return true;
@@ -326,10 +335,11 @@ int pi_launches_per_layer(const pi_layer_desc* desc) {
     // predictor: 2 per token chunk; compaction: 1; then FC1 + FC2 + the FC2
     // reduction (tcgen05 path: all tokens at once) or FC1 and FC2 per chunk + 1
     // tcgen05 path: predictor u + finish + s, compaction, FC1 + finish, FC2 + reduction
-    if (p.tc && p.r % 16 == 0) return 3 + 1 + 2 + 2;
-    if (p.st) return 3 + 1 + 2 + 2;   // same structure on CUDA cores (plus a mask memset)
-    if (p.tc) return 2 * chunks + 1 + 2 + 2;
-    return 2 * chunks + 1 + chunks + chunks + 1;
+    // predictor: u GEMM + finish + s GEMM on the streamed paths, else 2 per token chunk
+    const int pred = (p.pred == 2 && p.r % 16 == 0) || p.pred == 1 ? 3 : 2 * chunks;
+    // FC1 + finish and FC2 + reduction on the streamed paths, else 1 per chunk each + 1
+    const int ffn = (p.tc || p.st) ? 4 : chunks + chunks + 1;
+    return pred + 1 + ffn;
 }
 
 const char* pi_status_string(pi_status s) {

@@ -27,6 +27,8 @@ struct Plan {
     bool fused;     // pi_ffn_layer / pi_ffn_stack take the fused persistent kernel
     bool tc;        // FC1 / FC2 take the tcgen05 batched path (batch 16..32, fp16 weights)
     bool st;        // ... or the CUDA-core streamed batched path (batch 2..8, fp16 weights)
+    int pred;       // predictor path (its weights are fp16 for every weight type):
+                    // 2 tcgen05 (batch 16..32), 1 streamed CUDA cores (batch 2..8), 0 chunked
     size_t part_floats;  // FC2 partial sums of whichever FC2 path the plan takes
     size_t off_mask, off_idx, off_count, off_h, off_upart, off_part, off_xbuf, off_live, off_uhl, total;
 };
@@ -64,6 +66,7 @@ cudaError_t launch_count_active(const Plan& p, const int32_t* count, const float
 
 // ---- tcgen05 batched path (pi_tc.cu) ----
 bool tc_supported(const Plan& p);
+bool tc_pred_supported(const Plan& p);   // predictor only (any weight type)
 int tc_tokens(const Plan& p);       // N of the MMAs: batch rounded up to 16 or 32
 size_t tc_part_floats(const Plan& p);  // partial tiles of the stream-K splits
 size_t tc_uhl_bytes(const Plan& p);    // u as fp16 hi | lo rows
@@ -86,6 +89,7 @@ cudaError_t launch_fc2_reduce(const Plan& p, int nt, int G, int slots, const flo
 
 // ---- CUDA-core streamed batched path (pi_stream.cu, batch 2..8, fp16 weights) ----
 bool st_supported(const Plan& p);
+bool st_pred_supported(const Plan& p);   // predictor only (any weight type)
 int st_tokens(const Plan& p);          // token slots of the kernels: 2, 4 or 8
 size_t st_part_floats(const Plan& p);
 size_t st_u_bytes(const Plan& p);      // u as fp32 rows [B][r]

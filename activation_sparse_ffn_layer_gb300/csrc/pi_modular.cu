@@ -449,11 +449,11 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 
 cudaError_t launch_predict(const Plan& p, const __half* x, const __half* p1, const __half* p2,
                            const __half* bpred, float tau, uint32_t* mask, void* ws, cudaStream_t s) {
-    if (p.tc && p.r % 16 == 0)
+    if (p.pred == 2 && p.r % 16 == 0)
         return launch_predict_tc(p, x, p1, p2, bpred, tau, mask,
                                  reinterpret_cast<float*>(static_cast<char*>(ws) + p.off_part),
                                  reinterpret_cast<__half*>(static_cast<char*>(ws) + p.off_uhl), s);
-    if (p.st)
+    if (p.pred == 1)
         return launch_predict_st(p, x, p1, p2, bpred, tau, mask,
                                  reinterpret_cast<float*>(static_cast<char*>(ws) + p.off_part),
                                  reinterpret_cast<float*>(static_cast<char*>(ws) + p.off_uhl), s);

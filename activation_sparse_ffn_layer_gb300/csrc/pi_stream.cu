@@ -633,9 +633,9 @@ cudaError_t launch_rows_tb(const SArgs& a, int tb, int grid, cudaStream_t s) {
 
 }  // namespace
 
-bool st_supported(const Plan& p) {
-    return !p.int4 && p.B >= 2 && p.B <= 8 && p.d % 128 == 0 && p.nsm <= kMaxCtas;
-}
+bool st_pred_supported(const Plan& p) { return p.B >= 2 && p.B <= 8 && p.d % 128 == 0 && p.nsm <= kMaxCtas; }
+
+bool st_supported(const Plan& p) { return !p.int4 && st_pred_supported(p); }
 
 int st_tokens(const Plan& p) { return p.B <= 2 ? 2 : (p.B <= 4 ? 4 : 8); }
 

@@ -858,9 +858,9 @@ int u_grid(const Plan& p) {
 }
 }  // namespace
 
-bool tc_supported(const Plan& p) {
-    return !p.int4 && p.B >= 16 && p.B <= 32 && p.d % 128 == 0 && p.nsm <= kMaxCtas;
-}
+bool tc_pred_supported(const Plan& p) { return p.B >= 16 && p.B <= 32 && p.d % 128 == 0 && p.nsm <= kMaxCtas; }
+
+bool tc_supported(const Plan& p) { return !p.int4 && tc_pred_supported(p); }
 
 int tc_tokens(const Plan& p) { return p.B <= 16 ? 16 : 32; }
 
