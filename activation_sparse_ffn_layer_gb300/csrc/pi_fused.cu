@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
             ring_uses[q] = 0;
         }
     }
-    unsigned w2_uses = 0;   // completed-or-pending phases of w1_mbar and w2_mbar (used in pairs)
+    unsigned w1_uses = 0, w2_uses = 0;   // completed-or-pending phases of w1_mbar, w2_mbar
     bool w1_pending = false, w2_pending = false;
 
     // barrier targets: the counter holds G arrivals per barrier ever completed
@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
         if (inflight >= 0) mbar_drain(&pred_mbar, (unsigned)(inflight & 1), tmo);
         for (int q = 0; q < ns; ++q)
             if (ring_uses[q] > 0) mbar_drain(&ring_full[q], (unsigned)((ring_uses[q] - 1) & 1), tmo);
-        if (w1_pending) mbar_drain(&w1_mbar, (w2_uses - 1) & 1u, tmo);
+        if (w1_pending) mbar_drain(&w1_mbar, (w1_uses - 1) & 1u, tmo);
         if (w2_pending) mbar_drain(&w2_mbar, (w2_uses - 1) & 1u, tmo);
         if (c == 0 && tid == 0) {
             const unsigned long long next = ebase + (unsigned long long)kBarriersPerLayer * p.L;
@@ -672,15 +672,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
         // first); W2t rows of neurons whose FC1 output turns out to be zero are
         // loaded but not used.  The region held this layer's predictor slices,
         // consumed before the last grid barrier.
-        const bool rows_staged = nmine > 0 && nmine * (fc1_rows + 1) * wrow <= p.stage_bytes;
+        // FC1 rows are staged whenever they fit; W2t rows too when both fit
+        const bool w1_staged = nmine > 0 && nmine * fc1_rows * wrow <= p.stage_bytes;
+        const bool w2_staged = w1_staged && nmine * (fc1_rows + 1) * wrow <= p.stage_bytes;
         unsigned char* s_w1 = stage;                                  // [nmine] W1 (gate) rows
         unsigned char* s_wu = stage + (size_t)nmine * wrow;           // [nmine] up rows (gated)
         unsigned char* s_w2 = stage + (size_t)nmine * fc1_rows * wrow;  // [nmine] W2t rows
-        if (rows_staged) {
+        if (w1_staged) {
             if (tid == 0) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 mbar_arrive_expect_tx(&w1_mbar, (unsigned)(nmine * fc1_rows * wrow));
-                mbar_arrive_expect_tx(&w2_mbar, (unsigned)(nmine * wrow));
+                if (w2_staged) mbar_arrive_expect_tx(&w2_mbar, (unsigned)(nmine * wrow));
                 auto stage_row = [&](unsigned char* dst, const void* codes, const __half* scales, size_t k,
                                      unsigned long long* mb) {
                     if (KIND != 2) {
@@ -695,11 +697,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                 if (KIND == 1)
                     for (int q = 0; q < nmine; ++q)
                         stage_row(s_wu + (size_t)q * wrow, ly.wu, nullptr, (size_t)lidx[q], &w1_mbar);
-                for (int q = 0; q < nmine; ++q)
-                    stage_row(s_w2 + (size_t)q * wrow, ly.w2t, ly.w2ts, (size_t)lidx[q], &w2_mbar);
+                if (w2_staged)
+                    for (int q = 0; q < nmine; ++q)
+                        stage_row(s_w2 + (size_t)q * wrow, ly.w2t, ly.w2ts, (size_t)lidx[q], &w2_mbar);
             }
-            ++w2_uses;
-            w1_pending = w2_pending = true;
+            ++w1_uses;
+            w1_pending = true;
+            if (w2_staged) {
+                ++w2_uses;
+                w2_pending = true;
+            }
         }
 
         // FC1: (neuron, segment) items spread over all warps so that every warp
@@ -715,14 +722,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
             nseg = KIND == 2 ? (ng + segE - 1) / segE : (d + segE - 1) / segE;
             float* part = red;           // [nmine * nseg]
             float* partu = red + 2048;   // gated: up-projection partials
-            if (rows_staged && mbar_wait(&w1_mbar, (w2_uses - 1) & 1u, tmo, &bad)) w1_pending = false;
+            if (w1_staged && mbar_wait(&w1_mbar, (w1_uses - 1) & 1u, tmo, &bad)) w1_pending = false;
             for (int it = warp; it < nmine * nseg; it += kWarps) {
                 const int q = it / nseg, sg = it % nseg;
                 const int k = lidx[q];
                 float acc = 0.f, accu = 0.f;
                 if (KIND != 2) {
                     const int e0 = sg * segE, e1 = min(d, e0 + segE);
-                    if (rows_staged) {
+                    if (w1_staged) {
                         const __half* row = reinterpret_cast<const __half*>(s_w1 + (size_t)q * wrow);
                         const __half* rowu = reinterpret_cast<const __half*>(s_wu + (size_t)q * wrow);
 #pragma unroll 4
@@ -740,33 +747,38 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                         }
                     }
                 } else {
+                    // lane L takes the 8-element words L, L+32, ... of the
+                    // segment (4 lanes per scale group): 4-byte code loads and
+                    // x loads 32 bytes apart across lanes, the two 16-byte
+                    // halves swapped on lanes with bit 2 set so that the 8
+                    // lanes of a shared-memory phase hit 8 different bank groups
                     const int gs0 = sg * segE, gs1 = min(ng, gs0 + segE);
-                    const uint8_t* row = rows_staged ? s_w1 + (size_t)q * wrow
-                                                     : static_cast<const uint8_t*>(ly.w1) + (size_t)k * (d / 2);
-                    const __half* sc = rows_staged ? reinterpret_cast<const __half*>(s_w1 + (size_t)q * wrow + d / 2)
-                                                   : ly.w1s + (size_t)k * ng;
+                    const uint8_t* row = w1_staged ? s_w1 + (size_t)q * wrow
+                                                   : static_cast<const uint8_t*>(ly.w1) + (size_t)k * (d / 2);
+                    const __half* sc = w1_staged ? reinterpret_cast<const __half*>(s_w1 + (size_t)q * wrow + d / 2)
+                                                 : ly.w1s + (size_t)k * ng;
+                    const int sw = (lane >> 2) & 1;
 #pragma unroll 4
-                    for (int g = gs0 + lane; g < gs1; g += 32) {
-                        const uint4 qv = rows_staged ? *reinterpret_cast<const uint4*>(row + (size_t)g * 16)
-                                                     : ld_stream16(row + (size_t)g * 16);
-                        const float s = __half2float(sc[g]);
-                        const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
-                        float pt = 0.f;
-#pragma unroll
-                        for (int wi = 0; wi < 4; ++wi) {
-                            float qf[8];
-                            q8_to_f8(qw[wi], qf);
-                            const float4 xa = reinterpret_cast<const float4*>(xf + g * 32 + wi * 8)[0];
-                            const float4 xb = reinterpret_cast<const float4*>(xf + g * 32 + wi * 8)[1];
-                            pt = fmaf(qf[0], xa.x, pt);
-                            pt = fmaf(qf[1], xa.y, pt);
-                            pt = fmaf(qf[2], xa.z, pt);
-                            pt = fmaf(qf[3], xa.w, pt);
-                            pt = fmaf(qf[4], xb.x, pt);
-                            pt = fmaf(qf[5], xb.y, pt);
-                            pt = fmaf(qf[6], xb.z, pt);
-                            pt = fmaf(qf[7], xb.w, pt);
-                        }
+                    for (int wd = 4 * gs0 + lane; wd < 4 * gs1; wd += 32) {
+                        uint32_t cw;
+                        if (w1_staged)
+                            cw = *reinterpret_cast<const uint32_t*>(row + (size_t)wd * 4);
+                        else
+                            asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(cw) : "l"(row + (size_t)wd * 4));
+                        const float s = __half2float(sc[wd >> 2]);
+                        float qf[8];
+                        q8_to_f8(cw, qf);
+                        const float4* xp = reinterpret_cast<const float4*>(xf + (size_t)wd * 8);
+                        const float4 x0 = xp[sw], x1 = xp[sw ^ 1];
+                        const float4 xa = sw ? x1 : x0, xb = sw ? x0 : x1;
+                        float pt = qf[0] * xa.x;
+                        pt = fmaf(qf[1], xa.y, pt);
+                        pt = fmaf(qf[2], xa.z, pt);
+                        pt = fmaf(qf[3], xa.w, pt);
+                        pt = fmaf(qf[4], xb.x, pt);
+                        pt = fmaf(qf[5], xb.y, pt);
+                        pt = fmaf(qf[6], xb.z, pt);
+                        pt = fmaf(qf[7], xb.w, pt);
                         acc = fmaf(s, pt, acc);
                     }
                 }
@@ -803,8 +815,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
 
         // FC2: the whole CTA accumulates its neurons' W2t rows; rows whose
         // FC1 output is zero are skipped (ReLU removed them from FC2)
-        if (rows_staged && mbar_wait(&w2_mbar, (w2_uses - 1) & 1u, tmo, &bad)) w2_pending = false;
-        if (KIND != 2 && rows_staged) {
+        if (w2_staged && mbar_wait(&w2_mbar, (w2_uses - 1) & 1u, tmo, &bad)) w2_pending = false;
+        if (KIND != 2 && w2_staged) {
             float acc[NCH][8];
 #pragma unroll
             for (int ch = 0; ch < NCH; ++ch)
@@ -901,7 +913,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                     const float hv = q < nmine ? lh[q] : 0.f;
                     hs[b] = 0.f;
                     if (hv != 0.f && mine) {
-                        if (rows_staged) {
+                        if (w2_staged) {
                             const unsigned char* row = s_w2 + (size_t)q * wrow;
                             wv[b] = *reinterpret_cast<const uint4*>(row + col / 2);
                             hs[b] = hv * __half2float(reinterpret_cast<const __half*>(row + d / 2)[col / 32]);
