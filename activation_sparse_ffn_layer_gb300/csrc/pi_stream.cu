@@ -406,6 +406,7 @@ struct SArgs2 {
 struct Piece2 {
     int ct, j0, j1;
 };
+constexpr int kMaxPieces2 = 16;
 PI_DEV void piece2(long long u0, long long u1, int n, int which, Piece2* out) {
     const int ct = (int)(u0 / n) + which;
     const long long lo = (long long)ct * n, hi = lo + n;
@@ -429,6 +430,13 @@ __global__ void __launch_bounds__(kSThreads, 1) k_fc2_st(SArgs2 a) {
     const long long u0 = U * g / G, u1 = U * (g + 1) / G;
     if (u0 >= u1) return;
     const int npiece = (int)((u1 - 1) / n - u0 / n) + 1;
+    // this CTA's pieces, computed once (64-bit divisions stay out of the loops)
+    __shared__ Piece2 ptab[kMaxPieces2];
+    if (npiece > kMaxPieces2) {
+        if (threadIdx.x == 0) atomicExch(a.status, (int)PI_ERR_WORKSPACE);
+        return;
+    }
+    if (threadIdx.x < npiece) piece2(u0, u1, n, threadIdx.x, &ptab[threadIdx.x]);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         for (int s = 0; s < C::S; ++s) {
@@ -449,14 +457,12 @@ __global__ void __launch_bounds__(kSThreads, 1) k_fc2_st(SArgs2 a) {
         const int t = tid, w = t >> 5, l = t & 31;
         int total = 0;
         for (int p = 0; p < npiece; ++p) {
-            Piece2 pc;
-            piece2(u0, u1, n, p, &pc);
+            const Piece2 pc = ptab[p];
             total += (pc.j1 - pc.j0 + 63) / 64;
         }
         int fq = 0, fpiece = 0, fst = 0;
         auto copy_ids = [&]() {
-            Piece2 pc;
-            piece2(u0, u1, n, fpiece, &pc);
+            const Piece2 pc = ptab[fpiece];
             const int jb = pc.j0 + 64 * fst;
             const int kk = t & 63;
             const int j = jb + kk;
@@ -479,8 +485,7 @@ __global__ void __launch_bounds__(kSThreads, 1) k_fc2_st(SArgs2 a) {
         int it = 0;
         bool ok = true;
         for (int pi_ = 0; pi_ < npiece && ok; ++pi_) {
-            Piece2 pc;
-            piece2(u0, u1, n, pi_, &pc);
+            const Piece2 pc = ptab[pi_];
             const int nst = (pc.j1 - pc.j0 + 63) / 64;
             const int col0 = pc.ct * 128;
             for (int st = 0; st < nst; ++st, ++it) {
@@ -539,8 +544,7 @@ __global__ void __launch_bounds__(kSThreads, 1) k_fc2_st(SArgs2 a) {
             for (int t = 0; t < TB; ++t) acc[e][t] = 0.f;
         int it = 0;
         for (int p = 0; p < npiece; ++p) {
-            Piece2 pc;
-            piece2(u0, u1, n, p, &pc);
+            const Piece2 pc = ptab[p];
             const int nst = (pc.j1 - pc.j0 + 63) / 64;
             bool ok = true;
             for (int st = 0; st < nst; ++st, ++it) {

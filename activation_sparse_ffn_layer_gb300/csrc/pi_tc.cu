@@ -69,6 +69,14 @@ PI_DEV uint64_t sdesc_sw128(unsigned addr) {
     return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
+// 128-byte-swizzled MN-major layout (the W2t tile of FC2): atoms of 8 K-rows x
+// 64 MN-elements (1024 bytes, 1024-byte aligned), 16-byte chunk c of row k at
+// position c ^ (k % 8); lbo = bytes between atoms adjacent in MN, sbo = bytes
+// between 8-row groups adjacent in K.
+PI_DEV uint64_t sdesc_sw128_mn(unsigned addr, unsigned lbo, unsigned sbo) {
+    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
 // Instruction descriptor of kind::f16: fp32 D, fp16 A and B, A major-ness,
 // B K-major, N >> 3 at bit 17, M >> 4 at bit 24.
 PI_DEV unsigned idesc_f16(int M, int N, bool a_mn_major) {
@@ -547,6 +555,7 @@ struct TcFc2Args {
 struct Piece {
     int ct, j0, j1;
 };
+constexpr int kMaxPieces = 16;   // pieces of one CTA's stream-K range
 
 // Pieces of CTA g: the column tiles its range [u0, u1) of the (tile, row)
 // space touches, with the row interval inside each.
@@ -576,6 +585,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fc2_tc(TcFc2Args a) {
     const long long u0 = U * g / G, u1 = U * (g + 1) / G;
     if (u0 >= u1) return;
     const int npiece = (int)((u1 - 1) / n - u0 / n) + 1;
+    // this CTA's pieces, computed once (64-bit divisions stay out of the loops)
+    __shared__ Piece ptab[kMaxPieces];
+    if (npiece > kMaxPieces) {
+        if (threadIdx.x == 0) atomicExch(a.status, (int)PI_ERR_WORKSPACE);
+        return;
+    }
+    if (threadIdx.x < npiece) fc2_piece(u0, u1, n, threadIdx.x, &ptab[threadIdx.x]);
     unsigned char* ring = align1024(dsm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -604,7 +620,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fc2_tc(TcFc2Args a) {
         // stage; 64 rows x B floats of h are copied raw and converted to
         // (hi, lo) fp16 once every loader's copies of the stage have landed
         const int t = tid, w = t >> 5, l = t & 31;
-        const int mc = 4 * w + (l >> 3);
         const bool vec = (a.B & 3) == 0 && (reinterpret_cast<uintptr_t>(a.h) & 15) == 0;
         int it = 0;     // stage being issued
         int cv = 0;     // next stage to convert and publish
@@ -638,8 +653,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fc2_tc(TcFc2Args a) {
         };
         // publish stage cv: every loader's copies for it have landed
         auto publish = [&]() {
-            Piece pc;
-            fc2_piece(u0, u1, n, cv_piece, &pc);
+            const Piece pc = ptab[cv_piece];
             convert(cv, pc, cv_st);
             fence_async_smem();
             bar_arrive(&full[cv % C::S]);
@@ -655,14 +669,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fc2_tc(TcFc2Args a) {
         int32_t* slive = sidx + C::S * 64;
         int total = 0;
         for (int p = 0; p < npiece; ++p) {
-            Piece pc;
-            fc2_piece(u0, u1, n, p, &pc);
+            const Piece pc = ptab[p];
             total += (pc.j1 - pc.j0 + 63) / 64;
         }
         int fq = 0, fpiece = 0, fst = 0;  // next stage whose row ids to copy
         auto copy_ids = [&]() {
-            Piece pc;
-            fc2_piece(u0, u1, n, fpiece, &pc);
+            const Piece pc = ptab[fpiece];
             const int jb = pc.j0 + 64 * fst;
             const int kk = t & 63;
             const int j = jb + kk;
@@ -683,8 +695,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fc2_tc(TcFc2Args a) {
         cp_wait_all();
         loaders_sync_any(false);
         for (int pi_ = 0; pi_ < npiece && ok; ++pi_) {
-            Piece pc;
-            fc2_piece(u0, u1, n, pi_, &pc);
+            const Piece pc = ptab[pi_];
             const int nst = (pc.j1 - pc.j0 + 63) / 64;
             const int col0 = pc.ct * 128;
             for (int st = 0; st < nst; ++st, ++it) {
@@ -694,20 +705,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fc2_tc(TcFc2Args a) {
                 unsigned char* sb = ring + (size_t)s * C::STAGE;
                 const int jb = pc.j0 + 64 * st;
                 if (good) {
+                    // W2t tile, 128-byte-swizzled MN-major: a warp instruction
+                    // copies 2 rows x 256 contiguous bytes (lane: row half
+                    // l >> 4, 16-byte column chunk c16 = l & 15)
+                    const int c16 = l & 15;
                     int kv[8];
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
-                        const int kk = 8 * q + (l & 7);
+                        const int kk = 2 * (4 * q + w) + (l >> 4);
                         const bool in = jb + kk < pc.j1;
                         const bool alive = a.live == nullptr || slive[s * 64 + kk] != 0;
                         kv[q] = (in && alive) ? sidx[s * 64 + kk] : -1;
                     }
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
-                        const int kk = 8 * q + (l & 7);
-                        unsigned char* dst = sb + mc * 128 + (kk >> 3) * 2048 + (kk & 7) * 16;
+                        const int kk = 2 * (4 * q + w) + (l >> 4);
+                        unsigned char* dst = sb + (c16 >> 3) * 1024 + (kk >> 3) * 2048 + (kk & 7) * 128 +
+                                             (((c16 & 7) ^ (kk & 7)) << 4);
                         if (kv[q] >= 0)
-                            cp16(dst, a.w2t + (size_t)kv[q] * a.d + col0 + mc * 8);
+                            cp16(dst, a.w2t + (size_t)kv[q] * a.d + col0 + c16 * 8);
                         else
                             *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
                     }
@@ -768,8 +784,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fc2_tc(TcFc2Args a) {
         int it = 0;
         bool ok = true;
         for (int p = 0; p < npiece && ok; ++p) {
-            Piece pc;
-            fc2_piece(u0, u1, n, p, &pc);
+            const Piece pc = ptab[p];
             const int nst = (pc.j1 - pc.j0 + 63) / 64;
             const int b = p & 1;
             if (p >= 2 && !bar_wait(&acce[b], ((p >> 1) - 1) & 1, ctl)) {
@@ -789,7 +804,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fc2_tc(TcFc2Args a) {
                 const unsigned sbop = sa + kTileA;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t ad = sdesc(sa + kk * 4096, 2048, 128);
+                    const uint64_t ad = sdesc_sw128_mn(sa + kk * 4096, 1024, 2048);
                     const uint64_t bd = sdesc(sbop + kk * 2 * (2 * NT * 16), 2 * NT * 16, 128);
                     mma_f16(dcol, ad, bd, idesc, (st | kk) ? 1u : 0u);
                 }
