@@ -73,6 +73,7 @@ bool make_plan(const pi_layer_desc& desc, Plan* p) {
     q.fused = q.B == 1 && fused_supported(q.d, q.F, q.r, q.int4, q.nsm);
     q.tc = tc_supported(q);
     q.st = !q.tc && st_supported(q);
+    q.st4 = !q.tc && !q.st && st4_supported(q);
     q.pred = tc_pred_supported(q) ? 2 : (st_pred_supported(q) ? 1 : 0);
     {
         // partial sums of whichever paths the plan takes (the stream-K sizes
@@ -80,6 +81,7 @@ bool make_plan(const pi_layer_desc& desc, Plan* p) {
         size_t part = (size_t)q.fc2_splits * q.B * q.d;
         if (q.pred == 2 || q.tc) part = std::max(part, tc_part_floats(q));
         if (q.pred == 1 || q.st) part = std::max(part, st_part_floats(q));
+        if (q.st4) part = std::max(part, st4_part_floats(q));
         q.part_floats = part;
     }
     size_t off = q.xchg_bytes;
@@ -202,7 +204,7 @@ cudaError_t run_stack(const Plan& p, int n, const LayerPtrs* lp, const int* rank
             e = launch_fc1(q, cur, w, idx, cnt, q.B > 1 ? mask : nullptr, at<float>(ws, p.off_part), h, live, s);
         if (e == cudaSuccess && layer_counts) e = launch_count_active(q, cnt, h, layer_counts + 2 * l, s);
         if (e == cudaSuccess)
-            e = launch_fc2(q, h, idx, cnt, w, (q.tc || q.st) ? live : nullptr, at<float>(ws, p.off_part), y, s);
+            e = launch_fc2(q, h, idx, cnt, w, (q.tc || q.st || q.st4) ? live : nullptr, at<float>(ws, p.off_part), y, s);
         if (e != cudaSuccess) return e;
         if (l + 1 < n) {
             __half* nxt = x_trace ? x_trace + (size_t)l * p.B * p.d : xbuf + (size_t)(l % 2) * p.B * p.d;
@@ -338,7 +340,7 @@ int pi_launches_per_layer(const pi_layer_desc* desc) {
     // predictor: u GEMM + finish + s GEMM on the streamed paths, else 2 per token chunk
     const int pred = (p.pred == 2 && p.r % 16 == 0) || p.pred == 1 ? 3 : 2 * chunks;
     // FC1 + finish and FC2 + reduction on the streamed paths, else 1 per chunk each + 1
-    const int ffn = (p.tc || p.st) ? 4 : chunks + chunks + 1;
+    const int ffn = (p.tc || p.st) ? 4 : p.st4 ? 2 + 2 * ((p.B + 7) / 8) : chunks + chunks + 1;
     return pred + 1 + ffn;
 }
 

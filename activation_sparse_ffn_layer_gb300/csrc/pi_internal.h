@@ -27,6 +27,7 @@ struct Plan {
     bool fused;     // pi_ffn_layer / pi_ffn_stack take the fused persistent kernel
     bool tc;        // FC1 / FC2 take the tcgen05 batched path (batch 16..32, fp16 weights)
     bool st;        // ... or the CUDA-core streamed batched path (batch 2..8, fp16 weights)
+    bool st4;       // ... or its INT4 variant (batch 2..16, ReLU FFN)
     int pred;       // predictor path (its weights are fp16 for every weight type):
                     // 2 tcgen05 (batch 16..32), 1 streamed CUDA cores (batch 2..8), 0 chunked
     size_t part_floats;  // FC2 partial sums of whichever FC2 path the plan takes
@@ -79,13 +80,14 @@ cudaError_t launch_fc1_tc(const Plan& p, const __half* x, const LayerPtrs& w, co
 cudaError_t launch_fc2_tc(const Plan& p, const float* h, const int32_t* idx, const int32_t* count,
                           const LayerPtrs& w, const int32_t* live, float* partial, float* y, cudaStream_t s);
 
-// fixed-order finishing of the stream-K partials (shared by both batched paths):
-// nt = partial columns per token group, G = CTAs of the split, slots = tiles per CTA
-cudaError_t launch_fc1_finish(const Plan& p, int nt, int G, int slots, const float* part, const int32_t* count,
-                              const int32_t* idx, const __half* b1, const uint32_t* mask, float* h, int32_t* live,
-                              cudaStream_t s);
-cudaError_t launch_fc2_reduce(const Plan& p, int nt, int G, int slots, const float* part, const int32_t* count,
-                              const __half* b2, float* y, cudaStream_t s);
+// fixed-order finishing of the stream-K partials (shared by the batched paths):
+// nt = partial columns per token group, G = CTAs of the split, slots = tiles per
+// CTA, nk = K-chunks per FC1 row, tw = FC2 column-tile width, nb tokens from b0
+cudaError_t launch_fc1_finish(const Plan& p, int nt, int G, int slots, int nk, const float* part,
+                              const int32_t* count, const int32_t* idx, const __half* b1, const uint32_t* mask,
+                              float* h, int32_t* live, cudaStream_t s);
+cudaError_t launch_fc2_reduce(const Plan& p, int nt, int G, int slots, int tw, int nb, int b0, const float* part,
+                              const int32_t* count, const __half* b2, float* y, cudaStream_t s);
 
 // ---- CUDA-core streamed batched path (pi_stream.cu, batch 2..8, fp16 weights) ----
 bool st_supported(const Plan& p);
@@ -101,6 +103,15 @@ cudaError_t launch_fc1_st(const Plan& p, const __half* x, const LayerPtrs& w, co
                           cudaStream_t s);
 cudaError_t launch_fc2_st(const Plan& p, const float* h, const int32_t* idx, const int32_t* count,
                           const LayerPtrs& w, const int32_t* live, float* partial, float* y, cudaStream_t s);
+
+// ---- CUDA-core streamed batched path for INT4 weights (pi_stream4.cu, batch 2..16) ----
+bool st4_supported(const Plan& p);
+size_t st4_part_floats(const Plan& p);
+cudaError_t launch_fc1_st4(const Plan& p, const __half* x, const LayerPtrs& w, const int32_t* idx,
+                           const int32_t* count, const uint32_t* mask, float* part, float* h, int32_t* live,
+                           cudaStream_t s);
+cudaError_t launch_fc2_st4(const Plan& p, const float* h, const int32_t* idx, const int32_t* count,
+                           const LayerPtrs& w, const int32_t* live, float* partial, float* y, cudaStream_t s);
 
 // ---- fused persistent stack (batch 1) ----
 struct FusedStackArgs {

@@ -493,6 +493,7 @@ cudaError_t launch_fc1(const Plan& p, const __half* x, const LayerPtrs& w, const
                        cudaStream_t s) {
     if (p.tc) return launch_fc1_tc(p, x, w, idx, count, mask, partial, h, live, s);
     if (p.st) return launch_fc1_st(p, x, w, idx, count, mask, partial, h, live, s);
+    if (p.st4) return launch_fc1_st4(p, x, w, idx, count, mask, partial, h, live, s);
     const int kind = p.int4 ? 2 : (p.gated ? 1 : 0);
     return for_token_chunks(p.B, [&](int b0, int tb) -> cudaError_t {
         const size_t sm = (size_t)tb * p.d * sizeof(__half);
@@ -518,6 +519,7 @@ cudaError_t launch_fc2(const Plan& p, const float* h, const int32_t* idx, const 
                        const LayerPtrs& w, const int32_t* live, float* partial, float* y, cudaStream_t s) {
     if (p.tc) return launch_fc2_tc(p, h, idx, count, w, live, partial, y, s);
     if (p.st) return launch_fc2_st(p, h, idx, count, w, live, partial, y, s);
+    if (p.st4) return launch_fc2_st4(p, h, idx, count, w, live, partial, y, s);
     cudaError_t e = for_token_chunks(p.B, [&](int b0, int tb) -> cudaError_t {
         dim3 grid(p.fc2_tiles, p.fc2_splits);
 #define PI_FC2(TBV, IV)                                                                       \

@@ -126,7 +126,7 @@ PI_DEV void cover_setup(long long U, int G, int nk, int tile, int* slot, int* rn
 
 // Ascending-CTA sum; loads go out eight at a time so their latencies overlap.
 PI_DEV float sum_cover(const float* __restrict__ part, const int* slot, const int* rng, int slots, int cols,
-                       int col, int m) {
+                       int col, int m, int tw = 128) {
     float acc = 0.f;
     for (int g0 = rng[0]; g0 <= rng[1]; g0 += 8) {
         float v[8];
@@ -134,7 +134,7 @@ PI_DEV float sum_cover(const float* __restrict__ part, const int* slot, const in
         for (int k = 0; k < 8; ++k) {
             const int g = g0 + k;
             const int sl = g <= rng[1] ? slot[g] : -1;
-            v[k] = (sl >= 0 && sl < slots) ? __ldcg(part + (((size_t)g * slots + sl) * cols + col) * 128 + m) : 0.f;
+            v[k] = (sl >= 0 && sl < slots) ? __ldcg(part + (((size_t)g * slots + sl) * cols + col) * tw + m) : 0.f;
         }
 #pragma unroll
         for (int k = 0; k < 8; ++k) acc += v[k];

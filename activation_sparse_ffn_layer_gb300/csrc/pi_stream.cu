@@ -712,7 +712,7 @@ cudaError_t launch_fc1_st(const Plan& p, const __half* x, const LayerPtrs& w, co
     a.timeout_ns = kStTimeoutNs;
     cudaError_t e = p.gated ? launch_rows_tb<1>(a, tb, G, s) : launch_rows_tb<0>(a, tb, G, s);
     if (e != cudaSuccess) return e;
-    return launch_fc1_finish(p, tb, G, a.slots, part, count, idx, w.b1, mask, h, live, s);
+    return launch_fc1_finish(p, tb, G, a.slots, cdiv(p.d, 64), part, count, idx, w.b1, mask, h, live, s);
 }
 
 cudaError_t launch_fc2_st(const Plan& p, const float* h, const int32_t* idx, const int32_t* count,
@@ -733,7 +733,7 @@ cudaError_t launch_fc2_st(const Plan& p, const float* h, const int32_t* idx, con
 #undef PI_FC2ST
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return launch_fc2_reduce(p, tb, G, slots, partial, count, w.b2, y, s);
+    return launch_fc2_reduce(p, tb, G, slots, 128, p.B, 0, partial, count, w.b2, y, s);
 }
 
 }  // namespace pi

@@ -830,26 +830,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fc2_tc(TcFc2Args a) {
     }
 }
 
-// y[t, c] = b2[c] + sum over the CTAs whose range touches column tile c / 128
-// of their partial (ascending CTA order: reproducible).  Block: the 128
-// columns of one tile x 8 tokens.
+// y[b0 + t, c] = b2[c] + sum over the CTAs whose range touches column tile
+// c / tw of their partial (ascending CTA order: reproducible), for the nb
+// tokens of this pass.  Block: the tw columns of one tile x 1024 / tw tokens.
 __global__ void __launch_bounds__(1024) k_fc2_tc_reduce(const float* __restrict__ part, int slots, int G,
-                                                        const int32_t* __restrict__ count, int B, int NT, int d,
-                                                        const __half* __restrict__ b2, float* __restrict__ y) {
+                                                        const int32_t* __restrict__ count, int nb, int b0, int NT,
+                                                        int d, int tw, const __half* __restrict__ b2,
+                                                        float* __restrict__ y) {
     __shared__ int slot[kMaxCtas];
     __shared__ int rng[2];
     const int ct = blockIdx.x;
-    const int m = threadIdx.x & 127, t = blockIdx.y * 8 + (threadIdx.x >> 7);
+    const int m = threadIdx.x % tw, t = blockIdx.y * (1024 / tw) + threadIdx.x / tw;
     const int n = *count;
-    const int c = ct * 128 + m;
+    const int c = ct * tw + m;
     if (n == 0) {  // uniform over the block
-        if (t < B) y[(size_t)t * d + c] = __half2float(b2[c]);
+        if (t < nb) y[(size_t)(b0 + t) * d + c] = __half2float(b2[c]);
         return;
     }
-    cover_setup((long long)(d / 128) * n, G, n, ct, slot, rng);
+    cover_setup((long long)(d / tw) * n, G, n, ct, slot, rng);
     __syncthreads();
-    if (t >= B) return;
-    y[(size_t)t * d + c] = __half2float(b2[c]) + sum_cover(part, slot, rng, slots, NT, t, m);
+    if (t >= nb) return;
+    y[(size_t)(b0 + t) * d + c] = __half2float(b2[c]) + sum_cover(part, slot, rng, slots, NT, t, m, tw);
 }
 
 template <typename K>
@@ -980,22 +981,24 @@ cudaError_t launch_fc1_tc(const Plan& p, const __half* x, const LayerPtrs& w, co
     return cudaGetLastError();
 }
 
-cudaError_t launch_fc1_finish(const Plan& p, int nt, int G, int slots, const float* part, const int32_t* count,
-                              const int32_t* idx, const __half* b1, const uint32_t* mask, float* h, int32_t* live,
-                              cudaStream_t s) {
+cudaError_t launch_fc1_finish(const Plan& p, int nt, int G, int slots, int nk, const float* part,
+                              const int32_t* count, const int32_t* idx, const __half* b1, const uint32_t* mask,
+                              float* h, int32_t* live, cudaStream_t s) {
     const int blocks = ceil_div(p.F, 32);
     if (p.gated)
-        k_fc1_finish<true><<<blocks, 32 * p.B, 0, s>>>(part, slots, G, ceil_div(p.d, 64), count, p.B, nt, idx, b1,
-                                                       mask, p.W, h, live);
+        k_fc1_finish<true><<<blocks, 32 * p.B, 0, s>>>(part, slots, G, nk, count, p.B, nt, idx, b1, mask, p.W, h,
+                                                       live);
     else
-        k_fc1_finish<false><<<blocks, 32 * p.B, 0, s>>>(part, slots, G, ceil_div(p.d, 64), count, p.B, nt, idx, b1,
-                                                        mask, p.W, h, live);
+        k_fc1_finish<false><<<blocks, 32 * p.B, 0, s>>>(part, slots, G, nk, count, p.B, nt, idx, b1, mask, p.W, h,
+                                                        live);
     return cudaGetLastError();
 }
 
-cudaError_t launch_fc2_reduce(const Plan& p, int nt, int G, int slots, const float* part, const int32_t* count,
-                              const __half* b2, float* y, cudaStream_t s) {
-    k_fc2_tc_reduce<<<dim3(p.d / 128, ceil_div(p.B, 8)), 1024, 0, s>>>(part, slots, G, count, p.B, nt, p.d, b2, y);
+cudaError_t launch_fc2_reduce(const Plan& p, int nt, int G, int slots, int tw, int nb, int b0, const float* part,
+                              const int32_t* count, const __half* b2, float* y, cudaStream_t s) {
+    const int tpb = 1024 / tw;
+    k_fc2_tc_reduce<<<dim3(p.d / tw, ceil_div(nb, tpb)), 1024, 0, s>>>(part, slots, G, count, nb, b0, nt, p.d, tw,
+                                                                        b2, y);
     return cudaGetLastError();
 }
 
@@ -1019,8 +1022,8 @@ cudaError_t launch_fc2_tc(const Plan& p, const float* h, const int32_t* idx, con
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    k_fc2_tc_reduce<<<dim3(p.d / 128, ceil_div(p.B, 8)), 1024, 0, s>>>(partial, slots, G, count, p.B, nt, p.d,
-                                                                        w.b2, y);
+    k_fc2_tc_reduce<<<dim3(p.d / 128, ceil_div(p.B, 8)), 1024, 0, s>>>(partial, slots, G, count, p.B, 0, nt, p.d,
+                                                                        128, w.b2, y);
     return cudaGetLastError();
 }
 
