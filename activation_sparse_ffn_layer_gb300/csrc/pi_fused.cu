@@ -4,13 +4,16 @@
 // Per layer (PowerInfer summary (CSDN): "Adaptive sparse predictor",
 // "Neuron-aware operator", "Background"):
 //   A  u-partials  = P1[i, segment] . x              (items spread over all warps)
-//   B  mask units  = 16 rows of (P2 u + b > tau)      (units spread over CTAs)
-//   C  compaction of the mask (every CTA, redundantly), then this CTA's equal
-//      share of the active list: FC1 rows (bias + ReLU [+ gate]) and the FC2
-//      gather-accumulate of its neurons into a private partial y
+//   B  mask bits   = (P2 u + b > tau) of this CTA's own rows, then FC1 of its
+//      own predicted rows (bias + ReLU [+ gate]) and the FC2 gather-accumulate
+//      of those neurons into a private partial y -- no exchange of the mask:
+//      a CTA computes the FFN of exactly the neurons it predicted
 //   D  y columns   = b2 + sum of all partials (fixed order), sum of squares
 //   (next layer)   x = fp16(y / sqrt(mean(y^2) + eps))
-// with one grid barrier after each phase.
+// with one grid barrier after each phase (three per layer).  Rows are owned in
+// pieces of 8: the pieces of round k (G consecutive pieces) go to the CTAs in
+// ascending order for even k and descending order for odd k, so that the hot
+// rows at the start of the table spread over all CTAs.
 //
 // The barrier is a single counter: each CTA adds 1 with release semantics and
 // spins (one thread, acquire loads) until the count reaches the barrier's
@@ -35,9 +38,11 @@ __device__ int g_pi_status = 0;
 
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 256;
+constexpr int kCols = 8 * kThreads;   // fp16 FC2 columns of one chunk (8 per thread)
 constexpr int kWarps = kThreads / 32;
-constexpr int kBarriersPerLayer = 4;
+constexpr int kBarriersPerLayer = 3;
+constexpr int kMaxUnits = 64;   // 16-row units (two 8-row pieces) per CTA
 constexpr int kRingMax = 8;   // P2 ring slots at most
 
 PI_DEV unsigned long long globaltimer() {
@@ -157,11 +162,10 @@ struct FusedParams {
     unsigned long long* epoch;  // [1] barriers completed by earlier launches
     unsigned* counter;          // [1] barrier arrivals (mod 2^32)
     float* xu;                  // [max su*r]
-    uint32_t* xmask;            // [W]
     float* xyp;                 // [G][d]
     float* xy;                  // [d]
     float* xss;                 // [G]
-    uint32_t* mask_out;         // [W] plain mask of the last layer
+    uint32_t* mask_out;         // [W] mask of the last layer (written by the owners of its pieces)
     int32_t* idx_out;           // [F]
     int32_t* count_out;         // [1]
     float* h_out;               // [F]
@@ -177,8 +181,10 @@ struct FusedParams {
 // Dynamic smem layout (bytes): xf float[d] | u float[rmax] | ustage float[usmax]
 //   | scratch | m16 int[M] | upre int[M+1] | lidx int[cap] | lh float[cap]
 //   | P1 slice | P2 slice | bias slice   (the last three only with pred_smem)
-// The mask and active-list buffers (m16 .. lh) are live only in phase C before
-// FC2 ends, so the P2 ring may span them together with the staging region.
+// lidx / lh hold this CTA's own active rows from the end of its mask units to
+// the end of FC2 (to the end of the step in the last layer, where m16 / upre
+// then take the whole mask for the list positions); the P2 ring, idle then,
+// spans m16 .. lh together with the staging region.
 struct SmemPlan {
     int d, rmax, usmax, M, cap;
     int p1s = 0, p2s = 0, b1s = 0;  // shared predictor buffers (bytes, 16-aligned), 0 if unused
@@ -198,6 +204,35 @@ struct SmemPlan {
     __host__ __device__ int bytes() const { return off_stage() + stage; }
 };
 
+// dot of 8 fp16 weights with 8 fp32 values in registers
+PI_DEV float dot8r(const uint4& w, const float4& xa, const float4& xb) {
+    float wf[8];
+    h8_to_f8(w, wf);
+    float acc = wf[0] * xa.x;
+    acc = fmaf(wf[1], xa.y, acc);
+    acc = fmaf(wf[2], xa.z, acc);
+    acc = fmaf(wf[3], xa.w, acc);
+    acc = fmaf(wf[4], xb.x, acc);
+    acc = fmaf(wf[5], xb.y, acc);
+    acc = fmaf(wf[6], xb.z, acc);
+    acc = fmaf(wf[7], xb.w, acc);
+    return acc;
+}
+// dot of 8 INT4 codes with 8 fp32 values in registers
+PI_DEV float dotq8r(uint32_t cw, const float4& xa, const float4& xb) {
+    float qf[8];
+    q8_to_f8(cw, qf);
+    float acc = qf[0] * xa.x;
+    acc = fmaf(qf[1], xa.y, acc);
+    acc = fmaf(qf[2], xa.z, acc);
+    acc = fmaf(qf[3], xa.w, acc);
+    acc = fmaf(qf[4], xb.x, acc);
+    acc = fmaf(qf[5], xb.y, acc);
+    acc = fmaf(qf[6], xb.z, acc);
+    acc = fmaf(qf[7], xb.w, acc);
+    return acc;
+}
+
 // dot of 8 fp16 weights with 8 fp32 values in smem
 PI_DEV float dot8(const uint4& w, const float* xs) {
     float wf[8];
@@ -213,6 +248,31 @@ PI_DEV float dot8(const uint4& w, const float* xs) {
     acc = fmaf(wf[6], b.z, acc);
     acc = fmaf(wf[7], b.w, acc);
     return acc;
+}
+
+// Halving butterfly over a warp: v[b] is this lane's partial sum of row b
+// (N = 8 or 4 rows); on return lane L holds the warp's total of row
+// fold_row<N>(L) (a fixed order: 9 shuffles for 8 rows, 6 for 4).
+template <int N>
+PI_DEV int fold_row(int lane) {
+    return N == 8 ? ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1)
+                  : ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
+}
+template <int N>
+PI_DEV float fold(float (&v)[N], int lane) {
+    int o = 16;
+#pragma unroll
+    for (int n = N / 2; n >= 1; n /= 2, o /= 2) {
+        const bool hi = lane & o;
+#pragma unroll
+        for (int k = 0; k < n; ++k) {
+            const float send = hi ? v[k] : v[k + n];
+            const float keep = hi ? v[k + n] : v[k];
+            v[k] = keep + __shfl_xor_sync(FULL, send, o);
+        }
+    }
+    for (; o >= 1; o /= 2) v[0] += __shfl_xor_sync(FULL, v[0], o);
+    return v[0];
 }
 
 // Block-wide exclusive scan of one int per thread (kThreads threads).
@@ -262,7 +322,7 @@ __device__ unsigned long long g_pi_trace_clk[96 * kTraceSlots * kTraceCtas];
 #endif
 
 // KIND 0: fp16 rows; 1: fp16 gate + up rows; 2: INT4 group-32 rows.
-// NCH: 4096-column chunks of d that each thread covers in FC2 (fp16 rows).
+// NCH: kCols-column chunks of d that each thread covers in FC2 (fp16 rows).
 template <int KIND, int NCH>
 __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_constant__ FusedParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
@@ -275,7 +335,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
         rmax = max(rmax, p.layers[l].r);
         usmax = max(usmax, p.layers[l].r * p.layers[l].su);
     }
-    const int cap = F / G + 2;
+    // this CTA's own 8-row pieces: own piece i is global piece piece_of(i)
+    const int P = (F + 7) / 8;
+    auto piece_of = [&](int i) { return i * G + ((i & 1) ? G - 1 - c : c); };
+    const int npc = P / G + (piece_of(P / G) < P ? 1 : 0);
+    const int nunits = (npc + 1) / 2;   // unit k = own pieces 2k, 2k+1
+    const int cap = 16 * ((P + 2 * G - 1) / (2 * G));
     SmemPlan sp{d, rmax, usmax, M, cap};
     sp.p1s = p.pred_smem ? p.p1s_bytes : 0;
     sp.p2s = p.pred_smem ? p.p2s_bytes : 0;
@@ -300,6 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
     const int fc1_rows = KIND == 1 ? 2 : 1;   // gate and up rows when gated
     __shared__ int bad;
     __shared__ float rs_s;
+    __shared__ uint16_t ubits[kMaxUnits];   // mask bits of this CTA's units (bit kk = row kk)
+    __shared__ int nmine_s;
     __shared__ __align__(8) unsigned long long pred_mbar;
     __shared__ __align__(8) unsigned long long w1_mbar;   // staged FC1 rows
     __shared__ __align__(8) unsigned long long w2_mbar;   // staged W2t rows
@@ -344,55 +411,66 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
 
     // This CTA's share of layer l's predictor: P1 items [q0, q1) (item q =
     // row q/su, segment q%su; consecutive items are contiguous in memory) and
-    // mask units [m0, m1) (16 rows of P2 each, contiguous).
+    // the P2 rows of its own pieces.
     // (sizes here are far below 2^32 / G, so 32-bit unsigned arithmetic is exact)
     auto item_range = [&](const FusedLayer& ly, int* q0, int* q1) {
         const unsigned items = (unsigned)(ly.r * ly.su);
         *q0 = (int)(items * (unsigned)c / (unsigned)G);
         *q1 = (int)(items * (unsigned)(c + 1) / (unsigned)G);
     };
-    const int um0 = (int)((unsigned)M * (unsigned)c / (unsigned)G);
-    const int um1 = (int)((unsigned)M * (unsigned)(c + 1) / (unsigned)G);
-    const int row0 = um0 * 16, row1 = min(F, um1 * 16);
     // element offset of item q in P1
     auto item_off = [&](const FusedLayer& ly, int q) -> size_t {
         const int i = q / ly.su, sg = q % ly.su;
         return (size_t)i * d + (size_t)sg * ly.seg;
     };
-    // thread 0: bulk-copy layer l's predictor slice into shared memory
+    // warp 0: bulk-copy layer l's predictor slice into shared memory (lane 0
+    // arms the mbarrier with the total, then the lanes issue the copies)
     auto issue_predictor = [&](int l) {
         const FusedLayer& ly = p.layers[l];
         int q0, q1;
         item_range(ly, &q0, &q1);
         const size_t e0 = item_off(ly, q0), e1 = q1 < ly.r * ly.su ? item_off(ly, q1) : (size_t)ly.r * d;
         const unsigned b_p1 = (unsigned)(2 * (e1 - e0));
-        const unsigned b_p2 = (unsigned)(2 * (size_t)ly.r * (row1 - row0));
-        const unsigned b_b1 = (unsigned)(2 * ((row1 - row0) & ~7));     // whole 16-byte pieces
+        // own piece i: its rows of P2 at p2s row 8i, its bias (whole pieces only) at b1s[8i]
+        unsigned b_p2 = 0, b_b1 = 0;
+        for (int i = 0; i < npc; ++i) {
+            const int rows = min(8, F - 8 * piece_of(i));
+            b_p2 += (unsigned)(2 * ly.r * rows);
+            b_b1 += rows == 8 ? 16u : 0u;
+        }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive_expect_tx(&pred_mbar, b_p1 + b_p2 + b_b1);
-        if (b_p1) bulk_g2s(p1s, ly.p1 + e0, b_p1, &pred_mbar);
-        if (b_p2) bulk_g2s(p2s, ly.p2 + (size_t)row0 * ly.r, b_p2, &pred_mbar);
-        if (b_b1) bulk_g2s(b1s, ly.b1 + row0, b_b1, &pred_mbar);
+        if (lane == 0) mbar_arrive_expect_tx(&pred_mbar, b_p1 + b_p2 + b_b1);
+        __syncwarp();
+        if (b_p1 && lane == 0) bulk_g2s(p1s, ly.p1 + e0, b_p1, &pred_mbar);
+        for (int i = lane; i < npc; i += 32) {
+            const int rb = 8 * piece_of(i);
+            const int rows = min(8, F - rb);
+            bulk_g2s(p2s + (size_t)8 * i * ly.r, ly.p2 + (size_t)rb * ly.r, (unsigned)(2 * ly.r * rows), &pred_mbar);
+            if (rows == 8) bulk_g2s(b1s + 8 * i, ly.b1 + rb, 16u, &pred_mbar);
+        }
     };
-    // P2 ring (no shared predictor slices): unit k of this CTA's range goes to
-    // slot k % ns; issued by one thread (the first ns units of a layer by thread
-    // 0, later ones by the warp that owns the slot), which counts the slot's uses.
-    const int nunits = um1 - um0;
+    // P2 ring (no shared predictor slices): unit k (own pieces 2k, 2k+1, rows
+    // 16 apart in the slot) goes to slot k % ns; issued by one thread (the first
+    // ns units of a layer by thread 0, later ones by the warp that owns the
+    // slot), which counts the slot's uses.
     auto issue_unit = [&](const FusedLayer& ly, int k) {
         const int q = k % ns;
-        const int rb = row0 + 16 * k;
-        const int rows = min(16, row1 - rb);
-        const unsigned bytes = (unsigned)(2 * rows * ly.r);
+        unsigned bytes = 0;
+        for (int h = 0; h < 2 && 2 * k + h < npc; ++h) bytes += (unsigned)(2 * ly.r * min(8, F - 8 * piece_of(2 * k + h)));
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         mbar_arrive_expect_tx(&ring_full[q], bytes);
-        bulk_g2s(ring + (size_t)q * p.ring_unit, ly.p2 + (size_t)rb * ly.r, bytes, &ring_full[q]);
+        for (int h = 0; h < 2 && 2 * k + h < npc; ++h) {
+            const int rb = 8 * piece_of(2 * k + h);
+            bulk_g2s(ring + (size_t)q * p.ring_unit + (size_t)16 * h * ly.r, ly.p2 + (size_t)rb * ly.r,
+                     (unsigned)(2 * ly.r * min(8, F - rb)), &ring_full[q]);
+        }
         ring_uses[q] += 1;
     };
     // uses of slot q in one layer (every layer has the same units)
     auto ring_per_layer = [&](int q) { return nunits > q ? (nunits - 1 - q) / ns + 1 : 0; };
     __syncthreads();
     if (p.pred_smem) {
-        if (tid == 0) issue_predictor(0);
+        if (warp == 0) issue_predictor(0);
         inflight = 0;
     } else if (ns > 0 && tid == 0) {
         for (int k = 0; k < ns && k < nunits; ++k) issue_unit(p.layers[0], k);
@@ -412,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
             if (l + 1 < p.L && (p.pred_smem || ns > 0)) {
                 __syncthreads();   // the region may still hold this CTA's staged FC rows
                 if (p.pred_smem) {
-                    if (tid == 0) issue_predictor(l + 1);
+                    if (warp == 0) issue_predictor(l + 1);
                     inflight = l + 1;
                 } else if (tid == 0) {
                     for (int k = 0; k < ns && k < nunits; ++k) issue_unit(p.layers[l + 1], k);
@@ -425,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
         if (l == 0) {
             for (int i = tid; i < d; i += kThreads) xf[i] = __half2float(p.x_in[i]);
         } else {
-            constexpr int NY = 2 * NCH;   // d <= NCH * 4096: at most 2*NCH float4 of y per thread
+            constexpr int NY = 2 * NCH;   // d <= NCH * kCols: at most 2*NCH float4 of y per thread
             float4 yv[NY];
 #pragma unroll
             for (int b = 0; b < NY; ++b) {
@@ -440,23 +518,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
             }
             __syncthreads();
             const float rs = rs_s;
+            auto put_x = [&](int i4, const float4& y4) {
+                const __half h0 = __float2half_rn(y4.x * rs), h1 = __float2half_rn(y4.y * rs);
+                const __half h2 = __float2half_rn(y4.z * rs), h3 = __float2half_rn(y4.w * rs);
+                reinterpret_cast<float4*>(xf)[i4] =
+                    make_float4(__half2float(h0), __half2float(h1), __half2float(h2), __half2float(h3));
+                if (p.x_trace && c == 0) {
+                    __half* xt = p.x_trace + (size_t)(l - 1) * d + i4 * 4;
+                    xt[0] = h0;
+                    xt[1] = h1;
+                    xt[2] = h2;
+                    xt[3] = h3;
+                }
+            };
 #pragma unroll
             for (int b = 0; b < NY; ++b) {
                 const int i4 = tid + b * kThreads;
-                if (i4 < d / 4) {
-                    const __half h0 = __float2half_rn(yv[b].x * rs), h1 = __float2half_rn(yv[b].y * rs);
-                    const __half h2 = __float2half_rn(yv[b].z * rs), h3 = __float2half_rn(yv[b].w * rs);
-                    reinterpret_cast<float4*>(xf)[i4] =
-                        make_float4(__half2float(h0), __half2float(h1), __half2float(h2), __half2float(h3));
-                    if (p.x_trace && c == 0) {
-                        __half* xt = p.x_trace + (size_t)(l - 1) * d + i4 * 4;
-                        xt[0] = h0;
-                        xt[1] = h1;
-                        xt[2] = h2;
-                        xt[3] = h3;
-                    }
-                }
+                if (i4 < d / 4) put_x(i4, yv[b]);
             }
+            // columns past the register-prefetched ones
+            for (int i4 = tid + NY * kThreads; i4 < d / 4; i4 += kThreads) put_x(i4, ld_cg4(p.xy + i4 * 4));
         }
         __syncthreads();
         PI_STAMP(l, 1);
@@ -502,7 +583,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
         {
             const int nvec = r / 8;
             const int vpl = (nvec + 31) / 32;
-            // this CTA's units [um0, um1): one warp per unit of 16 rows.  Lane L
+            // this CTA's units: one warp per unit of 16 rows (own pieces 2k and
+            // 2k+1, local row kk = 8 * piece + row in piece).  Lane L
             // accumulates, for each of the 16 rows, the products of the row's
             // vectors L, L+32, ... with u; a halving butterfly then leaves the
             // full dot product of row (L >> 1) in lanes L (16 shuffles for 16
@@ -512,12 +594,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
             // order by one warp, so a wait never sees an older phase of its slot.
             const int mstep = ns > 0 ? ns : kWarps;
             const bool unit_warp = ns == 0 || warp < ns;
-            for (int m = um0 + warp; unit_warp && m < um1; m += mstep) {
-                const int rbase = m * 16;
+            for (int m = warp; unit_warp && m < nunits; m += mstep) {
+                // first rows of the unit's two pieces (F: no second piece)
+                const int pb0 = 8 * piece_of(2 * m);
+                const int pb1 = 2 * m + 1 < npc ? 8 * piece_of(2 * m + 1) : F;
                 const __half* p2r = nullptr;   // this unit's rows in the ring
                 if (ns > 0) {
-                    const int k = m - um0;     // k % ns == warp
-                    if (!mbar_wait(&ring_full[warp], (unsigned)((l * ring_per_layer(warp) + k / ns) & 1), tmo, &bad))
+                    if (!mbar_wait(&ring_full[warp], (unsigned)((l * ring_per_layer(warp) + m / ns) & 1), tmo, &bad))
                         break;
                     p2r = reinterpret_cast<const __half*>(ring + (size_t)warp * p.ring_unit);
                 }
@@ -542,12 +625,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                         uint4 w[8];
 #pragma unroll
                         for (int k = 0; k < 8; ++k) {
-                            const int row = min(rbase + 8 * h + k, F - 1);
+                            // rows past F (short last piece, missing second piece) read
+                            // a row in bounds; their result is never used
+                            const int kk = 8 * h + k;
                             w[k] = p.pred_smem
-                                       ? *reinterpret_cast<const uint4*>(p2s + (size_t)(row - row0) * r + vc * 8)
+                                       ? *reinterpret_cast<const uint4*>(p2s + (size_t)(16 * m + kk) * r + vc * 8)
                                    : p2r != nullptr
-                                       ? *reinterpret_cast<const uint4*>(p2r + (size_t)(row - rbase) * r + vc * 8)
-                                       : ld_stream16(ly.p2 + (size_t)row * r + vc * 8);
+                                       ? *reinterpret_cast<const uint4*>(p2r + (size_t)kk * r + vc * 8)
+                                       : ld_stream16(ly.p2 + (size_t)min((h ? pb1 : pb0) + k, F - 1) * r + vc * 8);
                         }
 #pragma unroll
                         for (int k = 0; k < 8; ++k) {
@@ -590,17 +675,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                 v[0] += __shfl_xor_sync(FULL, v[0], 1);
                 // lane L now holds row k = 8*b16 + 4*b8 + 2*b4 + b2 of the unit
                 const int k = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
-                const int row = rbase + k;
+                const int row = (k < 8 ? pb0 : pb1) + (k & 7);
                 bool pred = false;
                 if (row < F && (lane & 1) == 0) {
-                    const int rl = row - row0;
-                    const float bk = (p.pred_smem && rl < ((row1 - row0) & ~7)) ? __half2float(b1s[rl])
-                                                                               : __half2float(ly.b1[row]);
+                    // staged bias of whole pieces
+                    const bool staged = p.pred_smem && (k < 8 ? pb0 + 8 <= F : pb1 + 8 <= F);
+                    const float bk = staged ? __half2float(b1s[16 * m + k]) : __half2float(ly.b1[row]);
                     pred = v[0] + bk > p.tau;
                 }
                 const unsigned bal = __ballot_sync(FULL, pred);
-                // the unit's slot is read: refill it with unit k + ns of this layer
-                if (ns > 0 && lane == 0 && m - um0 + ns < nunits) issue_unit(ly, m - um0 + ns);
+                // the unit's slot is read: refill it with unit m + ns of this layer
+                if (ns > 0 && lane == 0 && m + ns < nunits) issue_unit(ly, m + ns);
                 if (lane == 0) {
                     unsigned bits = 0;
                     // the bit of row kk(L) sits at ballot position L (even lanes)
@@ -609,288 +694,315 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                         const int kk = ((L2 >> 4) & 1) * 8 + ((L2 >> 3) & 1) * 4 + ((L2 >> 2) & 1) * 2 + ((L2 >> 1) & 1);
                         bits |= ((bal >> L2) & 1u) << kk;
                     }
-                    reinterpret_cast<uint16_t*>(p.xmask)[m] = (uint16_t)bits;
-                    if (l == p.L - 1) reinterpret_cast<uint16_t*>(p.mask_out)[m] = (uint16_t)bits;
+                    ubits[m] = (uint16_t)bits;
+                    if (l == p.L - 1) {
+                        uint8_t* mb = reinterpret_cast<uint8_t*>(p.mask_out);
+                        mb[pb0 / 8] = (uint8_t)(bits & 0xFFu);
+                        if (pb1 < F) mb[pb1 / 8] = (uint8_t)(bits >> 8);
+                    }
                 }
             }
-            if ((M & 1) && c == 0 && tid == 0) {
-                reinterpret_cast<uint16_t*>(p.xmask)[M] = 0;   // bits past F
-                if (l == p.L - 1) reinterpret_cast<uint16_t*>(p.mask_out)[M] = 0;
+            if (l == p.L - 1 && c == 0) {
+                // mask bytes past the last piece
+                uint8_t* mb = reinterpret_cast<uint8_t*>(p.mask_out);
+                for (int b = P + tid; b < 4 * p.W; b += kThreads) mb[b] = 0;
             }
         }
-        if (!sync()) { leave(); return; }
+        __syncthreads();
         PI_STAMP(l, 3);
 
-        // ---------------------------------------------------------- phase C
-        int n_total;
-        {
-            // every CTA reads the whole mask (coalesced) and scans it
-            for (int w = tid; w < p.W; w += kThreads) reinterpret_cast<uint32_t*>(m16)[w] = __ldcg(p.xmask + w);
+        if (*(volatile int*)&bad) { leave(); return; }
+
+        // ---------------------------------------------------------- phase B, FFN
+        // this CTA's active rows, in unit order (a fixed order: FC2 sums them in it)
+        if (warp == 0) {
+            int base = 0;
+            for (int m0 = 0; m0 < nunits; m0 += 32) {
+                const int m = m0 + lane;
+                const unsigned bits = m < nunits ? (unsigned)ubits[m] : 0u;
+                const int cnt = __popc(bits);
+                int incl = cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int t = __shfl_up_sync(FULL, incl, o);
+                    if (lane >= o) incl += t;
+                }
+                int pos = base + incl - cnt;
+                if (m < nunits) {
+                    const int pb0 = 8 * piece_of(2 * m);
+                    const int pb1 = 2 * m + 1 < npc ? 8 * piece_of(2 * m + 1) : F;
+                    unsigned b = bits;
+                    while (b) {
+                        const int kk = __ffs(b) - 1;
+                        b &= b - 1u;
+                        lidx[pos++] = (kk < 8 ? pb0 : pb1) + (kk & 7);
+                    }
+                }
+                base += __shfl_sync(FULL, incl, 31);
+            }
+            if (lane == 0) nmine_s = base;
+        }
+        __syncthreads();
+        const int nmine = nmine_s;
+        if (p.layer_counts && tid == 0 && nmine) atomicAdd(p.layer_counts + 2 * l, nmine);
+        // FC1 bias of row k: own piece k / 8 / G holds it in the staged slice
+        // (whole pieces); read before the FC rows overwrite the slice
+        auto bias_of = [&](int k) -> float {
+            const int gp = k >> 3;
+            return p.pred_smem && 8 * gp + 8 <= F ? __half2float(b1s[8 * (gp / G) + (k & 7)])
+                                                  : __half2float(ly.b1[k]);
+        };
+        if (p.pred_smem) {
+            for (int q = tid; q < nmine; q += kThreads) lh[q] = bias_of(lidx[q]);
             __syncthreads();
-            const int per = (M + kThreads - 1) / kThreads;
-            int cnt = 0;
-            for (int e = 0; e < per; ++e) {
-                const int m = tid * per + e;
-                if (m < M) cnt += __popc((unsigned)m16[m]);
-            }
-            int total;
-            int run = block_exscan(cnt, scr, &total);
-            for (int e = 0; e < per; ++e) {
-                const int m = tid * per + e;
-                if (m < M) {
-                    upre[m] = run;
-                    run += __popc((unsigned)m16[m]);
-                }
-            }
-            if (tid == 0) upre[M] = total;
-            n_total = total;
         }
-        __syncthreads();
-        const int j0 = (int)((unsigned)n_total * (unsigned)c / (unsigned)G);
-        const int j1 = (int)((unsigned)n_total * (unsigned)(c + 1) / (unsigned)G);
-        const int nmine = j1 - j0;
-        // collect this CTA's neuron ids (storage rows) of list positions [j0, j1)
-        for (int m = tid; m < M; m += kThreads) {
-            const int lo = upre[m], hi = upre[m + 1];
-            if (hi <= j0 || lo >= j1) continue;
-            unsigned bits = (unsigned)m16[m];
-            int pos = lo;
-            while (bits) {
-                const int b = __ffs(bits) - 1;
-                bits &= bits - 1u;
-                if (pos >= j0 && pos < j1) {
-                    lidx[pos - j0] = m * 16 + b;
-                    if (l == p.L - 1) p.idx_out[pos] = m * 16 + b;
-                }
-                ++pos;
-            }
-        }
-        if (l == p.L - 1 && c == 0 && tid == 0) *p.count_out = n_total;
-        __syncthreads();
-        // few rows per CTA: stage all of this CTA's FC1 rows, then its W2t rows, in
-        // shared memory now with bulk copies (FC1 rows first, so they arrive
-        // first); W2t rows of neurons whose FC1 output turns out to be zero are
-        // loaded but not used.  The region held this layer's predictor slices,
-        // consumed before the last grid barrier.
-        // FC1 rows are staged whenever they fit; W2t rows too when both fit
-        const bool w1_staged = nmine > 0 && nmine * fc1_rows * wrow <= p.stage_bytes;
-        const bool w2_staged = w1_staged && nmine * (fc1_rows + 1) * wrow <= p.stage_bytes;
+        // few rows per CTA: stage its FC1 rows and as many W2t rows as fit besides
+        // them in shared memory now with bulk copies (FC1 rows first, so they
+        // arrive first); the remaining W2t rows follow into the FC1 rows' place
+        // once FC1 has read them.  W2t rows of neurons whose FC1 output turns
+        // out to be zero are loaded but not used.  The region held this layer's
+        // predictor slices (or P2 ring), read by now.
+        const int w1b = nmine * fc1_rows * wrow;
+        const bool w1_staged = nmine > 0 && w1b <= p.stage_bytes;
+        const int n2a = w1_staged ? min(nmine, (p.stage_bytes - w1b) / wrow) : min(nmine, p.stage_bytes / wrow);
+        const bool late = w1_staged && n2a < nmine;   // W2t rows [n2a, nmine) staged after FC1
         unsigned char* s_w1 = stage;                                  // [nmine] W1 (gate) rows
         unsigned char* s_wu = stage + (size_t)nmine * wrow;           // [nmine] up rows (gated)
-        unsigned char* s_w2 = stage + (size_t)nmine * fc1_rows * wrow;  // [nmine] W2t rows
-        if (w1_staged) {
-            if (tid == 0) {
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                mbar_arrive_expect_tx(&w1_mbar, (unsigned)(nmine * fc1_rows * wrow));
-                if (w2_staged) mbar_arrive_expect_tx(&w2_mbar, (unsigned)(nmine * wrow));
-                auto stage_row = [&](unsigned char* dst, const void* codes, const __half* scales, size_t k,
-                                     unsigned long long* mb) {
-                    if (KIND != 2) {
-                        bulk_g2s(dst, static_cast<const __half*>(codes) + k * d, 2u * d, mb);
-                    } else {
-                        bulk_g2s(dst, static_cast<const uint8_t*>(codes) + k * (d / 2), (unsigned)(d / 2), mb);
-                        bulk_g2s(dst + d / 2, scales + k * (d / 32), (unsigned)(d / 16), mb);
-                    }
-                };
-                for (int q = 0; q < nmine; ++q)
+        unsigned char* s_w2 = stage + (w1_staged ? (size_t)w1b : 0);  // [n2a] W2t rows
+        auto stage_row = [&](unsigned char* dst, const void* codes, const __half* scales, size_t k,
+                             unsigned long long* mb) {
+            if (KIND != 2) {
+                bulk_g2s(dst, static_cast<const __half*>(codes) + k * d, 2u * d, mb);
+            } else {
+                bulk_g2s(dst, static_cast<const uint8_t*>(codes) + k * (d / 2), (unsigned)(d / 2), mb);
+                bulk_g2s(dst + d / 2, scales + k * (d / 32), (unsigned)(d / 16), mb);
+            }
+        };
+        if (warp == 0 && (w1_staged || n2a > 0)) {
+            // lane 0 arms the mbarriers, then the 32 lanes issue the row copies
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            if (lane == 0) {
+                if (w1_staged) mbar_arrive_expect_tx(&w1_mbar, (unsigned)w1b);
+                if (n2a > 0) mbar_arrive_expect_tx(&w2_mbar, (unsigned)(n2a * wrow));
+            }
+            __syncwarp();
+            if (w1_staged) {
+                for (int q = lane; q < nmine; q += 32)
                     stage_row(s_w1 + (size_t)q * wrow, ly.w1, ly.w1s, (size_t)lidx[q], &w1_mbar);
                 if (KIND == 1)
-                    for (int q = 0; q < nmine; ++q)
+                    for (int q = lane; q < nmine; q += 32)
                         stage_row(s_wu + (size_t)q * wrow, ly.wu, nullptr, (size_t)lidx[q], &w1_mbar);
-                if (w2_staged)
-                    for (int q = 0; q < nmine; ++q)
-                        stage_row(s_w2 + (size_t)q * wrow, ly.w2t, ly.w2ts, (size_t)lidx[q], &w2_mbar);
             }
+            for (int q = lane; q < n2a; q += 32)
+                stage_row(s_w2 + (size_t)q * wrow, ly.w2t, ly.w2ts, (size_t)lidx[q], &w2_mbar);
+        }
+        if (w1_staged) {
             ++w1_uses;
             w1_pending = true;
-            if (w2_staged) {
-                ++w2_uses;
-                w2_pending = true;
-            }
+        }
+        if (n2a > 0) {
+            ++w2_uses;
+            w2_pending = true;
         }
 
-        // FC1: (neuron, segment) items spread over all warps so that every warp
-        // has loads in flight; segment dot products are combined in a fixed order
+        // FC1, the whole CTA on RB rows at a time (8; 4 gate + up pairs): thread
+        // t takes the 8-element words t, t + kThreads, ... of the rows (x read once per
+        // word and batch, used for RB rows); fold reduces a warp's partials, and
+        // the 16 warp sums of a row are added in a fixed order.  Rows come from the staged copies or,
+        // when they did not fit, straight from global memory.
         {
-            for (int q = tid; q < nmine; q += kThreads) lh[q] = __half2float(ly.b1[lidx[q]]);  // bias
-            const int ng = d / 32;
-            const int maxseg = KIND == 2 ? max(1, ng / 32) : max(1, d / 256);
-            int nseg = nmine > 0 ? kWarps / nmine : 1;
-            nseg = max(1, min(nseg, maxseg));
-            const int segE = KIND == 2 ? ((ng + nseg - 1) / nseg + 31) / 32 * 32   // groups
-                                       : ((d + nseg - 1) / nseg + 255) / 256 * 256;  // elements
-            nseg = KIND == 2 ? (ng + segE - 1) / segE : (d + segE - 1) / segE;
-            float* part = red;           // [nmine * nseg]
-            float* partu = red + 2048;   // gated: up-projection partials
+            if (!p.pred_smem)
+                for (int q = tid; q < nmine; q += kThreads) lh[q] = bias_of(lidx[q]);
             if (w1_staged && mbar_wait(&w1_mbar, (w1_uses - 1) & 1u, tmo, &bad)) w1_pending = false;
-            for (int it = warp; it < nmine * nseg; it += kWarps) {
-                const int q = it / nseg, sg = it % nseg;
-                const int k = lidx[q];
-                float acc = 0.f, accu = 0.f;
-                if (KIND != 2) {
-                    const int e0 = sg * segE, e1 = min(d, e0 + segE);
-                    if (w1_staged) {
-                        const __half* row = reinterpret_cast<const __half*>(s_w1 + (size_t)q * wrow);
-                        const __half* rowu = reinterpret_cast<const __half*>(s_wu + (size_t)q * wrow);
-#pragma unroll 4
-                        for (int e = e0 + lane * 8; e < e1; e += 256) {
-                            acc += dot8(*reinterpret_cast<const uint4*>(row + e), xf + e);
-                            if (KIND == 1) accu += dot8(*reinterpret_cast<const uint4*>(rowu + e), xf + e);
-                        }
-                    } else {
-                        const __half* row = static_cast<const __half*>(ly.w1) + (size_t)k * d;
-                        const __half* rowu = KIND == 1 ? ly.wu + (size_t)k * d : nullptr;
-#pragma unroll 8
-                        for (int e = e0 + lane * 8; e < e1; e += 256) {
-                            acc += dot8(ld_stream16(row + e), xf + e);
-                            if (KIND == 1) accu += dot8(ld_stream16(rowu + e), xf + e);
+            float* part = red;           // [128 rows][kWarps]
+            float* partu = red + 2048;   // gated: up-projection partials
+            const int nwd = d / 8;
+            constexpr int RB = KIND == 1 ? 4 : 8;
+            // rows [qb, qe) (at most 128); word(q, wd, cw, sc) / up(q, wd) fetch
+            // word wd of row q (fp16: 8 weights in a uint4; INT4: the code word in
+            // cw.x and its group scale in sc)
+            auto fc1_block = [&](int qb, int qe, auto word, auto up) {
+                for (int q0 = qb; q0 < qe; q0 += RB) {
+                    float v[RB], vu[RB];
+#pragma unroll
+                    for (int b = 0; b < RB; ++b) v[b] = vu[b] = 0.f;
+                    for (int wd = tid; wd < nwd; wd += kThreads) {
+                        const float4 xa = reinterpret_cast<const float4*>(xf)[2 * wd];
+                        const float4 xb = reinterpret_cast<const float4*>(xf)[2 * wd + 1];
+#pragma unroll
+                        for (int b = 0; b < RB; ++b) {
+                            const int q = q0 + b;
+                            if (q >= qe) break;
+                            uint4 cw;
+                            float sc;
+                            word(q, wd, cw, sc);
+                            if (KIND != 2) {
+                                v[b] += dot8r(cw, xa, xb);
+                                if (KIND == 1) vu[b] += dot8r(up(q, wd), xa, xb);
+                            } else {
+                                v[b] = fmaf(sc, dotq8r(cw.x, xa, xb), v[b]);
+                            }
                         }
                     }
+                    const int rb = fold_row<RB>(lane);
+                    const float tv = fold<RB>(v, lane);
+                    const float tu = KIND == 1 ? fold<RB>(vu, lane) : 0.f;
+                    if ((lane & (32 / RB - 1)) == 0 && q0 + rb < qe) {
+                        part[(q0 - qb + rb) * kWarps + warp] = tv;
+                        if (KIND == 1) partu[(q0 - qb + rb) * kWarps + warp] = tu;
+                    }
+                }
+            };
+            const __half* w1g = static_cast<const __half*>(ly.w1);
+            const uint8_t* w1q = static_cast<const uint8_t*>(ly.w1);
+            const __half* w1sg = ly.w1s;
+            const __half* wug = ly.wu;
+            for (int qb = 0; qb < nmine; qb += 128) {
+                const int qe = min(nmine, qb + 128);
+                if (w1_staged) {
+                    fc1_block(
+                        qb, qe,
+                        [&](int q, int wd, uint4& cw, float& sc) {
+                            const unsigned char* row = s_w1 + (size_t)q * wrow;
+                            if (KIND != 2) {
+                                cw = reinterpret_cast<const uint4*>(row)[wd];
+                            } else {
+                                cw.x = reinterpret_cast<const uint32_t*>(row)[wd];
+                                sc = __half2float(reinterpret_cast<const __half*>(row + d / 2)[wd >> 2]);
+                            }
+                        },
+                        [&](int q, int wd) { return reinterpret_cast<const uint4*>(s_wu + (size_t)q * wrow)[wd]; });
                 } else {
-                    // lane L takes the 8-element words L, L+32, ... of the
-                    // segment (4 lanes per scale group): 4-byte code loads and
-                    // x loads 32 bytes apart across lanes, the two 16-byte
-                    // halves swapped on lanes with bit 2 set so that the 8
-                    // lanes of a shared-memory phase hit 8 different bank groups
-                    const int gs0 = sg * segE, gs1 = min(ng, gs0 + segE);
-                    const uint8_t* row = w1_staged ? s_w1 + (size_t)q * wrow
-                                                   : static_cast<const uint8_t*>(ly.w1) + (size_t)k * (d / 2);
-                    const __half* sc = w1_staged ? reinterpret_cast<const __half*>(s_w1 + (size_t)q * wrow + d / 2)
-                                                 : ly.w1s + (size_t)k * ng;
-                    const int sw = (lane >> 2) & 1;
-#pragma unroll 4
-                    for (int wd = 4 * gs0 + lane; wd < 4 * gs1; wd += 32) {
-                        uint32_t cw;
-                        if (w1_staged)
-                            cw = *reinterpret_cast<const uint32_t*>(row + (size_t)wd * 4);
-                        else
-                            asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(cw) : "l"(row + (size_t)wd * 4));
-                        const float s = __half2float(sc[wd >> 2]);
-                        float qf[8];
-                        q8_to_f8(cw, qf);
-                        const float4* xp = reinterpret_cast<const float4*>(xf + (size_t)wd * 8);
-                        const float4 x0 = xp[sw], x1 = xp[sw ^ 1];
-                        const float4 xa = sw ? x1 : x0, xb = sw ? x0 : x1;
-                        float pt = qf[0] * xa.x;
-                        pt = fmaf(qf[1], xa.y, pt);
-                        pt = fmaf(qf[2], xa.z, pt);
-                        pt = fmaf(qf[3], xa.w, pt);
-                        pt = fmaf(qf[4], xb.x, pt);
-                        pt = fmaf(qf[5], xb.y, pt);
-                        pt = fmaf(qf[6], xb.z, pt);
-                        pt = fmaf(qf[7], xb.w, pt);
-                        acc = fmaf(s, pt, acc);
+                    fc1_block(
+                        qb, qe,
+                        [&](int q, int wd, uint4& cw, float& sc) {
+                            const size_t k = (size_t)lidx[q];
+                            if (KIND != 2) {
+                                cw = ld_stream16(w1g + k * d + 8 * wd);
+                            } else {
+                                asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];"
+                                    : "=r"(cw.x)
+                                    : "l"(w1q + k * (d / 2) + 4 * wd));
+                                sc = __half2float(w1sg[k * (d / 32) + (wd >> 2)]);
+                            }
+                        },
+                        [&](int q, int wd) { return ld_stream16(wug + (size_t)lidx[q] * d + 8 * wd); });
+                }
+                __syncthreads();
+                for (int q = qb + tid; q < qe; q += kThreads) {
+                    float z = 0.f, zu = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kWarps; ++w) {
+                        z += part[(q - qb) * kWarps + w];
+                        if (KIND == 1) zu += partu[(q - qb) * kWarps + w];
                     }
+                    z += lh[q];
+                    float hv = z > 0.f ? z : 0.f;
+                    if (KIND == 1) hv *= zu;
+                    lh[q] = hv;
                 }
-                acc = warp_sum(acc);
-                if (KIND == 1) accu = warp_sum(accu);
-                if (lane == 0) {
-                    part[it] = acc;
-                    if (KIND == 1) partu[it] = accu;
-                }
-            }
-            __syncthreads();
-            for (int q = tid; q < nmine; q += kThreads) {
-                float z = 0.f, zu = 0.f;
-                for (int sg = 0; sg < nseg; ++sg) {
-                    z += part[q * nseg + sg];
-                    if (KIND == 1) zu += partu[q * nseg + sg];
-                }
-                z += lh[q];
-                float hv = z > 0.f ? z : 0.f;
-                if (KIND == 1) hv *= zu;
-                lh[q] = hv;
-                if (l == p.L - 1) p.h_out[j0 + q] = hv;
+                __syncthreads();
             }
             if (p.layer_counts) {
                 int nz = 0;
                 for (int q = tid; q < nmine; q += kThreads) nz += lh[q] != 0.f ? 1 : 0;
                 nz = __reduce_add_sync(FULL, nz);
                 if (lane == 0 && nz) atomicAdd(p.layer_counts + 2 * l + 1, nz);
-                if (c == 0 && tid == 0) p.layer_counts[2 * l] = n_total;
             }
         }
-        __syncthreads();
+        // FC1 has read its rows: the W2t rows that did not fit take their place
+        if (late) {
+            if (warp == 0) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                if (lane == 0) mbar_arrive_expect_tx(&w1_mbar, (unsigned)((nmine - n2a) * wrow));
+                __syncwarp();
+                for (int q = n2a + lane; q < nmine; q += 32)
+                    stage_row(stage + (size_t)(q - n2a) * wrow, ly.w2t, ly.w2ts, (size_t)lidx[q], &w1_mbar);
+            }
+            ++w1_uses;
+            w1_pending = true;
+        }
         PI_STAMP(l, 4);
 
         // FC2: the whole CTA accumulates its neurons' W2t rows; rows whose
-        // FC1 output is zero are skipped (ReLU removed them from FC2)
-        if (w2_staged && mbar_wait(&w2_mbar, (w2_uses - 1) & 1u, tmo, &bad)) w2_pending = false;
-        if (KIND != 2 && w2_staged) {
-            float acc[NCH][8];
-#pragma unroll
-            for (int ch = 0; ch < NCH; ++ch)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[ch][e] = 0.f;
-            for (int q = 0; q < nmine; ++q) {
-                const float hq = lh[q];
-                if (hq == 0.f) continue;
-                const __half* row = reinterpret_cast<const __half*>(s_w2 + (size_t)q * wrow);
-#pragma unroll
-                for (int ch = 0; ch < NCH; ++ch) {
-                    const int col = ch * 4096 + tid * 8;
-                    if (col < d) {
-                        float wf[8];
-                        h8_to_f8(*reinterpret_cast<const uint4*>(row + col), wf);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[ch][e] = fmaf(hq, wf[e], acc[ch][e]);
-                    }
-                }
+        // FC1 output is zero are skipped (ReLU removed them from FC2).  Row q's
+        // W2t data: staged early (q < n2a), staged after FC1 (late), or read
+        // from global memory.
+        // rows [qa, qe): load(q, col) fetches 16 bytes of row q at column col
+        // (fp16: 8 weights; INT4: 32 codes) and, for INT4, the group scale in sc
+        const __half* w2g = static_cast<const __half*>(ly.w2t);
+        const uint8_t* w2q = static_cast<const uint8_t*>(ly.w2t);
+        const __half* w2sg = ly.w2ts;
+        auto smem_rows = [&](const unsigned char* base, int q0) {
+            return [=](int q, int col, float& sc) {
+                const unsigned char* row = base + (size_t)(q - q0) * wrow;
+                if (KIND == 2) sc = __half2float(reinterpret_cast<const __half*>(row + d / 2)[col / 32]);
+                return *reinterpret_cast<const uint4*>(row + (KIND == 2 ? col / 2 : 2 * col));
+            };
+        };
+        auto global_rows = [&](int q, int col, float& sc) {
+            const size_t k = (size_t)lidx[q];
+            if (KIND == 2) {
+                sc = __half2float(w2sg[k * (d / 32) + col / 32]);
+                return ld_stream16(w2q + k * (d / 2) + col / 2);
             }
-            issue_next();
-            float* dst = p.xyp + (size_t)c * d;
-#pragma unroll
-            for (int ch = 0; ch < NCH; ++ch) {
-                const int col = ch * 4096 + tid * 8;
-                if (col < d) {
-                    float4* o = reinterpret_cast<float4*>(dst + col);
-                    __stcg(o, make_float4(acc[ch][0], acc[ch][1], acc[ch][2], acc[ch][3]));
-                    __stcg(o + 1, make_float4(acc[ch][4], acc[ch][5], acc[ch][6], acc[ch][7]));
-                }
-            }
-        } else if (KIND != 2) {
+            return ld_stream16(w2g + k * d + col);
+        };
+        if (n2a > 0 && mbar_wait(&w2_mbar, (w2_uses - 1) & 1u, tmo, &bad)) w2_pending = false;
+        if (KIND != 2) {
             constexpr int RB = NCH == 1 ? 4 : (NCH == 2 ? 2 : 1);
             float acc[NCH][8];
 #pragma unroll
             for (int ch = 0; ch < NCH; ++ch)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) acc[ch][e] = 0.f;
-            for (int q0 = 0; q0 < nmine; q0 += RB) {
-                uint4 wv[RB][NCH];
-                float hv[RB];
+            auto fc2_rows = [&](int qa, int qe, auto load) {
+                for (int q0 = qa; q0 < qe; q0 += RB) {
+                    uint4 wv[RB][NCH];
+                    float hv[RB];
 #pragma unroll
-                for (int b = 0; b < RB; ++b) {
-                    const int q = q0 + b;
-                    hv[b] = q < nmine ? lh[q] : 0.f;
-                    if (hv[b] != 0.f) {
-                        const __half* row = static_cast<const __half*>(ly.w2t) + (size_t)lidx[q] * d;
+                    for (int b = 0; b < RB; ++b) {
+                        const int q = q0 + b;
+                        hv[b] = q < qe ? lh[q] : 0.f;
+                        if (hv[b] != 0.f) {
+#pragma unroll
+                            for (int ch = 0; ch < NCH; ++ch) {
+                                const int col = ch * kCols + tid * 8;
+                                float sc;
+                                if (col < d) wv[b][ch] = load(q, col, sc);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int b = 0; b < RB; ++b) {
+                        if (hv[b] == 0.f) continue;
 #pragma unroll
                         for (int ch = 0; ch < NCH; ++ch) {
-                            const int col = ch * 4096 + tid * 8;
-                            if (col < d) wv[b][ch] = ld_stream16(row + col);
+                            const int col = ch * kCols + tid * 8;
+                            if (col < d) {
+                                float wf[8];
+                                h8_to_f8(wv[b][ch], wf);
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) acc[ch][e] = fmaf(hv[b], wf[e], acc[ch][e]);
+                            }
                         }
                     }
                 }
-#pragma unroll
-                for (int b = 0; b < RB; ++b) {
-                    if (hv[b] == 0.f) continue;
-#pragma unroll
-                    for (int ch = 0; ch < NCH; ++ch) {
-                        const int col = ch * 4096 + tid * 8;
-                        if (col < d) {
-                            float wf[8];
-                            h8_to_f8(wv[b][ch], wf);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) acc[ch][e] = fmaf(hv[b], wf[e], acc[ch][e]);
-                        }
-                    }
+            };
+            if (n2a > 0) fc2_rows(0, n2a, smem_rows(s_w2, 0));
+            if (nmine > n2a) {
+                if (late) {
+                    if (mbar_wait(&w1_mbar, (w1_uses - 1) & 1u, tmo, &bad)) w1_pending = false;
+                    fc2_rows(n2a, nmine, smem_rows(stage, n2a));
+                } else {
+                    fc2_rows(n2a, nmine, global_rows);
                 }
             }
             issue_next();
             float* dst = p.xyp + (size_t)c * d;
 #pragma unroll
             for (int ch = 0; ch < NCH; ++ch) {
-                const int col = ch * 4096 + tid * 8;
+                const int col = ch * kCols + tid * 8;
                 if (col < d) {
                     float4* o = reinterpret_cast<float4*>(dst + col);
                     __stcg(o, make_float4(acc[ch][0], acc[ch][1], acc[ch][2], acc[ch][3]));
@@ -898,51 +1010,68 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                 }
             }
         } else {
-            // INT4: each thread owns 32 consecutive columns (one scale group)
-            float acc[32];
+            // INT4: a thread owns scale groups tid and tid + kThreads (32
+            // consecutive columns each)
+            constexpr int NG = 2;
+            float acc[NG][32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-            const int col = tid * 32;
-            const bool mine = col < d;
-            for (int q0 = 0; q0 < nmine; q0 += 4) {
-                uint4 wv[4];
-                float hs[4];
+            for (int g = 0; g < NG; ++g)
 #pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    const int q = q0 + b;
-                    const float hv = q < nmine ? lh[q] : 0.f;
-                    hs[b] = 0.f;
-                    if (hv != 0.f && mine) {
-                        if (w2_staged) {
-                            const unsigned char* row = s_w2 + (size_t)q * wrow;
-                            wv[b] = *reinterpret_cast<const uint4*>(row + col / 2);
-                            hs[b] = hv * __half2float(reinterpret_cast<const __half*>(row + d / 2)[col / 32]);
-                        } else {
-                            const size_t k = (size_t)lidx[q];
-                            wv[b] = ld_stream16(static_cast<const uint8_t*>(ly.w2t) + k * (d / 2) + col / 2);
-                            hs[b] = hv * __half2float(ly.w2ts[k * (d / 32) + col / 32]);
+                for (int e = 0; e < 32; ++e) acc[g][e] = 0.f;
+            auto fc2_rows = [&](int qa, int qe, auto load) {
+                for (int q0 = qa; q0 < qe; q0 += 2) {
+                    uint4 wv[2][NG];
+                    float hs[2][NG];
+#pragma unroll
+                    for (int b = 0; b < 2; ++b) {
+                        const int q = q0 + b;
+                        const float hv = q < qe ? lh[q] : 0.f;
+#pragma unroll
+                        for (int g = 0; g < NG; ++g) {
+                            const int col = (tid + g * kThreads) * 32;
+                            hs[b][g] = 0.f;
+                            if (hv != 0.f && col < d) {
+                                float sc;
+                                wv[b][g] = load(q, col, sc);
+                                hs[b][g] = hv * sc;
+                            }
                         }
                     }
+#pragma unroll
+                    for (int b = 0; b < 2; ++b)
+#pragma unroll
+                        for (int g = 0; g < NG; ++g) {
+                            if (hs[b][g] == 0.f) continue;
+                            const uint32_t qw[4] = {wv[b][g].x, wv[b][g].y, wv[b][g].z, wv[b][g].w};
+#pragma unroll
+                            for (int wi = 0; wi < 4; ++wi) {
+                                float qf[8];
+                                q8_to_f8(qw[wi], qf);
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) acc[g][wi * 8 + e] = fmaf(hs[b][g], qf[e], acc[g][wi * 8 + e]);
+                            }
+                        }
                 }
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    if (hs[b] == 0.f) continue;
-                    const uint32_t qw[4] = {wv[b].x, wv[b].y, wv[b].z, wv[b].w};
-#pragma unroll
-                    for (int wi = 0; wi < 4; ++wi) {
-                        float qf[8];
-                        q8_to_f8(qw[wi], qf);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[wi * 8 + e] = fmaf(hs[b], qf[e], acc[wi * 8 + e]);
-                    }
+            };
+            if (n2a > 0) fc2_rows(0, n2a, smem_rows(s_w2, 0));
+            if (nmine > n2a) {
+                if (late) {
+                    if (mbar_wait(&w1_mbar, (w1_uses - 1) & 1u, tmo, &bad)) w1_pending = false;
+                    fc2_rows(n2a, nmine, smem_rows(stage, n2a));
+                } else {
+                    fc2_rows(n2a, nmine, global_rows);
                 }
             }
             issue_next();
-            if (mine) {
-                float4* o = reinterpret_cast<float4*>(p.xyp + (size_t)c * d + col);
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    __stcg(o + e, make_float4(acc[4 * e], acc[4 * e + 1], acc[4 * e + 2], acc[4 * e + 3]));
+            for (int g = 0; g < NG; ++g) {
+                const int col = (tid + g * kThreads) * 32;
+                if (col < d) {
+                    float4* o = reinterpret_cast<float4*>(p.xyp + (size_t)c * d + col);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        __stcg(o + e, make_float4(acc[g][4 * e], acc[g][4 * e + 1], acc[g][4 * e + 2], acc[g][4 * e + 3]));
+                }
             }
         }
         PI_STAMP(l, 5);
@@ -1002,6 +1131,36 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                 }
             }
         }
+        if (l == p.L - 1) {
+            // the active list of the last layer in storage order: every CTA scans the
+            // whole mask (complete since the last barrier) and places its own rows
+            for (int w = tid; w < p.W; w += kThreads) reinterpret_cast<uint32_t*>(m16)[w] = __ldcg(p.mask_out + w);
+            __syncthreads();
+            const int per = (M + kThreads - 1) / kThreads;
+            int cnt = 0;
+            for (int e = 0; e < per; ++e) {
+                const int m = tid * per + e;
+                if (m < M) cnt += __popc((unsigned)m16[m]);
+            }
+            int total;
+            int run = block_exscan(cnt, scr, &total);
+            for (int e = 0; e < per; ++e) {
+                const int m = tid * per + e;
+                if (m < M) {
+                    upre[m] = run;
+                    run += __popc((unsigned)m16[m]);
+                }
+            }
+            __syncthreads();
+            const int nmine = nmine_s;
+            for (int q = tid; q < nmine; q += kThreads) {
+                const int k = lidx[q];
+                const int pos = upre[k >> 4] + __popc((unsigned)m16[k >> 4] & ((1u << (k & 15)) - 1u));
+                p.idx_out[pos] = k;
+                p.h_out[pos] = lh[q];
+            }
+            if (c == 0 && tid == 0) *p.count_out = total;
+        }
         PI_STAMP(l, 7);
         if (!sync()) { leave(); return; }
     }
@@ -1043,18 +1202,15 @@ cudaError_t launch_kind(const FusedParams& prm, int G, size_t smem, cudaStream_t
 
 size_t up256(size_t v) { return (v + 255) / 256 * 256; }
 
-// exchange region: epoch | counter | xu | xmask | xyp | xy | xss
+// exchange region: epoch | counter | xu | xyp | xy | xss
 struct XchgLayout {
-    size_t counter, xu, xmask, xyp, xy, xss, total;
-    XchgLayout(int d, int F, size_t rmax_su, int G) {
-        const int W = (F + 31) / 32;
+    size_t counter, xu, xyp, xy, xss, total;
+    XchgLayout(int d, size_t rmax_su, int G) {
         size_t off = 256;
         counter = off;
         off += 256;
         xu = off;
         off += up256(4ull * rmax_su);
-        xmask = off;
-        off += up256(4ull * W + 4);
         xyp = off;
         off += up256(4ull * (size_t)G * d);
         xy = off;
@@ -1065,23 +1221,28 @@ struct XchgLayout {
     }
 };
 
+// own units (two 8-row pieces) of a CTA at most
+int max_units(int F, int G) { return ((F + 7) / 8 + 2 * G - 1) / (2 * G); }
+
 SmemPlan smem_plan(int d, int F, int rmax, size_t rmax_su, int G) {
-    return SmemPlan{d, rmax < 8 ? 8 : rmax, (int)rmax_su, (F + 15) / 16, F / G + 2};
+    return SmemPlan{d, rmax < 8 ? 8 : rmax, (int)rmax_su, (F + 15) / 16, 16 * max_units(F, G)};
 }
 
 }  // namespace
 
-size_t fused_workspace_bytes(int d, int F, size_t rmax_su, int G) { return XchgLayout(d, F, rmax_su, G).total; }
+size_t fused_workspace_bytes(int d, int F, size_t rmax_su, int G) { return XchgLayout(d, rmax_su, G).total; }
 
 bool fused_supported(int d, int F, int rmax, bool int4, int G) {
-    if (d > 16384 || d % 8 != 0 || G < 1) return false;
-    if (int4 && d % 32 != 0) return false;
+    if (d % 8 != 0 || G < 1) return false;
+    if (!int4 && d > 4 * kCols) return false;              // FC2: 8 columns per thread and chunk
+    if (int4 && (d % 32 != 0 || d > 64 * kThreads)) return false;  // FC2: two groups per thread
+    if (max_units(F, G) > kMaxUnits) return false;
     const size_t rmax_su = (size_t)16 * G + 2 * (size_t)rmax;
     return smem_plan(d, F, rmax, rmax_su, G).bytes() <= 220 * 1024;
 }
 
 cudaError_t launch_fused(const FusedStackArgs& a, cudaStream_t s) {
-    if (a.L < 1 || a.L > kMaxFusedLayers) return cudaErrorInvalidValue;
+    if (a.L < 1 || a.L > kMaxFusedLayers || max_units(a.F, a.G) > kMaxUnits) return cudaErrorInvalidValue;
     FusedParams prm = {};
     const int G = a.G;
     prm.L = a.L;
@@ -1095,12 +1256,11 @@ cudaError_t launch_fused(const FusedStackArgs& a, cudaStream_t s) {
     prm.x_in = a.x_in;
     prm.y_out = a.y_out;
     prm.x_trace = a.x_trace;
-    const XchgLayout xl(a.d, a.F, a.rmax_su, G);
+    const XchgLayout xl(a.d, a.rmax_su, G);
     char* ws = static_cast<char*>(a.xchg);
     prm.epoch = reinterpret_cast<unsigned long long*>(ws);
     prm.counter = reinterpret_cast<unsigned*>(ws + xl.counter);
     prm.xu = reinterpret_cast<float*>(ws + xl.xu);
-    prm.xmask = reinterpret_cast<uint32_t*>(ws + xl.xmask);
     prm.xyp = reinterpret_cast<float*>(ws + xl.xyp);
     prm.xy = reinterpret_cast<float*>(ws + xl.xy);
     prm.xss = reinterpret_cast<float*>(ws + xl.xss);
@@ -1124,7 +1284,7 @@ cudaError_t launch_fused(const FusedStackArgs& a, cudaStream_t s) {
         f.p2 = w.p2;
         f.r = a.ranks[l];
         // at most one (row, split) item per warp of the grid; splits >= 256 elements
-        int su = (16 * G) / f.r;
+        int su = (kWarps * G) / f.r;
         const int max_su = (a.d + 255) / 256;
         if (su > max_su) su = max_su;
         if (su < 1) su = 1;
@@ -1142,7 +1302,7 @@ cudaError_t launch_fused(const FusedStackArgs& a, cudaStream_t s) {
             const size_t items = (size_t)f.r * f.su;
             p1b = std::max(p1b, ((items + G - 1) / G) * (size_t)f.seg * 2);
         }
-        const size_t units = ((size_t)prm.M + G - 1) / G;
+        const size_t units = (size_t)max_units(a.F, G);
         const size_t p2b = units * 16 * (size_t)rmax * 2, b1b = units * 16 * 2;
         auto r16 = [](size_t v) { return (int)((v + 15) / 16 * 16); };
         SmemPlan with = sp;
@@ -1177,8 +1337,8 @@ cudaError_t launch_fused(const FusedStackArgs& a, cudaStream_t s) {
     }
     const size_t smem = sp.bytes();
     if (smem > 227 * 1024) return cudaErrorInvalidValue;
-    if (a.int4) return launch_kind<2, 1>(prm, G, smem, s);
-    const int nch = (a.d + 4095) / 4096;
+    if (a.int4) return launch_kind<2, 4>(prm, G, smem, s);
+    const int nch = (a.d + kCols - 1) / kCols;
     if (a.gated) {
         if (nch == 1) return launch_kind<1, 1>(prm, G, smem, s);
         if (nch == 2) return launch_kind<1, 2>(prm, G, smem, s);
