@@ -108,11 +108,17 @@ PI_DEV bool mbar_wait(unsigned long long* mbar, unsigned parity, long long timeo
 }
 
 // Grid barrier number `k` of this launch.  Returns false (and sets the status
-// word) if the wait exceeded timeout_ns or another CTA already failed.
-PI_DEV bool grid_sync(unsigned* counter, unsigned target, long long timeout_ns, int* bad) {
+// word) if the wait exceeded timeout_ns or another CTA already failed.  Warp 0
+// runs between() after this CTA's arrival, before waiting for the others.
+template <typename Between>
+PI_DEV bool grid_sync(unsigned* counter, unsigned target, long long timeout_ns, int* bad, Between&& between) {
     __syncthreads();
+    if (threadIdx.x < 32) {
+        if (threadIdx.x == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(counter) : "memory");
+        __syncwarp();
+        between();
+    }
     if (threadIdx.x == 0) {
-        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(counter) : "memory");
         unsigned v = ld_acquire(counter);
         if ((int)(v - target) < 0) {
             const unsigned long long t0 = globaltimer();
@@ -366,6 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
     __shared__ int bad;
     __shared__ float rs_s;
     __shared__ uint16_t ubits[kMaxUnits];   // mask bits of this CTA's units (bit kk = row kk)
+    __shared__ int ubase[kMaxUnits];        // list position of each unit's first active row
     __shared__ int nmine_s;
     __shared__ __align__(8) unsigned long long pred_mbar;
     __shared__ __align__(8) unsigned long long w1_mbar;   // staged FC1 rows
@@ -391,7 +398,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
     unsigned nbar = 0;
     auto sync = [&]() -> bool {
         ++nbar;
-        return grid_sync(p.counter, (unsigned)((ebase + nbar) * (unsigned long long)G), tmo, &bad);
+        return grid_sync(p.counter, (unsigned)((ebase + nbar) * (unsigned long long)G), tmo, &bad, [] {});
+    };
+    auto sync_then = [&](auto between) -> bool {
+        ++nbar;
+        return grid_sync(p.counter, (unsigned)((ebase + nbar) * (unsigned long long)G), tmo, &bad, between);
     };
     // CTA 0 advances the epoch when it leaves, by every barrier this launch
     // schedules (also after a failure: the counts then no longer matter, the
@@ -484,17 +495,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
     for (int l = 0; l < p.L; ++l) {
         const FusedLayer& ly = p.layers[l];
         const int r = ly.r;
-        // layer l's predictor slices are consumed by then (phase B ended with a
-        // barrier): bring in layer l+1's once this CTA's FC rows are loaded
+        // warp 0, after this CTA's arrival at the barrier that ends FC2 (its FC
+        // rows are read by then): bring in layer l+1's predictor slices
         auto issue_next = [&]() {
-            if (l + 1 < p.L && (p.pred_smem || ns > 0)) {
-                __syncthreads();   // the region may still hold this CTA's staged FC rows
-                if (p.pred_smem) {
-                    if (warp == 0) issue_predictor(l + 1);
-                    inflight = l + 1;
-                } else if (tid == 0) {
+            if (l + 1 < p.L) {
+                if (p.pred_smem)
+                    issue_predictor(l + 1);
+                else if (ns > 0 && lane == 0)
                     for (int k = 0; k < ns && k < nunits; ++k) issue_unit(p.layers[l + 1], k);
-                }
             }
         };
         PI_STAMP(l, 0);
@@ -714,48 +722,41 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
         if (*(volatile int*)&bad) { leave(); return; }
 
         // ---------------------------------------------------------- phase B, FFN
-        // this CTA's active rows, in unit order (a fixed order: FC2 sums them in it)
+        // this CTA's active rows, in unit order (a fixed order: FC2 sums them in
+        // it): warp 0 scans the units' counts, then thread (unit m, row kk) places
+        // its row, with its FC1 bias when the predictor slice holds it (read
+        // before the FC rows overwrite the slice)
         if (warp == 0) {
             int base = 0;
             for (int m0 = 0; m0 < nunits; m0 += 32) {
                 const int m = m0 + lane;
-                const unsigned bits = m < nunits ? (unsigned)ubits[m] : 0u;
-                const int cnt = __popc(bits);
+                const int cnt = m < nunits ? __popc((unsigned)ubits[m]) : 0;
                 int incl = cnt;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
                     const int t = __shfl_up_sync(FULL, incl, o);
                     if (lane >= o) incl += t;
                 }
-                int pos = base + incl - cnt;
-                if (m < nunits) {
-                    const int pb0 = 8 * piece_of(2 * m);
-                    const int pb1 = 2 * m + 1 < npc ? 8 * piece_of(2 * m + 1) : F;
-                    unsigned b = bits;
-                    while (b) {
-                        const int kk = __ffs(b) - 1;
-                        b &= b - 1u;
-                        lidx[pos++] = (kk < 8 ? pb0 : pb1) + (kk & 7);
-                    }
-                }
+                if (m < nunits) ubase[m] = base + incl - cnt;
                 base += __shfl_sync(FULL, incl, 31);
             }
             if (lane == 0) nmine_s = base;
         }
         __syncthreads();
+        for (int t = tid; t < 16 * nunits; t += kThreads) {
+            const int m = t >> 4, kk = t & 15;
+            const unsigned bits = ubits[m];
+            if ((bits >> kk) & 1u) {
+                const int pos = ubase[m] + __popc(bits & ((1u << kk) - 1u));
+                const int rb = 8 * piece_of(2 * m + (kk >> 3));
+                lidx[pos] = rb + (kk & 7);
+                if (p.pred_smem)
+                    lh[pos] = rb + 8 <= F ? __half2float(b1s[16 * m + kk]) : __half2float(ly.b1[rb + (kk & 7)]);
+            }
+        }
+        __syncthreads();
         const int nmine = nmine_s;
         if (p.layer_counts && tid == 0 && nmine) atomicAdd(p.layer_counts + 2 * l, nmine);
-        // FC1 bias of row k: own piece k / 8 / G holds it in the staged slice
-        // (whole pieces); read before the FC rows overwrite the slice
-        auto bias_of = [&](int k) -> float {
-            const int gp = k >> 3;
-            return p.pred_smem && 8 * gp + 8 <= F ? __half2float(b1s[8 * (gp / G) + (k & 7)])
-                                                  : __half2float(ly.b1[k]);
-        };
-        if (p.pred_smem) {
-            for (int q = tid; q < nmine; q += kThreads) lh[q] = bias_of(lidx[q]);
-            __syncthreads();
-        }
         // few rows per CTA: stage its FC1 rows and as many W2t rows as fit besides
         // them in shared memory now with bulk copies (FC1 rows first, so they
         // arrive first); the remaining W2t rows follow into the FC1 rows' place
@@ -778,22 +779,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                 bulk_g2s(dst + d / 2, scales + k * (d / 32), (unsigned)(d / 16), mb);
             }
         };
-        if (warp == 0 && (w1_staged || n2a > 0)) {
-            // lane 0 arms the mbarriers, then the 32 lanes issue the row copies
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            if (lane == 0) {
+        const int nwd = d / 8;   // 16-byte words of an fp16 row
+        const __half* w1g = static_cast<const __half*>(ly.w1);
+        const __half* wug = ly.wu;
+        const __half* w2g = static_cast<const __half*>(ly.w2t);
+        // row copies are spread over the warps (a warp issues its bulk copies one
+        // after the other): thread (warp, lane) takes rows warp + kWarps * lane, ...
+        const int qspread = warp + kWarps * lane;
+        if (w1_staged || n2a > 0) {
+            if (tid == 0) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 if (w1_staged) mbar_arrive_expect_tx(&w1_mbar, (unsigned)w1b);
                 if (n2a > 0) mbar_arrive_expect_tx(&w2_mbar, (unsigned)(n2a * wrow));
             }
-            __syncwarp();
-            if (w1_staged) {
-                for (int q = lane; q < nmine; q += 32)
+            __syncthreads();
+            if (w1_staged)
+                for (int q = qspread; q < nmine; q += kThreads) {
                     stage_row(s_w1 + (size_t)q * wrow, ly.w1, ly.w1s, (size_t)lidx[q], &w1_mbar);
-                if (KIND == 1)
-                    for (int q = lane; q < nmine; q += 32)
-                        stage_row(s_wu + (size_t)q * wrow, ly.wu, nullptr, (size_t)lidx[q], &w1_mbar);
-            }
-            for (int q = lane; q < n2a; q += 32)
+                    if (KIND == 1) stage_row(s_wu + (size_t)q * wrow, ly.wu, nullptr, (size_t)lidx[q], &w1_mbar);
+                }
+            for (int q = qspread; q < n2a; q += kThreads)
                 stage_row(s_w2 + (size_t)q * wrow, ly.w2t, ly.w2ts, (size_t)lidx[q], &w2_mbar);
         }
         if (w1_staged) {
@@ -812,11 +817,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
         // when they did not fit, straight from global memory.
         {
             if (!p.pred_smem)
-                for (int q = tid; q < nmine; q += kThreads) lh[q] = bias_of(lidx[q]);
+                for (int q = tid; q < nmine; q += kThreads) lh[q] = __half2float(ly.b1[lidx[q]]);
             if (w1_staged && mbar_wait(&w1_mbar, (w1_uses - 1) & 1u, tmo, &bad)) w1_pending = false;
             float* part = red;           // [128 rows][kWarps]
             float* partu = red + 2048;   // gated: up-projection partials
-            const int nwd = d / 8;
             constexpr int RB = KIND == 1 ? 4 : 8;
             // rows [qb, qe) (at most 128); word(q, wd, cw, sc) / up(q, wd) fetch
             // word wd of row q (fp16: 8 weights in a uint4; INT4: the code word in
@@ -853,10 +857,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                     }
                 }
             };
-            const __half* w1g = static_cast<const __half*>(ly.w1);
             const uint8_t* w1q = static_cast<const uint8_t*>(ly.w1);
             const __half* w1sg = ly.w1s;
-            const __half* wug = ly.wu;
             for (int qb = 0; qb < nmine; qb += 128) {
                 const int qe = min(nmine, qb + 128);
                 if (w1_staged) {
@@ -912,13 +914,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
         }
         // FC1 has read its rows: the W2t rows that did not fit take their place
         if (late) {
-            if (warp == 0) {
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                if (lane == 0) mbar_arrive_expect_tx(&w1_mbar, (unsigned)((nmine - n2a) * wrow));
-                __syncwarp();
-                for (int q = n2a + lane; q < nmine; q += 32)
-                    stage_row(stage + (size_t)(q - n2a) * wrow, ly.w2t, ly.w2ts, (size_t)lidx[q], &w1_mbar);
-            }
+            if (tid == 0) mbar_arrive_expect_tx(&w1_mbar, (unsigned)((nmine - n2a) * wrow));
+            __syncthreads();
+            for (int q = n2a + qspread; q < nmine; q += kThreads)
+                stage_row(stage + (size_t)(q - n2a) * wrow, ly.w2t, ly.w2ts, (size_t)lidx[q], &w1_mbar);
             ++w1_uses;
             w1_pending = true;
         }
@@ -930,7 +929,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
         // from global memory.
         // rows [qa, qe): load(q, col) fetches 16 bytes of row q at column col
         // (fp16: 8 weights; INT4: 32 codes) and, for INT4, the group scale in sc
-        const __half* w2g = static_cast<const __half*>(ly.w2t);
         const uint8_t* w2q = static_cast<const uint8_t*>(ly.w2t);
         const __half* w2sg = ly.w2ts;
         auto smem_rows = [&](const unsigned char* base, int q0) {
@@ -998,7 +996,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                     fc2_rows(n2a, nmine, global_rows);
                 }
             }
-            issue_next();
             float* dst = p.xyp + (size_t)c * d;
 #pragma unroll
             for (int ch = 0; ch < NCH; ++ch) {
@@ -1062,7 +1059,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                     fc2_rows(n2a, nmine, global_rows);
                 }
             }
-            issue_next();
 #pragma unroll
             for (int g = 0; g < NG; ++g) {
                 const int col = (tid + g * kThreads) * 32;
@@ -1075,7 +1071,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
             }
         }
         PI_STAMP(l, 5);
-        if (!sync()) { leave(); return; }
+        if (l + 1 < p.L && p.pred_smem) inflight = l + 1;
+        if (!sync_then(issue_next)) { leave(); return; }
         PI_STAMP(l, 6);
 
         // ---------------------------------------------------------- phase D
@@ -1085,6 +1082,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
             float ss_local = 0.f;
             for (int gi = warp; gi < ngm; gi += kWarps) {
                 const int col = (g0 + gi) * 4;
+                // b2 of the 4 columns, requested before the partials
+                __half b2v[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) b2v[e] = lane == 0 ? __ldg(ly.b2 + col + e) : __float2half(0.f);
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
                 constexpr int NB = 8;
                 for (int q0 = lane; q0 < G; q0 += NB * 32) {
@@ -1113,8 +1114,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                     acc.w += __shfl_xor_sync(FULL, acc.w, o);
                 }
                 if (lane == 0) {
-                    const float4 yv = make_float4(acc.x + __half2float(ly.b2[col]), acc.y + __half2float(ly.b2[col + 1]),
-                                                  acc.z + __half2float(ly.b2[col + 2]), acc.w + __half2float(ly.b2[col + 3]));
+                    const float4 yv = make_float4(acc.x + __half2float(b2v[0]), acc.y + __half2float(b2v[1]),
+                                                  acc.z + __half2float(b2v[2]), acc.w + __half2float(b2v[3]));
                     __stcg(reinterpret_cast<float4*>(p.xy + col), yv);
                     if (l == p.L - 1) *reinterpret_cast<float4*>(p.y_out + col) = yv;
                     ss_local += yv.x * yv.x + yv.y * yv.y + yv.z * yv.z + yv.w * yv.w;
@@ -1174,7 +1175,7 @@ __global__ void k_wait_nothing(long long timeout_ns) {
     __shared__ int bad;
     if (threadIdx.x == 0) bad = 0;
     // target 2 with one arrival: the count never gets there
-    (void)grid_sync(&g_never_incremented, g_never_incremented + 2u, timeout_ns, &bad);
+    (void)grid_sync(&g_never_incremented, g_never_incremented + 2u, timeout_ns, &bad, [] {});
     if (threadIdx.x == 0) atomicSub(&g_never_incremented, 1u);
 }
 

@@ -60,6 +60,9 @@ def _check_stack(cfg, L, token=0):
     ("gated-small", small(CONFIGS["c4"], d=1024, F=3000, rank=64), 3),
     ("int4-small", small(CONFIGS["c5"], d=1024, F=4100, rank=128), 3),
     ("ragged", small(CONFIGS["c1"], d=264, F=1001, rank=24), 3),
+    # wider than the columns each thread prefetches in registers (tail loop of x)
+    ("int4-wide", small(CONFIGS["c5"], d=10240, F=2048, rank=64), 2),
+    ("fp16-wide", small(CONFIGS["c4"], d=8192, F=2000, rank=64), 2),
 ])
 def test_stack_layers_match_oracle(name, cfg, L):
     _check_stack(cfg, L)
