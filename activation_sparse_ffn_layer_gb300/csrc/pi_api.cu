@@ -70,7 +70,7 @@ bool make_plan(const pi_layer_desc& desc, Plan* p) {
     // descriptor that shares the workspace), then the per-step buffers
     q.rmax_su = (size_t)16 * q.nsm + 2 * (size_t)q.r;
     q.xchg_bytes = up(fused_workspace_bytes(q.d, q.F, q.rmax_su, q.nsm));
-    q.fused = q.B == 1 && fused_supported(q.d, q.F, q.r, q.int4, q.nsm);
+    q.fused = q.B == 1 && fused_supported(q.d, q.F, q.r, q.int4, q.gated, q.nsm);
     q.tc = tc_supported(q);
     q.st = !q.tc && st_supported(q);
     q.st4 = !q.tc && !q.st && st4_supported(q);

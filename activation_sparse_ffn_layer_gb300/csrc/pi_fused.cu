@@ -23,8 +23,9 @@
 // kernel returns (the other CTAs then time out at their next barrier).
 // Exchanged data is written with plain stores and read with L2-only loads.
 //
-// While a layer's FC rows stream from HBM, the next layer's predictor rows of
-// this CTA are bulk-prefetched into L2.
+// Weights move into shared memory by bulk copies (TMA): a CTA's predictor slice
+// of the next layer is requested while the current layer's partial sums are
+// reduced, and its FC rows stream through a ring of row slots.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -44,14 +45,12 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kBarriersPerLayer = 3;
 constexpr int kMaxUnits = 64;   // 16-row units (two 8-row pieces) per CTA
 constexpr int kRingMax = 8;   // P2 ring slots at most
+constexpr int kMaxFcSlots = 32;   // FC row ring slots at most
 
 PI_DEV unsigned long long globaltimer() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
     return t;
-}
-PI_DEV void prefetch_l2(const void* p, unsigned bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 PI_DEV unsigned ld_acquire(const unsigned* p) {
     unsigned v;
@@ -94,8 +93,9 @@ PI_DEV void mbar_drain(unsigned long long* mbar, unsigned parity, long long time
 }
 
 // Wait (bounded) until the mbarrier phase with this parity has completed.
-PI_DEV bool mbar_wait(unsigned long long* mbar, unsigned parity, long long timeout_ns, int* bad) {
-    if (mbar_test(mbar, parity)) return true;
+// The spinning part stays out of line: the kernel waits at many places, and
+// one copy of the loop keeps its code (fetched afresh every layer) small.
+__device__ __noinline__ bool mbar_wait_slow(unsigned long long* mbar, unsigned parity, long long timeout_ns, int* bad) {
     const unsigned long long t0 = globaltimer();
     while (!mbar_test(mbar, parity)) {
         if ((long long)(globaltimer() - t0) > timeout_ns || *(volatile int*)bad) {
@@ -105,6 +105,9 @@ PI_DEV bool mbar_wait(unsigned long long* mbar, unsigned parity, long long timeo
         }
     }
     return true;
+}
+PI_DEV bool mbar_wait(unsigned long long* mbar, unsigned parity, long long timeout_ns, int* bad) {
+    return mbar_test(mbar, parity) || mbar_wait_slow(mbar, parity, timeout_ns, bad);
 }
 
 // Grid barrier number `k` of this launch.  Returns false (and sets the status
@@ -181,6 +184,7 @@ struct FusedParams {
     int stage_bytes;            // shared staging region (predictor slices, then this CTA's FC rows)
     int ring_slots;             // without pred_smem: P2 units stream through this many slots of
     int ring_unit;              // ring_unit bytes (16 rows of the largest rank) in the staging region
+    int fc_slots;               // FC row slots (one weight row each) in the staging region
     FusedLayer layers[kMaxFusedLayers];
 };
 
@@ -375,14 +379,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
     __shared__ int ubase[kMaxUnits];        // list position of each unit's first active row
     __shared__ int nmine_s;
     __shared__ __align__(8) unsigned long long pred_mbar;
-    __shared__ __align__(8) unsigned long long w1_mbar;   // staged FC1 rows
-    __shared__ __align__(8) unsigned long long w2_mbar;   // staged W2t rows
+    __shared__ __align__(8) unsigned long long fc_full[kMaxFcSlots];   // FC row ring
+    __shared__ __align__(8) unsigned long long w1_mbar, w2_mbar;       // FC rows when all fit
     __shared__ __align__(8) unsigned long long ring_full[kRingMax];   // P2 unit ring
     __shared__ int ring_uses[kRingMax];                                // copies issued per slot
     const int ns = p.ring_slots;
     if (tid == 0) {
         bad = 0;
         mbar_init(&pred_mbar, 1);
+        for (int q = 0; q < kMaxFcSlots; ++q) mbar_init(&fc_full[q], 1);
         mbar_init(&w1_mbar, 1);
         mbar_init(&w2_mbar, 1);
         for (int q = 0; q < kRingMax; ++q) {
@@ -390,8 +395,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
             ring_uses[q] = 0;
         }
     }
-    unsigned w1_uses = 0, w2_uses = 0;   // completed-or-pending phases of w1_mbar, w2_mbar
-    bool w1_pending = false, w2_pending = false;
+    unsigned fseq = 0;    // ring FC row copies of earlier layers (the ring's running element index)
+    unsigned fc_hi = 0;   // ring FC row copies issued so far
+    unsigned w12_uses = 0;      // phases armed on w1_mbar / w2_mbar
+    bool w12_pending = false;   // ... of which the last is not yet waited for
 
     // barrier targets: the counter holds G arrivals per barrier ever completed
     const unsigned long long ebase = __ldcg(p.epoch);
@@ -412,8 +419,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
         if (inflight >= 0) mbar_drain(&pred_mbar, (unsigned)(inflight & 1), tmo);
         for (int q = 0; q < ns; ++q)
             if (ring_uses[q] > 0) mbar_drain(&ring_full[q], (unsigned)((ring_uses[q] - 1) & 1), tmo);
-        if (w1_pending) mbar_drain(&w1_mbar, (w1_uses - 1) & 1u, tmo);
-        if (w2_pending) mbar_drain(&w2_mbar, (w2_uses - 1) & 1u, tmo);
+        if (w12_pending) {
+            mbar_drain(&w1_mbar, (w12_uses - 1) & 1u, tmo);
+            mbar_drain(&w2_mbar, (w12_uses - 1) & 1u, tmo);
+        }
+        // the last copy issued into each FC row slot
+        const unsigned S = (unsigned)p.fc_slots;
+        for (unsigned g = fc_hi > S ? fc_hi - S : 0u; g < fc_hi; ++g) mbar_drain(&fc_full[g % S], (g / S) & 1u, tmo);
         if (c == 0 && tid == 0) {
             const unsigned long long next = ebase + (unsigned long long)kBarriersPerLayer * p.L;
             __stcg(p.epoch, next);
@@ -757,76 +769,135 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
         __syncthreads();
         const int nmine = nmine_s;
         if (p.layer_counts && tid == 0 && nmine) atomicAdd(p.layer_counts + 2 * l, nmine);
-        // few rows per CTA: stage its FC1 rows and as many W2t rows as fit besides
-        // them in shared memory now with bulk copies (FC1 rows first, so they
-        // arrive first); the remaining W2t rows follow into the FC1 rows' place
-        // once FC1 has read them.  W2t rows of neurons whose FC1 output turns
-        // out to be zero are loaded but not used.  The region held this layer's
-        // predictor slices (or P2 ring), read by now.
-        const int w1b = nmine * fc1_rows * wrow;
-        const bool w1_staged = nmine > 0 && w1b <= p.stage_bytes;
-        const int n2a = w1_staged ? min(nmine, (p.stage_bytes - w1b) / wrow) : min(nmine, p.stage_bytes / wrow);
-        const bool late = w1_staged && n2a < nmine;   // W2t rows [n2a, nmine) staged after FC1
-        unsigned char* s_w1 = stage;                                  // [nmine] W1 (gate) rows
-        unsigned char* s_wu = stage + (size_t)nmine * wrow;           // [nmine] up rows (gated)
-        unsigned char* s_w2 = stage + (w1_staged ? (size_t)w1b : 0);  // [n2a] W2t rows
-        auto stage_row = [&](unsigned char* dst, const void* codes, const __half* scales, size_t k,
-                             unsigned long long* mb) {
-            if (KIND != 2) {
-                bulk_g2s(dst, static_cast<const __half*>(codes) + k * d, 2u * d, mb);
-            } else {
-                bulk_g2s(dst, static_cast<const uint8_t*>(codes) + k * (d / 2), (unsigned)(d / 2), mb);
-                bulk_g2s(dst + d / 2, scales + k * (d / 32), (unsigned)(d / 16), mb);
+        // FC rows stream through a ring of S row slots in the staging region
+        // (which held this layer's predictor slices or P2 ring, read by now):
+        // the sequence is this CTA's FC1 rows (gated: gate and up row of each
+        // neuron), then its W2t rows; element i lands in slot (fseq + i) % S.
+        // Bulk copies run up to S elements ahead; a batch's slots are refilled
+        // as soon as the whole CTA has read them.  W2t rows of neurons whose FC1
+        // output turns out to be zero are loaded but not used.
+        const int S = p.fc_slots;
+        const int fc1n = nmine * fc1_rows;
+        const int T = fc1n + nmine;
+        // all rows fit: element i sits in slot i, the FC1 rows complete on one
+        // mbarrier and the W2t rows on another (no per-row waits)
+        const bool fits = T <= S;
+        auto slot_of = [&](int i) { return fits ? i : (int)((fseq + (unsigned)i) % (unsigned)S); };
+        // slot and wait parity of element i, advanced one element at a time (no
+        // division per row); take() waits for the element in ring mode (every
+        // thread) and returns its row
+        struct Cursor {
+            int slot;
+            unsigned par;
+        };
+        auto cursor_at = [&](int i) {
+            const unsigned g = fits ? (unsigned)i : fseq + (unsigned)i;
+            return Cursor{(int)(g % (unsigned)S), (g / (unsigned)S) & 1u};
+        };
+        auto step = [&](Cursor& cu) {
+            if (++cu.slot == S) {
+                cu.slot = 0;
+                cu.par ^= 1u;
             }
         };
-        const int nwd = d / 8;   // 16-byte words of an fp16 row
-        const __half* w1g = static_cast<const __half*>(ly.w1);
-        const __half* wug = ly.wu;
-        const __half* w2g = static_cast<const __half*>(ly.w2t);
+        auto take = [&](Cursor& cu) -> const unsigned char* {
+            const unsigned char* r = stage + (size_t)cu.slot * wrow;
+            step(cu);
+            return r;
+        };
+        // ring mode: every thread waits for the n elements from cu on (a plain
+        // loop of its own, outside the unrolled row loops)
+        auto wait_n = [&](Cursor cu, int n) {
+            if (fits) return;
+            for (int e = 0; e < n; ++e) {
+                mbar_wait(&fc_full[cu.slot], cu.par, tmo, &bad);
+                step(cu);
+            }
+        };
         // row copies are spread over the warps (a warp issues its bulk copies one
-        // after the other): thread (warp, lane) takes rows warp + kWarps * lane, ...
+        // after the other): elements [a, b) go to threads (warp, lane) in the order
+        // warp + kWarps * lane
         const int qspread = warp + kWarps * lane;
-        if (w1_staged || n2a > 0) {
-            if (tid == 0) {
+        auto issue_range = [&](int a, int b) {
+            if (a + qspread >= b) return;
+            if (!fits) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            for (int i = a + qspread; i < b; i += kThreads) {
+                const int sl = slot_of(i);
+                unsigned long long* mb = fits ? (i < fc1n ? &w1_mbar : &w2_mbar) : &fc_full[sl];
+                unsigned char* dst = stage + (size_t)sl * wrow;
+                const size_t k = (size_t)lidx[i < fc1n ? i / fc1_rows : i - fc1n];
+                if (!fits) mbar_arrive_expect_tx(mb, (unsigned)wrow);
+                if (KIND != 2) {
+                    const __half* src = i >= fc1n ? static_cast<const __half*>(ly.w2t)
+                                        : (KIND == 1 && (i & 1)) ? ly.wu
+                                                                 : static_cast<const __half*>(ly.w1);
+                    bulk_g2s(dst, src + k * d, 2u * d, mb);
+                } else {
+                    const bool w2 = i >= fc1n;
+                    const uint8_t* codes = static_cast<const uint8_t*>(w2 ? ly.w2t : ly.w1);
+                    const __half* scales = w2 ? ly.w2ts : ly.w1s;
+                    bulk_g2s(dst, codes + k * (d / 2), (unsigned)(d / 2), mb);
+                    bulk_g2s(dst + d / 2, scales + k * (d / 32), (unsigned)(d / 16), mb);
+                }
+            }
+        };
+        int issued = min(S, T);
+        if (fits) {
+            if (tid == 0 && T > 0) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                if (w1_staged) mbar_arrive_expect_tx(&w1_mbar, (unsigned)w1b);
-                if (n2a > 0) mbar_arrive_expect_tx(&w2_mbar, (unsigned)(n2a * wrow));
+                mbar_arrive_expect_tx(&w1_mbar, (unsigned)(fc1n * wrow));
+                mbar_arrive_expect_tx(&w2_mbar, (unsigned)(nmine * wrow));
             }
             __syncthreads();
-            if (w1_staged)
-                for (int q = qspread; q < nmine; q += kThreads) {
-                    stage_row(s_w1 + (size_t)q * wrow, ly.w1, ly.w1s, (size_t)lidx[q], &w1_mbar);
-                    if (KIND == 1) stage_row(s_wu + (size_t)q * wrow, ly.wu, nullptr, (size_t)lidx[q], &w1_mbar);
-                }
-            for (int q = qspread; q < n2a; q += kThreads)
-                stage_row(s_w2 + (size_t)q * wrow, ly.w2t, ly.w2ts, (size_t)lidx[q], &w2_mbar);
+            if (T > 0) {
+                ++w12_uses;
+                w12_pending = true;
+            }
+        } else {
+            fc_hi = fseq + (unsigned)issued;
         }
-        if (w1_staged) {
-            ++w1_uses;
-            w1_pending = true;
-        }
-        if (n2a > 0) {
-            ++w2_uses;
-            w2_pending = true;
-        }
+        // FC1 rows first (spread over the warps on their own, so they are queued first)
+        issue_range(0, min(issued, fc1n));
+        issue_range(fc1n, issued);
+        // after a batch ending at element e has been read by every thread (ring mode)
+        auto refill = [&](int e) {
+            const int hi = min(T, e + S);
+            if (hi > issued) {
+                issue_range(issued, hi);
+                issued = hi;
+                fc_hi = fseq + (unsigned)issued;
+            }
+        };
 
-        // FC1, the whole CTA on RB rows at a time (8; 4 gate + up pairs): thread
-        // t takes the 8-element words t, t + kThreads, ... of the rows (x read once per
-        // word and batch, used for RB rows); fold reduces a warp's partials, and
-        // the 16 warp sums of a row are added in a fixed order.  Rows come from the staged copies or,
-        // when they did not fit, straight from global memory.
+        // FC1, the whole CTA on rbn neurons at a time: thread t takes the 8-element
+        // words t, t + kThreads, ... of the rows (x read once per word and batch);
+        // fold reduces a warp's partials, and the kWarps warp sums of a row are
+        // added in a fixed order
         {
             if (!p.pred_smem)
                 for (int q = tid; q < nmine; q += kThreads) lh[q] = __half2float(ly.b1[lidx[q]]);
-            if (w1_staged && mbar_wait(&w1_mbar, (w1_uses - 1) & 1u, tmo, &bad)) w1_pending = false;
             float* part = red;           // [128 rows][kWarps]
             float* partu = red + 2048;   // gated: up-projection partials
+            const int nwd = d / 8;
             constexpr int RB = KIND == 1 ? 4 : 8;
-            // rows [qb, qe) (at most 128); word(q, wd, cw, sc) / up(q, wd) fetch
-            // word wd of row q (fp16: 8 weights in a uint4; INT4: the code word in
-            // cw.x and its group scale in sc)
-            auto fc1_block = [&](int qb, int qe, auto word, auto up) {
-                for (int q0 = qb; q0 < qe; q0 += RB) {
+            const int rbn = max(1, min(RB, S / (2 * fc1_rows)));   // half the slots per batch
+            if (fits && nmine > 0 && mbar_wait(&w1_mbar, (w12_uses - 1) & 1u, tmo, &bad)) w12_pending = false;
+            Cursor cu = cursor_at(0);
+            for (int qb = 0; qb < nmine; qb += 128) {
+                const int qe = min(nmine, qb + 128);
+                for (int q0 = qb; q0 < qe; q0 += rbn) {
+                    const int q1 = min(qe, q0 + rbn);
+                    wait_n(cu, (q1 - q0) * fc1_rows);
+                    const unsigned char* rw[RB];
+                    const unsigned char* ru[RB];
+#pragma unroll
+                    for (int b = 0; b < RB; ++b) {
+                        rw[b] = ru[b] = stage;
+                        if (q0 + b < q1) {
+                            rw[b] = take(cu);
+                            if (KIND == 1) ru[b] = take(cu);
+                        }
+                    }
                     float v[RB], vu[RB];
 #pragma unroll
                     for (int b = 0; b < RB; ++b) v[b] = vu[b] = 0.f;
@@ -836,59 +907,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
 #pragma unroll
                         for (int b = 0; b < RB; ++b) {
                             const int q = q0 + b;
-                            if (q >= qe) break;
-                            uint4 cw;
-                            float sc;
-                            word(q, wd, cw, sc);
+                            if (q >= q1) break;
+                            const unsigned char* row = rw[b];
                             if (KIND != 2) {
-                                v[b] += dot8r(cw, xa, xb);
-                                if (KIND == 1) vu[b] += dot8r(up(q, wd), xa, xb);
+                                v[b] += dot8r(reinterpret_cast<const uint4*>(row)[wd], xa, xb);
+                                if (KIND == 1) vu[b] += dot8r(reinterpret_cast<const uint4*>(ru[b])[wd], xa, xb);
                             } else {
-                                v[b] = fmaf(sc, dotq8r(cw.x, xa, xb), v[b]);
+                                const uint32_t cw = reinterpret_cast<const uint32_t*>(row)[wd];
+                                const float sc = __half2float(reinterpret_cast<const __half*>(row + d / 2)[wd >> 2]);
+                                v[b] = fmaf(sc, dotq8r(cw, xa, xb), v[b]);
                             }
                         }
                     }
                     const int rb = fold_row<RB>(lane);
                     const float tv = fold<RB>(v, lane);
                     const float tu = KIND == 1 ? fold<RB>(vu, lane) : 0.f;
-                    if ((lane & (32 / RB - 1)) == 0 && q0 + rb < qe) {
+                    if ((lane & (32 / RB - 1)) == 0 && q0 + rb < q1) {
                         part[(q0 - qb + rb) * kWarps + warp] = tv;
                         if (KIND == 1) partu[(q0 - qb + rb) * kWarps + warp] = tu;
                     }
-                }
-            };
-            const uint8_t* w1q = static_cast<const uint8_t*>(ly.w1);
-            const __half* w1sg = ly.w1s;
-            for (int qb = 0; qb < nmine; qb += 128) {
-                const int qe = min(nmine, qb + 128);
-                if (w1_staged) {
-                    fc1_block(
-                        qb, qe,
-                        [&](int q, int wd, uint4& cw, float& sc) {
-                            const unsigned char* row = s_w1 + (size_t)q * wrow;
-                            if (KIND != 2) {
-                                cw = reinterpret_cast<const uint4*>(row)[wd];
-                            } else {
-                                cw.x = reinterpret_cast<const uint32_t*>(row)[wd];
-                                sc = __half2float(reinterpret_cast<const __half*>(row + d / 2)[wd >> 2]);
-                            }
-                        },
-                        [&](int q, int wd) { return reinterpret_cast<const uint4*>(s_wu + (size_t)q * wrow)[wd]; });
-                } else {
-                    fc1_block(
-                        qb, qe,
-                        [&](int q, int wd, uint4& cw, float& sc) {
-                            const size_t k = (size_t)lidx[q];
-                            if (KIND != 2) {
-                                cw = ld_stream16(w1g + k * d + 8 * wd);
-                            } else {
-                                asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];"
-                                    : "=r"(cw.x)
-                                    : "l"(w1q + k * (d / 2) + 4 * wd));
-                                sc = __half2float(w1sg[k * (d / 32) + (wd >> 2)]);
-                            }
-                        },
-                        [&](int q, int wd) { return ld_stream16(wug + (size_t)lidx[q] * d + 8 * wd); });
+                    if (issued < T) {   // the batch's slots are read by every thread: refill them
+                        __syncthreads();
+                        refill(q1 * fc1_rows);
+                    }
                 }
                 __syncthreads();
                 for (int q = qb + tid; q < qe; q += kThreads) {
@@ -912,88 +953,59 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                 if (lane == 0 && nz) atomicAdd(p.layer_counts + 2 * l + 1, nz);
             }
         }
-        // FC1 has read its rows: the W2t rows that did not fit take their place
-        if (late) {
-            if (tid == 0) mbar_arrive_expect_tx(&w1_mbar, (unsigned)((nmine - n2a) * wrow));
-            __syncthreads();
-            for (int q = n2a + qspread; q < nmine; q += kThreads)
-                stage_row(stage + (size_t)(q - n2a) * wrow, ly.w2t, ly.w2ts, (size_t)lidx[q], &w1_mbar);
-            ++w1_uses;
-            w1_pending = true;
-        }
         PI_STAMP(l, 4);
 
-        // FC2: the whole CTA accumulates its neurons' W2t rows; rows whose
-        // FC1 output is zero are skipped (ReLU removed them from FC2).  Row q's
-        // W2t data: staged early (q < n2a), staged after FC1 (late), or read
-        // from global memory.
-        // rows [qa, qe): load(q, col) fetches 16 bytes of row q at column col
-        // (fp16: 8 weights; INT4: 32 codes) and, for INT4, the group scale in sc
-        const uint8_t* w2q = static_cast<const uint8_t*>(ly.w2t);
-        const __half* w2sg = ly.w2ts;
-        auto smem_rows = [&](const unsigned char* base, int q0) {
-            return [=](int q, int col, float& sc) {
-                const unsigned char* row = base + (size_t)(q - q0) * wrow;
-                if (KIND == 2) sc = __half2float(reinterpret_cast<const __half*>(row + d / 2)[col / 32]);
-                return *reinterpret_cast<const uint4*>(row + (KIND == 2 ? col / 2 : 2 * col));
-            };
-        };
-        auto global_rows = [&](int q, int col, float& sc) {
-            const size_t k = (size_t)lidx[q];
-            if (KIND == 2) {
-                sc = __half2float(w2sg[k * (d / 32) + col / 32]);
-                return ld_stream16(w2q + k * (d / 2) + col / 2);
-            }
-            return ld_stream16(w2g + k * d + col);
-        };
-        if (n2a > 0 && mbar_wait(&w2_mbar, (w2_uses - 1) & 1u, tmo, &bad)) w2_pending = false;
+        // FC2: the whole CTA accumulates its neurons' W2t rows (rb2 rows per
+        // batch); rows whose FC1 output is zero are skipped (ReLU removed them)
         if (KIND != 2) {
-            constexpr int RB = NCH == 1 ? 4 : (NCH == 2 ? 2 : 1);
+            constexpr int RB2 = NCH == 1 ? 8 : (NCH == 2 ? 4 : 2);
+            const int rb2 = max(1, min(RB2, S / 2));
             float acc[NCH][8];
 #pragma unroll
             for (int ch = 0; ch < NCH; ++ch)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) acc[ch][e] = 0.f;
-            auto fc2_rows = [&](int qa, int qe, auto load) {
-                for (int q0 = qa; q0 < qe; q0 += RB) {
-                    uint4 wv[RB][NCH];
-                    float hv[RB];
+            if (fits && nmine > 0) mbar_wait(&w2_mbar, (w12_uses - 1) & 1u, tmo, &bad);
+            Cursor cu = cursor_at(fc1n);
+            for (int q0 = 0; q0 < nmine; q0 += rb2) {
+                const int q1 = min(nmine, q0 + rb2);
+                wait_n(cu, q1 - q0);
+                const unsigned char* rr[RB2];
 #pragma unroll
-                    for (int b = 0; b < RB; ++b) {
-                        const int q = q0 + b;
-                        hv[b] = q < qe ? lh[q] : 0.f;
-                        if (hv[b] != 0.f) {
+                for (int b = 0; b < RB2; ++b) rr[b] = q0 + b < q1 ? take(cu) : stage;
+                uint4 wv[RB2][NCH];
+                float hv[RB2];
 #pragma unroll
-                            for (int ch = 0; ch < NCH; ++ch) {
-                                const int col = ch * kCols + tid * 8;
-                                float sc;
-                                if (col < d) wv[b][ch] = load(q, col, sc);
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int b = 0; b < RB; ++b) {
-                        if (hv[b] == 0.f) continue;
+                for (int b = 0; b < RB2; ++b) {
+                    const int q = q0 + b;
+                    const unsigned char* r = rr[b];
+                    hv[b] = q < q1 ? lh[q] : 0.f;
+                    if (hv[b] != 0.f) {
+                        const __half* row = reinterpret_cast<const __half*>(r);
 #pragma unroll
                         for (int ch = 0; ch < NCH; ++ch) {
                             const int col = ch * kCols + tid * 8;
-                            if (col < d) {
-                                float wf[8];
-                                h8_to_f8(wv[b][ch], wf);
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) acc[ch][e] = fmaf(hv[b], wf[e], acc[ch][e]);
-                            }
+                            if (col < d) wv[b][ch] = *reinterpret_cast<const uint4*>(row + col);
                         }
                     }
                 }
-            };
-            if (n2a > 0) fc2_rows(0, n2a, smem_rows(s_w2, 0));
-            if (nmine > n2a) {
-                if (late) {
-                    if (mbar_wait(&w1_mbar, (w1_uses - 1) & 1u, tmo, &bad)) w1_pending = false;
-                    fc2_rows(n2a, nmine, smem_rows(stage, n2a));
-                } else {
-                    fc2_rows(n2a, nmine, global_rows);
+#pragma unroll
+                for (int b = 0; b < RB2; ++b) {
+                    if (hv[b] == 0.f) continue;
+#pragma unroll
+                    for (int ch = 0; ch < NCH; ++ch) {
+                        const int col = ch * kCols + tid * 8;
+                        if (col < d) {
+                            float wf[8];
+                            h8_to_f8(wv[b][ch], wf);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) acc[ch][e] = fmaf(hv[b], wf[e], acc[ch][e]);
+                        }
+                    }
+                }
+                if (issued < T) {
+                    __syncthreads();
+                    refill(fc1n + q1);
                 }
             }
             float* dst = p.xyp + (size_t)c * d;
@@ -1010,53 +1022,54 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
             // INT4: a thread owns scale groups tid and tid + kThreads (32
             // consecutive columns each)
             constexpr int NG = 2;
+            const int rb2 = max(1, min(2, S / 2));
             float acc[NG][32];
 #pragma unroll
             for (int g = 0; g < NG; ++g)
 #pragma unroll
                 for (int e = 0; e < 32; ++e) acc[g][e] = 0.f;
-            auto fc2_rows = [&](int qa, int qe, auto load) {
-                for (int q0 = qa; q0 < qe; q0 += 2) {
-                    uint4 wv[2][NG];
-                    float hs[2][NG];
+            if (fits && nmine > 0) mbar_wait(&w2_mbar, (w12_uses - 1) & 1u, tmo, &bad);
+            Cursor cu = cursor_at(fc1n);
+            for (int q0 = 0; q0 < nmine; q0 += rb2) {
+                const int q1 = min(nmine, q0 + rb2);
+                wait_n(cu, q1 - q0);
+                const unsigned char* rr[2];
 #pragma unroll
-                    for (int b = 0; b < 2; ++b) {
-                        const int q = q0 + b;
-                        const float hv = q < qe ? lh[q] : 0.f;
+                for (int b = 0; b < 2; ++b) rr[b] = q0 + b < q1 ? take(cu) : stage;
+                uint4 wv[2][NG];
+                float hs[2][NG];
 #pragma unroll
-                        for (int g = 0; g < NG; ++g) {
-                            const int col = (tid + g * kThreads) * 32;
-                            hs[b][g] = 0.f;
-                            if (hv != 0.f && col < d) {
-                                float sc;
-                                wv[b][g] = load(q, col, sc);
-                                hs[b][g] = hv * sc;
-                            }
+                for (int b = 0; b < 2; ++b) {
+                    const int q = q0 + b;
+                    const unsigned char* row = rr[b];
+                    const float hv = q < q1 ? lh[q] : 0.f;
+#pragma unroll
+                    for (int g = 0; g < NG; ++g) {
+                        const int col = (tid + g * kThreads) * 32;
+                        hs[b][g] = 0.f;
+                        if (hv != 0.f && col < d) {
+                            wv[b][g] = *reinterpret_cast<const uint4*>(row + col / 2);
+                            hs[b][g] = hv * __half2float(reinterpret_cast<const __half*>(row + d / 2)[col / 32]);
                         }
                     }
-#pragma unroll
-                    for (int b = 0; b < 2; ++b)
-#pragma unroll
-                        for (int g = 0; g < NG; ++g) {
-                            if (hs[b][g] == 0.f) continue;
-                            const uint32_t qw[4] = {wv[b][g].x, wv[b][g].y, wv[b][g].z, wv[b][g].w};
-#pragma unroll
-                            for (int wi = 0; wi < 4; ++wi) {
-                                float qf[8];
-                                q8_to_f8(qw[wi], qf);
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) acc[g][wi * 8 + e] = fmaf(hs[b][g], qf[e], acc[g][wi * 8 + e]);
-                            }
-                        }
                 }
-            };
-            if (n2a > 0) fc2_rows(0, n2a, smem_rows(s_w2, 0));
-            if (nmine > n2a) {
-                if (late) {
-                    if (mbar_wait(&w1_mbar, (w1_uses - 1) & 1u, tmo, &bad)) w1_pending = false;
-                    fc2_rows(n2a, nmine, smem_rows(stage, n2a));
-                } else {
-                    fc2_rows(n2a, nmine, global_rows);
+#pragma unroll
+                for (int b = 0; b < 2; ++b)
+#pragma unroll
+                    for (int g = 0; g < NG; ++g) {
+                        if (hs[b][g] == 0.f) continue;
+                        const uint32_t qw[4] = {wv[b][g].x, wv[b][g].y, wv[b][g].z, wv[b][g].w};
+#pragma unroll
+                        for (int wi = 0; wi < 4; ++wi) {
+                            float qf[8];
+                            q8_to_f8(qw[wi], qf);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) acc[g][wi * 8 + e] = fmaf(hs[b][g], qf[e], acc[g][wi * 8 + e]);
+                        }
+                    }
+                if (issued < T) {
+                    __syncthreads();
+                    refill(fc1n + q1);
                 }
             }
 #pragma unroll
@@ -1070,6 +1083,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                 }
             }
         }
+        if (!fits) fseq += (unsigned)T;
+        // (both FC mbarriers of the fitting case are waited for by every thread by now)
+        if (!*(volatile int*)&bad) w12_pending = false;
         PI_STAMP(l, 5);
         if (l + 1 < p.L && p.pred_smem) inflight = l + 1;
         if (!sync_then(issue_next)) { leave(); return; }
@@ -1233,13 +1249,24 @@ SmemPlan smem_plan(int d, int F, int rmax, size_t rmax_su, int G) {
 
 size_t fused_workspace_bytes(int d, int F, size_t rmax_su, int G) { return XchgLayout(d, rmax_su, G).total; }
 
-bool fused_supported(int d, int F, int rmax, bool int4, int G) {
+// FC row slots of the staging region: at least two batches of one neuron's rows
+int fc_slots_for(int d, bool int4, int stage_bytes) {
+    const int wrow = int4 ? d / 2 + d / 16 : 2 * d;
+    const int n = stage_bytes / wrow;
+    return n < kMaxFcSlots ? n : kMaxFcSlots;
+}
+
+bool fused_supported(int d, int F, int rmax, bool int4, bool gated, int G) {
     if (d % 8 != 0 || G < 1) return false;
+    if (int4 && d % 256 != 0) return false;                  // 16-byte bulk copies of the scale rows
     if (!int4 && d > 4 * kCols) return false;              // FC2: 8 columns per thread and chunk
     if (int4 && (d % 32 != 0 || d > 64 * kThreads)) return false;  // FC2: two groups per thread
     if (max_units(F, G) > kMaxUnits) return false;
     const size_t rmax_su = (size_t)16 * G + 2 * (size_t)rmax;
-    return smem_plan(d, F, rmax, rmax_su, G).bytes() <= 220 * 1024;
+    const SmemPlan sp = smem_plan(d, F, rmax, rmax_su, G);
+    const long long room = 227ll * 1024 - 1024 - sp.off_stage();
+    if (room <= 0) return false;
+    return fc_slots_for(d, int4, (int)(room / 16 * 16)) >= (gated ? 4 : 2);
 }
 
 cudaError_t launch_fused(const FusedStackArgs& a, cudaStream_t s) {
@@ -1321,12 +1348,13 @@ cudaError_t launch_fused(const FusedStackArgs& a, cudaStream_t s) {
     // the staging region takes the rest of shared memory (leaving room for the
     // kernel's static shared variables); it must at least hold the predictor slices
     {
-        const bool tma_ok = !a.int4 || (a.d % 256 == 0);     // 16-byte multiples for INT4 scales
         const int pred = sp.p1s + sp.p2s + sp.b1s;
         const long long room = 227ll * 1024 - 1024 - sp.off_stage();
-        const int st = tma_ok ? (int)(room / 16 * 16) : pred;
+        const int st = (int)(room / 16 * 16);
         sp.stage = st > pred ? st : pred;
-        prm.stage_bytes = tma_ok ? sp.stage : 0;
+        prm.stage_bytes = sp.stage;
+        prm.fc_slots = fc_slots_for(a.d, a.int4, sp.stage);
+        if (prm.fc_slots < (a.gated ? 4 : 2)) return cudaErrorInvalidValue;
         // predictor slices too large for shared memory: stream P2 in 16-row units
         // through the mask/list buffers and the staging region
         const int unit = 16 * rmax * 2;

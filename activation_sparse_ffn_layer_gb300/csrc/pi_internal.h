@@ -133,7 +133,7 @@ struct FusedStackArgs {
     int32_t* layer_counts;    // nullable [L][2] (zeroed by the caller of launch_fused)
 };
 size_t fused_workspace_bytes(int d, int F, size_t rmax_su, int G);
-bool fused_supported(int d, int F, int rmax, bool int4, int G);
+bool fused_supported(int d, int F, int rmax, bool int4, bool gated, int G);
 cudaError_t launch_fused(const FusedStackArgs& a, cudaStream_t s);
 cudaError_t launch_wait_nothing(long long timeout_ns, cudaStream_t s);
 cudaError_t read_and_clear_status(int* out, cudaStream_t s);
