@@ -207,6 +207,14 @@ def run_ours(args):
     tokens = make_tokens(cfg, 0, T, device="cuda")
     st = DecodeStack(layers, batch=B, tau=cfg.tau, eps=cfg.rms_eps)
     weight_bytes = sum(w.nbytes() for w in layers)
+    # a stack whose weights fit in L2 (c1) is timed over R copies of itself in
+    # rotation (one copy per step, more than twice L2 in all), so every step
+    # reads its weights from HBM
+    R = 1
+    if weight_bytes < 2 * L2_BYTES:
+        R = min(32, -(-2 * L2_BYTES // weight_bytes))
+    stacks = [st] + [DecodeStack([clone_layer(w) for w in layers], batch=B, tau=cfg.tau, eps=cfg.rms_eps)
+                     for _ in range(R - 1)]
 
     # per-step algorithmic bytes (untimed)
     counts = measure_counts(st, tokens, B)
@@ -220,12 +228,14 @@ def run_ours(args):
     n_pred_mean = sum(n for per in counts for n, _ in per) / (NS * L)
     n_relu_mean = sum(z for per in counts for _, z in per) / (NS * L)
 
-    st.capture()
+    for s_ in stacks:
+        s_.capture()
     stream = torch.cuda.current_stream()
     K, W = args.steps, args.warmup
-    for i in range(W):
-        st.x_in.copy_(tokens[(i % NS) * B:(i % NS + 1) * B])
-        st.replay()
+    for i in range(max(W, R)):
+        s_ = stacks[i % R]
+        s_.x_in.copy_(tokens[(i % NS) * B:(i % NS + 1) * B])
+        s_.replay()
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -237,9 +247,10 @@ def run_ours(args):
         e0.record(stream)
         for i in range(K):
             t = (W + i) % NS
-            st.x_in.copy_(tokens[t * B:(t + 1) * B])
+            s_ = stacks[(W + i) % R]
+            s_.x_in.copy_(tokens[t * B:(t + 1) * B])
             ka[i].record(stream)
-            st.replay()
+            s_.replay()
             kb[i].record(stream)
         e1.record(stream)
         torch.cuda.synchronize()
@@ -273,7 +284,9 @@ def run_ours(args):
         "config": {"workload": f"{cfg.key}: {cfg.name}, batch {B}, {L} layers per step",
                    "batch": B, "layers": L, "d": cfg.d, "ffn": cfg.F, "tokens_cycled": T,
                    "weights": "int4-g32" if cfg.int4 else "fp16",
-                   "l2": f"inputs larger than L2 ({weight_bytes / 1e9:.1f} GB of layer weights per step)",
+                   "l2": (f"inputs larger than L2 ({weight_bytes / 1e9:.1f} GB of layer weights per step)" if R == 1 else
+                          f"inputs larger than L2: {R} copies of the {weight_bytes / 1e6:.1f} MB stack in rotation, "
+                          f"one per step ({R * weight_bytes / 1e6:.0f} MB)"),
                    "parallelism": "replicas" if world > 1 else "single"},
         "achieved_gbs_step": round(step_bytes / (ms / K / 1e3) / 1e9, 1),
         "frac_step": round(step_bytes / (ms / K / 1e3) / 1e9 / peak, 4),
@@ -291,6 +304,20 @@ def run_ours(args):
         print(json.dumps(out), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+L2_BYTES = 129 * 1000 * 1000   # GB300 L2 (nominal)
+
+
+def clone_layer(w):
+    """A copy of a layer's weights in fresh device memory (same values)."""
+    import dataclasses
+    import torch
+    kw = {}
+    for f in dataclasses.fields(w):
+        v = getattr(w, f.name)
+        kw[f.name] = v.clone() if isinstance(v, torch.Tensor) and v.is_cuda else v
+    return type(w)(**kw)
 
 
 def time_e2e(st, tokens, K, W, B=1):
