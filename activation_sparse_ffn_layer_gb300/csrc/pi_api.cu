@@ -319,7 +319,9 @@ pi_status pi_ffn_stack(const pi_layer_desc* desc, int n_layers, const pi_layer_w
 }
 
 pi_status pi_rmsnorm_half(int d, int batch, const float* y, float eps, pi_half* x_out, void* stream) {
-    if (d <= 0 || batch <= 0 || !y || !x_out || !(eps >= 0.f)) return PI_ERR_INVALID_ARG;
+    if (d <= 0 || d % 4 != 0 || batch <= 0 || !y || !x_out || !(eps >= 0.f) || !aligned16(y) ||
+        (reinterpret_cast<uintptr_t>(x_out) & 7u) != 0)
+        return PI_ERR_INVALID_ARG;
     return from_cuda(launch_rmsnorm(d, batch, y, eps, reinterpret_cast<__half*>(x_out),
                                     static_cast<cudaStream_t>(stream)));
 }
@@ -340,7 +342,7 @@ int pi_launches_per_layer(const pi_layer_desc* desc) {
     // predictor: u GEMM + finish + s GEMM on the streamed paths, else 2 per token chunk
     const int pred = (p.pred == 2 && p.r % 16 == 0) || p.pred == 1 ? 3 : 2 * chunks;
     // FC1 + finish and FC2 + reduction on the streamed paths, else 1 per chunk each + 1
-    const int ffn = (p.tc || p.st) ? 4 : p.st4 ? 2 + 2 * ((p.B + 7) / 8) : chunks + chunks + 1;
+    const int ffn = (p.tc || p.st || p.st4) ? 4 : chunks + chunks + 1;
     return pred + 1 + ffn;
 }
 

@@ -380,25 +380,51 @@ __global__ void __launch_bounds__(256) k_fc2_reduce(const float* __restrict__ pa
 
 // -------------------------------------------------------------- normalisation
 
-__global__ void __launch_bounds__(256) k_rmsnorm(const float* __restrict__ y, int d, float eps,
-                                                 __half* __restrict__ x) {
-    __shared__ float red[8];
-    const float* yb = y + (size_t)blockIdx.x * d;
+// x_b = fp16(y_b / sqrt(mean(y_b^2) + eps)): one block of 1024 threads per
+// token; each thread keeps its float4 words of y in registers between the
+// sum of squares and the scaling (d % 4 == 0), the block sum in a fixed order.
+constexpr int kNormThreads = 1024;
+constexpr int kNormWords = 4;   // float4 words per thread held in registers (d <= 16384)
+__global__ void __launch_bounds__(kNormThreads) k_rmsnorm(const float* __restrict__ y, int d, float eps,
+                                                          __half* __restrict__ x) {
+    __shared__ float red[32];
+    const float4* yb = reinterpret_cast<const float4*>(y + (size_t)blockIdx.x * d);
+    const int n4 = d / 4;
+    float4 v[kNormWords];
     float ss = 0.f;
-    for (int c = threadIdx.x; c < d; c += blockDim.x) ss = fmaf(yb[c], yb[c], ss);
+#pragma unroll
+    for (int k = 0; k < kNormWords; ++k) {
+        const int i4 = threadIdx.x + k * kNormThreads;
+        v[k] = i4 < n4 ? __ldg(yb + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < kNormWords; ++k) ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+    for (int i4 = threadIdx.x + kNormWords * kNormThreads; i4 < n4; i4 += kNormThreads) {
+        const float4 t = __ldg(yb + i4);
+        ss += t.x * t.x + t.y * t.y + t.z * t.z + t.w * t.w;
+    }
     ss = warp_sum(ss);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (lane == 0) red[warp] = ss;
     __syncthreads();
     if (warp == 0) {
-        float v = lane < 8 ? red[lane] : 0.f;
-        v = warp_sum(v);
-        if (lane == 0) red[0] = v;
+        float t = red[lane];
+        t = warp_sum(t);
+        if (lane == 0) red[0] = t;
     }
     __syncthreads();
     const float scale = rsqrtf(red[0] / (float)d + eps);
-    __half* xb = x + (size_t)blockIdx.x * d;
-    for (int c = threadIdx.x; c < d; c += blockDim.x) xb[c] = __float2half_rn(yb[c] * scale);
+    __half2* xb = reinterpret_cast<__half2*>(x + (size_t)blockIdx.x * d);
+    auto put = [&](int i4, const float4& t) {
+        xb[2 * i4] = __halves2half2(__float2half_rn(t.x * scale), __float2half_rn(t.y * scale));
+        xb[2 * i4 + 1] = __halves2half2(__float2half_rn(t.z * scale), __float2half_rn(t.w * scale));
+    };
+#pragma unroll
+    for (int k = 0; k < kNormWords; ++k) {
+        const int i4 = threadIdx.x + k * kNormThreads;
+        if (i4 < n4) put(i4, v[k]);
+    }
+    for (int i4 = threadIdx.x + kNormWords * kNormThreads; i4 < n4; i4 += kNormThreads) put(i4, __ldg(yb + i4));
 }
 
 // out[0] = n, out[1] = number of listed neurons with a non-zero h for some token
@@ -543,7 +569,7 @@ cudaError_t launch_count_active(const Plan& p, const int32_t* count, const float
 }
 
 cudaError_t launch_rmsnorm(int d, int B, const float* y, float eps, __half* x, cudaStream_t s) {
-    k_rmsnorm<<<B, 256, 0, s>>>(y, d, eps, x);
+    k_rmsnorm<<<B, kNormThreads, 0, s>>>(y, d, eps, x);
     return cudaGetLastError();
 }
 

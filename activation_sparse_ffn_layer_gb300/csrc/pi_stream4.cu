@@ -322,7 +322,9 @@ __global__ void __launch_bounds__(kQThreads, 1) k_fc1_st4(Q1Args a) {
 
 template <int TB>
 struct Q2Cfg {
-    static constexpr int HP = TB | 1;                    // padded h row (floats)
+    // padded h row (floats): odd for TB <= 8 (lanes read one float of 8 rows);
+    // 20 for TB = 16 (lanes read their row's 16 floats as 4 float4 from 4 rows)
+    static constexpr int HP = TB == 16 ? 20 : (TB | 1);
     static constexpr int RAW = 64 * HP * 4;
     static constexpr int IDX = 64 * 2 * 4;
     static constexpr int STAGE = kQTile2 + RAW;
@@ -472,11 +474,17 @@ __global__ void __launch_bounds__(kQThreads, 1) k_fc2_st4(Q2Args a) {
             for (int q = it - C::LAG < 0 ? 0 : it - C::LAG; q < it; ++q) bar_arrive(&full[q % C::S]);
         }
     } else {
-        // lane (mc = 4cw + (lane >> 3), rg = lane & 7): 8 columns x rows rg + 8i
-        const int cw = warp - 4, mc = 4 * cw + (lane >> 3), rg = lane & 7;
-        float acc[8][TB];
+        // TB <= 8: lane (mc = 4cw + (lane >> 3), rg = lane & 7) owns 8 columns and rows rg + 8i;
+        // TB = 16: lane (mq = 8cw + (lane & 7), rg = lane >> 3) owns 4 columns and rows rg + 4i
+        // (all 16 tokens in one pass: the W2t rows are read once)
+        constexpr int CPL = TB == 16 ? 4 : 8;   // columns per lane
+        constexpr int NRG = TB == 16 ? 4 : 8;   // row groups (lanes sharing the columns)
+        const int cw = warp - 4;
+        const int col0 = TB == 16 ? (8 * cw + (lane & 7)) * 4 : (4 * cw + (lane >> 3)) * 8;
+        const int rg = TB == 16 ? lane >> 3 : lane & 7;
+        float acc[CPL][TB];
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
+        for (int e = 0; e < CPL; ++e)
 #pragma unroll
             for (int tt = 0; tt < TB; ++tt) acc[e][tt] = 0.f;
         int it = 0;
@@ -492,19 +500,35 @@ __global__ void __launch_bounds__(kQThreads, 1) k_fc2_st4(Q2Args a) {
                 }
                 const unsigned char* sb = ring + (size_t)s * C::STAGE;
                 const float* raw = reinterpret_cast<const float*>(sb + kQTile2);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int kk = rg + 8 * i;
-                    const uint32_t cwd = *reinterpret_cast<const uint32_t*>(sb + kk * kQPitch + mc * 4);
-                    const float scl = __half2float(*reinterpret_cast<const __half*>(sb + kk * kQPitch + 128 + (mc >> 2) * 2));
+#pragma unroll 4
+                for (int i = 0; i < 64 / NRG; ++i) {
+                    const int kk = rg + NRG * i;
+                    const unsigned char* rowp = sb + kk * kQPitch;
+                    const uint32_t cwd = TB == 16 ? (uint32_t)*reinterpret_cast<const uint16_t*>(rowp + col0 / 2)
+                                                  : *reinterpret_cast<const uint32_t*>(rowp + col0 / 2);
+                    const float scl = __half2float(*reinterpret_cast<const __half*>(rowp + 128 + (col0 / 32) * 2));
                     float qf[8];
                     q8_to_f8(cwd, qf);
+                    float hv[TB];
+                    if (TB == 16) {
+#pragma unroll
+                        for (int v4 = 0; v4 < TB / 4; ++v4) {
+                            const float4 h4 = reinterpret_cast<const float4*>(raw + kk * C::HP)[v4];
+                            hv[4 * v4] = h4.x;
+                            hv[4 * v4 + 1] = h4.y;
+                            hv[4 * v4 + 2] = h4.z;
+                            hv[4 * v4 + 3] = h4.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int tt = 0; tt < TB; ++tt) hv[tt] = raw[kk * C::HP + tt];
+                    }
 #pragma unroll
                     for (int tt = 0; tt < TB; ++tt) {
                         if (tt < a.nb) {
-                            const float hs = raw[kk * C::HP + tt] * scl;
+                            const float hs = hv[tt] * scl;
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) acc[e][tt] = fmaf(hs, qf[e], acc[e][tt]);
+                            for (int e = 0; e < CPL; ++e) acc[e][tt] = fmaf(hs, qf[e], acc[e][tt]);
                         }
                     }
                 }
@@ -513,31 +537,38 @@ __global__ void __launch_bounds__(kQThreads, 1) k_fc2_st4(Q2Args a) {
             }
             if (!ok) break;
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
+            for (int e = 0; e < CPL; ++e)
 #pragma unroll
                 for (int tt = 0; tt < TB; ++tt) {
                     float v = acc[e][tt];
-                    v += __shfl_xor_sync(FULL, v, 1);
-                    v += __shfl_xor_sync(FULL, v, 2);
-                    v += __shfl_xor_sync(FULL, v, 4);
+                    if (TB == 16) {
+                        v += __shfl_xor_sync(FULL, v, 8);
+                        v += __shfl_xor_sync(FULL, v, 16);
+                    } else {
+                        v += __shfl_xor_sync(FULL, v, 1);
+                        v += __shfl_xor_sync(FULL, v, 2);
+                        v += __shfl_xor_sync(FULL, v, 4);
+                    }
                     acc[e][tt] = v;
                 }
             if (rg == 0) {
                 if (p < a.slots) {
-                    float* dst = a.part + ((size_t)g * a.slots + p) * TB * 256 + mc * 8;
+                    float* dst = a.part + ((size_t)g * a.slots + p) * TB * 256 + col0;
 #pragma unroll
                     for (int tt = 0; tt < TB; ++tt)
                         if (tt < a.nb) {
                             float4* o = reinterpret_cast<float4*>(dst + (size_t)tt * 256);
-                            o[0] = make_float4(acc[0][tt], acc[1][tt], acc[2][tt], acc[3][tt]);
-                            o[1] = make_float4(acc[4][tt], acc[5][tt], acc[6][tt], acc[7][tt]);
+#pragma unroll
+                            for (int e4 = 0; e4 < CPL / 4; ++e4)
+                                o[e4] = make_float4(acc[4 * e4][tt], acc[4 * e4 + 1][tt], acc[4 * e4 + 2][tt],
+                                                    acc[4 * e4 + 3][tt]);
                         }
                 } else {
                     atomicExch(a.status, (int)PI_ERR_WORKSPACE);
                 }
             }
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
+            for (int e = 0; e < CPL; ++e)
 #pragma unroll
                 for (int tt = 0; tt < TB; ++tt) acc[e][tt] = 0.f;
         }
@@ -551,7 +582,7 @@ cudaError_t prep_q(K kernel, size_t smem) {
 int qdiv(int a, int b) { return (a + b - 1) / b; }
 int qslots(int tiles, int G) { return qdiv(tiles, G) + 2; }
 int q1_tokens(int B) { return B <= 4 ? 4 : (B <= 8 ? 8 : 16); }
-int q2_tokens(int B) { return B <= 4 ? 4 : 8; }
+int q2_tokens(int B) { return B <= 4 ? 4 : (B <= 8 ? 8 : 16); }
 
 }  // namespace
 
@@ -605,7 +636,7 @@ cudaError_t launch_fc2_st4(const Plan& p, const float* h, const int32_t* idx, co
             if (e != cudaSuccess) return e;                              \
             k_fc2_st4<TBV><<<G, kQThreads, Q2Cfg<TBV>::SMEM, s>>>(a);     \
         }
-        PI_Q2(4) else PI_Q2(8)
+        PI_Q2(4) else PI_Q2(8) else PI_Q2(16)
 #undef PI_Q2
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;

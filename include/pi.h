@@ -217,7 +217,8 @@ PI_API pi_status pi_workspace_layout(const pi_layer_desc *desc, pi_workspace_lay
 /*
  * Inter-layer normalisation of a decode stack: x_out[b, c] =
  * fp16(y[b, c] / sqrt(mean_c(y[b, :]^2) + eps)) with round-to-nearest-even.
- * y: [B, d] fp32; x_out: [B, d] fp16.
+ * y: [B, d] fp32, 16-byte aligned; x_out: [B, d] fp16, 8-byte aligned; d a
+ * multiple of 4 (else PI_ERR_INVALID_ARG).  One block per token.
  */
 PI_API pi_status pi_rmsnorm_half(int d, int batch, const float *y, float eps, pi_half *x_out,
                           void *stream);

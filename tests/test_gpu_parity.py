@@ -212,7 +212,7 @@ def test_layer_empty_and_full_masks():
 def test_rmsnorm_parity():
     P = _pi()
     rng = np.random.default_rng(5)
-    for d, B in ((768, 1), (4096, 3), (12288, 2), (8, 1)):
+    for d, B in ((768, 1), (4096, 3), (12288, 2), (8, 1), (20000, 2)):
         y = (rng.standard_normal((B, d)) * rng.uniform(0.01, 3.0)).astype(np.float32)
         yd = torch.from_numpy(y).to(DEV)
         x = torch.empty(B, d, dtype=torch.float16, device=DEV)
