@@ -199,7 +199,7 @@ struct SmemPlan {
     int d, rmax, usmax, M, cap;
     int p1s = 0, p2s = 0, b1s = 0;  // shared predictor buffers (bytes, 16-aligned), 0 if unused
     int stage = 0;                  // staging region (bytes, 16-aligned): the predictor buffers
-                                    // in phases A-B, this CTA's FC rows in phase C
+                                    // up to the mask bits, then the ring of this CTA's FC rows
     __host__ __device__ int off_u() const { return d * 4; }
     __host__ __device__ int off_ust() const { return off_u() + rmax * 4; }
     __host__ __device__ int off_scr() const { return ((off_ust() + ((usmax + 3) / 4) * 16 + 15) / 16) * 16; }

@@ -143,7 +143,9 @@ __global__ void __launch_bounds__(1024) k_compact(const uint32_t* __restrict__ m
         const int w = w0 + threadIdx.x;
         uint32_t bits = 0u;
         if (w < W) {
-            for (int b = 0; b < B; ++b) bits |= mask[(size_t)b * W + w];
+            // tokens' words requested 8 at a time (independent loads in flight)
+#pragma unroll 8
+            for (int b = 0; b < B; ++b) bits |= __ldg(mask + (size_t)b * W + w);
             if (w == W - 1 && (F & 31)) bits &= (1u << (F & 31)) - 1u;
         }
         const int c = __popc(bits);

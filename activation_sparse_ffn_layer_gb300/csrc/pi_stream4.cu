@@ -36,6 +36,19 @@ constexpr int kQTile = 128 * kQPitch;
 constexpr int kQTile2 = 64 * kQPitch;
 constexpr long long kQTimeoutNs = 2000000000ll;
 
+// Barriers of the 256 compute threads (ids 0 and 1 are the CTA's and the
+// loaders'): a plain one, and one that ORs a flag so all take the same branch
+PI_DEV void compute_sync() { asm volatile("bar.sync 2, 256;" ::: "memory"); }
+PI_DEV bool compute_sync_any(bool v) {
+    unsigned r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred p, 2, 256, q;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(r)
+        : "r"((unsigned)v)
+        : "memory");
+    return r != 0;
+}
+
 // 16 codes (low nibble first) of one 64-bit word -> exact floats
 PI_DEV void q16_to_f16(uint2 w, float (&f)[16]) {
     float a[8], b[8];
@@ -56,10 +69,17 @@ struct Q1Cfg {
     // shared-memory phase read 8 disjoint bank quads
     static constexpr int XROW = 8 * 80;
     static constexpr int STAGE = kQTile + TB * XROW;
-    static constexpr int S0 = kQBudget / STAGE > 12 ? 12 : kQBudget / STAGE;
+    // the stage's x converted to fp32 once for all compute lanes: per token 8
+    // groups of 32 floats at a 36-float pitch (8 group lanes hit 8 bank quads)
+    // (for 8 tokens and more; with 4 the lanes convert their own x words)
+    static constexpr bool PRE = TB >= 8;
+    static constexpr int XF_GROUP = 36;
+    static constexpr int XF_TOKEN = 8 * XF_GROUP;
+    static constexpr int XF = PRE ? TB * XF_TOKEN * 4 : 0;
+    static constexpr int S0 = (kQBudget - XF) / STAGE > 12 ? 12 : (kQBudget - XF) / STAGE;
     static constexpr int S = S0 & ~1;
     static constexpr int LAGP = S / 2 >= 4 ? S / 2 - 2 : S / 2 - 1;
-    static constexpr size_t SMEM = (size_t)S * STAGE + 16;
+    static constexpr size_t SMEM = (size_t)S * STAGE + XF + 16;
 };
 
 struct Q1Args {
@@ -117,6 +137,7 @@ __global__ void __launch_bounds__(kQThreads, 1) k_fc1_st4(Q1Args a) {
     __syncthreads();
     const Ctl ctl{a.status, a.timeout_ns, &abort_flag};
     const size_t cpr = (size_t)a.K / 2, spr = (size_t)a.K / 32;   // code bytes, scales per row
+    float* xsf = reinterpret_cast<float*>(ring + (size_t)C::S * C::STAGE);   // [TB][XF_TOKEN] fp32 x
 
     if (warp < 4) {
         const int t = tid, w = t >> 5, l = t & 31;
@@ -244,11 +265,28 @@ __global__ void __launch_bounds__(kQThreads, 1) k_fc1_st4(Q1Args a) {
             bool ok = true;
             for (int ks = sp.kc0; ks < sp.kc1; ++ks, ++it) {
                 const int s = it % C::S;
-                if (!bar_wait(&full[s], (it / C::S) & 1, ctl)) {
+                // every compute thread has left the previous stage (its x scratch is
+                // free); stop together if a wait failed
+                const bool got = bar_wait(&full[s], (it / C::S) & 1, ctl);
+                if (C::PRE ? compute_sync_any(!got) : !got) {
                     ok = false;
                     break;
                 }
                 const unsigned char* st = ring + (size_t)s * C::STAGE;
+                if (C::PRE) {
+                    // convert the stage's x once: thread tc takes 8-element words tc, tc + 256, ...
+                    const int tc = tid - 128;
+                    for (int wdx = tc; wdx < a.B * 32; wdx += 256) {
+                        const int tok = wdx >> 5, kx = wdx & 31, grp = kx >> 2;
+                        float xv8[8];
+                        h8_to_f8(*reinterpret_cast<const uint4*>(st + kQTile + tok * C::XROW + grp * 80 + (kx & 3) * 16),
+                                 xv8);
+                        float4* o = reinterpret_cast<float4*>(xsf + tok * C::XF_TOKEN + grp * C::XF_GROUP + (kx & 3) * 8);
+                        o[0] = make_float4(xv8[0], xv8[1], xv8[2], xv8[3]);
+                        o[1] = make_float4(xv8[4], xv8[5], xv8[6], xv8[7]);
+                    }
+                    compute_sync();
+                }
                 float sc[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
@@ -265,15 +303,27 @@ __global__ void __launch_bounds__(kQThreads, 1) k_fc1_st4(Q1Args a) {
                         q16_to_f16(*reinterpret_cast<const uint2*>(st + (4 * cw + rg + 32 * i) * kQPitch + c * 16 +
                                                                    half * 8),
                                    q[i]);
-                    const unsigned char* xs = st + kQTile + c * 80 + half * 32;
+                    const float* xs = xsf + c * C::XF_GROUP + half * 16;
+                    const unsigned char* xh = st + kQTile + c * 80 + half * 32;
 #pragma unroll
                     for (int tt = 0; tt < TB; ++tt) {
                         if (tt < a.B) {
                             float xv[16];
-                            h8_to_f8(*reinterpret_cast<const uint4*>(xs + tt * C::XROW),
-                                     *reinterpret_cast<float(*)[8]>(xv));
-                            h8_to_f8(*reinterpret_cast<const uint4*>(xs + tt * C::XROW + 16),
-                                     *reinterpret_cast<float(*)[8]>(xv + 8));
+                            if (C::PRE) {
+#pragma unroll
+                                for (int v4 = 0; v4 < 4; ++v4) {
+                                    const float4 x4 = reinterpret_cast<const float4*>(xs + tt * C::XF_TOKEN)[v4];
+                                    xv[4 * v4] = x4.x;
+                                    xv[4 * v4 + 1] = x4.y;
+                                    xv[4 * v4 + 2] = x4.z;
+                                    xv[4 * v4 + 3] = x4.w;
+                                }
+                            } else {
+                                h8_to_f8(*reinterpret_cast<const uint4*>(xh + tt * C::XROW),
+                                         *reinterpret_cast<float(*)[8]>(xv));
+                                h8_to_f8(*reinterpret_cast<const uint4*>(xh + tt * C::XROW + 16),
+                                         *reinterpret_cast<float(*)[8]>(xv + 8));
+                            }
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
                                 float pt = q[i][0] * xv[0];
