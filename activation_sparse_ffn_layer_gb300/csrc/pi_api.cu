@@ -74,6 +74,7 @@ bool make_plan(const pi_layer_desc& desc, Plan* p) {
     q.tc = tc_supported(q);
     q.st = !q.tc && st_supported(q);
     q.st4 = !q.tc && !q.st && st4_supported(q);
+    q.fc1_tc4 = q.st4 && tc4_supported(q);
     q.pred = tc_pred_supported(q) ? 2 : (st_pred_supported(q) ? 1 : 0);
     {
         // partial sums of whichever paths the plan takes (the stream-K sizes
@@ -82,6 +83,7 @@ bool make_plan(const pi_layer_desc& desc, Plan* p) {
         if (q.pred == 2 || q.tc) part = std::max(part, tc_part_floats(q));
         if (q.pred == 1 || q.st) part = std::max(part, st_part_floats(q));
         if (q.st4) part = std::max(part, st4_part_floats(q));
+        if (q.fc1_tc4) part = std::max(part, tc_part_floats(q));
         q.part_floats = part;
     }
     size_t off = q.xchg_bytes;

@@ -28,6 +28,7 @@ struct Plan {
     bool tc;        // FC1 / FC2 take the tcgen05 batched path (batch 16..32, fp16 weights)
     bool st;        // ... or the CUDA-core streamed batched path (batch 2..8, fp16 weights)
     bool st4;       // ... or its INT4 variant (batch 2..16, ReLU FFN)
+    bool fc1_tc4;   // INT4 FC1 on the tensor cores (fp16 hi | lo dequantisation; batch 16)
     int pred;       // predictor path (its weights are fp16 for every weight type):
                     // 2 tcgen05 (batch 16..32), 1 streamed CUDA cores (batch 2..8), 0 chunked
     size_t part_floats;  // FC2 partial sums of whichever FC2 path the plan takes
@@ -79,6 +80,10 @@ cudaError_t launch_fc1_tc(const Plan& p, const __half* x, const LayerPtrs& w, co
                           cudaStream_t s);
 cudaError_t launch_fc2_tc(const Plan& p, const float* h, const int32_t* idx, const int32_t* count,
                           const LayerPtrs& w, const int32_t* live, float* partial, float* y, cudaStream_t s);
+bool tc4_supported(const Plan& p);
+cudaError_t launch_fc1_tc4(const Plan& p, const __half* x, const LayerPtrs& w, const int32_t* idx,
+                           const int32_t* count, const uint32_t* mask, float* part, float* h, int32_t* live,
+                           cudaStream_t s);
 
 // fixed-order finishing of the stream-K partials (shared by the batched paths):
 // nt = partial columns per token group, G = CTAs of the split, slots = tiles per

@@ -521,6 +521,7 @@ cudaError_t launch_fc1(const Plan& p, const __half* x, const LayerPtrs& w, const
                        cudaStream_t s) {
     if (p.tc) return launch_fc1_tc(p, x, w, idx, count, mask, partial, h, live, s);
     if (p.st) return launch_fc1_st(p, x, w, idx, count, mask, partial, h, live, s);
+    if (p.fc1_tc4) return launch_fc1_tc4(p, x, w, idx, count, mask, partial, h, live, s);
     if (p.st4) return launch_fc1_st4(p, x, w, idx, count, mask, partial, h, live, s);
     const int kind = p.int4 ? 2 : (p.gated ? 1 : 0);
     return for_token_chunks(p.B, [&](int b0, int tb) -> cudaError_t {

@@ -125,6 +125,10 @@ constexpr int tmem_cols_for(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 1
 //   MODE 1  FC1 gated      A = Wg and Wu rows (gathered),   Bop = x
 //   MODE 2  predictor u    A = P1 rows,                     Bop = x
 //   MODE 3  predictor s    A = P2 rows,                     Bop = u (hi | lo fp16)
+//   MODE 4  FC1, INT4 rows A = W1 codes x group scales as two fp16 tiles
+//                          hi = fp16(q s) and lo = fp16(q s - hi), both
+//                          multiplied into the same accumulator (hi + lo
+//                          carries q s to within 2^-24), Bop = x
 // Modes 0-2 split the (tile x K-chunk) space evenly over the CTAs and write
 // one partial tile per tile touched; a finish kernel adds the partials of each
 // tile in ascending CTA order and applies the epilogue.  Mode 3 has short K
@@ -134,26 +138,35 @@ constexpr int tmem_cols_for(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 1
 
 template <int MODE, int NT>
 struct RowsCfg {
-    static constexpr bool GATHER = MODE <= 1;
+    static constexpr bool Q4 = MODE == 4;
+    static constexpr bool GATHER = MODE <= 1 || Q4;
     static constexpr bool DIRECT = MODE == 3;
-    static constexpr int NA = MODE == 1 ? 2 : 1;            // A operand tiles per stage
+    static constexpr int NA = (MODE == 1 || Q4) ? 2 : 1;   // A operand tiles per stage
+    static constexpr int NACC = MODE == 1 ? 2 : 1;          // accumulators (gate and up)
     static constexpr int NB = DIRECT ? 2 * NT : NT;          // B operand rows
     static constexpr int X = NB * 128;                       // NB rows x 64 fp16
     static constexpr int STAGE = NA * kTileA + X;
     // even ring of stages, filled two K-chunks at a time (256 contiguous bytes
-    // of every row per visit); LAGP pairs of copies stay in flight
-    static constexpr int S0 = kRingBudget / STAGE > 12 ? 12 : kRingBudget / STAGE;
+    // of every row per visit); LAGP pairs of copies stay in flight.  INT4:
+    // 4 stages, fed from a deeper ring of raw K-chunks (per row 32 bytes of
+    // codes and 4 of scales at a 48-byte pitch, then the chunk of x)
+    static constexpr int S0 = Q4 ? 4 : (kRingBudget / STAGE > 12 ? 12 : kRingBudget / STAGE);
     static constexpr int S = S0 & ~1;
     static constexpr int LAGP = S / 2 >= 4 ? S / 2 - 2 : S / 2 - 1;
-    static constexpr int ACC = NA * NB;                      // TMEM columns per accumulator buffer
-    static constexpr int COLS = NA * NT;                     // partial columns (modes 0-2)
+    static constexpr int RAWB = 128 * 48 + X;
+    static constexpr int RS0 = Q4 ? (kRingBudget - S * STAGE) / RAWB : 0;
+    static constexpr int RS = RS0 > 12 ? 12 : RS0;
+    static constexpr int ACC = NACC * NB;                    // TMEM columns per accumulator buffer
+    static constexpr int COLS = NACC * NT;                   // partial columns (modes 0-2, 4)
     static constexpr int TMEM = tmem_cols_for(2 * ACC);
-    static constexpr size_t SMEM = (size_t)S * STAGE + 1024;
+    static constexpr size_t SMEM = (size_t)S * STAGE + (size_t)RS * RAWB + 1024;
 };
 
 struct TcRowsArgs {
     const __half* a0;      // A rows (row length K)
     const __half* a1;      // up-projection rows (gated FC1)
+    const uint8_t* q;      // mode 4: W1 codes [F][K/2]
+    const __half* qs;      // mode 4: W1 group scales [F][K/32]
     const int32_t* idx;    // gathered row ids (FC1)
     const int32_t* count;  // device row count (FC1), else R rows
     int R;
@@ -169,6 +182,156 @@ struct TcRowsArgs {
     int* status;
     long long timeout_ns;
 };
+
+// cp.async.wait_group with a count known only at run time (0 .. 11)
+PI_DEV void cp_wait_n(int n) {
+    switch (n) {
+        case 0: cp_wait<0>(); break;
+        case 1: cp_wait<1>(); break;
+        case 2: cp_wait<2>(); break;
+        case 3: cp_wait<3>(); break;
+        case 4: cp_wait<4>(); break;
+        case 5: cp_wait<5>(); break;
+        case 6: cp_wait<6>(); break;
+        case 7: cp_wait<7>(); break;
+        case 8: cp_wait<8>(); break;
+        case 9: cp_wait<9>(); break;
+        case 10: cp_wait<10>(); break;
+        default: cp_wait<11>(); break;
+    }
+}
+
+// 8 INT4 codes (element e in bits 4e..4e+3, two's complement) times the scale
+// s, as fp16 hi = fp16(q s) and lo = fp16(q s - hi), elements in order.  The
+// codes become exact fp16 values through the 1024 + n bit pattern; fp16
+// multiply and fma round once, so hi + lo = q s up to the fp16 spacing of lo.
+PI_DEV void q8_hi_lo(uint32_t w, __half2 s2, uint4& hi, uint4& lo) {
+    const uint32_t u = w ^ 0x88888888u;   // n + 8 in 0..15
+    const __half2 k1032 = __float2half2_rn(1032.f);
+    uint32_t ph[4], pl[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        uint32_t t = ((u >> (4 * k)) & 0x000F000Fu) | 0x64006400u;   // (1024 + n_k, 1024 + n_{k+4})
+        const __half2 q = __hsub2(*reinterpret_cast<__half2*>(&t), k1032);
+        const __half2 h = __hmul2(q, s2);
+        const __half2 l = __hfma2(q, s2, __hneg2(h));
+        ph[k] = *reinterpret_cast<const uint32_t*>(&h);
+        pl[k] = *reinterpret_cast<const uint32_t*>(&l);
+    }
+    // pairs (e_k, e_{k+4}) -> (e0 e1)(e2 e3)(e4 e5)(e6 e7)
+    hi = make_uint4(__byte_perm(ph[0], ph[1], 0x5410), __byte_perm(ph[2], ph[3], 0x5410),
+                    __byte_perm(ph[0], ph[1], 0x7632), __byte_perm(ph[2], ph[3], 0x7632));
+    lo = make_uint4(__byte_perm(pl[0], pl[1], 0x5410), __byte_perm(pl[2], pl[3], 0x5410),
+                    __byte_perm(pl[0], pl[1], 0x7632), __byte_perm(pl[2], pl[3], 0x7632));
+}
+
+// Loaders of the INT4 FC1 (mode 4): loader thread t owns row t of every tile.
+// It copies its row's K-chunk (32 bytes of codes, 4 of scales) and its share
+// of the x chunk into a raw ring RS-1 chunks ahead with cp.async, and for the
+// current chunk, once its own copies have landed and the stage is free,
+// writes the hi and lo fp16 rows into the stage's two A tiles (128-byte
+// swizzle) and its x share into the B tile, then arrives on `full`.  A thread
+// reads only what it copied itself, so the raw ring needs no barrier.
+template <typename C, typename SpanOf>
+PI_DEV void q4_loader(const TcRowsArgs& a, unsigned char* ring, const SpanOf& span, int npiece, int R,
+                      unsigned long long* full, unsigned long long* empty, const Ctl& ctl) {
+    const int t = threadIdx.x;
+    unsigned char* raw = ring + (size_t)C::S * C::STAGE;
+    const size_t cpr = (size_t)a.K / 2, spr = (size_t)a.K / 32;   // code bytes, scales per row
+    int total = 0;
+    for (int p = 0; p < npiece; ++p) {
+        const Span sp = span(p);
+        total += sp.kc1 - sp.kc0;
+    }
+    // issue cursor (runs RS-1 chunks ahead) and its row id
+    int ip = 0;
+    Span isp = span(0);
+    int iks = isp.kc0;
+    auto row_id = [&](int tile) {
+        const int rr = 128 * tile + t;
+        return rr < R ? a.idx[rr] : -1;
+    };
+    int irow = row_id(isp.tile);
+    auto issue = [&](int j) {
+        unsigned char* b = raw + (size_t)(j % C::RS) * C::RAWB;
+        if (irow >= 0) {
+            const uint8_t* src = a.q + (size_t)irow * cpr + (size_t)iks * 32;
+            cp16(b + t * 48, src);
+            cp16(b + t * 48 + 16, src + 16);
+            cp4(b + t * 48 + 32, a.qs + (size_t)irow * spr + (size_t)iks * 2);
+        }
+        const int k0 = iks * 64;
+        for (int pp = t; pp < C::NB * 8; pp += kLoaders) {
+            const int gg = pp >> 5, ll = pp & 31;
+            const int tok = 8 * (gg >> 1) + (ll & 7), kx = 4 * (gg & 1) + (ll >> 3);
+            if (tok < a.bop_rows)
+                cp16(b + 128 * 48 + kx * (C::NB * 16) + (tok >> 3) * 128 + (tok & 7) * 16,
+                     a.bop + (size_t)tok * a.K + k0 + kx * 8);
+        }
+        cp_commit();
+        if (++iks == isp.kc1 && ip + 1 < npiece) {
+            ++ip;
+            isp = span(ip);
+            iks = isp.kc0;
+            irow = row_id(isp.tile);
+        }
+    };
+    const int ahead = C::RS - 1;
+    int issued = 0;
+    while (issued < total && issued < ahead) issue(issued++);
+    // conversion cursor
+    int cp = 0;
+    Span csp = span(0);
+    int cks = csp.kc0;
+    for (int j = 0; j < total; ++j) {
+        if (issued < total) issue(issued++);
+        const int s = j % C::S;
+        bool good = true;
+        if (j >= C::S && !bar_wait(&empty[s], ((j / C::S) - 1) & 1, ctl)) good = false;
+        if (loaders_sync_any(!good)) break;   // stop together
+        cp_wait_n(issued - 1 - j);            // this thread's copies of chunk j have landed
+        const unsigned char* b = raw + (size_t)(j % C::RS) * C::RAWB;
+        unsigned char* st = ring + (size_t)s * C::STAGE;
+        const bool valid = 128 * csp.tile + t < R;
+        const unsigned rowoff = (t >> 3) * 1024 + (t & 7) * 128;
+        if (valid) {
+            const uint4 c0 = *reinterpret_cast<const uint4*>(b + t * 48);
+            const uint4 c1 = *reinterpret_cast<const uint4*>(b + t * 48 + 16);
+            const __half2 sc = *reinterpret_cast<const __half2*>(b + t * 48 + 32);
+            const __half2 s0 = __low2half2(sc), s1 = __high2half2(sc);
+            const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint4 hi, lo;
+                q8_hi_lo(cw[c], c < 4 ? s0 : s1, hi, lo);
+                const unsigned off = rowoff + ((c ^ (t & 7)) << 4);
+                *reinterpret_cast<uint4*>(st + off) = hi;
+                *reinterpret_cast<uint4*>(st + kTileA + off) = lo;
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                *reinterpret_cast<uint4*>(st + rowoff + (c << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(st + kTileA + rowoff + (c << 4)) = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        for (int pp = t; pp < C::NB * 8; pp += kLoaders) {
+            const int gg = pp >> 5, ll = pp & 31;
+            const int tok = 8 * (gg >> 1) + (ll & 7), kx = 4 * (gg & 1) + (ll >> 3);
+            const unsigned xo = kx * (C::NB * 16) + (tok >> 3) * 128 + (tok & 7) * 16;
+            *reinterpret_cast<uint4*>(st + 2 * kTileA + xo) =
+                tok < a.bop_rows ? *reinterpret_cast<const uint4*>(b + 128 * 48 + xo) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_async_smem();
+        bar_arrive(&full[s]);
+        if (++cks == csp.kc1 && cp + 1 < npiece) {
+            ++cp;
+            csp = span(cp);
+            cks = csp.kc0;
+        }
+    }
+    cp_wait_all();
+}
 
 template <int MODE, int NT>
 __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
@@ -237,7 +400,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
     const unsigned tmem = tmem_slot;
     const Ctl ctl{a.status, a.timeout_ns, &abort_flag};
 
-    if (warp < 4) {
+    if (warp < 4 && C::Q4) {
+        if constexpr (C::Q4) q4_loader<C>(a, ring, span, npiece, R, full, empty, ctl);
+    } else if (warp < 4) {
         // ---- loaders.  A tiles use the 128-byte-swizzled layout, so the 8
         // lanes of one shared-memory phase copy the 8 chunks of one row's 128
         // bytes without bank conflicts.  Stages go out in pairs: a warp
@@ -398,9 +563,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
                     if (lane == 0 && t < a.B && word < a.W) a.mask[(size_t)t * a.W + word] = bits;
                 }
             } else {
-                float v[C::NA][NT];
+                float v[C::NACC][NT];
 #pragma unroll
-                for (int q = 0; q < C::NA; ++q)
+                for (int q = 0; q < C::NACC; ++q)
 #pragma unroll
                     for (int c = 0; c < NT; c += 16) tmem_ld16(ta + q * C::NB + c, v[q] + c);
                 tmem_wait_ld();
@@ -409,7 +574,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
                 if (p < a.slots) {
                     float* dst = a.part + ((size_t)g * a.slots + p) * C::COLS * 128 + m;
 #pragma unroll
-                    for (int q = 0; q < C::NA; ++q)
+                    for (int q = 0; q < C::NACC; ++q)
 #pragma unroll
                         for (int t = 0; t < NT; ++t)
                             if (t < a.B) dst[(size_t)(q * NT + t) * 128] = v[q][t];
@@ -447,6 +612,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
                     const unsigned acc = (ks > sp.kc0 || kk > 0) ? 1u : 0u;
                     mma_f16(dcol, sdesc_sw128(sa + kk * 32), bd, idesc, acc);
                     if (MODE == 1) mma_f16(dcol + C::NB, sdesc_sw128(sa + kTileA + kk * 32), bd, idesc, acc);
+                    if (MODE == 4) mma_f16(dcol, sdesc_sw128(sa + kTileA + kk * 32), bd, idesc, 1u);   // + lo
                 }
                 mma_commit(&empty[s]);
             }
@@ -874,6 +1040,10 @@ int u_grid(const Plan& p) {
 }
 }  // namespace
 
+bool tc4_supported(const Plan& p) {
+    return p.int4 && !p.gated && p.B >= 16 && p.B <= 32 && p.d % 256 == 0 && p.nsm <= kMaxCtas;
+}
+
 bool tc_pred_supported(const Plan& p) { return p.B >= 16 && p.B <= 32 && p.d % 128 == 0 && p.nsm <= kMaxCtas; }
 
 bool tc_supported(const Plan& p) { return !p.int4 && tc_pred_supported(p); }
@@ -979,6 +1149,30 @@ cudaError_t launch_fc1_tc(const Plan& p, const __half* x, const LayerPtrs& w, co
         k_fc1_finish<false><<<blocks, 32 * p.B, 0, s>>>(part, a.slots, G, ceil_div(p.d, 64), count, p.B, nt, idx, w.b1,
                                                     mask, p.W, h, live);
     return cudaGetLastError();
+}
+
+cudaError_t launch_fc1_tc4(const Plan& p, const __half* x, const LayerPtrs& w, const int32_t* idx,
+                           const int32_t* count, const uint32_t* mask, float* part, float* h, int32_t* live,
+                           cudaStream_t s) {
+    int* status = status_word();
+    if (status == nullptr) return cudaErrorInvalidDevice;
+    const int G = p.nsm, nt = tc_tokens(p);
+    TcRowsArgs a{};
+    a.q = static_cast<const uint8_t*>(w.w1);
+    a.qs = w.w1s;
+    a.idx = idx;
+    a.count = count;
+    a.bop = x;
+    a.bop_rows = p.B;
+    a.K = p.d;
+    a.B = p.B;
+    a.part = part;
+    a.slots = slots_for(ceil_div(p.F, 128), G);
+    a.status = status;
+    a.timeout_ns = kTcTimeoutNs;
+    cudaError_t e = launch_rows_nt<4>(a, nt, G, s);
+    if (e != cudaSuccess) return e;
+    return launch_fc1_finish(p, nt, G, a.slots, ceil_div(p.d, 64), part, count, idx, w.b1, mask, h, live, s);
 }
 
 cudaError_t launch_fc1_finish(const Plan& p, int nt, int G, int slots, int nk, const float* part,
