@@ -28,7 +28,7 @@ struct Plan {
     bool tc;        // FC1 / FC2 take the tcgen05 batched path (batch 16..32, fp16 weights)
     bool st;        // ... or the CUDA-core streamed batched path (batch 2..8, fp16 weights)
     bool st4;       // ... or its INT4 variant (batch 2..16, ReLU FFN)
-    bool fc1_tc4;   // INT4 FC1 on the tensor cores (fp16 hi | lo dequantisation; batch 16)
+    bool fc1_tc4;   // INT4 FC1 on the tensor cores (codes as fp16, group scales in the epilogue; batch 16-32)
     int pred;       // predictor path (its weights are fp16 for every weight type):
                     // 2 tcgen05 (batch 16..32), 1 streamed CUDA cores (batch 2..8), 0 chunked
     size_t part_floats;  // FC2 partial sums of whichever FC2 path the plan takes

@@ -1,5 +1,5 @@
 // pi_tc.cu -- the batched union path on the tcgen05 tensor cores (batch 16..32,
-// fp16 weights).
+// fp16 weights, and the FC1 of INT4 weights).
 //
 // At batch B the union of the B tokens' predicted neurons is gathered once and
 // both FFN products become dense contractions over the gathered rows
@@ -125,10 +125,10 @@ constexpr int tmem_cols_for(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 1
 //   MODE 1  FC1 gated      A = Wg and Wu rows (gathered),   Bop = x
 //   MODE 2  predictor u    A = P1 rows,                     Bop = x
 //   MODE 3  predictor s    A = P2 rows,                     Bop = u (hi | lo fp16)
-//   MODE 4  FC1, INT4 rows A = W1 codes x group scales as two fp16 tiles
-//                          hi = fp16(q s) and lo = fp16(q s - hi), both
-//                          multiplied into the same accumulator (hi + lo
-//                          carries q s to within 2^-24), Bop = x
+//   MODE 4  FC1, INT4 rows A = W1 codes as exact fp16 integers, Bop = x;
+//                          each group of 32 along K has its own TMEM
+//                          accumulator, which the epilogue scales by the
+//                          row's group scale and adds up in registers
 // Modes 0-2 split the (tile x K-chunk) space evenly over the CTAs and write
 // one partial tile per tile touched; a finish kernel adds the partials of each
 // tile in ascending CTA order and applies the epilogue.  Mode 3 has short K
@@ -141,25 +141,28 @@ struct RowsCfg {
     static constexpr bool Q4 = MODE == 4;
     static constexpr bool GATHER = MODE <= 1 || Q4;
     static constexpr bool DIRECT = MODE == 3;
-    static constexpr int NA = (MODE == 1 || Q4) ? 2 : 1;   // A operand tiles per stage
+    static constexpr int NA = MODE == 1 ? 2 : 1;            // A operand tiles per stage
     static constexpr int NACC = MODE == 1 ? 2 : 1;          // accumulators (gate and up)
     static constexpr int NB = DIRECT ? 2 * NT : NT;          // B operand rows
     static constexpr int X = NB * 128;                       // NB rows x 64 fp16
-    static constexpr int STAGE = NA * kTileA + X;
+    static constexpr int STAGE = Q4 ? kTileA : NA * kTileA + X;   // INT4: x is read from the raw ring
     // even ring of stages, filled two K-chunks at a time (256 contiguous bytes
     // of every row per visit); LAGP pairs of copies stay in flight.  INT4:
     // 4 stages, fed from a deeper ring of raw K-chunks (per row 32 bytes of
     // codes and 4 of scales at a 48-byte pitch, then the chunk of x)
-    static constexpr int S0 = Q4 ? 4 : (kRingBudget / STAGE > 12 ? 12 : kRingBudget / STAGE);
-    static constexpr int S = S0 & ~1;
+    static constexpr int S0 = kRingBudget / STAGE > 12 ? 12 : kRingBudget / STAGE;
+    static constexpr int S = Q4 ? 4 : S0 & ~1;
     static constexpr int LAGP = S / 2 >= 4 ? S / 2 - 2 : S / 2 - 1;
-    static constexpr int RAWB = 128 * 48 + X;
-    static constexpr int RS0 = Q4 ? (kRingBudget - S * STAGE) / RAWB : 0;
-    static constexpr int RS = RS0 > 12 ? 12 : RS0;
+    static constexpr int KQ = Q4 ? 4 : 1;                    // K-chunks per unit of the split
+    static constexpr int RAWQ = 128 * 144 + 4 * X;
+    static constexpr int RQ0 = Q4 ? (kRingBudget - S * STAGE) / RAWQ : 0;
+    static constexpr int RQ = RQ0 > 8 ? 8 : RQ0;
+    static constexpr int NGS = Q4 ? 8 : 1;                   // INT4: TMEM group accumulators (32 of K each)
     static constexpr int ACC = NACC * NB;                    // TMEM columns per accumulator buffer
     static constexpr int COLS = NACC * NT;                   // partial columns (modes 0-2, 4)
-    static constexpr int TMEM = tmem_cols_for(2 * ACC);
-    static constexpr size_t SMEM = (size_t)S * STAGE + (size_t)RS * RAWB + 1024;
+    static constexpr int TMEM = tmem_cols_for(Q4 ? NGS * NB : 2 * ACC);
+    static constexpr size_t SMEM = (size_t)S * STAGE + (size_t)RQ * RAWQ + 1024;
+    static_assert(!Q4 || RQ >= 2 + S / 4, "INT4 raw ring too shallow");
 };
 
 struct TcRowsArgs {
@@ -201,136 +204,233 @@ PI_DEV void cp_wait_n(int n) {
     }
 }
 
-// 8 INT4 codes (element e in bits 4e..4e+3, two's complement) times the scale
-// s, as fp16 hi = fp16(q s) and lo = fp16(q s - hi), elements in order.  The
-// codes become exact fp16 values through the 1024 + n bit pattern; fp16
-// multiply and fma round once, so hi + lo = q s up to the fp16 spacing of lo.
-PI_DEV void q8_hi_lo(uint32_t w, __half2 s2, uint4& hi, uint4& lo) {
+// 8 INT4 codes (element e in bits 4e..4e+3, two's complement) as 8 fp16
+// integers in element order.  The 1024 + n bit pattern makes n = q + 8 an
+// exact fp16 value; subtracting 1032 is exact.
+PI_DEV uint4 q8_f16(uint32_t w) {
     const uint32_t u = w ^ 0x88888888u;   // n + 8 in 0..15
     const __half2 k1032 = __float2half2_rn(1032.f);
-    uint32_t ph[4], pl[4];
+    uint32_t ph[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         uint32_t t = ((u >> (4 * k)) & 0x000F000Fu) | 0x64006400u;   // (1024 + n_k, 1024 + n_{k+4})
         const __half2 q = __hsub2(*reinterpret_cast<__half2*>(&t), k1032);
-        const __half2 h = __hmul2(q, s2);
-        const __half2 l = __hfma2(q, s2, __hneg2(h));
-        ph[k] = *reinterpret_cast<const uint32_t*>(&h);
-        pl[k] = *reinterpret_cast<const uint32_t*>(&l);
+        ph[k] = *reinterpret_cast<const uint32_t*>(&q);
     }
     // pairs (e_k, e_{k+4}) -> (e0 e1)(e2 e3)(e4 e5)(e6 e7)
-    hi = make_uint4(__byte_perm(ph[0], ph[1], 0x5410), __byte_perm(ph[2], ph[3], 0x5410),
-                    __byte_perm(ph[0], ph[1], 0x7632), __byte_perm(ph[2], ph[3], 0x7632));
-    lo = make_uint4(__byte_perm(pl[0], pl[1], 0x5410), __byte_perm(pl[2], pl[3], 0x5410),
-                    __byte_perm(pl[0], pl[1], 0x7632), __byte_perm(pl[2], pl[3], 0x7632));
+    return make_uint4(__byte_perm(ph[0], ph[1], 0x5410), __byte_perm(ph[2], ph[3], 0x5410),
+                      __byte_perm(ph[0], ph[1], 0x7632), __byte_perm(ph[2], ph[3], 0x7632));
 }
 
-// Loaders of the INT4 FC1 (mode 4): loader thread t owns row t of every tile.
-// It copies its row's K-chunk (32 bytes of codes, 4 of scales) and its share
-// of the x chunk into a raw ring RS-1 chunks ahead with cp.async, and for the
-// current chunk, once its own copies have landed and the stage is free,
-// writes the hi and lo fp16 rows into the stage's two A tiles (128-byte
-// swizzle) and its x share into the B tile, then arrives on `full`.  A thread
-// reads only what it copied itself, so the raw ring needs no barrier.
+// Loaders of the INT4 FC1 (mode 4).  The CTA's K range is split in quads of
+// four K-chunks.  A quad of a 128-row tile is copied by all 128 loaders with
+// cp.async into a raw ring entry, RQ-2 quads ahead: per row the 128 contiguous
+// bytes of codes (eight lanes per row, so a warp instruction reads four rows'
+// runs) at a 144-byte pitch, then the quad's x in the B-tile layout, which the
+// MMAs read in place.  For each chunk of the current quad, once the stage is
+// free, loader t writes row t's 64 codes as fp16 into the stage's A tile
+// (128-byte swizzle) and arrives on `full`.  A barrier per quad makes every
+// loader's copies visible; an entry is refilled only after the MMAs of its
+// previous quad have completed (the stage waits of the quad after it).
 template <typename C, typename SpanOf>
 PI_DEV void q4_loader(const TcRowsArgs& a, unsigned char* ring, const SpanOf& span, int npiece, int R,
-                      unsigned long long* full, unsigned long long* empty, const Ctl& ctl) {
+                      const int* srow, unsigned long long* full, unsigned long long* empty, const Ctl& ctl) {
+    static_assert(C::S % 4 == 0, "stages must be a multiple of a quad");
     const int t = threadIdx.x;
     unsigned char* raw = ring + (size_t)C::S * C::STAGE;
-    const size_t cpr = (size_t)a.K / 2, spr = (size_t)a.K / 32;   // code bytes, scales per row
-    int total = 0;
+    const size_t cpr = (size_t)a.K / 2;   // code bytes per row
+    int nquad = 0;
     for (int p = 0; p < npiece; ++p) {
         const Span sp = span(p);
-        total += sp.kc1 - sp.kc0;
+        nquad += (sp.kc1 - sp.kc0) / 4;
     }
-    // issue cursor (runs RS-1 chunks ahead) and its row id
+    // x rows of padded tokens stay zero in every entry (never copied)
+    for (int pp = t; pp < C::RQ * 4 * C::NB * 8; pp += kLoaders) {
+        const int e = pp / (4 * C::NB * 8), q = pp % (C::NB * 8), c = (pp / (C::NB * 8)) % 4;
+        const int gg = q >> 5, ll = q & 31;
+        const int tok = 8 * (gg >> 1) + (ll & 7), kx = 4 * (gg & 1) + (ll >> 3);
+        if (tok >= a.bop_rows)
+            *reinterpret_cast<uint4*>(raw + (size_t)e * C::RAWQ + 128 * 144 + c * C::X + kx * (C::NB * 16) +
+                                      (tok >> 3) * 128 + (tok & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    // issue cursor and the row ids it copies: rows (t >> 3) + 16 i of the tile
     int ip = 0;
     Span isp = span(0);
-    int iks = isp.kc0;
-    auto row_id = [&](int tile) {
-        const int rr = 128 * tile + t;
-        return rr < R ? a.idx[rr] : -1;
-    };
-    int irow = row_id(isp.tile);
-    auto issue = [&](int j) {
-        unsigned char* b = raw + (size_t)(j % C::RS) * C::RAWB;
-        if (irow >= 0) {
-            const uint8_t* src = a.q + (size_t)irow * cpr + (size_t)iks * 32;
-            cp16(b + t * 48, src);
-            cp16(b + t * 48 + 16, src + 16);
-            cp4(b + t * 48 + 32, a.qs + (size_t)irow * spr + (size_t)iks * 2);
-        }
-        const int k0 = iks * 64;
-        for (int pp = t; pp < C::NB * 8; pp += kLoaders) {
-            const int gg = pp >> 5, ll = pp & 31;
+    int iq = isp.kc0 / 4;
+    int crow[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) crow[i] = srow[(t >> 3) + 16 * i];
+    auto issue = [&](int qn) {
+        unsigned char* b = raw + (size_t)(qn % C::RQ) * C::RAWQ;
+        const size_t co = (size_t)iq * 128 + (t & 7) * 16;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (crow[i] >= 0) cp16(b + ((t >> 3) + 16 * i) * 144 + (t & 7) * 16, a.q + (size_t)crow[i] * cpr + co);
+        const int k0 = iq * 256;
+#pragma unroll
+        for (int pp = t; pp < 4 * C::NB * 8; pp += kLoaders) {
+            const int c = pp / (C::NB * 8), q = pp % (C::NB * 8);
+            const int gg = q >> 5, ll = q & 31;
             const int tok = 8 * (gg >> 1) + (ll & 7), kx = 4 * (gg & 1) + (ll >> 3);
             if (tok < a.bop_rows)
-                cp16(b + 128 * 48 + kx * (C::NB * 16) + (tok >> 3) * 128 + (tok & 7) * 16,
-                     a.bop + (size_t)tok * a.K + k0 + kx * 8);
+                cp16(b + 128 * 144 + c * C::X + kx * (C::NB * 16) + (tok >> 3) * 128 + (tok & 7) * 16,
+                     a.bop + (size_t)tok * a.K + k0 + c * 64 + kx * 8);
         }
         cp_commit();
-        if (++iks == isp.kc1 && ip + 1 < npiece) {
+        if (++iq == isp.kc1 / 4 && ip + 1 < npiece) {
             ++ip;
             isp = span(ip);
-            iks = isp.kc0;
-            irow = row_id(isp.tile);
+            iq = isp.kc0 / 4;
+            const int base = 128 * isp.tile;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int rr = base + (t >> 3) + 16 * i;
+                crow[i] = rr < R ? __ldg(a.idx + rr) : -1;
+            }
         }
     };
-    const int ahead = C::RS - 1;
+    const int ahead = C::RQ - 1 - C::S / 4;
     int issued = 0;
-    while (issued < total && issued < ahead) issue(issued++);
+    while (issued < nquad && issued < ahead) issue(issued++);
     // conversion cursor
     int cp = 0;
     Span csp = span(0);
-    int cks = csp.kc0;
-    for (int j = 0; j < total; ++j) {
-        if (issued < total) issue(issued++);
-        const int s = j % C::S;
-        bool good = true;
-        if (j >= C::S && !bar_wait(&empty[s], ((j / C::S) - 1) & 1, ctl)) good = false;
-        if (loaders_sync_any(!good)) break;   // stop together
-        cp_wait_n(issued - 1 - j);            // this thread's copies of chunk j have landed
-        const unsigned char* b = raw + (size_t)(j % C::RS) * C::RAWB;
-        unsigned char* st = ring + (size_t)s * C::STAGE;
+    int cq = csp.kc0 / 4;
+    int j = 0;
+    bool stop = false;
+    const unsigned rowoff = (t >> 3) * 1024 + (t & 7) * 128;
+    for (int qd = 0; qd < nquad && !stop; ++qd) {
+        cp_wait_n(issued - 1 - qd);   // this thread's copies of quad qd have landed
+        loaders_sync_any(false);      // and everyone's
+        const unsigned char* b = raw + (size_t)(qd % C::RQ) * C::RAWQ;
         const bool valid = 128 * csp.tile + t < R;
-        const unsigned rowoff = (t >> 3) * 1024 + (t & 7) * 128;
-        if (valid) {
-            const uint4 c0 = *reinterpret_cast<const uint4*>(b + t * 48);
-            const uint4 c1 = *reinterpret_cast<const uint4*>(b + t * 48 + 16);
-            const __half2 sc = *reinterpret_cast<const __half2*>(b + t * 48 + 32);
-            const __half2 s0 = __low2half2(sc), s1 = __high2half2(sc);
-            const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint4 hi, lo;
-                q8_hi_lo(cw[c], c < 4 ? s0 : s1, hi, lo);
-                const unsigned off = rowoff + ((c ^ (t & 7)) << 4);
-                *reinterpret_cast<uint4*>(st + off) = hi;
-                *reinterpret_cast<uint4*>(st + kTileA + off) = lo;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c, ++j) {
+            const int s = j % C::S;
+            bool good = true;
+            if (j >= C::S && !bar_wait(&empty[s], ((j / C::S) - 1) & 1, ctl)) good = false;
+            if (loaders_sync_any(!good)) {   // stop together
+                stop = true;
+                break;
             }
-        } else {
+            // the stage waits of this quad's first chunk cover the MMAs of
+            // quad qd-1 (S >= 4): its entry can take quad qd + ahead
+            if (c == 0 && issued < nquad) issue(issued++);
+            unsigned char* st = ring + (size_t)s * C::STAGE;
+            if (valid) {
+                const uint4 c0 = *reinterpret_cast<const uint4*>(b + t * 144 + c * 32);
+                const uint4 c1 = *reinterpret_cast<const uint4*>(b + t * 144 + c * 32 + 16);
+                const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                *reinterpret_cast<uint4*>(st + rowoff + (c << 4)) = make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4*>(st + kTileA + rowoff + (c << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                for (int e = 0; e < 8; ++e)
+                    *reinterpret_cast<uint4*>(st + rowoff + ((e ^ (t & 7)) << 4)) = q8_f16(cw[e]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    *reinterpret_cast<uint4*>(st + rowoff + ((e ^ (t & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
             }
+            fence_async_smem();
+            bar_arrive(&full[s]);
         }
-        for (int pp = t; pp < C::NB * 8; pp += kLoaders) {
-            const int gg = pp >> 5, ll = pp & 31;
-            const int tok = 8 * (gg >> 1) + (ll & 7), kx = 4 * (gg & 1) + (ll >> 3);
-            const unsigned xo = kx * (C::NB * 16) + (tok >> 3) * 128 + (tok & 7) * 16;
-            *reinterpret_cast<uint4*>(st + 2 * kTileA + xo) =
-                tok < a.bop_rows ? *reinterpret_cast<const uint4*>(b + 128 * 48 + xo) : make_uint4(0u, 0u, 0u, 0u);
-        }
-        fence_async_smem();
-        bar_arrive(&full[s]);
-        if (++cks == csp.kc1 && cp + 1 < npiece) {
+        if (++cq == csp.kc1 / 4 && cp + 1 < npiece) {
             ++cp;
             csp = span(cp);
-            cks = csp.kc0;
+            cq = csp.kc0 / 4;
         }
     }
     cp_wait_all();
+}
+
+// MMA issuer of the INT4 FC1: per K-chunk two groups of 32, each into the
+// next of NGS TMEM accumulators (K-steps 2h and 2h+1 of the stage's A tile
+// against the x chunk in the raw ring), committed to that accumulator's
+// `gfull`; the stage is released once all of the chunk's MMAs are done.
+template <typename C>
+PI_DEV bool q4_mma(const TcRowsArgs& a, unsigned char* ring, int total, unsigned tmem, unsigned long long* full,
+                   unsigned long long* empty, unsigned long long* gfull, unsigned long long* gempty, const Ctl& ctl,
+                   int& it) {
+    const unsigned idesc = idesc_f16(128, C::NB, false);
+    const unsigned rawa = su32(ring + (size_t)C::S * C::STAGE);
+    int gi = 0;
+    for (it = 0; it < total; ++it) {
+        const int s = it % C::S;
+        if (!bar_wait(&full[s], (it / C::S) & 1, ctl)) return false;
+        tc_after();
+        const unsigned sa = su32(ring + (size_t)s * C::STAGE);
+        const unsigned sx = rawa + (unsigned)((it >> 2) % C::RQ) * C::RAWQ + 128 * 144 + (unsigned)(it & 3) * C::X;
+        for (int h = 0; h < 2; ++h, ++gi) {
+            const int gs = gi % C::NGS;
+            if (gi >= C::NGS && !bar_wait(&gempty[gs], ((gi / C::NGS) - 1) & 1, ctl)) return false;
+            tc_after();
+            const unsigned dcol = tmem + (unsigned)(gs * C::NB);
+#pragma unroll
+            for (int kk = 2 * h; kk < 2 * h + 2; ++kk)
+                mma_f16(dcol, sdesc_sw128(sa + kk * 32), sdesc(sx + kk * 2 * C::NB * 16, C::NB * 16, 128), idesc,
+                        (unsigned)(kk & 1));
+            mma_commit(&gfull[gs]);
+        }
+        mma_commit(&empty[s]);
+    }
+    return true;
+}
+
+// Epilogue of the INT4 FC1: TMEM lane m = row m of the tile.  For each group
+// accumulator in order it reads the NT columns, frees the accumulator and adds
+// them times the row's group scale (read from global memory, a quad of eight
+// scales two quads ahead) into register sums; at the end of a piece the sums
+// are its partial tile.
+template <typename C, int NT, typename SpanOf>
+PI_DEV void q4_epilogue(const TcRowsArgs& a, const SpanOf& span, int npiece, int R, int g, unsigned tmem,
+                        unsigned long long* gfull, unsigned long long* gempty, const Ctl& ctl) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = warp - 4, m = 32 * e + lane;
+    const size_t spr = (size_t)a.K / 32;
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    const unsigned tl = tmem + ((unsigned)(32 * e) << 16);
+    int gi = 0;
+    for (int p = 0; p < npiece; ++p) {
+        const Span sp = span(p);
+        const int r = 128 * sp.tile + m;
+        const int rid = r < R ? __ldg(a.idx + r) : -1;
+        const uint4* sq = reinterpret_cast<const uint4*>(a.qs + (size_t)(rid < 0 ? 0 : rid) * spr) + sp.kc0 / 4;
+        const int nq = (sp.kc1 - sp.kc0) / 4;
+        float z[NT];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) z[t] = 0.f;
+        uint4 s_cur = rid >= 0 ? __ldg(sq) : zero;
+        uint4 s_next = rid >= 0 && nq > 1 ? __ldg(sq + 1) : zero;
+        for (int q = 0; q < nq; ++q) {
+            const uint4 sc = s_cur;
+            s_cur = s_next;
+            s_next = rid >= 0 && q + 2 < nq ? __ldg(sq + q + 2) : zero;
+            const uint32_t sw[4] = {sc.x, sc.y, sc.z, sc.w};
+#pragma unroll
+            for (int h = 0; h < 8; ++h, ++gi) {
+                const int gs = gi % C::NGS;
+                if (!__all_sync(FULL, bar_wait(&gfull[gs], (gi / C::NGS) & 1, ctl))) return;
+                tc_after();
+                float v[NT];
+#pragma unroll
+                for (int c = 0; c < NT; c += 16) tmem_ld16(tl + (unsigned)(gs * C::NB + c), v + c);
+                tmem_wait_ld();
+                tc_before();
+                __syncwarp();
+                if (lane == 0) bar_arrive(&gempty[gs]);
+                const uint32_t w = sw[h >> 1];
+                const float sg = __half2float(__ushort_as_half((unsigned short)((h & 1) ? (w >> 16) : (w & 0xFFFFu))));
+#pragma unroll
+                for (int t = 0; t < NT; ++t) z[t] = fmaf(sg, v[t], z[t]);
+            }
+        }
+        if (p < a.slots) {
+            float* dst = a.part + ((size_t)g * a.slots + p) * C::COLS * 128 + m;
+#pragma unroll
+            for (int t = 0; t < NT; ++t)
+                if (t < a.B) dst[(size_t)t * 128] = z[t];
+        } else if (lane == 0) {
+            atomicExch(a.status, (int)PI_ERR_WORKSPACE);
+        }
+    }
 }
 
 template <int MODE, int NT>
@@ -338,6 +438,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
     using C = RowsCfg<MODE, NT>;
     extern __shared__ unsigned char dsm[];
     __shared__ __align__(8) unsigned long long full[C::S], empty[C::S], accf[2], acce[2], drain;
+    __shared__ __align__(8) unsigned long long gfull[C::NGS], gempty[C::NGS];   // INT4 group accumulators
     __shared__ unsigned tmem_slot;
     __shared__ int abort_flag;
     __shared__ int srow[128];  // A row ids of the current tile (-1 past the end)
@@ -346,13 +447,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
     const int G = gridDim.x, g = blockIdx.x;
     const int ntile = (R + 127) / 128;
     const int nk = (a.K + 63) / 64;
-    const long long U = (long long)ntile * nk;
+    const int nu = C::Q4 ? nk / C::KQ : nk;   // units per tile (INT4: quads; K % 256 == 0)
+    const long long U = (long long)ntile * nu;
     const long long u0 = U * g / G, u1 = U * (g + 1) / G;
     int npiece;
     if (C::DIRECT)
         npiece = ntile > g ? (ntile - 1 - g) / G + 1 : 0;
     else
-        npiece = u0 < u1 ? (int)((u1 - 1) / nk - u0 / nk) + 1 : 0;
+        npiece = u0 < u1 ? (int)((u1 - 1) / nu - u0 / nu) + 1 : 0;
     if (npiece == 0) return;
     auto span = [&](int p) {
         Span s;
@@ -361,10 +463,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
             s.kc0 = 0;
             s.kc1 = nk;
         } else {
-            s.tile = (int)(u0 / nk) + p;
-            const long long lo = (long long)s.tile * nk;
-            s.kc0 = (int)((u0 > lo ? u0 : lo) - lo);
-            s.kc1 = (int)((u1 < lo + nk ? u1 : lo + nk) - lo);
+            s.tile = (int)(u0 / nu) + p;
+            const long long lo = (long long)s.tile * nu;
+            s.kc0 = C::KQ * (int)((u0 > lo ? u0 : lo) - lo);
+            s.kc1 = C::KQ * (int)((u1 < lo + nu ? u1 : lo + nu) - lo);
         }
         return s;
     };
@@ -383,6 +485,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
                 bar_init(&accf[b], 1);
                 bar_init(&acce[b], 128);
             }
+            if (C::Q4)
+                for (int q = 0; q < C::NGS; ++q) {
+                    bar_init(&gfull[q], 1);
+                    bar_init(&gempty[q], 4);
+                }
             bar_init(&drain, 1);
             abort_flag = 0;
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -401,7 +508,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
     const Ctl ctl{a.status, a.timeout_ns, &abort_flag};
 
     if (warp < 4 && C::Q4) {
-        if constexpr (C::Q4) q4_loader<C>(a, ring, span, npiece, R, full, empty, ctl);
+        if constexpr (C::Q4) q4_loader<C>(a, ring, span, npiece, R, srow, full, empty, ctl);
     } else if (warp < 4) {
         // ---- loaders.  A tiles use the 128-byte-swizzled layout, so the 8
         // lanes of one shared-memory phase copy the 8 chunks of one row's 128
@@ -534,6 +641,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
             }
         }
         cp_wait_all();
+    } else if (warp < 8 && C::Q4) {
+        if constexpr (C::Q4) q4_epilogue<C, NT>(a, span, npiece, R, g, tmem, gfull, gempty, ctl);
     } else if (warp < 8) {
         // ---- epilogue: TMEM lane m = row m of the tile
         const int e = warp - 4, m = 32 * e + lane;
@@ -588,7 +697,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
         const unsigned idesc = idesc_f16(128, C::NB, false);
         int it = 0;
         bool ok = true;
-        for (int p = 0; p < npiece && ok; ++p) {
+        if constexpr (C::Q4) {
+            int total = 0;
+            for (int p = 0; p < npiece; ++p) {
+                const Span sp = span(p);
+                total += sp.kc1 - sp.kc0;
+            }
+            ok = q4_mma<C>(a, ring, total, tmem, full, empty, gfull, gempty, ctl, it);
+        }
+        for (int p = 0; p < npiece && ok && !C::Q4; ++p) {
             const Span sp = span(p);
             const int b = p & 1;
             if (p >= 2 && !bar_wait(&acce[b], ((p >> 1) - 1) & 1, ctl)) {
@@ -612,7 +729,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
                     const unsigned acc = (ks > sp.kc0 || kk > 0) ? 1u : 0u;
                     mma_f16(dcol, sdesc_sw128(sa + kk * 32), bd, idesc, acc);
                     if (MODE == 1) mma_f16(dcol + C::NB, sdesc_sw128(sa + kTileA + kk * 32), bd, idesc, acc);
-                    if (MODE == 4) mma_f16(dcol, sdesc_sw128(sa + kTileA + kk * 32), bd, idesc, 1u);   // + lo
                 }
                 mma_commit(&empty[s]);
             }
@@ -1172,7 +1288,7 @@ cudaError_t launch_fc1_tc4(const Plan& p, const __half* x, const LayerPtrs& w, c
     a.timeout_ns = kTcTimeoutNs;
     cudaError_t e = launch_rows_nt<4>(a, nt, G, s);
     if (e != cudaSuccess) return e;
-    return launch_fc1_finish(p, nt, G, a.slots, ceil_div(p.d, 64), part, count, idx, w.b1, mask, h, live, s);
+    return launch_fc1_finish(p, nt, G, a.slots, p.d / 256, part, count, idx, w.b1, mask, h, live, s);
 }
 
 cudaError_t launch_fc1_finish(const Plan& p, int nt, int G, int slots, int nk, const float* part,
