@@ -89,6 +89,15 @@ PI_DEV void mma_f16(unsigned tmem_d, uint64_t a, uint64_t b, unsigned idesc, uns
         "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// Same with the A operand in tensor memory (row m of A in lane m, two fp16
+// per 32-bit column along K)
+PI_DEV void mma_f16_ta(unsigned tmem_d, unsigned tmem_a, uint64_t b, unsigned idesc, unsigned accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 PI_DEV void mma_commit(unsigned long long* b) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(b))
                  : "memory");
@@ -105,6 +114,28 @@ PI_DEV void tmem_ld16(unsigned taddr, float* v) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 PI_DEV void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// 32 consecutive 32-bit columns of this thread's TMEM lane
+PI_DEV void tmem_st32(unsigned taddr, const uint32_t* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+        "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+PI_DEV void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// One arrival per loader warp on a stage's `full` barrier (which counts
+// warps): __syncwarp orders every lane's shared-memory writes, each already
+// fenced for the async proxy by its own thread, before lane 0's release.
+// 128 arrivals on one barrier word would serialise.
+constexpr int kLoaderWarps = 4;
+PI_DEV void warp_arrive(unsigned long long* b) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) bar_arrive(b);
+}
 
 PI_DEV void tmem_alloc(unsigned* slot, unsigned cols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(slot)), "r"(cols)
@@ -115,7 +146,7 @@ PI_DEV void tmem_free(unsigned base, unsigned cols) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(cols) : "memory");
 }
 
-constexpr int tmem_cols_for(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : 256; }
+constexpr int tmem_cols_for(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512; }
 
 // ------------------------------------------------- row-tile GEMMs (FC1, predictor)
 //
@@ -145,24 +176,26 @@ struct RowsCfg {
     static constexpr int NACC = MODE == 1 ? 2 : 1;          // accumulators (gate and up)
     static constexpr int NB = DIRECT ? 2 * NT : NT;          // B operand rows
     static constexpr int X = NB * 128;                       // NB rows x 64 fp16
-    static constexpr int STAGE = Q4 ? kTileA : NA * kTileA + X;   // INT4: x is read from the raw ring
+    static constexpr int STAGE = Q4 ? 0 : NA * kTileA + X;   // INT4: A in TMEM, x read from the raw ring
     // even ring of stages, filled two K-chunks at a time (256 contiguous bytes
     // of every row per visit); LAGP pairs of copies stay in flight.  INT4:
     // 4 stages, fed from a deeper ring of raw K-chunks (per row 32 bytes of
     // codes and 4 of scales at a 48-byte pitch, then the chunk of x)
-    static constexpr int S0 = kRingBudget / STAGE > 12 ? 12 : kRingBudget / STAGE;
-    static constexpr int S = Q4 ? 4 : S0 & ~1;
+    static constexpr int S0 = Q4 ? 0 : kRingBudget / STAGE > 12 ? 12 : kRingBudget / STAGE;
+    static constexpr int S = Q4 ? 8 : S0 & ~1;
     static constexpr int LAGP = S / 2 >= 4 ? S / 2 - 2 : S / 2 - 1;
     static constexpr int KQ = Q4 ? 4 : 1;                    // K-chunks per unit of the split
     static constexpr int RAWQ = 128 * 144 + 4 * X;
     static constexpr int RQ0 = Q4 ? (kRingBudget - S * STAGE) / RAWQ : 0;
     static constexpr int RQ = RQ0 > 8 ? 8 : RQ0;
-    static constexpr int NGS = Q4 ? 8 : 1;                   // INT4: TMEM group accumulators (32 of K each)
+    static constexpr int CS = Q4 ? 4 : 1;                    // INT4: TMEM accumulator slots, 2 groups of 32 each
+    static constexpr int ACOL = 2 * CS * NB;                 // INT4: first TMEM column of the S A stages (32 each)
     static constexpr int ACC = NACC * NB;                    // TMEM columns per accumulator buffer
     static constexpr int COLS = NACC * NT;                   // partial columns (modes 0-2, 4)
-    static constexpr int TMEM = tmem_cols_for(Q4 ? NGS * NB : 2 * ACC);
+    static constexpr int TMEM = tmem_cols_for(Q4 ? ACOL + 32 * S : 2 * ACC);
     static constexpr size_t SMEM = (size_t)S * STAGE + (size_t)RQ * RAWQ + 1024;
     static_assert(!Q4 || RQ >= 2 + S / 4, "INT4 raw ring too shallow");
+    static_assert(!Q4 || S >= CS, "INT4: a stage barrier must not run a phase ahead of the epilogue");
 };
 
 struct TcRowsArgs {
@@ -228,13 +261,15 @@ PI_DEV uint4 q8_f16(uint32_t w) {
 // bytes of codes (eight lanes per row, so a warp instruction reads four rows'
 // runs) at a 144-byte pitch, then the quad's x in the B-tile layout, which the
 // MMAs read in place.  For each chunk of the current quad, once the stage is
-// free, loader t writes row t's 64 codes as fp16 into the stage's A tile
-// (128-byte swizzle) and arrives on `full`.  A barrier per quad makes every
+// free, loader t writes row t's 64 codes as fp16 into TMEM lane t of the
+// stage's A columns (tcgen05.st, so shared memory carries only the raw copies
+// and x) and arrives on `full`.  A barrier per quad makes every
 // loader's copies visible; an entry is refilled only after the MMAs of its
 // previous quad have completed (the stage waits of the quad after it).
 template <typename C, typename SpanOf>
 PI_DEV void q4_loader(const TcRowsArgs& a, unsigned char* ring, const SpanOf& span, int npiece, int R,
-                      const int* srow, unsigned long long* full, unsigned long long* empty, const Ctl& ctl) {
+                      const int* srow, unsigned tmem, unsigned long long* full, unsigned long long* empty,
+                      const Ctl& ctl) {
     static_assert(C::S % 4 == 0, "stages must be a multiple of a quad");
     const int t = threadIdx.x;
     unsigned char* raw = ring + (size_t)C::S * C::STAGE;
@@ -298,39 +333,59 @@ PI_DEV void q4_loader(const TcRowsArgs& a, unsigned char* ring, const SpanOf& sp
     int cq = csp.kc0 / 4;
     int j = 0;
     bool stop = false;
-    const unsigned rowoff = (t >> 3) * 1024 + (t & 7) * 128;
-    for (int qd = 0; qd < nquad && !stop; ++qd) {
-        cp_wait_n(issued - 1 - qd);   // this thread's copies of quad qd have landed
-        loaders_sync_any(false);      // and everyone's
+    const int lane = t & 31;
+    const unsigned tlane = tmem + ((unsigned)(t & ~31) << 16) + (unsigned)C::ACOL;
+    for (int qd = 0; qd < nquad; ++qd) {
+        cp_wait_n(issued - 1 - qd);             // this thread's copies of quad qd have landed
+        if (loaders_sync_any(stop)) break;      // and everyone's; a warp that gave up stops all
         const unsigned char* b = raw + (size_t)(qd % C::RQ) * C::RAWQ;
         const bool valid = 128 * csp.tile + t < R;
+        // the TMEM store of a chunk completes while the next one is converted
+        int pending = -1;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c, ++j) {
             const int s = j % C::S;
-            bool good = true;
-            if (j >= C::S && !bar_wait(&empty[s], ((j / C::S) - 1) & 1, ctl)) good = false;
-            if (loaders_sync_any(!good)) {   // stop together
-                stop = true;
-                break;
+            if (j >= C::S) {   // lane 0 waits for the stage's previous MMAs for the warp
+                bool good = true;
+                if (lane == 0) good = bar_wait(&empty[s], ((j / C::S) - 1) & 1, ctl);
+                if (!__shfl_sync(FULL, good ? 1 : 0, 0)) {
+                    stop = true;
+                    break;
+                }
             }
             // the stage waits of this quad's first chunk cover the MMAs of
-            // quad qd-1 (S >= 4): its entry can take quad qd + ahead
+            // quad qd-1-S/4: its entry can take quad qd + ahead
             if (c == 0 && issued < nquad) issue(issued++);
-            unsigned char* st = ring + (size_t)s * C::STAGE;
+            uint32_t av[32];
             if (valid) {
                 const uint4 c0 = *reinterpret_cast<const uint4*>(b + t * 144 + c * 32);
                 const uint4 c1 = *reinterpret_cast<const uint4*>(b + t * 144 + c * 32 + 16);
                 const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    *reinterpret_cast<uint4*>(st + rowoff + ((e ^ (t & 7)) << 4)) = q8_f16(cw[e]);
+                for (int e = 0; e < 8; ++e) {
+                    const uint4 h = q8_f16(cw[e]);
+                    av[4 * e] = h.x;
+                    av[4 * e + 1] = h.y;
+                    av[4 * e + 2] = h.z;
+                    av[4 * e + 3] = h.w;
+                }
             } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    *reinterpret_cast<uint4*>(st + rowoff + ((e ^ (t & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                for (int e = 0; e < 32; ++e) av[e] = 0u;
             }
-            fence_async_smem();
-            bar_arrive(&full[s]);
+            if (pending >= 0) {
+                tmem_wait_st();
+                tc_before();
+                warp_arrive(&full[pending]);
+            }
+            tc_after();   // after the stage's previous MMAs (waited for above)
+            tmem_st32(tlane + (unsigned)(32 * s), av);
+            pending = s;
+        }
+        if (pending >= 0) {
+            tmem_wait_st();
+            tc_before();
+            warp_arrive(&full[pending]);
         }
         if (++cq == csp.kc1 / 4 && cp + 1 < npiece) {
             ++cp;
@@ -341,53 +396,53 @@ PI_DEV void q4_loader(const TcRowsArgs& a, unsigned char* ring, const SpanOf& sp
     cp_wait_all();
 }
 
-// MMA issuer of the INT4 FC1: per K-chunk two groups of 32, each into the
-// next of NGS TMEM accumulators (K-steps 2h and 2h+1 of the stage's A tile
-// against the x chunk in the raw ring), committed to that accumulator's
-// `gfull`; the stage is released once all of the chunk's MMAs are done.
+// MMA issuer of the INT4 FC1.  Chunk j owns accumulator slot j % CS: two
+// TMEM accumulators of NB columns, one per group of 32 along K (K-steps 0-1
+// and 2-3 of the stage's A columns in TMEM against the x chunk in the raw
+// ring).  One
+// commit per chunk, on `empty[j % S]`, frees the stage for the loaders and
+// tells the epilogue that the chunk's two accumulators are final; the slot is
+// reused once the epilogue has read it (`cempty`).  The issuing thread runs a
+// chain of dependent instructions, so the loop keeps it short: one wait per
+// barrier per chunk and descriptors advanced by adding the byte offset >> 4.
 template <typename C>
-PI_DEV bool q4_mma(const TcRowsArgs& a, unsigned char* ring, int total, unsigned tmem, unsigned long long* full,
-                   unsigned long long* empty, unsigned long long* gfull, unsigned long long* gempty, const Ctl& ctl,
-                   int& it) {
+PI_DEV bool q4_mma(unsigned char* ring, int total, unsigned tmem, unsigned long long* full,
+                   unsigned long long* empty, unsigned long long* cempty, const Ctl& ctl, int& it) {
     const unsigned idesc = idesc_f16(128, C::NB, false);
-    const unsigned rawa = su32(ring + (size_t)C::S * C::STAGE);
-    int gi = 0;
+    const uint64_t bd0 = sdesc(su32(ring + (size_t)C::S * C::STAGE) + 128 * 144, C::NB * 16, 128);
+    int qslot = 0;
     for (it = 0; it < total; ++it) {
-        const int s = it % C::S;
+        const int s = it % C::S, cs = it % C::CS;
         if (!bar_wait(&full[s], (it / C::S) & 1, ctl)) return false;
+        if (it >= C::CS && !bar_wait(&cempty[cs], ((it / C::CS) - 1) & 1, ctl)) return false;
         tc_after();
-        const unsigned sa = su32(ring + (size_t)s * C::STAGE);
-        const unsigned sx = rawa + (unsigned)((it >> 2) % C::RQ) * C::RAWQ + 128 * 144 + (unsigned)(it & 3) * C::X;
-        for (int h = 0; h < 2; ++h, ++gi) {
-            const int gs = gi % C::NGS;
-            if (gi >= C::NGS && !bar_wait(&gempty[gs], ((gi / C::NGS) - 1) & 1, ctl)) return false;
-            tc_after();
-            const unsigned dcol = tmem + (unsigned)(gs * C::NB);
+        const unsigned ta = tmem + (unsigned)(C::ACOL + 32 * s);
+        const uint64_t bd = bd0 + (uint64_t)((qslot * C::RAWQ + (it & 3) * C::X) >> 4);
+        const unsigned dcol = tmem + (unsigned)(2 * cs * C::NB);
 #pragma unroll
-            for (int kk = 2 * h; kk < 2 * h + 2; ++kk)
-                mma_f16(dcol, sdesc_sw128(sa + kk * 32), sdesc(sx + kk * 2 * C::NB * 16, C::NB * 16, 128), idesc,
-                        (unsigned)(kk & 1));
-            mma_commit(&gfull[gs]);
-        }
+        for (int kk = 0; kk < 4; ++kk)
+            mma_f16_ta(dcol + (unsigned)((kk >> 1) * C::NB), ta + (unsigned)(8 * kk),
+                       bd + (uint64_t)((kk * 2 * C::NB * 16) >> 4), idesc, (unsigned)(kk & 1));
         mma_commit(&empty[s]);
+        if ((it & 3) == 3) qslot = qslot + 1 == C::RQ ? 0 : qslot + 1;
     }
     return true;
 }
 
-// Epilogue of the INT4 FC1: TMEM lane m = row m of the tile.  For each group
-// accumulator in order it reads the NT columns, frees the accumulator and adds
-// them times the row's group scale (read from global memory, a quad of eight
-// scales two quads ahead) into register sums; at the end of a piece the sums
-// are its partial tile.
+// Epilogue of the INT4 FC1: TMEM lane m = row m of the tile.  For each chunk
+// in order it waits for the chunk's commit, reads its two group accumulators,
+// frees the slot and adds them times the row's group scales (read from global
+// memory, a quad of eight scales two quads ahead) into register sums; at the
+// end of a piece the sums are its partial tile.
 template <typename C, int NT, typename SpanOf>
 PI_DEV void q4_epilogue(const TcRowsArgs& a, const SpanOf& span, int npiece, int R, int g, unsigned tmem,
-                        unsigned long long* gfull, unsigned long long* gempty, const Ctl& ctl) {
+                        unsigned long long* empty, unsigned long long* cempty, const Ctl& ctl) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = warp - 4, m = 32 * e + lane;
     const size_t spr = (size_t)a.K / 32;
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
     const unsigned tl = tmem + ((unsigned)(32 * e) << 16);
-    int gi = 0;
+    int j = 0;
     for (int p = 0; p < npiece; ++p) {
         const Span sp = span(p);
         const int r = 128 * sp.tile + m;
@@ -405,21 +460,24 @@ PI_DEV void q4_epilogue(const TcRowsArgs& a, const SpanOf& span, int npiece, int
             s_next = rid >= 0 && q + 2 < nq ? __ldg(sq + q + 2) : zero;
             const uint32_t sw[4] = {sc.x, sc.y, sc.z, sc.w};
 #pragma unroll
-            for (int h = 0; h < 8; ++h, ++gi) {
-                const int gs = gi % C::NGS;
-                if (!__all_sync(FULL, bar_wait(&gfull[gs], (gi / C::NGS) & 1, ctl))) return;
+            for (int c = 0; c < 4; ++c, ++j) {
+                const int s = j % C::S, cs = j % C::CS;
+                if (!__all_sync(FULL, bar_wait(&empty[s], (j / C::S) & 1, ctl))) return;
                 tc_after();
-                float v[NT];
+                float v0[NT], v1[NT];
 #pragma unroll
-                for (int c = 0; c < NT; c += 16) tmem_ld16(tl + (unsigned)(gs * C::NB + c), v + c);
+                for (int k = 0; k < NT; k += 16) {
+                    tmem_ld16(tl + (unsigned)(2 * cs * C::NB + k), v0 + k);
+                    tmem_ld16(tl + (unsigned)((2 * cs + 1) * C::NB + k), v1 + k);
+                }
                 tmem_wait_ld();
                 tc_before();
                 __syncwarp();
-                if (lane == 0) bar_arrive(&gempty[gs]);
-                const uint32_t w = sw[h >> 1];
-                const float sg = __half2float(__ushort_as_half((unsigned short)((h & 1) ? (w >> 16) : (w & 0xFFFFu))));
+                if (lane == 0) bar_arrive(&cempty[cs]);
+                const float s0 = __half2float(__ushort_as_half((unsigned short)(sw[c] & 0xFFFFu)));
+                const float s1 = __half2float(__ushort_as_half((unsigned short)(sw[c] >> 16)));
 #pragma unroll
-                for (int t = 0; t < NT; ++t) z[t] = fmaf(sg, v[t], z[t]);
+                for (int t = 0; t < NT; ++t) z[t] = fmaf(s1, v1[t], fmaf(s0, v0[t], z[t]));
             }
         }
         if (p < a.slots) {
@@ -438,7 +496,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
     using C = RowsCfg<MODE, NT>;
     extern __shared__ unsigned char dsm[];
     __shared__ __align__(8) unsigned long long full[C::S], empty[C::S], accf[2], acce[2], drain;
-    __shared__ __align__(8) unsigned long long gfull[C::NGS], gempty[C::NGS];   // INT4 group accumulators
+    __shared__ __align__(8) unsigned long long cempty[C::CS];   // INT4 accumulator slots read
     __shared__ unsigned tmem_slot;
     __shared__ int abort_flag;
     __shared__ int srow[128];  // A row ids of the current tile (-1 past the end)
@@ -478,7 +536,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
     if (warp == 8) {
         if (lane == 0) {
             for (int s = 0; s < C::S; ++s) {
-                bar_init(&full[s], kLoaders);
+                bar_init(&full[s], kLoaderWarps);
                 bar_init(&empty[s], 1);
             }
             for (int b = 0; b < 2; ++b) {
@@ -486,10 +544,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
                 bar_init(&acce[b], 128);
             }
             if (C::Q4)
-                for (int q = 0; q < C::NGS; ++q) {
-                    bar_init(&gfull[q], 1);
-                    bar_init(&gempty[q], 4);
-                }
+                for (int q = 0; q < C::CS; ++q) bar_init(&cempty[q], 4);
             bar_init(&drain, 1);
             abort_flag = 0;
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -508,7 +563,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
     const Ctl ctl{a.status, a.timeout_ns, &abort_flag};
 
     if (warp < 4 && C::Q4) {
-        if constexpr (C::Q4) q4_loader<C>(a, ring, span, npiece, R, srow, full, empty, ctl);
+        if constexpr (C::Q4) q4_loader<C>(a, ring, span, npiece, R, srow, tmem, full, empty, ctl);
     } else if (warp < 4) {
         // ---- loaders.  A tiles use the 128-byte-swizzled layout, so the 8
         // lanes of one shared-memory phase copy the 8 chunks of one row's 128
@@ -618,8 +673,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
             if (pd >= 0) {
                 cp_wait<C::LAGP>();
                 fence_async_smem();
-                bar_arrive(&full[(2 * pd) % C::S]);
-                if (2 * pd + 1 < total) bar_arrive(&full[(2 * pd + 1) % C::S]);
+                warp_arrive(&full[(2 * pd) % C::S]);
+                if (2 * pd + 1 < total) warp_arrive(&full[(2 * pd + 1) % C::S]);
             }
         }
         if (ok) {
@@ -636,13 +691,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
                 else
                     cp_wait<0>();
                 fence_async_smem();
-                bar_arrive(&full[(2 * pd) % C::S]);
-                if (2 * pd + 1 < total) bar_arrive(&full[(2 * pd + 1) % C::S]);
+                warp_arrive(&full[(2 * pd) % C::S]);
+                if (2 * pd + 1 < total) warp_arrive(&full[(2 * pd + 1) % C::S]);
             }
         }
         cp_wait_all();
     } else if (warp < 8 && C::Q4) {
-        if constexpr (C::Q4) q4_epilogue<C, NT>(a, span, npiece, R, g, tmem, gfull, gempty, ctl);
+        if constexpr (C::Q4) q4_epilogue<C, NT>(a, span, npiece, R, g, tmem, empty, cempty, ctl);
     } else if (warp < 8) {
         // ---- epilogue: TMEM lane m = row m of the tile
         const int e = warp - 4, m = 32 * e + lane;
@@ -703,7 +758,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
                 const Span sp = span(p);
                 total += sp.kc1 - sp.kc0;
             }
-            ok = q4_mma<C>(a, ring, total, tmem, full, empty, gfull, gempty, ctl, it);
+            ok = q4_mma<C>(ring, total, tmem, full, empty, cempty, ctl, it);
         }
         for (int p = 0; p < npiece && ok && !C::Q4; ++p) {
             const Span sp = span(p);
@@ -879,7 +934,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fc2_tc(TcFc2Args a) {
 
     if (tid == 0) {
         for (int s = 0; s < C::S; ++s) {
-            bar_init(&full[s], kLoaders);
+            bar_init(&full[s], kLoaderWarps);
             bar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -938,7 +993,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fc2_tc(TcFc2Args a) {
             const Piece pc = ptab[cv_piece];
             convert(cv, pc, cv_st);
             fence_async_smem();
-            bar_arrive(&full[cv % C::S]);
+            warp_arrive(&full[cv % C::S]);
             ++cv;
             if (64 * (++cv_st) >= pc.j1 - pc.j0) {
                 ++cv_piece;
