@@ -26,6 +26,14 @@ PI_DEV void bar_init(unsigned long long* b, unsigned count) {
 PI_DEV void bar_arrive(unsigned long long* b) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
 }
+// One arrival per warp on a barrier that counts warps: __syncwarp orders
+// every lane's prior shared-memory writes (cp.async results its own wait has
+// completed, or stores it fenced for the async proxy) before lane 0's
+// release.  A hundred arrivals on one barrier word would serialise.
+PI_DEV void warp_arrive(unsigned long long* b) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) bar_arrive(b);
+}
 PI_DEV bool bar_try(unsigned long long* b, unsigned parity) {
     unsigned ok;
     asm volatile(

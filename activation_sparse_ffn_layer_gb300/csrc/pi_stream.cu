@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(kSThreads, 1) k_rows_st(SArgs a) {
     if (warp == 4) {
         if (lane == 0) {
             for (int s = 0; s < C::S; ++s) {
-                bar_init(&full[s], kSLoaders);
+                bar_init(&full[s], kSLoaders / 32);
                 bar_init(&empty[s], kSCompute);
             }
             abort_flag = 0;
@@ -229,8 +229,8 @@ __global__ void __launch_bounds__(kSThreads, 1) k_rows_st(SArgs a) {
             const int pd = it / 2 - C::LAGP;
             if (pd >= 0) {
                 cp_wait<C::LAGP>();
-                bar_arrive(&full[(2 * pd) % C::S]);
-                if (2 * pd + 1 < total) bar_arrive(&full[(2 * pd + 1) % C::S]);
+                warp_arrive(&full[(2 * pd) % C::S]);
+                if (2 * pd + 1 < total) warp_arrive(&full[(2 * pd + 1) % C::S]);
             }
         }
         if (ok) {
@@ -245,8 +245,8 @@ __global__ void __launch_bounds__(kSThreads, 1) k_rows_st(SArgs a) {
                     cp_wait<1>();
                 else
                     cp_wait<0>();
-                bar_arrive(&full[(2 * pd) % C::S]);
-                if (2 * pd + 1 < total) bar_arrive(&full[(2 * pd + 1) % C::S]);
+                warp_arrive(&full[(2 * pd) % C::S]);
+                if (2 * pd + 1 < total) warp_arrive(&full[(2 * pd + 1) % C::S]);
             }
         }
         cp_wait_all();
@@ -440,7 +440,7 @@ __global__ void __launch_bounds__(kSThreads, 1) k_fc2_st(SArgs2 a) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         for (int s = 0; s < C::S; ++s) {
-            bar_init(&full[s], kSLoaders);
+            bar_init(&full[s], kSLoaders / 32);
             bar_init(&empty[s], kSCompute);
         }
         abort_flag = 0;
@@ -527,12 +527,12 @@ __global__ void __launch_bounds__(kSThreads, 1) k_fc2_st(SArgs2 a) {
                     ok = false;
                     break;
                 }
-                if (it >= C::LAG) bar_arrive(&full[(it - C::LAG) % C::S]);
+                if (it >= C::LAG) warp_arrive(&full[(it - C::LAG) % C::S]);
             }
         }
         cp_wait_all();
         if (!loaders_sync_any(!ok || *(volatile int*)&abort_flag)) {
-            for (int q = it - C::LAG < 0 ? 0 : it - C::LAG; q < it; ++q) bar_arrive(&full[q % C::S]);
+            for (int q = it - C::LAG < 0 ? 0 : it - C::LAG; q < it; ++q) warp_arrive(&full[q % C::S]);
         }
     } else {
         // ---- compute warps: lane (mc = 2cw + (lane >> 4), rg = lane & 15)

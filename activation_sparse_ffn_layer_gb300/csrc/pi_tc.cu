@@ -127,15 +127,7 @@ PI_DEV void tmem_st32(unsigned taddr, const uint32_t* v) {
 }
 PI_DEV void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// One arrival per loader warp on a stage's `full` barrier (which counts
-// warps): __syncwarp orders every lane's shared-memory writes, each already
-// fenced for the async proxy by its own thread, before lane 0's release.
-// 128 arrivals on one barrier word would serialise.
-constexpr int kLoaderWarps = 4;
-PI_DEV void warp_arrive(unsigned long long* b) {
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) bar_arrive(b);
-}
+constexpr int kLoaderWarps = kLoaders / 32;   // arrivals on a stage's `full` barrier
 
 PI_DEV void tmem_alloc(unsigned* slot, unsigned cols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(slot)), "r"(cols)
@@ -340,14 +332,15 @@ PI_DEV void q4_loader(const TcRowsArgs& a, unsigned char* ring, const SpanOf& sp
         if (loaders_sync_any(stop)) break;      // and everyone's; a warp that gave up stops all
         const unsigned char* b = raw + (size_t)(qd % C::RQ) * C::RAWQ;
         const bool valid = 128 * csp.tile + t < R;
-        // the TMEM store of a chunk completes while the next one is converted
-        int pending = -1;
+        // two chunks per step: 16 independent conversions keep the warp busy
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c, ++j) {
-            const int s = j % C::S;
-            if (j >= C::S) {   // lane 0 waits for the stage's previous MMAs for the warp
+        for (int c = 0; c < 4; c += 2, j += 2) {
+            const int s0 = j % C::S, s1 = (j + 1) % C::S;
+            if (j >= C::S) {   // lane 0 waits for the stages' previous MMAs for the warp
                 bool good = true;
-                if (lane == 0) good = bar_wait(&empty[s], ((j / C::S) - 1) & 1, ctl);
+                if (lane == 0)
+                    good = bar_wait(&empty[s0], ((j / C::S) - 1) & 1, ctl) &&
+                           bar_wait(&empty[s1], (((j + 1) / C::S) - 1) & 1, ctl);
                 if (!__shfl_sync(FULL, good ? 1 : 0, 0)) {
                     stop = true;
                     break;
@@ -356,36 +349,31 @@ PI_DEV void q4_loader(const TcRowsArgs& a, unsigned char* ring, const SpanOf& sp
             // the stage waits of this quad's first chunk cover the MMAs of
             // quad qd-1-S/4: its entry can take quad qd + ahead
             if (c == 0 && issued < nquad) issue(issued++);
-            uint32_t av[32];
+            uint32_t av[2][32];
             if (valid) {
-                const uint4 c0 = *reinterpret_cast<const uint4*>(b + t * 144 + c * 32);
-                const uint4 c1 = *reinterpret_cast<const uint4*>(b + t * 144 + c * 32 + 16);
-                const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                const uint4* src = reinterpret_cast<const uint4*>(b + t * 144 + c * 32);
+                const uint4 q0 = src[0], q1 = src[1], q2 = src[2], q3 = src[3];
+                const uint32_t cw[16] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w,
+                                         q2.x, q2.y, q2.z, q2.w, q3.x, q3.y, q3.z, q3.w};
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
+                for (int e = 0; e < 16; ++e) {
                     const uint4 h = q8_f16(cw[e]);
-                    av[4 * e] = h.x;
-                    av[4 * e + 1] = h.y;
-                    av[4 * e + 2] = h.z;
-                    av[4 * e + 3] = h.w;
+                    av[e >> 3][4 * (e & 7)] = h.x;
+                    av[e >> 3][4 * (e & 7) + 1] = h.y;
+                    av[e >> 3][4 * (e & 7) + 2] = h.z;
+                    av[e >> 3][4 * (e & 7) + 3] = h.w;
                 }
             } else {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) av[e] = 0u;
+                for (int e = 0; e < 32; ++e) av[0][e] = av[1][e] = 0u;
             }
-            if (pending >= 0) {
-                tmem_wait_st();
-                tc_before();
-                warp_arrive(&full[pending]);
-            }
-            tc_after();   // after the stage's previous MMAs (waited for above)
-            tmem_st32(tlane + (unsigned)(32 * s), av);
-            pending = s;
-        }
-        if (pending >= 0) {
+            tc_after();   // after the stages' previous MMAs (waited for above)
+            tmem_st32(tlane + (unsigned)(32 * s0), av[0]);
+            tmem_st32(tlane + (unsigned)(32 * s1), av[1]);
             tmem_wait_st();
             tc_before();
-            warp_arrive(&full[pending]);
+            warp_arrive(&full[s0]);
+            warp_arrive(&full[s1]);
         }
         if (++cq == csp.kc1 / 4 && cp + 1 < npiece) {
             ++cp;
