@@ -748,6 +748,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
             }
             ok = q4_mma<C>(ring, total, tmem, full, empty, cempty, ctl, it);
         }
+        const uint64_t ad0 = sdesc_sw128(su32(ring));
+        const uint64_t bd0 = sdesc(su32(ring) + C::NA * kTileA, C::NB * 16, 128);
         for (int p = 0; p < npiece && ok && !C::Q4; ++p) {
             const Span sp = span(p);
             const int b = p & 1;
@@ -764,14 +766,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
                     break;
                 }
                 tc_after();
-                const unsigned sa = su32(ring + (size_t)s * C::STAGE);
-                const unsigned sx = sa + C::NA * kTileA;
-                const int ksteps = (a.K - 64 * ks < 64 ? a.K - 64 * ks : 64) / 16;
-                for (int kk = 0; kk < ksteps; ++kk) {
-                    const uint64_t bd = sdesc(sx + kk * 2 * C::NB * 16, C::NB * 16, 128);
-                    const unsigned acc = (ks > sp.kc0 || kk > 0) ? 1u : 0u;
-                    mma_f16(dcol, sdesc_sw128(sa + kk * 32), bd, idesc, acc);
-                    if (MODE == 1) mma_f16(dcol + C::NB, sdesc_sw128(sa + kTileA + kk * 32), bd, idesc, acc);
+                // descriptors advance by byte offset >> 4 from stage 0's: the
+                // issuing thread is one dependent chain, so its loop stays short
+                const uint64_t so = (uint64_t)((s * C::STAGE) >> 4);
+                const uint64_t ad = ad0 + so, bd = bd0 + so;
+                const unsigned first = ks > sp.kc0 ? 1u : 0u;
+                if (64 * ks + 64 <= a.K) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t bk = bd + (uint64_t)((kk * 2 * C::NB * 16) >> 4);
+                        const unsigned acc = kk > 0 ? 1u : first;
+                        mma_f16(dcol, ad + (uint64_t)(2 * kk), bk, idesc, acc);
+                        if (MODE == 1) mma_f16(dcol + C::NB, ad + (uint64_t)((kTileA >> 4) + 2 * kk), bk, idesc, acc);
+                    }
+                } else {
+                    const int ksteps = (a.K - 64 * ks) / 16;
+                    for (int kk = 0; kk < ksteps; ++kk) {
+                        const uint64_t bk = bd + (uint64_t)((kk * 2 * C::NB * 16) >> 4);
+                        const unsigned acc = kk > 0 ? 1u : first;
+                        mma_f16(dcol, ad + (uint64_t)(2 * kk), bk, idesc, acc);
+                        if (MODE == 1) mma_f16(dcol + C::NB, ad + (uint64_t)((kTileA >> 4) + 2 * kk), bk, idesc, acc);
+                    }
                 }
                 mma_commit(&empty[s]);
             }
