@@ -1214,8 +1214,10 @@ int u_grid(const Plan& p) {
 }
 }  // namespace
 
+// The INT4 batched plan covers 2 <= B <= 16 (its FC2 runs on CUDA cores);
+// FC1 moves to the tensor cores at 16 tokens, one N = 16 tile.
 bool tc4_supported(const Plan& p) {
-    return p.int4 && !p.gated && p.B >= 16 && p.B <= 32 && p.d % 256 == 0 && p.nsm <= kMaxCtas;
+    return p.int4 && !p.gated && p.B == 16 && p.d % 256 == 0 && p.nsm <= kMaxCtas;
 }
 
 bool tc_pred_supported(const Plan& p) { return p.B >= 16 && p.B <= 32 && p.d % 128 == 0 && p.nsm <= kMaxCtas; }
@@ -1344,7 +1346,7 @@ cudaError_t launch_fc1_tc4(const Plan& p, const __half* x, const LayerPtrs& w, c
     a.slots = slots_for(ceil_div(p.F, 128), G);
     a.status = status;
     a.timeout_ns = kTcTimeoutNs;
-    cudaError_t e = launch_rows_nt<4>(a, nt, G, s);
+    cudaError_t e = launch_rows<4, 16>(a, G, s);
     if (e != cudaSuccess) return e;
     return launch_fc1_finish(p, nt, G, a.slots, p.d / 256, part, count, idx, w.b1, mask, h, live, s);
 }
