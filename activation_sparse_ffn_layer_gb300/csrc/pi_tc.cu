@@ -230,21 +230,25 @@ PI_DEV void cp_wait_n(int n) {
 }
 
 // 8 INT4 codes (element e in bits 4e..4e+3, two's complement) as 8 fp16
-// integers in element order.  The 1024 + n bit pattern makes n = q + 8 an
-// exact fp16 value; subtracting 1032 is exact.
+// integers in element order, three operations per pair: byte b of w (elements
+// 2b and 2b+1, sign-flipped to n = q + 8) is spread to both halves, the low
+// half keeps bits 0-3 and the high half bits 4-7 under the fp16 pattern of
+// 1024, giving 1024 + n and 1024 + 16 n; one fp16 fma with (1, 1/16) and
+// (-1032, -72) returns q for both, exactly (every intermediate is an fp16
+// integer or a multiple of 1/16 below 128).
 PI_DEV uint4 q8_f16(uint32_t w) {
-    const uint32_t u = w ^ 0x88888888u;   // n + 8 in 0..15
-    const __half2 k1032 = __float2half2_rn(1032.f);
-    uint32_t ph[4];
+    const uint32_t u = w ^ 0x88888888u;
+    const uint32_t scale = 0x2C003C00u;   // (1, 1/16)
+    const uint32_t offset = 0xD480E408u;  // (-1032, -72)
+    uint32_t r[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        uint32_t t = ((u >> (4 * k)) & 0x000F000Fu) | 0x64006400u;   // (1024 + n_k, 1024 + n_{k+4})
-        const __half2 q = __hsub2(*reinterpret_cast<__half2*>(&t), k1032);
-        ph[k] = *reinterpret_cast<const uint32_t*>(&q);
+    for (int b = 0; b < 4; ++b) {
+        uint32_t t = (__byte_perm(u, 0u, 0x1111u * (unsigned)b) & 0x00F0000Fu) | 0x64006400u;
+        const __half2 q = __hfma2(*reinterpret_cast<const __half2*>(&t), *reinterpret_cast<const __half2*>(&scale),
+                                  *reinterpret_cast<const __half2*>(&offset));
+        r[b] = *reinterpret_cast<const uint32_t*>(&q);
     }
-    // pairs (e_k, e_{k+4}) -> (e0 e1)(e2 e3)(e4 e5)(e6 e7)
-    return make_uint4(__byte_perm(ph[0], ph[1], 0x5410), __byte_perm(ph[2], ph[3], 0x5410),
-                      __byte_perm(ph[0], ph[1], 0x7632), __byte_perm(ph[2], ph[3], 0x7632));
+    return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
 // Loaders of the INT4 FC1 (mode 4).  The CTA's K range is split in quads of
