@@ -14,8 +14,10 @@
 //
 // One CTA per SM, three warp roles:
 //   warps 0-3  load: cp.async 16-byte copies of the gathered rows straight into
-//              the tensor cores' shared-memory operand layout (no swizzle:
-//              8 rows x 16 bytes per core matrix), a ring of stages;
+//              the tensor cores' shared-memory operand layouts (A tiles with
+//              the 128-byte swizzle, B as 8 x 16-byte core matrices), a ring
+//              of stages; for INT4 rows they also convert the codes to fp16
+//              and store the A operand into tensor memory (tcgen05.st);
 //   warp  8    one thread issues tcgen05.mma (fp16 x fp16 -> fp32 in TMEM);
 //   warps 4-7  drain the TMEM accumulators (tcgen05.ld) and apply the epilogue.
 // Ring slots are handed over with mbarriers: loaders arrive on `full` after
@@ -25,8 +27,9 @@
 // word becomes PI_ERR_TIMEOUT, the CTA drains its own copies and MMAs, frees
 // its tensor memory and returns.
 //
-// FC1 work split: each CTA takes an equal contiguous share of the union list,
-// cut into tiles of at most 128 rows, so every SM streams the same bytes.
+// FC1 work split: the (128-row tile x K-chunk) space is cut into equal
+// contiguous ranges per CTA ("stream-K"; INT4 in quads of four K-chunks), so
+// every SM streams the same bytes; a finish kernel adds the partial tiles.
 // FC2 work split: the (column tile x union row) space is cut into equal
 // contiguous ranges per CTA ("stream-K"); each CTA writes one partial tile per
 // column tile it touches and a fixed-order reduction adds the partials to b2.
@@ -170,9 +173,10 @@ struct RowsCfg {
     static constexpr int X = NB * 128;                       // NB rows x 64 fp16
     static constexpr int STAGE = Q4 ? 0 : NA * kTileA + X;   // INT4: A in TMEM, x read from the raw ring
     // even ring of stages, filled two K-chunks at a time (256 contiguous bytes
-    // of every row per visit); LAGP pairs of copies stay in flight.  INT4:
-    // 4 stages, fed from a deeper ring of raw K-chunks (per row 32 bytes of
-    // codes and 4 of scales at a 48-byte pitch, then the chunk of x)
+    // of every row per visit); LAGP pairs of copies stay in flight.  INT4: 8
+    // A stages in TMEM (32 columns each), fed from a ring of RQ raw quads in
+    // shared memory (per row 128 bytes of codes at a 144-byte pitch, then the
+    // quad's x, which the MMAs read in place)
     static constexpr int S0 = Q4 ? 0 : kRingBudget / STAGE > 12 ? 12 : kRingBudget / STAGE;
     static constexpr int S = Q4 ? 8 : S0 & ~1;
     static constexpr int LAGP = S / 2 >= 4 ? S / 2 - 2 : S / 2 - 1;
