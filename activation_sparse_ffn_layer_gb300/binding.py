@@ -33,6 +33,11 @@ class pi_workspace_layout_t(C.Structure):
     _fields_ = [(n, C.c_size_t) for n in ("mask", "idx", "count", "h", "total")]
 
 
+class pi_stack_plan_t(C.Structure):
+    _fields_ = [(n, C.c_int) for n in ("fused", "ctas", "pred_in_smem", "p2_ring_slots", "fc_row_slots",
+                                       "smem_bytes")]
+
+
 class PiError(RuntimeError):
     def __init__(self, fn: str, status: int, msg: str):
         super().__init__(f"{fn}: {msg} (status {status})")
@@ -44,7 +49,7 @@ _lib = None
 EXPORTS = ("pi_workspace_bytes", "pi_workspace_layout", "pi_predict", "pi_compact", "pi_sparse_fc1",
            "pi_sparse_fc2", "pi_ffn_layer", "pi_rmsnorm_half", "pi_status_string",
            "pi_last_device_status", "pi_launches_per_layer", "pi_ffn_stack", "pi_debug_wait_timeout",
-           "pi_sparse_fc2_noalloc")
+           "pi_sparse_fc2_noalloc", "pi_stack_plan")
 
 
 def library_path() -> str:
@@ -79,6 +84,7 @@ def lib(path: Optional[str] = None):
         "pi_ffn_stack": (I, [D, I, C.POINTER(pi_layer_weights), P, P, Fl, Fl, P, S, P, P, P, P]),
         "pi_debug_wait_timeout": (I, [C.c_longlong, P]),
         "pi_sparse_fc2_noalloc": (I, [D, P, P, P, Wt, P, P]),
+        "pi_stack_plan": (I, [D, I, P, C.POINTER(pi_stack_plan_t)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -201,6 +207,13 @@ def weights_array(layers):
 
 def ranks_array(layers):
     return (C.c_int * len(layers))(*[int(w.r) for w in layers])
+
+
+def pi_stack_plan(desc, n_layers: int, ranks=None) -> pi_stack_plan_t:
+    """How a pi_ffn_stack step of `n_layers` layers runs on the current device."""
+    out = pi_stack_plan_t()
+    _check("pi_stack_plan", lib().pi_stack_plan(C.byref(desc), int(n_layers), ranks, C.byref(out)))
+    return out
 
 
 def pi_debug_wait_timeout(timeout_ns: int):

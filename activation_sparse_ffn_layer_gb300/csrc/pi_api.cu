@@ -328,6 +328,37 @@ pi_status pi_rmsnorm_half(int d, int batch, const float* y, float eps, pi_half* 
                                     static_cast<cudaStream_t>(stream)));
 }
 
+pi_status pi_stack_plan(const pi_layer_desc* desc, int n_layers, const int* ranks, pi_stack_plan_t* out) {
+    Plan p;
+    if (!desc || !out || !make_plan(*desc, &p)) return PI_ERR_INVALID_ARG;
+    if (n_layers < 1 || n_layers > kMaxStackLayers) return PI_ERR_INVALID_ARG;
+    *out = pi_stack_plan_t{};
+    if (!p.fused) return PI_OK;
+    int rk[kMaxStackLayers];
+    for (int l = 0; l < n_layers; ++l) {
+        rk[l] = ranks ? ranks[l] : p.r;
+        if (rk[l] <= 0 || rk[l] % 8 != 0 || rk[l] > p.r) return PI_ERR_INVALID_ARG;
+    }
+    FusedStackArgs a{};
+    a.L = n_layers;
+    a.d = p.d;
+    a.F = p.F;
+    a.G = p.nsm;
+    a.int4 = p.int4;
+    a.gated = p.gated;
+    a.ranks = rk;
+    a.rmax_su = p.rmax_su;
+    FusedStackConfig c{};
+    if (!fused_stack_config(a, &c)) return PI_OK;
+    out->fused = 1;
+    out->ctas = p.nsm;
+    out->pred_in_smem = c.pred_smem;
+    out->p2_ring_slots = c.ring_slots;
+    out->fc_row_slots = c.fc_slots;
+    out->smem_bytes = c.smem_bytes;
+    return PI_OK;
+}
+
 int pi_launches_per_layer(const pi_layer_desc* desc) {
     Plan p;
     if (!desc || !make_plan(*desc, &p)) return -1;

@@ -29,6 +29,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "pi_common.cuh"
 #include "pi_internal.h"
@@ -1269,47 +1270,21 @@ bool fused_supported(int d, int F, int rmax, bool int4, bool gated, int G) {
     return fc_slots_for(d, int4, (int)(room / 16 * 16)) >= (gated ? 4 : 2);
 }
 
-cudaError_t launch_fused(const FusedStackArgs& a, cudaStream_t s) {
-    if (a.L < 1 || a.L > kMaxFusedLayers || max_units(a.F, a.G) > kMaxUnits) return cudaErrorInvalidValue;
-    FusedParams prm = {};
+// Work split and shared-memory plan of one stack step (no pointers needed:
+// the layers' ranks and the shapes decide it).  Returns false if the stack
+// cannot run on the fused kernel.
+static bool plan_fused(const FusedStackArgs& a, FusedParams* out, size_t* smem_out) {
+    if (a.L < 1 || a.L > kMaxFusedLayers || max_units(a.F, a.G) > kMaxUnits) return false;
+    FusedParams& prm = *out;
     const int G = a.G;
     prm.L = a.L;
     prm.d = a.d;
     prm.F = a.F;
     prm.M = (a.F + 15) / 16;
     prm.W = (a.F + 31) / 32;
-    prm.tau = a.tau;
-    prm.eps = a.eps;
-    prm.timeout_ns = a.timeout_ns;
-    prm.x_in = a.x_in;
-    prm.y_out = a.y_out;
-    prm.x_trace = a.x_trace;
-    const XchgLayout xl(a.d, a.rmax_su, G);
-    char* ws = static_cast<char*>(a.xchg);
-    prm.epoch = reinterpret_cast<unsigned long long*>(ws);
-    prm.counter = reinterpret_cast<unsigned*>(ws + xl.counter);
-    prm.xu = reinterpret_cast<float*>(ws + xl.xu);
-    prm.xyp = reinterpret_cast<float*>(ws + xl.xyp);
-    prm.xy = reinterpret_cast<float*>(ws + xl.xy);
-    prm.xss = reinterpret_cast<float*>(ws + xl.xss);
-    prm.mask_out = a.mask_out;
-    prm.idx_out = a.idx_out;
-    prm.count_out = a.count_out;
-    prm.h_out = a.h_out;
-    prm.layer_counts = a.layer_counts;
     int rmax = 8;
     for (int l = 0; l < a.L; ++l) {
-        const LayerPtrs& w = a.layers[l];
         FusedLayer& f = prm.layers[l];
-        f.w1 = w.w1;
-        f.w1s = w.w1s;
-        f.b1 = w.b1;
-        f.wu = w.wu;
-        f.w2t = w.w2t;
-        f.w2ts = w.w2ts;
-        f.b2 = w.b2;
-        f.p1 = w.p1;
-        f.p2 = w.p2;
         f.r = a.ranks[l];
         // at most one (row, split) item per warp of the grid; splits >= 256 elements
         int su = (kWarps * G) / f.r;
@@ -1318,7 +1293,7 @@ cudaError_t launch_fused(const FusedStackArgs& a, cudaStream_t s) {
         if (su < 1) su = 1;
         f.seg = ((a.d / 8 + su - 1) / su) * 8;
         f.su = (a.d + f.seg - 1) / f.seg;
-        if ((size_t)f.su * f.r > a.rmax_su) return cudaErrorInvalidValue;
+        if ((size_t)f.su * f.r > a.rmax_su) return false;
         rmax = f.r > rmax ? f.r : rmax;
     }
     SmemPlan sp = smem_plan(a.d, a.F, rmax, a.rmax_su, G);
@@ -1354,7 +1329,7 @@ cudaError_t launch_fused(const FusedStackArgs& a, cudaStream_t s) {
         sp.stage = st > pred ? st : pred;
         prm.stage_bytes = sp.stage;
         prm.fc_slots = fc_slots_for(a.d, a.int4, sp.stage);
-        if (prm.fc_slots < (a.gated ? 4 : 2)) return cudaErrorInvalidValue;
+        if (prm.fc_slots < (a.gated ? 4 : 2)) return false;
         // predictor slices too large for shared memory: stream P2 in 16-row units
         // through the mask/list buffers and the staging region
         const int unit = 16 * rmax * 2;
@@ -1365,7 +1340,59 @@ cudaError_t launch_fused(const FusedStackArgs& a, cudaStream_t s) {
         }
     }
     const size_t smem = sp.bytes();
-    if (smem > 227 * 1024) return cudaErrorInvalidValue;
+    if (smem > 227 * 1024) return false;
+    *smem_out = smem;
+    return true;
+}
+
+bool fused_stack_config(const FusedStackArgs& a, FusedStackConfig* out) {
+    FusedParams prm = {};
+    size_t smem = 0;
+    if (!plan_fused(a, &prm, &smem)) return false;
+    out->pred_smem = prm.pred_smem;
+    out->ring_slots = prm.ring_slots;
+    out->fc_slots = prm.fc_slots;
+    out->smem_bytes = (int)smem;
+    return true;
+}
+
+cudaError_t launch_fused(const FusedStackArgs& a, cudaStream_t s) {
+    FusedParams prm = {};
+    size_t smem = 0;
+    if (!plan_fused(a, &prm, &smem)) return cudaErrorInvalidValue;
+    const int G = a.G;
+    prm.tau = a.tau;
+    prm.eps = a.eps;
+    prm.timeout_ns = a.timeout_ns;
+    prm.x_in = a.x_in;
+    prm.y_out = a.y_out;
+    prm.x_trace = a.x_trace;
+    const XchgLayout xl(a.d, a.rmax_su, G);
+    char* ws = static_cast<char*>(a.xchg);
+    prm.epoch = reinterpret_cast<unsigned long long*>(ws);
+    prm.counter = reinterpret_cast<unsigned*>(ws + xl.counter);
+    prm.xu = reinterpret_cast<float*>(ws + xl.xu);
+    prm.xyp = reinterpret_cast<float*>(ws + xl.xyp);
+    prm.xy = reinterpret_cast<float*>(ws + xl.xy);
+    prm.xss = reinterpret_cast<float*>(ws + xl.xss);
+    prm.mask_out = a.mask_out;
+    prm.idx_out = a.idx_out;
+    prm.count_out = a.count_out;
+    prm.h_out = a.h_out;
+    prm.layer_counts = a.layer_counts;
+    for (int l = 0; l < a.L; ++l) {
+        const LayerPtrs& w = a.layers[l];
+        FusedLayer& f = prm.layers[l];
+        f.w1 = w.w1;
+        f.w1s = w.w1s;
+        f.b1 = w.b1;
+        f.wu = w.wu;
+        f.w2t = w.w2t;
+        f.w2ts = w.w2ts;
+        f.b2 = w.b2;
+        f.p1 = w.p1;
+        f.p2 = w.p2;
+    }
     if (a.int4) return launch_kind<2, 4>(prm, G, smem, s);
     const int nch = (a.d + kCols - 1) / kCols;
     if (a.gated) {
@@ -1384,9 +1411,11 @@ cudaError_t launch_wait_nothing(long long timeout_ns, cudaStream_t s) {
 }
 
 int* status_word() {
+    static std::mutex mu;
     static int* cache[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
     if (cache[dev] == nullptr) {
         void* ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_pi_status) != cudaSuccess) return nullptr;

@@ -31,7 +31,7 @@ struct Plan {
     bool fc1_tc4;   // INT4 FC1 on the tensor cores (codes as fp16, group scales in the epilogue; batch 16-32)
     int pred;       // predictor path (its weights are fp16 for every weight type):
                     // 2 tcgen05 (batch 16..32), 1 streamed CUDA cores (batch 2..8), 0 chunked
-    size_t part_floats;  // FC2 partial sums of whichever FC2 path the plan takes
+    size_t part_floats;  // split partial sums: the largest need of the predictor, FC1 and FC2 paths taken
     size_t off_mask, off_idx, off_count, off_h, off_upart, off_part, off_xbuf, off_live, off_uhl, total;
 };
 
@@ -62,6 +62,8 @@ cudaError_t launch_fc1(const Plan& p, const __half* x, const LayerPtrs& w, const
                        cudaStream_t s);
 cudaError_t launch_fc2(const Plan& p, const float* h, const int32_t* idx, const int32_t* count,
                        const LayerPtrs& w, const int32_t* live, float* partial, float* y, cudaStream_t s);
+// partial-sum floats of the FC2 path launch_fc2 takes for this plan (FC2 alone)
+size_t fc2_part_floats(const Plan& p);
 cudaError_t launch_rmsnorm(int d, int B, const float* y, float eps, __half* x, cudaStream_t s);
 // out[0] = *count, out[1] = listed neurons whose h is non-zero for some token
 cudaError_t launch_count_active(const Plan& p, const int32_t* count, const float* h, int32_t* out, cudaStream_t s);
@@ -71,6 +73,7 @@ bool tc_supported(const Plan& p);
 bool tc_pred_supported(const Plan& p);   // predictor only (any weight type)
 int tc_tokens(const Plan& p);       // N of the MMAs: batch rounded up to 16 or 32
 size_t tc_part_floats(const Plan& p);  // partial tiles of the stream-K splits
+size_t tc_fc2_part_floats(const Plan& p);  // ... of the FC2 split alone
 size_t tc_uhl_bytes(const Plan& p);    // u as fp16 hi | lo rows
 cudaError_t launch_predict_tc(const Plan& p, const __half* x, const __half* p1, const __half* p2,
                               const __half* bpred, float tau, uint32_t* mask, float* part, __half* uhl,
@@ -99,6 +102,7 @@ bool st_supported(const Plan& p);
 bool st_pred_supported(const Plan& p);   // predictor only (any weight type)
 int st_tokens(const Plan& p);          // token slots of the kernels: 2, 4 or 8
 size_t st_part_floats(const Plan& p);
+size_t st_fc2_part_floats(const Plan& p);
 size_t st_u_bytes(const Plan& p);      // u as fp32 rows [B][r]
 cudaError_t launch_predict_st(const Plan& p, const __half* x, const __half* p1, const __half* p2,
                               const __half* bpred, float tau, uint32_t* mask, float* part, float* u32,
@@ -112,6 +116,7 @@ cudaError_t launch_fc2_st(const Plan& p, const float* h, const int32_t* idx, con
 // ---- CUDA-core streamed batched path for INT4 weights (pi_stream4.cu, batch 2..16) ----
 bool st4_supported(const Plan& p);
 size_t st4_part_floats(const Plan& p);
+size_t st4_fc2_part_floats(const Plan& p);
 cudaError_t launch_fc1_st4(const Plan& p, const __half* x, const LayerPtrs& w, const int32_t* idx,
                            const int32_t* count, const uint32_t* mask, float* part, float* h, int32_t* live,
                            cudaStream_t s);
@@ -140,6 +145,15 @@ struct FusedStackArgs {
 size_t fused_workspace_bytes(int d, int F, size_t rmax_su, int G);
 bool fused_supported(int d, int F, int rmax, bool int4, bool gated, int G);
 cudaError_t launch_fused(const FusedStackArgs& a, cudaStream_t s);
+// How a stack step would run on the fused kernel (shapes and ranks of `a`
+// only; its pointers are not read).  False if the fused kernel cannot take it.
+struct FusedStackConfig {
+    int pred_smem;   // predictor slices staged whole in shared memory
+    int ring_slots;  // else P2 units stream through this many slots
+    int fc_slots;    // FC row slots
+    int smem_bytes;  // dynamic shared memory per CTA
+};
+bool fused_stack_config(const FusedStackArgs& a, FusedStackConfig* out);
 cudaError_t launch_wait_nothing(long long timeout_ns, cudaStream_t s);
 cudaError_t read_and_clear_status(int* out, cudaStream_t s);
 // Device address of the status word that bounded waits set on expiry (current device).

@@ -566,6 +566,13 @@ cudaError_t launch_fc2(const Plan& p, const float* h, const int32_t* idx, const 
     return cudaGetLastError();
 }
 
+size_t fc2_part_floats(const Plan& p) {
+    if (p.tc) return tc_fc2_part_floats(p);
+    if (p.st) return st_fc2_part_floats(p);
+    if (p.st4) return st4_fc2_part_floats(p);
+    return (size_t)p.fc2_splits * p.B * p.d;
+}
+
 cudaError_t launch_count_active(const Plan& p, const int32_t* count, const float* h, int32_t* out, cudaStream_t s) {
     k_count_active<<<1, 256, 0, s>>>(count, h, p.B, out);
     return cudaGetLastError();

@@ -22,7 +22,8 @@
 namespace pi {
 namespace {
 
-// 8 MiB of fp32 partial sums: the plan's FC2 partials must fit.
+// 8 MiB of fp32 partial sums: the FC2 partials of the path the plan takes
+// must fit (the predictor's and FC1's partials do not enter this call).
 constexpr size_t kNoallocScratchFloats = (size_t(8) << 20) / sizeof(float);
 
 static __device__ __align__(256) float g_fc2_scratch[kNoallocScratchFloats];
@@ -61,7 +62,7 @@ extern "C" pi_status pi_sparse_fc2_noalloc(const pi_layer_desc* desc, const floa
     if (!fc2_args_ok(p, h, idx, d_count, w, y)) return PI_ERR_INVALID_ARG;
     // every partial-sum slot the reduction reads is written by the same call
     // first, so nothing in the array has to start at zero
-    if (p.part_floats > kNoallocScratchFloats) return PI_ERR_WORKSPACE;
+    if (fc2_part_floats(p) > kNoallocScratchFloats) return PI_ERR_WORKSPACE;
     float* scratch = nullptr;
     if (scratch_address(&scratch) != cudaSuccess) return PI_ERR_CUDA;
     const cudaError_t e =

@@ -1,9 +1,9 @@
 // pi_stream.cu -- the batched union path on CUDA cores (batch 2..8, fp16
 // weights).
 //
-// Same work as the tensor-core path (PowerInfer (arXiv 2312.12456) §5
-// "Neuron-aware Inference Engine": the union's rows of W1 and W2t are read
-// once for all tokens), with the same streamed structure: one CTA per SM,
+// Same work as the tensor-core path (PowerInfer summary (CSDN), section
+// "Neuron-aware operator": only the rows of active neurons are processed; here
+// the union's rows of W1 and W2t are read once for all tokens), with the same streamed structure: one CTA per SM,
 // 4 loader warps fill a ring of stages with cp.async (paired K-chunks: 256
 // contiguous bytes of a row per visit), the (tile x K-chunk) or (column tile x
 // row) space is split evenly over the CTAs ("stream-K"), and fixed-order finish
@@ -650,6 +650,11 @@ size_t st_part_floats(const Plan& p) {
     const size_t pu = (size_t)u_grid_st(p) * slots_of(cdiv(p.r, 128), u_grid_st(p)) * tb * 128;
     size_t m = fc1 > fc2 ? fc1 : fc2;
     return m > pu ? m : pu;
+}
+
+size_t st_fc2_part_floats(const Plan& p) {
+    const size_t G = p.nsm > 0 ? p.nsm : 1;
+    return G * slots_of(p.d / 128, (int)G) * st_tokens(p) * 128;
 }
 
 size_t st_u_bytes(const Plan& p) { return (size_t)p.B * p.r * sizeof(float); }

@@ -3,9 +3,9 @@
 //
 // Same streamed structure as the fp16 batched kernels (loader warps filling a
 // cp.async ring, stream-K split over the CTAs, fixed-order finish kernels),
-// with the INT4 rows dequantised in registers (PowerInfer (arXiv 2312.12456)
-// §7 "Implementation": 4-bit models; the code q of an element is a signed
-// 4-bit integer, its value q * s with one fp16 scale s per 32 consecutive
+// with the INT4 rows dequantised in registers (PowerInfer summary (CSDN),
+// section "Introduction": 4-bit quantised models; the code q of an element is
+// a signed 4-bit integer, its value q * s with one fp16 scale s per 32 consecutive
 // elements of the row).  A stage holds 256 elements of each of 128 rows (FC1)
 // or 256 columns of each of 64 rows (FC2): 128 bytes of codes followed by the
 // 16 bytes of the 8 scales, a 144-byte pitch (9 x 16 bytes: the 8 lanes of a
@@ -645,6 +645,11 @@ size_t st4_part_floats(const Plan& p) {
     const size_t fc1 = G * qslots(qdiv(p.F, 128), (int)G) * q1_tokens(p.B) * 128;
     const size_t fc2 = G * qslots(p.d / 256, (int)G) * q2_tokens(p.B) * 256;
     return fc1 > fc2 ? fc1 : fc2;
+}
+
+size_t st4_fc2_part_floats(const Plan& p) {
+    const size_t G = p.nsm > 0 ? p.nsm : 1;
+    return G * qslots(p.d / 256, (int)G) * q2_tokens(p.B) * 256;
 }
 
 cudaError_t launch_fc1_st4(const Plan& p, const __half* x, const LayerPtrs& w, const int32_t* idx,

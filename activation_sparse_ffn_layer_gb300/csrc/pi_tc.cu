@@ -3,9 +3,9 @@
 //
 // At batch B the union of the B tokens' predicted neurons is gathered once and
 // both FFN products become dense contractions over the gathered rows
-// (PowerInfer (arXiv 2312.12456) §5 "Neuron-aware Inference Engine": only the
-// activated rows of W1 and columns of W2 are processed; §4.3 / Figure 6 for the
-// row-per-neuron layout):
+// (PowerInfer summary (CSDN), section "Neuron-aware operator": only the rows
+// and columns of active neurons are processed; section "Background": a neuron
+// is a row of W1 and a column of W2, stored here as a row of W2t):
 //
 //   FC1   Z[j, t] = sum_k W1[idx_j, k] x[t, k]        M = 128 listed neurons,
 //                                                      N = tokens, K = d
@@ -1241,6 +1241,11 @@ size_t tc_part_floats(const Plan& p) {
     const size_t pu = (size_t)u_grid(p) * slots_for(ceil_div(p.r, 128), u_grid(p)) * nt * 128;
     size_t m = fc1 > fc2 ? fc1 : fc2;
     return m > pu ? m : pu;
+}
+
+size_t tc_fc2_part_floats(const Plan& p) {
+    const size_t G = p.nsm > 0 ? p.nsm : 1;
+    return G * slots_for(p.d / 128, (int)G) * tc_tokens(p) * 128;
 }
 
 size_t tc_uhl_bytes(const Plan& p) { return (size_t)2 * tc_tokens(p) * p.r * sizeof(__half); }

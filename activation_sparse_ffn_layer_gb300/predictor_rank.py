@@ -1,9 +1,9 @@
 """Per-layer predictor sizing on synthetic inputs.
 
-PowerInfer (arXiv 2312.12456), "Adaptive sparse predictor": every layer gets
-its own predictor size; for a layer whose activations are skewed the size is
-lowered step by step while the predictor still finds at least 95 % of the
-neurons that really fire.  Here the predictor is the low-rank linear map
+PowerInfer summary (CSDN), section "Adaptive sparse predictor": every layer
+gets its own predictor size; for a layer whose activations are skewed the
+size is lowered step by step while the predictor still finds at least 95 % of
+the neurons that really fire.  Here the predictor is the low-rank linear map
 ``mask = (P2 (P1 x) + b1 > tau)`` with ``P1 = V_r^T``, ``P2 = U_r S_r`` from a
 truncated SVD of the layer's FC1 weights, so its size is the rank r; this
 module picks, per layer, the smallest rank (a multiple of ``step``) whose
@@ -54,17 +54,14 @@ def smallest_rank(recall_of: Callable[[int], float], candidates: Sequence[int], 
 
 
 def _fc1_weights_fp32(w) -> torch.Tensor:
-    """FC1 (gate) rows in storage order as fp32 (INT4 codes times their group scales)."""
+    """FC1 (gate) rows in storage order as fp32.  INT4 layers carry the
+    generator's own reconstruction (codes times group scales), made with
+    ``make_layer(..., keep_recon=True)``."""
     if not w.int4:
         return w.w1.float()
-    q = w.w1_q
-    lo = (q & 0xF).to(torch.int16)
-    hi = (q >> 4).to(torch.int16)
-    lo = torch.where(lo >= 8, lo - 16, lo)
-    hi = torch.where(hi >= 8, hi - 16, hi)
-    codes = torch.stack([lo, hi], dim=-1).reshape(w.F, w.d).float()
-    scales = w.w1_s.float().repeat_interleave(32, dim=1)
-    return codes * scales
+    if w.w1_recon is None:
+        raise ValueError("INT4 layer without its FC1 reconstruction: build it with make_layer(keep_recon=True)")
+    return w.w1_recon
 
 
 def _unpack(mask: torch.Tensor, F: int) -> torch.Tensor:
@@ -165,7 +162,7 @@ def main(argv=None):
     cfg = CONFIGS[args.config]
     x = make_tokens(cfg, 0, args.tokens, device="cuda")
     for l in range(args.layers):
-        w = make_layer(cfg, l, device="cuda")
+        w = make_layer(cfg, l, device="cuda", keep_recon=True)
         ch = LayerSizer(w, x, cfg.tau, max_rank=cfg.layer_rank(l)).choose(args.target, args.step,
                                                                           relative=args.relative)
         pred_bytes = 2 * ch.rank * (cfg.d + cfg.F)

@@ -162,10 +162,12 @@ PI_API pi_status pi_sparse_fc2(const pi_layer_desc *desc, const float *h, const 
  * workspace pi_sparse_fc2 needs.  Same arguments and result as pi_sparse_fc2
  * without the workspace; the FC2 partial sums live in an 8 MiB array inside
  * the library that every GPU loading the library holds until process exit.
- *  - Returns PI_ERR_WORKSPACE when the partial sums of `desc` exceed that
- *    array (splits x batch x d floats on the CUDA-core path; SMs x tiles per
- *    SM x 16 or 32 x 128 floats on the batch 16..32 tensor-core path);
- *    allocates nothing in any case.
+ *  - Returns PI_ERR_WORKSPACE when the FC2 partial sums of `desc` exceed that
+ *    array (2 Mi floats).  They are, with G the SM count: splits x batch x d
+ *    floats on the per-token path; G x (ceil(d/128/G) + 2) x T x 128 floats on
+ *    the streamed fp16 path (T = 2, 4 or 8 tokens) and on the batch 16..32
+ *    tensor-core path (T = 16 or 32); G x (ceil(d/256/G) + 2) x T x 256 on
+ *    the streamed INT4 path (T = 4, 8 or 16).  Allocates nothing in any case.
  *  - The first call on a device looks up the array's device address (once per
  *    device, with that device current); make that first call before any
  *    stream capture.
@@ -222,6 +224,24 @@ PI_API pi_status pi_workspace_layout(const pi_layer_desc *desc, pi_workspace_lay
  */
 PI_API pi_status pi_rmsnorm_half(int d, int batch, const float *y, float eps, pi_half *x_out,
                           void *stream);
+
+/* How one pi_ffn_stack step of `desc` (n_layers layers with the given ranks,
+ * NULL: all desc->rank) is executed on the current device.  Diagnostics: lets a
+ * caller or a test see which streaming mode the batch-1 persistent kernel
+ * takes for a shape.  Host only, launches nothing. */
+typedef struct {
+    int fused;         /* 1: one persistent launch per decode step (batch 1)      */
+    int ctas;          /* its thread blocks (one per SM)                          */
+    int pred_in_smem;  /* 1: a block's share of the predictor is copied whole into
+                          shared memory before it is used                         */
+    int p2_ring_slots; /* else: a block's P2 rows stream through this many slots of
+                          16 rows (0: read from global memory)                    */
+    int fc_row_slots;  /* FC weight rows a block holds in shared memory at once; a
+                          block whose predicted neurons need more rows (gated: 3
+                          per neuron, else 2) streams them through a ring          */
+    int smem_bytes;    /* dynamic shared memory per block                         */
+} pi_stack_plan_t;
+PI_API pi_status pi_stack_plan(const pi_layer_desc *desc, int n_layers, const int *ranks, pi_stack_plan_t *out);
 
 /* Number of kernel launches one pi_ffn_layer call issues for `desc` (-1 if
  * the descriptor is invalid). */

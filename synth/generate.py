@@ -65,6 +65,7 @@ class LayerWeights:
     w1_s: Optional[torch.Tensor] = None  # fp16 [F, d/32]
     w2t_q: Optional[torch.Tensor] = None
     w2t_s: Optional[torch.Tensor] = None
+    w1_recon: Optional[torch.Tensor] = None  # fp32 [F, d] q*s of the INT4 FC1 rows (keep_recon only)
 
     def tensors(self):
         return {f.name: getattr(self, f.name) for f in fields(self)
@@ -80,7 +81,8 @@ class LayerWeights:
         return LayerWeights(**kw)
 
     def nbytes(self) -> int:
-        return sum(t.numel() * t.element_size() for k, t in self.tensors().items() if k != "p_fire")
+        return sum(t.numel() * t.element_size() for k, t in self.tensors().items()
+                   if k not in ("p_fire", "w1_recon"))
 
 
 def _gen(seed: int, device) -> torch.Generator:
@@ -182,10 +184,13 @@ def neuron_table(p_fire: torch.Tensor, n_hot: int) -> torch.Tensor:
     return torch.cat([hot, cold]).to(torch.int32)
 
 
-def make_layer(cfg: Config, layer: int, device="cpu", *, table_override: Optional[torch.Tensor] = None) -> LayerWeights:
+def make_layer(cfg: Config, layer: int, device="cpu", *, table_override: Optional[torch.Tensor] = None,
+               keep_recon: bool = False) -> LayerWeights:
     """Draw one layer of a workload.  ``table_override`` (a permutation of
     ``range(F)``) replaces the hot-first neuron table; the layer is otherwise
-    identical, which lets tests check that the table order does not matter."""
+    identical, which lets tests check that the table order does not matter.
+    ``keep_recon`` keeps, for INT4 layers, the fp32 reconstruction of the FC1
+    rows that the calibration and the factorisation used (storage order)."""
     d, F = cfg.d, cfg.F
     r = min(cfg.layer_rank(layer), d, F)
     g = _gen(1000 * cfg.index + layer, device)
@@ -229,6 +234,8 @@ def make_layer(cfg: Config, layer: int, device="cpu", *, table_override: Optiona
     else:
         for k in ("w1_q", "w1_s", "w2t_q", "w2t_s"):
             out[k] = out[k][rows].contiguous()
+        if keep_recon:
+            out["w1_recon"] = w1[rows].contiguous()
     return LayerWeights(
         d=d, F=F, r=r, gated=cfg.gated, int4=cfg.int4,
         b1=b1.to(device)[rows].contiguous(),

@@ -24,7 +24,7 @@ def test_rank_choice_and_oracle_recall(kind, cfg):
     import activation_sparse_ffn_layer_gb300 as P
     from activation_sparse_ffn_layer_gb300.predictor_rank import LayerSizer
     P.lib()
-    w = make_layer(cfg, 0, device=DEV)
+    w = make_layer(cfg, 0, device=DEV, keep_recon=True)
     x = make_tokens(cfg, 0, 32, device=DEV)
     sz = LayerSizer(w, x, cfg.tau, max_rank=cfg.rank)
     ch = sz.choose(target=0.95, step=16)

@@ -1,0 +1,98 @@
+"""Batch-1 decode stacks at the full widths of the OPT-30B-, LLaMA-70B- and
+OPT-175B-shaped workloads, three layers deep, checked against the oracle layer
+by layer (mask outside the guard band, FC output, the normalised input of the
+next layer).
+
+At these widths a block's share of the predictor does not fit in shared
+memory, so the persistent kernel streams P2 through a ring of 16-row slots,
+and a block whose predicted neurons need more FC rows than it has row slots
+streams them through a ring whose position carries over from one layer to the
+next.  The test reads the plan the library takes (pi_stack_plan) and, from the
+GPU's own masks and the kernel's deal of 8-row pieces, which blocks ran their
+FC rows through the ring in which layers; it requires both ring modes to have
+run, in the first layer and in a later one."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synth import CONFIGS, make_layer, make_tokens
+from tests.parity import close, half_matches, mask_matches
+
+DEV = "cuda"
+
+
+def _pi():
+    import activation_sparse_ffn_layer_gb300 as P
+    P.lib()
+    return P
+
+
+def own_rows_per_block(mask_bits: np.ndarray, F: int, G: int) -> np.ndarray:
+    """Predicted rows of each block under the persistent kernel's deal: 8-row
+    pieces, round k of G consecutive pieces handed to blocks 0..G-1 in
+    ascending order for even k and descending order for odd k."""
+    P = (F + 7) // 8
+    piece = np.arange(P)
+    rnd, pos = piece // G, piece % G
+    owner = np.where(rnd % 2 == 0, pos, G - 1 - pos)
+    per_piece = np.add.reduceat(mask_bits.astype(np.int64), np.arange(0, F, 8))
+    return np.bincount(owner, weights=per_piece, minlength=G).astype(np.int64)
+
+
+def _unpack(words: np.ndarray, F: int) -> np.ndarray:
+    w = np.asarray(words, dtype=np.uint32)
+    bits = ((w[:, None] >> np.arange(32, dtype=np.uint32)[None, :]) & 1).astype(bool).ravel()
+    return bits[:F]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("key", ["c3", "c4", "c5"])
+def test_wide_stack_layers_match_oracle_in_ring_modes(key):
+    P = _pi()
+    from activation_sparse_ffn_layer_gb300.runtime import DecodeStack
+    cfg, L = CONFIGS[key], 3
+    ws = [make_layer(cfg, l, device=DEV) for l in range(L)]
+    x = make_tokens(cfg, 0, 1, device=DEV)
+    full = DecodeStack(ws, batch=1, tau=cfg.tau, eps=cfg.rms_eps)
+    plan = P.pi_stack_plan(full.desc, L, full.ranks)
+    assert plan.fused == 1, "batch-1 stack not on the persistent kernel"
+    assert plan.pred_in_smem == 0 and plan.p2_ring_slots >= 2, "P2 ring not taken"
+    xs_full, y_full = full.step_trace(x)
+    rows_per_neuron = 3 if cfg.gated else 2
+    ring_blocks = []
+    for l in range(L):
+        # a prefix run leaves layer l's mask in the workspace and returns its output
+        st = DecodeStack(ws[: l + 1], batch=1, tau=cfg.tau, eps=cfg.rms_eps)
+        xs, y = st.step_trace(x)
+        torch.cuda.synchronize()
+        for j in range(l + 1):
+            assert torch.equal(xs[j], xs_full[j]), f"layer {j} input differs between runs"
+        lay = P.pi_workspace_layout(st.desc)
+        W = (cfg.F + 31) // 32
+        mask = st.workspace[lay.mask:lay.mask + 4 * W].view(torch.int32).cpu().numpy().view(np.uint32)
+        host = oracle.host_layer(ws[l].to("cpu"))
+        xl = xs[l][0].cpu()
+        mask_matches(mask, oracle.predict(xl, host, cfg.tau), cfg.F, cfg.tau, f"{key} layer {l}")
+        close(y[0].cpu().numpy(), oracle.ffn_masked(xl, host, mask), f"{key} stack layer {l}")
+        if l + 1 < L:
+            _, pre, band = oracle.rmsnorm_half(y[0].cpu().numpy().astype(np.float64), cfg.rms_eps)
+            half_matches(xs_full[l + 1][0].cpu().view(torch.int16).numpy().view(np.uint16), pre, band,
+                         f"{key} normalised input of layer {l + 1}")
+        own = own_rows_per_block(_unpack(mask, cfg.F), cfg.F, plan.ctas)
+        ring_blocks.append(set(np.nonzero(own * rows_per_neuron > plan.fc_row_slots)[0].tolist()))
+        del host
+    close(y_full[0].cpu().numpy(), y[0].cpu().numpy(), "full run vs prefix run", max_abs=0, rel_l2=0)
+    assert ring_blocks[0], f"{key}: no block streamed its FC rows through the ring in layer 0"
+    assert any(ring_blocks[0] & ring_blocks[l] for l in range(1, L)), \
+        f"{key}: no block ran the FC row ring in layer 0 and again in a later layer"
+
+
+def test_own_rows_deal_small_example():
+    """The deal replica on a hand-worked case: F = 40 (5 pieces), G = 2:
+    pieces 0,1 -> blocks 0,1; pieces 2,3 -> blocks 1,0; piece 4 -> block 0."""
+    bits = np.zeros(40, dtype=bool)
+    bits[[0, 9, 10, 17, 26, 33, 39]] = True       # pieces 0, 1, 1, 2, 3, 4, 4
+    own = own_rows_per_block(bits, 40, 2)
+    # block 0: piece 0 (1) + piece 3 (1) + piece 4 (2) = 4; block 1: piece 1 (2) + piece 2 (1) = 3
+    assert own.tolist() == [4, 3]

@@ -1,6 +1,7 @@
 """Host logic of the per-layer predictor sizing (no GPU): the candidate scan,
-the mask unpacking and the INT4 FC1 decode used for the factorisation (pinned
-against the oracle's own FC1 of the same packed rows)."""
+the mask unpacking and the INT4 FC1 rows used for the factorisation (the
+generator's reconstruction, pinned against the oracle's own FC1 of the same
+packed rows)."""
 import numpy as np
 import torch
 
@@ -32,7 +33,7 @@ def test_unpack_bits():
 
 def test_int4_decode_matches_oracle_fc1():
     cfg = small(CONFIGS["c5"], d=256, F=96, rank=16)
-    w = make_layer(cfg, 0, device="cpu")
+    w = make_layer(cfg, 0, device="cpu", keep_recon=True)
     x = make_tokens(cfg, 0, 1, device="cpu")[0]
     W = _fc1_weights_fp32(w).double().numpy()
     z = W @ x.double().numpy() + w.b1.double().numpy()
