@@ -49,7 +49,7 @@ _lib = None
 EXPORTS = ("pi_workspace_bytes", "pi_workspace_layout", "pi_predict", "pi_compact", "pi_sparse_fc1",
            "pi_sparse_fc2", "pi_ffn_layer", "pi_rmsnorm_half", "pi_status_string",
            "pi_last_device_status", "pi_launches_per_layer", "pi_ffn_stack", "pi_debug_wait_timeout",
-           "pi_sparse_fc2_noalloc", "pi_stack_plan")
+           "pi_sparse_fc2_noalloc", "pi_stack_plan", "pi_debug_set_wait_timeout")
 
 
 def library_path() -> str:
@@ -85,6 +85,7 @@ def lib(path: Optional[str] = None):
         "pi_debug_wait_timeout": (I, [C.c_longlong, P]),
         "pi_sparse_fc2_noalloc": (I, [D, P, P, P, Wt, P, P]),
         "pi_stack_plan": (I, [D, I, P, C.POINTER(pi_stack_plan_t)]),
+        "pi_debug_set_wait_timeout": (I, [C.c_longlong]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -214,6 +215,10 @@ def pi_stack_plan(desc, n_layers: int, ranks=None) -> pi_stack_plan_t:
     out = pi_stack_plan_t()
     _check("pi_stack_plan", lib().pi_stack_plan(C.byref(desc), int(n_layers), ranks, C.byref(out)))
     return out
+
+
+def pi_debug_set_wait_timeout(timeout_ns: int):
+    _check("pi_debug_set_wait_timeout", lib().pi_debug_set_wait_timeout(int(timeout_ns)))
 
 
 def pi_debug_wait_timeout(timeout_ns: int):

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "pi_internal.h"
@@ -153,6 +154,12 @@ LayerPtrs layer_ptrs(const pi_layer_weights* w) { return ptrs(w); }
 
 constexpr int kMaxStackLayers = 96;
 constexpr long long kWaitTimeoutNs = 2000000000ll;  // 2 s per wait
+std::atomic<long long> g_wait_override_ns{0};
+
+long long wait_timeout_ns() {
+    const long long v = g_wait_override_ns.load(std::memory_order_relaxed);
+    return v > 0 ? v : kWaitTimeoutNs;
+}
 
 // One decode step through n layers: the fused persistent kernel when the plan
 // allows it, else the per-step kernels with the normalisation between layers.
@@ -178,7 +185,7 @@ cudaError_t run_stack(const Plan& p, int n, const LayerPtrs* lp, const int* rank
         a.gated = p.gated;
         a.tau = tau;
         a.eps = eps;
-        a.timeout_ns = kWaitTimeoutNs;
+        a.timeout_ns = wait_timeout_ns();
         a.layers = lp;
         a.ranks = rk;
         a.x_in = x;
@@ -395,6 +402,12 @@ pi_status pi_last_device_status(void* stream) {
     int v = 0;
     if (read_and_clear_status(&v, static_cast<cudaStream_t>(stream)) != cudaSuccess) return PI_ERR_CUDA;
     return v == 0 ? PI_OK : static_cast<pi_status>(v);
+}
+
+pi_status pi_debug_set_wait_timeout(long long timeout_ns) {
+    if (timeout_ns < 0 || timeout_ns > 10000000000ll) return PI_ERR_INVALID_ARG;
+    g_wait_override_ns.store(timeout_ns, std::memory_order_relaxed);
+    return PI_OK;
 }
 
 pi_status pi_debug_wait_timeout(long long timeout_ns, void* stream) {

@@ -37,6 +37,13 @@ struct Plan {
 
 bool make_plan(const pi_layer_desc& desc, Plan* p);
 
+// Limit of the bounded device-side waits of the next launches: 2 s, unless a
+// caller set another one with pi_debug_set_wait_timeout.  Draining a CTA's own
+// copies and MMAs after a failed wait always gets kDrainTimeoutNs, so a short
+// wait limit never lets a CTA leave with its copies in flight.
+long long wait_timeout_ns();
+constexpr long long kDrainTimeoutNs = 2000000000ll;
+
 struct LayerPtrs {
     const void* w1;
     const __half* w1s;

@@ -36,7 +36,6 @@ constexpr int kSCompute = 8;     // compute warps
 constexpr int kSBudget = 210 * 1024;
 constexpr int kPitch = 144;      // shared bytes of one row's 64 fp16 (128 + 16)
 constexpr int kTileS = 128 * kPitch;
-constexpr long long kStTimeoutNs = 2000000000ll;
 
 // ------------------------------------------------------------------ row GEMMs
 //   MODE 0  FC1            A = W1 rows (gathered),        Bop = x (fp16)
@@ -674,7 +673,7 @@ cudaError_t launch_predict_st(const Plan& p, const __half* x, const __half* p1, 
     a.part = part;
     a.slots = slots_of(cdiv(p.r, 128), Gu);
     a.status = status;
-    a.timeout_ns = kStTimeoutNs;
+    a.timeout_ns = wait_timeout_ns();
     cudaError_t e = launch_rows_tb<2>(a, tb, Gu, s);
     if (e != cudaSuccess) return e;
     k_u_finish32<<<cdiv(p.r, 32), 256, 0, s>>>(part, a.slots, Gu, cdiv(p.d, 64), p.r, p.B, tb, u32);
@@ -693,7 +692,7 @@ cudaError_t launch_predict_st(const Plan& p, const __half* x, const __half* p1, 
     b.mask = mask;
     b.W = p.W;
     b.status = status;
-    b.timeout_ns = kStTimeoutNs;
+    b.timeout_ns = wait_timeout_ns();
     return launch_rows_tb<3>(b, tb, p.nsm, s);
 }
 
@@ -714,7 +713,7 @@ cudaError_t launch_fc1_st(const Plan& p, const __half* x, const LayerPtrs& w, co
     a.part = part;
     a.slots = slots_of(cdiv(p.F, 128), G);
     a.status = status;
-    a.timeout_ns = kStTimeoutNs;
+    a.timeout_ns = wait_timeout_ns();
     cudaError_t e = p.gated ? launch_rows_tb<1>(a, tb, G, s) : launch_rows_tb<0>(a, tb, G, s);
     if (e != cudaSuccess) return e;
     return launch_fc1_finish(p, tb, G, a.slots, cdiv(p.d, 64), part, count, idx, w.b1, mask, h, live, s);
@@ -726,7 +725,7 @@ cudaError_t launch_fc2_st(const Plan& p, const float* h, const int32_t* idx, con
     if (status == nullptr) return cudaErrorInvalidDevice;
     const int tb = st_tokens(p), G = p.nsm;
     const int slots = slots_of(p.d / 128, G);
-    SArgs2 a{h, idx, count, static_cast<const __half*>(w.w2t), live, partial, status, kStTimeoutNs, p.B, p.d, slots};
+    SArgs2 a{h, idx, count, static_cast<const __half*>(w.w2t), live, partial, status, wait_timeout_ns(), p.B, p.d, slots};
     cudaError_t e;
 #define PI_FC2ST(TBV)                                                     \
     if (tb == TBV) {                                                      \

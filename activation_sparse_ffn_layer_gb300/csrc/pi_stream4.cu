@@ -34,7 +34,6 @@ constexpr int kQBudget = 210 * 1024;
 constexpr int kQPitch = 144;     // 128 bytes of codes + 16 bytes of scales
 constexpr int kQTile = 128 * kQPitch;
 constexpr int kQTile2 = 64 * kQPitch;
-constexpr long long kQTimeoutNs = 2000000000ll;
 
 // Barriers of the 256 compute threads (ids 0 and 1 are the CTA's and the
 // loaders'): a plain one, and one that ORs a flag so all take the same branch
@@ -659,7 +658,7 @@ cudaError_t launch_fc1_st4(const Plan& p, const __half* x, const LayerPtrs& w, c
     if (status == nullptr) return cudaErrorInvalidDevice;
     const int tb = q1_tokens(p.B), G = p.nsm;
     Q1Args a{static_cast<const uint8_t*>(w.w1), w.w1s, idx, count, x, p.d, p.B, part,
-             qslots(qdiv(p.F, 128), G), status, kQTimeoutNs};
+             qslots(qdiv(p.F, 128), G), status, wait_timeout_ns()};
     cudaError_t e;
 #define PI_Q1(TBV)                                                       \
     if (tb == TBV) {                                                     \
@@ -682,7 +681,7 @@ cudaError_t launch_fc2_st4(const Plan& p, const float* h, const int32_t* idx, co
     const int slots = qslots(p.d / 256, G);
     for (int b0 = 0; b0 < p.B; b0 += tb) {
         const int nb = p.B - b0 < tb ? p.B - b0 : tb;
-        Q2Args a{h, idx, count, static_cast<const uint8_t*>(w.w2t), w.w2ts, live, part, status, kQTimeoutNs,
+        Q2Args a{h, idx, count, static_cast<const uint8_t*>(w.w2t), w.w2ts, live, part, status, wait_timeout_ns(),
                  p.B, b0, nb, p.d, slots};
         cudaError_t e;
 #define PI_Q2(TBV)                                                       \

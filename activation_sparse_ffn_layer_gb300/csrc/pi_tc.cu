@@ -804,11 +804,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
             // every slot's last release has arrived before the CTA may exit
             for (int s = 0; s < C::S && s < it; ++s) {
                 const int last = s + ((it - 1 - s) / C::S) * C::S;
-                bar_drain(&empty[s], (last / C::S) & 1, a.timeout_ns);
+                bar_drain(&empty[s], (last / C::S) & 1, kDrainTimeoutNs);
             }
         } else {
             mma_commit(&drain);
-            bar_drain(&drain, 0, a.timeout_ns);
+            bar_drain(&drain, 0, kDrainTimeoutNs);
         }
     }
     tc_before();
@@ -1163,11 +1163,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fc2_tc(TcFc2Args a) {
         if (ok) {
             for (int s = 0; s < C::S && s < it; ++s) {
                 const int last = s + ((it - 1 - s) / C::S) * C::S;
-                bar_drain(&empty[s], (last / C::S) & 1, a.timeout_ns);
+                bar_drain(&empty[s], (last / C::S) & 1, kDrainTimeoutNs);
             }
         } else {
             mma_commit(&drain);
-            bar_drain(&drain, 0, a.timeout_ns);
+            bar_drain(&drain, 0, kDrainTimeoutNs);
         }
     }
     tc_before();
@@ -1206,7 +1206,6 @@ cudaError_t prep(K kernel, size_t smem) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 
-constexpr long long kTcTimeoutNs = 2000000000ll;
 
 }  // namespace
 
@@ -1286,7 +1285,7 @@ cudaError_t launch_predict_tc(const Plan& p, const __half* x, const __half* p1, 
     a.part = part;
     a.slots = slots_for(ceil_div(p.r, 128), Gu);
     a.status = status;
-    a.timeout_ns = kTcTimeoutNs;
+    a.timeout_ns = wait_timeout_ns();
     cudaError_t e = launch_rows_nt<2>(a, nt, Gu, s);
     if (e != cudaSuccess) return e;
     k_u_finish<<<ceil_div(p.r, 32), 32 * nt, 0, s>>>(part, a.slots, Gu, ceil_div(p.d, 64), p.r, p.B, nt, uhl);
@@ -1305,7 +1304,7 @@ cudaError_t launch_predict_tc(const Plan& p, const __half* x, const __half* p1, 
     b.mask = mask;
     b.W = p.W;
     b.status = status;
-    b.timeout_ns = kTcTimeoutNs;
+    b.timeout_ns = wait_timeout_ns();
     return launch_rows_nt<3>(b, nt, G, s);
 }
 
@@ -1327,7 +1326,7 @@ cudaError_t launch_fc1_tc(const Plan& p, const __half* x, const LayerPtrs& w, co
     a.part = part;
     a.slots = slots_for(ceil_div(p.F, 128), G);
     a.status = status;
-    a.timeout_ns = kTcTimeoutNs;
+    a.timeout_ns = wait_timeout_ns();
     cudaError_t e = p.gated ? launch_rows_nt<1>(a, nt, G, s) : launch_rows_nt<0>(a, nt, G, s);
     if (e != cudaSuccess) return e;
     const int blocks = ceil_div(p.F, 32);
@@ -1358,7 +1357,7 @@ cudaError_t launch_fc1_tc4(const Plan& p, const __half* x, const LayerPtrs& w, c
     a.part = part;
     a.slots = slots_for(ceil_div(p.F, 128), G);
     a.status = status;
-    a.timeout_ns = kTcTimeoutNs;
+    a.timeout_ns = wait_timeout_ns();
     cudaError_t e = launch_rows<4, 16>(a, G, s);
     if (e != cudaSuccess) return e;
     return launch_fc1_finish(p, nt, G, a.slots, p.d / 256, part, count, idx, w.b1, mask, h, live, s);
@@ -1391,7 +1390,7 @@ cudaError_t launch_fc2_tc(const Plan& p, const float* h, const int32_t* idx, con
     if (status == nullptr) return cudaErrorInvalidDevice;
     const int G = p.nsm, nt = tc_tokens(p);
     const int slots = slots_for(p.d / 128, G);
-    TcFc2Args a{h, idx, count, static_cast<const __half*>(w.w2t), live, partial, status, kTcTimeoutNs,
+    TcFc2Args a{h, idx, count, static_cast<const __half*>(w.w2t), live, partial, status, wait_timeout_ns(),
                 p.B, p.d, slots};
     cudaError_t e;
     if (nt == 16) {

@@ -1,13 +1,18 @@
 """Benchmark: sparse-FFN decode tokens/s at batch 1 on one GB300, with the
 achieved HBM bandwidth on the bytes the method must move.
 
-Default workload: the OPT-6.7B-shaped FFN stack (32 layers, d=4096, F=16384,
-predictor rank 256, Zipf(1.1) firing at 10%), one token per step through all
-32 layers (predictor -> compaction -> FC1 -> FC2, RMS normalisation between
-layers), inputs cycling over the run's 128 seeded tokens.  The 8.6 GB of
-layer weights read per step are far larger than L2, so no flush is needed.
+Default workload: the OPT-175B-shaped INT4 FFN stack at full depth (96 layers,
+d=12288, F=49152, predictor rank 1024, group-32 INT4 weights with fp16 scales,
+Zipf(1.1) firing at 6%), one token per step through all 96 layers (predictor
+-> compaction -> FC1 -> FC2, RMS normalisation between layers), inputs cycling
+over the run's 64 seeded tokens.  The 77 GB of layer weights read per step are
+far larger than L2, so no flush is needed.  After the headline, the other
+workloads are timed the same way at batch 1 and full depth (OPT-125M-shaped
+layer in rotation over copies larger than L2, OPT-6.7B-, OPT-30B- and
+LLaMA-70B-shaped stacks) and listed under "other_workloads", with the launch
+floor of the persistent kernel.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c2] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c5] [--impl ours|reference]
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
 instead (bounded sample of the same workload, scaled to tokens/s).
@@ -181,27 +186,31 @@ def recorded_traffic(config_key):
 
 # ------------------------------------------------------------------ our arm
 
-def run_ours(args):
+def step_bytes_of(cfg, layers, counts, B):
+    """Algorithmic bytes of each step of the run (list over steps)."""
+    L = len(layers)
+    per_step = []
+    for per in counts:
+        tot = 0
+        for l, (n, nz) in enumerate(per):
+            tot += layer_bytes(cfg, layers[l].r, n, nz, B)["total"]
+        tot += (L - 1) * B * (4 * cfg.d + 2 * cfg.d)   # inter-layer norm: read y, write x
+        per_step.append(tot)
+    return per_step
+
+
+def measure_stack(cfg, B, L, K, W, sample_clocks=True):
+    """Build a workload's stack on the GPU, count its algorithmic bytes
+    (untimed pass), capture one step as a CUDA graph and time K replays after
+    W warm-up replays.  Returns (result dict, objects for the e2e and CPU legs)."""
     import torch
-    import torch.distributed as dist
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl", init_method="env://")
-    torch.cuda.set_device(local)
-
-    import __graft_entry__
-    __graft_entry__.build()
-    import activation_sparse_ffn_layer_gb300 as P
     from activation_sparse_ffn_layer_gb300.runtime import DecodeStack
-    from synth import CONFIGS, make_layer, make_tokens
+    from synth import make_layer, make_tokens
 
-    cfg = CONFIGS[args.config]
-    B = args.batch
-    L = args.layers if args.layers else cfg.layers
+    t_gen = time.perf_counter()
     layers = [make_layer(cfg, l, device="cuda") for l in range(L)]
+    torch.cuda.synchronize()
+    t_gen = time.perf_counter() - t_gen
     NS = max(cfg.tokens // B, 4)          # distinct steps of B tokens, cycled
     T = NS * B
     tokens = make_tokens(cfg, 0, T, device="cuda")
@@ -216,33 +225,24 @@ def run_ours(args):
     stacks = [st] + [DecodeStack([clone_layer(w) for w in layers], batch=B, tau=cfg.tau, eps=cfg.rms_eps)
                      for _ in range(R - 1)]
 
-    # per-step algorithmic bytes (untimed)
     counts = measure_counts(st, tokens, B)
-    per_step = []
-    for per in counts:
-        tot = 0
-        for l, (n, nz) in enumerate(per):
-            tot += layer_bytes(cfg, layers[l].r, n, nz, B)["total"]
-        tot += (L - 1) * B * (4 * cfg.d + 2 * cfg.d)   # inter-layer norm: read y, write x
-        per_step.append(tot)
+    per_step = step_bytes_of(cfg, layers, counts, B)
     n_pred_mean = sum(n for per in counts for n, _ in per) / (NS * L)
     n_relu_mean = sum(z for per in counts for _, z in per) / (NS * L)
 
     for s_ in stacks:
         s_.capture()
     stream = torch.cuda.current_stream()
-    K, W = args.steps, args.warmup
     for i in range(max(W, R)):
         s_ = stacks[i % R]
         s_.x_in.copy_(tokens[(i % NS) * B:(i % NS + 1) * B])
         s_.replay()
     torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ka = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     kb = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    with ClockSampler(torch.cuda.current_device()) as clk:
+
+    def timed():
         torch.cuda.synchronize()
         e0.record(stream)
         for i in range(K):
@@ -254,13 +254,89 @@ def run_ours(args):
             kb[i].record(stream)
         e1.record(stream)
         torch.cuda.synchronize()
-    clocks = clk.summary()
+
+    clocks = None
+    if sample_clocks:
+        with ClockSampler(torch.cuda.current_device()) as clk:
+            timed()
+        clocks = clk.summary()
+    else:
+        timed()
     ms = e0.elapsed_time(e1)
     kernel_ms = sum(a.elapsed_time(b) for a, b in zip(ka, kb))
+    step_bytes = sum(per_step[(W + i) % NS] for i in range(K)) / K
+    res = dict(cfg=cfg, B=B, L=L, K=K, ms=ms, kernel_ms=kernel_ms, step_bytes=step_bytes,
+               n_pred=n_pred_mean, n_relu=n_relu_mean, weight_bytes=weight_bytes, R=R, T=T,
+               launches=st.launches_per_step(), clocks=clocks, gen_s=t_gen)
+    return res, (layers, st, tokens, stacks)
+
+
+def summary_line(res, peak):
+    """Compact per-workload figures for the extra-workload list."""
+    cfg, K, B = res["cfg"], res["K"], res["B"]
+    per_launch = res["kernel_ms"] / K
+    achieved = res["step_bytes"] / (per_launch / 1e3) / 1e9
+    return {"workload": f"{cfg.key}: {cfg.name}, batch {B}, {res['L']} layers per step",
+            "tokens_per_s": round(K * B / (res["ms"] / 1e3), 2), "us_per_step": round(res["ms"] / K * 1e3, 2),
+            "bytes_per_step": int(res["step_bytes"]), "achieved_gbs": round(achieved, 1),
+            "frac": round(achieved / peak, 4), "predicted_per_layer": round(res["n_pred"], 1),
+            "l2": ("inputs larger than L2" if res["R"] == 1 else
+                   f"{res['R']} copies of the stack in rotation, one per step"),
+            "steps": K}
+
+
+def launch_floor(K=200, W=20):
+    """Time of one graph-replayed step of the smallest stack the persistent
+    kernel takes (one layer, d = 256, F = 256, rank 8): the fixed cost of a
+    launch and its three grid barriers, with almost no bytes to move."""
+    import torch
+    from activation_sparse_ffn_layer_gb300.runtime import DecodeStack
+    from synth import CONFIGS, make_layer, make_tokens, small
+    cfg = small(CONFIGS["c1"], d=256, F=256, rank=8)
+    w = make_layer(cfg, 0, device="cuda")
+    st = DecodeStack([w], batch=1, tau=cfg.tau, eps=cfg.rms_eps)
+    st.x_in.copy_(make_tokens(cfg, 0, 1, device="cuda"))
+    st.capture()
+    for _ in range(W):
+        st.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        st.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return round(e0.elapsed_time(e1) / K * 1e3, 2)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from synth import CONFIGS
+
+    cfg = CONFIGS[args.config]
+    B = args.batch
+    L = args.layers if args.layers else cfg.layers
+    K, W = args.steps, args.warmup
+    if world > 1:
+        dist.barrier()
+    res, (layers, st, tokens, _stacks) = measure_stack(cfg, B, L, K, W)
+    ms = res["ms"]
     if world > 1:
         ms = max_over_ranks(ms, "cuda")
         dist.barrier()
-    step_bytes = sum(per_step[(W + i) % NS] for i in range(K)) / K
+    kernel_ms = res["kernel_ms"]
+    step_bytes = res["step_bytes"]
     tok_s = job_throughput(ms, K, B, world)
     peak, peak_kind = _peaks()
 
@@ -268,7 +344,7 @@ def run_ours(args):
     # only kernel); batch > 1: the per-step kernels of the graph, timed together
     per_launch = kernel_ms / K
     achieved = step_bytes / (per_launch / 1e3) / 1e9
-    fused = st.launches_per_step() == 1
+    fused = res["launches"] == 1
     traffic = recorded_traffic(cfg.key) if fused and B == 1 and L == cfg.layers else None
     roofline = {"kernel": "k_fused_stack (pi_ffn_stack)" if fused else "batched step (pi_ffn_stack graph)",
                 "bound": "hbm", "achieved": round(achieved, 1),
@@ -277,6 +353,7 @@ def run_ours(args):
                 "us_per_launch": round(per_launch * 1e3, 2), "share_of_step": round(kernel_ms / ms, 3)}
 
     e2e = time_e2e(st, tokens, K=min(K, 512), W=W, B=B)
+    weight_bytes, R, T = res["weight_bytes"], res["R"], res["T"]
     out = {
         "metric": METRIC, "value": round(tok_s, 2), "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": round(ms / K, 5), "higher_is_better": True, "scaling": "weak",
@@ -291,15 +368,31 @@ def run_ours(args):
         "achieved_gbs_step": round(step_bytes / (ms / K / 1e3) / 1e9, 1),
         "frac_step": round(step_bytes / (ms / K / 1e3) / 1e9 / peak, 4),
         "bytes_per_step": int(step_bytes),
-        "active": {"predicted_per_layer": round(n_pred_mean, 1), "relu_nonzero_per_layer": round(n_relu_mean, 1),
+        "active": {"predicted_per_layer": round(res["n_pred"], 1), "relu_nonzero_per_layer": round(res["n_relu"], 1),
                    "F": cfg.F},
         "roofline": roofline,
         "e2e": e2e,
-        "gpu_launches": K * st.launches_per_step(),
-        "clocks": clocks,
+        "gpu_launches": K * res["launches"],
+        "clocks": res["clocks"],
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(cfg, layers, st, tokens, budget_s=args.cpu_seconds)
+    if rank == 0 and world == 1 and B == 1 and not args.no_extras:
+        # the other workloads at batch 1 and full depth, each timed the same way
+        del layers, st, tokens, _stacks
+        torch.cuda.empty_cache()
+        extras = []
+        for key in args.extras.split(","):
+            if not key or key == cfg.key:
+                continue
+            ec = CONFIGS[key]
+            r_, objs = measure_stack(ec, 1, ec.layers, min(K, args.extra_steps) if ec.layers > 1 else
+                                     max(K, 200), W, sample_clocks=False)
+            extras.append(summary_line(r_, peak))
+            del objs
+            torch.cuda.empty_cache()
+        out["other_workloads"] = extras
+        out["launch_floor_us"] = launch_floor()
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
@@ -440,15 +533,18 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=4096)
+    ap.add_argument("--steps", type=int, default=256)
     ap.add_argument("--warmup", type=int, default=8)
-    ap.add_argument("--config", default="c2")
+    ap.add_argument("--config", default="c5")
     ap.add_argument("--batch", type=int, default=1, help="tokens per step (the headline workload is 1)")
     ap.add_argument("--layers", type=int, default=0, help="layers of the stack (0: the workload's own)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="time the headline workload only")
+    ap.add_argument("--extras", default="c1,c2,c3,c4", help="other batch-1 workloads timed after the headline")
+    ap.add_argument("--extra-steps", type=int, default=64)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -253,6 +253,17 @@ PI_API const char *pi_status_string(pi_status s);
  * by bounded device-side waits (PI_OK or PI_ERR_TIMEOUT). */
 PI_API pi_status pi_last_device_status(void *stream);
 
+/* Diagnostics: sets the limit of the bounded device-side waits of the launches
+ * that follow (grid barriers and copy/MMA stage waits; 1 ns .. 10 s; 0 restores
+ * the default 2 s).  Process-wide, for every device.  A short limit makes the
+ * kernels take their failure path: the wait gives up, the device status
+ * becomes PI_ERR_TIMEOUT, the block waits (always up to 2 s) for its own copies
+ * and tensor-core operations in flight, frees its tensor memory and returns.
+ * For testing that path; outputs of a call that timed out are undefined, and
+ * a workspace used by pi_ffn_layer or pi_ffn_stack must be zero-filled again
+ * before its next use. */
+PI_API pi_status pi_debug_set_wait_timeout(long long timeout_ns);
+
 /* Diagnostics: launches one wait on a word that nothing writes, bounded by
  * timeout_ns (1 ns .. 10 s).  The wait gives up, and the device status becomes
  * PI_ERR_TIMEOUT (read it with pi_last_device_status); the GPU context stays

@@ -139,3 +139,82 @@ def test_layer_counts_match_last_layer_workspace():
     assert cnt.shape == (3, 2)
     assert cnt[2, 0] == n and cnt[2, 1] == int((h != 0).sum())
     assert np.all(cnt[:, 1] <= cnt[:, 0]) and np.all(cnt[:, 0] > 0)
+
+
+def test_grid_barrier_wait_runs_out_and_next_step_matches_oracle():
+    """The persistent kernel's own grid barrier runs out.  The workspace's
+    barrier epoch is pushed far ahead of the arrival counter (a host-side
+    change of the caller-owned workspace), so the first barrier's target is
+    never reached; with a 5 ms wait limit every block gives up, the device
+    status reads PI_ERR_TIMEOUT and the context stays usable.  After the
+    workspace is zero-filled again the next step matches the oracle."""
+    import time
+    P = _pi()
+    from activation_sparse_ffn_layer_gb300.runtime import DecodeStack
+    cfg = small(CONFIGS["c2"], d=1024, F=4096, rank=64)
+    ws = [make_layer(cfg, l, device=DEV) for l in range(2)]
+    st = DecodeStack(ws, batch=1, tau=cfg.tau, eps=cfg.rms_eps)
+    x = make_tokens(cfg, 0, 1, device=DEV)
+    y0 = st.step(x).clone()
+    torch.cuda.synchronize()
+    assert P.pi_last_device_status() == 0
+    epoch = st.workspace[0:8].view(torch.int64)
+    epoch += 1000                               # 1000 barriers that never happened
+    P.pi_debug_set_wait_timeout(5_000_000)
+    try:
+        t0 = time.perf_counter()
+        st.step(x)
+        torch.cuda.synchronize()
+        elapsed = time.perf_counter() - t0
+    finally:
+        P.pi_debug_set_wait_timeout(0)
+    assert P.pi_last_device_status() == 4       # PI_ERR_TIMEOUT, then cleared
+    assert P.pi_last_device_status() == 0
+    assert elapsed < 1.0, f"the barrier gave up after {elapsed:.3f} s, not after its 5 ms limit"
+    st.workspace.zero_()
+    xs, y1 = st.step_trace(x)
+    torch.cuda.synchronize()
+    assert P.pi_last_device_status() == 0
+    assert torch.equal(y1, y0)
+    host = oracle.host_layer(ws[1].to("cpu"))
+    close(y1[0].cpu().numpy(), oracle.ffn_masked(xs[1][0].cpu(), host, _mask_of(P, st)), "step after timeout")
+
+
+def test_tensor_core_stage_wait_runs_out_and_frees_tensor_memory():
+    """A tcgen05 row kernel (batched FC1, 16 tokens) whose stage waits run out:
+    with a 1 ns wait limit the first wait that is not already satisfied gives
+    up, the block drains its own copies and MMAs, frees its tensor memory and
+    returns, and the status reads PI_ERR_TIMEOUT.  The same call afterwards
+    (which allocates tensor memory on every SM again) gives the bits of a
+    clean run."""
+    P = _pi()
+    cfg = small(CONFIGS["c3"], d=1024, F=4096, rank=64)
+    B = 16
+    w = make_layer(cfg, 0, device=DEV)
+    x = make_tokens(cfg, 0, B, device=DEV)
+    desc = P.layer_desc(w, B)
+    wsb = torch.zeros(P.pi_workspace_bytes(desc), dtype=torch.uint8, device=DEV)
+    mask = torch.zeros(B, (w.F + 31) // 32, dtype=torch.int32, device=DEV)
+    P.pi_predict(desc, x, w.p1, w.p2, w.b1, cfg.tau, mask, wsb)
+    idx = torch.zeros(w.F, dtype=torch.int32, device=DEV)
+    cnt = torch.zeros(1, dtype=torch.int32, device=DEV)
+    P.pi_compact(desc, mask, None, idx, None, cnt)
+    wsx = P.weights_struct(w)
+    h_ref = torch.zeros(w.F * B, dtype=torch.float32, device=DEV)
+    P.pi_sparse_fc1(desc, x, wsx, idx, cnt, mask, h_ref, wsb)
+    torch.cuda.synchronize()
+    assert P.pi_last_device_status() == 0
+    h_bad = torch.zeros_like(h_ref)
+    P.pi_debug_set_wait_timeout(1)
+    try:
+        P.pi_sparse_fc1(desc, x, wsx, idx, cnt, mask, h_bad, wsb)
+        torch.cuda.synchronize()
+    finally:
+        P.pi_debug_set_wait_timeout(0)
+    assert P.pi_last_device_status() == 4
+    for _ in range(3):
+        h = torch.zeros_like(h_ref)
+        P.pi_sparse_fc1(desc, x, wsx, idx, cnt, mask, h, wsb)
+        torch.cuda.synchronize()
+        assert P.pi_last_device_status() == 0
+        assert torch.equal(h, h_ref)
