@@ -189,7 +189,7 @@ struct FusedParams {
     FusedLayer layers[kMaxFusedLayers];
 };
 
-// Dynamic smem layout (bytes): xf float[d] | u float[rmax] | ustage float[usmax]
+// Dynamic smem layout (bytes): x half[d] | u float[rmax] | ustage float[usmax]
 //   | scratch | m16 int[M] | upre int[M+1] | lidx int[cap] | lh float[cap]
 //   | P1 slice | P2 slice | bias slice   (the last three only with pred_smem)
 // lidx / lh hold this CTA's own active rows from the end of its mask units to
@@ -201,7 +201,7 @@ struct SmemPlan {
     int p1s = 0, p2s = 0, b1s = 0;  // shared predictor buffers (bytes, 16-aligned), 0 if unused
     int stage = 0;                  // staging region (bytes, 16-aligned): the predictor buffers
                                     // up to the mask bits, then the ring of this CTA's FC rows
-    __host__ __device__ int off_u() const { return d * 4; }
+    __host__ __device__ int off_u() const { return ((d * 2 + 15) / 16) * 16; }
     __host__ __device__ int off_ust() const { return off_u() + rmax * 4; }
     __host__ __device__ int off_scr() const { return ((off_ust() + ((usmax + 3) / 4) * 16 + 15) / 16) * 16; }
     __host__ __device__ int off_m16() const { return off_scr() + 4096 * 4; }
@@ -215,49 +215,51 @@ struct SmemPlan {
     __host__ __device__ int bytes() const { return off_stage() + stage; }
 };
 
-// dot of 8 fp16 weights with 8 fp32 values in registers
-PI_DEV float dot8r(const uint4& w, const float4& xa, const float4& xb) {
-    float wf[8];
-    h8_to_f8(w, wf);
-    float acc = wf[0] * xa.x;
-    acc = fmaf(wf[1], xa.y, acc);
-    acc = fmaf(wf[2], xa.z, acc);
-    acc = fmaf(wf[3], xa.w, acc);
-    acc = fmaf(wf[4], xb.x, acc);
-    acc = fmaf(wf[5], xb.y, acc);
-    acc = fmaf(wf[6], xb.z, acc);
-    acc = fmaf(wf[7], xb.w, acc);
+// f32 result of a*b + c for binary16 a and b (the low 16 bits of a16, b16):
+// the product is exact, so this equals fmaf on the values widened to fp32.
+PI_DEV float fma_h(uint32_t a16, uint32_t b16, float c) {
+    float d;
+    const unsigned short a = (unsigned short)a16, b = (unsigned short)b16;
+    asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
+    return d;
+}
+// dot of 8 fp16 weights with 8 fp16 x values: exact products summed in
+// element order in fp32, with no conversion instructions
+PI_DEV float dot8hh(const uint4& w, const uint4& x) {
+    float acc = fma_h(w.x, x.x, -0.f);
+    acc = fma_h(w.x >> 16, x.x >> 16, acc);
+    acc = fma_h(w.y, x.y, acc);
+    acc = fma_h(w.y >> 16, x.y >> 16, acc);
+    acc = fma_h(w.z, x.z, acc);
+    acc = fma_h(w.z >> 16, x.z >> 16, acc);
+    acc = fma_h(w.w, x.w, acc);
+    acc = fma_h(w.w >> 16, x.w >> 16, acc);
     return acc;
 }
-// dot of 8 INT4 codes with 8 fp32 values in registers
-PI_DEV float dotq8r(uint32_t cw, const float4& xa, const float4& xb) {
-    float qf[8];
-    q8_to_f8(cw, qf);
-    float acc = qf[0] * xa.x;
-    acc = fmaf(qf[1], xa.y, acc);
-    acc = fmaf(qf[2], xa.z, acc);
-    acc = fmaf(qf[3], xa.w, acc);
-    acc = fmaf(qf[4], xb.x, acc);
-    acc = fmaf(qf[5], xb.y, acc);
-    acc = fmaf(qf[6], xb.z, acc);
-    acc = fmaf(qf[7], xb.w, acc);
-    return acc;
-}
-
-// dot of 8 fp16 weights with 8 fp32 values in smem
-PI_DEV float dot8(const uint4& w, const float* xs) {
-    float wf[8];
-    h8_to_f8(w, wf);
-    const float4 a = reinterpret_cast<const float4*>(xs)[0];
-    const float4 b = reinterpret_cast<const float4*>(xs)[1];
-    float acc = wf[0] * a.x;
-    acc = fmaf(wf[1], a.y, acc);
-    acc = fmaf(wf[2], a.z, acc);
-    acc = fmaf(wf[3], a.w, acc);
-    acc = fmaf(wf[4], b.x, acc);
-    acc = fmaf(wf[5], b.y, acc);
-    acc = fmaf(wf[6], b.z, acc);
-    acc = fmaf(wf[7], b.w, acc);
+// dot of 8 INT4 codes (element e in bits 4e..4e+3, two's complement) with 8
+// fp16 x values.  A code pair becomes exact fp16 integers without
+// conversions: with n = q + 8, the half 0x6400 | n holds 1024 + n, and one
+// half-precision subtraction of 1032 leaves q.  The pairs are elements
+// (e, e + 4), which sit 16 bits apart in the word; the products are summed in
+// element order.
+PI_DEV float dotq8h(uint32_t cw, const uint4& x) {
+    const uint32_t u = cw ^ 0x88888888u;
+    const __half2 k = __halves2half2(__ushort_as_half((unsigned short)0x6408u), __ushort_as_half((unsigned short)0x6408u));
+    uint32_t q[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t m = ((u >> (4 * i)) & 0x000F000Fu) | 0x64006400u;
+        const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&m), k);
+        q[i] = *reinterpret_cast<const uint32_t*>(&v);
+    }
+    float acc = fma_h(q[0], x.x, -0.f);         // element 0
+    acc = fma_h(q[1], x.x >> 16, acc);           // 1
+    acc = fma_h(q[2], x.y, acc);                 // 2
+    acc = fma_h(q[3], x.y >> 16, acc);           // 3
+    acc = fma_h(q[0] >> 16, x.z, acc);           // 4
+    acc = fma_h(q[1] >> 16, x.z >> 16, acc);     // 5
+    acc = fma_h(q[2] >> 16, x.w, acc);           // 6
+    acc = fma_h(q[3] >> 16, x.w >> 16, acc);     // 7
     return acc;
 }
 
@@ -357,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
     sp.p2s = p.pred_smem ? p.p2s_bytes : 0;
     sp.b1s = p.pred_smem ? p.b1s_bytes : 0;
     sp.stage = p.stage_bytes;
-    float* xf = reinterpret_cast<float*>(smem);
+    __half* xh = reinterpret_cast<__half*>(smem);   // the layer input, exactly fp16
     float* us = reinterpret_cast<float*>(smem + sp.off_u());
     float* ust = reinterpret_cast<float*>(smem + sp.off_ust());
     uint16_t* m16 = reinterpret_cast<uint16_t*>(smem + sp.off_m16());
@@ -417,16 +419,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
     // status word reports the failure)
     int inflight = -1;   // layer whose predictor copy is issued but not yet waited for
     auto leave = [&]() {
-        if (inflight >= 0) mbar_drain(&pred_mbar, (unsigned)(inflight & 1), tmo);
+        if (inflight >= 0) mbar_drain(&pred_mbar, (unsigned)(inflight & 1), kDrainTimeoutNs);
         for (int q = 0; q < ns; ++q)
-            if (ring_uses[q] > 0) mbar_drain(&ring_full[q], (unsigned)((ring_uses[q] - 1) & 1), tmo);
+            if (ring_uses[q] > 0) mbar_drain(&ring_full[q], (unsigned)((ring_uses[q] - 1) & 1), kDrainTimeoutNs);
         if (w12_pending) {
-            mbar_drain(&w1_mbar, (w12_uses - 1) & 1u, tmo);
-            mbar_drain(&w2_mbar, (w12_uses - 1) & 1u, tmo);
+            mbar_drain(&w1_mbar, (w12_uses - 1) & 1u, kDrainTimeoutNs);
+            mbar_drain(&w2_mbar, (w12_uses - 1) & 1u, kDrainTimeoutNs);
         }
         // the last copy issued into each FC row slot
         const unsigned S = (unsigned)p.fc_slots;
-        for (unsigned g = fc_hi > S ? fc_hi - S : 0u; g < fc_hi; ++g) mbar_drain(&fc_full[g % S], (g / S) & 1u, tmo);
+        for (unsigned g = fc_hi > S ? fc_hi - S : 0u; g < fc_hi; ++g) mbar_drain(&fc_full[g % S], (g / S) & 1u, kDrainTimeoutNs);
         if (c == 0 && tid == 0) {
             const unsigned long long next = ebase + (unsigned long long)kBarriersPerLayer * p.L;
             __stcg(p.epoch, next);
@@ -522,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
 
         // ---------------------------------------------------------- phase A
         if (l == 0) {
-            for (int i = tid; i < d; i += kThreads) xf[i] = __half2float(p.x_in[i]);
+            for (int i = tid; i < d; i += kThreads) xh[i] = p.x_in[i];
         } else {
             constexpr int NY = 2 * NCH;   // d <= NCH * kCols: at most 2*NCH float4 of y per thread
             float4 yv[NY];
@@ -542,8 +544,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
             auto put_x = [&](int i4, const float4& y4) {
                 const __half h0 = __float2half_rn(y4.x * rs), h1 = __float2half_rn(y4.y * rs);
                 const __half h2 = __float2half_rn(y4.z * rs), h3 = __float2half_rn(y4.w * rs);
-                reinterpret_cast<float4*>(xf)[i4] =
-                    make_float4(__half2float(h0), __half2float(h1), __half2float(h2), __half2float(h3));
+                reinterpret_cast<uint2*>(xh)[i4] =
+                    make_uint2((uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16),
+                               (uint32_t)__half_as_ushort(h2) | ((uint32_t)__half_as_ushort(h3) << 16));
                 if (p.x_trace && c == 0) {
                     __half* xt = p.x_trace + (size_t)(l - 1) * d + i4 * 4;
                     xt[0] = h0;
@@ -576,10 +579,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                 if (p.pred_smem) {
 #pragma unroll 4
                     for (int e = c0 + lane * 8; e < c1; e += 256)
-                        acc += dot8(*reinterpret_cast<const uint4*>(row + e), xf + e);
+                        acc += dot8hh(*reinterpret_cast<const uint4*>(row + e), *reinterpret_cast<const uint4*>(xh + e));
                 } else {
 #pragma unroll 8
-                    for (int e = c0 + lane * 8; e < c1; e += 256) acc += dot8(ld_stream16(row + e), xf + e);
+                    for (int e = c0 + lane * 8; e < c1; e += 256)
+                        acc += dot8hh(ld_stream16(row + e), *reinterpret_cast<const uint4*>(xh + e));
                 }
                 acc = warp_sum(acc);
                 if (lane == 0) p.xu[(size_t)sg * r + i] = acc;
@@ -903,20 +907,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
 #pragma unroll
                     for (int b = 0; b < RB; ++b) v[b] = vu[b] = 0.f;
                     for (int wd = tid; wd < nwd; wd += kThreads) {
-                        const float4 xa = reinterpret_cast<const float4*>(xf)[2 * wd];
-                        const float4 xb = reinterpret_cast<const float4*>(xf)[2 * wd + 1];
+                        const uint4 xv = reinterpret_cast<const uint4*>(xh)[wd];
 #pragma unroll
                         for (int b = 0; b < RB; ++b) {
                             const int q = q0 + b;
                             if (q >= q1) break;
                             const unsigned char* row = rw[b];
                             if (KIND != 2) {
-                                v[b] += dot8r(reinterpret_cast<const uint4*>(row)[wd], xa, xb);
-                                if (KIND == 1) vu[b] += dot8r(reinterpret_cast<const uint4*>(ru[b])[wd], xa, xb);
+                                v[b] += dot8hh(reinterpret_cast<const uint4*>(row)[wd], xv);
+                                if (KIND == 1) vu[b] += dot8hh(reinterpret_cast<const uint4*>(ru[b])[wd], xv);
                             } else {
                                 const uint32_t cw = reinterpret_cast<const uint32_t*>(row)[wd];
                                 const float sc = __half2float(reinterpret_cast<const __half*>(row + d / 2)[wd >> 2]);
-                                v[b] = fmaf(sc, dotq8r(cw, xa, xb), v[b]);
+                                v[b] = fmaf(sc, dotq8h(cw, xv), v[b]);
                             }
                         }
                     }
