@@ -49,6 +49,28 @@ PI_DEV void q8_to_f8(uint32_t w, float (&f)[8]) {
         f[e] = __uint_as_float(((u >> (4 * e)) & 0xFu) | 0x4B000000u) - 8388616.0f;
 }
 
+// Halving butterfly over a warp for 16 rows: v[k] is this lane's partial sum
+// of row k.  After the step with offset o a lane keeps the half of its values
+// selected by its bit o and adds the partner's copy of them, so on return
+// lanes L and L ^ 1 hold the warp's total of row fold16_row(L) (a fixed order:
+// 16 shuffles for 16 rows).
+PI_DEV int fold16_row(int lane) {
+    return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+}
+PI_DEV float fold16(float (&v)[16], int lane) {
+#pragma unroll
+    for (int n = 8, o = 16; n >= 1; n /= 2, o /= 2) {
+        const bool hi = lane & o;
+#pragma unroll
+        for (int k = 0; k < n; ++k) {
+            const float send = hi ? v[k] : v[k + n];
+            const float keep = hi ? v[k + n] : v[k];
+            v[k] = keep + __shfl_xor_sync(FULL, send, o);
+        }
+    }
+    return v[0] + __shfl_xor_sync(FULL, v[0], 1);
+}
+
 PI_DEV float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL, v, o);

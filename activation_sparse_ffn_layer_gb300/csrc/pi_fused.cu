@@ -317,7 +317,7 @@ PI_DEV int block_exscan(int v, int* scr, int* total) {
 
 #ifdef PI_PHASE_TRACE
 // Phase timestamps of every CTA: [layer][slot][cta] globaltimer ns and clock64.
-constexpr int kTraceSlots = 8;
+constexpr int kTraceSlots = 16;
 constexpr int kTraceCtas = 256;
 __device__ unsigned long long g_pi_trace[96 * kTraceSlots * kTraceCtas];
 __device__ unsigned long long g_pi_trace_clk[96 * kTraceSlots * kTraceCtas];
@@ -526,7 +526,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
         if (l == 0) {
             for (int i = tid; i < d; i += kThreads) xh[i] = p.x_in[i];
         } else {
-            constexpr int NY = 2 * NCH;   // d <= NCH * kCols: at most 2*NCH float4 of y per thread
+            // float4 of y per thread, all requested at once: fp16 rows have
+            // d <= NCH * kCols (2 NCH of them); INT4 rows to d = 12288 (wider ones loop)
+            constexpr int NY = KIND == 2 ? 12 : 2 * NCH;
             float4 yv[NY];
 #pragma unroll
             for (int b = 0; b < NY; ++b) {
@@ -589,6 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                 if (lane == 0) p.xu[(size_t)sg * r + i] = acc;
             }
         }
+        PI_STAMP(l, 8);
         if (!sync()) { leave(); return; }
         PI_STAMP(l, 2);
 
@@ -598,6 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
             for (int w4 = tid; w4 < nw / 4; w4 += kThreads)
                 reinterpret_cast<float4*>(ust)[w4] = ld_cg4(p.xu + w4 * 4);
             __syncthreads();
+            PI_STAMP(l, 9);
             for (int i = tid; i < r; i += kThreads) {
                 float acc = 0.f;
                 for (int s = 0; s < ly.su; ++s) acc += ust[s * r + i];
@@ -605,6 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
             }
         }
         __syncthreads();
+        PI_STAMP(l, 10);
         {
             const int nvec = r / 8;
             const int vpl = (nvec + 31) / 32;
@@ -772,8 +777,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
             }
         }
         __syncthreads();
+        if (p.layer_counts && tid == 0 && nmine_s) atomicAdd(p.layer_counts + 2 * l, nmine_s);
         const int nmine = nmine_s;
-        if (p.layer_counts && tid == 0 && nmine) atomicAdd(p.layer_counts + 2 * l, nmine);
+        PI_STAMP(l, 12);
         // FC rows stream through a ring of S row slots in the staging region
         // (which held this layer's predictor slices or P2 ring, read by now):
         // the sequence is this CTA's FC1 rows (gated: gate and up row of each
@@ -864,6 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
         // FC1 rows first (spread over the warps on their own, so they are queued first)
         issue_range(0, min(issued, fc1n));
         issue_range(fc1n, issued);
+        PI_STAMP(l, 13);
         // after a batch ending at element e has been read by every thread (ring mode)
         auto refill = [&](int e) {
             const int hi = min(T, e + S);
@@ -1097,28 +1104,87 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
 
         // ---------------------------------------------------------- phase D
         {
-            // this CTA's ngm 4-column groups: one warp per group, lanes over the
-            // G partials (q = lane, lane+32, ...), then a fixed xor-tree
-            float ss_local = 0.f;
-            for (int gi = warp; gi < ngm; gi += kWarps) {
-                const int col = (g0 + gi) * 4;
-                // b2 of the 4 columns, requested before the partials
-                __half b2v[4];
+            // this CTA's ngm 4-column groups, gpw = 32 / lpg at a time: the lpg
+            // lanes of a group in warp w add the partial rows q = lpg w + sub,
+            // + lpg kWarps, ... (a warp's loads of one row are consecutive 16-byte
+            // words), every load of a lane in flight at once (lpg grows when a
+            // CTA has few groups, so the rows per lane stay few); the lanes of a
+            // group are then combined by a fixed xor order, the warps' sums in
+            // warp order, and b2 added last
+            float4* red4 = reinterpret_cast<float4*>(red);   // [kWarps][gpw]
+            const int lpg = ngm <= 16 ? 2 : 1;
+            const int gpw = 32 / lpg;
+            float ss_local = 0.f;   // warp 0, lane L < gpw: squares of its groups, in chunk order
+            // with at most one group per warp, a warp takes a group with its lanes
+            // over all G partial rows (one round of loads, a fixed xor-tree)
+            if (ngm <= kWarps) {
+                if (warp < ngm) {
+                    const int col = (g0 + warp) * 4;
+                    __half b2v[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) b2v[e] = lane == 0 ? __ldg(ly.b2 + col + e) : __float2half(0.f);
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                constexpr int NB = 8;
-                for (int q0 = lane; q0 < G; q0 += NB * 32) {
-                    float4 v[NB];
+                    for (int e = 0; e < 4; ++e) b2v[e] = lane == 0 ? __ldg(ly.b2 + col + e) : __float2half(0.f);
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    constexpr int NB = 5;   // one round for up to 160 partial rows
+                    for (int q0 = lane; q0 < G; q0 += NB * 32) {
+                        float4 v[NB];
 #pragma unroll
-                    for (int b = 0; b < NB; ++b) {
-                        const int q = q0 + b * 32;
-                        if (q < G) v[b] = ld_cg4(p.xyp + (size_t)q * d + col);
+                        for (int b = 0; b < NB; ++b) {
+                            const int q = q0 + b * 32;
+                            if (q < G) v[b] = ld_cg4(p.xyp + (size_t)q * d + col);
+                        }
+#pragma unroll
+                        for (int b = 0; b < NB; ++b) {
+                            const int q = q0 + b * 32;
+                            if (q < G) {
+                                acc.x += v[b].x;
+                                acc.y += v[b].y;
+                                acc.z += v[b].z;
+                                acc.w += v[b].w;
+                            }
+                        }
                     }
 #pragma unroll
-                    for (int b = 0; b < NB; ++b) {
-                        const int q = q0 + b * 32;
-                        if (q < G) {
+                    for (int o = 16; o > 0; o >>= 1) {
+                        acc.x += __shfl_xor_sync(FULL, acc.x, o);
+                        acc.y += __shfl_xor_sync(FULL, acc.y, o);
+                        acc.z += __shfl_xor_sync(FULL, acc.z, o);
+                        acc.w += __shfl_xor_sync(FULL, acc.w, o);
+                    }
+                    if (lane == 0) {
+                        const float4 yv = make_float4(acc.x + __half2float(b2v[0]), acc.y + __half2float(b2v[1]),
+                                                      acc.z + __half2float(b2v[2]), acc.w + __half2float(b2v[3]));
+                        __stcg(reinterpret_cast<float4*>(p.xy + col), yv);
+                        if (l == p.L - 1) *reinterpret_cast<float4*>(p.y_out + col) = yv;
+                        red[kWarps * 32 + warp] = yv.x * yv.x + yv.y * yv.y + yv.z * yv.z + yv.w * yv.w;
+                    }
+                }
+                __syncthreads();
+                if (warp == 0 && lane < ngm) ss_local = red[kWarps * 32 + lane];
+            }
+            for (int gc = 0; gc < ngm && ngm > kWarps; gc += gpw) {
+                const int gl = lane / lpg, sub = lane % lpg;
+                const bool ok = gc + gl < ngm;
+                const int col = (g0 + (ok ? gc + gl : gc)) * 4;
+                // b2 of the group that lane L of warp 0 finishes, requested before the partials
+                const bool fin = warp == 0 && lane < gpw && gc + lane < ngm;
+                const int fcol = (g0 + gc + (fin ? lane : 0)) * 4;
+                __half b2v[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) b2v[e] = fin ? __ldg(ly.b2 + fcol + e) : __float2half(0.f);
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                constexpr int QB = 10;
+                const int qstep = kWarps * lpg;
+                for (int q0 = warp * lpg + sub; q0 < G; q0 += QB * qstep) {
+                    float4 v[QB];
+#pragma unroll
+                    for (int b = 0; b < QB; ++b) {
+                        const int q = q0 + b * qstep;
+                        if (ok && q < G) v[b] = ld_cg4(p.xyp + (size_t)q * d + col);
+                    }
+#pragma unroll
+                    for (int b = 0; b < QB; ++b) {
+                        const int q = q0 + b * qstep;
+                        if (ok && q < G) {
                             acc.x += v[b].x;
                             acc.y += v[b].y;
                             acc.z += v[b].z;
@@ -1126,30 +1192,37 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                         }
                     }
                 }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
+                for (int o = 1; o < lpg; o <<= 1) {
                     acc.x += __shfl_xor_sync(FULL, acc.x, o);
                     acc.y += __shfl_xor_sync(FULL, acc.y, o);
                     acc.z += __shfl_xor_sync(FULL, acc.z, o);
                     acc.w += __shfl_xor_sync(FULL, acc.w, o);
                 }
-                if (lane == 0) {
-                    const float4 yv = make_float4(acc.x + __half2float(b2v[0]), acc.y + __half2float(b2v[1]),
-                                                  acc.z + __half2float(b2v[2]), acc.w + __half2float(b2v[3]));
-                    __stcg(reinterpret_cast<float4*>(p.xy + col), yv);
-                    if (l == p.L - 1) *reinterpret_cast<float4*>(p.y_out + col) = yv;
+                if (sub == 0) red4[warp * gpw + gl] = acc;
+                __syncthreads();
+                if (fin) {
+                    float4 yv = red4[lane];
+                    for (int w = 1; w < kWarps; ++w) {
+                        const float4 t = red4[w * gpw + lane];
+                        yv.x += t.x;
+                        yv.y += t.y;
+                        yv.z += t.z;
+                        yv.w += t.w;
+                    }
+                    yv.x += __half2float(b2v[0]);
+                    yv.y += __half2float(b2v[1]);
+                    yv.z += __half2float(b2v[2]);
+                    yv.w += __half2float(b2v[3]);
+                    __stcg(reinterpret_cast<float4*>(p.xy + fcol), yv);
+                    if (l == p.L - 1) *reinterpret_cast<float4*>(p.y_out + fcol) = yv;
                     ss_local += yv.x * yv.x + yv.y * yv.y + yv.z * yv.z + yv.w * yv.w;
                 }
+                __syncthreads();   // red4 is reused by the next chunk
             }
-            if (l + 1 < p.L) {
+            if (l + 1 < p.L && warp == 0) {
                 // fixed-order sum of squares of this CTA's columns
-                if (lane == 0) red[warp] = ss_local;
-                __syncthreads();
-                if (tid == 0) {
-                    float t = 0.f;
-                    for (int w = 0; w < kWarps; ++w) t += red[w];
-                    __stcg(p.xss + c, t);
-                }
+                const float t = warp_sum(ss_local);
+                if (lane == 0) __stcg(p.xss + c, t);
             }
         }
         if (l == p.L - 1) {
@@ -1223,10 +1296,13 @@ cudaError_t launch_kind(const FusedParams& prm, int G, size_t smem, cudaStream_t
 
 size_t up256(size_t v) { return (v + 255) / 256 * 256; }
 
+// own units (two 8-row pieces) of a CTA at most
+int max_units(int F, int G) { return ((F + 7) / 8 + 2 * G - 1) / (2 * G); }
+
 // exchange region: epoch | counter | xu | xyp | xy | xss
 struct XchgLayout {
     size_t counter, xu, xyp, xy, xss, total;
-    XchgLayout(int d, size_t rmax_su, int G) {
+    XchgLayout(int d, int F, size_t rmax_su, int G) {
         size_t off = 256;
         counter = off;
         off += 256;
@@ -1242,16 +1318,13 @@ struct XchgLayout {
     }
 };
 
-// own units (two 8-row pieces) of a CTA at most
-int max_units(int F, int G) { return ((F + 7) / 8 + 2 * G - 1) / (2 * G); }
-
 SmemPlan smem_plan(int d, int F, int rmax, size_t rmax_su, int G) {
     return SmemPlan{d, rmax < 8 ? 8 : rmax, (int)rmax_su, (F + 15) / 16, 16 * max_units(F, G)};
 }
 
 }  // namespace
 
-size_t fused_workspace_bytes(int d, int F, size_t rmax_su, int G) { return XchgLayout(d, rmax_su, G).total; }
+size_t fused_workspace_bytes(int d, int F, size_t rmax_su, int G) { return XchgLayout(d, F, rmax_su, G).total; }
 
 // FC row slots of the staging region: at least two batches of one neuron's rows
 int fc_slots_for(int d, bool int4, int stage_bytes) {
@@ -1299,7 +1372,10 @@ static bool plan_fused(const FusedStackArgs& a, FusedParams* out, size_t* smem_o
         if ((size_t)f.su * f.r > a.rmax_su) return false;
         rmax = f.r > rmax ? f.r : rmax;
     }
-    SmemPlan sp = smem_plan(a.d, a.F, rmax, a.rmax_su, G);
+    // the u-partial staging buffer as the kernel sizes it: the largest r * su
+    size_t usmax = 8;
+    for (int l = 0; l < a.L; ++l) usmax = std::max(usmax, (size_t)prm.layers[l].r * prm.layers[l].su);
+    SmemPlan sp = smem_plan(a.d, a.F, rmax, usmax, G);
     // shared predictor slices when they fit: P1 items, P2 units and bias of one CTA
     {
         size_t p1b = 16;
@@ -1370,7 +1446,7 @@ cudaError_t launch_fused(const FusedStackArgs& a, cudaStream_t s) {
     prm.x_in = a.x_in;
     prm.y_out = a.y_out;
     prm.x_trace = a.x_trace;
-    const XchgLayout xl(a.d, a.rmax_su, G);
+    const XchgLayout xl(a.d, a.F, a.rmax_su, G);
     char* ws = static_cast<char*>(a.xchg);
     prm.epoch = reinterpret_cast<unsigned long long*>(ws);
     prm.counter = reinterpret_cast<unsigned*>(ws + xl.counter);

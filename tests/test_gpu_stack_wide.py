@@ -9,8 +9,9 @@ and a block whose predicted neurons need more FC rows than it has row slots
 streams them through a ring whose position carries over from one layer to the
 next.  The test reads the plan the library takes (pi_stack_plan) and, from the
 GPU's own masks and the kernel's deal of 8-row pieces, which blocks ran their
-FC rows through the ring in which layers; it requires both ring modes to have
-run, in the first layer and in a later one."""
+FC rows through the ring in which layers; it requires the P2 ring everywhere and
+the FC row ring, in the first layer and again in a later one, where the rows
+cannot fit (the gated stack)."""
 import numpy as np
 import pytest
 import torch
@@ -38,6 +39,11 @@ def own_rows_per_block(mask_bits: np.ndarray, F: int, G: int) -> np.ndarray:
     owner = np.where(rnd % 2 == 0, pos, G - 1 - pos)
     per_piece = np.add.reduceat(mask_bits.astype(np.int64), np.arange(0, F, 8))
     return np.bincount(owner, weights=per_piece, minlength=G).astype(np.int64)
+
+
+# the gated LLaMA-70B-shaped stack needs three 16 KB rows per neuron, more than
+# a block's row slots hold, so every block streams its FC rows through the ring
+FC_RING_EXPECTED = {"c4"}
 
 
 def _unpack(words: np.ndarray, F: int) -> np.ndarray:
@@ -79,13 +85,16 @@ def test_wide_stack_layers_match_oracle_in_ring_modes(key):
             _, pre, band = oracle.rmsnorm_half(y[0].cpu().numpy().astype(np.float64), cfg.rms_eps)
             half_matches(xs_full[l + 1][0].cpu().view(torch.int16).numpy().view(np.uint16), pre, band,
                          f"{key} normalised input of layer {l + 1}")
-        own = own_rows_per_block(_unpack(mask, cfg.F), cfg.F, plan.ctas)
-        ring_blocks.append(set(np.nonzero(own * rows_per_neuron > plan.fc_row_slots)[0].tolist()))
+        bits = _unpack(mask, cfg.F)
+        rows = own_rows_per_block(bits, cfg.F, plan.ctas)
+        ring_blocks.append(set(np.nonzero(rows * rows_per_neuron > plan.fc_row_slots)[0].tolist()))
         del host
     close(y_full[0].cpu().numpy(), y[0].cpu().numpy(), "full run vs prefix run", max_abs=0, rel_l2=0)
-    assert ring_blocks[0], f"{key}: no block streamed its FC rows through the ring in layer 0"
-    assert any(ring_blocks[0] & ring_blocks[l] for l in range(1, L)), \
-        f"{key}: no block ran the FC row ring in layer 0 and again in a later layer"
+    if key in FC_RING_EXPECTED:
+        # the ring's position carries over only for a block that used it before
+        assert ring_blocks[0], f"{key}: no block streamed its FC rows through the ring in layer 0"
+        assert any(ring_blocks[0] & ring_blocks[l] for l in range(1, L)), \
+            f"{key}: no block ran the FC row ring in layer 0 and again in a later layer"
 
 
 def test_own_rows_deal_small_example():
