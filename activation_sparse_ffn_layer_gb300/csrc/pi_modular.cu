@@ -288,50 +288,64 @@ __global__ void __launch_bounds__(256) k_fc1(const __half* __restrict__ x, int B
 #pragma unroll
         for (int t = 0; t < TB; ++t) acc[t] = accu[t] = 0.f;
         if (KIND != 2) {
+            // the row's words are requested U per lane at a time; products of
+            // fp16 weights and fp16 x are exact in fp32
             const uint4* row = reinterpret_cast<const uint4*>(static_cast<const __half*>(w.w1) + (size_t)k * d);
             const uint4* rowu = KIND == 1 ? reinterpret_cast<const uint4*>(w.wu + (size_t)k * d) : nullptr;
-#pragma unroll 4
-            for (int c = lane; c < nv; c += 32) {
-                float wf[8], uf[8];
-                h8_to_f8(ld_stream16(row + c), wf);
-                if (KIND == 1) h8_to_f8(ld_stream16(rowu + c), uf);
+            constexpr int U = (KIND == 1 || TB >= 4) ? 8 : 16;
+            for (int cb = lane; cb < nv; cb += 32 * U) {
+                uint4 wv[U], uv[U];
 #pragma unroll
-                for (int t = 0; t < TB; ++t) {
-                    float xf[8];
-                    h8_to_f8(reinterpret_cast<const uint4*>(xs + (size_t)t * d)[c], xf);
+                for (int u = 0; u < U; ++u) {
+                    const int c = cb + 32 * u;
+                    wv[u] = c < nv ? ld_stream16(row + c) : make_uint4(0u, 0u, 0u, 0u);
+                    if (KIND == 1) uv[u] = c < nv ? ld_stream16(rowu + c) : make_uint4(0u, 0u, 0u, 0u);
+                }
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        acc[t] = fmaf(wf[e], xf[e], acc[t]);
-                        if (KIND == 1) accu[t] = fmaf(uf[e], xf[e], accu[t]);
+                for (int u = 0; u < U; ++u) {
+                    const int c = cb + 32 * u;
+                    if (c >= nv) break;
+#pragma unroll
+                    for (int t = 0; t < TB; ++t) {
+                        const uint4 xw = reinterpret_cast<const uint4*>(xs + (size_t)t * d)[c];
+                        acc[t] += dot8hh(wv[u], xw);
+                        if (KIND == 1) accu[t] += dot8hh(uv[u], xw);
                     }
                 }
             }
         } else {
+            // groups of 32 codes (16 bytes) and their scales, U per lane at a
+            // time; codes become exact fp16 integers, products exact in fp32
             const int ng = d / 32;
             const uint4* row = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(w.w1) + (size_t)k * (d / 2));
             const __half* sc = w.w1s + (size_t)k * ng;
-#pragma unroll 2
-            for (int g = lane; g < ng; g += 32) {
-                const uint4 q = ld_stream16(row + g);
-                const float s = __half2float(sc[g]);
-                const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
-                float part[TB];
+            constexpr int U = 8;
+            for (int gb = lane; gb < ng; gb += 32 * U) {
+                uint4 qv[U];
+                float sv[U];
 #pragma unroll
-                for (int t = 0; t < TB; ++t) part[t] = 0.f;
-#pragma unroll
-                for (int wi = 0; wi < 4; ++wi) {
-                    float qf[8];
-                    q8_to_f8(qw[wi], qf);
-#pragma unroll
-                    for (int t = 0; t < TB; ++t) {
-                        float xf[8];
-                        h8_to_f8(*reinterpret_cast<const uint4*>(xs + (size_t)t * d + g * 32 + wi * 8), xf);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) part[t] = fmaf(qf[e], xf[e], part[t]);
-                    }
+                for (int u = 0; u < U; ++u) {
+                    const int g = gb + 32 * u;
+                    qv[u] = g < ng ? ld_stream16(row + g) : make_uint4(0u, 0u, 0u, 0u);
+                    sv[u] = g < ng ? __half2float(sc[g]) : 0.f;
                 }
 #pragma unroll
-                for (int t = 0; t < TB; ++t) acc[t] = fmaf(s, part[t], acc[t]);
+                for (int u = 0; u < U; ++u) {
+                    const int g = gb + 32 * u;
+                    if (g >= ng) break;
+                    const uint32_t qw[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w};
+                    float part[TB];
+#pragma unroll
+                    for (int t = 0; t < TB; ++t) part[t] = 0.f;
+#pragma unroll
+                    for (int wi = 0; wi < 4; ++wi) {
+#pragma unroll
+                        for (int t = 0; t < TB; ++t)
+                            part[t] += dotq8h(qw[wi], *reinterpret_cast<const uint4*>(xs + (size_t)t * d + g * 32 + wi * 8));
+                    }
+#pragma unroll
+                    for (int t = 0; t < TB; ++t) acc[t] = fmaf(sv[u], part[t], acc[t]);
+                }
             }
         }
 #pragma unroll
@@ -437,26 +451,57 @@ __global__ void __launch_bounds__(256) k_fc2_part(const float* __restrict__ h, i
     }
 }
 
-// y[b][c] = b2[c] + sum_{s = 0..S-1} part[s][b][c]   (fixed order: reproducible)
+// y[b][c] = b2[c] + sum_{s = 0..S-1} part[s][b][c], in a fixed order: a block
+// takes 32 consecutive float4 of y (lanes), its warps the splits s = w, w + 8,
+// ... (a warp's loads of one split are 512 contiguous bytes) with all of a
+// lane's loads of a round in flight; the 8 warp sums are added in warp order.
 __global__ void __launch_bounds__(256) k_fc2_reduce(const float* __restrict__ part, int S, int B,
                                                     int d, const __half* __restrict__ b2,
                                                     float* __restrict__ y) {
-    const int e4 = blockIdx.x * blockDim.x + threadIdx.x;
+    __shared__ float4 red[8][32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int total4 = B * d / 4;
-    if (e4 >= total4) return;
-    const int c = (e4 * 4) % d;
-    float4 acc = make_float4(__half2float(b2[c]), __half2float(b2[c + 1]), __half2float(b2[c + 2]),
-                             __half2float(b2[c + 3]));
-    const float4* p = reinterpret_cast<const float4*>(part) + e4;
-    const size_t stride = (size_t)B * d / 4;
-    for (int s = 0; s < S; ++s) {
-        const float4 v = p[(size_t)s * stride];
-        acc.x += v.x;
-        acc.y += v.y;
-        acc.z += v.z;
-        acc.w += v.w;
+    const int e4 = blockIdx.x * 32 + lane;
+    const bool ok = e4 < total4;
+    const float4* p = reinterpret_cast<const float4*>(part) + (ok ? e4 : 0);
+    const size_t stride = (size_t)total4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    constexpr int QB = 10;
+    for (int s0 = warp; s0 < S; s0 += 8 * QB) {
+        float4 v[QB];
+#pragma unroll
+        for (int b = 0; b < QB; ++b) {
+            const int sp = s0 + 8 * b;
+            if (ok && sp < S) v[b] = p[(size_t)sp * stride];
+        }
+#pragma unroll
+        for (int b = 0; b < QB; ++b) {
+            const int sp = s0 + 8 * b;
+            if (ok && sp < S) {
+                acc.x += v[b].x;
+                acc.y += v[b].y;
+                acc.z += v[b].z;
+                acc.w += v[b].w;
+            }
+        }
     }
-    reinterpret_cast<float4*>(y)[e4] = acc;
+    red[warp][lane] = acc;
+    __syncthreads();
+    if (warp == 0 && ok) {
+        const int c = (e4 * 4) % d;
+        float4 t = red[0][lane];
+        for (int w = 1; w < 8; ++w) {
+            t.x += red[w][lane].x;
+            t.y += red[w][lane].y;
+            t.z += red[w][lane].z;
+            t.w += red[w][lane].w;
+        }
+        t.x += __half2float(b2[c]);
+        t.y += __half2float(b2[c + 1]);
+        t.z += __half2float(b2[c + 2]);
+        t.w += __half2float(b2[c + 3]);
+        reinterpret_cast<float4*>(y)[e4] = t;
+    }
 }
 
 // -------------------------------------------------------------- normalisation
@@ -659,7 +704,7 @@ cudaError_t launch_fc2(const Plan& p, const float* h, const int32_t* idx, const 
     });
     if (e != cudaSuccess) return e;
     const int total4 = p.B * p.d / 4;
-    k_fc2_reduce<<<(total4 + 255) / 256, 256, 0, s>>>(partial, p.fc2_splits, p.B, p.d, w.b2, y);
+    k_fc2_reduce<<<(total4 + 31) / 32, 256, 0, s>>>(partial, p.fc2_splits, p.B, p.d, w.b2, y);
     return cudaGetLastError();
 }
 
