@@ -119,6 +119,16 @@ PI_DEV float fold16(float (&v)[16], int lane) {
     return v[0] + __shfl_xor_sync(FULL, v[0], 1);
 }
 
+// Programmatic dependent launch: a kernel launched with launch_pdl may be
+// scheduled while the previous kernel on its stream is still running.  Its
+// first statement waits until that kernel has completed and its memory is
+// visible, then lets the next kernel be scheduled in turn.  Nothing before
+// it reads another kernel's output or writes global memory.
+PI_DEV void pdl_entry() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+}
+
 PI_DEV float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL, v, o);

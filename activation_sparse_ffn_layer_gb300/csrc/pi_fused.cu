@@ -47,6 +47,7 @@ constexpr int kBarriersPerLayer = 3;
 constexpr int kMaxUnits = 64;   // 16-row units (two 8-row pieces) per CTA
 constexpr int kRingMax = 8;   // P2 ring slots at most
 constexpr int kMaxFcSlots = 32;   // FC row ring slots at most
+constexpr int kPrefetchUnits = 4; // P2 units brought into L2 during the u barrier
 
 PI_DEV unsigned long long globaltimer() {
     unsigned long long t;
@@ -85,6 +86,16 @@ PI_DEV void bulk_g2s(void* dst, const void* src, unsigned bytes, unsigned long l
                  "l"(src), "r"(bytes), "r"(smem_u32(mbar))
                  : "memory");
 }
+// Bring the 128-byte lines that hold [p, p + bytes) into L2 through the
+// load/store path (no registers written, nothing to wait for): thread t of n
+// takes lines t, t + n, ...
+PI_DEV void prefetch_lines(const void* p, size_t bytes, int t, int n) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(p) & ~(uintptr_t)127;
+    const uintptr_t a1 = reinterpret_cast<uintptr_t>(p) + bytes;
+    for (uintptr_t a = a0 + (uintptr_t)t * 128; a < a1; a += (uintptr_t)n * 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+}
+
 // Before leaving after a failure: wait (bounded) for this CTA's own bulk copy
 // still in flight, so none lands in shared memory after the CTA has exited.
 PI_DEV void mbar_drain(unsigned long long* mbar, unsigned parity, long long timeout_ns) {
@@ -544,7 +555,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
             }
         }
         PI_STAMP(l, 8);
-        if (!sync()) { leave(); return; }
+        // warp 0, after this CTA's arrival at the barrier that publishes u (HBM
+        // is idle while the grid waits): the P2 units the ring reaches right
+        // after its prefilled ones are brought into L2
+        auto prefetch_next_units = [&]() {
+            const int u0 = min(ns, nunits), u1 = min(nunits, u0 + kPrefetchUnits);
+            for (int i = 2 * u0; i < min(npc, 2 * u1); ++i) {
+                const int rb = 8 * piece_of(i);
+                prefetch_lines(ly.p2 + (size_t)rb * ly.r, (size_t)2 * ly.r * min(8, F - rb), lane, 32);
+            }
+        };
+        if (!p.pred_smem && ns > 0) {
+            if (!sync_then(prefetch_next_units)) { leave(); return; }
+        } else if (!sync()) { leave(); return; }
         PI_STAMP(l, 2);
 
         // ---------------------------------------------------------- phase B
@@ -846,6 +869,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
             constexpr int RB = KIND == 1 ? 4 : 8;
             const int rbn = max(1, min(RB, S / (2 * fc1_rows)));   // half the slots per batch
             if (fits && nmine > 0 && mbar_wait(&w1_mbar, (w12_uses - 1) & 1u, tmo, &bad)) w12_pending = false;
+            PI_STAMP(l, 14);
             Cursor cu = cursor_at(0);
             for (int qb = 0; qb < nmine; qb += 128) {
                 const int qe = min(nmine, qb + 128);
@@ -929,6 +953,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
 #pragma unroll
                 for (int e = 0; e < 8; ++e) acc[ch][e] = 0.f;
             if (fits && nmine > 0) mbar_wait(&w2_mbar, (w12_uses - 1) & 1u, tmo, &bad);
+            PI_STAMP(l, 15);
             Cursor cu = cursor_at(fc1n);
             for (int q0 = 0; q0 < nmine; q0 += rb2) {
                 const int q1 = min(nmine, q0 + rb2);
@@ -992,6 +1017,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
 #pragma unroll
                 for (int e = 0; e < 32; ++e) acc[g][e] = 0.f;
             if (fits && nmine > 0) mbar_wait(&w2_mbar, (w12_uses - 1) & 1u, tmo, &bad);
+            PI_STAMP(l, 15);
             Cursor cu = cursor_at(fc1n);
             for (int q0 = 0; q0 < nmine; q0 += rb2) {
                 const int q1 = min(nmine, q0 + rb2);

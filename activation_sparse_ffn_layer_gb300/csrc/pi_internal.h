@@ -6,9 +6,31 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/pi.h"
 
 namespace pi {
+
+// Launch `kernel` with programmatic dependent launch allowed, so that its grid
+// is scheduled while the previous kernel on the stream finishes; the kernel
+// must begin with pdl_entry() (or wait with griddepcontrol.wait before it
+// reads another kernel's output or writes global memory).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Work split chosen for one layer descriptor on the current device.  Both the
 // workspace size and every launch are derived from it, so they always agree.

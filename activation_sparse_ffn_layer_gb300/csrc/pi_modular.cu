@@ -26,9 +26,7 @@ template <int TB>
 __global__ void __launch_bounds__(256) k_predict_u(const __half* __restrict__ x, int B, int b0,
                                                    const __half* __restrict__ p1, int d, int r,
                                                    int seg, float* __restrict__ upart) {
-    // a programmatic dependent (the batch-1 score kernel) may start now: it
-    // waits for this grid's completion before it reads the partials
-    asm volatile("griddepcontrol.launch_dependents;");
+    pdl_entry();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int i = blockIdx.x * 8 + warp;
     const int s = blockIdx.y;
@@ -67,6 +65,7 @@ __global__ void __launch_bounds__(128) k_predict_s(const __half* __restrict__ p2
                                                    const float* __restrict__ upart, int usplits,
                                                    int B, int b0, int r, int F, int W, float tau,
                                                    uint32_t* __restrict__ mask) {
+    pdl_entry();
     extern __shared__ __align__(16) float us[];  // [TB][r]
     for (int e = threadIdx.x; e < TB * r; e += blockDim.x) {
         const int t = e / r, i = e - t * r;
@@ -160,6 +159,7 @@ __global__ void __launch_bounds__(256) k_predict_s1(const __half* __restrict__ p
     uint4 w[16];
     load(0, w);
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
     for (int i = threadIdx.x; i < r; i += blockDim.x) {
         float v = 0.f;
         for (int s = 0; s < usplits; ++s) v += upart[(size_t)s * r + i];
@@ -215,6 +215,7 @@ __global__ void __launch_bounds__(1024) k_compact(const uint32_t* __restrict__ m
                                                   int32_t* __restrict__ idx,
                                                   int32_t* __restrict__ orig,
                                                   int32_t* __restrict__ count) {
+    pdl_entry();
     __shared__ int wsum[32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int base = 0;
@@ -271,6 +272,7 @@ __global__ void __launch_bounds__(256) k_fc1(const __half* __restrict__ x, int B
                                              const int32_t* __restrict__ count,
                                              const uint32_t* __restrict__ mask, int W,
                                              float* __restrict__ h) {
+    pdl_entry();
     const int n = *count;
     if (n == 0) return;  // nothing predicted active: skip the layer's FC1 entirely
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -381,6 +383,7 @@ __global__ void __launch_bounds__(256) k_fc2_part(const float* __restrict__ h, i
                                                   const void* __restrict__ w2t,
                                                   const __half* __restrict__ w2ts,
                                                   float* __restrict__ part) {
+    pdl_entry();
     constexpr int CPT = INT4 ? 16 : 8;
     constexpr int CH = 256;
     const int n = *count;
@@ -458,6 +461,7 @@ __global__ void __launch_bounds__(256) k_fc2_part(const float* __restrict__ h, i
 __global__ void __launch_bounds__(256) k_fc2_reduce(const float* __restrict__ part, int S, int B,
                                                     int d, const __half* __restrict__ b2,
                                                     float* __restrict__ y) {
+    pdl_entry();
     __shared__ float4 red[8][32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int total4 = B * d / 4;
@@ -513,6 +517,7 @@ constexpr int kNormThreads = 1024;
 constexpr int kNormWords = 4;   // float4 words per thread held in registers (d <= 16384)
 __global__ void __launch_bounds__(kNormThreads) k_rmsnorm(const float* __restrict__ y, int d, float eps,
                                                           __half* __restrict__ x) {
+    pdl_entry();
     __shared__ float red[32];
     const float4* yb = reinterpret_cast<const float4*>(y + (size_t)blockIdx.x * d);
     const int n4 = d / 4;
@@ -556,6 +561,7 @@ __global__ void __launch_bounds__(kNormThreads) k_rmsnorm(const float* __restric
 // out[0] = n, out[1] = number of listed neurons with a non-zero h for some token
 __global__ void __launch_bounds__(256) k_count_active(const int32_t* __restrict__ count, const float* __restrict__ h,
                                                       int B, int32_t* __restrict__ out) {
+    pdl_entry();
     const int n = *count;
     int nz = 0;
     for (int j = threadIdx.x; j < n; j += blockDim.x) {
@@ -616,15 +622,15 @@ cudaError_t launch_predict(const Plan& p, const __half* x, const __half* p1, con
         const size_t sm = (size_t)tb * p.r * sizeof(float);
 #define PI_PRED(TBV)                                                                               \
     case TBV: {                                                                                    \
-        k_predict_u<TBV><<<gu, 256, 0, s>>>(x, p.B, b0, p1, p.d, p.r, p.u_seg, upart);             \
+        launch_pdl(k_predict_u<TBV>, gu, 256, 0, s, x, p.B, b0, p1, p.d, p.r, p.u_seg, upart);             \
         cudaError_t e = set_smem(k_predict_s<TBV>, sm);                                            \
         if (e != cudaSuccess) return e;                                                            \
-        k_predict_s<TBV><<<ws, 128, sm, s>>>(p2, bpred, upart, p.u_splits, p.B, b0, p.r, p.F, p.W, \
+        launch_pdl(k_predict_s<TBV>, ws, 128, sm, s, p2, bpred, upart, p.u_splits, p.B, b0, p.r, p.F, p.W, \
                                              tau, mask);                                           \
         break;                                                                                     \
     }
         if (tb == 1 && p.B == 1) {
-            k_predict_u<1><<<gu, 256, 0, s>>>(x, p.B, b0, p1, p.d, p.r, p.u_seg, upart);
+            launch_pdl(k_predict_u<1>, gu, 256, 0, s, x, p.B, b0, p1, p.d, p.r, p.u_seg, upart);
             const size_t sm1 = (size_t)p.r * sizeof(float);
             cudaError_t e = set_smem(k_predict_s1, sm1);
             if (e != cudaSuccess) return e;
@@ -654,7 +660,7 @@ cudaError_t launch_predict(const Plan& p, const __half* x, const __half* p1, con
 
 cudaError_t launch_compact(const Plan& p, const uint32_t* mask, const int32_t* table, int32_t* idx,
                            int32_t* orig, int32_t* count, cudaStream_t s) {
-    k_compact<<<1, 1024, 0, s>>>(mask, p.B, p.W, p.F, table, idx, orig, count);
+    launch_pdl(k_compact, 1, 1024, 0, s, mask, p.B, p.W, p.F, table, idx, orig, count);
     return cudaGetLastError();
 }
 
@@ -676,7 +682,7 @@ cudaError_t launch_fc1(const Plan& p, const __half* x, const LayerPtrs& w, const
     if (tb == TBV && kind == KV) {                                                            \
         e = set_smem(k_fc1<TBV, KV>, sm);                                                     \
         if (e != cudaSuccess) return e;                                                       \
-        k_fc1<TBV, KV><<<grid, 256, sm, s>>>(x, p.B, b0, p.d, w, idx, count, mask, p.W, h); \
+        launch_pdl(k_fc1<TBV, KV>, grid, 256, sm, s, x, p.B, b0, p.d, w, idx, count, mask, p.W, h); \
     }
         PI_FC1(1, 0) PI_FC1(2, 0) PI_FC1(4, 0) PI_FC1(8, 0)
         PI_FC1(1, 1) PI_FC1(2, 1) PI_FC1(4, 1) PI_FC1(8, 1)
@@ -695,7 +701,7 @@ cudaError_t launch_fc2(const Plan& p, const float* h, const int32_t* idx, const 
         dim3 grid(p.fc2_tiles, p.fc2_splits);
 #define PI_FC2(TBV, IV)                                                                       \
     if (tb == TBV && p.int4 == IV)                                                            \
-        k_fc2_part<TBV, IV><<<grid, 256, 0, s>>>(h, p.B, b0, idx, count, p.d, w.w2t, w.w2ts, \
+        launch_pdl(k_fc2_part<TBV, IV>, grid, 256, 0, s, h, p.B, b0, idx, count, p.d, w.w2t, w.w2ts, \
                                                  partial);
         PI_FC2(1, false) PI_FC2(2, false) PI_FC2(4, false) PI_FC2(8, false)
         PI_FC2(1, true) PI_FC2(2, true) PI_FC2(4, true) PI_FC2(8, true)
@@ -704,7 +710,7 @@ cudaError_t launch_fc2(const Plan& p, const float* h, const int32_t* idx, const 
     });
     if (e != cudaSuccess) return e;
     const int total4 = p.B * p.d / 4;
-    k_fc2_reduce<<<(total4 + 31) / 32, 256, 0, s>>>(partial, p.fc2_splits, p.B, p.d, w.b2, y);
+    launch_pdl(k_fc2_reduce, (total4 + 31) / 32, 256, 0, s, partial, p.fc2_splits, p.B, p.d, w.b2, y);
     return cudaGetLastError();
 }
 
@@ -716,12 +722,12 @@ size_t fc2_part_floats(const Plan& p) {
 }
 
 cudaError_t launch_count_active(const Plan& p, const int32_t* count, const float* h, int32_t* out, cudaStream_t s) {
-    k_count_active<<<1, 256, 0, s>>>(count, h, p.B, out);
+    launch_pdl(k_count_active, 1, 256, 0, s, count, h, p.B, out);
     return cudaGetLastError();
 }
 
 cudaError_t launch_rmsnorm(int d, int B, const float* y, float eps, __half* x, cudaStream_t s) {
-    k_rmsnorm<<<B, kNormThreads, 0, s>>>(y, d, eps, x);
+    launch_pdl(k_rmsnorm, B, kNormThreads, 0, s, y, d, eps, x);
     return cudaGetLastError();
 }
 

@@ -78,6 +78,7 @@ struct SArgs {
 
 template <int MODE, int TB>
 __global__ void __launch_bounds__(kSThreads, 1) k_rows_st(SArgs a) {
+    pdl_entry();
     using C = SCfg<MODE, TB>;
     extern __shared__ __align__(16) unsigned char ring[];
     __shared__ __align__(8) unsigned long long full[C::S], empty[C::S];
@@ -362,6 +363,7 @@ __global__ void __launch_bounds__(kSThreads, 1) k_rows_st(SArgs a) {
 // u[t][i] = sum of the P1 x partials in ascending CTA order, fp32 rows [B][r].
 __global__ void __launch_bounds__(256) k_u_finish32(const float* __restrict__ part, int slots, int G, int nk, int r,
                                                     int B, int NT, float* __restrict__ u) {
+    pdl_entry();
     __shared__ int slot[kMaxCtas];
     __shared__ int rng[2];
     const int i0 = blockIdx.x * 32;
@@ -417,6 +419,7 @@ PI_DEV void piece2(long long u0, long long u1, int n, int which, Piece2* out) {
 
 template <int TB>
 __global__ void __launch_bounds__(kSThreads, 1) k_fc2_st(SArgs2 a) {
+    pdl_entry();
     using C = SCfg2<TB>;
     extern __shared__ __align__(16) unsigned char ring[];
     __shared__ __align__(8) unsigned long long full[C::S], empty[C::S];
@@ -624,7 +627,7 @@ cudaError_t launch_rows(const SArgs& a, int grid, cudaStream_t s) {
     using C = SCfg<MODE, TB>;
     cudaError_t e = prep_st(k_rows_st<MODE, TB>, C::SMEM);
     if (e != cudaSuccess) return e;
-    k_rows_st<MODE, TB><<<grid, kSThreads, C::SMEM, s>>>(a);
+    launch_pdl(k_rows_st<MODE, TB>, grid, kSThreads, C::SMEM, s, a);
     return cudaGetLastError();
 }
 template <int MODE>
@@ -676,7 +679,7 @@ cudaError_t launch_predict_st(const Plan& p, const __half* x, const __half* p1, 
     a.timeout_ns = wait_timeout_ns();
     cudaError_t e = launch_rows_tb<2>(a, tb, Gu, s);
     if (e != cudaSuccess) return e;
-    k_u_finish32<<<cdiv(p.r, 32), 256, 0, s>>>(part, a.slots, Gu, cdiv(p.d, 64), p.r, p.B, tb, u32);
+    launch_pdl(k_u_finish32, cdiv(p.r, 32), 256, 0, s, part, a.slots, Gu, cdiv(p.d, 64), p.r, p.B, tb, u32);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     e = cudaMemsetAsync(mask, 0, sizeof(uint32_t) * (size_t)p.B * p.W, s);
@@ -731,7 +734,7 @@ cudaError_t launch_fc2_st(const Plan& p, const float* h, const int32_t* idx, con
     if (tb == TBV) {                                                      \
         e = prep_st(k_fc2_st<TBV>, SCfg2<TBV>::SMEM);                     \
         if (e != cudaSuccess) return e;                                   \
-        k_fc2_st<TBV><<<G, kSThreads, SCfg2<TBV>::SMEM, s>>>(a);           \
+        launch_pdl(k_fc2_st<TBV>, G, kSThreads, SCfg2<TBV>::SMEM, s, a);           \
     }
     PI_FC2ST(2) else PI_FC2ST(4) else PI_FC2ST(8)
 #undef PI_FC2ST

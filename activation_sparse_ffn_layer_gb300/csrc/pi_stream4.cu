@@ -96,6 +96,7 @@ struct Q1Args {
 
 template <int TB>
 __global__ void __launch_bounds__(kQThreads, 1) k_fc1_st4(Q1Args a) {
+    pdl_entry();
     using C = Q1Cfg<TB>;
     extern __shared__ __align__(16) unsigned char ring[];
     __shared__ __align__(8) unsigned long long full[C::S], empty[C::S];
@@ -402,6 +403,7 @@ constexpr int kQMaxPieces = 16;
 
 template <int TB>
 __global__ void __launch_bounds__(kQThreads, 1) k_fc2_st4(Q2Args a) {
+    pdl_entry();
     using C = Q2Cfg<TB>;
     extern __shared__ __align__(16) unsigned char ring[];
     __shared__ __align__(8) unsigned long long full[C::S], empty[C::S];
@@ -664,7 +666,7 @@ cudaError_t launch_fc1_st4(const Plan& p, const __half* x, const LayerPtrs& w, c
     if (tb == TBV) {                                                     \
         e = prep_q(k_fc1_st4<TBV>, Q1Cfg<TBV>::SMEM);                    \
         if (e != cudaSuccess) return e;                                  \
-        k_fc1_st4<TBV><<<G, kQThreads, Q1Cfg<TBV>::SMEM, s>>>(a);         \
+        launch_pdl(k_fc1_st4<TBV>, G, kQThreads, Q1Cfg<TBV>::SMEM, s, a);         \
     }
     PI_Q1(4) else PI_Q1(8) else PI_Q1(16)
 #undef PI_Q1
@@ -688,7 +690,7 @@ cudaError_t launch_fc2_st4(const Plan& p, const float* h, const int32_t* idx, co
         if (tb == TBV) {                                                 \
             e = prep_q(k_fc2_st4<TBV>, Q2Cfg<TBV>::SMEM);                \
             if (e != cudaSuccess) return e;                              \
-            k_fc2_st4<TBV><<<G, kQThreads, Q2Cfg<TBV>::SMEM, s>>>(a);     \
+            launch_pdl(k_fc2_st4<TBV>, G, kQThreads, Q2Cfg<TBV>::SMEM, s, a);     \
         }
         PI_Q2(4) else PI_Q2(8) else PI_Q2(16)
 #undef PI_Q2

@@ -489,6 +489,7 @@ PI_DEV void q4_epilogue(const TcRowsArgs& a, const SpanOf& span, int npiece, int
 
 template <int MODE, int NT>
 __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
+    pdl_entry();
     using C = RowsCfg<MODE, NT>;
     extern __shared__ unsigned char dsm[];
     __shared__ __align__(8) unsigned long long full[C::S], empty[C::S], accf[2], acce[2], drain;
@@ -828,6 +829,7 @@ __global__ void __launch_bounds__(1024) k_fc1_finish(const float* __restrict__ p
                                                      const int32_t* __restrict__ idx, const __half* __restrict__ b1,
                                                      const uint32_t* __restrict__ mask, int W,
                                                      float* __restrict__ h, int32_t* __restrict__ live) {
+    pdl_entry();
     __shared__ int slot[kMaxCtas];
     __shared__ int rng[2];
     __shared__ int any[32];
@@ -859,6 +861,7 @@ __global__ void __launch_bounds__(1024) k_fc1_finish(const float* __restrict__ p
 // padded tokens t >= B).  Block: 32 consecutive i (lane) x NT tokens (warp).
 __global__ void __launch_bounds__(1024) k_u_finish(const float* __restrict__ part, int slots, int G, int nk, int r,
                                                    int B, int NT, __half* __restrict__ uhl) {
+    pdl_entry();
     __shared__ int slot[kMaxCtas];
     __shared__ int rng[2];
     const int i0 = blockIdx.x * 32;
@@ -920,6 +923,7 @@ PI_DEV int fc2_piece(long long u0, long long u1, int n, int which, Piece* out) {
 
 template <int NT>
 __global__ void __launch_bounds__(kTcThreads, 1) k_fc2_tc(TcFc2Args a) {
+    pdl_entry();
     using C = Fc2Cfg<NT>;
     extern __shared__ unsigned char dsm[];
     __shared__ __align__(8) unsigned long long full[C::S], empty[C::S], accf[2], acce[2], drain;
@@ -1185,6 +1189,7 @@ __global__ void __launch_bounds__(1024) k_fc2_tc_reduce(const float* __restrict_
                                                         const int32_t* __restrict__ count, int nb, int b0, int NT,
                                                         int d, int tw, const __half* __restrict__ b2,
                                                         float* __restrict__ y) {
+    pdl_entry();
     __shared__ int slot[kMaxCtas];
     __shared__ int rng[2];
     const int ct = blockIdx.x;
@@ -1256,7 +1261,7 @@ cudaError_t launch_rows(const TcRowsArgs& a, int grid, cudaStream_t s) {
     using C = RowsCfg<MODE, NT>;
     cudaError_t e = prep(k_rows_tc<MODE, NT>, C::SMEM);
     if (e != cudaSuccess) return e;
-    k_rows_tc<MODE, NT><<<grid, kTcThreads, C::SMEM, s>>>(a);
+    launch_pdl(k_rows_tc<MODE, NT>, grid, kTcThreads, C::SMEM, s, a);
     return cudaGetLastError();
 }
 
@@ -1288,7 +1293,7 @@ cudaError_t launch_predict_tc(const Plan& p, const __half* x, const __half* p1, 
     a.timeout_ns = wait_timeout_ns();
     cudaError_t e = launch_rows_nt<2>(a, nt, Gu, s);
     if (e != cudaSuccess) return e;
-    k_u_finish<<<ceil_div(p.r, 32), 32 * nt, 0, s>>>(part, a.slots, Gu, ceil_div(p.d, 64), p.r, p.B, nt, uhl);
+    launch_pdl(k_u_finish, ceil_div(p.r, 32), 32 * nt, 0, s, part, a.slots, Gu, ceil_div(p.d, 64), p.r, p.B, nt, uhl);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // s = P2 u + b > tau over whole 128-row tiles, mask words by ballot
@@ -1331,10 +1336,10 @@ cudaError_t launch_fc1_tc(const Plan& p, const __half* x, const LayerPtrs& w, co
     if (e != cudaSuccess) return e;
     const int blocks = ceil_div(p.F, 32);
     if (p.gated)
-        k_fc1_finish<true><<<blocks, 32 * p.B, 0, s>>>(part, a.slots, G, ceil_div(p.d, 64), count, p.B, nt, idx, w.b1,
+        launch_pdl(k_fc1_finish<true>, blocks, 32 * p.B, 0, s, part, a.slots, G, ceil_div(p.d, 64), count, p.B, nt, idx, w.b1,
                                                    mask, p.W, h, live);
     else
-        k_fc1_finish<false><<<blocks, 32 * p.B, 0, s>>>(part, a.slots, G, ceil_div(p.d, 64), count, p.B, nt, idx, w.b1,
+        launch_pdl(k_fc1_finish<false>, blocks, 32 * p.B, 0, s, part, a.slots, G, ceil_div(p.d, 64), count, p.B, nt, idx, w.b1,
                                                     mask, p.W, h, live);
     return cudaGetLastError();
 }
@@ -1368,10 +1373,10 @@ cudaError_t launch_fc1_finish(const Plan& p, int nt, int G, int slots, int nk, c
                               float* h, int32_t* live, cudaStream_t s) {
     const int blocks = ceil_div(p.F, 32);
     if (p.gated)
-        k_fc1_finish<true><<<blocks, 32 * p.B, 0, s>>>(part, slots, G, nk, count, p.B, nt, idx, b1, mask, p.W, h,
+        launch_pdl(k_fc1_finish<true>, blocks, 32 * p.B, 0, s, part, slots, G, nk, count, p.B, nt, idx, b1, mask, p.W, h,
                                                        live);
     else
-        k_fc1_finish<false><<<blocks, 32 * p.B, 0, s>>>(part, slots, G, nk, count, p.B, nt, idx, b1, mask, p.W, h,
+        launch_pdl(k_fc1_finish<false>, blocks, 32 * p.B, 0, s, part, slots, G, nk, count, p.B, nt, idx, b1, mask, p.W, h,
                                                         live);
     return cudaGetLastError();
 }
@@ -1379,7 +1384,7 @@ cudaError_t launch_fc1_finish(const Plan& p, int nt, int G, int slots, int nk, c
 cudaError_t launch_fc2_reduce(const Plan& p, int nt, int G, int slots, int tw, int nb, int b0, const float* part,
                               const int32_t* count, const __half* b2, float* y, cudaStream_t s) {
     const int tpb = 1024 / tw;
-    k_fc2_tc_reduce<<<dim3(p.d / tw, ceil_div(nb, tpb)), 1024, 0, s>>>(part, slots, G, count, nb, b0, nt, p.d, tw,
+    launch_pdl(k_fc2_tc_reduce, dim3(p.d / tw, ceil_div(nb, tpb)), 1024, 0, s, part, slots, G, count, nb, b0, nt, p.d, tw,
                                                                         b2, y);
     return cudaGetLastError();
 }
@@ -1396,15 +1401,15 @@ cudaError_t launch_fc2_tc(const Plan& p, const float* h, const int32_t* idx, con
     if (nt == 16) {
         e = prep(k_fc2_tc<16>, Fc2Cfg<16>::SMEM);
         if (e != cudaSuccess) return e;
-        k_fc2_tc<16><<<G, kTcThreads, Fc2Cfg<16>::SMEM, s>>>(a);
+        launch_pdl(k_fc2_tc<16>, G, kTcThreads, Fc2Cfg<16>::SMEM, s, a);
     } else {
         e = prep(k_fc2_tc<32>, Fc2Cfg<32>::SMEM);
         if (e != cudaSuccess) return e;
-        k_fc2_tc<32><<<G, kTcThreads, Fc2Cfg<32>::SMEM, s>>>(a);
+        launch_pdl(k_fc2_tc<32>, G, kTcThreads, Fc2Cfg<32>::SMEM, s, a);
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    k_fc2_tc_reduce<<<dim3(p.d / 128, ceil_div(p.B, 8)), 1024, 0, s>>>(partial, slots, G, count, p.B, 0, nt, p.d,
+    launch_pdl(k_fc2_tc_reduce, dim3(p.d / 128, ceil_div(p.B, 8)), 1024, 0, s, partial, slots, G, count, p.B, 0, nt, p.d,
                                                                         128, w.b2, y);
     return cudaGetLastError();
 }

@@ -1,0 +1,155 @@
+"""Timing of the C-ABI entry points one by one on a workload's layer.
+
+For a configuration and batch size this times, through the library's own
+calls, ``pi_predict``, ``pi_compact``, ``pi_sparse_fc1``, ``pi_sparse_fc2``,
+``pi_rmsnorm_half`` and ``pi_ffn_layer`` (CUDA graphs of 10 calls, CUDA events,
+two layers in alternation so that neither is left in L2 by the previous call)
+and prints one JSON line per call with its time and the algorithmic bytes it
+moves: the predictor weights for ``pi_predict``, the listed rows for the FC
+calls (FC2 counts the rows whose FC1 output is non-zero for some token).
+
+    python -m activation_sparse_ffn_layer_gb300.entry_bench --config c2 --batch 1
+    python -m activation_sparse_ffn_layer_gb300.entry_bench --config c5 --batch 4 --once
+
+``--once`` runs every call a few times eagerly and then once more, without
+graphs or timing, which is the shape a profiler capture wants.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+
+import torch
+
+from . import binding as B
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def _peak_gbs() -> float:
+    try:
+        with open(os.path.join(os.path.dirname(HERE), "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"])
+    except Exception:
+        return 6800.0
+
+
+def _time(fn, reps: int = 200) -> float:
+    """Microseconds per call: graph-replayed batches of 10 calls."""
+    for _ in range(5):
+        fn()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(10):
+            fn()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps // 10):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps * 1e3
+
+
+def run(config: str, batch: int, once: bool = False):
+    from synth import CONFIGS, make_layer, make_tokens
+
+    B.lib()
+    cfg = CONFIGS[config]
+    dev = "cuda"
+    layers = [make_layer(cfg, l, device=dev) for l in range(2)]
+    d, F = cfg.d, cfg.F
+    x = make_tokens(cfg, 0, batch, device=dev)
+    desc = B.layer_desc(layers[0], batch)
+    ws = torch.zeros(B.pi_workspace_bytes(desc), dtype=torch.uint8, device=dev)
+    W = (F + 31) // 32
+    mask = torch.zeros(batch, W, dtype=torch.int32, device=dev)
+    idx = torch.zeros(F, dtype=torch.int32, device=dev)
+    cnt = torch.zeros(1, dtype=torch.int32, device=dev)
+    h = torch.zeros(F * batch, dtype=torch.float32, device=dev)
+    y = torch.zeros(batch, d, dtype=torch.float32, device=dev)
+    xn = torch.zeros(batch, d, dtype=torch.float16, device=dev)
+    wst = [B.weights_struct(w) for w in layers]
+    turn = [0]
+
+    def nxt() -> int:
+        turn[0] += 1
+        return turn[0] % 2
+
+    def predict():
+        w = layers[nxt()]
+        B.pi_predict(desc, x, w.p1, w.p2, w.b1, cfg.tau, mask, ws)
+
+    def compact():
+        B.pi_compact(desc, mask, None, idx, None, cnt)
+
+    def fc1():
+        B.pi_sparse_fc1(desc, x, wst[nxt()], idx, cnt, mask if batch > 1 else None, h, ws)
+
+    def fc2():
+        B.pi_sparse_fc2(desc, h, idx, cnt, wst[nxt()], y, ws)
+
+    def norm():
+        B.pi_rmsnorm_half(d, batch, y, cfg.rms_eps, xn)
+
+    def layer():
+        B.pi_ffn_layer(desc, x, wst[nxt()], cfg.tau, ws, y)
+
+    # one real pass so that the list, h and y hold this layer's values
+    predict()
+    compact()
+    fc1()
+    fc2()
+    torch.cuda.synchronize()
+    n = int(cnt.item())
+    live = int((h[: n * batch].view(n, batch) != 0).any(dim=1).sum().item()) if n else 0
+    calls = [("pi_predict", predict), ("pi_compact", compact), ("pi_sparse_fc1", fc1),
+             ("pi_sparse_fc2", fc2), ("pi_rmsnorm_half", norm), ("pi_ffn_layer", layer)]
+    if once:
+        for name, fn in calls:
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            fn()
+            torch.cuda.synchronize()
+        print(json.dumps({"config": config, "batch": batch, "listed": n, "live": live, "mode": "once"}))
+        return
+    w0 = layers[0]
+    row = d // 2 + d // 16 if cfg.int4 else 2 * d
+    pred_b = 2 * (w0.r * d + F * w0.r) + 2 * F
+    fc1_b = n * row * (2 if cfg.gated else 1)
+    fc2_b = live * row
+    moved = {"pi_predict": pred_b, "pi_compact": 4 * batch * W + 4 * n, "pi_sparse_fc1": fc1_b,
+             "pi_sparse_fc2": fc2_b, "pi_rmsnorm_half": batch * d * 6,
+             "pi_ffn_layer": pred_b + fc1_b + fc2_b}
+    peak = _peak_gbs()
+    for name, fn in calls:
+        us = _time(fn)
+        gbs = moved[name] / us / 1e3
+        print(json.dumps({"call": name, "config": config, "batch": batch, "us": round(us, 2),
+                          "bytes": moved[name], "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+                          "listed": n, "live": live}), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description="time the C-ABI entry points on one layer of a workload")
+    ap.add_argument("--config", default="c2")
+    ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--once", action="store_true", help="run each call once after a warm-up (profiler captures)")
+    args = ap.parse_args(argv)
+    assert torch.cuda.is_available(), "needs a CUDA GPU"
+    run(args.config, args.batch, args.once)
+
+
+if __name__ == "__main__":
+    main()
