@@ -33,6 +33,10 @@ class pi_workspace_layout_t(C.Structure):
     _fields_ = [(n, C.c_size_t) for n in ("mask", "idx", "count", "h", "total")]
 
 
+class pi_cold_tier(C.Structure):
+    _fields_ = [("n_hot", C.c_int)] + [(n, C.c_void_p) for n in ("w1", "w1_scales", "wu", "w2t", "w2t_scales")]
+
+
 class pi_stack_plan_t(C.Structure):
     _fields_ = [(n, C.c_int) for n in ("fused", "ctas", "pred_in_smem", "p2_ring_slots", "fc_row_slots",
                                        "smem_bytes")]
@@ -49,7 +53,8 @@ _lib = None
 EXPORTS = ("pi_workspace_bytes", "pi_workspace_layout", "pi_predict", "pi_compact", "pi_sparse_fc1",
            "pi_sparse_fc2", "pi_ffn_layer", "pi_rmsnorm_half", "pi_status_string",
            "pi_last_device_status", "pi_launches_per_layer", "pi_ffn_stack", "pi_debug_wait_timeout",
-           "pi_sparse_fc2_noalloc", "pi_stack_plan", "pi_debug_set_wait_timeout")
+           "pi_sparse_fc2_noalloc", "pi_stack_plan", "pi_debug_set_wait_timeout", "pi_sparse_fc1_tiered",
+           "pi_sparse_fc2_tiered", "pi_ffn_layer_tiered")
 
 
 def library_path() -> str:
@@ -86,6 +91,9 @@ def lib(path: Optional[str] = None):
         "pi_sparse_fc2_noalloc": (I, [D, P, P, P, Wt, P, P]),
         "pi_stack_plan": (I, [D, I, P, C.POINTER(pi_stack_plan_t)]),
         "pi_debug_set_wait_timeout": (I, [C.c_longlong]),
+        "pi_sparse_fc1_tiered": (I, [D, P, Wt, C.POINTER(pi_cold_tier), P, P, P, P, P]),
+        "pi_sparse_fc2_tiered": (I, [D, P, P, P, Wt, C.POINTER(pi_cold_tier), P, P, S, P]),
+        "pi_ffn_layer_tiered": (I, [D, P, Wt, C.POINTER(pi_cold_tier), Fl, P, S, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -208,6 +216,48 @@ def weights_array(layers):
 
 def ranks_array(layers):
     return (C.c_int * len(layers))(*[int(w.r) for w in layers])
+
+
+def _addr(t):
+    """Address of a tensor for the C ABI: device memory, or host memory the
+    GPU can address (pinned)."""
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError("expected a CUDA tensor or pinned host memory")
+    return C.c_void_p(t.data_ptr())
+
+
+def cold_tier(n_hot: int, w1=None, w1_scales=None, wu=None, w2t=None, w2t_scales=None) -> pi_cold_tier:
+    """A pi_cold_tier over tensors in device or pinned host memory (keep them alive)."""
+    s = pi_cold_tier()
+    s.n_hot = int(n_hot)
+    s.w1, s.w1_scales, s.wu = _addr(w1), _addr(w1_scales), _addr(wu)
+    s.w2t, s.w2t_scales = _addr(w2t), _addr(w2t_scales)
+    return s
+
+
+def pi_sparse_fc1_tiered(desc, x, wstruct, cold, idx, d_count, mask, h):
+    _check("pi_sparse_fc1_tiered", lib().pi_sparse_fc1_tiered(C.byref(desc), _ptr(x), C.byref(wstruct), C.byref(cold),
+                                                              _ptr(idx), _ptr(d_count), _ptr(mask), _ptr(h),
+                                                              _stream()))
+
+
+def pi_sparse_fc2_tiered(desc, h, idx, d_count, wstruct, cold, y, workspace):
+    _check("pi_sparse_fc2_tiered", lib().pi_sparse_fc2_tiered(C.byref(desc), _ptr(h), _ptr(idx), _ptr(d_count),
+                                                              C.byref(wstruct), C.byref(cold), _ptr(y),
+                                                              _ptr(workspace),
+                                                              workspace.numel() * workspace.element_size(),
+                                                              _stream()))
+
+
+def pi_ffn_layer_tiered(desc, x, wstruct, cold, tau: float, workspace, y):
+    _check("pi_ffn_layer_tiered", lib().pi_ffn_layer_tiered(C.byref(desc), _ptr(x), C.byref(wstruct), C.byref(cold),
+                                                            float(tau), _ptr(workspace),
+                                                            workspace.numel() * workspace.element_size(), _ptr(y),
+                                                            _stream()))
 
 
 def pi_stack_plan(desc, n_layers: int, ranks=None) -> pi_stack_plan_t:

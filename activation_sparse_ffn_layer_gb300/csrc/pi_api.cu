@@ -294,6 +294,95 @@ pi_status pi_sparse_fc2(const pi_layer_desc* desc, const float* h, const int32_t
                                 static_cast<cudaStream_t>(stream)));
 }
 
+}  // extern "C"
+
+namespace {
+
+// Checks the second tier against the plan and converts it (no second tier
+// when every row is hot).
+bool cold_ok(const Plan& p, const pi_cold_tier* c, bool need_w1, bool need_w2, ColdPtrs* out) {
+    if (!c || c->n_hot < 0 || c->n_hot > p.F) return false;
+    ColdPtrs k = no_cold_tier();
+    if (c->n_hot == p.F) {
+        *out = k;
+        return true;
+    }
+    if (need_w1) {
+        if (!c->w1 || !aligned16(c->w1)) return false;
+        if (p.int4 && !c->w1_scales) return false;
+        if (p.gated && (!c->wu || !aligned16(c->wu))) return false;
+    }
+    if (need_w2) {
+        if (!c->w2t || !aligned16(c->w2t)) return false;
+        if (p.int4 && !c->w2t_scales) return false;
+    }
+    k.n_hot = c->n_hot;
+    k.w1 = c->w1;
+    k.w1s = reinterpret_cast<const __half*>(c->w1_scales);
+    k.wu = reinterpret_cast<const __half*>(c->wu);
+    k.w2t = c->w2t;
+    k.w2ts = reinterpret_cast<const __half*>(c->w2t_scales);
+    *out = k;
+    return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+pi_status pi_sparse_fc1_tiered(const pi_layer_desc* desc, const pi_half* x, const pi_layer_weights* w,
+                               const pi_cold_tier* cold, const int32_t* idx, const int32_t* d_count,
+                               const uint32_t* mask, float* h, void* stream) {
+    Plan p;
+    if (!desc || !make_plan(*desc, &p)) return PI_ERR_INVALID_ARG;
+    ColdPtrs c;
+    if (!x || !aligned16(x) || !idx || !d_count || !h || !weights_ok(p, w, true, false, false) ||
+        !cold_ok(p, cold, true, false, &c))
+        return PI_ERR_INVALID_ARG;
+    if ((size_t)8 * p.d * sizeof(uint16_t) > 200 * 1024) return PI_ERR_UNSUPPORTED;
+    return from_cuda(launch_fc1_chunked(p, reinterpret_cast<const __half*>(x), ptrs(w), c, idx, d_count,
+                                        p.B > 1 ? mask : nullptr, h, static_cast<cudaStream_t>(stream)));
+}
+
+pi_status pi_sparse_fc2_tiered(const pi_layer_desc* desc, const float* h, const int32_t* idx,
+                               const int32_t* d_count, const pi_layer_weights* w, const pi_cold_tier* cold,
+                               float* y, void* workspace, size_t ws_bytes, void* stream) {
+    Plan p;
+    if (!desc || !make_plan(*desc, &p)) return PI_ERR_INVALID_ARG;
+    ColdPtrs c;
+    if (!h || !idx || !d_count || !y || !aligned16(y) || !weights_ok(p, w, false, true, false) ||
+        !cold_ok(p, cold, false, true, &c))
+        return PI_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace) || ws_bytes < p.total) return PI_ERR_WORKSPACE;
+    return from_cuda(launch_fc2_chunked(p, h, idx, d_count, ptrs(w), c, at<float>(workspace, p.off_part), y,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+pi_status pi_ffn_layer_tiered(const pi_layer_desc* desc, const pi_half* x, const pi_layer_weights* w,
+                              const pi_cold_tier* cold, float tau, void* workspace, size_t ws_bytes, float* y,
+                              void* stream) {
+    Plan p;
+    if (!desc || !make_plan(*desc, &p)) return PI_ERR_INVALID_ARG;
+    ColdPtrs c;
+    if (!x || !aligned16(x) || !y || !aligned16(y) || !weights_ok(p, w, true, true, true) ||
+        !cold_ok(p, cold, true, true, &c))
+        return PI_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace) || ws_bytes < p.total) return PI_ERR_WORKSPACE;
+    if ((size_t)8 * p.d * sizeof(uint16_t) > 200 * 1024) return PI_ERR_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const LayerPtrs l = ptrs(w);
+    const __half* xh = reinterpret_cast<const __half*>(x);
+    uint32_t* mask = at<uint32_t>(workspace, p.off_mask);
+    int32_t* idx = at<int32_t>(workspace, p.off_idx);
+    int32_t* cnt = at<int32_t>(workspace, p.off_count);
+    float* h = at<float>(workspace, p.off_h);
+    cudaError_t e = launch_predict(p, xh, l.p1, l.p2, l.b1, tau, mask, workspace, s);
+    if (e == cudaSuccess) e = launch_compact(p, mask, nullptr, idx, nullptr, cnt, s);
+    if (e == cudaSuccess) e = launch_fc1_chunked(p, xh, l, c, idx, cnt, p.B > 1 ? mask : nullptr, h, s);
+    if (e == cudaSuccess) e = launch_fc2_chunked(p, h, idx, cnt, l, c, at<float>(workspace, p.off_part), y, s);
+    return from_cuda(e);
+}
+
 pi_status pi_ffn_layer(const pi_layer_desc* desc, const pi_half* x, const pi_layer_weights* w, float tau,
                        void* workspace, size_t ws_bytes, float* y, void* stream) {
     Plan p;

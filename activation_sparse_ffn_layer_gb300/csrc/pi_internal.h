@@ -79,6 +79,27 @@ struct LayerPtrs {
     const int32_t* table;
 };
 
+// Second tier of a layer's FC rows: storage rows k >= n_hot are read from
+// these arrays at row k - n_hot (n_hot >= F: no second tier).
+struct ColdPtrs {
+    int n_hot;
+    const void* w1;
+    const __half* w1s;
+    const __half* wu;
+    const void* w2t;
+    const __half* w2ts;
+};
+inline ColdPtrs no_cold_tier() { return ColdPtrs{0x7fffffff, nullptr, nullptr, nullptr, nullptr, nullptr}; }
+
+// FC1 / FC2 on the per-token CUDA-core kernels (token chunks of <= 8) with a
+// second tier of rows; plain 16-byte loads, so the second tier may be host
+// memory the GPU addresses directly.
+cudaError_t launch_fc1_chunked(const Plan& p, const __half* x, const LayerPtrs& w, const ColdPtrs& cold,
+                               const int32_t* idx, const int32_t* count, const uint32_t* mask, float* h,
+                               cudaStream_t s);
+cudaError_t launch_fc2_chunked(const Plan& p, const float* h, const int32_t* idx, const int32_t* count,
+                               const LayerPtrs& w, const ColdPtrs& cold, float* partial, float* y, cudaStream_t s);
+
 // ws: the layer workspace (u partial sums and, on the tcgen05 path, u hi | lo rows)
 cudaError_t launch_predict(const Plan& p, const __half* x, const __half* p1, const __half* p2,
                            const __half* bpred, float tau, uint32_t* mask, void* ws, cudaStream_t s);

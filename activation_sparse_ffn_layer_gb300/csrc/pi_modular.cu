@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(1024) k_compact(const uint32_t* __restrict__ m
 // One warp per listed neuron (grid-stride), x for TB tokens staged in smem.
 template <int TB, int KIND>
 __global__ void __launch_bounds__(256) k_fc1(const __half* __restrict__ x, int B, int b0, int d,
-                                             LayerPtrs w, const int32_t* __restrict__ idx,
+                                             LayerPtrs w, ColdPtrs cold, const int32_t* __restrict__ idx,
                                              const int32_t* __restrict__ count,
                                              const uint32_t* __restrict__ mask, int W,
                                              float* __restrict__ h) {
@@ -292,8 +292,12 @@ __global__ void __launch_bounds__(256) k_fc1(const __half* __restrict__ x, int B
         if (KIND != 2) {
             // the row's words are requested U per lane at a time; products of
             // fp16 weights and fp16 x are exact in fp32
-            const uint4* row = reinterpret_cast<const uint4*>(static_cast<const __half*>(w.w1) + (size_t)k * d);
-            const uint4* rowu = KIND == 1 ? reinterpret_cast<const uint4*>(w.wu + (size_t)k * d) : nullptr;
+            // rows past the hot tier come from the second tier
+            const bool hot = k < cold.n_hot;
+            const size_t kr = hot ? (size_t)k : (size_t)(k - cold.n_hot);
+            const __half* w1b = static_cast<const __half*>(hot ? w.w1 : cold.w1);
+            const uint4* row = reinterpret_cast<const uint4*>(w1b + kr * d);
+            const uint4* rowu = KIND == 1 ? reinterpret_cast<const uint4*>((hot ? w.wu : cold.wu) + kr * d) : nullptr;
             constexpr int U = (KIND == 1 || TB >= 4) ? 8 : 16;
             for (int cb = lane; cb < nv; cb += 32 * U) {
                 uint4 wv[U], uv[U];
@@ -319,8 +323,11 @@ __global__ void __launch_bounds__(256) k_fc1(const __half* __restrict__ x, int B
             // groups of 32 codes (16 bytes) and their scales, U per lane at a
             // time; codes become exact fp16 integers, products exact in fp32
             const int ng = d / 32;
-            const uint4* row = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(w.w1) + (size_t)k * (d / 2));
-            const __half* sc = w.w1s + (size_t)k * ng;
+            const bool hot = k < cold.n_hot;
+            const size_t kr = hot ? (size_t)k : (size_t)(k - cold.n_hot);
+            const uint4* row = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(hot ? w.w1 : cold.w1) +
+                                                              kr * (d / 2));
+            const __half* sc = (hot ? w.w1s : cold.w1s) + kr * ng;
             constexpr int U = 8;
             for (int gb = lane; gb < ng; gb += 32 * U) {
                 uint4 qv[U];
@@ -381,7 +388,7 @@ __global__ void __launch_bounds__(256) k_fc2_part(const float* __restrict__ h, i
                                                   const int32_t* __restrict__ idx,
                                                   const int32_t* __restrict__ count, int d,
                                                   const void* __restrict__ w2t,
-                                                  const __half* __restrict__ w2ts,
+                                                  const __half* __restrict__ w2ts, ColdPtrs cold,
                                                   float* __restrict__ part) {
     pdl_entry();
     constexpr int CPT = INT4 ? 16 : 8;
@@ -417,9 +424,12 @@ __global__ void __launch_bounds__(256) k_fc2_part(const float* __restrict__ h, i
         for (int t = 0; t < cnt; ++t) {
             const int k = sidx[t];
             if (k < 0) continue;
+            // rows past the hot tier come from the second tier
+            const bool hot = k < cold.n_hot;
+            const size_t kr = hot ? (size_t)k : (size_t)(k - cold.n_hot);
             if (!INT4) {
                 float wf[8];
-                h8_to_f8(ld_stream16(static_cast<const __half*>(w2t) + (size_t)k * d + c), wf);
+                h8_to_f8(ld_stream16(static_cast<const __half*>(hot ? w2t : cold.w2t) + kr * d + c), wf);
 #pragma unroll
                 for (int tb = 0; tb < TB; ++tb) {
                     const float hv = sh[t * TB + tb];
@@ -427,8 +437,8 @@ __global__ void __launch_bounds__(256) k_fc2_part(const float* __restrict__ h, i
                     for (int e = 0; e < 8; ++e) acc[tb][e] = fmaf(hv, wf[e], acc[tb][e]);
                 }
             } else {
-                const uint2 q = ld_stream8(static_cast<const uint8_t*>(w2t) + (size_t)k * (d / 2) + c / 2);
-                const float sc = __half2float(w2ts[(size_t)k * (d / 32) + c / 32]);
+                const uint2 q = ld_stream8(static_cast<const uint8_t*>(hot ? w2t : cold.w2t) + kr * (d / 2) + c / 2);
+                const float sc = __half2float((hot ? w2ts : cold.w2ts)[kr * (d / 32) + c / 32]);
                 float qa[8], qb[8];
                 q8_to_f8(q.x, qa);
                 q8_to_f8(q.y, qb);
@@ -664,13 +674,9 @@ cudaError_t launch_compact(const Plan& p, const uint32_t* mask, const int32_t* t
     return cudaGetLastError();
 }
 
-cudaError_t launch_fc1(const Plan& p, const __half* x, const LayerPtrs& w, const int32_t* idx,
-                       const int32_t* count, const uint32_t* mask, float* partial, float* h, int32_t* live,
-                       cudaStream_t s) {
-    if (p.tc) return launch_fc1_tc(p, x, w, idx, count, mask, partial, h, live, s);
-    if (p.st) return launch_fc1_st(p, x, w, idx, count, mask, partial, h, live, s);
-    if (p.fc1_tc4) return launch_fc1_tc4(p, x, w, idx, count, mask, partial, h, live, s);
-    if (p.st4) return launch_fc1_st4(p, x, w, idx, count, mask, partial, h, live, s);
+cudaError_t launch_fc1_chunked(const Plan& p, const __half* x, const LayerPtrs& w, const ColdPtrs& cold,
+                               const int32_t* idx, const int32_t* count, const uint32_t* mask, float* h,
+                               cudaStream_t s) {
     const int kind = p.int4 ? 2 : (p.gated ? 1 : 0);
     return for_token_chunks(p.B, [&](int b0, int tb) -> cudaError_t {
         const size_t sm = (size_t)tb * p.d * sizeof(__half);
@@ -682,7 +688,7 @@ cudaError_t launch_fc1(const Plan& p, const __half* x, const LayerPtrs& w, const
     if (tb == TBV && kind == KV) {                                                            \
         e = set_smem(k_fc1<TBV, KV>, sm);                                                     \
         if (e != cudaSuccess) return e;                                                       \
-        launch_pdl(k_fc1<TBV, KV>, grid, 256, sm, s, x, p.B, b0, p.d, w, idx, count, mask, p.W, h); \
+        launch_pdl(k_fc1<TBV, KV>, grid, 256, sm, s, x, p.B, b0, p.d, w, cold, idx, count, mask, p.W, h); \
     }
         PI_FC1(1, 0) PI_FC1(2, 0) PI_FC1(4, 0) PI_FC1(8, 0)
         PI_FC1(1, 1) PI_FC1(2, 1) PI_FC1(4, 1) PI_FC1(8, 1)
@@ -692,17 +698,24 @@ cudaError_t launch_fc1(const Plan& p, const __half* x, const LayerPtrs& w, const
     });
 }
 
-cudaError_t launch_fc2(const Plan& p, const float* h, const int32_t* idx, const int32_t* count,
-                       const LayerPtrs& w, const int32_t* live, float* partial, float* y, cudaStream_t s) {
-    if (p.tc) return launch_fc2_tc(p, h, idx, count, w, live, partial, y, s);
-    if (p.st) return launch_fc2_st(p, h, idx, count, w, live, partial, y, s);
-    if (p.st4) return launch_fc2_st4(p, h, idx, count, w, live, partial, y, s);
+cudaError_t launch_fc1(const Plan& p, const __half* x, const LayerPtrs& w, const int32_t* idx,
+                       const int32_t* count, const uint32_t* mask, float* partial, float* h, int32_t* live,
+                       cudaStream_t s) {
+    if (p.tc) return launch_fc1_tc(p, x, w, idx, count, mask, partial, h, live, s);
+    if (p.st) return launch_fc1_st(p, x, w, idx, count, mask, partial, h, live, s);
+    if (p.fc1_tc4) return launch_fc1_tc4(p, x, w, idx, count, mask, partial, h, live, s);
+    if (p.st4) return launch_fc1_st4(p, x, w, idx, count, mask, partial, h, live, s);
+    return launch_fc1_chunked(p, x, w, no_cold_tier(), idx, count, mask, h, s);
+}
+
+cudaError_t launch_fc2_chunked(const Plan& p, const float* h, const int32_t* idx, const int32_t* count,
+                               const LayerPtrs& w, const ColdPtrs& cold, float* partial, float* y, cudaStream_t s) {
     cudaError_t e = for_token_chunks(p.B, [&](int b0, int tb) -> cudaError_t {
         dim3 grid(p.fc2_tiles, p.fc2_splits);
 #define PI_FC2(TBV, IV)                                                                       \
     if (tb == TBV && p.int4 == IV)                                                            \
         launch_pdl(k_fc2_part<TBV, IV>, grid, 256, 0, s, h, p.B, b0, idx, count, p.d, w.w2t, w.w2ts, \
-                                                 partial);
+                   cold, partial);
         PI_FC2(1, false) PI_FC2(2, false) PI_FC2(4, false) PI_FC2(8, false)
         PI_FC2(1, true) PI_FC2(2, true) PI_FC2(4, true) PI_FC2(8, true)
 #undef PI_FC2
@@ -712,6 +725,14 @@ cudaError_t launch_fc2(const Plan& p, const float* h, const int32_t* idx, const 
     const int total4 = p.B * p.d / 4;
     launch_pdl(k_fc2_reduce, (total4 + 31) / 32, 256, 0, s, partial, p.fc2_splits, p.B, p.d, w.b2, y);
     return cudaGetLastError();
+}
+
+cudaError_t launch_fc2(const Plan& p, const float* h, const int32_t* idx, const int32_t* count,
+                       const LayerPtrs& w, const int32_t* live, float* partial, float* y, cudaStream_t s) {
+    if (p.tc) return launch_fc2_tc(p, h, idx, count, w, live, partial, y, s);
+    if (p.st) return launch_fc2_st(p, h, idx, count, w, live, partial, y, s);
+    if (p.st4) return launch_fc2_st4(p, h, idx, count, w, live, partial, y, s);
+    return launch_fc2_chunked(p, h, idx, count, w, no_cold_tier(), partial, y, s);
 }
 
 size_t fc2_part_floats(const Plan& p) {

@@ -10,9 +10,12 @@ calls (FC2 counts the rows whose FC1 output is non-zero for some token).
 
     python -m activation_sparse_ffn_layer_gb300.entry_bench --config c2 --batch 1
     python -m activation_sparse_ffn_layer_gb300.entry_bench --config c5 --batch 4 --once
+    python -m activation_sparse_ffn_layer_gb300.entry_bench --config c4 --cold host
 
 ``--once`` runs every call a few times eagerly and then once more, without
-graphs or timing, which is the shape a profiler capture wants.
+graphs or timing, which is the shape a profiler capture wants.  ``--cold host``
+times the tiered FC calls instead, with the FC rows from ``--n-hot`` on (default
+0: all of them) in pinned host memory, read by the GPU directly.
 """
 from __future__ import annotations
 
@@ -61,7 +64,19 @@ def _time(fn, reps: int = 200) -> float:
     return e0.elapsed_time(e1) / reps * 1e3
 
 
-def run(config: str, batch: int, once: bool = False):
+def _cold_rows(w, n_hot: int, where: str):
+    """The FC rows of w from n_hot on, in pinned host memory or a device buffer."""
+    def cold(t):
+        if t is None:
+            return None
+        c = t[n_hot:].contiguous()
+        return c.cpu().pin_memory() if where == "host" else c.clone()
+    if w.int4:
+        return dict(w1=cold(w.w1_q), w1_scales=cold(w.w1_s), w2t=cold(w.w2t_q), w2t_scales=cold(w.w2t_s))
+    return dict(w1=cold(w.w1), wu=cold(w.wu), w2t=cold(w.w2t))
+
+
+def run(config: str, batch: int, once: bool = False, cold: str = "", n_hot: int = 0):
     from synth import CONFIGS, make_layer, make_tokens
 
     B.lib()
@@ -115,6 +130,24 @@ def run(config: str, batch: int, once: bool = False):
     live = int((h[: n * batch].view(n, batch) != 0).any(dim=1).sum().item()) if n else 0
     calls = [("pi_predict", predict), ("pi_compact", compact), ("pi_sparse_fc1", fc1),
              ("pi_sparse_fc2", fc2), ("pi_rmsnorm_half", norm), ("pi_ffn_layer", layer)]
+    if cold:
+        # the rows from n_hot on in a second tier (0: every FC row)
+        keep = [_cold_rows(w, n_hot, cold) for w in layers]
+        tiers = [B.cold_tier(n_hot, **k) for k in keep]
+
+        def fc1_t():
+            k = nxt()
+            B.pi_sparse_fc1_tiered(desc, x, wst[k], tiers[k], idx, cnt, mask if batch > 1 else None, h)
+
+        def fc2_t():
+            k = nxt()
+            B.pi_sparse_fc2_tiered(desc, h, idx, cnt, wst[k], tiers[k], y, ws)
+
+        def layer_t():
+            k = nxt()
+            B.pi_ffn_layer_tiered(desc, x, wst[k], tiers[k], cfg.tau, ws, y)
+        calls = [("pi_sparse_fc1_tiered", fc1_t), ("pi_sparse_fc2_tiered", fc2_t),
+                 ("pi_ffn_layer_tiered", layer_t)]
     if once:
         for name, fn in calls:
             for _ in range(3):
@@ -131,14 +164,19 @@ def run(config: str, batch: int, once: bool = False):
     fc2_b = live * row
     moved = {"pi_predict": pred_b, "pi_compact": 4 * batch * W + 4 * n, "pi_sparse_fc1": fc1_b,
              "pi_sparse_fc2": fc2_b, "pi_rmsnorm_half": batch * d * 6,
-             "pi_ffn_layer": pred_b + fc1_b + fc2_b}
+             "pi_ffn_layer": pred_b + fc1_b + fc2_b, "pi_sparse_fc1_tiered": fc1_b,
+             "pi_sparse_fc2_tiered": fc2_b, "pi_ffn_layer_tiered": pred_b + fc1_b + fc2_b}
+    extra = {}
+    if cold:
+        listed = idx[:n].cpu()
+        extra = {"cold": cold, "n_hot": n_hot, "listed_cold": int((listed >= n_hot).sum().item())}
     peak = _peak_gbs()
     for name, fn in calls:
         us = _time(fn)
         gbs = moved[name] / us / 1e3
         print(json.dumps({"call": name, "config": config, "batch": batch, "us": round(us, 2),
                           "bytes": moved[name], "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
-                          "listed": n, "live": live}), flush=True)
+                          "listed": n, "live": live, **extra}), flush=True)
 
 
 def main(argv=None):
@@ -146,9 +184,13 @@ def main(argv=None):
     ap.add_argument("--config", default="c2")
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--once", action="store_true", help="run each call once after a warm-up (profiler captures)")
+    ap.add_argument("--cold", default="", choices=["", "host", "device"],
+                    help="time the tiered FC calls with the rows past the hot prefix in pinned host memory "
+                         "or in a second device buffer")
+    ap.add_argument("--n-hot", type=int, default=0, help="rows kept in the first tier with --cold (0: none)")
     args = ap.parse_args(argv)
     assert torch.cuda.is_available(), "needs a CUDA GPU"
-    run(args.config, args.batch, args.once)
+    run(args.config, args.batch, args.once, args.cold, args.n_hot)
 
 
 if __name__ == "__main__":

@@ -164,7 +164,7 @@ def kernel_source_hash():
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "activation_sparse_ffn_layer_gb300", "csrc")
-    for name in ("pi_fused.cu", "pi_common.cuh", "pi_internal.h"):
+    for name in ("pi_fused.cu", "pi_common.cuh"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -282,6 +282,7 @@ def summary_line(res, peak):
             "frac": round(achieved / peak, 4), "predicted_per_layer": round(res["n_pred"], 1),
             "l2": ("inputs larger than L2" if res["R"] == 1 else
                    f"{res['R']} copies of the stack in rotation, one per step"),
+            "traffic": recorded_traffic(cfg.key) if res["launches"] == 1 and B == 1 and res["L"] == cfg.layers else None,
             "steps": K}
 
 

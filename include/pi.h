@@ -180,6 +180,48 @@ PI_API pi_status pi_sparse_fc2_noalloc(const pi_layer_desc *desc, const float *h
                                        void *stream);
 
 /*
+ * Second tier of a layer's FC rows (PowerInfer summary (CSDN), sections
+ * "Neuron placement and management" and "GPU-CPU hybrid execution": the hot
+ * neurons stay in GPU memory and the cold ones in the host's memory).  Storage
+ * rows 0 .. n_hot-1 (the hot prefix of the neuron table) are read from the
+ * pi_layer_weights arrays, rows n_hot .. F-1 from these arrays at row
+ * k - n_hot.  The arrays may be host memory that the GPU addresses directly
+ * (pinned and mapped, as from cudaHostAlloc; on a Grace-Blackwell system the
+ * Grace memory, read over NVLink-C2C) or device memory; they are read with
+ * plain 16-byte loads, never with bulk copies.  Same element layout as the
+ * pi_layer_weights arrays; 16-byte aligned.
+ */
+typedef struct {
+    int n_hot;                 /* 0 .. F                                              */
+    const void *w1;            /* [F - n_hot, d] fp16 or [F - n_hot, d/2] INT4 codes   */
+    const pi_half *w1_scales;  /* [F - n_hot, d/32] (INT4 only, else NULL)             */
+    const pi_half *wu;         /* [F - n_hot, d] fp16 (gated only, else NULL)          */
+    const void *w2t;           /* [F - n_hot, d] fp16 or INT4 codes                    */
+    const pi_half *w2t_scales; /* [F - n_hot, d/32] (INT4 only, else NULL)             */
+} pi_cold_tier;
+
+/*
+ * pi_sparse_fc1 / pi_sparse_fc2 with the rows of `cold` for the storage rows
+ * from cold->n_hot on (same results; the per-token CUDA-core kernels, in
+ * chunks of <= 8 tokens, for every batch size).  pi_sparse_fc1_tiered needs no
+ * workspace; pi_sparse_fc2_tiered takes pi_workspace_bytes(desc) bytes.
+ * PI_ERR_INVALID_ARG if n_hot is outside 0..F or a needed pointer is NULL or
+ * misaligned.
+ */
+PI_API pi_status pi_sparse_fc1_tiered(const pi_layer_desc *desc, const pi_half *x, const pi_layer_weights *w,
+                                      const pi_cold_tier *cold, const int32_t *idx, const int32_t *d_count,
+                                      const uint32_t *mask, float *h, void *stream);
+PI_API pi_status pi_sparse_fc2_tiered(const pi_layer_desc *desc, const float *h, const int32_t *idx,
+                                      const int32_t *d_count, const pi_layer_weights *w, const pi_cold_tier *cold,
+                                      float *y, void *workspace, size_t ws_bytes, void *stream);
+/* One decode layer whose cold FC rows live in `cold`: predictor (weights in
+ * w) -> compaction -> pi_sparse_fc1_tiered -> pi_sparse_fc2_tiered.  The
+ * workspace holds the same intermediates as for pi_ffn_layer. */
+PI_API pi_status pi_ffn_layer_tiered(const pi_layer_desc *desc, const pi_half *x, const pi_layer_weights *w,
+                                     const pi_cold_tier *cold, float tau, void *workspace, size_t ws_bytes,
+                                     float *y, void *stream);
+
+/*
  * One whole decode layer: predictor -> compaction -> FC1 -> FC2 on `stream`.
  * x: [B, d] fp16; y: [B, d] fp32.  The per-token masks, the union index list
  * and its count are left in the workspace (see pi_workspace_layout).
