@@ -469,7 +469,7 @@ int pi_launches_per_layer(const pi_layer_desc* desc) {
     // reduction (tcgen05 path: all tokens at once) or FC1 and FC2 per chunk + 1
     // tcgen05 path: predictor u + finish + s, compaction, FC1 + finish, FC2 + reduction
     // predictor: u GEMM + finish + s GEMM on the streamed paths, else 2 per token chunk
-    const int pred = (p.pred == 2 && p.r % 16 == 0) || p.pred == 1 ? 3 : 2 * chunks;
+    const int pred = (p.pred == 2 && p.r % 16 == 0) ? 3 : p.pred_units() ? 2 : p.pred == 1 ? 3 : 2 * chunks;
     // FC1 + finish and FC2 + reduction on the streamed paths, else 1 per chunk each + 1
     const int ffn = (p.tc || p.st || p.st4) ? 4 : chunks + chunks + 1;
     return pred + 1 + ffn;

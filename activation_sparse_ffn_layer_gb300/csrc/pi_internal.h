@@ -53,6 +53,10 @@ struct Plan {
     bool fc1_tc4;   // INT4 FC1 on the tensor cores (codes as fp16, group scales in the epilogue; batch 16-32)
     int pred;       // predictor path (its weights are fp16 for every weight type):
                     // 2 tcgen05 (batch 16..32), 1 streamed CUDA cores (batch 2..8), 0 chunked
+    // predictor of a small batch in one pass over P2 (16-row warp units, all
+    // tokens at once): up to 2 tokens at any rank, up to 4 up to rank 512
+    // (past that the streamed kernel is faster at 3-4 tokens)
+    bool pred_units() const { return pred != 2 && (B <= 2 || (B <= 4 && r <= 512)); }
     size_t part_floats;  // split partial sums: the largest need of the predictor, FC1 and FC2 paths taken
     size_t off_mask, off_idx, off_count, off_h, off_upart, off_part, off_xbuf, off_live, off_uhl, total;
 };

@@ -129,17 +129,19 @@ __global__ void __launch_bounds__(128) k_predict_s(const __half* __restrict__ p2
     }
 }
 
-// One token: mask bits of 16-row units.  A warp takes unit m (rows 16m ..
-// 16m+15), its lanes the rows' 8-element vectors v = lane, lane + 32, ...; the
-// 16 rows' vectors of one step are requested before any arithmetic on them.
-// A halving butterfly then leaves row k's dot product in lanes 2k', 2k'+1
-// (k = fold16_row), and one ballot gives the unit's 16 mask bits, stored as the
-// low or high half of mask word m / 2 (every unit up to 2 W is written, the
-// ones past F as zeros).  u is the sum of the split partials, staged per block.
+// TB tokens (1..4): mask bits of 16-row units.  A warp takes unit m (rows 16m
+// .. 16m+15), its lanes the rows' 8-element vectors v = lane, lane + 32, ...;
+// the 16 rows' vectors of one step are requested before any arithmetic on them
+// and used for every token.  A halving butterfly then leaves row k's dot
+// product in lanes 2k', 2k'+1 (k = fold16_row), and one ballot per token gives
+// the unit's 16 mask bits, stored as the low or high half of mask word m / 2
+// (every unit up to 2 W is written, the ones past F as zeros).  u is the sum of
+// the split partials, staged per block.
+template <int TB>
 __global__ void __launch_bounds__(256) k_predict_s1(const __half* __restrict__ p2, const __half* __restrict__ bias,
-                                                    const float* __restrict__ upart, int usplits, int r, int F,
-                                                    int W, float tau, uint32_t* __restrict__ mask) {
-    extern __shared__ __align__(16) float us[];  // [r]
+                                                    const float* __restrict__ upart, int usplits, int B, int b0,
+                                                    int r, int F, int W, float tau, uint32_t* __restrict__ mask) {
+    extern __shared__ __align__(16) float us[];  // [TB][r]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m = blockIdx.x * 8 + warp;
     const int nvec = r / 8;
@@ -160,49 +162,59 @@ __global__ void __launch_bounds__(256) k_predict_s1(const __half* __restrict__ p
     load(0, w);
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
-    for (int i = threadIdx.x; i < r; i += blockDim.x) {
+    for (int e = threadIdx.x; e < TB * r; e += blockDim.x) {
+        const int t = e / r, i = e - t * r;
         float v = 0.f;
-        for (int s = 0; s < usplits; ++s) v += upart[(size_t)s * r + i];
-        us[i] = v;
+        for (int s = 0; s < usplits; ++s) v += upart[((size_t)s * B + b0 + t) * r + i];
+        us[e] = v;
     }
     __syncthreads();
     if (m >= 2 * W) return;
-    float v[16];
+    float v[TB][16];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) v[k] = 0.f;
+    for (int t = 0; t < TB; ++t)
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[t][k] = 0.f;
     for (int vi0 = 0; vi0 < nvec; vi0 += 32) {
         const int vi = vi0 + lane;
         const bool vok = vi < nvec;
         if (vi0 > 0) load(vi0, w);
         if (vok) {
-            const float4 ua = reinterpret_cast<const float4*>(us + vi * 8)[0];
-            const float4 ub = reinterpret_cast<const float4*>(us + vi * 8)[1];
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
                 float wf[8];
                 h8_to_f8(w[k], wf);
-                float a = v[k];
-                a = fmaf(wf[0], ua.x, a);
-                a = fmaf(wf[1], ua.y, a);
-                a = fmaf(wf[2], ua.z, a);
-                a = fmaf(wf[3], ua.w, a);
-                a = fmaf(wf[4], ub.x, a);
-                a = fmaf(wf[5], ub.y, a);
-                a = fmaf(wf[6], ub.z, a);
-                a = fmaf(wf[7], ub.w, a);
-                v[k] = a;
+#pragma unroll
+                for (int t = 0; t < TB; ++t) {
+                    const float4 ua = reinterpret_cast<const float4*>(us + t * r + vi * 8)[0];
+                    const float4 ub = reinterpret_cast<const float4*>(us + t * r + vi * 8)[1];
+                    float a = v[t][k];
+                    a = fmaf(wf[0], ua.x, a);
+                    a = fmaf(wf[1], ua.y, a);
+                    a = fmaf(wf[2], ua.z, a);
+                    a = fmaf(wf[3], ua.w, a);
+                    a = fmaf(wf[4], ub.x, a);
+                    a = fmaf(wf[5], ub.y, a);
+                    a = fmaf(wf[6], ub.z, a);
+                    a = fmaf(wf[7], ub.w, a);
+                    v[t][k] = a;
+                }
             }
         }
     }
-    const float tot = fold16(v, lane);
     const int k = 16 * m + fold16_row(lane);
-    const bool pred = (lane & 1) == 0 && k < F && tot + __half2float(bias[k < F ? k : 0]) > tau;
-    const unsigned bal = __ballot_sync(FULL, pred);
-    if (lane == 0) {
-        unsigned bits = 0;
+    const float bk = __half2float(bias[k < F ? k : 0]);
 #pragma unroll
-        for (int L = 0; L < 32; L += 2) bits |= ((bal >> L) & 1u) << fold16_row(L);
-        reinterpret_cast<uint16_t*>(mask)[m] = (uint16_t)bits;
+    for (int t = 0; t < TB; ++t) {
+        const float tot = fold16(v[t], lane);
+        const bool pred = (lane & 1) == 0 && k < F && tot + bk > tau;
+        const unsigned bal = __ballot_sync(FULL, pred);
+        if (lane == 0) {
+            unsigned bits = 0;
+#pragma unroll
+            for (int L = 0; L < 32; L += 2) bits |= ((bal >> L) & 1u) << fold16_row(L);
+            reinterpret_cast<uint16_t*>(mask + (size_t)(b0 + t) * W)[m] = (uint16_t)bits;
+        }
     }
 }
 
@@ -621,6 +633,27 @@ cudaError_t launch_predict(const Plan& p, const __half* x, const __half* p1, con
         return launch_predict_tc(p, x, p1, p2, bpred, tau, mask,
                                  reinterpret_cast<float*>(static_cast<char*>(ws) + p.off_part),
                                  reinterpret_cast<__half*>(static_cast<char*>(ws) + p.off_uhl), s);
+    if (p.pred_units()) {
+        // the whole batch in one chunk: P2 is read once for every token
+        float* upart = reinterpret_cast<float*>(static_cast<char*>(ws) + p.off_upart);
+        const dim3 gu((p.r + 7) / 8, p.u_splits);
+        const int tb = p.B, b0 = 0;
+        cudaError_t e = cudaSuccess;
+        const size_t sm1 = (size_t)tb * p.r * sizeof(float);
+        const dim3 gs((2 * p.W + 7) / 8);
+#define PI_PRED1(TBV)                                                                                        \
+    if (tb == TBV) {                                                                                          \
+        launch_pdl(k_predict_u<TBV>, gu, 256, 0, s, x, p.B, b0, p1, p.d, p.r, p.u_seg, upart);                 \
+        e = set_smem(k_predict_s1<TBV>, sm1);                                                                 \
+        if (e != cudaSuccess) return e;                                                                       \
+        e = launch_pdl(k_predict_s1<TBV>, gs, 256, sm1, s, p2, bpred, static_cast<const float*>(upart),      \
+                       p.u_splits, p.B, b0, p.r, p.F, p.W, tau, mask);                                        \
+    }
+        PI_PRED1(1) PI_PRED1(2) PI_PRED1(3) PI_PRED1(4)
+#undef PI_PRED1
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
     if (p.pred == 1)
         return launch_predict_st(p, x, p1, p2, bpred, tau, mask,
                                  reinterpret_cast<float*>(static_cast<char*>(ws) + p.off_part),
@@ -639,24 +672,6 @@ cudaError_t launch_predict(const Plan& p, const __half* x, const __half* p1, con
                                              tau, mask);                                           \
         break;                                                                                     \
     }
-        if (tb == 1 && p.B == 1) {
-            launch_pdl(k_predict_u<1>, gu, 256, 0, s, x, p.B, b0, p1, p.d, p.r, p.u_seg, upart);
-            const size_t sm1 = (size_t)p.r * sizeof(float);
-            cudaError_t e = set_smem(k_predict_s1, sm1);
-            if (e != cudaSuccess) return e;
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3((2 * p.W + 7) / 8);
-            cfg.blockDim = dim3(256);
-            cfg.dynamicSmemBytes = sm1;
-            cfg.stream = s;
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-            attr[0].val.programmaticStreamSerializationAllowed = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            return cudaLaunchKernelEx(&cfg, k_predict_s1, p2, bpred, static_cast<const float*>(upart), p.u_splits,
-                                      p.r, p.F, p.W, tau, mask);
-        }
         switch (tb) {
             PI_PRED(1)
             PI_PRED(2)

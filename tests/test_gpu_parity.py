@@ -72,7 +72,7 @@ def test_predict_mask_parity_small(shape):
         mask_matches(mask.cpu().numpy().view(np.uint32), o, w.F, cfg.tau, f"token {t}")
 
 
-@pytest.mark.parametrize("batch", [2, 3, 8, 11])
+@pytest.mark.parametrize("batch", [2, 3, 4, 8, 11])
 def test_predict_batched_matches_per_token(batch):
     P = _pi()
     cfg = small(CONFIGS["c3"], d=512, F=2080, rank=96, per_layer_rates=())
