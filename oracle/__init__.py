@@ -45,11 +45,12 @@ def lib():
         L.oracle_ffn_masked.argtypes = [C.c_int, C.c_int, C.c_int, P, P, P, P, P, P, P, P, P]
         L.oracle_ffn_dense.argtypes = [C.c_int, C.c_int, C.c_int, P, P, P, P, P, P, P]
         L.oracle_rmsnorm_half.argtypes = [C.c_int, P, C.c_double, C.c_double, P, P, P]
+        L.oracle_attn_heads.argtypes = [C.c_int] * 6 + [P] * 10
         L.oracle_set_threads.argtypes = [C.c_int]
         L.oracle_threads.restype = C.c_int
         for name in ("oracle_decode_row", "oracle_predict", "oracle_compact", "oracle_mask_union",
                      "oracle_fc1", "oracle_fc2", "oracle_ffn_masked", "oracle_ffn_dense",
-                     "oracle_rmsnorm_half"):
+                     "oracle_rmsnorm_half", "oracle_attn_heads"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -247,3 +248,56 @@ def layer_step(x, w, tau: float, eps: float = 1e-6):
     idx, _, n = compact(pr["mask"], L.F, L.table)
     y = ffn_masked(x, L, pr["mask"])
     return dict(mask=pr["mask"], s=pr["s"], band=pr["band"], idx=idx, count=n, y=y)
+
+
+# ------------------------------------------------------- attention heads
+
+def attn_predict(x, p1, p2, bp, tau: float, unit_roundoff: float = FP32_UNIT_ROUNDOFF):
+    """Head predictor of one token (oracle_predict with F = number of heads):
+    dict(u, s, band, mask)."""
+    xb = _np(x, np.uint16)
+    P1, P2, BP = _np(p1, np.uint16), _np(p2, np.uint16), _np(bp, np.uint16)
+    r, d = P1.shape
+    H = P2.shape[0]
+    u = np.empty(r, np.float64)
+    s = np.empty(H, np.float64)
+    band = np.empty(H, np.float64)
+    mask = np.empty((H + 31) // 32, np.uint32)
+    _check(lib().oracle_predict(d, H, r, _p(xb), _p(P1), _p(P2), _p(BP), float(tau), float(unit_roundoff),
+                                _p(u), _p(s), _p(band), _p(mask)), "oracle_predict")
+    return dict(u=u, s=s, band=band, mask=mask)
+
+
+def attn_heads(x, wqkv, bqkv, wot, bo, head_mask, kcache, vcache, pos, H: int, KVH: int, dh: int):
+    """One decode token per sequence through the head-sparse attention block.
+
+    x [B, d] fp16; wqkv [(H + 2 KVH) dh, d], bqkv, wot [H dh, d], bo [d] fp16;
+    head_mask [B, ceil(H/32)] uint32; kcache, vcache [B, KVH, smax, dh] fp16
+    (not modified: updated copies are returned); pos [B] ints.
+    Returns dict(y [B, d] float64, o [B, H dh] float64, kcache, vcache as
+    uint16 bit arrays with position pos[b] written)."""
+    xb = _np(x, np.uint16)
+    if xb.ndim == 1:
+        xb = xb[None]
+    B, d = xb.shape
+    W, Bq, Wo, Bo = _np(wqkv, np.uint16), _np(bqkv, np.uint16), _np(wot, np.uint16), _np(bo, np.uint16)
+    m = _np(head_mask, np.uint32).reshape(B, -1)
+    kc = _np(kcache, np.uint16).copy()
+    vc = _np(vcache, np.uint16).copy()
+    smax = kc.shape[-2]
+    kc = kc.reshape(B, KVH, smax, dh)
+    vc = vc.reshape(B, KVH, smax, dh)
+    ps = [int(v) for v in np.asarray(pos).ravel()]
+    y = np.empty((B, d), np.float64)
+    o = np.empty((B, H * dh), np.float64)
+    for b in range(B):
+        kb = np.ascontiguousarray(kc[b])
+        vb = np.ascontiguousarray(vc[b])
+        xr = np.ascontiguousarray(xb[b])
+        mr = np.ascontiguousarray(m[b])
+        yr = np.empty(d, np.float64)
+        orow = np.empty(H * dh, np.float64)
+        _check(lib().oracle_attn_heads(d, H, KVH, dh, smax, ps[b], _p(xr), _p(W), _p(Bq), _p(Wo), _p(Bo),
+                                       _p(mr), _p(kb), _p(vb), _p(orow), _p(yr)), "oracle_attn_heads")
+        kc[b], vc[b], y[b], o[b] = kb, vb, yr, orow
+    return dict(y=y, o=o, kcache=kc, vcache=vc)

@@ -33,7 +33,13 @@
  *    the low nibble, value q * scale, one scale per 32 consecutive elements;
  *  - gated layer: h = ReLU(Wg x + bg) * (Wu x);
  *  - inter-layer normalisation: x' = fp16(y / sqrt(mean(y^2) + eps)), round
- *    to nearest even.
+ *    to nearest even;
+ *  - attention heads as the self-attention block's neurons (see
+ *    oracle_attn_heads): the head mask comes from the same low-rank predictor
+ *    form (oracle_predict with F = heads); a head not predicted active adds
+ *    nothing to this token's output, but the token's key and value are
+ *    projected for every KV head and stored as binary16, so the cache stays
+ *    complete for later tokens.
  *
  * Every function returns 0 on success and a negative value on a bad argument.
  */
@@ -411,5 +417,122 @@ int oracle_rmsnorm_half(int d, const double *y, double eps, double unit_roundoff
         if (band)
             band[c] = 2.0 * rel * fabs(v);
     }
+    return 0;
+}
+
+/* ------------------------------------------------------- attention heads */
+
+/*
+ * One decode token through a self-attention block whose neurons are its
+ * heads.  Sources: PowerInfer summary (CSDN), section "Background", paragraph
+ * on activation sparsity (in the self-attention block about half of the heads
+ * contribute little, so that block is sparse too) and section "Adaptive
+ * sparse predictor"; the unite.ai page, section on adaptive sparsity
+ * predictors (one predictor for the MLP block and one for the self-attention
+ * block of each layer, and only the neurons predicted active are computed).
+ *
+ * For the token x (binary16, length d) with cache positions 0 .. pos-1 filled:
+ *   k_g = Wk_g x + bk_g,  v_g = Wv_g x + bv_g   for every KV head g, stored as
+ *                          binary16 (nearest even) at cache position pos;
+ *   for every head h whose bit is set in head_mask (KV head g = h / (H/KVH)):
+ *     q   = Wq_h x + bq_h
+ *     a_t = exp(e_t - max_t e_t) / sum_t exp(e_t - max_t e_t),
+ *           e_t = (q . K_g[t]) / sqrt(dh),   t = 0 .. pos (the new token included)
+ *     o_h = sum_t a_t V_g[t]
+ *   y = bo + sum over those h of  sum_i o_h[i] * Wot[h*dh + i, :]
+ * Heads whose bit is clear: no query, no attention, no output-projection rows.
+ *
+ * Layouts (binary16 bit patterns): wqkv [(H + 2 KVH) dh, d] with the query
+ * rows of head h at h*dh, the key rows of KV head g at (H + g) dh and its value
+ * rows at (H + KVH + g) dh; bqkv [(H + 2 KVH) dh]; wot = Wo transposed,
+ * [H dh, d], row j = column j of Wo; bo [d]; kcache, vcache [KVH, smax, dh]
+ * (position pos is written); head_mask ceil(H/32) words.  y [d] out;
+ * o_out (nullable) [H dh]: every o_h, zero for heads left out.
+ */
+int oracle_attn_heads(int d, int H, int KVH, int dh, int smax, int pos, const uint16_t *x,
+                      const uint16_t *wqkv, const uint16_t *bqkv, const uint16_t *wot,
+                      const uint16_t *bo, const uint32_t *head_mask, uint16_t *kcache,
+                      uint16_t *vcache, double *o_out, double *y)
+{
+    if (d <= 0 || H <= 0 || KVH <= 0 || H % KVH != 0 || dh <= 0 || smax <= 0 || pos < 0 ||
+        pos >= smax || !x || !wqkv || !bqkv || !wot || !bo || !head_mask || !kcache || !vcache || !y)
+        return -1;
+    const int G = H / KVH;
+    const long nkv = 2L * KVH * dh;
+    double *kv = (double *)malloc(sizeof(double) * (size_t)nkv);
+    double *q = (double *)malloc(sizeof(double) * (size_t)dh);
+    double *e = (double *)malloc(sizeof(double) * (size_t)(pos + 1));
+    double *o = (double *)malloc(sizeof(double) * (size_t)dh);
+    if (!kv || !q || !e || !o) {
+        free(kv);
+        free(q);
+        free(e);
+        free(o);
+        return -2;
+    }
+    /* keys and values of the new token, every KV head */
+#pragma omp parallel for schedule(static)
+    for (long j = 0; j < nkv; ++j) {
+        long row = (long)H * dh + j;
+        double acc = oracle_half_to_double(bqkv[row]);
+        for (int c = 0; c < d; ++c)
+            acc += oracle_half_to_double(wqkv[row * d + c]) * oracle_half_to_double(x[c]);
+        kv[j] = acc;
+    }
+    for (int g = 0; g < KVH; ++g)
+        for (int i = 0; i < dh; ++i) {
+            long at = ((long)g * smax + pos) * dh + i;
+            kcache[at] = oracle_double_to_half(kv[(long)g * dh + i]);
+            vcache[at] = oracle_double_to_half(kv[(long)KVH * dh + (long)g * dh + i]);
+        }
+    for (int c = 0; c < d; ++c)
+        y[c] = oracle_half_to_double(bo[c]);
+    if (o_out)
+        memset(o_out, 0, sizeof(double) * (size_t)H * dh);
+    const double inv_sqrt = 1.0 / sqrt((double)dh);
+    for (int h = 0; h < H; ++h) {
+        if (!mask_bit(head_mask, h))
+            continue;
+        const int g = h / G;
+        for (int i = 0; i < dh; ++i) {
+            long row = (long)h * dh + i;
+            double acc = oracle_half_to_double(bqkv[row]);
+            for (int c = 0; c < d; ++c)
+                acc += oracle_half_to_double(wqkv[row * d + c]) * oracle_half_to_double(x[c]);
+            q[i] = acc;
+        }
+        double emax = -INFINITY;
+        for (int t = 0; t <= pos; ++t) {
+            double acc = 0.0;
+            for (int i = 0; i < dh; ++i)
+                acc += q[i] * oracle_half_to_double(kcache[((long)g * smax + t) * dh + i]);
+            e[t] = acc * inv_sqrt;
+            if (e[t] > emax)
+                emax = e[t];
+        }
+        double den = 0.0;
+        for (int t = 0; t <= pos; ++t)
+            den += exp(e[t] - emax);
+        for (int i = 0; i < dh; ++i)
+            o[i] = 0.0;
+        for (int t = 0; t <= pos; ++t) {
+            double a = exp(e[t] - emax) / den;
+            for (int i = 0; i < dh; ++i)
+                o[i] += a * oracle_half_to_double(vcache[((long)g * smax + t) * dh + i]);
+        }
+        if (o_out)
+            memcpy(o_out + (long)h * dh, o, sizeof(double) * (size_t)dh);
+#pragma omp parallel for schedule(static)
+        for (int c = 0; c < d; ++c) {
+            double acc = 0.0;
+            for (int i = 0; i < dh; ++i)
+                acc += o[i] * oracle_half_to_double(wot[((long)h * dh + i) * d + c]);
+            y[c] += acc;
+        }
+    }
+    free(kv);
+    free(q);
+    free(e);
+    free(o);
     return 0;
 }

@@ -6,3 +6,5 @@ Holds workload shapes (:mod:`synth.configs`) and the tensor generator
 from .configs import CONFIGS, Config, small  # noqa: F401
 from .generate import (LayerWeights, make_layer, make_tokens, neuron_table,  # noqa: F401
                        zipf_probabilities, outlier_channels, hot_coverage, predictor_param_share)
+from .attention import (ATTN_CONFIGS, AttnConfig, AttnWeights, make_attn, make_kv_cache,  # noqa: F401
+                        decode_lengths, small_attn)
