@@ -45,7 +45,7 @@ def lib():
         L.oracle_ffn_masked.argtypes = [C.c_int, C.c_int, C.c_int, P, P, P, P, P, P, P, P, P]
         L.oracle_ffn_dense.argtypes = [C.c_int, C.c_int, C.c_int, P, P, P, P, P, P, P]
         L.oracle_rmsnorm_half.argtypes = [C.c_int, P, C.c_double, C.c_double, P, P, P]
-        L.oracle_attn_heads.argtypes = [C.c_int] * 6 + [P] * 10
+        L.oracle_attn_heads.argtypes = [C.c_int] * 6 + [P] * 10 + [C.c_double, P, P]
         L.oracle_set_threads.argtypes = [C.c_int]
         L.oracle_threads.restype = C.c_int
         for name in ("oracle_decode_row", "oracle_predict", "oracle_compact", "oracle_mask_union",
@@ -268,14 +268,16 @@ def attn_predict(x, p1, p2, bp, tau: float, unit_roundoff: float = FP32_UNIT_ROU
     return dict(u=u, s=s, band=band, mask=mask)
 
 
-def attn_heads(x, wqkv, bqkv, wot, bo, head_mask, kcache, vcache, pos, H: int, KVH: int, dh: int):
+def attn_heads(x, wqkv, bqkv, wot, bo, head_mask, kcache, vcache, pos, H: int, KVH: int, dh: int,
+               unit_roundoff: float = FP32_UNIT_ROUNDOFF):
     """One decode token per sequence through the head-sparse attention block.
 
     x [B, d] fp16; wqkv [(H + 2 KVH) dh, d], bqkv, wot [H dh, d], bo [d] fp16;
     head_mask [B, ceil(H/32)] uint32; kcache, vcache [B, KVH, smax, dh] fp16
     (not modified: updated copies are returned); pos [B] ints.
     Returns dict(y [B, d] float64, o [B, H dh] float64, kcache, vcache as
-    uint16 bit arrays with position pos[b] written)."""
+    uint16 bit arrays with position pos[b] written, kv_pre / kv_band [B, 2 KVH dh]:
+    the new keys then values before rounding, and the fp32 evaluation bound)."""
     xb = _np(x, np.uint16)
     if xb.ndim == 1:
         xb = xb[None]
@@ -290,6 +292,8 @@ def attn_heads(x, wqkv, bqkv, wot, bo, head_mask, kcache, vcache, pos, H: int, K
     ps = [int(v) for v in np.asarray(pos).ravel()]
     y = np.empty((B, d), np.float64)
     o = np.empty((B, H * dh), np.float64)
+    pre = np.empty((B, 2 * KVH * dh), np.float64)
+    band = np.empty((B, 2 * KVH * dh), np.float64)
     for b in range(B):
         kb = np.ascontiguousarray(kc[b])
         vb = np.ascontiguousarray(vc[b])
@@ -297,7 +301,10 @@ def attn_heads(x, wqkv, bqkv, wot, bo, head_mask, kcache, vcache, pos, H: int, K
         mr = np.ascontiguousarray(m[b])
         yr = np.empty(d, np.float64)
         orow = np.empty(H * dh, np.float64)
+        pr = np.empty(2 * KVH * dh, np.float64)
+        bd = np.empty(2 * KVH * dh, np.float64)
         _check(lib().oracle_attn_heads(d, H, KVH, dh, smax, ps[b], _p(xr), _p(W), _p(Bq), _p(Wo), _p(Bo),
-                                       _p(mr), _p(kb), _p(vb), _p(orow), _p(yr)), "oracle_attn_heads")
-        kc[b], vc[b], y[b], o[b] = kb, vb, yr, orow
-    return dict(y=y, o=o, kcache=kc, vcache=vc)
+                                       _p(mr), _p(kb), _p(vb), _p(orow), _p(yr), float(unit_roundoff), _p(pr),
+                                       _p(bd)), "oracle_attn_heads")
+        kc[b], vc[b], y[b], o[b], pre[b], band[b] = kb, vb, yr, orow, pr, bd
+    return dict(y=y, o=o, kcache=kc, vcache=vc, kv_pre=pre, kv_band=band)

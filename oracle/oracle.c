@@ -448,11 +448,16 @@ int oracle_rmsnorm_half(int d, const double *y, double eps, double unit_roundoff
  * [H dh, d], row j = column j of Wo; bo [d]; kcache, vcache [KVH, smax, dh]
  * (position pos is written); head_mask ceil(H/32) words.  y [d] out;
  * o_out (nullable) [H dh]: every o_h, zero for heads left out.
+ * kv_pre, kv_band (nullable) [2 KVH dh]: the keys then the values before
+ * rounding, and a bound (factor-2 margin) on how far an fp32 evaluation of
+ * each, in any summation order with unit roundoff `unit_roundoff`, can be
+ * from it: 2 gamma(d + 1) (sum_c |w_c x_c| + |b|).
  */
 int oracle_attn_heads(int d, int H, int KVH, int dh, int smax, int pos, const uint16_t *x,
                       const uint16_t *wqkv, const uint16_t *bqkv, const uint16_t *wot,
                       const uint16_t *bo, const uint32_t *head_mask, uint16_t *kcache,
-                      uint16_t *vcache, double *o_out, double *y)
+                      uint16_t *vcache, double *o_out, double *y, double unit_roundoff,
+                      double *kv_pre, double *kv_band)
 {
     if (d <= 0 || H <= 0 || KVH <= 0 || H % KVH != 0 || dh <= 0 || smax <= 0 || pos < 0 ||
         pos >= smax || !x || !wqkv || !bqkv || !wot || !bo || !head_mask || !kcache || !vcache || !y)
@@ -475,9 +480,17 @@ int oracle_attn_heads(int d, int H, int KVH, int dh, int smax, int pos, const ui
     for (long j = 0; j < nkv; ++j) {
         long row = (long)H * dh + j;
         double acc = oracle_half_to_double(bqkv[row]);
-        for (int c = 0; c < d; ++c)
-            acc += oracle_half_to_double(wqkv[row * d + c]) * oracle_half_to_double(x[c]);
+        double mag = fabs(acc);
+        for (int c = 0; c < d; ++c) {
+            double t = oracle_half_to_double(wqkv[row * d + c]) * oracle_half_to_double(x[c]);
+            acc += t;
+            mag += fabs(t);
+        }
         kv[j] = acc;
+        if (kv_pre)
+            kv_pre[j] = acc;
+        if (kv_band)
+            kv_band[j] = 2.0 * gamma_n((double)d + 1.0, unit_roundoff) * mag;
     }
     for (int g = 0; g < KVH; ++g)
         for (int i = 0; i < dh; ++i) {
