@@ -10,4 +10,5 @@ from .binding import (PiError, desc_of, layer_desc, lib, library_path, pi_compac
                       pi_sparse_fc2_noalloc, pi_stack_plan, cold_tier, pi_sparse_fc1_tiered,
                       pi_sparse_fc2_tiered, pi_ffn_layer_tiered,
                       pi_status_string, pi_workspace_bytes, pi_workspace_layout, ranks_array,
-                      weights_array, weights_struct)
+                      weights_array, weights_struct, attn_desc, attn_desc_of, attn_weights_struct,
+                      pi_attn_heads, pi_attn_workspace_bytes)

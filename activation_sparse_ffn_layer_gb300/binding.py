@@ -42,6 +42,14 @@ class pi_stack_plan_t(C.Structure):
                                        "smem_bytes")]
 
 
+class pi_attn_desc(C.Structure):
+    _fields_ = [(n, C.c_int) for n in ("d", "heads", "kv_heads", "head_dim", "rank", "batch", "max_seq")]
+
+
+class pi_attn_weights(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in ("wqkv", "bqkv", "wot", "bo", "p1", "p2", "bp")]
+
+
 class PiError(RuntimeError):
     def __init__(self, fn: str, status: int, msg: str):
         super().__init__(f"{fn}: {msg} (status {status})")
@@ -54,7 +62,7 @@ EXPORTS = ("pi_workspace_bytes", "pi_workspace_layout", "pi_predict", "pi_compac
            "pi_sparse_fc2", "pi_ffn_layer", "pi_rmsnorm_half", "pi_status_string",
            "pi_last_device_status", "pi_launches_per_layer", "pi_ffn_stack", "pi_debug_wait_timeout",
            "pi_sparse_fc2_noalloc", "pi_stack_plan", "pi_debug_set_wait_timeout", "pi_sparse_fc1_tiered",
-           "pi_sparse_fc2_tiered", "pi_ffn_layer_tiered")
+           "pi_sparse_fc2_tiered", "pi_ffn_layer_tiered", "pi_attn_workspace_bytes", "pi_attn_heads")
 
 
 def library_path() -> str:
@@ -94,6 +102,9 @@ def lib(path: Optional[str] = None):
         "pi_sparse_fc1_tiered": (I, [D, P, Wt, C.POINTER(pi_cold_tier), P, P, P, P, P]),
         "pi_sparse_fc2_tiered": (I, [D, P, P, P, Wt, C.POINTER(pi_cold_tier), P, P, S, P]),
         "pi_ffn_layer_tiered": (I, [D, P, Wt, C.POINTER(pi_cold_tier), Fl, P, S, P, P]),
+        "pi_attn_workspace_bytes": (S, [C.POINTER(pi_attn_desc)]),
+        "pi_attn_heads": (I, [C.POINTER(pi_attn_desc), P, C.POINTER(pi_attn_weights), P, P, P, Fl, P, P, P, S,
+                              P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -290,3 +301,33 @@ def pi_launches_per_layer(desc) -> int:
 
 def pi_last_device_status() -> int:
     return int(lib().pi_last_device_status(_stream()))
+
+
+# ------------------------------------------------------- head-sparse attention
+
+def attn_desc_of(d: int, heads: int, kv_heads: int, head_dim: int, rank: int, batch: int = 1,
+                 max_seq: int = 1024) -> pi_attn_desc:
+    return pi_attn_desc(d, heads, kv_heads, head_dim, rank, batch, max_seq)
+
+
+def attn_desc(w, batch: int = 1, max_seq: int = 1024) -> pi_attn_desc:
+    return attn_desc_of(w.d, w.H, w.KVH, w.dh, w.r, batch, max_seq)
+
+
+def attn_weights_struct(w) -> pi_attn_weights:
+    """A pi_attn_weights over an attention block's device tensors (keep `w` alive)."""
+    s = pi_attn_weights()
+    s.wqkv, s.bqkv, s.wot, s.bo = _ptr(w.wqkv), _ptr(w.bqkv), _ptr(w.wot), _ptr(w.bo)
+    s.p1, s.p2, s.bp = _ptr(w.p1), _ptr(w.p2), _ptr(w.bp)
+    return s
+
+
+def pi_attn_workspace_bytes(desc: pi_attn_desc) -> int:
+    return int(lib().pi_attn_workspace_bytes(C.byref(desc)))
+
+
+def pi_attn_heads(desc, x, wstruct, kcache, vcache, pos, tau: float, head_mask, y, workspace):
+    _check("pi_attn_heads", lib().pi_attn_heads(C.byref(desc), _ptr(x), C.byref(wstruct), _ptr(kcache),
+                                                _ptr(vcache), _ptr(pos), float(tau), _ptr(head_mask), _ptr(y),
+                                                _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                                _stream()))

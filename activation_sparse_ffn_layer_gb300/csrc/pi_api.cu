@@ -110,12 +110,12 @@ bool weights_ok(const Plan& p, const pi_layer_weights* w, bool need_w1, bool nee
     if (!w) return false;
     if (need_w1) {
         if (!w->w1 || !w->b1 || !aligned16(w->w1)) return false;
-        if (p.int4 && (!w->w1_scales)) return false;
+        if (p.int4 && (!w->w1_scales || !aligned16(w->w1_scales))) return false;
         if (p.gated && (!w->wu || !aligned16(w->wu))) return false;
     }
     if (need_w2) {
         if (!w->w2t || !w->b2 || !aligned16(w->w2t)) return false;
-        if (p.int4 && !w->w2t_scales) return false;
+        if (p.int4 && (!w->w2t_scales || !aligned16(w->w2t_scales))) return false;
     }
     if (need_pred) {
         if (!w->p1 || !w->p2 || !w->b1 || !aligned16(w->p1) || !aligned16(w->p2)) return false;
@@ -485,6 +485,29 @@ const char* pi_status_string(pi_status s) {
         case PI_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     }
     return "unknown status";
+}
+
+size_t pi_attn_workspace_bytes(const pi_attn_desc* desc) {
+    AttnPlan q;
+    if (!desc || !make_attn_plan(*desc, &q)) return 0;
+    return q.total;
+}
+
+pi_status pi_attn_heads(const pi_attn_desc* desc, const pi_half* x, const pi_attn_weights* w, pi_half* kcache,
+                        pi_half* vcache, const int32_t* pos, float tau, uint32_t* head_mask, float* y,
+                        void* workspace, size_t ws_bytes, void* stream) {
+    AttnPlan q;
+    if (!desc || !make_attn_plan(*desc, &q)) return PI_ERR_INVALID_ARG;
+    if (!x || !w || !kcache || !vcache || !pos || !head_mask || !y || !aligned16(x) || !aligned16(kcache) ||
+        !aligned16(vcache) || !aligned16(y) || !aligned16(head_mask))
+        return PI_ERR_INVALID_ARG;
+    if (!w->wqkv || !w->bqkv || !w->wot || !w->bo || !w->p1 || !w->p2 || !w->bp || !aligned16(w->wqkv) ||
+        !aligned16(w->wot) || !aligned16(w->p1) || !aligned16(w->p2))
+        return PI_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace) || ws_bytes < q.total) return PI_ERR_WORKSPACE;
+    return from_cuda(launch_attn(q, reinterpret_cast<const __half*>(x), *w, reinterpret_cast<__half*>(kcache),
+                                 reinterpret_cast<__half*>(vcache), pos, tau, head_mask, y, workspace,
+                                 static_cast<cudaStream_t>(stream)));
 }
 
 pi_status pi_last_device_status(void* stream) {

@@ -51,6 +51,8 @@ struct Plan {
     bool st;        // ... or the CUDA-core streamed batched path (batch 2..8, fp16 weights)
     bool st4;       // ... or its INT4 variant (batch 2..16, ReLU FFN)
     bool fc1_tc4;   // INT4 FC1 on the tensor cores (codes as fp16, group scales in the epilogue; batch 16-32)
+    bool proj;      // rows are a plain projection (bias, no activation): the
+                    // query/key/value rows of the attention block, not FFN rows
     int pred;       // predictor path (its weights are fp16 for every weight type):
                     // 2 tcgen05 (batch 16..32), 1 streamed CUDA cores (batch 2..8), 0 chunked
     // predictor of a small batch in one pass over P2 (16-row warp units, all
@@ -116,6 +118,19 @@ cudaError_t launch_fc1(const Plan& p, const __half* x, const LayerPtrs& w, const
                        cudaStream_t s);
 cudaError_t launch_fc2(const Plan& p, const float* h, const int32_t* idx, const int32_t* count,
                        const LayerPtrs& w, const int32_t* live, float* partial, float* y, cudaStream_t s);
+// ---- head-sparse attention block (pi_attn.cu) ----
+struct AttnPlan {
+    int d, H, KVH, dh, B, smax, WH, nsplit;
+    Plan pred;   // head predictor (F = heads)
+    Plan proj;   // query/key/value projections (F = rows of Wqkv)
+    Plan out;    // output projection (F = rows of Wo^T)
+    size_t off_pred, off_slot, off_cnt, off_idx, off_proj, off_ppart, off_apart, off_fpart, total;
+};
+bool make_attn_plan(const pi_attn_desc& a, AttnPlan* out);
+cudaError_t launch_attn(const AttnPlan& q, const __half* x, const pi_attn_weights& w, __half* kcache,
+                        __half* vcache, const int32_t* pos, float tau, uint32_t* head_mask, float* y, void* ws,
+                        cudaStream_t s);
+
 // partial-sum floats of the FC2 path launch_fc2 takes for this plan (FC2 alone)
 size_t fc2_part_floats(const Plan& p);
 cudaError_t launch_rmsnorm(int d, int B, const float* y, float eps, __half* x, cudaStream_t s);
@@ -135,6 +150,9 @@ cudaError_t launch_predict_tc(const Plan& p, const __half* x, const __half* p1, 
 cudaError_t launch_fc1_tc(const Plan& p, const __half* x, const LayerPtrs& w, const int32_t* idx,
                           const int32_t* count, const uint32_t* mask, float* part, float* h, int32_t* live,
                           cudaStream_t s);
+// INT4 FC2 at 16 tokens on the tensor cores (plans with fc1_tc4)
+cudaError_t launch_fc2_tc4(const Plan& p, const float* h, const int32_t* idx, const int32_t* count,
+                           const LayerPtrs& w, const int32_t* live, float* partial, float* y, cudaStream_t s);
 cudaError_t launch_fc2_tc(const Plan& p, const float* h, const int32_t* idx, const int32_t* count,
                           const LayerPtrs& w, const int32_t* live, float* partial, float* y, cudaStream_t s);
 bool tc4_supported(const Plan& p);

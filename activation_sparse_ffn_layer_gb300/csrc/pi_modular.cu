@@ -276,7 +276,9 @@ __global__ void __launch_bounds__(1024) k_compact(const uint32_t* __restrict__ m
 
 // ------------------------------------------------------------------------ FC1
 
-// KIND 0: fp16 rows; 1: fp16 gate + up rows (gated); 2: INT4 group-32 rows.
+// KIND 0: fp16 rows; 1: fp16 gate + up rows (gated); 2: INT4 group-32 rows;
+// 3: fp16 rows as a plain projection (bias, no activation: the query, key and
+// value rows of the head-sparse attention block).
 // One warp per listed neuron (grid-stride), x for TB tokens staged in smem.
 template <int TB, int KIND>
 __global__ void __launch_bounds__(256) k_fc1(const __half* __restrict__ x, int B, int b0, int d,
@@ -379,7 +381,7 @@ __global__ void __launch_bounds__(256) k_fc1(const __half* __restrict__ x, int B
         for (int t = 0; t < TB; ++t) {
             if (lane == t) {
                 const float z = acc[t] + bk;
-                float hv = z > 0.f ? z : 0.f;
+                float hv = KIND == 3 ? z : (z > 0.f ? z : 0.f);
                 if (KIND == 1) hv *= accu[t];
                 if (mask != nullptr && B > 1 && !((mask[(size_t)(b0 + t) * W + (k >> 5)] >> (k & 31)) & 1u))
                     hv = 0.f;
@@ -692,7 +694,7 @@ cudaError_t launch_compact(const Plan& p, const uint32_t* mask, const int32_t* t
 cudaError_t launch_fc1_chunked(const Plan& p, const __half* x, const LayerPtrs& w, const ColdPtrs& cold,
                                const int32_t* idx, const int32_t* count, const uint32_t* mask, float* h,
                                cudaStream_t s) {
-    const int kind = p.int4 ? 2 : (p.gated ? 1 : 0);
+    const int kind = p.proj ? 3 : p.int4 ? 2 : (p.gated ? 1 : 0);
     return for_token_chunks(p.B, [&](int b0, int tb) -> cudaError_t {
         const size_t sm = (size_t)tb * p.d * sizeof(__half);
         const int blocks_max = (p.F + 7) / 8;
@@ -708,6 +710,7 @@ cudaError_t launch_fc1_chunked(const Plan& p, const __half* x, const LayerPtrs& 
         PI_FC1(1, 0) PI_FC1(2, 0) PI_FC1(4, 0) PI_FC1(8, 0)
         PI_FC1(1, 1) PI_FC1(2, 1) PI_FC1(4, 1) PI_FC1(8, 1)
         PI_FC1(1, 2) PI_FC1(2, 2) PI_FC1(4, 2) PI_FC1(8, 2)
+        PI_FC1(1, 3) PI_FC1(2, 3) PI_FC1(4, 3) PI_FC1(8, 3)
 #undef PI_FC1
         return cudaGetLastError();
     });
@@ -746,6 +749,7 @@ cudaError_t launch_fc2(const Plan& p, const float* h, const int32_t* idx, const 
                        const LayerPtrs& w, const int32_t* live, float* partial, float* y, cudaStream_t s) {
     if (p.tc) return launch_fc2_tc(p, h, idx, count, w, live, partial, y, s);
     if (p.st) return launch_fc2_st(p, h, idx, count, w, live, partial, y, s);
+    if (p.fc1_tc4) return launch_fc2_tc4(p, h, idx, count, w, live, partial, y, s);
     if (p.st4) return launch_fc2_st4(p, h, idx, count, w, live, partial, y, s);
     return launch_fc2_chunked(p, h, idx, count, w, no_cold_tier(), partial, y, s);
 }
@@ -753,6 +757,7 @@ cudaError_t launch_fc2(const Plan& p, const float* h, const int32_t* idx, const 
 size_t fc2_part_floats(const Plan& p) {
     if (p.tc) return tc_fc2_part_floats(p);
     if (p.st) return st_fc2_part_floats(p);
+    if (p.fc1_tc4) return tc_fc2_part_floats(p);
     if (p.st4) return st4_fc2_part_floats(p);
     return (size_t)p.fc2_splits * p.B * p.d;
 }

@@ -81,6 +81,9 @@ PI_DEV void cp16(void* dst, const void* src) {
 PI_DEV void cp4(void* dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(su32(dst)), "l"(src));
 }
+PI_DEV void cp8(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(su32(dst)), "l"(src));
+}
 PI_DEV void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 PI_DEV void cp_wait() {

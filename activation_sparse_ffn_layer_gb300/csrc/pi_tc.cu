@@ -821,9 +821,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
 }
 
 // h[j, t] = act(Z[j, t] + b1[idx_j]) (gated: times Zu[j, t]), zero where token
-// t's own mask does not list idx_j; live[j] = some h[j, :] != 0.
+// t's own mask does not list idx_j; live[j] = some h[j, :] != 0.  act is ReLU
+// for FFN rows and the identity for projection rows (RELU = false).
 // Block: 32 consecutive rows (lane) x B tokens (warp).
-template <bool GATED>
+template <bool GATED, bool RELU>
 __global__ void __launch_bounds__(1024) k_fc1_finish(const float* __restrict__ part, int slots, int G, int nk,
                                                      const int32_t* __restrict__ count, int B, int NT,
                                                      const int32_t* __restrict__ idx, const __half* __restrict__ b1,
@@ -846,7 +847,7 @@ __global__ void __launch_bounds__(1024) k_fc1_finish(const float* __restrict__ p
         const int m = j & 127;
         const int k = idx[j];
         float v = sum_cover(part, slot, rng, slots, cols, t, m) + __half2float(b1[k]);
-        v = v > 0.f ? v : 0.f;
+        if (RELU) v = v > 0.f ? v : 0.f;
         if (GATED) v *= sum_cover(part, slot, rng, slots, cols, NT + t, m);
         if (mask != nullptr && !((mask[(size_t)t * W + (k >> 5)] >> (k & 31)) & 1u)) v = 0.f;
         h[(size_t)j * B + t] = v;
@@ -1182,6 +1183,326 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fc2_tc(TcFc2Args a) {
     }
 }
 
+// ------------------------------------------------------------ FC2, INT4 rows
+//
+// y[t, c] = sum_j h[j, t] q[j, c] s[j, c / 32] with the stream-K split of the
+// fp16 FC2.  The W2t codes enter the MMA as exact fp16 integers (A: 128
+// columns x 64 rows per stage, MN-major, as the fp16 rows), and the group
+// scale, which changes along the rows (K) and along the 32-column groups of
+// the tile (M), moves into the B operand: for each of the tile's four groups g
+// and token t, B holds v = h[j, t] s[j, g] as hi = fp16(v) and
+// lo = fp16((v - hi) 2^11), N = 4 groups x 16 tokens x (hi | lo) = 128.  An
+// accumulator column (g, t, .) is meaningful only for the tile's columns of
+// group g; epilogue warp e owns TMEM lanes 32e .. 32e+31 (group e) and reads
+// its columns (e, t, hi | lo): y = D_hi + 2^-11 D_lo.  Scaling lo up keeps it
+// out of the fp16 subnormals wherever hi is normal, so the pair carries about
+// 22 bits of v.
+//
+// Loaders (warps 0-3) copy each stage's codes (64 rows x 64 bytes), scales
+// (64 rows x 4) and h rows raw into a ring of RQ entries LAG stages ahead,
+// with the row ids and live flags copied LAG + 1 stages ahead of that; once a
+// stage's copies have landed (and its MMA stage is free) they write the A and
+// B operands, fence them for the tensor cores and arrive on `full`.
+template <int NT>
+struct Fc2qCfg {
+    static constexpr int N = 8 * NT;                     // 4 groups x NT tokens x (hi | lo)
+    static constexpr int BOP = N * 64 * 2;
+    static constexpr int STAGE = kTileA + BOP;
+    static constexpr int S = 4;
+    static constexpr int LAG = 6;
+    static constexpr int RQ = LAG + 2;                   // raw entries
+    static constexpr int IDR = 2 * LAG + 2;              // row-id slots
+    static constexpr int RCODE = 64 * 64;
+    static constexpr int RSC = 64 * 8;
+    static constexpr int RVAL = 64 * 4;
+    static constexpr int RH = 64 * NT * 4;
+    static constexpr int RAW = RCODE + RSC + RVAL + RH;
+    static constexpr int IDS = 64 * 2 * 4;               // 64 row ids + 64 live flags
+    static constexpr int ACC = N;
+    static constexpr int TMEM = tmem_cols_for(2 * ACC);
+    static constexpr size_t SMEM = (size_t)S * STAGE + (size_t)RQ * RAW + (size_t)IDR * IDS + 1024;
+    static_assert(STAGE % 1024 == 0 && RAW % 16 == 0, "stage alignment");
+};
+
+struct TcFc2qArgs {
+    const float* h;        // [count][B]
+    const int32_t* idx;
+    const int32_t* count;
+    const uint8_t* q;      // W2t codes [F][d/2]
+    const __half* qs;      // W2t group scales [F][d/32]
+    const int32_t* live;   // nullable
+    float* part;           // [G][slots][NT][128]
+    int* status;
+    long long timeout_ns;
+    int B, d, slots;
+};
+
+template <int NT>
+__global__ void __launch_bounds__(kTcThreads, 1) k_fc2q_tc(TcFc2qArgs a) {
+    pdl_entry();
+    using C = Fc2qCfg<NT>;
+    extern __shared__ unsigned char dsm[];
+    __shared__ __align__(8) unsigned long long full[C::S], empty[C::S], accf[2], acce[2], drain;
+    __shared__ unsigned tmem_slot;
+    __shared__ int abort_flag;
+
+    const int n = *a.count;
+    const int G = gridDim.x, g = blockIdx.x;
+    const int nct = a.d / 128;
+    const long long U = (long long)nct * n;
+    const long long u0 = U * g / G, u1 = U * (g + 1) / G;
+    if (u0 >= u1) return;
+    const int npiece = (int)((u1 - 1) / n - u0 / n) + 1;
+    __shared__ Piece ptab[kMaxPieces];
+    if (npiece > kMaxPieces) {
+        if (threadIdx.x == 0) atomicExch(a.status, (int)PI_ERR_WORKSPACE);
+        return;
+    }
+    if (threadIdx.x < npiece) fc2_piece(u0, u1, n, threadIdx.x, &ptab[threadIdx.x]);
+    unsigned char* ring = align1024(dsm);
+    unsigned char* raw0 = ring + (size_t)C::S * C::STAGE;
+    int32_t* ids0 = reinterpret_cast<int32_t*>(raw0 + (size_t)C::RQ * C::RAW);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid == 0) {
+        for (int s = 0; s < C::S; ++s) {
+            bar_init(&full[s], kLoaderWarps);
+            bar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            bar_init(&accf[b], 1);
+            bar_init(&acce[b], 128);
+        }
+        bar_init(&drain, 1);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 8) tmem_alloc(&tmem_slot, C::TMEM);
+    tc_before();
+    __syncthreads();
+    tc_after();
+    const unsigned tmem = tmem_slot;
+    const Ctl ctl{a.status, a.timeout_ns, &abort_flag};
+
+    if (warp < 4) {
+        const int t = tid;
+        const bool vec = (a.B & 3) == 0 && (reinterpret_cast<uintptr_t>(a.h) & 15) == 0;
+        const size_t cpr = (size_t)a.d / 2, spr = (size_t)a.d / 32;
+        int total = 0;
+        for (int p = 0; p < npiece; ++p) total += (ptab[p].j1 - ptab[p].j0 + 63) / 64;
+        // cursors: row-id copies, raw copies, conversions (piece, stage in piece)
+        int fq = 0, fpiece = 0, fst = 0;
+        int ipc = 0, ist = 0;
+        int cpc = 0, cst = 0;
+        auto copy_ids = [&]() {
+            const Piece pc = ptab[fpiece];
+            const int kk = t & 63;
+            const int j = pc.j0 + 64 * fst + kk;
+            int32_t* sl = ids0 + (fq % C::IDR) * 128;
+            if (j < pc.j1) {
+                if (t < 64)
+                    cp4(sl + kk, a.idx + j);
+                else if (a.live != nullptr)
+                    cp4(sl + 64 + kk, a.live + j);
+            }
+            ++fq;
+            if (64 * (++fst) >= pc.j1 - pc.j0) {
+                ++fpiece;
+                fst = 0;
+            }
+        };
+        auto issue = [&](int q) {
+            const Piece pc = ptab[ipc];
+            const int jb = pc.j0 + 64 * ist;
+            const int nrow = pc.j1 - jb < 64 ? pc.j1 - jb : 64;
+            const int col0 = pc.ct * 128;
+            const int32_t* sl = ids0 + (q % C::IDR) * 128;
+            unsigned char* rw = raw0 + (size_t)(q % C::RQ) * C::RAW;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int c = t + 128 * i, r = c >> 2, part = c & 3;
+                if (r < nrow && (a.live == nullptr || sl[64 + r] != 0))
+                    cp16(rw + r * 64 + part * 16, a.q + (size_t)sl[r] * cpr + col0 / 2 + part * 16);
+            }
+            if (t < 64) {
+                const bool ok = t < nrow && (a.live == nullptr || sl[64 + t] != 0);
+                reinterpret_cast<int*>(rw + C::RCODE + C::RSC)[t] = ok ? 1 : 0;
+                if (ok) cp8(rw + C::RCODE + 8 * t, a.qs + (size_t)sl[t] * spr + col0 / 32);
+            }
+            unsigned char* hd = rw + C::RCODE + C::RSC + C::RVAL;
+            const float* hsrc = a.h + (size_t)jb * a.B;
+            if (vec) {
+                for (int c = t; c < nrow * a.B / 4; c += kLoaders) cp16(hd + 16 * c, hsrc + 4 * c);
+            } else {
+                for (int c = t; c < nrow * a.B; c += kLoaders) cp4(hd + 4 * c, hsrc + c);
+            }
+            if (64 * (++ist) >= pc.j1 - pc.j0) {
+                ++ipc;
+                ist = 0;
+            }
+        };
+        auto convert = [&](int q) {
+            const unsigned char* rw = raw0 + (size_t)(q % C::RQ) * C::RAW;
+            unsigned char* sb = ring + (size_t)(q % C::S) * C::STAGE;
+            // A: word c of row r holds columns 8c .. 8c+7 of the tile
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int w = t + 128 * i, r = w >> 4, c = w & 15;
+                const uint4 hv = q8_f16(*reinterpret_cast<const uint32_t*>(rw + r * 64 + 4 * c));
+                *reinterpret_cast<uint4*>(sb + (c >> 3) * 1024 + (r >> 3) * 2048 + (r & 7) * 128 +
+                                          (((c & 7) ^ (r & 7)) << 4)) = hv;
+            }
+            // B: rows 8 kc .. 8 kc + 7 of token tok, every group
+            const int kc = t >> 4, tok = t & 15;
+            const int* val = reinterpret_cast<const int*>(rw + C::RCODE + C::RSC);
+            const float* hr = reinterpret_cast<const float*>(rw + C::RCODE + C::RSC + C::RVAL);
+            float hv[8];
+            uint2 sc[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int r = 8 * kc + e;
+                const bool ok = tok < a.B && val[r] != 0;
+                hv[e] = ok ? hr[r * a.B + tok] : 0.f;
+                sc[e] = ok ? *reinterpret_cast<const uint2*>(rw + C::RCODE + 8 * r) : make_uint2(0u, 0u);
+            }
+            unsigned char* bo = sb + kTileA + kc * (C::N * 16);
+#pragma unroll
+            for (int grp = 0; grp < 4; ++grp) {
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int e2 = 0; e2 < 4; ++e2) {
+                    float v[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const uint2 w = sc[2 * e2 + u];
+                        const uint32_t word = grp < 2 ? w.x : w.y;
+                        const float sv = __half2float(__ushort_as_half((unsigned short)(word >> (16 * (grp & 1)))));
+                        v[u] = hv[2 * e2 + u] * sv;
+                    }
+                    const __half2 h2 = __floats2half2_rn(v[0], v[1]);
+                    const float2 bk = __half22float2(h2);
+                    const __half2 l2 = __floats2half2_rn((v[0] - bk.x) * 2048.f, (v[1] - bk.y) * 2048.f);
+                    hi[e2] = *reinterpret_cast<const uint32_t*>(&h2);
+                    lo[e2] = *reinterpret_cast<const uint32_t*>(&l2);
+                }
+                const int nh = 2 * NT * grp + tok, nl = nh + NT;
+                *reinterpret_cast<uint4*>(bo + (nh >> 3) * 128 + (nh & 7) * 16) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(bo + (nl >> 3) * 128 + (nl & 7) * 16) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+            if (64 * (++cst) >= ptab[cpc].j1 - ptab[cpc].j0) {
+                ++cpc;
+                cst = 0;
+            }
+        };
+        while (fq < total && fq <= C::LAG) copy_ids();
+        cp_commit();
+        cp_wait_all();
+        loaders_sync_any(false);
+        bool ok = true;
+        for (int q = 0; q < total + C::LAG; ++q) {
+            if (q < total) {
+                issue(q);
+                if (fq < total) copy_ids();   // ids of stage q + LAG + 1
+            }
+            cp_commit();
+            const int cv = q - C::LAG;
+            if (cv < 0) continue;
+            cp_wait<C::LAG>();   // this thread's copies of stage cv (and the ids of stage q + 1) have landed
+            if (loaders_sync_any(!ok || *(volatile int*)&abort_flag)) {
+                ok = false;
+                break;
+            }
+            if (cv >= C::S) {   // the MMAs of stage cv - S have released the operand stage
+                bool good = true;
+                if (lane == 0) good = bar_wait(&empty[cv % C::S], ((cv / C::S) - 1) & 1, ctl);
+                if (!__shfl_sync(FULL, good ? 1 : 0, 0)) {
+                    ok = false;
+                    continue;   // the next barrier stops every loader
+                }
+            }
+            convert(cv);
+            fence_async_smem();
+            warp_arrive(&full[cv % C::S]);
+        }
+        cp_wait_all();
+    } else if (warp < 8) {
+        // ---- epilogue: TMEM lane m = column col0 + m, group e = m / 32
+        const int e = warp - 4, m = 32 * e + lane;
+        for (int p = 0; p < npiece; ++p) {
+            const int b = p & 1;
+            if (!bar_wait(&accf[b], (p >> 1) & 1, ctl)) break;
+            tc_after();
+            float vh[NT], vl[NT];
+            const unsigned ta = tmem + ((unsigned)(32 * e) << 16) + (unsigned)(b * C::ACC + 2 * NT * e);
+#pragma unroll
+            for (int c = 0; c < NT; c += 16) {
+                tmem_ld16(ta + c, vh + c);
+                tmem_ld16(ta + NT + c, vl + c);
+            }
+            tmem_wait_ld();
+            tc_before();
+            bar_arrive(&acce[b]);
+            if (p < a.slots) {
+                float* dst = a.part + (((size_t)g * a.slots + p) * NT) * 128 + m;
+#pragma unroll
+                for (int t = 0; t < NT; ++t)
+                    if (t < a.B) dst[(size_t)t * 128] = fmaf(vl[t], 1.0f / 2048.0f, vh[t]);
+            } else if (lane == 0) {
+                atomicExch(a.status, (int)PI_ERR_WORKSPACE);
+            }
+        }
+    } else if (lane == 0) {
+        // ---- MMA issuer: A = W2t codes (M = 128 columns, MN-major), B = h s (hi | lo per group)
+        const unsigned idesc = idesc_f16(128, C::N, true);
+        int it = 0;
+        bool ok = true;
+        for (int p = 0; p < npiece && ok; ++p) {
+            const Piece pc = ptab[p];
+            const int nst = (pc.j1 - pc.j0 + 63) / 64;
+            const int b = p & 1;
+            if (p >= 2 && !bar_wait(&acce[b], ((p >> 1) - 1) & 1, ctl)) {
+                ok = false;
+                break;
+            }
+            tc_after();
+            const unsigned dcol = tmem + (unsigned)(b * C::ACC);
+            for (int st = 0; st < nst; ++st, ++it) {
+                const int s = it % C::S;
+                if (!bar_wait(&full[s], (it / C::S) & 1, ctl)) {
+                    ok = false;
+                    break;
+                }
+                tc_after();
+                const unsigned sa = su32(ring + (size_t)s * C::STAGE);
+                const unsigned sbop = sa + kTileA;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t ad = sdesc_sw128_mn(sa + kk * 4096, 1024, 2048);
+                    const uint64_t bd = sdesc(sbop + kk * 2 * (C::N * 16), C::N * 16, 128);
+                    mma_f16(dcol, ad, bd, idesc, (st | kk) ? 1u : 0u);
+                }
+                mma_commit(&empty[s]);
+            }
+            if (ok) mma_commit(&accf[b]);
+        }
+        if (ok) {
+            for (int s = 0; s < C::S && s < it; ++s) {
+                const int last = s + ((it - 1 - s) / C::S) * C::S;
+                bar_drain(&empty[s], (last / C::S) & 1, kDrainTimeoutNs);
+            }
+        } else {
+            mma_commit(&drain);
+            bar_drain(&drain, 0, kDrainTimeoutNs);
+        }
+    }
+    tc_before();
+    __syncthreads();
+    if (warp == 8) {
+        tc_after();
+        tmem_free(tmem, C::TMEM);
+    }
+}
+
 // y[b0 + t, c] = b2[c] + sum over the CTAs whose range touches column tile
 // c / tw of their partial (ascending CTA order: reproducible), for the nb
 // tokens of this pass.  Block: the tw columns of one tile x 1024 / tw tokens.
@@ -1334,14 +1655,7 @@ cudaError_t launch_fc1_tc(const Plan& p, const __half* x, const LayerPtrs& w, co
     a.timeout_ns = wait_timeout_ns();
     cudaError_t e = p.gated ? launch_rows_nt<1>(a, nt, G, s) : launch_rows_nt<0>(a, nt, G, s);
     if (e != cudaSuccess) return e;
-    const int blocks = ceil_div(p.F, 32);
-    if (p.gated)
-        launch_pdl(k_fc1_finish<true>, blocks, 32 * p.B, 0, s, part, a.slots, G, ceil_div(p.d, 64), count, p.B, nt, idx, w.b1,
-                                                   mask, p.W, h, live);
-    else
-        launch_pdl(k_fc1_finish<false>, blocks, 32 * p.B, 0, s, part, a.slots, G, ceil_div(p.d, 64), count, p.B, nt, idx, w.b1,
-                                                    mask, p.W, h, live);
-    return cudaGetLastError();
+    return launch_fc1_finish(p, nt, G, a.slots, ceil_div(p.d, 64), part, count, idx, w.b1, mask, h, live, s);
 }
 
 cudaError_t launch_fc1_tc4(const Plan& p, const __half* x, const LayerPtrs& w, const int32_t* idx,
@@ -1373,11 +1687,14 @@ cudaError_t launch_fc1_finish(const Plan& p, int nt, int G, int slots, int nk, c
                               float* h, int32_t* live, cudaStream_t s) {
     const int blocks = ceil_div(p.F, 32);
     if (p.gated)
-        launch_pdl(k_fc1_finish<true>, blocks, 32 * p.B, 0, s, part, slots, G, nk, count, p.B, nt, idx, b1, mask, p.W, h,
-                                                       live);
+        launch_pdl(k_fc1_finish<true, true>, blocks, 32 * p.B, 0, s, part, slots, G, nk, count, p.B, nt, idx, b1, mask,
+                   p.W, h, live);
+    else if (p.proj)
+        launch_pdl(k_fc1_finish<false, false>, blocks, 32 * p.B, 0, s, part, slots, G, nk, count, p.B, nt, idx, b1, mask,
+                   p.W, h, live);
     else
-        launch_pdl(k_fc1_finish<false>, blocks, 32 * p.B, 0, s, part, slots, G, nk, count, p.B, nt, idx, b1, mask, p.W, h,
-                                                        live);
+        launch_pdl(k_fc1_finish<false, true>, blocks, 32 * p.B, 0, s, part, slots, G, nk, count, p.B, nt, idx, b1, mask,
+                   p.W, h, live);
     return cudaGetLastError();
 }
 
@@ -1386,6 +1703,24 @@ cudaError_t launch_fc2_reduce(const Plan& p, int nt, int G, int slots, int tw, i
     const int tpb = 1024 / tw;
     launch_pdl(k_fc2_tc_reduce, dim3(p.d / tw, ceil_div(nb, tpb)), 1024, 0, s, part, slots, G, count, nb, b0, nt, p.d, tw,
                                                                         b2, y);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fc2_tc4(const Plan& p, const float* h, const int32_t* idx, const int32_t* count,
+                           const LayerPtrs& w, const int32_t* live, float* partial, float* y, cudaStream_t s) {
+    int* status = status_word();
+    if (status == nullptr) return cudaErrorInvalidDevice;
+    const int G = p.nsm;
+    const int slots = slots_for(p.d / 128, G);
+    TcFc2qArgs a{h, idx, count, static_cast<const uint8_t*>(w.w2t), w.w2ts, live, partial, status,
+                 wait_timeout_ns(), p.B, p.d, slots};
+    cudaError_t e = prep(k_fc2q_tc<16>, Fc2qCfg<16>::SMEM);
+    if (e != cudaSuccess) return e;
+    launch_pdl(k_fc2q_tc<16>, G, kTcThreads, Fc2qCfg<16>::SMEM, s, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    launch_pdl(k_fc2_tc_reduce, dim3(p.d / 128, ceil_div(p.B, 8)), 1024, 0, s, static_cast<const float*>(partial),
+               slots, G, count, p.B, 0, 16, p.d, 128, w.b2, y);
     return cudaGetLastError();
 }
 

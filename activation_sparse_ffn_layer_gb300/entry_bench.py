@@ -12,6 +12,12 @@ calls (FC2 counts the rows whose FC1 output is non-zero for some token).
     python -m activation_sparse_ffn_layer_gb300.entry_bench --config c5 --batch 4 --once
     python -m activation_sparse_ffn_layer_gb300.entry_bench --config c4 --cold host
 
+``--attn`` times ``pi_attn_heads`` (the head-sparse attention block) instead,
+on the workload's attention shape with a decode-length cache; its bytes are
+the head predictor, the query rows of the heads some token uses, every key
+and value row, the output-projection rows of those heads and the cache rows
+the active (head, token) pairs read.
+
 ``--once`` runs every call a few times eagerly and then once more, without
 graphs or timing, which is the shape a profiler capture wants.  ``--cold host``
 times the tiered FC calls instead, with the FC rows from ``--n-hot`` on (default
@@ -179,6 +185,61 @@ def run(config: str, batch: int, once: bool = False, cold: str = "", n_hot: int 
                           "listed": n, "live": live, **extra}), flush=True)
 
 
+def run_attn(config: str, batch: int, once: bool = False, max_seq: int = 1024):
+    from synth import ATTN_CONFIGS, decode_lengths, make_attn, make_kv_cache
+
+    B.lib()
+    cfg = ATTN_CONFIGS[config]
+    dev = "cuda"
+    blocks = [make_attn(cfg, l, device=dev) for l in range(2)]
+    H, KVH, dh, d = cfg.heads, cfg.kv_heads, cfg.head_dim, cfg.d
+    lengths = decode_lengths(cfg, batch)
+    caches = [make_kv_cache(cfg, lengths, seed=l, device=dev, max_seq=max_seq) for l in range(2)]
+    g = torch.Generator(device=dev).manual_seed(7)
+    x = torch.randn(batch, d, generator=g, device=dev).to(torch.float16)
+    desc = B.attn_desc(blocks[0], batch, max_seq)
+    ws = torch.empty(B.pi_attn_workspace_bytes(desc), dtype=torch.uint8, device=dev)
+    pos = torch.tensor(lengths, dtype=torch.int32, device=dev)
+    mask = torch.zeros(batch, (H + 31) // 32, dtype=torch.int32, device=dev)
+    y = torch.zeros(batch, d, dtype=torch.float32, device=dev)
+    st = [B.attn_weights_struct(w) for w in blocks]
+    turn = [0]
+
+    def call():
+        turn[0] += 1
+        k = turn[0] % 2
+        B.pi_attn_heads(desc, x, st[k], caches[k][0], caches[k][1], pos, cfg.tau, mask, y, ws)
+
+    call()
+    torch.cuda.synchronize()
+    if once:
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        call()
+        torch.cuda.synchronize()
+        print(json.dumps({"call": "pi_attn_heads", "config": config, "batch": batch, "mode": "once"}))
+        return
+    # bytes of the block for the masks the call computes (both blocks alike)
+    call()
+    torch.cuda.synchronize()
+    m = mask.cpu().numpy().astype("int64") & 0xFFFFFFFF
+    on = [[(int(m[b, h // 32]) >> (h % 32)) & 1 for h in range(H)] for b in range(batch)]
+    union = sum(1 for h in range(H) if any(on[b][h] for b in range(batch)))
+    pairs_kv = sum(lengths[b] * on[b][h] for b in range(batch) for h in range(H))
+    w0 = blocks[0]
+    row = 2 * d
+    moved = (2 * (w0.r * d + H * w0.r + H) + (union + 2 * KVH) * dh * row + 2 * (union + 2 * KVH) * dh
+             + union * dh * row + pairs_kv * 2 * dh * 2 + batch * d * 2 + batch * d * 4)
+    us = _time(call)
+    gbs = moved / us / 1e3
+    peak = _peak_gbs()
+    print(json.dumps({"call": "pi_attn_heads", "config": config, "batch": batch, "us": round(us, 2),
+                      "bytes": moved, "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+                      "heads": H, "union_heads": union, "active_pairs": int(sum(map(sum, on))),
+                      "cache_lengths": lengths[:4], "max_seq": max_seq}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description="time the C-ABI entry points on one layer of a workload")
     ap.add_argument("--config", default="c2")
@@ -188,9 +249,13 @@ def main(argv=None):
                     help="time the tiered FC calls with the rows past the hot prefix in pinned host memory "
                          "or in a second device buffer")
     ap.add_argument("--n-hot", type=int, default=0, help="rows kept in the first tier with --cold (0: none)")
+    ap.add_argument("--attn", action="store_true", help="time the head-sparse attention block instead")
     args = ap.parse_args(argv)
     assert torch.cuda.is_available(), "needs a CUDA GPU"
-    run(args.config, args.batch, args.once, args.cold, args.n_hot)
+    if args.attn:
+        run_attn(args.config, args.batch, args.once)
+    else:
+        run(args.config, args.batch, args.once, args.cold, args.n_hot)
 
 
 if __name__ == "__main__":

@@ -132,7 +132,10 @@ PI_API pi_status pi_compact(const pi_layer_desc *desc, const uint32_t *mask, con
  * b's own mask bit idx_j is 0.  h: [F*B] fp32 (neuron-major).
  * For 16 <= B <= 32, fp16 weights and d % 128 == 0 the rows are gathered once
  * for all B tokens and multiplied on the tcgen05 tensor cores (fp16 x fp16
- * products, fp32 accumulation); otherwise CUDA cores in chunks of <= 8 tokens.
+ * products, fp32 accumulation); so are INT4 rows of a ReLU layer at B = 16
+ * with d % 256 == 0 (codes as exact fp16 integers, group scales applied per
+ * 32-element group); INT4 at 2 <= B <= 16 otherwise streams on CUDA cores;
+ * the rest runs on CUDA cores in chunks of <= 8 tokens.
  * workspace: >= pi_workspace_bytes(desc) bytes, 16-byte aligned (partial
  * sums of the tensor-core split).
  */
@@ -147,7 +150,10 @@ PI_API pi_status pi_sparse_fc1(const pi_layer_desc *desc, const pi_half *x, cons
  * Reduced without atomics in a fixed order (bitwise reproducible).
  * Under the same conditions as pi_sparse_fc1 the tensor cores take it, with h
  * split into fp16 hi = fp16(h) and lo = fp16(h - hi) so that fp32 accuracy is
- * kept.
+ * kept.  INT4 rows at B = 16: the codes are the exact fp16 A operand and the
+ * row's group scale moves into B, one (hi, lo) pair of h * scale per token and
+ * 32-column group, lo = fp16((h * scale - hi) * 2^11) (scaled out again in the
+ * epilogue).
  */
 PI_API pi_status pi_sparse_fc2(const pi_layer_desc *desc, const float *h, const int32_t *idx,
                         const int32_t *d_count, const pi_layer_weights *w, float *y,
@@ -166,8 +172,9 @@ PI_API pi_status pi_sparse_fc2(const pi_layer_desc *desc, const float *h, const 
  *    array (2 Mi floats).  They are, with G the SM count: splits x batch x d
  *    floats on the per-token path; G x (ceil(d/128/G) + 2) x T x 128 floats on
  *    the streamed fp16 path (T = 2, 4 or 8 tokens) and on the batch 16..32
- *    tensor-core path (T = 16 or 32); G x (ceil(d/256/G) + 2) x T x 256 on
- *    the streamed INT4 path (T = 4, 8 or 16).  Allocates nothing in any case.
+ *    tensor-core path (T = 16 or 32) and on the INT4 tensor-core path at 16
+ *    tokens (T = 16); G x (ceil(d/256/G) + 2) x T x 256 on the streamed INT4
+ *    path (T = 4, 8 or 16).  Allocates nothing in any case.
  *  - The first call on a device looks up the array's device address (once per
  *    device, with that device current); make that first call before any
  *    stream capture.
@@ -266,6 +273,67 @@ PI_API pi_status pi_workspace_layout(const pi_layer_desc *desc, pi_workspace_lay
  */
 PI_API pi_status pi_rmsnorm_half(int d, int batch, const float *y, float eps, pi_half *x_out,
                           void *stream);
+
+/*
+ * Head-sparse self-attention block of one decode step (PowerInfer summary
+ * (CSDN), section "Background", paragraph on activation sparsity: in the
+ * self-attention block about half of the heads contribute little for a given
+ * input; unite.ai page, section on adaptive sparsity predictors: each layer
+ * has one activity predictor for its MLP block and one for its self-attention
+ * block, and only the neurons predicted active are computed).  The block's
+ * neurons are its heads.  For each sequence b (one new token x_b at cache
+ * position pos[b]):
+ *   1. head mask: u = P1 x_b, s = P2 u + bp, head h active iff s_h > tau
+ *      (the predictor of pi_predict with F = heads);
+ *   2. k_g = Wk_g x_b + bk_g and v_g = Wv_g x_b + bv_g for EVERY KV head g,
+ *      stored as binary16 (round to nearest even) at position pos[b] of the
+ *      caches, so later tokens find a complete cache;
+ *   3. for each active head h (KV head g = h / (heads / kv_heads)):
+ *      q = Wq_h x_b + bq_h;  a_t = softmax_t(q . K_g[t] / sqrt(head_dim)) over
+ *      t = 0 .. pos[b] (the token's own key included);  o_h = sum_t a_t V_g[t];
+ *   4. y_b = bo + sum over active h of Wo[:, h*dh .. h*dh+dh-1] o_h.
+ * A head that is not active for the token adds nothing to y_b: its query,
+ * its pass over the cache and its Wo columns are skipped.  Arithmetic in fp32
+ * on fp16 weights and caches; the output projection is reduced in a fixed
+ * order (bitwise reproducible).
+ */
+typedef struct {
+    int d;         /* model width (multiple of 8)                                  */
+    int heads;     /* query heads H (1 .. 1024)                                    */
+    int kv_heads;  /* key/value heads KVH, dividing H (H: multi-head attention)    */
+    int head_dim;  /* dh: 64 or 128                                                */
+    int rank;      /* head predictor rank (multiple of 8)                          */
+    int batch;     /* sequences B, one new token each (1 .. 32)                    */
+    int max_seq;   /* cache capacity smax per sequence and KV head                 */
+} pi_attn_desc;
+
+typedef struct {
+    const pi_half *wqkv; /* [(H + 2 KVH) dh, d]: query rows of head h at h*dh, key rows of KV
+                            head g at (H + g) dh, value rows at (H + KVH + g) dh            */
+    const pi_half *bqkv; /* [(H + 2 KVH) dh] (zeros for a model without biases)           */
+    const pi_half *wot;  /* [H dh, d]: Wo transposed, row j = column j of Wo              */
+    const pi_half *bo;   /* [d]                                                           */
+    const pi_half *p1;   /* [rank, d]  head predictor input layer                         */
+    const pi_half *p2;   /* [H, rank]  head predictor output layer                        */
+    const pi_half *bp;   /* [H]        head predictor bias                                */
+} pi_attn_weights;
+
+/* Bytes of workspace pi_attn_heads needs for `desc` (0 if it is invalid). */
+PI_API size_t pi_attn_workspace_bytes(const pi_attn_desc *desc);
+
+/*
+ * x: [B, d] fp16.  kcache, vcache: [B, KVH, max_seq, head_dim] fp16 (in:
+ * positions below pos[b] of sequence b; out: position pos[b] written).
+ * pos: [B] int32 on the device.  head_mask: [B, ceil(H/32)] uint32 out (the
+ * predicted-active heads).  y: [B, d] fp32 out.  All 16-byte aligned.
+ * The workspace needs no zero fill.  A pos[b] outside 0 .. max_seq-1 leaves
+ * sequence b's cache untouched and its y equal to bo, and sets the device
+ * status read by pi_last_device_status to PI_ERR_INVALID_ARG.
+ */
+PI_API pi_status pi_attn_heads(const pi_attn_desc *desc, const pi_half *x, const pi_attn_weights *w,
+                               pi_half *kcache, pi_half *vcache, const int32_t *pos, float tau,
+                               uint32_t *head_mask, float *y, void *workspace, size_t ws_bytes,
+                               void *stream);
 
 /* How one pi_ffn_stack step of `desc` (n_layers layers with the given ranks,
  * NULL: all desc->rank) is executed on the current device.  Diagnostics: lets a
