@@ -13,8 +13,9 @@
 //   row list    k_attn_list: query rows of the heads active for some token
 //               of the batch, then every key and value row
 //   projections the FFN's FC1 row paths with the activation left out
-//               (launch_fc1 on a plan of projection rows: per-token kernel,
-//               streamed at 2..8 tokens, tcgen05 at 16..32)
+//               (launch_fc1 on a plan of projection rows: the per-token
+//               kernel up to 4 tokens and at 9..15, streamed at 5..8,
+//               tcgen05 at 16..32)
 //   attention   k_attn_decode: per (head, token, split of the positions) a
 //               pass over the key and value cache with a running softmax
 //   combine     k_attn_combine: the splits of each active (head, token) are
@@ -288,6 +289,10 @@ bool make_attn_plan(const pi_attn_desc& a, AttnPlan* out) {
     // projections: rows of Wqkv; output projection: rows of Wo^T
     if (!make_plan(pi_layer_desc{a.d, rows, 8, a.batch, PI_W_F16, 0}, &q.proj)) return false;
     q.proj.proj = true;
+    // the projection rows are long contiguous runs (whole heads): up to 4
+    // tokens the per-token row kernel (a warp per row, one token chunk)
+    // streams them faster than the streamed tile path, which wins at 5..8
+    if (q.B <= 4) q.proj.st = false;
     if (!make_plan(pi_layer_desc{a.d, a.heads * a.head_dim, 8, a.batch, PI_W_F16, 0}, &q.out)) return false;
     // splits of the positions: about four blocks per SM for a batch whose
     // tokens use half of the heads, at least 32 positions per split

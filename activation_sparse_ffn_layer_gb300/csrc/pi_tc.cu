@@ -1198,11 +1198,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fc2_tc(TcFc2Args a) {
 // out of the fp16 subnormals wherever hi is normal, so the pair carries about
 // 22 bits of v.
 //
-// Loaders (warps 0-3) copy each stage's codes (64 rows x 64 bytes), scales
-// (64 rows x 4) and h rows raw into a ring of RQ entries LAG stages ahead,
-// with the row ids and live flags copied LAG + 1 stages ahead of that; once a
-// stage's copies have landed (and its MMA stage is free) they write the A and
-// B operands, fence them for the tensor cores and arrive on `full`.
+// Eight loader warps (two per SM sub-partition: the per-stage work is a chain
+// of dependent shared-memory loads and conversions that one warp per
+// sub-partition cannot overlap) copy each stage's codes (64 rows x 64 bytes),
+// scales (64 rows x 4) and h rows raw into a ring of RQ entries LAG stages
+// ahead, with the row ids and live flags copied LAG + 1 stages ahead of that.
+// In one loop step they wait for stage cv's copies, then issue stage cv + LAG
+// and write stage cv's A and B operands in the same instruction stream (the
+// two are independent, so their latencies overlap), fence the operands for the
+// tensor cores and arrive on `full`.
+constexpr int kQLoaderWarps = 8;
+constexpr int kQLoaders = 32 * kQLoaderWarps;
+constexpr int kQThreads = kQLoaders + 128 + 32;   // loaders, 4 epilogue warps, MMA warp
+
+// barrier 1 over the kQLoaders loader threads, OR of a flag
+PI_DEV bool qloaders_sync_any(bool v) {
+    unsigned r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred p, 1, %2, q;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(r)
+        : "r"((unsigned)v), "n"(kQLoaders)
+        : "memory");
+    return r != 0;
+}
+
 template <int NT>
 struct Fc2qCfg {
     static constexpr int N = 8 * NT;                     // 4 groups x NT tokens x (hi | lo)
@@ -1210,7 +1229,7 @@ struct Fc2qCfg {
     static constexpr int STAGE = kTileA + BOP;
     static constexpr int S = 4;
     static constexpr int LAG = 6;
-    static constexpr int RQ = LAG + 2;                   // raw entries
+    static constexpr int RQ = LAG + 1;                   // raw entries
     static constexpr int IDR = 2 * LAG + 2;              // row-id slots
     static constexpr int RCODE = 64 * 64;
     static constexpr int RSC = 64 * 8;
@@ -1222,6 +1241,7 @@ struct Fc2qCfg {
     static constexpr int TMEM = tmem_cols_for(2 * ACC);
     static constexpr size_t SMEM = (size_t)S * STAGE + (size_t)RQ * RAW + (size_t)IDR * IDS + 1024;
     static_assert(STAGE % 1024 == 0 && RAW % 16 == 0, "stage alignment");
+    static_assert(NT == 16 && kQLoaders == 256, "thread mappings below assume 16 tokens, 256 loaders");
 };
 
 struct TcFc2qArgs {
@@ -1238,7 +1258,7 @@ struct TcFc2qArgs {
 };
 
 template <int NT>
-__global__ void __launch_bounds__(kTcThreads, 1) k_fc2q_tc(TcFc2qArgs a) {
+__global__ void __launch_bounds__(kQThreads, 1) k_fc2q_tc(TcFc2qArgs a) {
     pdl_entry();
     using C = Fc2qCfg<NT>;
     extern __shared__ unsigned char dsm[];
@@ -1263,10 +1283,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fc2q_tc(TcFc2qArgs a) {
     unsigned char* raw0 = ring + (size_t)C::S * C::STAGE;
     int32_t* ids0 = reinterpret_cast<int32_t*>(raw0 + (size_t)C::RQ * C::RAW);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    constexpr int kEpi = kQLoaderWarps, kMma = kQLoaderWarps + 4;
 
     if (tid == 0) {
         for (int s = 0; s < C::S; ++s) {
-            bar_init(&full[s], kLoaderWarps);
+            bar_init(&full[s], kQLoaderWarps);
             bar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -1277,14 +1298,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fc2q_tc(TcFc2qArgs a) {
         abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 8) tmem_alloc(&tmem_slot, C::TMEM);
+    if (warp == kMma) tmem_alloc(&tmem_slot, C::TMEM);
     tc_before();
     __syncthreads();
     tc_after();
     const unsigned tmem = tmem_slot;
     const Ctl ctl{a.status, a.timeout_ns, &abort_flag};
 
-    if (warp < 4) {
+    if (warp < kEpi) {
         const int t = tid;
         const bool vec = (a.B & 3) == 0 && (reinterpret_cast<uintptr_t>(a.h) & 15) == 0;
         const size_t cpr = (size_t)a.d / 2, spr = (size_t)a.d / 32;
@@ -1302,7 +1323,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fc2q_tc(TcFc2qArgs a) {
             if (j < pc.j1) {
                 if (t < 64)
                     cp4(sl + kk, a.idx + j);
-                else if (a.live != nullptr)
+                else if (t < 128 && a.live != nullptr)
                     cp4(sl + 64 + kk, a.live + j);
             }
             ++fq;
@@ -1318,9 +1339,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fc2q_tc(TcFc2qArgs a) {
             const int col0 = pc.ct * 128;
             const int32_t* sl = ids0 + (q % C::IDR) * 128;
             unsigned char* rw = raw0 + (size_t)(q % C::RQ) * C::RAW;
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int c = t + 128 * i, r = c >> 2, part = c & 3;
+            {   // codes: 16-byte chunk t of the stage, row t / 4
+                const int r = t >> 2, part = t & 3;
                 if (r < nrow && (a.live == nullptr || sl[64 + r] != 0))
                     cp16(rw + r * 64 + part * 16, a.q + (size_t)sl[r] * cpr + col0 / 2 + part * 16);
             }
@@ -1332,9 +1352,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fc2q_tc(TcFc2qArgs a) {
             unsigned char* hd = rw + C::RCODE + C::RSC + C::RVAL;
             const float* hsrc = a.h + (size_t)jb * a.B;
             if (vec) {
-                for (int c = t; c < nrow * a.B / 4; c += kLoaders) cp16(hd + 16 * c, hsrc + 4 * c);
+                for (int c = t; c < nrow * a.B / 4; c += kQLoaders) cp16(hd + 16 * c, hsrc + 4 * c);
             } else {
-                for (int c = t; c < nrow * a.B; c += kLoaders) cp4(hd + 4 * c, hsrc + c);
+                for (int c = t; c < nrow * a.B; c += kQLoaders) cp4(hd + 4 * c, hsrc + c);
             }
             if (64 * (++ist) >= pc.j1 - pc.j0) {
                 ++ipc;
@@ -1346,42 +1366,38 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fc2q_tc(TcFc2qArgs a) {
             unsigned char* sb = ring + (size_t)(q % C::S) * C::STAGE;
             // A: word c of row r holds columns 8c .. 8c+7 of the tile
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int w = t + 128 * i, r = w >> 4, c = w & 15;
+            for (int i = 0; i < 4; ++i) {
+                const int w = t + kQLoaders * i, r = w >> 4, c = w & 15;
                 const uint4 hv = q8_f16(*reinterpret_cast<const uint32_t*>(rw + r * 64 + 4 * c));
                 *reinterpret_cast<uint4*>(sb + (c >> 3) * 1024 + (r >> 3) * 2048 + (r & 7) * 128 +
                                           (((c & 7) ^ (r & 7)) << 4)) = hv;
             }
-            // B: rows 8 kc .. 8 kc + 7 of token tok, every group
-            const int kc = t >> 4, tok = t & 15;
+            // B: rows 8 kc .. 8 kc + 7 of token tok, groups 2 gp and 2 gp + 1
+            const int tok = t & 15, kc = (t >> 4) & 7, gp = t >> 7;
             const int* val = reinterpret_cast<const int*>(rw + C::RCODE + C::RSC);
             const float* hr = reinterpret_cast<const float*>(rw + C::RCODE + C::RSC + C::RVAL);
             float hv[8];
-            uint2 sc[8];
+            uint32_t sw[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int r = 8 * kc + e;
                 const bool ok = tok < a.B && val[r] != 0;
                 hv[e] = ok ? hr[r * a.B + tok] : 0.f;
-                sc[e] = ok ? *reinterpret_cast<const uint2*>(rw + C::RCODE + 8 * r) : make_uint2(0u, 0u);
+                sw[e] = ok ? reinterpret_cast<const uint32_t*>(rw + C::RCODE + 8 * r)[gp] : 0u;
             }
             unsigned char* bo = sb + kTileA + kc * (C::N * 16);
 #pragma unroll
-            for (int grp = 0; grp < 4; ++grp) {
+            for (int u = 0; u < 2; ++u) {
+                const int grp = 2 * gp + u;
                 uint32_t hi[4], lo[4];
 #pragma unroll
                 for (int e2 = 0; e2 < 4; ++e2) {
-                    float v[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const uint2 w = sc[2 * e2 + u];
-                        const uint32_t word = grp < 2 ? w.x : w.y;
-                        const float sv = __half2float(__ushort_as_half((unsigned short)(word >> (16 * (grp & 1)))));
-                        v[u] = hv[2 * e2 + u] * sv;
-                    }
-                    const __half2 h2 = __floats2half2_rn(v[0], v[1]);
+                    const float s0 = __half2float(__ushort_as_half((unsigned short)(sw[2 * e2] >> (16 * u))));
+                    const float s1 = __half2float(__ushort_as_half((unsigned short)(sw[2 * e2 + 1] >> (16 * u))));
+                    const float v0 = hv[2 * e2] * s0, v1 = hv[2 * e2 + 1] * s1;
+                    const __half2 h2 = __floats2half2_rn(v0, v1);
                     const float2 bk = __half22float2(h2);
-                    const __half2 l2 = __floats2half2_rn((v[0] - bk.x) * 2048.f, (v[1] - bk.y) * 2048.f);
+                    const __half2 l2 = __floats2half2_rn((v0 - bk.x) * 2048.f, (v1 - bk.y) * 2048.f);
                     hi[e2] = *reinterpret_cast<const uint32_t*>(&h2);
                     lo[e2] = *reinterpret_cast<const uint32_t*>(&l2);
                 }
@@ -1397,37 +1413,43 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fc2q_tc(TcFc2qArgs a) {
         while (fq < total && fq <= C::LAG) copy_ids();
         cp_commit();
         cp_wait_all();
-        loaders_sync_any(false);
+        qloaders_sync_any(false);
         bool ok = true;
         for (int q = 0; q < total + C::LAG; ++q) {
+            const int cv = q - C::LAG;
+            if (cv >= 0) {
+                // this thread's copies of stage cv (and the ids of stage q) have
+                // landed; every loader's, after the barrier
+                cp_wait<C::LAG - 1>();
+                if (qloaders_sync_any(!ok || *(volatile int*)&abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (cv >= C::S) {   // the MMAs of stage cv - S have released the operand stage
+                    bool good = true;
+                    if (lane == 0) good = bar_wait(&empty[cv % C::S], ((cv / C::S) - 1) & 1, ctl);
+                    if (!__shfl_sync(FULL, good ? 1 : 0, 0)) {
+                        ok = false;
+                        cp_commit();
+                        continue;   // the next barrier stops every loader
+                    }
+                }
+            }
             if (q < total) {
                 issue(q);
                 if (fq < total) copy_ids();   // ids of stage q + LAG + 1
             }
+            if (cv >= 0) convert(cv);
             cp_commit();
-            const int cv = q - C::LAG;
-            if (cv < 0) continue;
-            cp_wait<C::LAG>();   // this thread's copies of stage cv (and the ids of stage q + 1) have landed
-            if (loaders_sync_any(!ok || *(volatile int*)&abort_flag)) {
-                ok = false;
-                break;
+            if (cv >= 0) {
+                fence_async_smem();
+                warp_arrive(&full[cv % C::S]);
             }
-            if (cv >= C::S) {   // the MMAs of stage cv - S have released the operand stage
-                bool good = true;
-                if (lane == 0) good = bar_wait(&empty[cv % C::S], ((cv / C::S) - 1) & 1, ctl);
-                if (!__shfl_sync(FULL, good ? 1 : 0, 0)) {
-                    ok = false;
-                    continue;   // the next barrier stops every loader
-                }
-            }
-            convert(cv);
-            fence_async_smem();
-            warp_arrive(&full[cv % C::S]);
         }
         cp_wait_all();
-    } else if (warp < 8) {
+    } else if (warp < kMma) {
         // ---- epilogue: TMEM lane m = column col0 + m, group e = m / 32
-        const int e = warp - 4, m = 32 * e + lane;
+        const int e = warp - kEpi, m = 32 * e + lane;
         for (int p = 0; p < npiece; ++p) {
             const int b = p & 1;
             if (!bar_wait(&accf[b], (p >> 1) & 1, ctl)) break;
@@ -1497,7 +1519,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_fc2q_tc(TcFc2qArgs a) {
     }
     tc_before();
     __syncthreads();
-    if (warp == 8) {
+    if (warp == kMma) {
         tc_after();
         tmem_free(tmem, C::TMEM);
     }
@@ -1716,7 +1738,7 @@ cudaError_t launch_fc2_tc4(const Plan& p, const float* h, const int32_t* idx, co
                  wait_timeout_ns(), p.B, p.d, slots};
     cudaError_t e = prep(k_fc2q_tc<16>, Fc2qCfg<16>::SMEM);
     if (e != cudaSuccess) return e;
-    launch_pdl(k_fc2q_tc<16>, G, kTcThreads, Fc2qCfg<16>::SMEM, s, a);
+    launch_pdl(k_fc2q_tc<16>, G, kQThreads, Fc2qCfg<16>::SMEM, s, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     launch_pdl(k_fc2_tc_reduce, dim3(p.d / 128, ceil_div(p.B, 8)), 1024, 0, s, static_cast<const float*>(partial),
