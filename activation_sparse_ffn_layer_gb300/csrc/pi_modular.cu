@@ -434,35 +434,62 @@ __global__ void __launch_bounds__(256) k_fc2_part(const float* __restrict__ h, i
         }
         __syncthreads();
         if (!active) continue;
-#pragma unroll 4
-        for (int t = 0; t < cnt; ++t) {
-            const int k = sidx[t];
-            if (k < 0) continue;
-            // rows past the hot tier come from the second tier
-            const bool hot = k < cold.n_hot;
-            const size_t kr = hot ? (size_t)k : (size_t)(k - cold.n_hot);
+        // rows in batches of U: the batch's loads are all requested before the
+        // first is used; the products are added in row order as before
+        constexpr int U = TB <= 2 ? 8 : 4;
+        for (int t0 = 0; t0 < cnt; t0 += U) {
+            int kk[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) kk[u] = t0 + u < cnt ? sidx[t0 + u] : -1;
             if (!INT4) {
-                float wf[8];
-                h8_to_f8(ld_stream16(static_cast<const __half*>(hot ? w2t : cold.w2t) + kr * d + c), wf);
+                uint4 wv[U];
 #pragma unroll
-                for (int tb = 0; tb < TB; ++tb) {
-                    const float hv = sh[t * TB + tb];
+                for (int u = 0; u < U; ++u) {
+                    // rows past the hot tier come from the second tier
+                    const int k = kk[u];
+                    const bool hot = k < cold.n_hot;
+                    const size_t kr = hot ? (size_t)k : (size_t)(k - cold.n_hot);
+                    wv[u] = k >= 0 ? ld_stream16(static_cast<const __half*>(hot ? w2t : cold.w2t) + kr * d + c)
+                                   : make_uint4(0u, 0u, 0u, 0u);
+                }
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[tb][e] = fmaf(hv, wf[e], acc[tb][e]);
+                for (int u = 0; u < U; ++u) {
+                    if (kk[u] < 0) continue;
+                    float wf[8];
+                    h8_to_f8(wv[u], wf);
+#pragma unroll
+                    for (int tb = 0; tb < TB; ++tb) {
+                        const float hv = sh[(t0 + u) * TB + tb];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[tb][e] = fmaf(hv, wf[e], acc[tb][e]);
+                    }
                 }
             } else {
-                const uint2 q = ld_stream8(static_cast<const uint8_t*>(hot ? w2t : cold.w2t) + kr * (d / 2) + c / 2);
-                const float sc = __half2float((hot ? w2ts : cold.w2ts)[kr * (d / 32) + c / 32]);
-                float qa[8], qb[8];
-                q8_to_f8(q.x, qa);
-                q8_to_f8(q.y, qb);
+                uint2 qv[U];
+                float sv[U];
 #pragma unroll
-                for (int tb = 0; tb < TB; ++tb) {
-                    const float hv = sh[t * TB + tb] * sc;
+                for (int u = 0; u < U; ++u) {
+                    const int k = kk[u];
+                    const bool hot = k < cold.n_hot;
+                    const size_t kr = hot ? (size_t)k : (size_t)(k - cold.n_hot);
+                    qv[u] = k >= 0 ? ld_stream8(static_cast<const uint8_t*>(hot ? w2t : cold.w2t) + kr * (d / 2) + c / 2)
+                                   : make_uint2(0u, 0u);
+                    sv[u] = k >= 0 ? __half2float((hot ? w2ts : cold.w2ts)[kr * (d / 32) + c / 32]) : 0.f;
+                }
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        acc[tb][e] = fmaf(hv, qa[e], acc[tb][e]);
-                        acc[tb][8 + e] = fmaf(hv, qb[e], acc[tb][8 + e]);
+                for (int u = 0; u < U; ++u) {
+                    if (kk[u] < 0) continue;
+                    float qa[8], qb[8];
+                    q8_to_f8(qv[u].x, qa);
+                    q8_to_f8(qv[u].y, qb);
+#pragma unroll
+                    for (int tb = 0; tb < TB; ++tb) {
+                        const float hv = sh[(t0 + u) * TB + tb] * sv[u];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            acc[tb][e] = fmaf(hv, qa[e], acc[tb][e]);
+                            acc[tb][8 + e] = fmaf(hv, qb[e], acc[tb][8 + e]);
+                        }
                     }
                 }
             }
