@@ -185,7 +185,9 @@ def run(config: str, batch: int, once: bool = False, cold: str = "", n_hot: int 
                           "listed": n, "live": live, **extra}), flush=True)
 
 
-def run_attn(config: str, batch: int, once: bool = False, max_seq: int = 1024):
+def run_attn(config: str, batch: int, once: bool = False, max_seq: int = 1024, quiet: bool = False):
+    """Times pi_attn_heads; returns the result line as a dict (also printed
+    unless quiet)."""
     from synth import ATTN_CONFIGS, decode_lengths, make_attn, make_kv_cache
 
     B.lib()
@@ -234,10 +236,13 @@ def run_attn(config: str, batch: int, once: bool = False, max_seq: int = 1024):
     us = _time(call)
     gbs = moved / us / 1e3
     peak = _peak_gbs()
-    print(json.dumps({"call": "pi_attn_heads", "config": config, "batch": batch, "us": round(us, 2),
-                      "bytes": moved, "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
-                      "heads": H, "union_heads": union, "active_pairs": int(sum(map(sum, on))),
-                      "cache_lengths": lengths[:4], "max_seq": max_seq}), flush=True)
+    res = {"call": "pi_attn_heads", "config": config, "workload": cfg.name, "batch": batch, "us": round(us, 2),
+           "bytes": moved, "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+           "heads": H, "union_heads": union, "active_pairs": int(sum(map(sum, on))),
+           "cache_lengths": lengths[:4], "max_seq": max_seq}
+    if not quiet:
+        print(json.dumps(res), flush=True)
+    return res
 
 
 def main(argv=None):

@@ -10,7 +10,8 @@ far larger than L2, so no flush is needed.  After the headline, the other
 workloads are timed the same way at batch 1 and full depth (OPT-125M-shaped
 layer in rotation over copies larger than L2, OPT-6.7B-, OPT-30B- and
 LLaMA-70B-shaped stacks) and listed under "other_workloads", with the launch
-floor of the persistent kernel.
+floor of the persistent kernel and one batch-1 call of the head-sparse
+attention block of the same model shape ("attention_heads").
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config c5] [--impl ours|reference]
 
@@ -394,6 +395,13 @@ def run_ours(args):
             torch.cuda.empty_cache()
         out["other_workloads"] = extras
         out["launch_floor_us"] = launch_floor()
+        # the head-sparse attention block of the same model shape, batch 1
+        from activation_sparse_ffn_layer_gb300.entry_bench import run_attn
+        if cfg.key in ("c2", "c3", "c4", "c5"):
+            a = run_attn(cfg.key, 1, quiet=True)
+            out["attention_heads"] = {k: a[k] for k in ("workload", "batch", "us", "bytes", "gbs", "frac_of_peak",
+                                                        "heads", "union_heads", "cache_lengths")}
+            torch.cuda.empty_cache()
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
