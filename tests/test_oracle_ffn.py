@@ -10,6 +10,9 @@
 - invariant (iii): brute force over all 2^F masks of a tiny layer: every
   mask's contribution is the sum of its single neurons' contributions;
 - gated and INT4 layers reduce, in special cases, to the plain fp16 layer;
+- FC1, FC2 and the gated FC1 against a layer worked by hand
+  (tests/golden/ffn_small.txt); the gated layer in general against torch's
+  products in fp64;
 - the normalisation against hand-worked values and its guard band.
 """
 import itertools
@@ -207,3 +210,64 @@ def test_rmsnorm_band_bounds_fp32_evaluation():
             # the fp64 pre-rounding value of the float32 input
             _, pre32, _ = oracle.rmsnorm_half(y32.astype(np.float64), 1e-6)
             assert np.all(np.abs(v32 - pre32) <= band / 2 + 1e-300)
+
+
+def _fixture(name):
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                k, *v = line.split()
+                out.setdefault(k, []).append([float(t) for t in v])
+    return out
+
+
+def _hand_layer(g, gated):
+    h16 = lambda rows: np.asarray(rows, dtype=np.float64).astype(np.float16)
+    F = len(g["w1"])
+    d = len(g["x"][0])
+    return SimpleNamespace(d=d, F=F, r=1, int4=False, gated=gated, w1=h16(g["w1"]), b1=h16(g["b1"][0]),
+                           wu=h16(g["wu"]) if gated else None, w2t=h16(g["w2t"]), b2=h16(g["b2"][0]),
+                           p1=np.zeros((1, d), np.float16), p2=np.zeros((F, 1), np.float16),
+                           table=np.arange(F, dtype=np.int32))
+
+
+def test_fc1_fc2_hand_example():
+    g = _fixture("ffn_small.txt")
+    x = np.asarray(g["x"][0], dtype=np.float64).astype(np.float16)
+    for gated, hk, yk in ((False, "h", "y"), (True, "h_gated", "y_gated")):
+        L = _hand_layer(g, gated)
+        idx = np.arange(L.F, dtype=np.int32)
+        h = oracle.fc1(x, L, idx)
+        np.testing.assert_array_equal(h, g[hk][0])
+        np.testing.assert_array_equal(oracle.fc2(h, L, idx), g[yk][0])
+        np.testing.assert_array_equal(oracle.ffn_dense(x, L), g[yk][0])
+        np.testing.assert_array_equal(oracle.ffn_masked(x, L, _mask_from_bits([True] * L.F)), g[yk][0])
+    L = _hand_layer(g, False)
+    idx = np.asarray(g["fc2_idx"][0], dtype=np.int32)
+    np.testing.assert_array_equal(oracle.fc2(np.asarray(g["fc2_h"][0]), L, idx), g["fc2_y"][0])
+    # FC1 on a sub-list returns the listed rows' outputs in list order
+    np.testing.assert_array_equal(oracle.fc1(x, L, np.asarray([2, 1], np.int32)), [0.0, 0.5])
+
+
+def test_gated_layer_matches_torch_products():
+    rng = np.random.default_rng(21)
+    d, F = 48, 40
+    wg = (rng.standard_normal((F, d)) * 0.2).astype(np.float16)
+    wu = (rng.standard_normal((F, d)) * 0.2).astype(np.float16)
+    w2t = (rng.standard_normal((F, d)) * 0.2).astype(np.float16)
+    bg = (rng.standard_normal(F) * 0.3).astype(np.float16)
+    b2 = (rng.standard_normal(d) * 0.1).astype(np.float16)
+    x = rng.standard_normal(d).astype(np.float16)
+    L = SimpleNamespace(d=d, F=F, r=1, int4=False, gated=True, w1=wg, b1=bg, wu=wu, w2t=w2t, b2=b2,
+                        p1=np.zeros((1, d), np.float16), p2=np.zeros((F, 1), np.float16),
+                        table=np.arange(F, dtype=np.int32))
+    t = lambda a: torch.from_numpy(np.asarray(a, dtype=np.float64))
+    gate = torch.nn.functional.linear(t(x), t(wg), t(bg))
+    up = torch.nn.functional.linear(t(x), t(wu))
+    h = torch.relu(gate) * up
+    y = torch.nn.functional.linear(h, t(w2t).T, t(b2))
+    np.testing.assert_allclose(oracle.fc1(x, L, np.arange(F, dtype=np.int32)), h.numpy(), rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(oracle.ffn_dense(x, L), y.numpy(), rtol=1e-12, atol=1e-13)
+    assert 0 < int((h.numpy() != 0).sum()) < F

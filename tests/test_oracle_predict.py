@@ -5,7 +5,8 @@
   exactly the set of neurons the FFN's ReLU keeps (checked through the
   oracle's separate FFN code);
 - the guard band really bounds fp32 evaluations of the score;
-- compaction against hand-worked masks and against its defining properties.
+- compaction against hand-worked masks and against its defining properties;
+- the batch union of masks against a hand-worked example (tests/golden/mask_union_small.txt).
 """
 import os
 from types import SimpleNamespace
@@ -171,3 +172,11 @@ def test_mask_union_is_bitwise_or():
         for b in range(5):
             acc |= int(masks[b, w])
         assert int(u[w]) == acc
+
+
+def test_mask_union_hand_example():
+    g = _fixture("mask_union_small.txt")
+    F = int(g["F"][0][0])
+    masks = np.asarray(g["mask"], dtype=np.uint64).astype(np.uint32)
+    u = oracle.mask_union(masks, F)
+    assert [int(v) for v in u] == [int(v) for v in g["union"][0]]
