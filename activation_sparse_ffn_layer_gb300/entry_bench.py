@@ -185,9 +185,11 @@ def run(config: str, batch: int, once: bool = False, cold: str = "", n_hot: int 
                           "listed": n, "live": live, **extra}), flush=True)
 
 
-def run_attn(config: str, batch: int, once: bool = False, max_seq: int = 1024, quiet: bool = False):
+def run_attn(config: str, batch: int, once: bool = False, max_seq: int = 1024, quiet: bool = False,
+             context: int = 0):
     """Times pi_attn_heads; returns the result line as a dict (also printed
-    unless quiet)."""
+    unless quiet).  context > 0: every sequence's cache holds that many
+    positions (the capacity grows to fit) instead of the decode-length mix."""
     from synth import ATTN_CONFIGS, decode_lengths, make_attn, make_kv_cache
 
     B.lib()
@@ -196,6 +198,9 @@ def run_attn(config: str, batch: int, once: bool = False, max_seq: int = 1024, q
     blocks = [make_attn(cfg, l, device=dev) for l in range(2)]
     H, KVH, dh, d = cfg.heads, cfg.kv_heads, cfg.head_dim, cfg.d
     lengths = decode_lengths(cfg, batch)
+    if context > 0:
+        lengths = [context] * batch
+        max_seq = max(max_seq, context + 1)
     caches = [make_kv_cache(cfg, lengths, seed=l, device=dev, max_seq=max_seq) for l in range(2)]
     g = torch.Generator(device=dev).manual_seed(7)
     x = torch.randn(batch, d, generator=g, device=dev).to(torch.float16)
@@ -255,10 +260,12 @@ def main(argv=None):
                          "or in a second device buffer")
     ap.add_argument("--n-hot", type=int, default=0, help="rows kept in the first tier with --cold (0: none)")
     ap.add_argument("--attn", action="store_true", help="time the head-sparse attention block instead")
+    ap.add_argument("--context", type=int, default=0, help="with --attn: cache positions per sequence "
+                    "(default: a 128-token prompt plus ragged decode steps)")
     args = ap.parse_args(argv)
     assert torch.cuda.is_available(), "needs a CUDA GPU"
     if args.attn:
-        run_attn(args.config, args.batch, args.once)
+        run_attn(args.config, args.batch, args.once, context=args.context)
     else:
         run(args.config, args.batch, args.once, args.cold, args.n_hot)
 

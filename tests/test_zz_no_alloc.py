@@ -55,6 +55,8 @@ def _case(P, cfg, batch, token0):
     ("gated-b32", small(CONFIGS["c4"], d=8192, F=2048, rank=64), 32),
     # INT4 streamed CUDA-core path
     ("int4-b3", small(CONFIGS["c5"], d=1024, F=4100, rank=64), 3),
+    # INT4 tensor-core FC2 (16 tokens)
+    ("int4-b16", small(CONFIGS["c5"], d=1024, F=4100, rank=64), 16),
 ])
 def test_noalloc_fc2_matches_workspace_fc2_twice(kind, cfg, batch):
     import activation_sparse_ffn_layer_gb300 as P
