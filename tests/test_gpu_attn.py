@@ -110,18 +110,19 @@ def test_attn_heads_small(P, H, KVH, dh, d, smax, lengths):
     assert 0 < on.sum() < on.size, "the synthetic head predictor should keep some heads and drop others"
 
 
-@pytest.mark.parametrize("B", [2, 8, 16, 32])
-def test_attn_heads_batches(P, B):
-    """Batches that take the output projection's streamed (2..8) and
-    tensor-core (16..32) paths."""
-    cfg = small_attn(ATTN_CONFIGS["c2"], d=512, heads=8, kv_heads=8, head_dim=64, rank=8, max_seq=48,
+@pytest.mark.parametrize("B,d", [(2, 512), (5, 512), (8, 512), (11, 512), (16, 512), (32, 512), (16, 320)])
+def test_attn_heads_batches(P, B, d):
+    """Batches that take each projection and output-projection path: per-token
+    (1..4, 9..15, and widths off the tensor-core tiles), streamed (5..8),
+    tensor cores (16..32)."""
+    cfg = small_attn(ATTN_CONFIGS["c2"], d=d, heads=8, kv_heads=8, head_dim=64, rank=8, max_seq=48,
                      index=90 + B)
     w = make_attn(cfg)
     lengths = [(7 * b + 3) % 48 for b in range(B)]
     kc, vc = make_kv_cache(cfg, lengths, seed=B)
     x = _tokens(cfg.d, B, 200 + B)
     g = _run(P, cfg, w, x, lengths, kc, vc, cfg.tau)
-    _check(cfg, w, x, lengths, kc, vc, g, f"B{B}")
+    _check(cfg, w, x, lengths, kc, vc, g, f"B{B} d{d}")
 
 
 def test_attn_heads_no_head_and_all_heads(P):
