@@ -10,7 +10,8 @@
 //      a CTA computes the FFN of exactly the neurons it predicted
 //   D  y columns   = b2 + sum of all partials (fixed order), sum of squares
 //   (next layer)   x = fp16(y / sqrt(mean(y^2) + eps))
-// with one grid barrier after each phase (three per layer).  Rows are owned in
+// with one grid barrier after each phase (three per layer; the last layer's
+// third is the end of the grid).  Rows are owned in
 // pieces of 8: the pieces of round k (G consecutive pieces) go to the CTAs in
 // ascending order for even k and descending order for odd k, so that the hot
 // rows at the start of the table spread over all CTAs.
@@ -393,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
         const unsigned S = (unsigned)p.fc_slots;
         for (unsigned g = fc_hi > S ? fc_hi - S : 0u; g < fc_hi; ++g) mbar_drain(&fc_full[g % S], (g / S) & 1u, kDrainTimeoutNs);
         if (c == 0 && tid == 0) {
-            const unsigned long long next = ebase + (unsigned long long)kBarriersPerLayer * p.L;
+            const unsigned long long next = ebase + (unsigned long long)kBarriersPerLayer * p.L - 1;
             __stcg(p.epoch, next);
         }
     };
@@ -1234,7 +1235,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
             if (c == 0 && tid == 0) *p.count_out = total;
         }
         PI_STAMP(l, 7);
-        if (!sync()) { leave(); return; }
+        // the next layer's input needs every CTA's columns of y; after the last
+        // layer the end of the grid publishes them
+        if (l + 1 < p.L && !sync()) { leave(); return; }
     }
     leave();
 }
