@@ -34,6 +34,10 @@ PI_DEV void warp_arrive(unsigned long long* b) {
     __syncwarp();
     if ((threadIdx.x & 31) == 0) bar_arrive(b);
 }
+// one arrival that also expects `bytes` of asynchronous copies (TMA) on the barrier
+PI_DEV void bar_arrive_expect_tx(unsigned long long* b, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
+}
 PI_DEV bool bar_try(unsigned long long* b, unsigned parity) {
     unsigned ok;
     asm volatile(

@@ -38,7 +38,11 @@
 // lo = fp16(h - hi), placed as extra N columns: hi + lo carries 22 bits of h,
 // so the product keeps fp32-level accuracy.  Weights and x are fp16 already,
 // and fp16 x fp16 products are exact in the fp32 accumulator.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
 
 #include "pi_common.cuh"
 #include "pi_internal.h"
@@ -99,6 +103,15 @@ PI_DEV void mma_f16_ta(unsigned tmem_d, unsigned tmem_a, uint64_t b, unsigned id
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(tmem_d),
         "r"(tmem_a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// 2-D tiled TMA load of the box at (x = inner element, y = row) into shared
+// memory, completing on the barrier (the tensor map carries shape, box and swizzle)
+PI_DEV void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, unsigned long long* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            su32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(su32(bar))
         : "memory");
 }
 PI_DEV void mma_commit(unsigned long long* b) {
@@ -195,6 +208,9 @@ struct RowsCfg {
 };
 
 struct TcRowsArgs {
+    CUtensorMap tma_a;     // modes 2-3 with use_tma: A rows [R][K] fp16, box 64 x 128, 128-byte swizzle
+    CUtensorMap tma_b;     // ... and the B operand rows [bop_rows][K], box 64 x NB
+    int use_tma;           // 1: one thread loads A and B tiles by TMA (contiguous A rows)
     const __half* a0;      // A rows (row length K)
     const __half* a1;      // up-projection rows (gated FC1)
     const uint8_t* q;      // mode 4: W1 codes [F][K/2]
@@ -488,9 +504,12 @@ PI_DEV void q4_epilogue(const TcRowsArgs& a, const SpanOf& span, int npiece, int
 }
 
 template <int MODE, int NT>
-__global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
+__global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(const __grid_constant__ TcRowsArgs a) {
     pdl_entry();
     using C = RowsCfg<MODE, NT>;
+    // contiguous A rows (predictor P1, P2) may come by TMA: one thread issues
+    // the A and B tiles of each stage (128-byte swizzle, the MMA layout)
+    const bool TMA = (MODE == 2 || MODE == 3) && a.use_tma != 0;
     extern __shared__ unsigned char dsm[];
     __shared__ __align__(8) unsigned long long full[C::S], empty[C::S], accf[2], acce[2], drain;
     __shared__ __align__(8) unsigned long long cempty[C::CS];   // INT4 accumulator slots read
@@ -533,7 +552,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
     if (warp == 8) {
         if (lane == 0) {
             for (int s = 0; s < C::S; ++s) {
-                bar_init(&full[s], kLoaderWarps);
+                bar_init(&full[s], TMA ? 1 : kLoaderWarps);
                 bar_init(&empty[s], 1);
             }
             for (int b = 0; b < 2; ++b) {
@@ -561,6 +580,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
 
     if (warp < 4 && C::Q4) {
         if constexpr (C::Q4) q4_loader<C>(a, ring, span, npiece, R, srow, tmem, full, empty, ctl);
+    } else if (warp < 4 && TMA) {
+        // ---- TMA producer (one thread): stage it = (piece, K-chunk) in order
+        if (tid == 0) {
+            constexpr unsigned kBytes = (unsigned)(C::NA * kTileA + C::X);
+            int it = 0;
+            bool ok = true;
+            for (int p = 0; p < npiece && ok; ++p) {
+                const Span sp = span(p);
+                for (int ks = sp.kc0; ks < sp.kc1; ++ks, ++it) {
+                    const int s = it % C::S;
+                    if (it >= C::S && !bar_wait(&empty[s], ((it / C::S) - 1) & 1, ctl)) {
+                        ok = false;
+                        break;
+                    }
+                    unsigned char* st = ring + (size_t)s * C::STAGE;
+                    bar_arrive_expect_tx(&full[s], kBytes);
+                    tma_load_2d(st, &a.tma_a, 64 * ks, 128 * sp.tile, &full[s]);
+                    tma_load_2d(st + C::NA * kTileA, &a.tma_b, 64 * ks, 0, &full[s]);
+                }
+            }
+            // every copy issued has landed before the CTA may exit
+            for (int s = 0; s < C::S && s < it; ++s) {
+                const int last = s + ((it - 1 - s) / C::S) * C::S;
+                bar_drain(&full[s], (last / C::S) & 1, kDrainTimeoutNs);
+            }
+        }
     } else if (warp < 4) {
         // ---- loaders.  A tiles use the 128-byte-swizzled layout, so the 8
         // lanes of one shared-memory phase copy the 8 chunks of one row's 128
@@ -758,7 +803,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
             ok = q4_mma<C>(ring, total, tmem, full, empty, cempty, ctl, it);
         }
         const uint64_t ad0 = sdesc_sw128(su32(ring));
-        const uint64_t bd0 = sdesc(su32(ring) + C::NA * kTileA, C::NB * 16, 128);
+        // B: swizzled like A when it comes by TMA, else core matrices of 8 rows
+        const uint64_t bd0 = TMA ? sdesc_sw128(su32(ring) + C::NA * kTileA)
+                                 : sdesc(su32(ring) + C::NA * kTileA, C::NB * 16, 128);
+        const uint64_t bstep = TMA ? 2u : (uint64_t)((2 * C::NB * 16) >> 4);   // per K-step of 16
         for (int p = 0; p < npiece && ok && !C::Q4; ++p) {
             const Span sp = span(p);
             const int b = p & 1;
@@ -783,7 +831,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
                 if (64 * ks + 64 <= a.K) {
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t bk = bd + (uint64_t)((kk * 2 * C::NB * 16) >> 4);
+                        const uint64_t bk = bd + bstep * (uint64_t)kk;
                         const unsigned acc = kk > 0 ? 1u : first;
                         mma_f16(dcol, ad + (uint64_t)(2 * kk), bk, idesc, acc);
                         if (MODE == 1) mma_f16(dcol + C::NB, ad + (uint64_t)((kTileA >> 4) + 2 * kk), bk, idesc, acc);
@@ -791,7 +839,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_rows_tc(TcRowsArgs a) {
                 } else {
                     const int ksteps = (a.K - 64 * ks) / 16;
                     for (int kk = 0; kk < ksteps; ++kk) {
-                        const uint64_t bk = bd + (uint64_t)((kk * 2 * C::NB * 16) >> 4);
+                        const uint64_t bk = bd + bstep * (uint64_t)kk;
                         const unsigned acc = kk > 0 ? 1u : first;
                         mma_f16(dcol, ad + (uint64_t)(2 * kk), bk, idesc, acc);
                         if (MODE == 1) mma_f16(dcol + C::NB, ad + (uint64_t)((kTileA >> 4) + 2 * kk), bk, idesc, acc);
@@ -1559,6 +1607,37 @@ cudaError_t prep(K kernel, size_t smem) {
 
 namespace {
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (the library
+// links only the CUDA runtime)
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// Tensor map of `rows` fp16 rows of `inner` elements (row stride inner * 2
+// bytes) read in boxes of 64 elements x box_rows rows with the 128-byte
+// swizzle of the MMA operand tiles; rows and columns past the end read as zero.
+bool rows_tensor_map(CUtensorMap* m, const void* base, int inner, int rows, int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
+    if (fn == nullptr || (reinterpret_cast<uintptr_t>(base) & 15) != 0 || (inner * 2) % 16 != 0) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    const cuuint32_t es[2] = {1u, 1u};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 int slots_for(int tiles, int G) { return ceil_div(tiles, G) + 2; }
 // CTAs of the u = P1 x split.  P1 is small: at least 8 K-chunks per CTA keeps
 // the number of partials per u element (the finish kernel's fan-in) low.
@@ -1629,6 +1708,8 @@ cudaError_t launch_predict_tc(const Plan& p, const __half* x, const __half* p1, 
     a.bop = x;
     a.bop_rows = p.B;
     a.K = p.d;
+    // P1 rows and x by TMA (the loaders' gather path stays for a failed encode)
+    a.use_tma = rows_tensor_map(&a.tma_a, p1, p.d, p.r, 128) && rows_tensor_map(&a.tma_b, x, p.d, p.B, nt) ? 1 : 0;
     a.B = p.B;
     a.part = part;
     a.slots = slots_for(ceil_div(p.r, 128), Gu);
@@ -1646,6 +1727,8 @@ cudaError_t launch_predict_tc(const Plan& p, const __half* x, const __half* p1, 
     b.bop = uhl;
     b.bop_rows = 2 * nt;
     b.K = p.r;
+    b.use_tma = rows_tensor_map(&b.tma_a, p2, p.r, p.F, 128) && rows_tensor_map(&b.tma_b, uhl, p.r, 2 * nt, 2 * nt)
+                    ? 1 : 0;
     b.B = p.B;
     b.bias = bpred;
     b.tau = tau;
