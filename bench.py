@@ -290,7 +290,8 @@ def summary_line(res, peak):
 def launch_floor(K=200, W=20):
     """Time of one graph-replayed step of the smallest stack the persistent
     kernel takes (one layer, d = 256, F = 256, rank 8): the fixed cost of a
-    launch and its three grid barriers, with almost no bytes to move."""
+    launch and its two grid barriers (a one-layer step), with almost no bytes
+    to move."""
     import torch
     from activation_sparse_ffn_layer_gb300.runtime import DecodeStack
     from synth import CONFIGS, make_layer, make_tokens, small
