@@ -201,22 +201,27 @@ struct FusedParams {
     FusedLayer layers[kMaxFusedLayers];
 };
 
-// Dynamic smem layout (bytes): x half[d] | u float[rmax] | ustage float[usmax]
+// Dynamic smem layout (bytes): x half[d] | u / ustage float[max(rmax, usmax)]
 //   | scratch | m16 int[M] | upre int[M+1] | lidx int[cap] | lh float[cap]
 //   | P1 slice | P2 slice | bias slice   (the last three only with pred_smem)
 // lidx / lh hold this CTA's own active rows from the end of its mask units to
 // the end of FC2 (to the end of the step in the last layer, where m16 / upre
 // then take the whole mask for the list positions); the P2 ring, idle then,
-// spans m16 .. lh together with the staging region.
+// spans m16 .. lh together with the staging region.  The u partials are
+// staged where u goes: thread i reads entries i, r + i, ... of the staging and
+// then writes u[i], which no other thread reads.  The scratch holds FC1's warp
+// sums of 128 rows (gated: and of the up rows) and the reduction's float4 sums.
 struct SmemPlan {
-    int d, rmax, usmax, M, cap;
+    int d, rmax, usmax, M, cap, gated;
     int p1s = 0, p2s = 0, b1s = 0;  // shared predictor buffers (bytes, 16-aligned), 0 if unused
     int stage = 0;                  // staging region (bytes, 16-aligned): the predictor buffers
                                     // up to the mask bits, then the ring of this CTA's FC rows
     __host__ __device__ int off_u() const { return ((d * 2 + 15) / 16) * 16; }
-    __host__ __device__ int off_ust() const { return off_u() + rmax * 4; }
-    __host__ __device__ int off_scr() const { return ((off_ust() + ((usmax + 3) / 4) * 16 + 15) / 16) * 16; }
-    __host__ __device__ int off_m16() const { return off_scr() + 4096 * 4; }
+    __host__ __device__ int off_ust() const { return off_u(); }
+    __host__ __device__ int off_scr() const {
+        return ((off_u() + (((rmax > usmax ? rmax : usmax) + 3) / 4) * 16 + 15) / 16) * 16;
+    }
+    __host__ __device__ int off_m16() const { return off_scr() + (gated ? 8192 : 4096); }
     __host__ __device__ int off_upre() const { return off_m16() + ((M + 1) / 2) * 8; }
     __host__ __device__ int off_lidx() const { return off_upre() + (M + 1) * 4; }
     __host__ __device__ int off_lh() const { return off_lidx() + cap * 4; }
@@ -318,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
     const int npc = P / G + (piece_of(P / G) < P ? 1 : 0);
     const int nunits = (npc + 1) / 2;   // unit k = own pieces 2k, 2k+1
     const int cap = 16 * ((P + 2 * G - 1) / (2 * G));
-    SmemPlan sp{d, rmax, usmax, M, cap};
+    SmemPlan sp{d, rmax, usmax, M, cap, KIND == 1};
     sp.p1s = p.pred_smem ? p.p1s_bytes : 0;
     sp.p2s = p.pred_smem ? p.p2s_bytes : 0;
     sp.b1s = p.pred_smem ? p.b1s_bytes : 0;
@@ -865,7 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
             if (!p.pred_smem)
                 for (int q = tid; q < nmine; q += kThreads) lh[q] = __half2float(ly.b1[lidx[q]]);
             float* part = red;           // [128 rows][kWarps]
-            float* partu = red + 2048;   // gated: up-projection partials
+            float* partu = red + 1024;   // gated: up-projection partials
             const int nwd = d / 8;
             constexpr int RB = KIND == 1 ? 4 : 8;
             const int rbn = max(1, min(RB, S / (2 * fc1_rows)));   // half the slots per batch
@@ -1299,8 +1304,8 @@ struct XchgLayout {
     }
 };
 
-SmemPlan smem_plan(int d, int F, int rmax, size_t rmax_su, int G) {
-    return SmemPlan{d, rmax < 8 ? 8 : rmax, (int)rmax_su, (F + 15) / 16, 16 * max_units(F, G)};
+SmemPlan smem_plan(int d, int F, int rmax, size_t rmax_su, int G, bool gated) {
+    return SmemPlan{d, rmax < 8 ? 8 : rmax, (int)rmax_su, (F + 15) / 16, 16 * max_units(F, G), gated};
 }
 
 }  // namespace
@@ -1321,7 +1326,7 @@ bool fused_supported(int d, int F, int rmax, bool int4, bool gated, int G) {
     if (int4 && (d % 32 != 0 || d > 64 * kThreads)) return false;  // FC2: two groups per thread
     if (max_units(F, G) > kMaxUnits) return false;
     const size_t rmax_su = (size_t)16 * G + 2 * (size_t)rmax;
-    const SmemPlan sp = smem_plan(d, F, rmax, rmax_su, G);
+    const SmemPlan sp = smem_plan(d, F, rmax, rmax_su, G, gated);
     const long long room = 227ll * 1024 - 1024 - sp.off_stage();
     if (room <= 0) return false;
     return fc_slots_for(d, int4, (int)(room / 16 * 16)) >= (gated ? 4 : 2);
@@ -1356,7 +1361,7 @@ static bool plan_fused(const FusedStackArgs& a, FusedParams* out, size_t* smem_o
     // the u-partial staging buffer as the kernel sizes it: the largest r * su
     size_t usmax = 8;
     for (int l = 0; l < a.L; ++l) usmax = std::max(usmax, (size_t)prm.layers[l].r * prm.layers[l].su);
-    SmemPlan sp = smem_plan(a.d, a.F, rmax, usmax, G);
+    SmemPlan sp = smem_plan(a.d, a.F, rmax, usmax, G, a.gated);
     // shared predictor slices when they fit: P1 items, P2 units and bias of one CTA
     {
         size_t p1b = 16;

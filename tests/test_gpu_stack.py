@@ -24,9 +24,10 @@ def _mask_of(P, st):
     return st.workspace[lay.mask:lay.mask + 4 * W].view(torch.int32).cpu().numpy().view(np.uint32)
 
 
-def _check_stack(cfg, L, token=0):
+def _check_stack(cfg, L, token=0, p2_ring=False):
     """Run prefixes of the stack (1..L layers): the workspace then holds layer
-    l's mask, y_out is layer l's output and x_trace its inputs."""
+    l's mask, y_out is layer l's output and x_trace its inputs.  With p2_ring
+    the plan must stream P2 through the ring of 16-row slots."""
     P = _pi()
     from activation_sparse_ffn_layer_gb300.runtime import DecodeStack
     ws = [make_layer(cfg, l, device=DEV) for l in range(L)]
@@ -34,6 +35,9 @@ def _check_stack(cfg, L, token=0):
     x = make_tokens(cfg, token, 1, device=DEV)
     ambiguous = 0
     full = DecodeStack(ws, batch=1, tau=cfg.tau, eps=cfg.rms_eps)
+    if p2_ring:
+        plan = P.pi_stack_plan(full.desc, L, full.ranks)
+        assert plan.fused == 1 and plan.pred_in_smem == 0 and plan.p2_ring_slots >= 2, "P2 ring not taken"
     xs_full, y_full = full.step_trace(x)
     for l in range(L):
         st = DecodeStack(ws[: l + 1], batch=1, tau=cfg.tau, eps=cfg.rms_eps)
@@ -66,6 +70,19 @@ def _check_stack(cfg, L, token=0):
 ])
 def test_stack_layers_match_oracle(name, cfg, L):
     _check_stack(cfg, L)
+
+
+@pytest.mark.parametrize("name,cfg,L", [
+    # rank 1024 over 16390 rows: a block's P2 share (≥ 6 units of 32 KB) does not
+    # fit in shared memory, so P2 streams through the ring, whose slots and
+    # mbarrier phases carry over from layer to layer; ragged F (a short last
+    # piece), INT4, gated and plain fp16 rows
+    ("int4-ring", small(CONFIGS["c5"], d=1280, F=16390, rank=1024), 3),
+    ("gated-ring", small(CONFIGS["c4"], d=1024, F=16390, rank=1024), 3),
+    ("fp16-ring", small(CONFIGS["c2"], d=1024, F=16390, rank=1024), 3),
+])
+def test_stack_p2_ring_matches_oracle(name, cfg, L):
+    _check_stack(cfg, L, p2_ring=True)
 
 
 def test_stack_c2_full_shape_first_layers():

@@ -58,7 +58,11 @@ def test_wide_stack_layers_match_oracle_in_ring_modes(key):
     P = _pi()
     from activation_sparse_ffn_layer_gb300.runtime import DecodeStack
     cfg, L = CONFIGS[key], 3
-    ws = [make_layer(cfg, l, device=DEV) for l in range(L)]
+    # the three layers with the largest predictor ranks, in stack order (the
+    # OPT-30B-shaped stack's ranks vary from layer to layer; its largest ones are
+    # what the full stack's shared-memory plan is sized for)
+    picked = sorted(sorted(range(cfg.layers), key=lambda l: -cfg.layer_rank(l))[:L])
+    ws = [make_layer(cfg, l, device=DEV) for l in picked]
     x = make_tokens(cfg, 0, 1, device=DEV)
     full = DecodeStack(ws, batch=1, tau=cfg.tau, eps=cfg.rms_eps)
     plan = P.pi_stack_plan(full.desc, L, full.ranks)
