@@ -198,7 +198,9 @@ cudaError_t run_stack(const Plan& p, int n, const LayerPtrs* lp, const int* rank
         a.count_out = cnt;
         a.h_out = h;
         a.layer_counts = layer_counts;
-        return launch_fused(a, s);
+        FusedStackConfig fc{};
+        if (fused_stack_config(a, &fc)) return launch_fused(a, s);
+        // ranks too large for the persistent kernel's P2 ring: the per-step kernels
     }
     const __half* cur = x;
     __half* xbuf = at<__half>(ws, p.off_xbuf);
@@ -464,7 +466,21 @@ int pi_launches_per_layer(const pi_layer_desc* desc) {
         b0 += left >= 8 ? 8 : left >= 4 ? 4 : left >= 2 ? 2 : 1;
         ++chunks;
     }
-    if (p.fused) return 1;  // one persistent kernel
+    if (p.fused) {
+        // one persistent kernel, when its P2 ring fits the rank
+        const int rk[1] = {p.r};
+        FusedStackArgs a{};
+        a.L = 1;
+        a.d = p.d;
+        a.F = p.F;
+        a.G = p.nsm;
+        a.int4 = p.int4;
+        a.gated = p.gated;
+        a.ranks = rk;
+        a.rmax_su = p.rmax_su;
+        FusedStackConfig c{};
+        if (fused_stack_config(a, &c)) return 1;
+    }
     // predictor: 2 per token chunk; compaction: 1; then FC1 + FC2 + the FC2
     // reduction (tcgen05 path: all tokens at once) or FC1 and FC2 per chunk + 1
     // tcgen05 path: predictor u + finish + s, compaction, FC1 + finish, FC2 + reduction

@@ -306,7 +306,7 @@ __device__ unsigned long long g_pi_trace_clk[96 * kTraceSlots * kTraceCtas];
 // KIND 0: fp16 rows; 1: fp16 gate + up rows; 2: INT4 group-32 rows.
 // NCH: kCols-column chunks of d that each thread covers in FC2 (fp16 rows).
 // PS: each CTA's predictor slices are staged whole in shared memory (else P2
-// streams through the ring, or from global memory); fixed at compile time, so
+// streams through the ring of 16-row slots); fixed at compile time, so
 // a kernel holds the code of one mode only (measured 3-5 % faster per layer
 // than one kernel branching at run time: the code of each phase is fetched
 // afresh every layer).
@@ -472,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
     if (PS) {
         if (warp == 0) issue_predictor(0);
         inflight = 0;
-    } else if (ns > 0 && tid == 0) {
+    } else if (tid == 0) {
         for (int k = 0; k < ns && k < nunits; ++k) issue_unit(p.layers[0], k);
     }
 
@@ -490,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
             if (l + 1 < p.L) {
                 if (PS)
                     issue_predictor(l + 1);
-                else if (ns > 0 && lane == 0)
+                else if (lane == 0)
                     for (int k = 0; k < ns && k < nunits; ++k) issue_unit(p.layers[l + 1], k);
             }
         };
@@ -576,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                 prefetch_lines(ly.p2 + (size_t)rb * ly.r, (size_t)2 * ly.r * min(8, F - rb), lane, 32);
             }
         };
-        if (!PS && ns > 0) {
+        if (!PS) {
             if (!sync_then(prefetch_next_units)) { leave(); return; }
         } else if (!sync()) { leave(); return; }
         PI_STAMP(l, 2);
@@ -608,14 +608,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
             // With the P2 ring, warp q < ns owns slot q and takes units q, q+ns,
             // ...: each slot's copies are waited for, read and refilled in
             // order by one warp, so a wait never sees an older phase of its slot.
-            const int mstep = ns > 0 ? ns : kWarps;
-            const bool unit_warp = ns == 0 || warp < ns;
+            const int mstep = PS ? kWarps : ns;
+            const bool unit_warp = PS || warp < ns;
             for (int m = warp; unit_warp && m < nunits; m += mstep) {
                 // first rows of the unit's two pieces (F: no second piece)
                 const int pb0 = 8 * piece_of(2 * m);
                 const int pb1 = 2 * m + 1 < npc ? 8 * piece_of(2 * m + 1) : F;
                 const __half* p2r = nullptr;   // this unit's rows in the ring
-                if (ns > 0) {
+                if (!PS) {
                     if (!mbar_wait(&ring_full[warp], (unsigned)((l * ring_per_layer(warp) + m / ns) & 1), tmo, &bad))
                         break;
                     p2r = reinterpret_cast<const __half*>(ring + (size_t)warp * p.ring_unit);
@@ -644,11 +644,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                             // rows past F (short last piece, missing second piece) read
                             // a row in bounds; their result is never used
                             const int kk = 8 * h + k;
-                            w[k] = PS
-                                       ? *reinterpret_cast<const uint4*>(p2s + (size_t)(16 * m + kk) * r + vc * 8)
-                                   : p2r != nullptr
-                                       ? *reinterpret_cast<const uint4*>(p2r + (size_t)kk * r + vc * 8)
-                                       : ld_stream16(ly.p2 + (size_t)min((h ? pb1 : pb0) + k, F - 1) * r + vc * 8);
+                            w[k] = PS ? *reinterpret_cast<const uint4*>(p2s + (size_t)(16 * m + kk) * r + vc * 8)
+                                      : *reinterpret_cast<const uint4*>(p2r + (size_t)kk * r + vc * 8);
                         }
 #pragma unroll
                         for (int k = 0; k < 8; ++k) {
@@ -701,7 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                 }
                 const unsigned bal = __ballot_sync(FULL, pred);
                 // the unit's slot is read: refill it with unit m + ns of this layer
-                if (ns > 0 && lane == 0 && m + ns < nunits) issue_unit(ly, m + ns);
+                if (!PS && lane == 0 && m + ns < nunits) issue_unit(ly, m + ns);
                 if (lane == 0) {
                     unsigned bits = 0;
                     // the bit of row kk(L) sits at ballot position L (even lanes)
@@ -1404,7 +1401,8 @@ static bool plan_fused(const FusedStackArgs& a, FusedParams* out, size_t* smem_o
         // through the mask/list buffers and the staging region
         const int unit = 16 * rmax * 2;
         const int slots = prm.stage_bytes > 0 ? (prm.stage_bytes + sp.off_stage() - sp.off_m16()) / unit : 0;
-        if (!prm.pred_smem && slots >= 2) {
+        if (!prm.pred_smem) {
+            if (slots < 2) return false;   // neither fits: the per-step kernels run the stack
             prm.ring_slots = slots < kRingMax ? slots : kRingMax;
             prm.ring_unit = unit;
         }

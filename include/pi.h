@@ -345,7 +345,8 @@ typedef struct {
     int pred_in_smem;  /* 1: a block's share of the predictor is copied whole into
                           shared memory before it is used                         */
     int p2_ring_slots; /* else: a block's P2 rows stream through this many slots of
-                          16 rows (0: read from global memory)                    */
+                          16 rows (a rank whose ring cannot hold two slots runs
+                          on the per-step kernels: fused = 0)                     */
     int fc_row_slots;  /* FC weight rows a block holds in shared memory at once; a
                           block whose predicted neurons need more rows (gated: 3
                           per neuron, else 2) streams them through a ring          */
