@@ -577,8 +577,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
             }
         };
         if (!PS) {
-            if (!sync_then(prefetch_next_units)) { leave(); return; }
-        } else if (!sync()) { leave(); return; }
+            if (!sync_then(prefetch_next_units)) break;
+        } else if (!sync()) break;
         PI_STAMP(l, 2);
 
         // ---------------------------------------------------------- phase B
@@ -724,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
         __syncthreads();
         PI_STAMP(l, 3);
 
-        if (*(volatile int*)&bad) { leave(); return; }
+        if (*(volatile int*)&bad) break;
 
         // ---------------------------------------------------------- phase B, FFN
         // this CTA's active rows, in unit order (a fixed order: FC2 sums them in
@@ -1085,7 +1085,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
         if (!*(volatile int*)&bad) w12_pending = false;
         PI_STAMP(l, 5);
         if (l + 1 < p.L && PS) inflight = l + 1;
-        if (!sync_then(issue_next)) { leave(); return; }
+        if (!sync_then(issue_next)) break;
         PI_STAMP(l, 6);
 
         // ---------------------------------------------------------- phase D
@@ -1211,40 +1211,43 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_stack(const __grid_consta
                 if (lane == 0) __stcg(p.xss + c, t);
             }
         }
-        if (l == p.L - 1) {
-            // the active list of the last layer in storage order: every CTA scans the
-            // whole mask (complete since the last barrier) and places its own rows
-            for (int w = tid; w < p.W; w += kThreads) reinterpret_cast<uint32_t*>(m16)[w] = __ldcg(p.mask_out + w);
-            __syncthreads();
-            const int per = (M + kThreads - 1) / kThreads;
-            int cnt = 0;
-            for (int e = 0; e < per; ++e) {
-                const int m = tid * per + e;
-                if (m < M) cnt += __popc((unsigned)m16[m]);
-            }
-            int total;
-            int run = block_exscan(cnt, scr, &total);
-            for (int e = 0; e < per; ++e) {
-                const int m = tid * per + e;
-                if (m < M) {
-                    upre[m] = run;
-                    run += __popc((unsigned)m16[m]);
-                }
-            }
-            __syncthreads();
-            const int nmine = nmine_s;
-            for (int q = tid; q < nmine; q += kThreads) {
-                const int k = lidx[q];
-                const int pos = upre[k >> 4] + __popc((unsigned)m16[k >> 4] & ((1u << (k & 15)) - 1u));
-                p.idx_out[pos] = k;
-                p.h_out[pos] = lh[q];
-            }
-            if (c == 0 && tid == 0) *p.count_out = total;
-        }
         PI_STAMP(l, 7);
         // the next layer's input needs every CTA's columns of y; after the last
         // layer the end of the grid publishes them
-        if (l + 1 < p.L && !sync()) { leave(); return; }
+        if (l + 1 < p.L && !sync()) break;
+    }
+    // (a failure anywhere left the loop early with bad set; the code of the
+    // last layer's list and of the exit stays out of the layer loop)
+    __syncthreads();
+    if (!*(volatile int*)&bad) {
+        // the active list of the last layer in storage order: every CTA scans the
+        // whole mask (complete since the last barrier) and places its own rows
+        for (int w = tid; w < p.W; w += kThreads) reinterpret_cast<uint32_t*>(m16)[w] = __ldcg(p.mask_out + w);
+        __syncthreads();
+        const int per = (M + kThreads - 1) / kThreads;
+        int cnt = 0;
+        for (int e = 0; e < per; ++e) {
+            const int m = tid * per + e;
+            if (m < M) cnt += __popc((unsigned)m16[m]);
+        }
+        int total;
+        int run = block_exscan(cnt, scr, &total);
+        for (int e = 0; e < per; ++e) {
+            const int m = tid * per + e;
+            if (m < M) {
+                upre[m] = run;
+                run += __popc((unsigned)m16[m]);
+            }
+        }
+        __syncthreads();
+        const int nmine = nmine_s;
+        for (int q = tid; q < nmine; q += kThreads) {
+            const int k = lidx[q];
+            const int pos = upre[k >> 4] + __popc((unsigned)m16[k >> 4] & ((1u << (k & 15)) - 1u));
+            p.idx_out[pos] = k;
+            p.h_out[pos] = lh[q];
+        }
+        if (c == 0 && tid == 0) *p.count_out = total;
     }
     leave();
 }
