@@ -85,6 +85,21 @@ def test_stack_p2_ring_matches_oracle(name, cfg, L):
     _check_stack(cfg, L, p2_ring=True)
 
 
+def test_stack_rank_beyond_the_ring_runs_per_step_kernels():
+    """Rank 4096: a 16-row P2 unit is 128 KB, so fewer than two ring slots fit
+    in shared memory; the plan drops the persistent kernel and the step runs on
+    the per-step kernels, still matching the oracle layer by layer."""
+    P = _pi()
+    from activation_sparse_ffn_layer_gb300.runtime import DecodeStack
+    cfg = small(CONFIGS["c2"], d=4096, F=5000, rank=4096)
+    ws = [make_layer(cfg, l, device=DEV) for l in range(2)]
+    st = DecodeStack(ws, batch=1, tau=cfg.tau, eps=cfg.rms_eps)
+    assert P.pi_stack_plan(st.desc, 2, st.ranks).fused == 0
+    assert P.pi_launches_per_layer(st.desc) > 1
+    del st, ws
+    _check_stack(cfg, 2)
+
+
 def test_stack_c2_full_shape_first_layers():
     _check_stack(CONFIGS["c2"], 3)
 
