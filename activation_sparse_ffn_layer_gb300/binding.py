@@ -61,8 +61,9 @@ _lib = None
 EXPORTS = ("pi_workspace_bytes", "pi_workspace_layout", "pi_predict", "pi_compact", "pi_sparse_fc1",
            "pi_sparse_fc2", "pi_ffn_layer", "pi_rmsnorm_half", "pi_status_string",
            "pi_last_device_status", "pi_launches_per_layer", "pi_ffn_stack", "pi_debug_wait_timeout",
-           "pi_sparse_fc2_noalloc", "pi_stack_plan", "pi_debug_set_wait_timeout", "pi_sparse_fc1_tiered",
-           "pi_sparse_fc2_tiered", "pi_ffn_layer_tiered", "pi_attn_workspace_bytes", "pi_attn_heads")
+           "pi_sparse_fc2_noalloc", "pi_stack_plan", "pi_stack_plan_for", "pi_debug_set_wait_timeout",
+           "pi_sparse_fc1_tiered", "pi_sparse_fc2_tiered", "pi_ffn_layer_tiered", "pi_attn_workspace_bytes",
+           "pi_attn_heads")
 
 
 def library_path() -> str:
@@ -98,6 +99,7 @@ def lib(path: Optional[str] = None):
         "pi_debug_wait_timeout": (I, [C.c_longlong, P]),
         "pi_sparse_fc2_noalloc": (I, [D, P, P, P, Wt, P, P]),
         "pi_stack_plan": (I, [D, I, P, C.POINTER(pi_stack_plan_t)]),
+        "pi_stack_plan_for": (I, [D, I, P, I, C.POINTER(pi_stack_plan_t)]),
         "pi_debug_set_wait_timeout": (I, [C.c_longlong]),
         "pi_sparse_fc1_tiered": (I, [D, P, Wt, C.POINTER(pi_cold_tier), P, P, P, P, P]),
         "pi_sparse_fc2_tiered": (I, [D, P, P, P, Wt, C.POINTER(pi_cold_tier), P, P, S, P]),
@@ -275,6 +277,14 @@ def pi_stack_plan(desc, n_layers: int, ranks=None) -> pi_stack_plan_t:
     """How a pi_ffn_stack step of `n_layers` layers runs on the current device."""
     out = pi_stack_plan_t()
     _check("pi_stack_plan", lib().pi_stack_plan(C.byref(desc), int(n_layers), ranks, C.byref(out)))
+    return out
+
+
+def pi_stack_plan_for(desc, n_layers: int, sm_count: int, ranks=None) -> pi_stack_plan_t:
+    """The same plan for a device with `sm_count` SMs (host only, no device)."""
+    out = pi_stack_plan_t()
+    _check("pi_stack_plan_for", lib().pi_stack_plan_for(C.byref(desc), int(n_layers), ranks, int(sm_count),
+                                                        C.byref(out)))
     return out
 
 

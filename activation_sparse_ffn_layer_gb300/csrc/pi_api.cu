@@ -34,7 +34,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
-bool make_plan(const pi_layer_desc& desc, Plan* p) {
+bool make_plan(const pi_layer_desc& desc, Plan* p, int sm_count) {
     if (desc.d <= 0 || desc.d % 8 != 0 || desc.ffn <= 0 || desc.rank <= 0 || desc.rank % 8 != 0 ||
         desc.batch < 1 || desc.batch > 32 || desc.d > (1 << 16) || desc.rank > 8192 ||
         desc.ffn > (1 << 22))
@@ -50,7 +50,7 @@ bool make_plan(const pi_layer_desc& desc, Plan* p) {
     q.int4 = desc.wdtype == PI_W_INT4_G32;
     q.gated = desc.gated == 1;
     q.W = (q.F + 31) / 32;
-    q.nsm = device_sms();
+    q.nsm = sm_count > 0 ? sm_count : device_sms();
     if (q.nsm <= 0) q.nsm = 1;
     // predictor P1 x: enough (row, split) warps to cover the GPU twice, splits >= 256 elements
     const int row_blocks = (q.r + 7) / 8;
@@ -426,9 +426,10 @@ pi_status pi_rmsnorm_half(int d, int batch, const float* y, float eps, pi_half* 
                                     static_cast<cudaStream_t>(stream)));
 }
 
-pi_status pi_stack_plan(const pi_layer_desc* desc, int n_layers, const int* ranks, pi_stack_plan_t* out) {
+namespace {
+pi_status stack_plan(const pi_layer_desc* desc, int n_layers, const int* ranks, int sm_count, pi_stack_plan_t* out) {
     Plan p;
-    if (!desc || !out || !make_plan(*desc, &p)) return PI_ERR_INVALID_ARG;
+    if (!desc || !out || !make_plan(*desc, &p, sm_count)) return PI_ERR_INVALID_ARG;
     if (n_layers < 1 || n_layers > kMaxStackLayers) return PI_ERR_INVALID_ARG;
     *out = pi_stack_plan_t{};
     if (!p.fused) return PI_OK;
@@ -455,6 +456,17 @@ pi_status pi_stack_plan(const pi_layer_desc* desc, int n_layers, const int* rank
     out->fc_row_slots = c.fc_slots;
     out->smem_bytes = c.smem_bytes;
     return PI_OK;
+}
+}  // namespace
+
+pi_status pi_stack_plan(const pi_layer_desc* desc, int n_layers, const int* ranks, pi_stack_plan_t* out) {
+    return stack_plan(desc, n_layers, ranks, 0, out);
+}
+
+pi_status pi_stack_plan_for(const pi_layer_desc* desc, int n_layers, const int* ranks, int sm_count,
+                            pi_stack_plan_t* out) {
+    if (sm_count < 1 || sm_count > 4096) return PI_ERR_INVALID_ARG;
+    return stack_plan(desc, n_layers, ranks, sm_count, out);
 }
 
 int pi_launches_per_layer(const pi_layer_desc* desc) {

@@ -63,7 +63,8 @@ struct Plan {
     size_t off_mask, off_idx, off_count, off_h, off_upart, off_part, off_xbuf, off_live, off_uhl, total;
 };
 
-bool make_plan(const pi_layer_desc& desc, Plan* p);
+// sm_count > 0 plans for a device with that many SMs instead of the current one
+bool make_plan(const pi_layer_desc& desc, Plan* p, int sm_count = 0);
 
 // Limit of the bounded device-side waits of the next launches: 2 s, unless a
 // caller set another one with pi_debug_set_wait_timeout.  Draining a CTA's own

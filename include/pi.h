@@ -353,6 +353,12 @@ typedef struct {
     int smem_bytes;    /* dynamic shared memory per block                         */
 } pi_stack_plan_t;
 PI_API pi_status pi_stack_plan(const pi_layer_desc *desc, int n_layers, const int *ranks, pi_stack_plan_t *out);
+/* The same plan for a device with `sm_count` SMs (1..4096) instead of the
+ * current device: host only, no device is queried, so the plan can be checked
+ * where there is no GPU.  PI_ERR_INVALID_ARG for a bad descriptor, layer count,
+ * rank or SM count. */
+PI_API pi_status pi_stack_plan_for(const pi_layer_desc *desc, int n_layers, const int *ranks, int sm_count,
+                                   pi_stack_plan_t *out);
 
 /* Number of kernel launches one pi_ffn_layer call issues for `desc` (-1 if
  * the descriptor is invalid). */
