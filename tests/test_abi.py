@@ -51,3 +51,35 @@ def test_host_validation_without_launch(P):
     assert L.pi_compact(C.byref(ok), None, None, None, None, None, None) == 1
     assert L.pi_ffn_layer(None, None, None, 0.0, None, 0, None, None) == 1
     assert L.pi_rmsnorm_half(0, 1, None, 1e-6, None, None) == 1
+
+
+def test_attention_descriptor_validation_without_launch(P):
+    """pi_attn_workspace_bytes sizes only valid blocks; pi_attn_heads rejects a
+    bad descriptor or missing pointers on the host (status 1), a missing
+    workspace with status 5, and launches nothing."""
+    L = P.lib()
+    ok = P.attn_desc_of(256, 8, 2, 64, 16, 2, 64)
+    assert P.pi_attn_workspace_bytes(ok) > 0
+    bad = [
+        P.attn_desc_of(250, 8, 2, 64, 16, 2, 64),     # d not a multiple of 8
+        P.attn_desc_of(256, 8, 3, 64, 16, 2, 64),     # heads not a multiple of the KV heads
+        P.attn_desc_of(256, 8, 2, 96, 16, 2, 64),     # head_dim other than 64 / 128
+        P.attn_desc_of(256, 8, 2, 64, 12, 2, 64),     # rank not a multiple of 8
+        P.attn_desc_of(256, 8, 2, 64, 16, 33, 64),    # batch above 32
+        P.attn_desc_of(256, 8, 2, 64, 16, 2, 0),      # no cache positions
+        P.attn_desc_of(256, 0, 1, 64, 16, 2, 64),     # no heads
+    ]
+    for b in bad:
+        assert P.pi_attn_workspace_bytes(b) == 0
+        assert L.pi_attn_heads(C.byref(b), None, None, None, None, None, 0.0, None, None, None, 0, None) == 1
+    w = P.binding.pi_attn_weights()
+    assert L.pi_attn_heads(C.byref(ok), None, C.byref(w), None, None, None, 0.0, None, None, None, 0, None) == 1
+    assert L.pi_attn_heads(None, None, None, None, None, None, 0.0, None, None, None, 0, None) == 1
+    # every pointer present and 16-byte aligned (never dereferenced: the
+    # workspace check comes first), the workspace missing or too small
+    fake = C.c_void_p(1 << 20)
+    wf = P.binding.pi_attn_weights(*([1 << 20] * 7))
+    need = P.pi_attn_workspace_bytes(ok)
+    for ws, nbytes in ((None, need), (fake, need - 16)):
+        assert L.pi_attn_heads(C.byref(ok), fake, C.byref(wf), fake, fake, fake, 0.0, fake, fake, ws, nbytes,
+                               None) == 5
